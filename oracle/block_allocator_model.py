@@ -1,0 +1,136 @@
+"""Host semantics of the KV block allocator, written as a plain Python model.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  The C++ allocator in
+the library is checked against this model operation by operation, bit-exact.
+
+What the pages fix ("PagedAttention (vLLM) -- Virtual memory cho AI"):
+* section "Co che Block Table": the cache is cut into fixed blocks (typically
+  16 tokens); each sequence has a table from logical block i (tokens
+  16i..16i+15) to a physical block anywhere in memory; a block is handed out
+  only when a token actually needs it (100 tokens -> 7 blocks = 112 slots
+  instead of 256 blocks for a 4096-token reservation); freed blocks, even small
+  ones released mid-run, are reused at once with no defragmentation.
+* section "Copy-on-Write cho Beam Search": branches of beam search / parallel
+  sampling share the physical blocks of their common prefix and split a block
+  only when their tokens start to differ.
+
+Readings where the pages are silent (each listed in the design notes):
+* free list: a LIFO stack that hands out block 0 first, then 1, 2, ...; a
+  freed sequence pushes its blocks in table order (so its last block is the
+  next one handed out);
+* copy-on-write happens on ``append_slot`` into a partially filled last block
+  whose reference count is above one: a fresh block is taken, the pair
+  (src, dst) is reported for the device copy and src loses one reference; the
+  last remaining holder writes in place; a shared *full* block is never copied;
+* running out of blocks returns ERR_OOM and changes nothing;
+* waste = 1 - occupied slots / allocated slots, every physical block counted
+  once however many sequences share it.
+"""
+from __future__ import annotations
+
+OK = 0
+ERR_INVALID = 1
+ERR_OOM = 2
+
+
+class BlockAllocatorModel:
+    def __init__(self, num_blocks: int, block_size: int):
+        if num_blocks <= 0 or block_size <= 0:
+            raise ValueError("num_blocks and block_size must be positive")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        # top of the stack is the list's end: block 0 is handed out first
+        self._free = list(range(self.num_blocks - 1, -1, -1))
+        self._ref = [0] * self.num_blocks
+        self._seqs = {}  # seq id -> [table (list of block ids), num_tokens]
+
+    # -- internal -----------------------------------------------------------
+    def _take(self) -> int:
+        b = self._free.pop()
+        self._ref[b] = 1
+        return b
+
+    def _release(self, b: int) -> None:
+        self._ref[b] -= 1
+        if self._ref[b] == 0:
+            self._free.append(b)
+
+    # -- operations (return a status, plus results) --------------------------
+    def add_seq(self, seq: int, num_tokens: int) -> int:
+        """A new sequence holding ``num_tokens`` tokens (a prompt)."""
+        if seq in self._seqs or num_tokens < 0:
+            return ERR_INVALID
+        need = -(-num_tokens // self.block_size)
+        if need > len(self._free):
+            return ERR_OOM
+        table = [self._take() for _ in range(need)]
+        self._seqs[seq] = [table, num_tokens]
+        return OK
+
+    def append_slot(self, seq: int):
+        """Room for one more token of ``seq``.  Returns (status, slot, cow_src,
+        cow_dst); cow_src/cow_dst are -1 when no copy is needed."""
+        if seq not in self._seqs:
+            return ERR_INVALID, -1, -1, -1
+        table, n = self._seqs[seq]
+        offset = n % self.block_size
+        src = dst = -1
+        if offset == 0:
+            # last block full (or no block yet): a fresh block for this token
+            if not self._free:
+                return ERR_OOM, -1, -1, -1
+            table.append(self._take())
+        elif self._ref[table[-1]] > 1:
+            # the partially filled last block is shared: copy before writing
+            if not self._free:
+                return ERR_OOM, -1, -1, -1
+            src = table[-1]
+            dst = self._take()
+            self._ref[src] -= 1
+            table[-1] = dst
+        slot = table[-1] * self.block_size + offset
+        self._seqs[seq][1] = n + 1
+        return OK, slot, src, dst
+
+    def fork(self, parent: int, child: int) -> int:
+        """``child`` starts as ``parent``, sharing every block by reference."""
+        if parent not in self._seqs or child in self._seqs or parent == child:
+            return ERR_INVALID
+        table, n = self._seqs[parent]
+        for b in table:
+            self._ref[b] += 1
+        self._seqs[child] = [list(table), n]
+        return OK
+
+    def free_seq(self, seq: int) -> int:
+        if seq not in self._seqs:
+            return ERR_INVALID
+        table, _ = self._seqs.pop(seq)
+        for b in table:
+            self._release(b)
+        return OK
+
+    # -- queries --------------------------------------------------------------
+    def block_table(self, seq: int):
+        return list(self._seqs[seq][0])
+
+    def num_tokens(self, seq: int) -> int:
+        return self._seqs[seq][1]
+
+    def num_free(self) -> int:
+        return len(self._free)
+
+    def refcount(self, block: int) -> int:
+        return self._ref[block]
+
+    def sequences(self):
+        return sorted(self._seqs)
+
+    def waste(self):
+        """(occupied slots, allocated slots) with each live block counted once."""
+        fill = {}
+        for table, n in self._seqs.values():
+            for i, b in enumerate(table):
+                used = min(self.block_size, max(0, n - i * self.block_size))
+                fill[b] = max(fill.get(b, 0), used)
+        return sum(fill.values()), len(fill) * self.block_size
