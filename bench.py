@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path for one batch: the host allocator hands every
+running sequence the slot of its new token (copy-on-write pairs, if any, go to
+block_copy), kv_cache_write scatters the new K/V into the paged pool, and
+paged_attention_decode attends each sequence's query to its whole context
+through the block tables (split into partitions plus a merge when long).
+
+Default workload: GQA decode, bf16 -- 64 sequences, context lengths uniform in
+[64, 2048], 32 query / 8 KV heads, head_dim 128, block 16, a pool of the
+needed blocks + 10% handed out in shuffled order.  Data are synthetic N(0,1).
+
+Prints ONE JSON line (rank 0).  `value` is the unique KV bytes the step's
+attention reads divided by the device time of the step, with every input
+resident in HBM; `e2e` is the same metric through the public Python API with
+host buffers (allocator on the host, H2D of the step's inputs, D2H of the
+output, all inside the timed region).  `--impl reference` times the fp64 CPU
+oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_cache_279_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-decode attention KV GB/s (% of GB300 HBM peak); decode tokens/s"
+WORKLOADS = {
+    "gqa": wl.GQA_BF16,
+    "tiny": wl.TINY_FP32,
+    "long": wl.LONG_BF16,
+    "mixed": wl.MIXED_BF16,
+}
+ROTATE = {"gqa": 4, "tiny": 1, "long": 1, "mixed": 4}  # batches rotated to defeat L2 reuse
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa")
+    p.add_argument("--block-size", type=int, default=0, help="override the block size (mixed sweep)")
+    p.add_argument("--partition-size", type=int, default=0)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (one process per GPU, independent replicas)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """Largest value of x over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="pkv_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        smax = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[2] > 250.0] or rows
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(1, 5)
+                          if i < len(r[3]) and r[3][i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": smax,
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------------------
+# workload construction (through the library: allocator + cache write)
+# ---------------------------------------------------------------------------
+def shape_for(args) -> wl.DecodeShape:
+    shape = WORKLOADS[args.workload]
+    if args.block_size:
+        shape = wl.DecodeShape(shape.name, shape.num_seqs, shape.num_heads, shape.num_kv_heads,
+                               shape.head_dim, args.block_size, shape.dtype, shape.num_layers,
+                               shape.partition_size)
+    return shape
+
+
+def kv_bytes(lens, shape) -> int:
+    """Unique K and V bytes one attention pass reads (every cached token once)."""
+    elt = torch.tensor([], dtype=shape.dtype).element_size()
+    return int(sum(int(x) for x in lens)) * shape.num_kv_heads * shape.head_dim * 2 * elt
+
+
+def algorithmic_decode_bytes(lens, shape) -> int:
+    """Bytes one paged_attention_decode call must move: the K/V of every cached
+    token, the query and output rows, the block-table entries and lengths."""
+    elt = torch.tensor([], dtype=shape.dtype).element_size()
+    S = len(lens)
+    blocks = sum(-(-int(x) // shape.block_size) for x in lens)
+    qo = 2 * S * shape.num_heads * shape.head_dim * elt
+    return kv_bytes(lens, shape) + qo + 4 * blocks + 4 * S
+
+
+class Batch:
+    """One resident decode batch: pool, allocator, tables and step inputs."""
+
+    def __init__(self, pkv, shape, lens, seed, device, partition_size):
+        B = shape.block_size
+        self.shape = shape
+        self.device = device
+        self.lens = [int(x) for x in lens]
+        S = len(self.lens)
+        need = sum(-(-L // B) for L in self.lens)
+        self.num_blocks = max(1, math.ceil(1.1 * need)) + 2 * S
+        self.alloc = pkv.BlockAllocator(self.num_blocks, B)
+        # hand blocks out in a random order, as after a long run of frees
+        order = wl.draw_block_ids(self.num_blocks, seed)
+        for i in range(self.num_blocks):
+            assert self.alloc.add_seq(-1 - i, B) == 0
+        for b in order[::-1]:
+            assert self.alloc.free_seq(-1 - int(b)) == 0
+        g = torch.Generator(device=device)
+        g.manual_seed(int(wl.sub_seed(seed, 9)))
+        Hkv, D = shape.num_kv_heads, shape.head_dim
+        self.k_cache = torch.zeros((self.num_blocks, Hkv, B, D), dtype=shape.dtype, device=device)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        # the context before this step: written through the library
+        for s, L in enumerate(self.lens):
+            assert self.alloc.add_seq(s, L - 1) == 0
+            if L > 1:
+                slots = torch.from_numpy(self.alloc.slots(s, 0, L - 1)).to(device)
+                k = torch.randn((L - 1, Hkv, D), generator=g, device=device).to(shape.dtype)
+                v = torch.randn((L - 1, Hkv, D), generator=g, device=device).to(shape.dtype)
+                pkv.kv_cache_write(k, v, self.k_cache, self.v_cache, slots)
+        # this step's new token for every sequence
+        self.seq_ids = np.arange(S, dtype=np.int64)
+        st, slots, pairs = self.alloc.append_slots(self.seq_ids)
+        assert st == 0 and len(pairs) == 0
+        self.max_blocks = max(-(-L // B) for L in self.lens) + 4
+        tables, seq_lens = self.alloc.block_tables(self.seq_ids, self.max_blocks)
+        self.max_seq_len = self.max_blocks * B
+        self.slot_mapping = torch.from_numpy(slots).to(device)
+        self.block_tables = torch.from_numpy(tables).to(device)
+        self.seq_lens = torch.from_numpy(seq_lens).to(device)
+        self.q = torch.randn((S, shape.num_heads, D), generator=g, device=device).to(shape.dtype)
+        self.k_new = torch.randn((S, Hkv, D), generator=g, device=device).to(shape.dtype)
+        self.v_new = torch.randn((S, Hkv, D), generator=g, device=device).to(shape.dtype)
+        self.out = torch.empty_like(self.q)
+        self.partition_size = partition_size
+        ws = pkv.paged_attention_workspace_size(S, shape.num_heads, D, self.max_seq_len,
+                                                partition_size)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.pkv = pkv
+
+    def write(self):
+        self.pkv.kv_cache_write(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slot_mapping)
+
+    def decode(self):
+        self.pkv.paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache,
+                                        self.block_tables, self.seq_lens, self.shape.scale,
+                                        self.max_seq_len, self.partition_size, self.workspace)
+
+    def step(self):
+        self.write()
+        self.decode()
+
+    def launches_per_step(self) -> int:
+        S = len(self.lens)
+        ws = self.pkv.paged_attention_workspace_size(S, self.shape.num_heads, self.shape.head_dim,
+                                                     self.max_seq_len, self.partition_size)
+        return 2 + (1 if ws > 0 else 0)
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm caches (tensor maps, smem opt-in, symbol addresses) outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graphs(graphs, steps, warmup, stream):
+    """Replay graphs[i % n] `steps` times after `warmup` untimed replays;
+    returns per-replay device milliseconds (CUDA events on the stream)."""
+    n = len(graphs)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            graphs[i % n].replay()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            graphs[i % n].replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample(shape, seed, budget_s):
+    """Time the fp64 oracle, as it stands, on one freshly drawn batch of the
+    same workload, repeating the call until about `budget_s` seconds of work.
+    Returns (GB/s, cores, description, seconds, calls)."""
+    import oracle
+    lens = wl.draw_lengths(shape, seed + 1).tolist()
+    cores = oracle.max_threads()
+    q = wl.draw_query(shape, seed + 1).float().numpy()
+    ks, vs = [], []
+    for i, L in enumerate(lens):
+        k, v = wl.draw_seq_kv(shape, seed + 1, i, L)
+        ks.append(k.float().numpy())
+        vs.append(v.float().numpy())
+    done_s, calls = 0.0, 0
+    while done_s < budget_s and calls < 1000:
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, ks, vs, shape.scale)
+        done_s += time.perf_counter() - t0
+        calls += 1
+    gbs = calls * kv_bytes(lens, shape) / done_s / 1e9
+    desc = (f"fp64 oracle, {calls} call(s) over one {len(lens)}-sequence batch of the "
+            f"{shape.name} workload, {cores} threads, {done_s:.1f} s")
+    return gbs, cores, desc, done_s, calls
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    shape = shape_for(args)
+    lens = wl.draw_lengths(shape, args.seed + 1).tolist()
+    per_step = max(1, len(lens) // 4)  # a bounded sample per step
+    import oracle
+    cores = oracle.max_threads()
+    times, bytes_ = [], []
+    q = wl.draw_query(shape, args.seed + 1).float().numpy()
+    kv = [tuple(t.float().numpy() for t in wl.draw_seq_kv(shape, args.seed + 1, s, L))
+          for s, L in enumerate(lens)]
+    for i in range(args.warmup + args.steps):
+        idx = [((i * per_step) + j) % len(lens) for j in range(per_step)]
+        t0 = time.perf_counter()
+        oracle.decode_attention(q[idx], [kv[s][0] for s in idx], [kv[s][1] for s in idx], shape.scale)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            bytes_.append(kv_bytes([lens[s] for s in idx], shape))
+    total_s = sum(times)
+    value = sum(bytes_) / total_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_s / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(shape, args, len(lens)),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} of {len(lens)} sequences per step, fp64 CPU oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(shape, args, S):
+    return {"workload": f"{shape.name}: {S} seqs, {shape.num_heads}q/{shape.num_kv_heads}kv heads, "
+                        f"head_dim {shape.head_dim}, block {shape.block_size}",
+            "num_seqs": S, "num_heads": shape.num_heads, "num_kv_heads": shape.num_kv_heads,
+            "head_dim": shape.head_dim, "block_size": shape.block_size,
+            "partition_size": args.partition_size or "auto",
+            "l2": f"inputs larger than L2: {ROTATE.get(args.workload, 1)} resident batches rotated"}
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    import paged_kv_cache_279_gb300 as pkv
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    shape = shape_for(args)
+    nrot = ROTATE.get(args.workload, 1)
+    seed = args.seed + 1000 * rank
+    batches = []
+    for r in range(nrot):
+        lens = wl.draw_lengths(shape, seed + r).tolist()
+        batches.append(Batch(pkv, shape, lens, seed + r, device, args.partition_size))
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device)
+    step_graphs = [capture(b.step, stream) for b in batches]
+    decode_graphs = [capture(b.decode, stream) for b in batches]
+    assert pkv.read_device_errors() == 0
+
+    steps, warmup = args.steps, max(3, args.warmup)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        step_ms = time_graphs(step_graphs, steps, warmup, stream)
+        decode_ms = time_graphs(decode_graphs, steps, warmup, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    bytes_per = [kv_bytes(b.lens, shape) for b in batches]
+    step_bytes = sum(bytes_per[i % nrot] for i in range(steps))
+    local_s = sum(step_ms) / 1e3
+    total_s = max_over_ranks(local_s, world, device)
+    total_bytes = sum_over_ranks(step_bytes, world, device)
+    value = total_bytes / total_s / 1e9
+    ms_per_step = 1e3 * total_s / steps
+    seqs_per_step = sum(len(b.lens) for b in batches) / nrot
+    layers = shape.num_layers
+    tokens_per_s = world * seqs_per_step / (layers * ms_per_step / 1e3)
+
+    # roofline of the dominant kernel (the decode call), timed live above
+    alg = [algorithmic_decode_bytes(b.lens, shape) for b in batches]
+    dec_alg_bytes = sum(alg[i % nrot] for i in range(steps)) / steps
+    dec_ms = sum(decode_ms) / steps
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    achieved = dec_alg_bytes / (dec_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": "paged_attention_decode (partition kernel + merge kernel)",
+                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+                "decode_us": round(dec_ms * 1e3, 2)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(pkv, shape, args, device, stream, seed, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, desc, secs, _ = oracle_sample(shape, seed, args.cpu_budget)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if shape.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": config_of(shape, args, len(batches[0].lens)),
+            "decode_tokens_per_s": round(tokens_per_s, 1),
+            "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": batches[0].launches_per_step() * steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(pkv, shape, args, device, stream, seed, world):
+    """The step through the public API with host buffers: the allocator appends
+    a token for every sequence on the host, the step's inputs go H2D from
+    pinned memory, the kernels run, the output comes back D2H."""
+    lens = wl.draw_lengths(shape, seed + 77).tolist()
+    b = Batch(pkv, shape, lens, seed + 77, device, args.partition_size)
+    S = len(lens)
+    steps = args.steps
+    extra_blocks = b.num_blocks  # capacity check for the appended tokens
+    h_q = b.q.cpu().pin_memory()
+    h_k = b.k_new.cpu().pin_memory()
+    h_v = b.v_new.cpu().pin_memory()
+    h_out = torch.empty_like(h_q).pin_memory()
+    cap = b.max_blocks + (steps + args.warmup) // shape.block_size + 2
+    h_tab = torch.empty((S, cap), dtype=torch.int32).pin_memory()
+    h_len = torch.empty(S, dtype=torch.int32).pin_memory()
+    h_slot = torch.empty(S, dtype=torch.int64).pin_memory()
+    d_tab = torch.empty((S, cap), dtype=torch.int32, device=device)
+    d_len = torch.empty(S, dtype=torch.int32, device=device)
+    d_slot = torch.empty(S, dtype=torch.int64, device=device)
+    d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
+    max_seq_len = cap * shape.block_size
+    ws = torch.empty(max(256, pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim,
+                                                                 max_seq_len, args.partition_size)),
+                     dtype=torch.uint8, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len, h_slot))
+    d2h = h_out.numel() * h_out.element_size()
+    del extra_blocks
+    ms, byts = [], []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + steps):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            st, slots, pairs = b.alloc.append_slots(b.seq_ids)
+            if st != 0 or len(pairs):
+                raise RuntimeError("allocator could not serve the step")
+            tab, ln = b.alloc.block_tables(b.seq_ids, cap)
+            h_slot.numpy()[:] = slots
+            h_tab.numpy()[:] = tab
+            h_len.numpy()[:] = ln
+            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len),
+                         (d_slot, h_slot)):
+                d.copy_(h, non_blocking=True)
+            pkv.kv_cache_write(d_k, d_v, b.k_cache, b.v_cache, d_slot)
+            pkv.paged_attention_decode(b.out, d_q, b.k_cache, b.v_cache, d_tab, d_len, shape.scale,
+                                       max_seq_len, args.partition_size, ws)
+            h_out.copy_(b.out, non_blocking=True)
+            ev1.record(stream)
+            ev1.synchronize()  # the host reads the step's result
+            if i >= args.warmup:
+                ms.append(ev0.elapsed_time(ev1))
+                byts.append(kv_bytes(ln.tolist(), shape))
+    local_s = sum(ms) / 1e3
+    total_s = max_over_ranks(local_s, world, device)
+    total_b = sum_over_ranks(sum(byts), world, device)
+    return {"value": round(total_b / total_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * total_s / steps, 4)}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

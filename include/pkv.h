@@ -1,0 +1,270 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache library (GB300, sm_103a).
+ *
+ * The method ("PagedAttention (vLLM) -- Virtual memory cho AI", sections
+ * "Co che Block Table", "Copy-on-Write cho Beam Search" and "Tai sao no hoat
+ * dong"): the KV cache is cut into fixed-size blocks (typically 16 tokens)
+ * that sit anywhere in a physical pool; each sequence owns a block table from
+ * logical block i (tokens iB .. iB+B-1) to a physical block; blocks are handed
+ * out only when a token needs one; branches of beam search share prefix blocks
+ * and copy a block only when they diverge inside it; the attention kernel
+ * receives the block table and gathers K/V from the scattered blocks.
+ *
+ * Conventions for every call below
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or retains device memory.  Pointers
+ *     marked "host" are ordinary host memory, only read during the call.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Device work is enqueued on it; no call synchronises the device, except
+ *     pkv_read_device_errors, which waits for the stream.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns PKV_ERR_INVALID (or PKV_ERR_UNSUPPORTED for a valid but
+ *     unsupported shape) and enqueues nothing.  A failed launch returns
+ *     PKV_ERR_CUDA.  No call raises, exits, traps or asserts on the device.
+ *   - Index data that lives on the device (slot mappings, block tables,
+ *     sequence lengths, copy pairs) cannot be checked before launch.  Kernels
+ *     check every such index before using it: an out-of-range value is never
+ *     dereferenced, the affected token, block or pair is skipped, and a bit is
+ *     set in a device-side error word read by pkv_read_device_errors.
+ *
+ * KV cache layout (one K and one V tensor per layer):
+ *   [num_blocks][num_kv_heads][block_size][head_dim], row-major, element type
+ *   dtype.  One (block, kv head) is a contiguous block_size x head_dim slab
+ *   (4 KiB for bf16, block 16, head_dim 128).  Base addresses must be 16-byte
+ *   aligned.
+ *
+ * Supported shapes: head_dim in {64, 128}; block_size in {8, 16, 32};
+ *   num_heads a multiple of num_kv_heads with at most 8 query heads per KV head;
+ *   dtype PKV_F32 or PKV_BF16.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_EXPORT __attribute__((visibility("default")))
+#else
+#define PKV_EXPORT
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,     /* bad argument (null pointer, size, sequence id) */
+    PKV_ERR_OOM = 2,         /* the allocator has no free block; nothing changed */
+    PKV_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    PKV_ERR_UNSUPPORTED = 4, /* valid shape outside the supported set */
+    PKV_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+} pkv_status;
+
+typedef enum pkv_dtype {
+    PKV_F32 = 0,  /* float32 in, float32 math, float32 out (no TF32, no bf16) */
+    PKV_BF16 = 1  /* bfloat16 storage, float32 accumulation, bf16 output (RNE) */
+} pkv_dtype;
+
+/* Bits of the device-side error word (see pkv_read_device_errors). */
+#define PKV_DEVERR_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SEQ_LEN 2u   /* seq_len < 0 or above max_seq_len / table capacity */
+#define PKV_DEVERR_SLOT 4u      /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_COPY_PAIR 8u /* block_copy pair outside [0, num_blocks) or src == dst */
+#define PKV_DEVERR_TIMEOUT 16u  /* a bounded wait inside a kernel ran out */
+
+/* Human-readable name of a status code; never NULL. */
+PKV_EXPORT const char *pkv_status_string(int status);
+
+/* Version of this ABI (incremented on any signature change). */
+PKV_EXPORT int pkv_abi_version(void);
+
+/*
+ * kv_cache_write -- store the K/V of new tokens in their cache slots.
+ *
+ * Source: "PagedAttention (vLLM) -- Virtual memory cho AI", section "Co che
+ * Block Table" (a token lives in physical block table[pos / B] at offset
+ * pos % B; blocks are filled as tokens are produced) and "KV cache &
+ * PagedAttention -- vi sao chatbot AI ton bo nho" (aiwiki.vn), third
+ * paragraph (keys/values are stored for reuse in later steps).
+ *
+ *   k_new, v_new   device, [num_tokens][num_kv_heads][head_dim], dtype, contiguous
+ *   k_cache, v_cache  device, cache layout above, written in place
+ *   slot_mapping   device int64 [num_tokens]: slot = physical_block * block_size
+ *                  + offset.  slot < 0: the token is skipped (padding).
+ *                  slot >= num_blocks * block_size: skipped, PKV_DEVERR_SLOT set.
+ * Two tokens mapped to the same slot race (one of them wins).  The copy is
+ * bit-exact.  num_tokens == 0 enqueues nothing and returns PKV_OK.
+ */
+PKV_EXPORT pkv_status kv_cache_write(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                          const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, int dtype,
+                          void *stream);
+
+/*
+ * paged_attention_workspace_size -- bytes of device scratch that
+ * paged_attention_decode needs for the same (num_seqs, num_heads, head_dim,
+ * max_seq_len, partition_size).  0 when a single pass suffices (every
+ * sequence fits one partition).  The scratch holds one partial result per
+ * (sequence, query head, partition): running max, running sum and an
+ * unnormalised output row, all float32.
+ */
+PKV_EXPORT size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                      int max_seq_len, int partition_size);
+
+/*
+ * paged_attention_decode -- attention of one new query per sequence over its
+ * paged KV cache.
+ *
+ * Source: aiwiki.vn page above, second paragraph (the current query against
+ * the keys of the visible positions; the weights combine the values);
+ * troisinh page, section "Tai sao no hoat dong", item "Kernel scatter-gather"
+ * (the kernel takes the block table and gathers K/V from scattered blocks into
+ * on-chip memory before the softmax).  For sequence s, query head h, kv head
+ * g = h / (num_heads / num_kv_heads):
+ *     out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K[s,t,g,:]) * V[s,t,g,:]
+ * over t < seq_lens[s], where token t of sequence s is read from physical block
+ * block_tables[s][t / block_size] at offset t % block_size.  The new token must
+ * already be in the cache (call kv_cache_write first).  seq_lens[s] == 0 gives
+ * an all-zero output row.
+ *
+ *   out            device [num_seqs][num_heads][head_dim], dtype
+ *   q              device [num_seqs][num_heads][head_dim], dtype
+ *   k_cache, v_cache  device, cache layout above
+ *   block_tables   device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                  ceil(seq_lens[s] / block_size) are never read
+ *   seq_lens       device int32 [num_seqs], each in [0, max_seq_len] and
+ *                  <= max_blocks_per_seq * block_size (larger values are
+ *                  clamped and flagged with PKV_DEVERR_SEQ_LEN)
+ *   scale          multiplies every q.k score (typically 1/sqrt(head_dim))
+ *   partition_size 0 = let the library choose; otherwise a positive multiple of
+ *                  16.  Contexts longer than one partition are split: each
+ *                  partition is attended independently and a reduction kernel
+ *                  merges the partials (max-rescaled sums), all on `stream`.
+ *   workspace      device scratch of at least paged_attention_workspace_size()
+ *                  bytes for the same arguments (may be NULL when that is 0),
+ *                  256-byte aligned.  Contents need no initialisation; calls
+ *                  that share a workspace must be ordered on the device.
+ * Results do not depend on which physical blocks hold the tokens: the order of
+ * arithmetic depends only on logical positions, so any permutation of the pool
+ * gives bit-identical outputs.
+ */
+PKV_EXPORT pkv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int num_seqs, int num_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                  float scale, int partition_size, void *workspace,
+                                  size_t workspace_bytes, int dtype, void *stream);
+
+/*
+ * block_copy -- copy whole physical blocks, in every layer, for K and V.
+ *
+ * Source: troisinh page, section "Copy-on-Write cho Beam Search": sequences
+ * share the physical blocks of a common prefix and a block is split (copied)
+ * only when their tokens start to differ.  block_allocator_append_slot reports
+ * the (src, dst) pair to copy.
+ *
+ *   k_caches, v_caches  host arrays of num_layers device pointers (one cache
+ *                       tensor per layer, cache layout above)
+ *   block_pairs    device int64 [num_pairs][2] = (src, dst) physical block ids.
+ *                  A pair outside [0, num_blocks), or with src == dst, is
+ *                  skipped and flags PKV_DEVERR_COPY_PAIR.  A dst must not be
+ *                  the src or dst of another pair in the same call.
+ *   block_bytes    bytes of one physical block of one layer's K (or V) tensor:
+ *                  num_kv_heads * block_size * head_dim * element size; a
+ *                  positive multiple of 16.
+ * The copy is bit-exact.  num_pairs == 0 or num_layers == 0 returns PKV_OK.
+ */
+PKV_EXPORT pkv_status block_copy(void *const *k_caches, void *const *v_caches, int num_layers,
+                      const int64_t *block_pairs, int num_pairs, int num_blocks,
+                      size_t block_bytes, void *stream);
+
+/*
+ * pkv_read_device_errors -- wait for `stream`, then return in *flags_out the
+ * PKV_DEVERR_* bits set by kernels of this library on the current device since
+ * the last clear; clear != 0 resets the word afterwards.
+ */
+PKV_EXPORT pkv_status pkv_read_device_errors(uint32_t *flags_out, int clear, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator.
+ *
+ * Source: troisinh page, sections "Co che Block Table" (fixed blocks, a
+ * per-sequence table, a block only when a token needs it; 100 tokens -> 7
+ * blocks of 16; freed blocks reused at once without defragmentation) and
+ * "Copy-on-Write cho Beam Search"; aiwiki.vn page, paging paragraphs (blocks
+ * added on demand, waste concentrated in each sequence's last block, prefix
+ * blocks shared between branches).
+ *
+ * Policy: free blocks form a LIFO stack that first hands out 0, 1, 2, ...; a
+ * freed sequence pushes its blocks in table order.  Every operation is
+ * all-or-nothing: PKV_ERR_OOM / PKV_ERR_INVALID leave the state unchanged.
+ * A handle is not thread-safe; it owns host memory only.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_allocator pkv_allocator;
+
+/* NULL on bad arguments (num_blocks < 1, block_size < 1) or out of memory. */
+PKV_EXPORT pkv_allocator *block_allocator_create(int num_blocks, int block_size);
+PKV_EXPORT void block_allocator_destroy(pkv_allocator *a);
+
+/* New sequence `seq` holding num_tokens tokens (a prompt): ceil(n/B) blocks. */
+PKV_EXPORT pkv_status block_allocator_add_seq(pkv_allocator *a, int64_t seq, int64_t num_tokens);
+
+/* Room for one more token of `seq`.  *slot_out receives its slot.  If the last
+ * block is full (or absent) a fresh block is taken.  If the last block is
+ * partially filled and shared (reference count > 1), a fresh block replaces it
+ * in this sequence's table, the shared block loses one reference and
+ * (*cow_src_out, *cow_dst_out) name the pair to copy with block_copy before the
+ * token is written; otherwise both are -1.  Output pointers may be NULL. */
+PKV_EXPORT pkv_status block_allocator_append_slot(pkv_allocator *a, int64_t seq, int64_t *slot_out,
+                                       int32_t *cow_src_out, int32_t *cow_dst_out);
+
+/* One decode step's worth of append_slot for n distinct sequences, in order.
+ * slots_out: host int64 [n]; cow_pairs_out: host int64 [n][2] receives the
+ * (src, dst) pairs to copy, *n_cow_out of them (ready for block_copy).  All or
+ * nothing: PKV_ERR_OOM if the free stack cannot serve every sequence,
+ * PKV_ERR_INVALID for an unknown or repeated id; then nothing changes. */
+PKV_EXPORT pkv_status block_allocator_append_slots(pkv_allocator *a, const int64_t *seqs, int n,
+                                        int64_t *slots_out, int64_t *cow_pairs_out,
+                                        int *n_cow_out);
+
+/* `child` starts as a copy of `parent` that shares every block (refcount + 1). */
+PKV_EXPORT pkv_status block_allocator_fork(pkv_allocator *a, int64_t parent, int64_t child);
+
+/* Drop `seq`; blocks whose reference count reaches 0 return to the free stack. */
+PKV_EXPORT pkv_status block_allocator_free_seq(pkv_allocator *a, int64_t seq);
+
+/* Copy the block table of `seq` into out[0 .. cap); *n_out = its length.
+ * PKV_ERR_INVALID if the table is longer than cap (nothing written). */
+PKV_EXPORT pkv_status block_allocator_block_table(const pkv_allocator *a, int64_t seq, int32_t *out,
+                                       int cap, int *n_out);
+
+/* Dense tables for n sequences: out is host int32 [n][cap], rows padded with
+ * `pad`; seq_lens_out (host int32 [n], may be NULL) receives token counts. */
+PKV_EXPORT pkv_status block_allocator_block_tables(const pkv_allocator *a, const int64_t *seqs, int n,
+                                        int32_t *out, int cap, int32_t pad,
+                                        int32_t *seq_lens_out);
+
+/* Slots of token positions start .. start+count-1 of `seq` (all must exist). */
+PKV_EXPORT pkv_status block_allocator_slots(const pkv_allocator *a, int64_t seq, int64_t start,
+                                 int64_t count, int64_t *out);
+
+/* Token count of `seq`, or -1 if it does not exist. */
+PKV_EXPORT int64_t block_allocator_num_tokens(const pkv_allocator *a, int64_t seq);
+PKV_EXPORT int block_allocator_num_free(const pkv_allocator *a);
+/* Reference count of a physical block, -1 if the id is out of range. */
+PKV_EXPORT int block_allocator_refcount(const pkv_allocator *a, int32_t block);
+
+/* Occupied slots and allocated slots over all live sequences, each physical
+ * block counted once however many sequences share it.  Waste fraction =
+ * 1 - used / allocated. */
+PKV_EXPORT pkv_status block_allocator_waste(const pkv_allocator *a, int64_t *used_tokens,
+                                 int64_t *allocated_slots);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,111 @@
+"""Test-side helpers: place contiguous per-sequence K/V into a paged pool on
+the host, move things to the GPU, and compare GPU results with the oracle under
+the stated tolerances.  Nothing here is used by the library."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_279_gb300 as pkv
+from paged_kv_cache_279_gb300 import workloads as wl
+
+BF16_MAX_ABS = 1e-2
+BF16_MEAN_ABS = 1e-3
+F32_MAX_ABS = 1e-5
+
+
+def token_slots(table_row, length, block_size):
+    """Slots of positions 0..length-1: logical block p // B of the table, offset p % B."""
+    pos = np.arange(length, dtype=np.int64)
+    return np.asarray(table_row, dtype=np.int64)[pos // block_size] * block_size + pos % block_size
+
+
+def place_paged(k_seqs, v_seqs, tables, num_blocks, block_size, dtype, fill=float("nan")):
+    """Host pools [NB, Hkv, B, D] holding each sequence's tokens at the slots its
+    table names; every other slot holds ``fill``."""
+    Hkv, D = k_seqs[0].shape[1], k_seqs[0].shape[2]
+    kc = torch.full((num_blocks, Hkv, block_size, D), fill, dtype=dtype)
+    vc = torch.full_like(kc, fill)
+    for s, (k, v) in enumerate(zip(k_seqs, v_seqs)):
+        L = k.shape[0]
+        if L == 0:
+            continue
+        slots = torch.from_numpy(token_slots(tables[s], L, block_size))
+        kc[slots // block_size, :, slots % block_size, :] = k
+        vc[slots // block_size, :, slots % block_size, :] = v
+    return kc, vc
+
+
+def make_decode_case(shape: wl.DecodeShape, lens, seed=0, num_blocks=None, fill=float("nan"),
+                     table_seed=None, extra_blocks=0):
+    """Contiguous data (for the oracle) and a randomly placed paged pool (for the GPU)."""
+    lens = [int(x) for x in lens]
+    B = shape.block_size
+    counts = [-(-L // B) for L in lens]
+    NB = num_blocks or max(1, sum(counts) + extra_blocks)
+    maxB = max(1, max(counts) if counts else 1)
+    tables = wl.random_block_tables(counts, NB, maxB, seed if table_seed is None else table_seed)
+    ks, vs = zip(*[wl.draw_seq_kv(shape, seed, s, L) for s, L in enumerate(lens)])
+    q = wl.draw_query(shape, seed, num_seqs=len(lens))
+    kc, vc = place_paged(ks, vs, tables, NB, B, shape.dtype, fill)
+    return dict(q=q, ks=list(ks), vs=list(vs), tables=tables, lens=lens, kc=kc, vc=vc, NB=NB,
+                maxB=maxB)
+
+
+def run_decode(case, shape, partition_size=0, max_seq_len=None, device="cuda"):
+    q = case["q"].to(device)
+    out = torch.empty_like(q)
+    maxL = max_seq_len if max_seq_len is not None else max(1, max(case["lens"]))
+    pkv.paged_attention_decode(
+        out, q, case["kc_dev"] if "kc_dev" in case else case["kc"].to(device),
+        case["vc_dev"] if "vc_dev" in case else case["vc"].to(device),
+        torch.from_numpy(case["tables"]).to(device),
+        torch.tensor(case["lens"], dtype=torch.int32, device=device), shape.scale, maxL,
+        partition_size=partition_size)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_out(case, shape, seqs=None):
+    idx = range(len(case["lens"])) if seqs is None else seqs
+    q = case["q"].float().numpy()[list(idx)]
+    ks = [case["ks"][s].float().numpy() for s in idx]
+    vs = [case["vs"][s].float().numpy() for s in idx]
+    return oracle.decode_attention(q, ks, vs, shape.scale)
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.exp2(np.floor(np.log2(ax)) - 7)
+
+
+def assert_bf16_close(got: torch.Tensor, ref: np.ndarray, what=""):
+    """max-abs 1e-2 and mean-abs 1e-3 against the fp64 oracle; where |ref| >= 4
+    one bf16 rounding alone can exceed 1e-2, so there the bound is one bf16 ulp."""
+    g = got.double().cpu().numpy()
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    big = np.abs(ref) >= 4.0
+    small_err = err[~big]
+    assert small_err.size == 0 or small_err.max() <= BF16_MAX_ABS, f"{what}: max abs err {small_err.max():.3e}"
+    if big.any():
+        assert np.all(err[big] <= bf16_ulp(ref[big])), f"{what}: large-value error above one ulp"
+    assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def assert_f32_close(got: torch.Tensor, ref: np.ndarray, what=""):
+    g = got.double().cpu().numpy()
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    assert err.max() <= F32_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def bits(t: torch.Tensor) -> torch.Tensor:
+    """Integer view for bit-exact comparisons (NaN payloads included)."""
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)

@@ -1,0 +1,81 @@
+"""The C-ABI library loads without a GPU, exports every function that
+include/pkv.h declares, and rejects bad arguments on the host before any
+device work (these calls return before touching CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_279_gb300 as pkv
+from paged_kv_cache_279_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    # every declaration is marked PKV_EXPORT: take the identifier before "("
+    names = re.findall(r"^PKV_EXPORT [^;(]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = _lib.load()
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), f"libpkv.so does not export {n}"
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_status_strings_and_version():
+    lib = _lib.load()
+    assert lib.pkv_abi_version() == 1
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(2) == b"out of KV blocks"
+    assert lib.pkv_status_string(99) == b"unknown status"
+
+
+def test_host_validation_rejects_before_launch():
+    lib = _lib.load()
+    # unsupported head_dim / block size / dtype: rejected on the host
+    assert lib.kv_cache_write(None, None, None, None, None, 4, 8, 96, 16, 64, 1, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert lib.kv_cache_write(None, None, None, None, None, 4, 8, 128, 12, 64, 1, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert lib.kv_cache_write(None, None, None, None, None, 4, 8, 128, 16, 64, 7, None) == pkv.PKV_ERR_UNSUPPORTED
+    # null pointers with work to do
+    assert lib.kv_cache_write(None, None, None, None, None, 4, 8, 128, 16, 64, 1, None) == pkv.PKV_ERR_INVALID
+    # nothing to do is fine
+    assert lib.kv_cache_write(None, None, None, None, None, 0, 8, 128, 16, 64, 1, None) == pkv.PKV_OK
+    dec = lib.paged_attention_decode
+    common = dict(S=2, Hq=32, Hkv=8, D=128, B=16, maxB=4, NB=16, maxL=64)
+
+    def call(S=2, Hq=32, Hkv=8, D=128, B=16, maxB=4, NB=16, maxL=64, P=0, dt=1, scale=0.1):
+        return dec(None, None, None, None, None, None, S, Hq, Hkv, D, B, maxB, NB, maxL, scale, P,
+                   None, 0, dt, None)
+    assert call(Hq=30) == pkv.PKV_ERR_INVALID          # Hq not a multiple of Hkv
+    assert call(Hq=72) == pkv.PKV_ERR_UNSUPPORTED      # 9 query heads per KV head
+    assert call(D=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(P=24) == pkv.PKV_ERR_INVALID           # partition not a multiple of 16
+    assert call(scale=float("nan")) == pkv.PKV_ERR_INVALID
+    assert call(S=0) == pkv.PKV_OK
+    assert call() == pkv.PKV_ERR_INVALID               # null pointers
+    assert lib.block_copy(None, None, 0, None, 5, 16, 4096, None) == pkv.PKV_OK
+    assert lib.block_copy(None, None, 2, None, 5, 16, 4096, None) == pkv.PKV_ERR_INVALID
+    assert lib.block_copy(None, None, 2, None, 5, 16, 4000, None) == pkv.PKV_ERR_INVALID
+    flags = ctypes.c_uint32()
+    assert lib.pkv_read_device_errors(None, 0, None) == pkv.PKV_ERR_INVALID
+    del flags
+
+
+def test_workspace_size_formula():
+    lib = _lib.load()
+    # a single partition needs no scratch
+    assert lib.paged_attention_workspace_size(64, 32, 128, 512, 512) == 0
+    # 8 sequences x 32 heads x 32 partitions: o (fp32, 128 wide) + max + sum
+    n = 8 * 32 * 32
+    want = n * 128 * 4 + ((n * 4 + 255) // 256) * 256 * 2
+    assert lib.paged_attention_workspace_size(8, 32, 128, 16000, 512) == want
+    assert lib.paged_attention_workspace_size(8, 32, 128, 16000, 0) == want  # default is 512
+    assert lib.paged_attention_workspace_size(8, 32, 128, 16000, 24) == 0    # invalid partition

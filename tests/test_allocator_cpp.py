@@ -1,0 +1,150 @@
+"""The library's C++ allocator against the oracle's allocator model,
+operation by operation (statuses, slots, copy pairs, tables, refcounts,
+free counts and waste must all be identical)."""
+import random
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_279_gb300 as pkv
+from oracle import BlockAllocatorModel
+
+
+def assert_same_state(c, m, seqs):
+    assert c.num_free() == m.num_free()
+    for b in range(m.num_blocks):
+        assert c.refcount(b) == m.refcount(b)
+    for s in seqs:
+        assert c.block_table(s) == m.block_table(s)
+        assert c.num_tokens(s) == m.num_tokens(s)
+    assert c.waste() == m.waste()
+
+
+def run_ops(ops, num_blocks, block_size):
+    c = pkv.BlockAllocator(num_blocks, block_size)
+    m = BlockAllocatorModel(num_blocks, block_size)
+    for op in ops:
+        kind = op[0]
+        if kind == "add":
+            assert c.add_seq(op[1], op[2]) == m.add_seq(op[1], op[2])
+        elif kind == "append":
+            assert c.append_slot(op[1]) == m.append_slot(op[1])
+        elif kind == "fork":
+            assert c.fork(op[1], op[2]) == m.fork(op[1], op[2])
+        elif kind == "free":
+            assert c.free_seq(op[1]) == m.free_seq(op[1])
+        assert_same_state(c, m, m.sequences())
+    return c, m
+
+
+def random_ops(rnd, n, block_size):
+    ops, ids = [], []
+    for _ in range(n):
+        r = rnd.random()
+        if r < 0.2 or not ids:
+            ids.append(len(ids) + rnd.randint(0, 2))  # occasionally a duplicate id
+            ops.append(("add", ids[-1], rnd.randint(0, 3 * block_size)))
+        elif r < 0.65:
+            ops.append(("append", rnd.choice(ids + [999])))
+        elif r < 0.8:
+            child = len(ids) + 100
+            ops.append(("fork", rnd.choice(ids), child))
+            ids.append(child)
+        else:
+            ops.append(("free", rnd.choice(ids)))
+    return ops
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_sequences_match_model(seed):
+    rnd = random.Random(seed)
+    B = rnd.choice([1, 4, 8, 16, 32])
+    run_ops(random_ops(rnd, 250, B), rnd.randint(1, 48), B)
+
+
+def test_hypothesis_sequences_match_model():
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    op = st.one_of(
+        st.tuples(st.just("add"), st.integers(0, 6), st.integers(0, 40)),
+        st.tuples(st.just("append"), st.integers(0, 6)),
+        st.tuples(st.just("fork"), st.integers(0, 6), st.integers(0, 6)),
+        st.tuples(st.just("free"), st.integers(0, 6)),
+    )
+
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True)
+    @hyp.given(st.lists(op, max_size=60), st.integers(1, 20), st.sampled_from([1, 2, 4, 16]))
+    def prop(ops, nb, bs):
+        run_ops(ops, nb, bs)
+
+    prop()
+
+
+def test_beam_fork_copy_pairs_and_dense_tables():
+    c = pkv.BlockAllocator(400, 16)
+    assert c.add_seq(0, 1032) == 0
+    for k in range(1, 8):
+        assert c.fork(0, k) == 0
+    pairs = []
+    for k in range(8):
+        st, slot, src, dst = c.append_slot(k)
+        assert st == 0
+        if src >= 0:
+            pairs.append((src, dst))
+    assert len(pairs) == 7
+    tables, lens = c.block_tables(list(range(8)), cap=70, pad=-5)
+    assert tables.shape == (8, 70) and (lens == 1033).all()
+    assert (tables[:, 66:] == -5).all()
+    assert len(set(tables[:, 64].tolist())) == 8  # every beam now owns its last block
+    assert (tables[:, :64] == tables[0, :64]).all()  # full prefix blocks still shared
+    slots = c.slots(3, 1030, 3)
+    t3 = c.block_table(3)
+    assert slots.tolist() == [t3[p // 16] * 16 + p % 16 for p in (1030, 1031, 1032)]
+    with pytest.raises(pkv.PkvError):
+        c.slots(3, 1030, 10)  # past the end
+    with pytest.raises(pkv.PkvError):
+        c.block_tables([0, 1], cap=10)  # too narrow
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_batched_append_matches_sequential_model(seed):
+    rnd = random.Random(100 + seed)
+    B = rnd.choice([4, 16])
+    NB = rnd.randint(8, 60)
+    c = pkv.BlockAllocator(NB, B)
+    m = BlockAllocatorModel(NB, B)
+    live = []
+    for sid in range(6):
+        n = rnd.randint(0, 2 * B)
+        assert c.add_seq(sid, n) == m.add_seq(sid, n)
+        if sid in m.sequences():
+            live.append(sid)
+    for sid in list(live)[:3]:
+        child = 100 + sid
+        if c.fork(sid, child) == 0:
+            m.fork(sid, child)
+            live.append(child)
+    for step in range(40):
+        batch = rnd.sample(live, rnd.randint(1, len(live)))
+        st, slots, pairs = c.append_slots(batch)
+        # model: all or nothing over the sequential semantics
+        need = sum(1 for s in batch
+                   if m.num_tokens(s) % B == 0 or m.refcount(m.block_table(s)[-1]) > 1)
+        if need > m.num_free():
+            assert st == 2
+            assert_same_state(c, m, live)
+            continue
+        assert st == 0
+        want_slots, want_pairs = [], []
+        for s in batch:
+            mst, slot, src, dst = m.append_slot(s)
+            assert mst == 0
+            want_slots.append(slot)
+            if src >= 0:
+                want_pairs.append((src, dst))
+        assert slots.tolist() == want_slots
+        assert [tuple(p) for p in pairs.tolist()] == want_pairs
+        assert_same_state(c, m, live)
+    st, _, _ = c.append_slots([live[0], live[0]])
+    assert st == 1  # repeated id

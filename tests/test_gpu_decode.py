@@ -1,0 +1,173 @@
+"""Paged decode attention on the GPU against the fp64 oracle, on sizes that
+span several tiles, partitions and ragged tails, plus the properties the
+method fixes: physical placement does not matter (bit-identical), a single
+token returns its value, constant values come back unchanged, the split into
+partitions does not change the result beyond rounding, empty contexts give
+zeros, and bad indices are reported without a fault."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_279_gb300 as pkv
+from paged_kv_cache_279_gb300 import workloads as wl
+from harness import (assert_bf16_close, assert_f32_close, bits, make_decode_case, oracle_out,
+                     run_decode)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clear_errors():
+    pkv.read_device_errors(clear=True)
+    yield
+
+
+def shape_of(Hq, Hkv, D, B, dtype=torch.bfloat16):
+    return wl.DecodeShape(f"t{Hq}_{Hkv}_{D}_{B}", 0, Hq, Hkv, D, B, dtype)
+
+
+def test_tiny_fp32_workload_with_cache_write():
+    """4 sequences {1, 17, 33, 100}, 4/4 heads, head_dim 64, block 16, pool of 64
+    blocks assigned by a seeded permutation; the newest token of each sequence
+    is written with kv_cache_write before the decode."""
+    shape = wl.TINY_FP32
+    lens = wl.draw_lengths(shape, seed=0).tolist()
+    case = make_decode_case(shape, lens, seed=0, num_blocks=64)
+    kc, vc = case["kc"].clone(), case["vc"].clone()
+    # remove the newest token from the pool, then write it through the library
+    slots = []
+    for s, L in enumerate(lens):
+        slot = int(case["tables"][s][(L - 1) // 16]) * 16 + (L - 1) % 16
+        slots.append(slot)
+        kc[slot // 16, :, slot % 16] = float("nan")
+        vc[slot // 16, :, slot % 16] = float("nan")
+    case["kc_dev"], case["vc_dev"] = kc.cuda(), vc.cuda()
+    k_new = torch.stack([case["ks"][s][L - 1] for s, L in enumerate(lens)]).cuda()
+    v_new = torch.stack([case["vs"][s][L - 1] for s, L in enumerate(lens)]).cuda()
+    pkv.kv_cache_write(k_new, v_new, case["kc_dev"], case["vc_dev"],
+                       torch.tensor(slots, dtype=torch.int64, device="cuda"))
+    assert torch.equal(bits(case["kc_dev"].cpu()), bits(case["kc"]))
+    out = run_decode(case, shape)
+    assert_f32_close(out, oracle_out(case, shape), "tiny fp32")
+    assert pkv.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,B,lens,P", [
+    (32, 8, 128, 16, [1, 15, 16, 17, 100, 513, 1000], 0),
+    (32, 8, 128, 16, [1, 15, 16, 17, 100, 513, 1000], 64),
+    (64, 8, 128, 16, [3, 700, 1100], 128),
+    (8, 8, 128, 16, [5, 47, 300], 0),      # MHA
+    (16, 8, 128, 16, [33, 257], 48),       # 2 query heads per KV head
+    (32, 8, 64, 16, [9, 160, 999], 256),
+    (32, 4, 128, 8, [1, 8, 9, 95, 600], 96),
+    (32, 4, 128, 32, [1, 31, 32, 33, 700], 64),
+    (24, 4, 64, 32, [2, 2000], 512),
+    (8, 1, 128, 16, [4096], 0),            # one KV head, 8 partitions
+])
+def test_bf16_decode_matches_oracle(Hq, Hkv, D, B, lens, P):
+    shape = shape_of(Hq, Hkv, D, B)
+    case = make_decode_case(shape, lens, seed=Hq + D + B + P, extra_blocks=7)
+    out = run_decode(case, shape, partition_size=P)
+    assert_bf16_close(out, oracle_out(case, shape), f"{shape.name} P={P}")
+    assert pkv.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,B", [(4, 4, 64, 16), (8, 2, 128, 8), (16, 2, 64, 32)])
+@pytest.mark.parametrize("P", [0, 32])
+def test_fp32_decode_matches_oracle(Hq, Hkv, D, B, P):
+    shape = shape_of(Hq, Hkv, D, B, torch.float32)
+    case = make_decode_case(shape, [1, 30, 77, 130], seed=3 + Hq + B)
+    out = run_decode(case, shape, partition_size=P)
+    assert_f32_close(out, oracle_out(case, shape), f"fp32 {shape.name} P={P}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_physical_placement_is_irrelevant_bit_identical(dtype):
+    shape = shape_of(32, 8, 128, 16, dtype)
+    lens = [1, 37, 300, 1024]
+    a = make_decode_case(shape, lens, seed=11, table_seed=1, extra_blocks=40)
+    b = make_decode_case(shape, lens, seed=11, table_seed=2, extra_blocks=40)
+    assert not np.array_equal(a["tables"], b["tables"])
+    for P in (0, 64):
+        oa = run_decode(a, shape, partition_size=P)
+        ob = run_decode(b, shape, partition_size=P)
+        assert torch.equal(bits(oa.cpu()), bits(ob.cpu()))
+
+
+def test_single_token_context_returns_its_value_exactly():
+    shape = shape_of(64, 8, 128, 16)
+    case = make_decode_case(shape, [1] * 9, seed=4)
+    out = run_decode(case, shape).cpu()
+    for s in range(9):
+        want = case["vs"][s][0].repeat_interleave(8, dim=0)  # [Hq, D]
+        assert torch.equal(bits(out[s]), bits(want))
+
+
+def test_constant_values_come_back_unchanged():
+    shape = shape_of(32, 8, 128, 16)
+    case = make_decode_case(shape, [5, 200, 1500], seed=5)
+    for s, v in enumerate(case["vs"]):
+        v.fill_(1.5)
+    case["vc"] = torch.where(torch.isnan(case["vc"]), case["vc"], torch.full_like(case["vc"], 1.5))
+    out = run_decode(case, shape, partition_size=64).float().cpu()
+    assert torch.all(out == 1.5)
+
+
+def test_partition_sizes_agree():
+    shape = shape_of(32, 8, 128, 16)
+    lens = [700, 2048, 16, 1]
+    case = make_decode_case(shape, lens, seed=6)
+    ref = oracle_out(case, shape)
+    outs = {}
+    for P in (16, 64, 512, 4096, 0):
+        outs[P] = run_decode(case, shape, partition_size=P)
+        assert_bf16_close(outs[P], ref, f"P={P}")
+    # one partition covering everything is the plain single pass
+    assert torch.equal(bits(run_decode(case, shape, partition_size=2048).cpu()),
+                       bits(run_decode(case, shape, partition_size=4096).cpu()))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_empty_context_gives_zeros(dtype):
+    shape = shape_of(8, 2, 64, 16, dtype)
+    case = make_decode_case(shape, [0, 20, 0, 600], seed=7)
+    out = run_decode(case, shape, partition_size=64).float().cpu()
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert torch.isfinite(out).all()
+    ref = oracle_out(case, shape)
+    if dtype == torch.bfloat16:
+        assert_bf16_close(out.to(torch.bfloat16), ref)
+    else:
+        assert_f32_close(out, ref)
+
+
+def test_bad_block_id_and_length_are_flagged_not_faulted():
+    shape = shape_of(32, 8, 128, 16)
+    case = make_decode_case(shape, [40, 40], seed=8)
+    case["tables"] = case["tables"].copy()
+    case["tables"][0, 1] = case["NB"] + 5          # out of the pool
+    case["tables"][1, 0] = -3
+    out = run_decode(case, shape)
+    assert pkv.read_device_errors() & pkv.DEVERR_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
+    # a length beyond max_seq_len is clamped and reported
+    case2 = make_decode_case(shape, [40, 64], seed=9)
+    run_decode(case2, shape, max_seq_len=48)
+    assert pkv.read_device_errors() & pkv.DEVERR_SEQ_LEN
+
+
+def test_workspace_too_small_is_rejected():
+    shape = shape_of(32, 8, 128, 16)
+    case = make_decode_case(shape, [1000], seed=10)
+    q = case["q"].cuda()
+    need = pkv.paged_attention_workspace_size(1, 32, 128, 1000, 64)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_attention_decode(torch.empty_like(q), q, case["kc"].cuda(), case["vc"].cuda(),
+                                   torch.from_numpy(case["tables"]).cuda(),
+                                   torch.tensor([1000], dtype=torch.int32, device="cuda"),
+                                   shape.scale, 1000, partition_size=64, workspace=ws)
+    assert e.value.status == pkv.PKV_ERR_INVALID
