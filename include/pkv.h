@@ -59,7 +59,8 @@ typedef enum pkv_status {
     PKV_ERR_OOM = 2,         /* the allocator has no free block; nothing changed */
     PKV_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
     PKV_ERR_UNSUPPORTED = 4, /* valid shape outside the supported set */
-    PKV_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+    PKV_ERR_TIMEOUT = 5,     /* reserved: a bounded device wait gave up */
+    PKV_ERR_TOO_LARGE = 6    /* needs more than the library's built-in scratch */
 } pkv_status;
 
 typedef enum pkv_dtype {
@@ -180,6 +181,44 @@ PKV_EXPORT pkv_status paged_attention_decode(void *out, const void *q, const voi
 PKV_EXPORT pkv_status block_copy(void *const *k_caches, void *const *v_caches, int num_layers,
                       const int64_t *block_pairs, int num_pairs, int num_blocks,
                       size_t block_bytes, void *stream);
+
+/*
+ * paged_attention_decode_noalloc -- paged_attention_decode for callers that
+ * cannot allocate device memory.  No passage of the pages has a counterpart:
+ * this entry point exists for the caller, not for the method.
+ *
+ * Some callers have no way to hand the library a scratch buffer: code that
+ * runs where cudaMalloc is forbidden or unavailable (inside a custom memory
+ * pool that owns all device memory, a plugin host that only passes tensors
+ * in and out, a runtime that must not allocate on its decode path).  This
+ * variant takes the same inputs and outputs as paged_attention_decode minus
+ * the workspace; the split-K partials live instead in a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library, which every
+ * GPU that loads the library keeps until the process exits.
+ *
+ *   partition_size 0 = 512-token partitions; otherwise as for
+ *                  paged_attention_decode.  The split always uses fixed
+ *                  partitions plus the merge kernel.
+ *   Returns PKV_ERR_TOO_LARGE, with nothing enqueued, when the partials for
+ *   (num_seqs, num_heads, head_dim, max_seq_len, partition_size) need more
+ *   than PKV_NOALLOC_SCRATCH_BYTES (see paged_attention_workspace_size).
+ *   Every other argument and error behaves as in paged_attention_decode.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress) with the device current; make that first call before
+ * any stream capture.  Every call on a device shares the one array and leaves
+ * its partials there: nothing in it has to start at zero (each call writes
+ * every partial it later reads), but calls whose work overlaps on the GPU --
+ * two streams, or two host threads -- race on it and must be serialised by
+ * the caller.  The call itself allocates nothing.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+PKV_EXPORT pkv_status paged_attention_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int num_seqs, int num_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                  float scale, int partition_size, int dtype, void *stream);
 
 /*
  * pkv_read_device_errors -- wait for `stream`, then return in *flags_out the

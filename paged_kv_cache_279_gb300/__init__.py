@@ -21,7 +21,9 @@ import torch
 
 from . import _lib
 
-PKV_OK, PKV_ERR_INVALID, PKV_ERR_OOM, PKV_ERR_CUDA, PKV_ERR_UNSUPPORTED, PKV_ERR_TIMEOUT = range(6)
+(PKV_OK, PKV_ERR_INVALID, PKV_ERR_OOM, PKV_ERR_CUDA, PKV_ERR_UNSUPPORTED, PKV_ERR_TIMEOUT,
+ PKV_ERR_TOO_LARGE) = range(7)
+NOALLOC_SCRATCH_BYTES = 16 << 20
 PKV_F32, PKV_BF16 = 0, 1
 DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 

@@ -25,6 +25,9 @@ SIGNATURES = {
     "paged_attention_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                        c_float, c_int, c_void_p, c_size_t, c_int, c_void_p]),
+    "paged_attention_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                               c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                               c_int, c_int, c_float, c_int, c_int, c_void_p]),
     "block_copy": (c_int, [P(c_void_p), P(c_void_p), c_int, c_void_p, c_int, c_int, c_size_t,
                            c_void_p]),
     "pkv_read_device_errors": (c_int, [P(c_uint32), c_int, c_void_p]),

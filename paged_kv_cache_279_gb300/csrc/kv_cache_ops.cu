@@ -97,6 +97,7 @@ PKV_API const char *pkv_status_string(int status) {
         case PKV_ERR_CUDA: return "CUDA error";
         case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
         case PKV_ERR_TIMEOUT: return "device wait timed out";
+        case PKV_ERR_TOO_LARGE: return "needs more scratch than the library's built-in array";
         default: return "unknown status";
     }
 }

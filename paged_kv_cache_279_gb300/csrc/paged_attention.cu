@@ -825,3 +825,51 @@ PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *
     }
     return rc;
 }
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace (paged_attention_decode_noalloc).
+// For callers that cannot allocate device memory, the split-K partials live
+// in this array, compiled into the library and resident on every device that
+// loads it until the process exits.  Host code must not use the symbol's
+// name as a device address (on the host it is only a stand-in); the device
+// address is looked up once per device below.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call for that device (with the device current).  nullptr on failure.
+static void *noalloc_scratch_address() {
+    static std::mutex mu;
+    static void *ptrs[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress((void **)&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+PKV_API pkv_status paged_attention_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                                  const void *v_cache, const int32_t *block_tables,
+                                                  const int32_t *seq_lens, int num_seqs, int num_heads,
+                                                  int num_kv_heads, int head_dim, int block_size,
+                                                  int max_blocks_per_seq, int num_blocks,
+                                                  int max_seq_len, float scale, int partition_size,
+                                                  int dtype, void *stream) {
+    if (partition_size < 0 || partition_size % kTile != 0) return PKV_ERR_INVALID;
+    const int P = partition_size > 0 ? partition_size : 512;
+    const size_t need = paged_attention_workspace_size(num_seqs, num_heads, head_dim, max_seq_len, P);
+    if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_TOO_LARGE;
+    void *scratch = nullptr;
+    if (need > 0) {
+        scratch = noalloc_scratch_address();
+        if (!scratch) return PKV_ERR_CUDA;
+    }
+    return paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                  num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                  num_blocks, max_seq_len, scale, P, scratch,
+                                  need > 0 ? PKV_NOALLOC_SCRATCH_BYTES : 0, dtype, stream);
+}
