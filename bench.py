@@ -239,7 +239,7 @@ class Batch:
         self.partition_size = partition_size
         ws = pkv.paged_attention_workspace_size(S, shape.num_heads, D, self.max_seq_len,
                                                 partition_size)
-        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         self.pkv = pkv
 
     def write(self):
@@ -472,7 +472,7 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     d_slot = torch.empty(S, dtype=torch.int64, device=device)
     d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
     max_seq_len = cap * shape.block_size
-    ws = torch.empty(max(256, pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim,
+    ws = torch.zeros(max(256, pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim,
                                                                  max_seq_len, args.partition_size)),
                      dtype=torch.uint8, device=device)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len, h_slot))

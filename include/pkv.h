@@ -106,10 +106,11 @@ PKV_EXPORT pkv_status kv_cache_write(const void *k_new, const void *v_new, void 
 /*
  * paged_attention_workspace_size -- bytes of device scratch that
  * paged_attention_decode needs for the same (num_seqs, num_heads, head_dim,
- * max_seq_len, partition_size).  0 when a single pass suffices (every
- * sequence fits one partition).  The scratch holds one partial result per
- * (sequence, query head, partition): running max, running sum and an
- * unnormalised output row, all float32.
+ * max_seq_len, partition_size).  With partition_size > 0 it is 0 when a
+ * single pass suffices (every sequence fits one partition).  The scratch holds
+ * one partial result per (sequence, query head, piece of context): running
+ * max, running sum and an unnormalised output row, all float32; with
+ * partition_size == 0 also one piece count per (sequence, query head).
  */
 PKV_EXPORT size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
                                       int max_seq_len, int partition_size);
@@ -139,10 +140,15 @@ PKV_EXPORT size_t paged_attention_workspace_size(int num_seqs, int num_heads, in
  *                  <= max_blocks_per_seq * block_size (larger values are
  *                  clamped and flagged with PKV_DEVERR_SEQ_LEN)
  *   scale          multiplies every q.k score (typically 1/sqrt(head_dim))
- *   partition_size 0 = let the library choose; otherwise a positive multiple of
- *                  16.  Contexts longer than one partition are split: each
- *                  partition is attended independently and a reduction kernel
- *                  merges the partials (max-rescaled sums), all on `stream`.
+ *   partition_size a positive multiple of 16: contexts longer than one
+ *                  partition are split into partitions of that many tokens,
+ *                  each attended independently, and a reduction kernel merges
+ *                  the partials (max-rescaled sums), all on `stream`.
+ *                  0 = balanced split (bf16): all (sequence, kv head) contexts
+ *                  are laid end to end and cut into equal shares of at least
+ *                  256 tokens, one per resident warp; a context cut by share
+ *                  boundaries is merged by the same reduction kernel.  fp32
+ *                  (or more than 8192 sequences) uses 512-token partitions.
  *   workspace      device scratch of at least paged_attention_workspace_size()
  *                  bytes for the same arguments (may be NULL when that is 0),
  *                  256-byte aligned.  Contents need no initialisation; calls

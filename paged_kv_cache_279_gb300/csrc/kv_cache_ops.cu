@@ -39,6 +39,9 @@ kv_cache_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__
                       const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
                       int num_kv_heads, int chunks_per_row, int block_size,
                       int64_t num_slots, unsigned int *err) {
+    // a dependent decode kernel may start its launch while this one runs; it
+    // waits for this grid before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t per_token = (int64_t)num_kv_heads * chunks_per_row;
     const int64_t total = num_tokens * per_token;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;

@@ -59,6 +59,7 @@ struct DecodeArgs {
     float *part_o;  // [S][Hq][max_parts][D]
     float *part_m;  // [S][Hq][max_parts]
     float *part_l;  // [S][Hq][max_parts]
+    int *pieces;    // [S][Hkv]: partials of each segment (balanced path)
     int num_seqs, num_heads, num_kv_heads, group;
     int block_size, max_blocks, num_blocks, max_seq_len;
     int partition_size, max_parts;
@@ -72,6 +73,15 @@ struct DecodeArgs {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on
+// (no-op when launched without the attribute), and let dependents launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -251,11 +261,214 @@ struct Bf16Layout {
     static constexpr int kMergeBytes = (kGMax * D + 2 * kGMax) * 4;
 };
 
+constexpr int kBtCache = 256;  // block ids of one partition kept in shared memory
+
 template <int D, int NW, int NS>
 constexpr int bf16_smem_bytes() {
-    return NW * NS * Bf16Layout<D>::kStageBytes + NW * NS * 8 + 1024;
+    return NW * NS * Bf16Layout<D>::kStageBytes + NW * NS * 8 + kBtCache * 4 + 1024;
 }
 
+// Running softmax state of one warp for up to 8 query heads (MMA fragment
+// layout: this lane holds heads 2tq and 2tq+1, head_dim rows r0 and r0+8 of
+// every 16-row slice).
+template <int D>
+struct WarpAcc {
+    float m0, m1, l0, l1;
+    float o[D / 16][4];
+    __device__ __forceinline__ void reset() {
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    }
+};
+
+// Q^T as the MMA B operand: lane holds query head r0 (zero past the group),
+// head_dim pairs 16ks + 2tq (+8).
+template <int D>
+__device__ __forceinline__ void load_q_fragments(const DecodeArgs &a, int seq, int kvh, int lane,
+                                                 uint32_t (&qb)[D / 16][2]) {
+    const int r0 = lane >> 2, tq = lane & 3;
+    const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(a.q) +
+                                ((int64_t)seq * a.num_heads + kvh * a.group + r0) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        if (r0 < a.group) {
+            qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tq);
+            qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tq);
+        } else {
+            qb[ks][0] = qb[ks][1] = 0u;
+        }
+    }
+}
+
+// Attend one staged 16-token tile (K at sk, V at sv, 128-byte swizzled
+// halves).  row_ok has a bit per token row that belongs to the context and
+// came from a valid block; other rows are masked and their V zeroed.
+template <int D>
+__device__ __forceinline__ void attend_tile(unsigned char *sk, unsigned char *sv, uint32_t row_ok,
+                                            const uint32_t (&qb)[D / 16][2], float sl2,
+                                            WarpAcc<D> &acc, int lane) {
+    using Lay = Bf16Layout<D>;
+    const int r0 = lane >> 2;
+    if (row_ok != 0xffffu) {
+        // masked rows hold stale, unwritten or substituted slots: zero their
+        // V so that a zero weight never meets a NaN
+        for (int e = lane; e < Lay::kHalves * kTile * 8; e += 32) {
+            const int h = e / (kTile * 8), rr = (e / 8) % kTile, c = e % 8;
+            if (!((row_ok >> rr) & 1u))
+                *reinterpret_cast<uint4 *>(sv + h * Lay::kHalfBytes + rr * 128 + c * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+    }
+    const uint32_t ska = smem_u32(sk), sva = smem_u32(sv);
+    const int lj = lane >> 3, lr = lane & 7;
+
+    // S^T (16 tokens x 8 heads) = K_tile . Q^T
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const int tok = lr + 8 * (lj & 1);
+        const int chunk = 2 * (ks & 3) + (lj >> 1);
+        const uint32_t addr = ska + (ks >> 2) * Lay::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+        uint32_t x0, x1, x2, x3;
+        ldmatrix_x4(addr, x0, x1, x2, x3);
+        mma_bf16_16816(sc, x0, x1, x2, x3, qb[ks][0], qb[ks][1]);
+    }
+
+    // online softmax, base 2; rows r0 and r0+8, columns 2tq and 2tq+1
+    const bool ok_lo = (row_ok >> r0) & 1u, ok_hi = (row_ok >> (r0 + 8)) & 1u;
+    const float s0 = ok_lo ? sc[0] * sl2 : -INFINITY;
+    const float s1 = ok_lo ? sc[1] * sl2 : -INFINITY;
+    const float s2 = ok_hi ? sc[2] * sl2 : -INFINITY;
+    const float s3 = ok_hi ? sc[3] * sl2 : -INFINITY;
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+    }
+    const float mn0 = fmaxf(acc.m0, mx0), mn1 = fmaxf(acc.m1, mx1);
+    // reference points stay finite even if nothing valid has been seen yet
+    const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(acc.m0 - rf0), al1 = exp2f(acc.m1 - rf1);
+    acc.m0 = mn0;
+    acc.m1 = mn1;
+    const uint32_t p01 = pack_bf16x2(exp2f(s0 - rf0), exp2f(s1 - rf1));
+    const uint32_t p23 = pack_bf16x2(exp2f(s2 - rf0), exp2f(s3 - rf1));
+    // the sum uses the same rounded weights as the numerator
+    acc.l0 = acc.l0 * al0 + (bf16x2_lo(p01) + bf16x2_lo(p23));
+    acc.l1 = acc.l1 * al1 + (bf16x2_hi(p01) + bf16x2_hi(p23));
+    const uint32_t pb0 = movmatrix_trans(p01);
+    const uint32_t pb1 = movmatrix_trans(p23);
+
+    // O^T (head_dim x 8 heads) = O^T * alpha + V_tile^T . P^T
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        acc.o[mt][0] *= al0;
+        acc.o[mt][1] *= al1;
+        acc.o[mt][2] *= al0;
+        acc.o[mt][3] *= al1;
+        const int tok = lr + 8 * (lj >> 1);
+        const int chunk = 2 * (mt & 3) + (lj & 1);
+        const uint32_t addr = sva + (mt >> 2) * Lay::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+        uint32_t x0, x1, x2, x3;
+        ldmatrix_x4_trans(addr, x0, x1, x2, x3);
+        mma_bf16_16816(acc.o[mt], x0, x1, x2, x3, pb0, pb1);
+    }
+}
+
+// Finish a warp's sums and park (o[kGMax][D], m[kGMax], l[kGMax]) at `dst`
+// for the cross-warp merge.  `empty` marks a warp that saw no tile.
+// Layout at dst: o[ng][D], then m[kGMax], then l[kGMax]; heads g >= ng are
+// not stored.
+template <int D>
+__device__ __forceinline__ void park_partial(WarpAcc<D> &acc, bool empty, float *dst, int lane,
+                                             int ng = kGMax) {
+    const int r0 = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {  // column sums over the 16 token rows
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, sh);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, sh);
+    }
+    if (empty) {
+        acc.m0 = acc.m1 = -INFINITY;
+        acc.l0 = acc.l1 = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int d = 16 * mt + r0 + 8 * (j >> 1);
+            const int g = 2 * tq + (j & 1);
+            if (g < ng) dst[g * D + d] = acc.o[mt][j];
+        }
+    }
+    if (r0 == 0) {
+        dst[ng * D + 2 * tq] = acc.m0;
+        dst[ng * D + 2 * tq + 1] = acc.m1;
+        dst[ng * D + kGMax + 2 * tq] = acc.l0;
+        dst[ng * D + kGMax + 2 * tq + 1] = acc.l1;
+    }
+}
+
+// Rows of the tile starting at token t0 that belong to the context (< tok_end)
+// and come from a block id inside the pool.
+template <typename BlockOf>
+__device__ __forceinline__ uint32_t tile_rows_ok(int t0, int tok_end, int B, int boxh, int num_blocks,
+                                                 BlockOf block_of) {
+    uint32_t row_ok = 0;
+    for (int sb = 0; sb < kTile / boxh; ++sb) {
+        const int tok = t0 + sb * boxh;
+        if (tok >= tok_end) break;
+        const int blk = block_of(tok / B);
+        if (blk >= 0 && blk < num_blocks) row_ok |= ((1u << boxh) - 1u) << (sb * boxh);
+    }
+    const int valid = min(kTile, tok_end - t0);
+    return row_ok & ((1u << valid) - 1u);
+}
+
+// Gather the 16-token tile starting at token t0 of (sequence, kv head kvh)
+// into a ring stage with 2-D TMA boxes; one lane calls this.
+template <int D, typename BlockOf>
+__device__ __forceinline__ void issue_tile(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                           unsigned char *stage, uint64_t *bar, int t0, int tok_end,
+                                           int kvh, const DecodeArgs &a, BlockOf block_of) {
+    using Lay = Bf16Layout<D>;
+    const int B = a.block_size;
+    const int boxh = B < kTile ? B : kTile;
+    int ys[kTile / 8];
+    int nsub = 0;
+    for (int sb = 0; sb < kTile / boxh; ++sb) {
+        const int tok = t0 + sb * boxh;
+        if (tok >= tok_end) break;
+        const int lb = tok / B;
+        int blk = block_of(lb);
+        if (blk < 0 || blk >= a.num_blocks) {
+            // never dereferenced out of range: read block 0 instead and mask
+            // these rows out of the softmax (tile_rows_ok)
+            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+            blk = 0;
+        }
+        ys[nsub++] = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
+    }
+    const uint32_t bytes = (uint32_t)(nsub * Lay::kHalves * boxh * 128 * 2);
+    const uint32_t b = smem_u32(bar);
+    mbar_arrive_expect_tx(bar, bytes);
+    const uint32_t dk = smem_u32(stage);
+    const uint32_t dv = dk + Lay::kKVBytes;
+    for (int sb = 0; sb < nsub; ++sb) {
+#pragma unroll
+        for (int h = 0; h < Lay::kHalves; ++h) {
+            const uint32_t off = h * Lay::kHalfBytes + sb * boxh * 128;
+            tma_load_2d(dk + off, tm_k, b, h * 64, ys[sb]);
+            tma_load_2d(dv + off, tm_v, b, h * 64, ys[sb]);
+        }
+    }
+}
+
+// One CTA per (sequence, kv head, partition): the fixed-partition path.
 template <int D, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32)
 decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -265,6 +478,8 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     WorkItem w;
     if (!resolve_item(a, w)) return;
@@ -276,84 +491,39 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned char *ring = smem + warp * NS * Lay::kStageBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * NS * Lay::kStageBytes) + warp * NS;
+    int *bt_s = reinterpret_cast<int *>(smem + NW * NS * Lay::kStageBytes + NW * NS * 8);
     if (lane == 0) {
 #pragma unroll
         for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
     }
-    __syncwarp();
 
-    const int G = a.group;
-    const int Hkv = a.num_kv_heads;
-    const int B = a.block_size;
-    const int r0 = lane >> 2;  // fragment row group
-    const int tq = lane & 3;   // fragment thread-in-group
-
-    // Q^T as the MMA B operand: lane holds query head r0, head_dim pairs.
-    uint32_t qb[D / 16][2];
-    {
-        const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(a.q) +
-                                    ((int64_t)w.seq * a.num_heads + w.kvh * G + r0) * D;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            if (r0 < G) {
-                qb[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * tq);
-                qb[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * tq);
-            } else {
-                qb[ks][0] = qb[ks][1] = 0u;
-            }
-        }
-    }
-
+    // The partition's block ids, read once into shared memory so that no TMA
+    // issue waits on a global load.
     const int32_t *bt = a.block_tables + (int64_t)w.seq * a.max_blocks;
+    const int lb0 = w.tok_begin / a.block_size;
+    const int nblk = (w.tok_end - 1) / a.block_size - lb0 + 1;
+    for (int i = threadIdx.x; i < nblk && i < kBtCache; i += NW * 32) bt_s[i] = bt[lb0 + i];
+    __syncthreads();
+    auto block_of = [&](int lb) { return lb - lb0 < kBtCache ? bt_s[lb - lb0] : bt[lb]; };
+
+    uint32_t qb[D / 16][2];
+    load_q_fragments<D>(a, w.seq, w.kvh, lane, qb);
+
     const int ntiles = (w.tok_end - w.tok_begin + kTile - 1) / kTile;
     const int nmine = ntiles > warp ? (ntiles - warp + NW - 1) / NW : 0;
-    const int boxh = B < kTile ? B : kTile;
-
-    // Lane 0 only: gather tile `tile` of this item into ring slot `buf`.
+    const int boxh = a.block_size < kTile ? a.block_size : kTile;
     auto issue = [&](int tile, int buf) {
-        const int t0 = w.tok_begin + tile * kTile;
-        int ys[kTile / 8];
-        int nsub = 0;
-        for (int sb = 0; sb < kTile / boxh; ++sb) {
-            const int tok = t0 + sb * boxh;
-            if (tok >= w.tok_end) break;
-            const int lb = tok / B;
-            int blk = bt[lb];
-            if (blk < 0 || blk >= a.num_blocks) {
-                // never dereferenced out of range: read block 0 instead and
-                // mask these rows out of the softmax (see row_ok below)
-                flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                blk = 0;
-            }
-            ys[nsub++] = (int)(((int64_t)blk * Hkv + w.kvh) * B + (tok - lb * B));
-        }
-        const uint32_t bytes = (uint32_t)(nsub * Lay::kHalves * boxh * 128 * 2);
-        const uint32_t bar = smem_u32(&bars[buf]);
-        mbar_arrive_expect_tx(&bars[buf], bytes);
-        const uint32_t dk = smem_u32(ring + buf * Lay::kStageBytes);
-        const uint32_t dv = dk + Lay::kKVBytes;
-        for (int sb = 0; sb < nsub; ++sb) {
-#pragma unroll
-            for (int h = 0; h < Lay::kHalves; ++h) {
-                const uint32_t off = h * Lay::kHalfBytes + sb * boxh * 128;
-                tma_load_2d(dk + off, &tm_k, bar, h * 64, ys[sb]);
-                tma_load_2d(dv + off, &tm_v, bar, h * 64, ys[sb]);
-            }
-        }
+        issue_tile<D>(&tm_k, &tm_v, ring + buf * Lay::kStageBytes, &bars[buf],
+                      w.tok_begin + tile * kTile, w.tok_end, w.kvh, a, block_of);
     };
-
     if (lane == 0) {
         for (int i = 0; i < NS && i < nmine; ++i) issue(warp + i * NW, i);
     }
 
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    const float sl2 = a.scale_log2;
+    WarpAcc<D> acc;
+    acc.reset();
     bool dead = false;
-
     for (int i = 0; i < nmine; ++i) {
         const int buf = i % NS;
         if (!mbar_wait_bounded(&bars[buf], (uint32_t)((i / NS) & 1))) {
@@ -361,86 +531,10 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
             dead = true;
             break;
         }
-        const int tile = warp + i * NW;
-        const int t0 = w.tok_begin + tile * kTile;
-        // rows of this tile that hold a token of the context from a valid block
-        uint32_t row_ok = 0;
-        for (int sb = 0; sb < kTile / boxh; ++sb) {
-            const int tok = t0 + sb * boxh;
-            if (tok >= w.tok_end) break;
-            const int blk = bt[tok / B];
-            if (blk >= 0 && blk < a.num_blocks) row_ok |= ((1u << boxh) - 1u) << (sb * boxh);
-        }
-        const int valid = min(kTile, w.tok_end - t0);
-        row_ok &= (1u << valid) - 1u;
+        const int t0 = w.tok_begin + (warp + i * NW) * kTile;
+        const uint32_t row_ok = tile_rows_ok(t0, w.tok_end, a.block_size, boxh, a.num_blocks, block_of);
         unsigned char *sk = ring + buf * Lay::kStageBytes;
-        unsigned char *sv = sk + Lay::kKVBytes;
-        if (row_ok != 0xffffu) {
-            // masked rows hold stale, unwritten or substituted slots: zero their
-            // V so that a zero weight never meets a NaN
-            for (int e = lane; e < Lay::kHalves * kTile * 8; e += 32) {
-                const int h = e / (kTile * 8), rr = (e / 8) % kTile, c = e % 8;
-                if (!((row_ok >> rr) & 1u))
-                    *reinterpret_cast<uint4 *>(sv + h * Lay::kHalfBytes + rr * 128 + c * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
-        }
-        const uint32_t ska = smem_u32(sk), sva = smem_u32(sv);
-        const int lj = lane >> 3, lr = lane & 7;
-
-        // S^T (16 tokens x 8 heads) = K_tile . Q^T
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int tok = lr + 8 * (lj & 1);
-            const int chunk = 2 * (ks & 3) + (lj >> 1);
-            const uint32_t addr = ska + (ks >> 2) * Lay::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-            uint32_t x0, x1, x2, x3;
-            ldmatrix_x4(addr, x0, x1, x2, x3);
-            mma_bf16_16816(sc, x0, x1, x2, x3, qb[ks][0], qb[ks][1]);
-        }
-
-        // online softmax, base 2; rows r0 and r0+8, columns 2tq and 2tq+1
-        const bool ok_lo = (row_ok >> r0) & 1u, ok_hi = (row_ok >> (r0 + 8)) & 1u;
-        const float s0 = ok_lo ? sc[0] * sl2 : -INFINITY;
-        const float s1 = ok_lo ? sc[1] * sl2 : -INFINITY;
-        const float s2 = ok_hi ? sc[2] * sl2 : -INFINITY;
-        const float s3 = ok_hi ? sc[3] * sl2 : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-        for (int sh = 4; sh < 32; sh <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        // reference points stay finite even if nothing valid has been seen yet
-        const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m0 - rf0), al1 = exp2f(m1 - rf1);
-        m0 = mn0;
-        m1 = mn1;
-        const uint32_t p01 = pack_bf16x2(exp2f(s0 - rf0), exp2f(s1 - rf1));
-        const uint32_t p23 = pack_bf16x2(exp2f(s2 - rf0), exp2f(s3 - rf1));
-        // the sum uses the same rounded weights as the numerator
-        l0 = l0 * al0 + (bf16x2_lo(p01) + bf16x2_lo(p23));
-        l1 = l1 * al1 + (bf16x2_hi(p01) + bf16x2_hi(p23));
-        const uint32_t pb0 = movmatrix_trans(p01);
-        const uint32_t pb1 = movmatrix_trans(p23);
-
-        // O^T (head_dim x 8 heads) = O^T * alpha + V_tile^T . P^T
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-            const int tok = lr + 8 * (lj >> 1);
-            const int chunk = 2 * (mt & 3) + (lj & 1);
-            const uint32_t addr = sva + (mt >> 2) * Lay::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-            uint32_t x0, x1, x2, x3;
-            ldmatrix_x4_trans(addr, x0, x1, x2, x3);
-            mma_bf16_16816(o[mt], x0, x1, x2, x3, pb0, pb1);
-        }
+        attend_tile<D>(sk, sk + Lay::kKVBytes, row_ok, qb, a.scale_log2, acc, lane);
         __syncwarp();
         if (lane == 0 && i + NS < nmine) {
             fence_proxy_async();
@@ -448,39 +542,362 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
     }
 
-    // column sums over the 16 token rows held across lanes r0 = 0..7
-#pragma unroll
-    for (int sh = 4; sh < 32; sh <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
-    }
-    if (dead || nmine == 0) {
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
-    }
-
     // Each warp parks its partial in its own (now idle) ring.
-    float *mine = reinterpret_cast<float *>(ring);
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int d = 16 * mt + r0 + 8 * (j >> 1);
-            const int g = 2 * tq + (j & 1);
-            mine[g * D + d] = o[mt][j];
-        }
-    }
-    if (r0 == 0) {
-        mine[kGMax * D + 2 * tq] = m0;
-        mine[kGMax * D + 2 * tq + 1] = m1;
-        mine[kGMax * D + kGMax + 2 * tq] = l0;
-        mine[kGMax * D + kGMax + 2 * tq + 1] = l1;
-    }
+    park_partial<D>(acc, dead || nmine == 0, reinterpret_cast<float *>(ring), lane);
     __syncthreads();
     const float *bufs[NW];
 #pragma unroll
     for (int k = 0; k < NW; ++k) bufs[k] = reinterpret_cast<const float *>(smem + k * NS * Lay::kStageBytes);
     merge_warps_and_store<__nv_bfloat16, D, NW, true>(a, w, bufs);
+}
+
+// ---------------------------------------------------------------------------
+// Balanced (stream-K) bf16 kernel.  All (sequence, kv head) segments are laid
+// end to end as one list of 16-token tiles, and each persistent CTA takes an
+// equal, contiguous share of that list.  Inside a CTA the warps take every
+// NW-th tile and keep their TMA rings running across segment boundaries.
+// Where a segment ends inside the share, the warps merge through shared
+// memory and the CTA stores the result: the final rows if it holds the whole
+// segment, otherwise one partial ("piece") that the piece-merge kernel
+// combines.  Every CTA streams the same number of bytes, so no SM idles in a
+// tail wave and no ring drains between work items.
+// ---------------------------------------------------------------------------
+constexpr int kMinTilesPerCta = 16;  // >= 256 tokens per share: bounds pieces per segment
+
+constexpr int kYCache = 768;  // tiles of a share whose TMA rows are staged in shared memory
+
+// Shared-memory layout of the balanced kernel (host and device agree on it).
+// Offsets are from the 1024-aligned base.
+struct StreamKLayout {
+    int ring, bars, ycache, masks, prefix, total;
+    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs) {
+        ring = NW * NS * 2 * (D / 64) * kTile * 128;
+        bars = ring;
+        ycache = bars + NW * NS * 8;   // int2 per cached tile
+        masks = ycache + kYCache * 8;  // valid-row mask per cached tile
+        prefix = masks + kYCache * 4;
+        total = prefix + (num_seqs + 1) * 4 + 1024;  // + alignment slack
+    }
+};
+
+// Walks the tile list in increasing order: tile t lies in segment
+// (seq, kvh), whose first tile is seg_start and which has n tiles.
+struct SegCursor {
+    int seq, kvh, n;
+    int64_t seg_start;
+    __device__ __forceinline__ void seek(const int *prefix, int num_seqs, int hkv, int64_t t) {
+        int lo = 0, hi = num_seqs;  // largest seq with prefix[seq] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        seq = lo;
+        n = (prefix[seq + 1] - prefix[seq]) / hkv;
+        kvh = (int)((t - prefix[seq]) / n);
+        seg_start = prefix[seq] + (int64_t)kvh * n;
+    }
+    __device__ __forceinline__ void advance_to(const int *prefix, int hkv, int64_t t) {
+        while (t >= seg_start + n) {
+            seg_start += n;
+            if (++kvh == hkv) {
+                kvh = 0;
+                do {
+                    ++seq;
+                    n = (prefix[seq + 1] - prefix[seq]) / hkv;
+                } while (n == 0);
+                seg_start = prefix[seq];
+            }
+        }
+    }
+};
+
+// CTA whose share holds tile t when T tiles are split into `parts` shares
+// [floor(c T / parts), floor((c+1) T / parts)).
+__device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, int64_t parts) {
+    return ((t + 1) * parts + T - 1) / T - 1;
+}
+
+__device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
+
+// TMA rows and valid-row mask of one tile: tile `tile` of segment (seq, kvh)
+// of a context of `len` tokens.  y = -1 for a sub-block past the context.
+struct TileRows {
+    int y0, y1;
+    uint32_t mask;
+};
+
+__device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int kvh, int tile, int len) {
+    const int B = a.block_size;
+    const int boxh = B < kTile ? B : kTile;
+    const int32_t *bt = a.block_tables + (int64_t)seq * a.max_blocks;
+    TileRows r{-1, -1, 0u};
+    for (int sb = 0; sb < kTile / boxh; ++sb) {
+        const int tok = tile * kTile + sb * boxh;
+        if (tok >= len) break;
+        const int lb = tok / B;
+        int blk = bt[lb];
+        if (blk >= 0 && blk < a.num_blocks) {
+            r.mask |= ((1u << boxh) - 1u) << (sb * boxh);
+        } else {
+            // never dereferenced out of range: read block 0, rows masked out
+            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+            blk = 0;
+        }
+        const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
+        if (sb == 0) r.y0 = y; else r.y1 = y;
+    }
+    const int valid = min(kTile, len - tile * kTile);
+    r.mask &= (1u << valid) - 1u;
+    return r;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_rows(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                           unsigned char *stage, uint64_t *bar, int boxh, TileRows r) {
+    using Lay = Bf16Layout<D>;
+    const int nsub = r.y0 < 0 ? 0 : (r.y1 < 0 ? 1 : 2);
+    mbar_arrive_expect_tx(bar, (uint32_t)(nsub * Lay::kHalves * boxh * 128 * 2));
+    const uint32_t b = smem_u32(bar);
+    const uint32_t dk = smem_u32(stage);
+    const uint32_t dv = dk + Lay::kKVBytes;
+    for (int sb = 0; sb < nsub; ++sb) {
+        const int y = sb == 0 ? r.y0 : r.y1;
+#pragma unroll
+        for (int h = 0; h < Lay::kHalves; ++h) {
+            const uint32_t off = h * Lay::kHalfBytes + sb * boxh * 128;
+            tma_load_2d(dk + off, tm_k, b, h * 64, y);
+            tma_load_2d(dv + off, tm_v, b, h * 64, y);
+        }
+    }
+}
+
+// Store a warp's result for the piece [pa, pb) of segment `seg`: the final
+// rows when the piece is the whole segment, otherwise partial slot j.
+template <int D>
+__device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc, bool empty,
+                                            const SegCursor &seg, bool whole, int j, int lane) {
+    const int r0 = lane >> 2, tq = lane & 3, G = a.group;
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {  // column sums over the 16 token rows
+        acc.l0 += __shfl_xor_sync(0xffffffffu, acc.l0, sh);
+        acc.l1 += __shfl_xor_sync(0xffffffffu, acc.l1, sh);
+    }
+    if (empty) {
+        acc.m0 = acc.m1 = -INFINITY;
+        acc.l0 = acc.l1 = 0.f;
+    }
+    const int64_t row0 = (int64_t)seg.seq * a.num_heads + seg.kvh * G;
+    const float inv0 = acc.l0 > 0.f ? 1.f / acc.l0 : 0.f, inv1 = acc.l1 > 0.f ? 1.f / acc.l1 : 0.f;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int d = 16 * mt + r0 + 8 * (jj >> 1);
+            const int g = 2 * tq + (jj & 1);
+            if (g >= G) continue;
+            const int64_t row = row0 + g;
+            if (whole) {
+                store_out(static_cast<__nv_bfloat16 *>(a.out) + row * D + d,
+                          acc.o[mt][jj] * ((jj & 1) ? inv1 : inv0));
+            } else {
+                a.part_o[(row * a.max_parts + j) * D + d] = acc.o[mt][jj];
+            }
+        }
+    }
+    if (!whole && r0 == 0) {
+        if (2 * tq < G) {
+            a.part_m[(row0 + 2 * tq) * a.max_parts + j] = acc.m0;
+            a.part_l[(row0 + 2 * tq) * a.max_parts + j] = acc.l0;
+        }
+        if (2 * tq + 1 < G) {
+            a.part_m[(row0 + 2 * tq + 1) * a.max_parts + j] = acc.m1;
+            a.part_l[(row0 + 2 * tq + 1) * a.max_parts + j] = acc.l1;
+        }
+    }
+}
+
+// Balanced kernel: every warp of the grid takes an equal contiguous share of
+// the tile list (at least kMinTilesPerCta tiles) and streams it through its own
+// TMA ring.  Warps never wait for one another: where a segment (sequence, kv
+// head) ends inside a share, the warp stores its result for that piece -- the
+// final rows if the share holds the whole segment, otherwise a partial that
+// the merge kernel combines -- and carries on with the next segment.
+template <int D, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32)
+decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+    using Lay = Bf16Layout<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const StreamKLayout L(D, NW, NS, a.num_seqs);
+    uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + L.bars);
+    int2 *ycache = reinterpret_cast<int2 *>(smem + L.ycache);
+    uint32_t *mcache = reinterpret_cast<uint32_t *>(smem + L.masks);
+    int *prefix = reinterpret_cast<int *>(smem + L.prefix);
+    __shared__ int warp_sums[NW];
+    __shared__ int carry;
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int S = a.num_seqs, Hkv = a.num_kv_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cap = min(a.max_seq_len, a.max_blocks * a.block_size);
+
+    // prefix[s] = tiles of all segments of the sequences before s
+    if (threadIdx.x == 0) {
+        prefix[0] = 0;
+        carry = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < S; base += NW * 32) {
+        const int sq = base + threadIdx.x;
+        int v = 0;
+        if (sq < S) {
+            const int raw = a.seq_lens[sq];
+            if ((raw < 0 || raw > cap) && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+            v = Hkv * ((clamp_len(raw, cap) + kTile - 1) / kTile);
+        }
+        int x = v;  // inclusive warp scan
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, sh);
+            if (lane >= sh) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        int before = carry;
+        for (int k = 0; k < warp; ++k) before += warp_sums[k];
+        if (sq < S) prefix[sq + 1] = before + x;
+        __syncthreads();
+        if (threadIdx.x == NW * 32 - 1) carry = before + x;
+        __syncthreads();
+    }
+    const int64_t T = prefix[S];
+    int64_t parts = T / kMinTilesPerCta;  // warps that get a share
+    if (parts < 1) parts = 1;
+    if (parts > (int64_t)gridDim.x * NW) parts = (int64_t)gridDim.x * NW;
+    const int64_t gw0 = (int64_t)blockIdx.x * NW;
+    if (T == 0 || gw0 >= parts) return;
+    const int64_t cta_lo = gw0 * T / parts;
+    const int64_t cta_hi = (gw0 + NW < parts ? gw0 + NW : parts) * T / parts;
+
+    // Stage the TMA rows and valid-row masks of the CTA's first tiles, so that
+    // neither issuing nor attending a tile waits on a global load.  Each thread
+    // handles up to kPer tiles; all their loads are in flight together.
+    const int ncache = (int)(cta_hi - cta_lo < kYCache ? cta_hi - cta_lo : kYCache);
+    {
+        constexpr int kPer = (kYCache + NW * 32 - 1) / (NW * 32);
+        int sq[kPer], kv[kPer], tl[kPer], ln[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = threadIdx.x + u * NW * 32;
+            sq[u] = -1;
+            if (i < ncache) {
+                SegCursor c;
+                c.seek(prefix, S, Hkv, cta_lo + i);
+                sq[u] = c.seq;
+                kv[u] = c.kvh;
+                tl[u] = (int)(cta_lo + i - c.seg_start);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) ln[u] = sq[u] >= 0 ? clamp_len(a.seq_lens[sq[u]], cap) : 0;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            if (sq[u] < 0) continue;
+            const TileRows r = tile_rows(a, sq[u], kv[u], tl[u], ln[u]);
+            const int i = threadIdx.x + u * NW * 32;
+            ycache[i] = make_int2(r.y0, r.y1);
+            mcache[i] = r.mask;
+        }
+    }
+    unsigned char *ring = smem + warp * NS * Lay::kStageBytes;
+    uint64_t *bars = bars_all + warp * NS;
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < NS; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int64_t gw = gw0 + warp;
+    if (gw >= parts) return;  // no CTA-wide barrier follows
+    const int64_t lo = gw * T / parts, hi = (gw + 1) * T / parts;
+    const int ntiles = (int)(hi - lo);
+    const int boxh = a.block_size < kTile ? a.block_size : kTile;
+
+    // rows/mask of tile t (staged, or computed for tiles past the cache)
+    auto rows_of = [&](int64_t t, const SegCursor &c) -> TileRows {
+        const int64_t i = t - cta_lo;
+        if (i < ncache) {
+            const int2 y = ycache[i];
+            return TileRows{y.x, y.y, mcache[i]};
+        }
+        return tile_rows(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap));
+    };
+
+    SegCursor prod;  // lane 0: segment of the tile being issued (needed past the cache)
+    if (lane == 0) prod.seek(prefix, S, Hkv, lo);
+    auto issue = [&](int k, int buf) {
+        const int64_t t = lo + k;
+        if (t - cta_lo >= ncache) prod.advance_to(prefix, Hkv, t);
+        issue_rows<D>(&tm_k, &tm_v, ring + buf * Lay::kStageBytes, &bars[buf], boxh, rows_of(t, prod));
+    };
+    if (lane == 0) {
+        for (int i = 0; i < NS && i < ntiles; ++i) issue(i, i);
+    }
+
+    SegCursor seg;  // the segment being attended
+    seg.seek(prefix, S, Hkv, lo);
+    uint32_t qb[D / 16][2], qn[D / 16][2];
+    load_q_fragments<D>(a, seg.seq, seg.kvh, lane, qb);
+    int k = 0;
+    bool dead = false;
+    WarpAcc<D> acc;
+    for (;;) {
+        const int64_t pa = lo + k;  // this piece: tiles [pa, pb)
+        const int64_t seg_end = seg.seg_start + seg.n;
+        const int64_t pb = hi < seg_end ? hi : seg_end;
+        SegCursor nxt = seg;
+        if (pb < hi) {  // fetch the next piece's queries while this one runs
+            nxt.advance_to(prefix, Hkv, pb);
+            load_q_fragments<D>(a, nxt.seq, nxt.kvh, lane, qn);
+        }
+        acc.reset();
+        for (; lo + k < pb; ++k) {
+            const int buf = k % NS;
+            if (!dead && !mbar_wait_bounded(&bars[buf], (uint32_t)((k / NS) & 1))) {
+                if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                dead = true;
+            }
+            if (dead) continue;
+            const TileRows r = rows_of(lo + k, seg);
+            unsigned char *sk = ring + buf * Lay::kStageBytes;
+            attend_tile<D>(sk, sk + Lay::kKVBytes, r.mask, qb, a.scale_log2, acc, lane);
+            __syncwarp();
+            if (lane == 0 && k + NS < ntiles) {
+                fence_proxy_async();
+                issue(k + NS, buf);
+            }
+        }
+        const bool whole = pa == seg.seg_start && pb == seg_end;
+        const int64_t w0 = share_owner(seg.seg_start, T, parts);
+        store_piece<D>(a, acc, dead, seg, whole, (int)(gw - w0), lane);
+        if (lane == 0 && pa == seg.seg_start) {
+            // the warp holding a segment's first tile records its number of pieces
+            const int64_t w1 = share_owner(seg_end - 1, T, parts);
+            a.pieces[(int64_t)seg.seq * a.num_kv_heads + seg.kvh] = (int)(w1 - w0 + 1);
+        }
+        if (pb >= hi) break;
+        seg = nxt;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            qb[ks][0] = qn[ks][0];
+            qb[ks][1] = qn[ks][1];
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -490,6 +907,8 @@ template <typename T, int D, int NW>
 __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const DecodeArgs a) {
     constexpr int E = D / 32;  // head_dim elements per lane: d = lane + 32 j
     __shared__ float merge_buf[NW][kGMax * D + 2 * kGMax];
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     WorkItem w;
     if (!resolve_item(a, w)) return;
@@ -568,52 +987,84 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const DecodeArgs a
 
 // ---------------------------------------------------------------------------
 // Partition merge: out = sum_j e^{m_j - M} o_j / sum_j e^{m_j - M} l_j
+// PIECES = false: partials of fixed partitions, ceil(len / P) of them.
+// PIECES = true: partials of the balanced split, counted in a.pieces; this
+// kernel also writes the zero rows of empty contexts on that path.
 // ---------------------------------------------------------------------------
-template <typename T, int D, bool LOG2>
+template <typename T, int D, bool LOG2, bool PIECES>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) {
     constexpr int E = D / 32;  // consecutive head_dim elements per lane
+    constexpr int U = 8;       // partials whose rows are loaded together
+    grid_dependency_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // (sequence, query head)
     if (row >= (int64_t)a.num_seqs * a.num_heads) return;
     const int seq = (int)(row / a.num_heads);
     const int cap = min(a.max_seq_len, a.max_blocks * a.block_size);
-    int len = a.seq_lens[seq];
-    len = len < 0 ? 0 : (len > cap ? cap : len);
-    const int nparts = (len + a.partition_size - 1) / a.partition_size;
-    if (nparts <= 1) return;
-
     const float *pm = a.part_m + row * a.max_parts;
     const float *pl = a.part_l + row * a.max_parts;
-    const float *po = a.part_o + row * a.max_parts * D;
-    float M = -INFINITY;
-    for (int j = lane; j < nparts; j += 32) M = fmaxf(M, pm[j]);
+    const float *po = a.part_o + row * a.max_parts * D + lane * E;
+    // issue the length, the piece count and the first 32 (max, sum) pairs at
+    // once; pairs past the piece count are masked below
+    const int raw_len = a.seq_lens[seq];
+    int nparts = 0;
+    if (PIECES) {
+        const int h = (int)(row - (int64_t)seq * a.num_heads);
+        nparts = a.pieces[(int64_t)seq * a.num_kv_heads + h / a.group];
+    }
+    float mj = -INFINITY, lj = 0.f;
+    if (lane < a.max_parts) {
+        mj = pm[lane];
+        lj = pl[lane];
+    }
+    const int len = raw_len < 0 ? 0 : (raw_len > cap ? cap : raw_len);
+    T *dst = static_cast<T *>(a.out) + row * D + lane * E;
+    if (PIECES) {
+        if (len == 0) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) store_out(dst + e, 0.f);
+            return;
+        }
+    } else {
+        nparts = (len + a.partition_size - 1) / a.partition_size;
+    }
+    if (nparts <= 1) return;
+    if (lane >= nparts) {
+        mj = -INFINITY;
+        lj = 0.f;
+    }
+    float M = mj;
+    for (int j = lane + 32; j < nparts; j += 32) M = fmaxf(M, pm[j]);
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
     if (M == -INFINITY) M = 0.f;  // only if every block was invalid (flagged)
-    float lsum = 0.f;
-    for (int j = lane; j < nparts; j += 32) lsum += (LOG2 ? exp2f(pm[j] - M) : expf(pm[j] - M)) * pl[j];
+    auto ex = [&](float x) { return x == -INFINITY ? 0.f : (LOG2 ? exp2f(x - M) : expf(x - M)); };
+    const float wl = ex(mj);  // weight of partial `lane`
+    float lsum = wl * lj;
+    for (int j = lane + 32; j < nparts; j += 32) lsum += ex(pm[j]) * pl[j];
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, sh);
 
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int j = 0; j < nparts; ++j) {
-        const float c = LOG2 ? exp2f(pm[j] - M) : expf(pm[j] - M);
-        const float *src = po + (int64_t)j * D + lane * E;
-        if constexpr (E == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src);
-            acc[0] += c * v.x;
-            acc[1] += c * v.y;
-            acc[2] += c * v.z;
-            acc[3] += c * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(src);
-            acc[0] += c * v.x;
-            acc[1] += c * v.y;
+    for (int j0 = 0; j0 < nparts; j0 += U) {
+        float v[U][E];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {  // U independent row loads in flight
+            const int j = j0 + u < nparts ? j0 + u : nparts - 1;
+#pragma unroll
+            for (int e = 0; e < E; ++e) v[u][e] = po[(int64_t)j * D + e];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u;
+            const float wsh = __shfl_sync(0xffffffffu, wl, j & 31);
+            const float w = j >= nparts ? 0.f : (j < 32 ? wsh : ex(pm[j]));
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] += w * v[u][e];
         }
     }
-    T *dst = static_cast<T *>(a.out) + row * D + lane * E;
 #pragma unroll
     for (int e = 0; e < E; ++e) store_out(dst + e, lsum > 0.f ? acc[e] / lsum : 0.f);
 }
@@ -621,25 +1072,33 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-static int auto_partition_size(int num_seqs, int max_seq_len) {
-    (void)num_seqs;
-    (void)max_seq_len;
-    return 512;
-}
+// Fixed partitions used when the caller passes partition_size = 0 but the
+// balanced path does not apply (fp32, or more sequences than it scans).
+constexpr int kDefaultPartition = 512;
+constexpr int kMaxBalancedSeqs = 8192;
 
 static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WorkspaceLayout {
-    size_t o_off, m_off, l_off, total;
+    size_t o_off, m_off, l_off, pieces_off, total;
 };
 
-static WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t D, int64_t parts) {
+// parts = partial slots per (sequence, query head); `pieces` adds the
+// per-segment piece counts of the balanced path.
+static WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t D, int64_t parts, bool pieces) {
     WorkspaceLayout w;
     w.o_off = 0;
     w.m_off = round256((size_t)(S * Hq * parts * D * 4));
     w.l_off = w.m_off + round256((size_t)(S * Hq * parts * 4));
-    w.total = w.l_off + round256((size_t)(S * Hq * parts * 4));
+    w.pieces_off = w.l_off + round256((size_t)(S * Hq * parts * 4));
+    w.total = w.pieces_off + (pieces ? round256((size_t)(S * Hq * 4)) : 0);
     return w;
+}
+
+// Balanced path: a segment of L tokens spans at most ceil(L / 256) + 1 shares
+// because every share holds at least kMinTilesPerCta tiles (256 tokens).
+static int64_t balanced_slots(int max_seq_len) {
+    return ((int64_t)max_seq_len + kMinTilesPerCta * kTile - 1) / (kMinTilesPerCta * kTile) + 1;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -670,7 +1129,13 @@ static bool make_cache_map(CUtensorMap *map, const void *base, int64_t rows, int
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Opt a kernel in to the dynamic shared memory it needs (once per device).
+static bool make_cache_maps(const DecodeArgs &a, int D, CUtensorMap *mk, CUtensorMap *mv) {
+    const int boxh = a.block_size < kTile ? a.block_size : kTile;
+    const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
+    return make_cache_map(mk, a.k_cache, rows, D, boxh) && make_cache_map(mv, a.v_cache, rows, D, boxh);
+}
+
+// Opt a kernel in to the dynamic shared memory it may need (once per device).
 template <typename K>
 static bool ensure_smem(K kernel, int bytes, bool (&done)[128]) {
     int dev = 0;
@@ -683,15 +1148,43 @@ static bool ensure_smem(K kernel, int bytes, bool (&done)[128]) {
     return true;
 }
 
-// Launch shapes of the bf16 kernel: warps per CTA x ring stages per warp.
-// PKV_DECODE_VARIANT selects one for tuning sweeps; the default is the one
-// measured fastest on GB300.
-static int decode_variant() {
-    static int v = [] {
-        const char *s = std::getenv("PKV_DECODE_VARIANT");
-        return s ? std::atoi(s) : 0;
-    }();
-    return v;
+static int sm_count() {
+    static int counts[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream drains; it waits (griddepcontrol.wait)
+// before touching memory, so stream order is preserved.
+template <typename... KArgs, typename... Args>
+static pkv_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? launch_status() : PKV_ERR_CUDA;
+}
+
+// Launch shapes (warps per CTA x ring stages per warp).  The environment
+// variables PKV_DECODE_VARIANT / PKV_BALANCED_VARIANT select another shape
+// for tuning sweeps; the defaults are the shapes measured fastest on GB300.
+static int env_variant(const char *name) {
+    const char *s = std::getenv(name);
+    return s ? std::atoi(s) : 0;
 }
 
 template <int D, int NW, int NS>
@@ -700,37 +1193,61 @@ static pkv_status launch_bf16(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
     constexpr int smem = bf16_smem_bytes<D, NW, NS>();
     auto kern = decode_bf16_mma_kernel<D, NW, NS>;
     if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
-    const int boxh = a.block_size < kTile ? a.block_size : kTile;
-    const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, a.k_cache, rows, D, boxh) || !make_cache_map(&mv, a.v_cache, rows, D, boxh))
-        return PKV_ERR_CUDA;
-    kern<<<grid, NW * 32, smem, st>>>(mk, mv, a);
-    return launch_status();
+    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
+    return launch_pdl(kern, grid, dim3(NW * 32), smem, st, mk, mv, a);
 }
 
 template <int D>
 static pkv_status dispatch_bf16(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
-    switch (decode_variant()) {
-        case 1: return launch_bf16<D, 4, 2>(a, grid, st);
-        case 2: return launch_bf16<D, 4, 4>(a, grid, st);
+    static const int v = env_variant("PKV_DECODE_VARIANT");
+    switch (v) {
+        case 1: return launch_bf16<D, 4, 3>(a, grid, st);
+        case 2: return launch_bf16<D, 4, 1>(a, grid, st);
         case 3: return launch_bf16<D, 8, 2>(a, grid, st);
-        default: return launch_bf16<D, 4, 3>(a, grid, st);
+        default: return launch_bf16<D, 4, 2>(a, grid, st);
+    }
+}
+
+template <int D, int NW, int NS>
+static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
+    static bool done[128] = {};
+    auto kern = decode_bf16_streamk_kernel<D, NW, NS>;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs).total;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
+        per_sm < 1)
+        return PKV_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms < 1) return PKV_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
+    return launch_pdl(kern, dim3((unsigned)(sms * per_sm)), dim3(NW * 32), smem, st, mk, mv, a);
+}
+
+template <int D>
+static pkv_status dispatch_balanced(const DecodeArgs &a, cudaStream_t st) {
+    static const int v = env_variant("PKV_BALANCED_VARIANT");
+    switch (v) {
+        case 1: return launch_balanced<D, 4, 3>(a, st);
+        case 2: return launch_balanced<D, 8, 2>(a, st);
+        case 3: return launch_balanced<D, 4, 4>(a, st);
+        case 4: return launch_balanced<D, 8, 3>(a, st);
+        default: return launch_balanced<D, 4, 2>(a, st);
     }
 }
 
 template <typename T, int D>
 static pkv_status dispatch_simt(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
-    decode_simt_kernel<T, D, 4><<<grid, 128, 0, st>>>(a);
-    return launch_status();
+    return launch_pdl(decode_simt_kernel<T, D, 4>, grid, dim3(128), 0, st, a);
 }
 
-template <typename T, int D, bool LOG2>
+template <typename T, int D, bool LOG2, bool PIECES>
 static pkv_status launch_reduce(const DecodeArgs &a, cudaStream_t st) {
     const int64_t rows = (int64_t)a.num_seqs * a.num_heads;
     const unsigned blocks = (unsigned)((rows + 3) / 4);
-    decode_reduce_kernel<T, D, LOG2><<<blocks, 128, 0, st>>>(a);
-    return launch_status();
+    return launch_pdl(decode_reduce_kernel<T, D, LOG2, PIECES>, dim3(blocks), dim3(128), 0, st, a);
 }
 
 }  // namespace pkv
@@ -740,11 +1257,14 @@ using namespace pkv;
 PKV_API size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
                                               int max_seq_len, int partition_size) {
     if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
-    const int P = partition_size > 0 ? partition_size : auto_partition_size(num_seqs, max_seq_len);
-    if (P <= 0 || P % kTile != 0) return 0;
-    const int64_t parts = ((int64_t)max_seq_len + P - 1) / P;
+    if (partition_size < 0 || partition_size % kTile != 0) return 0;
+    if (partition_size == 0) {
+        // large enough for the balanced path and for its fixed-partition fallback
+        return workspace_layout(num_seqs, num_heads, head_dim, balanced_slots(max_seq_len), true).total;
+    }
+    const int64_t parts = ((int64_t)max_seq_len + partition_size - 1) / partition_size;
     if (parts <= 1) return 0;
-    return workspace_layout(num_seqs, num_heads, head_dim, parts).total;
+    return workspace_layout(num_seqs, num_heads, head_dim, parts, false).total;
 }
 
 PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
@@ -767,13 +1287,17 @@ PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *
     if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PKV_ERR_INVALID;
-    // TMA row coordinates are 32-bit: every (block, kv head, row) must be addressable,
-    // plus one out-of-range block used to neutralise bad block ids.
+    // TMA row coordinates are 32-bit: every (block, kv head, row) must be addressable.
     const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
     if (rows > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
+    // the balanced path counts tiles of all segments in 32-bit integers
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
+        return PKV_ERR_UNSUPPORTED;
 
-    const int P = partition_size > 0 ? partition_size : auto_partition_size(num_seqs, max_seq_len);
+    const bool balanced = partition_size == 0 && dtype == PKV_BF16 && max_seq_len > 0 &&
+                          num_seqs <= kMaxBalancedSeqs;
+    const int P = partition_size > 0 ? partition_size : kDefaultPartition;
     const int64_t parts64 = max_seq_len > P ? ((int64_t)max_seq_len + P - 1) / P : 1;
     if (parts64 > 65535) return PKV_ERR_INVALID;
     const int parts = (int)parts64;
@@ -799,29 +1323,40 @@ PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.err = device_error_word();
 
-    if (parts > 1) {
-        const WorkspaceLayout lay = workspace_layout(num_seqs, num_heads, head_dim, parts);
+    const bool split = balanced || parts > 1;
+    if (split) {
+        // partition_size == 0 sizes the workspace for the balanced layout (which
+        // also holds the fixed-partition fallback); otherwise fixed partitions
+        const int64_t slots = partition_size == 0 ? balanced_slots(max_seq_len) : parts;
+        const WorkspaceLayout lay = workspace_layout(num_seqs, num_heads, head_dim, slots, partition_size == 0);
         if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
             return PKV_ERR_INVALID;
         unsigned char *ws = static_cast<unsigned char *>(workspace);
         a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
         a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
         a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
+        a.pieces = partition_size == 0 ? reinterpret_cast<int *>(ws + lay.pieces_off) : nullptr;
+        a.max_parts = (int)slots;  // stride of the partial slots
     }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid((unsigned)num_seqs, (unsigned)num_kv_heads, (unsigned)parts);
     pkv_status rc;
-    if (dtype == PKV_BF16) {
+    if (balanced) {
+        rc = head_dim == 128 ? dispatch_balanced<128>(a, st) : dispatch_balanced<64>(a, st);
+        if (rc == PKV_OK)
+            rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, true>(a, st)
+                                 : launch_reduce<__nv_bfloat16, 64, true, true>(a, st);
+    } else if (dtype == PKV_BF16) {
         rc = head_dim == 128 ? dispatch_bf16<128>(a, grid, st) : dispatch_bf16<64>(a, grid, st);
         if (rc == PKV_OK && parts > 1)
-            rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true>(a, st)
-                                 : launch_reduce<__nv_bfloat16, 64, true>(a, st);
+            rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, false>(a, st)
+                                 : launch_reduce<__nv_bfloat16, 64, true, false>(a, st);
     } else {
         rc = head_dim == 128 ? dispatch_simt<float, 128>(a, grid, st) : dispatch_simt<float, 64>(a, grid, st);
         if (rc == PKV_OK && parts > 1)
-            rc = head_dim == 128 ? launch_reduce<float, 128, false>(a, st)
-                                 : launch_reduce<float, 64, false>(a, st);
+            rc = head_dim == 128 ? launch_reduce<float, 128, false, false>(a, st)
+                                 : launch_reduce<float, 64, false, false>(a, st);
     }
     return rc;
 }

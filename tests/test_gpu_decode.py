@@ -66,6 +66,9 @@ def test_tiny_fp32_workload_with_cache_write():
     (32, 4, 128, 32, [1, 31, 32, 33, 700], 64),
     (24, 4, 64, 32, [2, 2000], 512),
     (8, 1, 128, 16, [4096], 0),            # one KV head, 8 partitions
+    (32, 4, 128, 8, [1, 8, 9, 95, 600], 0),    # balanced split, block 8
+    (32, 4, 128, 32, [1, 31, 32, 33, 700], 0),  # balanced split, block 32
+    (32, 8, 64, 16, [9, 160, 999], 0),
 ])
 def test_bf16_decode_matches_oracle(Hq, Hkv, D, B, lens, P):
     shape = shape_of(Hq, Hkv, D, B)
@@ -171,3 +174,43 @@ def test_workspace_too_small_is_rejected():
                                    torch.tensor([1000], dtype=torch.int32, device="cuda"),
                                    shape.scale, 1000, partition_size=64, workspace=ws)
     assert e.value.status == pkv.PKV_ERR_INVALID
+
+
+@pytest.mark.parametrize("S,maxlen,Hq,Hkv", [(300, 3000, 32, 8), (8, 16000, 32, 8), (77, 700, 64, 8)])
+def test_balanced_split_many_sequences(S, maxlen, Hq, Hkv):
+    """partition_size 0: all (sequence, kv head) contexts cut into equal shares,
+    with empty contexts, contexts inside one share and contexts cut into many
+    pieces in the same call."""
+    shape = shape_of(Hq, Hkv, 128, 16)
+    rng = np.random.default_rng(S + maxlen)
+    lens = rng.integers(0, maxlen, size=S, endpoint=True)
+    lens[:3] = [0, 1, maxlen]
+    case = make_decode_case(shape, lens.tolist(), seed=S)
+    out = run_decode(case, shape, partition_size=0, max_seq_len=maxlen)
+    pick = sorted(set([0, 1, 2] + rng.choice(S, size=min(S, 12), replace=False).tolist()))
+    ref = oracle_out(case, shape, seqs=pick)
+    assert_bf16_close(out[pick], ref, f"balanced S={S}")
+    assert torch.all(out[0].float() == 0)
+    assert pkv.read_device_errors() == 0
+
+
+def test_balanced_workspace_reused_across_calls():
+    """One workspace, never cleared, serves many balanced calls in a row
+    (different lengths, different splits): nothing left over from an earlier
+    call may leak into a later one."""
+    shape = shape_of(32, 8, 128, 16)
+    need = pkv.paged_attention_workspace_size(40, 32, 128, 3000, 0)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN-like garbage
+    rng = np.random.default_rng(99)
+    for call in range(4):
+        lens = rng.integers(0, 3000, size=40, endpoint=True).tolist()
+        case = make_decode_case(shape, lens, seed=100 + call)
+        q = case["q"].cuda()
+        out = torch.full_like(q, float("nan"))
+        pkv.paged_attention_decode(out, q, case["kc"].cuda(), case["vc"].cuda(),
+                                   torch.from_numpy(case["tables"]).cuda(),
+                                   torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                   shape.scale, 3000, partition_size=0, workspace=ws)
+        torch.cuda.synchronize()
+        assert_bf16_close(out, oracle_out(case, shape), f"call {call}")
+    assert pkv.read_device_errors() == 0
