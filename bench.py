@@ -251,42 +251,48 @@ class Batch:
                                         self.max_seq_len, self.partition_size, self.workspace)
 
     def step(self):
-        self.write()
-        self.decode()
+        """Store every sequence's new token and attend: one library call."""
+        self.pkv.paged_attention_decode_append(self.out, self.q, self.k_new, self.v_new, self.k_cache,
+                                               self.v_cache, self.block_tables, self.seq_lens,
+                                               self.shape.scale, self.max_seq_len, self.partition_size,
+                                               self.workspace)
 
     def launches_per_step(self) -> int:
+        """Kernels one step launches: the attention kernel, the merge of split
+        contexts, and a separate store kernel on the paths that do not fuse it."""
         S = len(self.lens)
         ws = self.pkv.paged_attention_workspace_size(S, self.shape.num_heads, self.shape.head_dim,
                                                      self.max_seq_len, self.partition_size)
-        return 2 + (1 if ws > 0 else 0)
+        fused = self.partition_size == 0 and self.shape.dtype == torch.bfloat16
+        return 1 + (1 if ws > 0 else 0) + (0 if fused else 1)
 
 
-def capture(fn, stream):
+def capture(fns, stream):
+    """One CUDA graph that runs the callables in order (one per step)."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        fn()  # warm caches (tensor maps, smem opt-in, symbol addresses) outside capture
+        for fn in fns[:4]:
+            fn()  # warm caches (tensor maps, smem opt-in, symbol addresses) outside capture
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-            fn()
+            for fn in fns:
+                fn()
     torch.cuda.synchronize()
     return g
 
 
-def time_graphs(graphs, steps, warmup, stream):
-    """Replay graphs[i % n] `steps` times after `warmup` untimed replays;
-    returns per-replay device milliseconds (CUDA events on the stream)."""
-    n = len(graphs)
+def time_graph(graph, stream, repeats=1):
+    """Device milliseconds of `repeats` back-to-back replays of `graph`
+    (CUDA events on the launch stream, synchronised on both sides)."""
     with torch.cuda.stream(stream):
-        for i in range(warmup):
-            graphs[i % n].replay()
         torch.cuda.synchronize()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-        ev[0].record(stream)
-        for i in range(steps):
-            graphs[i % n].replay()
-            ev[i + 1].record(stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(repeats):
+            graph.replay()
+        e1.record(stream)
         torch.cuda.synchronize()
-    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return e0.elapsed_time(e1)
 
 
 # ---------------------------------------------------------------------------
@@ -382,21 +388,26 @@ def run_ours(args):
         batches.append(Batch(pkv, shape, lens, seed + r, device, args.partition_size))
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device)
-    step_graphs = [capture(b.step, stream) for b in batches]
-    decode_graphs = [capture(b.decode, stream) for b in batches]
+    steps, warmup = args.steps, max(3, args.warmup)
+    # exactly `steps` steps (and `steps` decode calls) in one graph each; the
+    # batches rotate so that no step re-reads the previous step's pool
+    warm_graph = capture([batches[i % nrot].step for i in range(warmup)], stream)
+    step_graph = capture([batches[i % nrot].step for i in range(steps)], stream)
+    decode_graph = capture([batches[i % nrot].decode for i in range(steps)], stream)
     assert pkv.read_device_errors() == 0
 
-    steps, warmup = args.steps, max(3, args.warmup)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        step_ms = time_graphs(step_graphs, steps, warmup, stream)
-        decode_ms = time_graphs(decode_graphs, steps, warmup, stream)
+        time_graph(warm_graph, stream)      # W untimed warm-up steps
+        step_total_ms = time_graph(step_graph, stream)
+        time_graph(warm_graph, stream)
+        decode_total_ms = time_graph(decode_graph, stream)
     torch.cuda.synchronize()
     barrier(world)
     bytes_per = [kv_bytes(b.lens, shape) for b in batches]
     step_bytes = sum(bytes_per[i % nrot] for i in range(steps))
-    local_s = sum(step_ms) / 1e3
+    local_s = step_total_ms / 1e3
     total_s = max_over_ranks(local_s, world, device)
     total_bytes = sum_over_ranks(step_bytes, world, device)
     value = total_bytes / total_s / 1e9
@@ -408,7 +419,7 @@ def run_ours(args):
     # roofline of the dominant kernel (the decode call), timed live above
     alg = [algorithmic_decode_bytes(b.lens, shape) for b in batches]
     dec_alg_bytes = sum(alg[i % nrot] for i in range(steps)) / steps
-    dec_ms = sum(decode_ms) / steps
+    dec_ms = decode_total_ms / steps
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -419,7 +430,7 @@ def run_ours(args):
     achieved = dec_alg_bytes / (dec_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": "paged_attention_decode (partition kernel + merge kernel)",
+                "kernel": "paged_attention_decode (attention kernel + merge kernel)",
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
                 "decode_us": round(dec_ms * 1e3, 2)}
 
@@ -458,7 +469,6 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     b = Batch(pkv, shape, lens, seed + 77, device, args.partition_size)
     S = len(lens)
     steps = args.steps
-    extra_blocks = b.num_blocks  # capacity check for the appended tokens
     h_q = b.q.cpu().pin_memory()
     h_k = b.k_new.cpu().pin_memory()
     h_v = b.v_new.cpu().pin_memory()
@@ -466,18 +476,15 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     cap = b.max_blocks + (steps + args.warmup) // shape.block_size + 2
     h_tab = torch.empty((S, cap), dtype=torch.int32).pin_memory()
     h_len = torch.empty(S, dtype=torch.int32).pin_memory()
-    h_slot = torch.empty(S, dtype=torch.int64).pin_memory()
     d_tab = torch.empty((S, cap), dtype=torch.int32, device=device)
     d_len = torch.empty(S, dtype=torch.int32, device=device)
-    d_slot = torch.empty(S, dtype=torch.int64, device=device)
     d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
     max_seq_len = cap * shape.block_size
     ws = torch.zeros(max(256, pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim,
                                                                  max_seq_len, args.partition_size)),
                      dtype=torch.uint8, device=device)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len, h_slot))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len))
     d2h = h_out.numel() * h_out.element_size()
-    del extra_blocks
     ms, byts = [], []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + steps):
@@ -487,15 +494,12 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             if st != 0 or len(pairs):
                 raise RuntimeError("allocator could not serve the step")
             tab, ln = b.alloc.block_tables(b.seq_ids, cap)
-            h_slot.numpy()[:] = slots
             h_tab.numpy()[:] = tab
             h_len.numpy()[:] = ln
-            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len),
-                         (d_slot, h_slot)):
+            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len)):
                 d.copy_(h, non_blocking=True)
-            pkv.kv_cache_write(d_k, d_v, b.k_cache, b.v_cache, d_slot)
-            pkv.paged_attention_decode(b.out, d_q, b.k_cache, b.v_cache, d_tab, d_len, shape.scale,
-                                       max_seq_len, args.partition_size, ws)
+            pkv.paged_attention_decode_append(b.out, d_q, d_k, d_v, b.k_cache, b.v_cache, d_tab, d_len,
+                                              shape.scale, max_seq_len, args.partition_size, ws)
             h_out.copy_(b.out, non_blocking=True)
             ev1.record(stream)
             ev1.synchronize()  # the host reads the step's result

@@ -189,6 +189,34 @@ PKV_EXPORT pkv_status block_copy(void *const *k_caches, void *const *v_caches, i
                       size_t block_bytes, void *stream);
 
 /*
+ * paged_attention_decode_append -- one decode step in one call: store each
+ * sequence's new token, then attend.
+ *
+ * Source: the same passages as kv_cache_write and paged_attention_decode; the
+ * new token is produced, stored in its block (troisinh page, "Co che Block
+ * Table") and attended together with the cached ones (aiwiki.vn page,
+ * second and third paragraphs).
+ *
+ * Equivalent to kv_cache_write of k_new[s] / v_new[s] at position
+ * seq_lens[s] - 1 of sequence s (the slot its block table gives for that
+ * position; sequences with seq_lens[s] == 0 store nothing) followed by
+ * paged_attention_decode with the same arguments.
+ *   k_new, v_new   device [num_seqs][num_kv_heads][head_dim], dtype, 16-byte aligned
+ *   k_cache, v_cache  written (the new token) and read
+ * With partition_size == 0 and bf16 the store happens inside the attention
+ * kernel, by the warp that attends the tile holding that position, just
+ * before it loads the tile; otherwise a store kernel runs first.  The result
+ * is the same either way.
+ */
+PKV_EXPORT pkv_status paged_attention_decode_append(void *out, const void *q, const void *k_new,
+                                  const void *v_new, void *k_cache, void *v_cache,
+                                  const int32_t *block_tables, const int32_t *seq_lens,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_blocks_per_seq, int num_blocks,
+                                  int max_seq_len, float scale, int partition_size,
+                                  void *workspace, size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that
  * cannot allocate device memory.  No passage of the pages has a counterpart:
  * this entry point exists for the caller, not for the method.

@@ -29,7 +29,8 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT =
 
 __all__ = [
     "PkvError", "kv_cache_write", "paged_attention_decode", "paged_attention_workspace_size",
-    "block_copy", "read_device_errors", "BlockAllocator", "library_path",
+    "paged_attention_decode_append", "block_copy", "read_device_errors", "BlockAllocator",
+    "library_path",
 ]
 
 
@@ -131,6 +132,39 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, sca
         S, Hq, Hkv, D, B, block_tables.shape[1], NB, int(max_seq_len), float(scale),
         int(partition_size), ws_ptr, ws_bytes, dt, _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                  scale: float, max_seq_len: int, partition_size: int = 0,
+                                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step: store k_new[s] / v_new[s] ([S, Hkv, D]) at position
+    seq_lens[s] - 1 of each sequence, then attend as paged_attention_decode."""
+    lib = _lib.load()
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if Dk != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if tuple(k_new.shape) != (S, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [S, Hkv, D]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables must be [S, maxB] and seq_lens [S]")
+    dt = _dtype_code(q)
+    for t, n in ((out, "out"), (k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{n} dtype differs from q")
+    need = paged_attention_workspace_size(S, Hq, D, max_seq_len, partition_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.paged_attention_decode_append(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
+        S, Hq, Hkv, D, B, block_tables.shape[1], NB, int(max_seq_len), float(scale),
+        int(partition_size), ws_ptr, ws_bytes, dt, _stream(stream))
+    _check(st, "paged_attention_decode_append")
     return out
 
 

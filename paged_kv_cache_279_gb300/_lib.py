@@ -25,6 +25,10 @@ SIGNATURES = {
     "paged_attention_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                        c_float, c_int, c_void_p, c_size_t, c_int, c_void_p]),
+    "paged_attention_decode_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                              c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                              c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                              c_void_p, c_size_t, c_int, c_void_p]),
     "paged_attention_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                                                c_int, c_int, c_float, c_int, c_int, c_void_p]),

@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdlib>
@@ -66,6 +67,12 @@ struct DecodeArgs {
     float scale;       // multiplies q.k
     float scale_log2;  // scale * log2(e), for the exp2 form of the softmax
     unsigned int *err;
+    // fused append: each sequence's new token [S][Hkv][D] goes to position
+    // seq_lens[s] - 1 before it is attended (nullptr: no append)
+    const void *k_new;
+    const void *v_new;
+    void *k_cache_w;
+    void *v_cache_w;
 };
 
 // ---------------------------------------------------------------------------
@@ -783,13 +790,26 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int64_t cta_lo = gw0 * T / parts;
     const int64_t cta_hi = (gw0 + NW < parts ? gw0 + NW : parts) * T / parts;
 
+    // The first piece's queries: fetched now, used after the staging below.
+    const int64_t gw = gw0 + warp;
+    const int64_t lo = gw * T / parts, hi = (gw + 1) * T / parts;
+    SegCursor seg;  // the segment being attended
+    uint32_t qb[D / 16][2], qn[D / 16][2];
+    if (gw < parts) {
+        seg.seek(prefix, S, Hkv, lo);
+        load_q_fragments<D>(a, seg.seq, seg.kvh, lane, qb);
+    }
+
     // Stage the TMA rows and valid-row masks of the CTA's first tiles, so that
     // neither issuing nor attending a tile waits on a global load.  Each thread
-    // handles up to kPer tiles; all their loads are in flight together.
+    // handles up to kPer tiles and issues all their loads (lengths and block
+    // ids, read speculatively and masked afterwards) before using any.
     const int ncache = (int)(cta_hi - cta_lo < kYCache ? cta_hi - cta_lo : kYCache);
     {
         constexpr int kPer = (kYCache + NW * 32 - 1) / (NW * 32);
-        int sq[kPer], kv[kPer], tl[kPer], ln[kPer];
+        const int B = a.block_size;
+        const int boxh = B < kTile ? B : kTile;
+        int sq[kPer], kv[kPer], tl[kPer], ln[kPer], b0[kPer], b1[kPer];
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int i = threadIdx.x + u * NW * 32;
@@ -803,14 +823,40 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
         }
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) ln[u] = sq[u] >= 0 ? clamp_len(a.seq_lens[sq[u]], cap) : 0;
+        for (int u = 0; u < kPer; ++u) {
+            if (sq[u] < 0) continue;
+            const int32_t *bt = a.block_tables + (int64_t)sq[u] * a.max_blocks;
+            // the tile's tokens lie inside the clamped length, hence inside the table
+            const int lb0 = min(tl[u] * kTile / B, a.max_blocks - 1);
+            const int lb1 = min((tl[u] * kTile + boxh) / B, a.max_blocks - 1);
+            ln[u] = a.seq_lens[sq[u]];
+            b0[u] = bt[lb0];
+            b1[u] = bt[lb1];
+        }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             if (sq[u] < 0) continue;
-            const TileRows r = tile_rows(a, sq[u], kv[u], tl[u], ln[u]);
+            const int len = clamp_len(ln[u], cap);
+            TileRows r{-1, -1, 0u};
+            for (int sb = 0; sb < kTile / boxh; ++sb) {
+                const int tok = tl[u] * kTile + sb * boxh;
+                if (tok >= len) break;
+                const int lb = tok / B;
+                int blk = sb == 0 ? b0[u] : b1[u];
+                if (blk >= 0 && blk < a.num_blocks) {
+                    r.mask |= ((1u << boxh) - 1u) << (sb * boxh);
+                } else {
+                    flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                    blk = 0;
+                }
+                const int y = (int)(((int64_t)blk * Hkv + kv[u]) * B + (tok - lb * B));
+                if (sb == 0) r.y0 = y; else r.y1 = y;
+            }
+            const int valid = min(kTile, len - tl[u] * kTile);
+            r.mask &= (1u << valid) - 1u;
             const int i = threadIdx.x + u * NW * 32;
             ycache[i] = make_int2(r.y0, r.y1);
-            mcache[i] = r.mask;
+            mcache[i] = r.mask | ((uint32_t)valid << 16);  // valid rows in bits 16..20
         }
     }
     unsigned char *ring = smem + warp * NS * Lay::kStageBytes;
@@ -822,18 +868,72 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     __syncthreads();
 
-    const int64_t gw = gw0 + warp;
     if (gw >= parts) return;  // no CTA-wide barrier follows
-    const int64_t lo = gw * T / parts, hi = (gw + 1) * T / parts;
     const int ntiles = (int)(hi - lo);
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
+
+    if (a.k_new) {
+        // Fused append: the warp whose share holds a segment's last tile stores
+        // that segment's new token (position len - 1) before any TMA reads it.
+        // Only this warp ever reads that tile, so no other ordering is needed.
+        // Targets come from the staged rows; all copies of up to kBatch
+        // segments are loaded before any is stored.
+        constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of one K (or V) row
+        constexpr int kBatch = 4;
+        const int part = lane / kChunks, ch = lane % kChunks;  // lanes past 2*kChunks idle
+        SegCursor c = seg;
+        bool more = true;
+        while (more) {
+            int64_t src_row[kBatch], dst_row[kBatch];
+            int n = 0;
+            while (more && n < kBatch) {
+                const int64_t last = c.seg_start + c.n - 1;
+                if (last >= lo && last < hi) {
+                    int64_t dst = -1;
+                    const int64_t i = last - cta_lo;
+                    if (i < ncache) {
+                        const uint32_t m = mcache[i];
+                        const int r = (int)(m >> 16) - 1;  // row of position len - 1 in its tile
+                        if ((m >> r) & 1u) {
+                            const int2 y = ycache[i];
+                            dst = r < boxh ? (int64_t)y.x + r : (int64_t)y.y + (r - boxh);
+                        }
+                    } else {
+                        const int len = clamp_len(a.seq_lens[c.seq], cap);
+                        const int pos = len - 1, lb = pos / a.block_size;
+                        const int blk = a.block_tables[(int64_t)c.seq * a.max_blocks + lb];
+                        if (blk >= 0 && blk < a.num_blocks)
+                            dst = ((int64_t)blk * Hkv + c.kvh) * a.block_size + (pos - lb * a.block_size);
+                    }
+                    src_row[n] = (int64_t)c.seq * Hkv + c.kvh;
+                    dst_row[n] = dst;
+                    ++n;
+                }
+                if (c.seg_start + c.n >= hi) more = false;
+                else c.advance_to(prefix, Hkv, c.seg_start + c.n);
+            }
+            uint4 v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (j < n && lane < 2 * kChunks && dst_row[j] >= 0)
+                    v[j] = static_cast<const uint4 *>(part ? a.v_new : a.k_new)[src_row[j] * kChunks + ch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (j < n && lane < 2 * kChunks && dst_row[j] >= 0)
+                    static_cast<uint4 *>(part ? a.v_cache_w : a.k_cache_w)[dst_row[j] * kChunks + ch] = v[j];
+        }
+        // generic-proxy stores, then the TMA (async proxy) of this warp reads them
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
 
     // rows/mask of tile t (staged, or computed for tiles past the cache)
     auto rows_of = [&](int64_t t, const SegCursor &c) -> TileRows {
         const int64_t i = t - cta_lo;
         if (i < ncache) {
             const int2 y = ycache[i];
-            return TileRows{y.x, y.y, mcache[i]};
+            return TileRows{y.x, y.y, mcache[i] & 0xffffu};
         }
         return tile_rows(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap));
     };
@@ -849,10 +949,6 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int i = 0; i < NS && i < ntiles; ++i) issue(i, i);
     }
 
-    SegCursor seg;  // the segment being attended
-    seg.seek(prefix, S, Hkv, lo);
-    uint32_t qb[D / 16][2], qn[D / 16][2];
-    load_q_fragments<D>(a, seg.seq, seg.kvh, lane, qb);
     int k = 0;
     bool dead = false;
     WarpAcc<D> acc;
@@ -897,6 +993,36 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             qb[ks][0] = qn[ks][0];
             qb[ks][1] = qn[ks][1];
         }
+    }
+}
+
+// Store each sequence's new token at position seq_lens[s] - 1 (looked up in
+// its block table): the write half of paged_attention_decode_append on the
+// paths that do not fuse it.  One thread per 16-byte chunk of K and of V.
+__global__ void __launch_bounds__(256)
+append_tokens_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, uint4 *k_cache,
+                     uint4 *v_cache, const int32_t *__restrict__ block_tables,
+                     const int32_t *__restrict__ seq_lens, int num_seqs, int num_kv_heads, int chunks,
+                     int block_size, int max_blocks, int num_blocks, int cap, unsigned int *err) {
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t total = (int64_t)num_seqs * num_kv_heads * chunks;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t sh = i / chunks;
+        const int c = (int)(i - sh * chunks);
+        const int s = (int)(sh / num_kv_heads), h = (int)(sh - (int64_t)s * num_kv_heads);
+        const int len = clamp_len(seq_lens[s], cap);
+        if (len == 0) continue;
+        const int pos = len - 1, lb = pos / block_size;
+        const int blk = block_tables[(int64_t)s * max_blocks + lb];
+        if (blk < 0 || blk >= num_blocks) {
+            if (c == 0) flag_error(err, PKV_DEVERR_BLOCK_ID);
+            continue;
+        }
+        const int64_t row = ((int64_t)blk * num_kv_heads + h) * block_size + (pos - lb * block_size);
+        k_cache[row * chunks + c] = k_new[i];
+        v_cache[row * chunks + c] = v_new[i];
     }
 }
 
@@ -1267,13 +1393,31 @@ PKV_API size_t paged_attention_workspace_size(int num_seqs, int num_heads, int h
     return workspace_layout(num_seqs, num_heads, head_dim, parts, false).total;
 }
 
-PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
-                                          const void *v_cache, const int32_t *block_tables,
-                                          const int32_t *seq_lens, int num_seqs, int num_heads,
-                                          int num_kv_heads, int head_dim, int block_size,
-                                          int max_blocks_per_seq, int num_blocks, int max_seq_len,
-                                          float scale, int partition_size, void *workspace,
-                                          size_t workspace_bytes, int dtype, void *stream) {
+static pkv_status append_tokens(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                                int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                                int num_blocks, int max_seq_len, int dtype, cudaStream_t st) {
+    if (num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 || max_seq_len < 0)
+        return PKV_ERR_INVALID;
+    if (!k_cache || !v_cache || !block_tables || !seq_lens || !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_INVALID;
+    const int elt = dtype == PKV_F32 ? 4 : 2;
+    const int chunks = head_dim * elt / 16;
+    const int64_t total = (int64_t)num_seqs * num_kv_heads * chunks;
+    const int64_t blocks = (total + 255) / 256;
+    const int cap = (int)std::min<int64_t>(max_seq_len, (int64_t)max_blocks_per_seq * block_size);
+    return launch_pdl(append_tokens_kernel, dim3((unsigned)(blocks < 65536 ? blocks : 65536)), dim3(256), 0, st,
+                      (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_cache, (uint4 *)v_cache,
+                      block_tables, seq_lens, num_seqs, num_kv_heads, chunks, block_size, max_blocks_per_seq,
+                      num_blocks, cap, device_error_word());
+}
+
+static pkv_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+                              int partition_size, void *workspace, size_t workspace_bytes, int dtype,
+                              void *stream, const void *k_new, const void *v_new) {
     if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||
         num_blocks < 1 || max_seq_len < 0 || partition_size < 0 || !std::isfinite(scale))
         return PKV_ERR_INVALID;
@@ -1322,6 +1466,10 @@ PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *
     a.scale = scale;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.err = device_error_word();
+    a.k_new = balanced ? k_new : nullptr;
+    a.v_new = balanced ? v_new : nullptr;
+    a.k_cache_w = const_cast<void *>(k_cache);
+    a.v_cache_w = const_cast<void *>(v_cache);
 
     const bool split = balanced || parts > 1;
     if (split) {
@@ -1359,6 +1507,48 @@ PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *
                                  : launch_reduce<float, 64, false, false>(a, st);
     }
     return rc;
+}
+
+PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *seq_lens, int num_seqs, int num_heads,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                          float scale, int partition_size, void *workspace,
+                                          size_t workspace_bytes, int dtype, void *stream) {
+    return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_seq_len,
+                       scale, partition_size, workspace, workspace_bytes, dtype, stream, nullptr, nullptr);
+}
+
+PKV_API pkv_status paged_attention_decode_append(
+    void *out, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+    const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads, int num_kv_heads,
+    int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+    int partition_size, void *workspace, size_t workspace_bytes, int dtype, void *stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    const bool fused = partition_size == 0 && dtype == PKV_BF16 && num_seqs > 0 &&
+                       num_seqs <= kMaxBalancedSeqs && max_seq_len > 0;
+    if (!fused) {
+        // other paths: the plain write (slot of position seq_lens[s] - 1 is
+        // looked up on the device) followed by the decode
+        if (num_seqs == 0) return PKV_OK;
+        if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+        if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+        if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+        const pkv_status rc = append_tokens(k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                            num_seqs, num_kv_heads, head_dim, block_size,
+                                            max_blocks_per_seq, num_blocks, max_seq_len, dtype,
+                                            static_cast<cudaStream_t>(stream));
+        if (rc != PKV_OK) return rc;
+        return paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                      num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                      num_blocks, max_seq_len, scale, partition_size, workspace,
+                                      workspace_bytes, dtype, stream);
+    }
+    return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_seq_len,
+                       scale, partition_size, workspace, workspace_bytes, dtype, stream, k_new, v_new);
 }
 
 // ---------------------------------------------------------------------------

@@ -214,3 +214,41 @@ def test_balanced_workspace_reused_across_calls():
         torch.cuda.synchronize()
         assert_bf16_close(out, oracle_out(case, shape), f"call {call}")
     assert pkv.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("P,dtype,B", [(0, torch.bfloat16, 16), (0, torch.bfloat16, 8), (0, torch.bfloat16, 32),
+                                       (64, torch.bfloat16, 16), (0, torch.float32, 16)])
+def test_decode_append_equals_write_then_decode(P, dtype, B):
+    """paged_attention_decode_append = store the newest token of every
+    sequence at position len - 1, then attend (fused into the balanced bf16
+    kernel, a separate store kernel on the other paths)."""
+    shape = shape_of(32, 8, 128, B, dtype)
+    lens = [1, 16, 17, 300, 0, 1500, 33]
+    case = make_decode_case(shape, lens, seed=31 + B + P)
+    kc, vc = case["kc"].clone(), case["vc"].clone()
+    k_new = torch.zeros((len(lens), 8, 128), dtype=dtype)
+    v_new = torch.zeros_like(k_new)
+    for s, L in enumerate(lens):
+        if L == 0:
+            continue
+        slot = int(case["tables"][s][(L - 1) // B]) * B + (L - 1) % B
+        kc[slot // B, :, slot % B] = float("nan")   # the newest token is not in the pool yet
+        vc[slot // B, :, slot % B] = float("nan")
+        k_new[s] = case["ks"][s][L - 1]
+        v_new[s] = case["vs"][s][L - 1]
+    dkc, dvc = kc.cuda(), vc.cuda()
+    q = case["q"].cuda()
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attention_decode_append(out, q, k_new.cuda(), v_new.cuda(), dkc, dvc,
+                                      torch.from_numpy(case["tables"]).cuda(),
+                                      torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                                      shape.scale, max(lens), partition_size=P)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(dkc.cpu()), bits(case["kc"])) and torch.equal(bits(dvc.cpu()), bits(case["vc"]))
+    ref = oracle_out(case, shape)
+    if dtype == torch.bfloat16:
+        assert_bf16_close(out, ref, f"append P={P} B={B}")
+    else:
+        assert_f32_close(out, ref, "append fp32")
+    assert torch.all(out[4].float() == 0)
+    assert pkv.read_device_errors() == 0
