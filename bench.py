@@ -45,8 +45,11 @@ WORKLOADS = {
     "tiny": wl.TINY_FP32,
     "long": wl.LONG_BF16,
     "mixed": wl.MIXED_BF16,
+    "beam": wl.BEAM_BF16,
+    "beam1032": wl.BEAM_BF16,
 }
-ROTATE = {"gqa": 4, "tiny": 1, "long": 1, "mixed": 4}  # batches rotated to defeat L2 reuse
+# batches rotated so that no step re-reads the previous step's pool from L2
+ROTATE = {"gqa": 4, "tiny": 1, "long": 1, "mixed": 4, "beam": 4, "beam1032": 4}
 
 
 def parse_args(argv=None):
@@ -222,10 +225,20 @@ class Batch:
                 k = torch.randn((L - 1, Hkv, D), generator=g, device=device).to(shape.dtype)
                 v = torch.randn((L - 1, Hkv, D), generator=g, device=device).to(shape.dtype)
                 pkv.kv_cache_write(k, v, self.k_cache, self.v_cache, slots)
-        # this step's new token for every sequence
-        self.seq_ids = np.arange(S, dtype=np.int64)
+        self._finish(pkv, g, np.arange(S, dtype=np.int64), partition_size)
+        self.unique_bytes = kv_bytes(self.lens, shape)
+        self.alg_bytes = algorithmic_decode_bytes(self.lens, shape)
+
+    def _finish(self, pkv, g, seq_ids, partition_size):
+        """This step's new token for every sequence: slots from the allocator
+        (copy-on-write pairs executed at once), tables, queries, workspace."""
+        shape, device, B = self.shape, self.device, self.shape.block_size
+        Hkv, D, S = shape.num_kv_heads, shape.head_dim, len(seq_ids)
+        self.seq_ids = seq_ids
         st, slots, pairs = self.alloc.append_slots(self.seq_ids)
-        assert st == 0 and len(pairs) == 0
+        assert st == 0
+        if len(pairs):
+            pkv.block_copy([self.k_cache], [self.v_cache], torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
         self.max_blocks = max(-(-L // B) for L in self.lens) + 4
         tables, seq_lens = self.alloc.block_tables(self.seq_ids, self.max_blocks)
         self.max_seq_len = self.max_blocks * B
@@ -241,6 +254,57 @@ class Batch:
                                                 partition_size)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         self.pkv = pkv
+
+    @classmethod
+    def beam(cls, pkv, shape, seed, device, partition_size, shared):
+        """Beam search: prompts of `shared` tokens, each forked into a beam
+        group that shares the prompt's blocks; every beam then produced its own
+        0-256 tokens (copy-on-write where a shared block was partially filled),
+        and this step adds one more token per beam."""
+        self = cls.__new__(cls)
+        B, Hkv, D = shape.block_size, shape.num_kv_heads, shape.head_dim
+        P_, W = wl.BEAM_PROMPTS, wl.BEAM_WIDTH
+        div = wl.draw_divergent_lengths(P_ * W, seed)
+        self.shape, self.device = shape, device
+        self.lens = [shared + int(d) + 1 for d in div]  # after this step's token
+        # room for the appended tokens of the e2e loop too (8 blocks per beam)
+        self.num_blocks = P_ * (-(-shared // B) + 1) + sum(-(-int(d) // B) + 10 for d in div) + 64
+        self.alloc = pkv.BlockAllocator(self.num_blocks, B)
+        order = wl.draw_block_ids(self.num_blocks, seed)
+        for i in range(self.num_blocks):
+            assert self.alloc.add_seq(-1 - i, B) == 0
+        for b in order[::-1]:
+            assert self.alloc.free_seq(-1 - int(b)) == 0
+        g = torch.Generator(device=device)
+        g.manual_seed(int(wl.sub_seed(seed, 9)))
+        self.k_cache = torch.zeros((self.num_blocks, Hkv, B, D), dtype=shape.dtype, device=device)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        for p in range(P_):
+            assert self.alloc.add_seq(p * W, shared) == 0
+            slots = torch.from_numpy(self.alloc.slots(p * W, 0, shared)).to(device)
+            k = torch.randn((shared, Hkv, D), generator=g, device=device).to(shape.dtype)
+            pkv.kv_cache_write(k, torch.randn_like(k), self.k_cache, self.v_cache, slots)
+            for c in range(1, W):
+                assert self.alloc.fork(p * W, p * W + c) == 0
+        for t in range(int(div.max())):
+            beams = [b for b in range(P_ * W) if div[b] > t]
+            st, slots, pairs = self.alloc.append_slots(beams)
+            assert st == 0
+            if len(pairs):
+                pkv.block_copy([self.k_cache], [self.v_cache],
+                               torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
+            k = torch.randn((len(beams), Hkv, D), generator=g, device=device).to(shape.dtype)
+            pkv.kv_cache_write(k, torch.randn_like(k), self.k_cache, self.v_cache,
+                               torch.from_numpy(slots).to(device))
+        self._finish(pkv, g, np.arange(P_ * W, dtype=np.int64), partition_size)
+        # bytes a step must read: each prompt once, each beam's own tokens once
+        elt = torch.tensor([], dtype=shape.dtype).element_size()
+        own = sum(int(d) + 1 for d in div)
+        self.unique_bytes = (P_ * shared + own) * Hkv * D * 2 * elt
+        blocks = P_ * -(-shared // B) + sum(-(-(int(d) + 1 + shared % B) // B) for d in div)
+        self.alg_bytes = (self.unique_bytes + 2 * len(self.lens) * shape.num_heads * D * elt
+                          + 4 * blocks + 4 * len(self.lens))
+        return self
 
     def write(self):
         self.pkv.kv_cache_write(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slot_mapping)
@@ -298,14 +362,14 @@ def time_graph(graph, stream, repeats=1):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_sample(shape, seed, budget_s):
+def oracle_sample(shape, seed, budget_s, lens):
     """Time the fp64 oracle, as it stands, on one freshly drawn batch of the
-    same workload, repeating the call until about `budget_s` seconds of work.
-    Returns (GB/s, cores, description, seconds, calls)."""
+    same workload (context lengths `lens`), repeating the call until about
+    `budget_s` seconds of work.  Returns (GB/s, cores, description, seconds,
+    calls)."""
     import oracle
-    lens = wl.draw_lengths(shape, seed + 1).tolist()
     cores = oracle.max_threads()
-    q = wl.draw_query(shape, seed + 1).float().numpy()
+    q = wl.draw_query(shape, seed + 1, num_seqs=len(lens)).float().numpy()
     ks, vs = [], []
     for i, L in enumerate(lens):
         k, v = wl.draw_seq_kv(shape, seed + 1, i, L)
@@ -329,12 +393,12 @@ def run_reference(args):
     if rank != 0:
         return 0
     shape = shape_for(args)
-    lens = wl.draw_lengths(shape, args.seed + 1).tolist()
+    lens = context_lengths(args, shape, args.seed + 1)
     per_step = max(1, len(lens) // 4)  # a bounded sample per step
     import oracle
     cores = oracle.max_threads()
     times, bytes_ = [], []
-    q = wl.draw_query(shape, args.seed + 1).float().numpy()
+    q = wl.draw_query(shape, args.seed + 1, num_seqs=len(lens)).float().numpy()
     kv = [tuple(t.float().numpy() for t in wl.draw_seq_kv(shape, args.seed + 1, s, L))
           for s, L in enumerate(lens)]
     for i in range(args.warmup + args.steps):
@@ -384,8 +448,7 @@ def run_ours(args):
     seed = args.seed + 1000 * rank
     batches = []
     for r in range(nrot):
-        lens = wl.draw_lengths(shape, seed + r).tolist()
-        batches.append(Batch(pkv, shape, lens, seed + r, device, args.partition_size))
+        batches.append(make_batch(pkv, shape, args, seed + r, device))
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device)
     steps, warmup = args.steps, max(3, args.warmup)
@@ -405,7 +468,8 @@ def run_ours(args):
         decode_total_ms = time_graph(decode_graph, stream)
     torch.cuda.synchronize()
     barrier(world)
-    bytes_per = [kv_bytes(b.lens, shape) for b in batches]
+    bytes_per = [b.unique_bytes for b in batches]
+    logical_per = [kv_bytes(b.lens, shape) for b in batches]
     step_bytes = sum(bytes_per[i % nrot] for i in range(steps))
     local_s = step_total_ms / 1e3
     total_s = max_over_ranks(local_s, world, device)
@@ -417,7 +481,7 @@ def run_ours(args):
     tokens_per_s = world * seqs_per_step / (layers * ms_per_step / 1e3)
 
     # roofline of the dominant kernel (the decode call), timed live above
-    alg = [algorithmic_decode_bytes(b.lens, shape) for b in batches]
+    alg = [b.alg_bytes for b in batches]
     dec_alg_bytes = sum(alg[i % nrot] for i in range(steps)) / steps
     dec_ms = decode_total_ms / steps
     peaks = {}
@@ -439,7 +503,8 @@ def run_ours(args):
         e2e = run_e2e(pkv, shape, args, device, stream, seed, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, cores, desc, secs, _ = oracle_sample(shape, seed, args.cpu_budget)
+        gbs, cores, desc, secs, _ = oracle_sample(shape, seed, args.cpu_budget,
+                                                  context_lengths(args, shape, seed + 1))
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": desc}
     if rank == 0:
@@ -450,6 +515,7 @@ def run_ours(args):
             "dtype": "bf16" if shape.dtype == torch.bfloat16 else "f32", "data": "synthetic",
             "config": config_of(shape, args, len(batches[0].lens)),
             "decode_tokens_per_s": round(tokens_per_s, 1),
+            "logical_kv_gbs": round(sum(logical_per[i % nrot] for i in range(steps)) / total_s / 1e9 * world, 2),
             "pct_of_hbm_peak": round(100 * value / peak, 2),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": batches[0].launches_per_step() * steps,
@@ -461,13 +527,28 @@ def run_ours(args):
     return 0
 
 
+def make_batch(pkv, shape, args, seed, device):
+    if args.workload.startswith("beam"):
+        shared = wl.BEAM_SHARED_PARTIAL if args.workload == "beam1032" else wl.BEAM_SHARED
+        return Batch.beam(pkv, shape, seed, device, args.partition_size, shared)
+    return Batch(pkv, shape, wl.draw_lengths(shape, seed).tolist(), seed, device, args.partition_size)
+
+
+def context_lengths(args, shape, seed):
+    """Context lengths of one batch of the workload (for the CPU oracle)."""
+    if args.workload.startswith("beam"):
+        shared = wl.BEAM_SHARED_PARTIAL if args.workload == "beam1032" else wl.BEAM_SHARED
+        div = wl.draw_divergent_lengths(wl.BEAM_PROMPTS * wl.BEAM_WIDTH, seed)
+        return [shared + int(d) + 1 for d in div]
+    return wl.draw_lengths(shape, seed).tolist()
+
+
 def run_e2e(pkv, shape, args, device, stream, seed, world):
     """The step through the public API with host buffers: the allocator appends
     a token for every sequence on the host, the step's inputs go H2D from
     pinned memory, the kernels run, the output comes back D2H."""
-    lens = wl.draw_lengths(shape, seed + 77).tolist()
-    b = Batch(pkv, shape, lens, seed + 77, device, args.partition_size)
-    S = len(lens)
+    b = make_batch(pkv, shape, args, seed + 77, device)
+    S = len(b.lens)
     steps = args.steps
     h_q = b.q.cpu().pin_memory()
     h_k = b.k_new.cpu().pin_memory()
@@ -505,7 +586,8 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             ev1.synchronize()  # the host reads the step's result
             if i >= args.warmup:
                 ms.append(ev0.elapsed_time(ev1))
-                byts.append(kv_bytes(ln.tolist(), shape))
+                # unique bytes: what the batch started with plus the tokens added since
+                byts.append(b.unique_bytes + kv_bytes(ln.tolist(), shape) - kv_bytes(b.lens, shape))
     local_s = sum(ms) / 1e3
     total_s = max_over_ranks(local_s, world, device)
     total_b = sum_over_ranks(sum(byts), world, device)
