@@ -297,6 +297,12 @@ class Batch:
             pkv.kv_cache_write(k, torch.randn_like(k), self.k_cache, self.v_cache,
                                torch.from_numpy(slots).to(device))
         self._finish(pkv, g, np.arange(P_ * W, dtype=np.int64), partition_size)
+        # beams of a prompt share its blocks: one group per prompt
+        offs, pre = self.alloc.prefix_groups(self.seq_ids)
+        self.group_offsets = torch.from_numpy(offs).to(device)
+        self.prefix_lens = torch.from_numpy(pre).to(device)
+        ws = pkv.paged_attention_grouped_workspace_size(len(self.lens), shape.num_heads, D, self.max_seq_len)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
         # bytes a step must read: each prompt once, each beam's own tokens once
         elt = torch.tensor([], dtype=shape.dtype).element_size()
         own = sum(int(d) + 1 for d in div)
@@ -306,16 +312,32 @@ class Batch:
                           + 4 * blocks + 4 * len(self.lens))
         return self
 
+    group_offsets = None
+
     def write(self):
         self.pkv.kv_cache_write(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slot_mapping)
 
     def decode(self):
+        if self.group_offsets is not None:
+            self.pkv.paged_attention_decode_grouped(self.out, self.q, self.k_cache, self.v_cache,
+                                                    self.block_tables, self.seq_lens, self.group_offsets,
+                                                    self.prefix_lens, self.shape.scale, self.max_seq_len,
+                                                    workspace=self.workspace)
+            return
         self.pkv.paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache,
                                         self.block_tables, self.seq_lens, self.shape.scale,
                                         self.max_seq_len, self.partition_size, self.workspace)
 
     def step(self):
-        """Store every sequence's new token and attend: one library call."""
+        """Store every sequence's new token and attend: one library call
+        (grouped by shared prefix for beam search)."""
+        if self.group_offsets is not None:
+            self.pkv.paged_attention_decode_grouped(self.out, self.q, self.k_cache, self.v_cache,
+                                                    self.block_tables, self.seq_lens, self.group_offsets,
+                                                    self.prefix_lens, self.shape.scale, self.max_seq_len,
+                                                    k_new=self.k_new, v_new=self.v_new,
+                                                    workspace=self.workspace)
+            return
         self.pkv.paged_attention_decode_append(self.out, self.q, self.k_new, self.v_new, self.k_cache,
                                                self.v_cache, self.block_tables, self.seq_lens,
                                                self.shape.scale, self.max_seq_len, self.partition_size,
@@ -327,6 +349,8 @@ class Batch:
         S = len(self.lens)
         ws = self.pkv.paged_attention_workspace_size(S, self.shape.num_heads, self.shape.head_dim,
                                                      self.max_seq_len, self.partition_size)
+        if self.group_offsets is not None:
+            return 3  # prefix kernel, attention kernel, merge
         fused = self.partition_size == 0 and self.shape.dtype == torch.bfloat16
         return 1 + (1 if ws > 0 else 0) + (0 if fused else 1)
 
@@ -561,9 +585,11 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     d_len = torch.empty(S, dtype=torch.int32, device=device)
     d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
     max_seq_len = cap * shape.block_size
-    ws = torch.zeros(max(256, pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim,
-                                                                 max_seq_len, args.partition_size)),
-                     dtype=torch.uint8, device=device)
+    ws_bytes = (pkv.paged_attention_grouped_workspace_size(S, shape.num_heads, shape.head_dim, max_seq_len)
+                if b.group_offsets is not None else
+                pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim, max_seq_len,
+                                                   args.partition_size))
+    ws = torch.zeros(max(256, ws_bytes), dtype=torch.uint8, device=device)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len))
     d2h = h_out.numel() * h_out.element_size()
     ms, byts = [], []
@@ -579,8 +605,16 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             h_len.numpy()[:] = ln
             for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len)):
                 d.copy_(h, non_blocking=True)
-            pkv.paged_attention_decode_append(b.out, d_q, d_k, d_v, b.k_cache, b.v_cache, d_tab, d_len,
-                                              shape.scale, max_seq_len, args.partition_size, ws)
+            if b.group_offsets is not None:
+                offs, pre = b.alloc.prefix_groups(b.seq_ids)  # beams sharing a prompt
+                d_offs = torch.from_numpy(offs).pin_memory().to(device, non_blocking=True)
+                d_pre = torch.from_numpy(pre).pin_memory().to(device, non_blocking=True)
+                pkv.paged_attention_decode_grouped(b.out, d_q, b.k_cache, b.v_cache, d_tab, d_len, d_offs,
+                                                   d_pre, shape.scale, max_seq_len, k_new=d_k, v_new=d_v,
+                                                   workspace=ws)
+            else:
+                pkv.paged_attention_decode_append(b.out, d_q, d_k, d_v, b.k_cache, b.v_cache, d_tab, d_len,
+                                                  shape.scale, max_seq_len, args.partition_size, ws)
             h_out.copy_(b.out, non_blocking=True)
             ev1.record(stream)
             ev1.synchronize()  # the host reads the step's result

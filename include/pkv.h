@@ -74,6 +74,8 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_SLOT 4u      /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEVERR_COPY_PAIR 8u /* block_copy pair outside [0, num_blocks) or src == dst */
 #define PKV_DEVERR_TIMEOUT 16u  /* a bounded wait inside a kernel ran out */
+#define PKV_DEVERR_PREFIX 32u   /* grouped decode: bad group offsets or prefix length, or a
+                                   member whose blocks differ from the leader's in the prefix */
 
 /* Human-readable name of a status code; never NULL. */
 PKV_EXPORT const char *pkv_status_string(int status);
@@ -217,6 +219,46 @@ PKV_EXPORT pkv_status paged_attention_decode_append(void *out, const void *q, co
                                   void *workspace, size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * paged_attention_decode_grouped -- decode for batches whose sequences share
+ * prefix blocks (beam search, parallel sampling), each shared block read once.
+ *
+ * Source: troisinh page, section "Copy-on-Write cho Beam Search" (branches
+ * of beam search / parallel sampling share the physical blocks of their common
+ * prefix) and aiwiki.vn page, paging paragraphs (blocks shared between
+ * branches instead of duplicated).  Same result as paged_attention_decode
+ * (or, with k_new/v_new, as paged_attention_decode_append).
+ *
+ *   group_offsets  device int32 [num_groups + 1]: group g is sequences
+ *                  group_offsets[g] .. group_offsets[g+1]-1; 0 = first entry,
+ *                  num_seqs = last; every sequence belongs to one group
+ *   prefix_lens    device int32 [num_groups]: tokens at the start of every
+ *                  member's context stored in the same physical blocks as the
+ *                  group's first member (its block-table entries are equal).
+ *                  A multiple of max(16, block_size); it is cut to the shortest
+ *                  member (minus one token when appending).  0 = no sharing.
+ *   k_new, v_new   device [num_seqs][num_kv_heads][head_dim] or both NULL: as
+ *                  in paged_attention_decode_append
+ *   workspace      at least paged_attention_grouped_workspace_size() bytes,
+ *                  256-byte aligned, no initialisation needed
+ * The shared part of each group is attended by one CTA per (group, kv head,
+ * 256 tokens), one warp per member, reading each tile once; each member's own
+ * tokens go through the balanced kernel; a merge kernel joins the two.
+ * A bad group description flags PKV_DEVERR_PREFIX; a member whose prefix
+ * blocks differ from the first member's has those blocks left out and flags
+ * PKV_DEVERR_PREFIX.  bf16 only, num_seqs <= 8192 (else PKV_ERR_UNSUPPORTED).
+ */
+PKV_EXPORT size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                              int max_seq_len);
+PKV_EXPORT pkv_status paged_attention_decode_grouped(void *out, const void *q, const void *k_new,
+                                  const void *v_new, void *k_cache, void *v_cache,
+                                  const int32_t *block_tables, const int32_t *seq_lens,
+                                  const int32_t *group_offsets, const int32_t *prefix_lens,
+                                  int num_groups, int num_seqs, int num_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int max_blocks_per_seq,
+                                  int num_blocks, int max_seq_len, float scale, void *workspace,
+                                  size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that
  * cannot allocate device memory.  No passage of the pages has a counterpart:
  * this entry point exists for the caller, not for the method.
@@ -319,6 +361,16 @@ PKV_EXPORT pkv_status block_allocator_block_table(const pkv_allocator *a, int64_
 PKV_EXPORT pkv_status block_allocator_block_tables(const pkv_allocator *a, const int64_t *seqs, int n,
                                         int32_t *out, int cap, int32_t pad,
                                         int32_t *seq_lens_out);
+
+/* Groups for paged_attention_decode_grouped: the given sequences, in order,
+ * are cut into runs whose block tables start with the same physical blocks
+ * (beams forked from one prompt).  group_offsets_out: host int32 [n + 1];
+ * prefix_lens_out: host int32 [n] (tokens in the shared full blocks, rounded
+ * down to a multiple of max(16, block_size); 0 for a single sequence);
+ * *num_groups_out = number of runs. */
+PKV_EXPORT pkv_status block_allocator_prefix_groups(const pkv_allocator *a, const int64_t *seqs, int n,
+                                         int32_t *group_offsets_out, int32_t *prefix_lens_out,
+                                         int *num_groups_out);
 
 /* Slots of token positions start .. start+count-1 of `seq` (all must exist). */
 PKV_EXPORT pkv_status block_allocator_slots(const pkv_allocator *a, int64_t seq, int64_t start,

@@ -25,11 +25,13 @@ from . import _lib
  PKV_ERR_TOO_LARGE) = range(7)
 NOALLOC_SCRATCH_BYTES = 16 << 20
 PKV_F32, PKV_BF16 = 0, 1
-DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, DEVERR_PREFIX = (
+    1, 2, 4, 8, 16, 32)
 
 __all__ = [
     "PkvError", "kv_cache_write", "paged_attention_decode", "paged_attention_workspace_size",
-    "paged_attention_decode_append", "block_copy", "read_device_errors", "BlockAllocator",
+    "paged_attention_decode_append", "paged_attention_decode_grouped",
+    "paged_attention_grouped_workspace_size", "block_copy", "read_device_errors", "BlockAllocator",
     "library_path",
 ]
 
@@ -168,6 +170,51 @@ def paged_attention_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_
     return out
 
 
+def paged_attention_grouped_workspace_size(num_seqs: int, num_heads: int, head_dim: int,
+                                           max_seq_len: int) -> int:
+    return int(_lib.load().paged_attention_grouped_workspace_size(num_seqs, num_heads, head_dim,
+                                                                  max_seq_len))
+
+
+def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, seq_lens, group_offsets,
+                                   prefix_lens, scale: float, max_seq_len: int, k_new=None, v_new=None,
+                                   workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode where the sequences of group g (group_offsets[g] .. [g+1]-1,
+    int32 on the device) share the blocks of their first prefix_lens[g]
+    tokens; each shared block is read once for the whole group.  With k_new /
+    v_new the new tokens are stored first, as in paged_attention_decode_append."""
+    lib = _lib.load()
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if Dk != D or tuple(out.shape) != (S, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables must be [S, maxB] and seq_lens [S]")
+    G = prefix_lens.shape[0]
+    if group_offsets.shape[0] != G + 1:
+        raise ValueError("group_offsets needs num_groups + 1 entries")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new, or neither")
+    if k_new is not None and (tuple(k_new.shape) != (S, Hkv, D) or v_new.shape != k_new.shape):
+        raise ValueError("k_new/v_new must be [S, Hkv, D]")
+    need = paged_attention_grouped_workspace_size(S, Hq, D, max_seq_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.paged_attention_decode_grouped(
+        _dev(out, "out"), _dev(q, "q"),
+        _dev(k_new, "k_new") if k_new is not None else None,
+        _dev(v_new, "v_new") if v_new is not None else None,
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32, 2), _dev(seq_lens, "seq_lens", torch.int32, 1),
+        _dev(group_offsets, "group_offsets", torch.int32, 1), _dev(prefix_lens, "prefix_lens", torch.int32, 1),
+        G, S, Hq, Hkv, D, B, block_tables.shape[1], NB, int(max_seq_len), float(scale), ws_ptr, ws_bytes,
+        _dtype_code(q), _stream(stream))
+    _check(st, "paged_attention_decode_grouped")
+    return out
+
+
 def block_copy(k_caches: Sequence[torch.Tensor], v_caches: Sequence[torch.Tensor],
                block_pairs: torch.Tensor, stream=None) -> None:
     """For every layer, K and V: block dst := block src for each (src, dst)
@@ -268,6 +315,17 @@ class BlockAllocator:
                                                       tables.ctypes.data, tables.shape[1],
                                                       int(pad), lens.ctypes.data), "block_tables")
         return tables, lens
+
+    def prefix_groups(self, seqs):
+        """(group_offsets int32 [G + 1], prefix_lens int32 [G]) for the
+        sequences in the given order (runs that start with the same blocks)."""
+        ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        offs = np.zeros(len(ids) + 1, dtype=np.int32)
+        pre = np.zeros(max(1, len(ids)), dtype=np.int32)
+        ng = ctypes.c_int(0)
+        _check(self._lib.block_allocator_prefix_groups(self._h, ids.ctypes.data, len(ids), offs.ctypes.data,
+                                                       pre.ctypes.data, ctypes.byref(ng)), "prefix_groups")
+        return offs[:ng.value + 1].copy(), pre[:ng.value].copy()
 
     def slots(self, seq: int, start: int, count: int) -> np.ndarray:
         out = np.empty(max(0, count), dtype=np.int64)

@@ -29,6 +29,13 @@ SIGNATURES = {
                                               c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                               c_int, c_int, c_int, c_int, c_int, c_float, c_int,
                                               c_void_p, c_size_t, c_int, c_void_p]),
+    "paged_attention_grouped_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "paged_attention_decode_grouped": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                               c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                               c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                               c_int, c_int, c_float, c_void_p, c_size_t, c_int,
+                                               c_void_p]),
+    "block_allocator_prefix_groups": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P(c_int)]),
     "paged_attention_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                                                c_int, c_int, c_float, c_int, c_int, c_void_p]),

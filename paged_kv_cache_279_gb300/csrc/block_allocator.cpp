@@ -194,6 +194,44 @@ pkv_status block_allocator_block_tables(const pkv_allocator *a, const int64_t *s
     return PKV_OK;
 }
 
+pkv_status block_allocator_prefix_groups(const pkv_allocator *a, const int64_t *seqs, int n,
+                                        int32_t *group_offsets_out, int32_t *prefix_lens_out,
+                                        int *num_groups_out) {
+    if (!a || n < 0 || (n > 0 && (!seqs || !group_offsets_out || !prefix_lens_out)) || !num_groups_out)
+        return PKV_ERR_INVALID;
+    std::vector<const pkv_allocator::Seq *> ss((size_t)n);
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seqs[i]);
+        if (it == a->seqs.end()) return PKV_ERR_INVALID;
+        ss[i] = &it->second;
+    }
+    const int64_t B = a->block_size;
+    const int64_t align = B > 16 ? B : 16;  // whole 16-token tiles and whole blocks
+    int g = 0;
+    group_offsets_out[0] = 0;
+    for (int i = 0; i < n;) {
+        // leading full blocks identical in the run of sequences starting at i
+        int64_t common = ss[i]->tokens / B;
+        int j = i + 1;
+        while (j < n) {
+            const auto &lt = ss[i]->table, &t = ss[j]->table;
+            int64_t c = 0;
+            const int64_t lim = std::min<int64_t>(common, ss[j]->tokens / B);
+            while (c < lim && lt[(size_t)c] == t[(size_t)c]) ++c;
+            if (c == 0) break;
+            common = c;
+            ++j;
+        }
+        const int64_t shared = j - i > 1 ? common * B / align * align : 0;
+        prefix_lens_out[g] = (int32_t)shared;
+        group_offsets_out[g + 1] = j;
+        ++g;
+        i = j;
+    }
+    *num_groups_out = g;
+    return PKV_OK;
+}
+
 pkv_status block_allocator_slots(const pkv_allocator *a, int64_t seq, int64_t start,
                                  int64_t count, int64_t *out) {
     if (!a || start < 0 || count < 0 || (count > 0 && !out)) return PKV_ERR_INVALID;

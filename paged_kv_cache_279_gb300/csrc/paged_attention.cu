@@ -61,6 +61,9 @@ struct DecodeArgs {
     float *part_m;  // [S][Hq][max_parts]
     float *part_l;  // [S][Hq][max_parts]
     int *pieces;    // [S][Hkv]: partials of each segment (balanced path)
+    int *seq_tok0;  // [S]: tokens of a shared prefix attended elsewhere (grouped path), or nullptr
+    int prefix_slot;      // grouped path: first partial slot of the prefix partials
+    int prefix_part;      // grouped path: tokens per prefix partition
     int num_seqs, num_heads, num_kv_heads, group;
     int block_size, max_blocks, num_blocks, max_seq_len;
     int partition_size, max_parts;
@@ -108,6 +111,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                  "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -312,13 +319,13 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs &a, int seq, i
 // Attend one staged 16-token tile (K at sk, V at sv, 128-byte swizzled
 // halves).  row_ok has a bit per token row that belongs to the context and
 // came from a valid block; other rows are masked and their V zeroed.
-template <int D>
+template <int D, bool kZeroMasked = true>
 __device__ __forceinline__ void attend_tile(unsigned char *sk, unsigned char *sv, uint32_t row_ok,
                                             const uint32_t (&qb)[D / 16][2], float sl2,
                                             WarpAcc<D> &acc, int lane) {
     using Lay = Bf16Layout<D>;
     const int r0 = lane >> 2;
-    if (row_ok != 0xffffu) {
+    if (kZeroMasked && row_ok != 0xffffu) {
         // masked rows hold stale, unwritten or substituted slots: zero their
         // V so that a zero weight never meets a NaN
         for (int e = lane; e < Lay::kHalves * kTile * 8; e += 32) {
@@ -331,16 +338,18 @@ __device__ __forceinline__ void attend_tile(unsigned char *sk, unsigned char *sv
     }
     const uint32_t ska = smem_u32(sk), sva = smem_u32(sv);
     const int lj = lane >> 3, lr = lane & 7;
+    // this lane's row of each 8x8 ldmatrix: token row and 16-byte chunk, 128-byte swizzle
+    const int ktok = lr + 8 * (lj & 1), vtok = lr + 8 * (lj >> 1);
+    const uint32_t krow = ska + ktok * 128, vrow = sva + vtok * 128;
+    const int kx = ktok & 7, vx = vtok & 7;
 
     // S^T (16 tokens x 8 heads) = K_tile . Q^T
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-        const int tok = lr + 8 * (lj & 1);
         const int chunk = 2 * (ks & 3) + (lj >> 1);
-        const uint32_t addr = ska + (ks >> 2) * Lay::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
         uint32_t x0, x1, x2, x3;
-        ldmatrix_x4(addr, x0, x1, x2, x3);
+        ldmatrix_x4(krow + (ks >> 2) * Lay::kHalfBytes + ((chunk ^ kx) << 4), x0, x1, x2, x3);
         mma_bf16_16816(sc, x0, x1, x2, x3, qb[ks][0], qb[ks][1]);
     }
 
@@ -359,29 +368,36 @@ __device__ __forceinline__ void attend_tile(unsigned char *sk, unsigned char *sv
     const float mn0 = fmaxf(acc.m0, mx0), mn1 = fmaxf(acc.m1, mx1);
     // reference points stay finite even if nothing valid has been seen yet
     const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
+    // the running maxima rarely move once a few tiles are in: rescale only then
+    const bool moved = __any_sync(0xffffffffu, mn0 != acc.m0 || mn1 != acc.m1);
     const float al0 = exp2f(acc.m0 - rf0), al1 = exp2f(acc.m1 - rf1);
     acc.m0 = mn0;
     acc.m1 = mn1;
     const uint32_t p01 = pack_bf16x2(exp2f(s0 - rf0), exp2f(s1 - rf1));
     const uint32_t p23 = pack_bf16x2(exp2f(s2 - rf0), exp2f(s3 - rf1));
     // the sum uses the same rounded weights as the numerator
-    acc.l0 = acc.l0 * al0 + (bf16x2_lo(p01) + bf16x2_lo(p23));
-    acc.l1 = acc.l1 * al1 + (bf16x2_hi(p01) + bf16x2_hi(p23));
+    if (moved) {
+        acc.l0 = acc.l0 * al0;
+        acc.l1 = acc.l1 * al1;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            acc.o[mt][0] *= al0;
+            acc.o[mt][1] *= al1;
+            acc.o[mt][2] *= al0;
+            acc.o[mt][3] *= al1;
+        }
+    }
+    acc.l0 += bf16x2_lo(p01) + bf16x2_lo(p23);
+    acc.l1 += bf16x2_hi(p01) + bf16x2_hi(p23);
     const uint32_t pb0 = movmatrix_trans(p01);
     const uint32_t pb1 = movmatrix_trans(p23);
 
-    // O^T (head_dim x 8 heads) = O^T * alpha + V_tile^T . P^T
+    // O^T (head_dim x 8 heads) += V_tile^T . P^T
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
-        acc.o[mt][0] *= al0;
-        acc.o[mt][1] *= al1;
-        acc.o[mt][2] *= al0;
-        acc.o[mt][3] *= al1;
-        const int tok = lr + 8 * (lj >> 1);
         const int chunk = 2 * (mt & 3) + (lj & 1);
-        const uint32_t addr = sva + (mt >> 2) * Lay::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
         uint32_t x0, x1, x2, x3;
-        ldmatrix_x4_trans(addr, x0, x1, x2, x3);
+        ldmatrix_x4_trans(vrow + (mt >> 2) * Lay::kHalfBytes + ((chunk ^ vx) << 4), x0, x1, x2, x3);
         mma_bf16_16816(acc.o[mt], x0, x1, x2, x3, pb0, pb1);
     }
 }
@@ -576,14 +592,15 @@ constexpr int kYCache = 768;  // tiles of a share whose TMA rows are staged in s
 // Shared-memory layout of the balanced kernel (host and device agree on it).
 // Offsets are from the 1024-aligned base.
 struct StreamKLayout {
-    int ring, bars, ycache, masks, prefix, total;
-    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs) {
+    int ring, bars, ycache, masks, prefix, toff, total;
+    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, bool grouped) {
         ring = NW * NS * 2 * (D / 64) * kTile * 128;
         bars = ring;
         ycache = bars + NW * NS * 8;   // int2 per cached tile
         masks = ycache + kYCache * 8;  // valid-row mask per cached tile
         prefix = masks + kYCache * 4;
-        total = prefix + (num_seqs + 1) * 4 + 1024;  // + alignment slack
+        toff = prefix + (num_seqs + 1) * 4;  // grouped: first token of each sequence's own part
+        total = toff + (grouped ? num_seqs * 4 : 0) + 1024;  // + alignment slack
     }
 };
 
@@ -633,13 +650,14 @@ struct TileRows {
     uint32_t mask;
 };
 
-__device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int kvh, int tile, int len) {
+__device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int kvh, int tile, int len,
+                                              int tok_off = 0) {
     const int B = a.block_size;
     const int boxh = B < kTile ? B : kTile;
     const int32_t *bt = a.block_tables + (int64_t)seq * a.max_blocks;
     TileRows r{-1, -1, 0u};
     for (int sb = 0; sb < kTile / boxh; ++sb) {
-        const int tok = tile * kTile + sb * boxh;
+        const int tok = tok_off + tile * kTile + sb * boxh;
         if (tok >= len) break;
         const int lb = tok / B;
         int blk = bt[lb];
@@ -653,7 +671,7 @@ __device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int 
         const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
         if (sb == 0) r.y0 = y; else r.y1 = y;
     }
-    const int valid = min(kTile, len - tile * kTile);
+    const int valid = min(kTile, len - tok_off - tile * kTile);
     r.mask &= (1u << valid) - 1u;
     return r;
 }
@@ -737,11 +755,13 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const StreamKLayout L(D, NW, NS, a.num_seqs);
+    const bool grouped = a.seq_tok0 != nullptr;
+    const StreamKLayout L(D, NW, NS, a.num_seqs, grouped);
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + L.bars);
     int2 *ycache = reinterpret_cast<int2 *>(smem + L.ycache);
     uint32_t *mcache = reinterpret_cast<uint32_t *>(smem + L.masks);
     int *prefix = reinterpret_cast<int *>(smem + L.prefix);
+    int *toff = reinterpret_cast<int *>(smem + L.toff);
     __shared__ int warp_sums[NW];
     __shared__ int carry;
 
@@ -764,7 +784,11 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (sq < S) {
             const int raw = a.seq_lens[sq];
             if ((raw < 0 || raw > cap) && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
-            v = Hkv * ((clamp_len(raw, cap) + kTile - 1) / kTile);
+            const int len = clamp_len(raw, cap);
+            // grouped: the shared prefix was attended by the prefix kernel
+            const int t0 = grouped ? min(max(a.seq_tok0[sq], 0), len) : 0;
+            if (grouped) toff[sq] = t0;
+            v = Hkv * ((len - t0 + kTile - 1) / kTile);
         }
         int x = v;  // inclusive warp scan
 #pragma unroll
@@ -826,6 +850,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int u = 0; u < kPer; ++u) {
             if (sq[u] < 0) continue;
             const int32_t *bt = a.block_tables + (int64_t)sq[u] * a.max_blocks;
+            if (grouped) tl[u] += toff[sq[u]] / kTile;  // token offsets are tile aligned
             // the tile's tokens lie inside the clamped length, hence inside the table
             const int lb0 = min(tl[u] * kTile / B, a.max_blocks - 1);
             const int lb1 = min((tl[u] * kTile + boxh) / B, a.max_blocks - 1);
@@ -935,7 +960,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int2 y = ycache[i];
             return TileRows{y.x, y.y, mcache[i] & 0xffffu};
         }
-        return tile_rows(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap));
+        return tile_rows(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap),
+                         grouped ? toff[c.seq] : 0);
     };
 
     SegCursor prod;  // lane 0: segment of the tile being issued (needed past the cache)
@@ -978,7 +1004,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 issue(k + NS, buf);
             }
         }
-        const bool whole = pa == seg.seg_start && pb == seg_end;
+        // a grouped sequence's own part is always a partial: the prefix joins it in the merge
+        const bool whole = pa == seg.seg_start && pb == seg_end && !(grouped && toff[seg.seq] > 0);
         const int64_t w0 = share_owner(seg.seg_start, T, parts);
         store_piece<D>(a, acc, dead, seg, whole, (int)(gw - w0), lane);
         if (lane == 0 && pa == seg.seg_start) {
@@ -1023,6 +1050,170 @@ append_tokens_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
         const int64_t row = ((int64_t)blk * num_kv_heads + h) * block_size + (pos - lb * block_size);
         k_cache[row * chunks + c] = k_new[i];
         v_cache[row * chunks + c] = v_new[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix kernel (grouped decode).  Sequences [off[g], off[g+1]) share
+// the physical blocks of their first prefix_lens[g] tokens (beam search,
+// parallel sampling).  One CTA per (group, kv head, prefix partition): warp 0
+// streams the partition's tiles once, through a ring shared by the whole CTA,
+// and each of the other warps attends one member's queries to every tile.  The
+// per-member partials join the member's own tokens in the merge kernel.
+// ---------------------------------------------------------------------------
+constexpr int kPrefixPart = 256;  // prefix tokens per CTA (at most 32 tiles: one lane each)
+constexpr int kPrefixMembers = 8; // members attended per pass over the prefix
+
+template <int D, int NS>
+constexpr int prefix_smem_bytes() {
+    return NS * Bf16Layout<D>::kStageBytes + 2 * NS * 8 + (kPrefixPart / 8 + 2) * 4 + 1024;
+}
+
+template <int D, int NS>
+__global__ void __launch_bounds__((kPrefixMembers + 1) * 32, 2)
+decode_bf16_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
+                          const int32_t *__restrict__ group_offsets,
+                          const int32_t *__restrict__ prefix_lens, int num_groups) {
+    using Lay = Bf16Layout<D>;
+    constexpr int NWP = kPrefixMembers;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * Lay::kStageBytes);
+    uint64_t *empty = full + NS;
+    int *bt_s = reinterpret_cast<int *>(empty + NS);
+    __shared__ int min_len;
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int g = blockIdx.x, kvh = blockIdx.y, part = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.num_seqs, B = a.block_size;
+    const int cap = min(a.max_seq_len, a.max_blocks * B);
+    int m0 = group_offsets[g], m1 = group_offsets[g + 1];
+    if (m0 < 0 || m1 > S || m1 < m0) {
+        if (threadIdx.x == 0 && kvh == 0 && part == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+        m0 = m1 = 0;
+    }
+    if (g == 0 && kvh == 0 && part == 0 && threadIdx.x == 0 &&
+        (group_offsets[0] != 0 || group_offsets[num_groups] != S))
+        flag_error(a.err, PKV_DEVERR_PREFIX);
+
+    // the shared part actually attended here: the group's prefix, cut to whole
+    // tiles and blocks and to the shortest member
+    const int align = B > kTile ? B : kTile;
+    const int pre_raw = prefix_lens[g];
+    if (threadIdx.x == 0) min_len = cap;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m1 - m0; i += blockDim.x) atomicMin(&min_len, clamp_len(a.seq_lens[m0 + i], cap));
+    __syncthreads();
+    int pre = pre_raw < 0 ? 0 : pre_raw;
+    if (pre % align != 0 && threadIdx.x == 0 && kvh == 0 && part == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+    // with an append, every member's new token must stay in its own part
+    pre = min(pre, min_len - (a.k_new ? 1 : 0)) / align * align;
+    if (pre < 0) pre = 0;
+    if (m1 - m0 < 1) pre = 0;
+    if (kvh == 0 && part == 0)
+        for (int i = threadIdx.x; i < m1 - m0; i += blockDim.x) a.seq_tok0[m0 + i] = pre;
+
+    const int t_begin = part * kPrefixPart;
+    const int t_end = min(pre, t_begin + kPrefixPart);
+    if (t_begin >= t_end) return;
+    const int ntiles = (t_end - t_begin) / kTile;  // pre is a whole number of tiles
+    const int boxh = B < kTile ? B : kTile;
+
+    // leader's block ids of this partition
+    const int32_t *bt = a.block_tables + (int64_t)m0 * a.max_blocks;
+    const int lb0 = t_begin / B, nblk = (t_end - 1) / B - lb0 + 1;
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) bt_s[i] = bt[lb0 + i];
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NWP);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int members = m1 - m0;
+    const int passes = (members + NWP - 1) / NWP;
+    const int iters = passes * ntiles;
+    if (warp == 0) {
+        // producer: the same tiles once per pass of up to NWP members
+        if (lane == 0) {
+            for (int it = 0; it < iters; ++it) {
+                const int st = it % NS;
+                if (it >= NS && !mbar_wait_bounded(&empty[st], (uint32_t)(((it / NS) - 1) & 1))) {
+                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int t0 = t_begin + (it % ntiles) * kTile;
+                TileRows r{-1, -1, 0u};
+                for (int sb = 0; sb < kTile / boxh; ++sb) {
+                    const int tok = t0 + sb * boxh;
+                    const int lb = tok / B;
+                    int blk = bt_s[lb - lb0];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        blk = 0;
+                    }
+                    const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
+                    if (sb == 0) r.y0 = y; else r.y1 = y;
+                }
+                issue_rows<D>(&tm_k, &tm_v, smem + st * Lay::kStageBytes, &full[st], boxh, r);
+            }
+        }
+        return;  // no CTA-wide barrier follows
+    }
+
+    // consumers: warp w attends member (pass * NWP + w - 1)
+    uint32_t qb[D / 16][2];
+    WarpAcc<D> acc;
+    bool dead = false;
+    for (int pass = 0; pass < passes; ++pass) {
+        const int mi = pass * NWP + warp - 1;
+        const bool active = mi < members;
+        const int sq = m0 + (active ? mi : 0);
+        const int32_t *mbt = a.block_tables + (int64_t)sq * a.max_blocks;
+        if (active) load_q_fragments<D>(a, sq, kvh, lane, qb);
+        // once per pass: lane i checks that tile i's blocks are valid and are this
+        // member's own (shared) blocks; bit i of tile_ok gives the answer
+        bool ok = false, bad = false;
+        if (active && lane < ntiles) {
+            const int ta = t_begin + lane * kTile;
+            const int lba = ta / B, lbb = (ta + kTile - 1) / B;
+            const int ba = bt_s[lba - lb0], bb = bt_s[lbb - lb0];
+            const bool va = ba >= 0 && ba < a.num_blocks, vb = bb >= 0 && bb < a.num_blocks;
+            const bool sa = mbt[lba] == ba, sb = mbt[lbb] == bb;
+            ok = va && vb && sa && sb;
+            bad = (va && !sa) || (vb && !sb);
+        }
+        const uint32_t tile_ok = __ballot_sync(0xffffffffu, ok);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+        acc.reset();
+        for (int i = 0; i < ntiles; ++i) {
+            const int it = pass * ntiles + i;
+            const int st = it % NS;
+            if (!dead && !mbar_wait_bounded(&full[st], (uint32_t)((it / NS) & 1))) {
+                if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                dead = true;
+            }
+            if (!dead && active) {
+                const uint32_t row_ok = (tile_ok >> i) & 1u ? 0xffffu : 0u;
+                unsigned char *sk = smem + st * Lay::kStageBytes;
+                attend_tile<D, false>(sk, sk + Lay::kKVBytes, row_ok, qb, a.scale_log2, acc, lane);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        if (active) {
+            SegCursor c;
+            c.seq = sq;
+            c.kvh = kvh;
+            store_piece<D>(a, acc, dead, c, false, a.prefix_slot + part, lane);
+        }
     }
 }
 
@@ -1133,11 +1324,13 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     // issue the length, the piece count and the first 32 (max, sum) pairs at
     // once; pairs past the piece count are masked below
     const int raw_len = a.seq_lens[seq];
-    int nparts = 0;
+    int nparts = 0, tok0 = 0;
     if (PIECES) {
         const int h = (int)(row - (int64_t)seq * a.num_heads);
         nparts = a.pieces[(int64_t)seq * a.num_kv_heads + h / a.group];
+        if (a.seq_tok0) tok0 = a.seq_tok0[seq];
     }
+    // speculative (max, sum) of the first 32 own pieces; masked below
     float mj = -INFINITY, lj = 0.f;
     if (lane < a.max_parts) {
         mj = pm[lane];
@@ -1145,40 +1338,53 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     }
     const int len = raw_len < 0 ? 0 : (raw_len > cap ? cap : raw_len);
     T *dst = static_cast<T *>(a.out) + row * D + lane * E;
+    int npre = 0;  // grouped: prefix partials at slots prefix_slot ...
     if (PIECES) {
         if (len == 0) {
 #pragma unroll
             for (int e = 0; e < E; ++e) store_out(dst + e, 0.f);
             return;
         }
+        tok0 = min(max(tok0, 0), len);
+        if (tok0 > 0) {
+            npre = (tok0 + a.prefix_part - 1) / a.prefix_part;
+            if (len == tok0) nparts = 0;  // nothing of its own: no piece was written
+        }
     } else {
         nparts = (len + a.partition_size - 1) / a.partition_size;
     }
-    if (nparts <= 1) return;
-    if (lane >= nparts) {
+    if (npre == 0 && nparts <= 1) return;
+    const int total = nparts + npre;
+    // partial j: own piece j, then prefix partition j - nparts
+    auto slot = [&](int j) { return j < nparts ? j : a.prefix_slot + (j - nparts); };
+    if (npre > 0 && lane < total && lane >= nparts) {
+        mj = pm[slot(lane)];
+        lj = pl[slot(lane)];
+    }
+    if (lane >= total) {
         mj = -INFINITY;
         lj = 0.f;
     }
     float M = mj;
-    for (int j = lane + 32; j < nparts; j += 32) M = fmaxf(M, pm[j]);
+    for (int j = lane + 32; j < total; j += 32) M = fmaxf(M, pm[slot(j)]);
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
     if (M == -INFINITY) M = 0.f;  // only if every block was invalid (flagged)
     auto ex = [&](float x) { return x == -INFINITY ? 0.f : (LOG2 ? exp2f(x - M) : expf(x - M)); };
     const float wl = ex(mj);  // weight of partial `lane`
     float lsum = wl * lj;
-    for (int j = lane + 32; j < nparts; j += 32) lsum += ex(pm[j]) * pl[j];
+    for (int j = lane + 32; j < total; j += 32) lsum += ex(pm[slot(j)]) * pl[slot(j)];
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, sh);
 
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int j0 = 0; j0 < nparts; j0 += U) {
+    for (int j0 = 0; j0 < total; j0 += U) {
         float v[U][E];
 #pragma unroll
         for (int u = 0; u < U; ++u) {  // U independent row loads in flight
-            const int j = j0 + u < nparts ? j0 + u : nparts - 1;
+            const int j = slot(j0 + u < total ? j0 + u : total - 1);
 #pragma unroll
             for (int e = 0; e < E; ++e) v[u][e] = po[(int64_t)j * D + e];
         }
@@ -1186,7 +1392,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
         for (int u = 0; u < U; ++u) {
             const int j = j0 + u;
             const float wsh = __shfl_sync(0xffffffffu, wl, j & 31);
-            const float w = j >= nparts ? 0.f : (j < 32 ? wsh : ex(pm[j]));
+            const float w = j >= total ? 0.f : (j < 32 ? wsh : ex(pm[slot(j)]));
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[e] += w * v[u][e];
         }
@@ -1339,8 +1545,8 @@ template <int D, int NW, int NS>
 static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
     static bool done[128] = {};
     auto kern = decode_bf16_streamk_kernel<D, NW, NS>;
-    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs).total, done)) return PKV_ERR_CUDA;
-    const int smem = StreamKLayout(D, NW, NS, a.num_seqs).total;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, true).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, a.seq_tok0 != nullptr).total;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
         per_sm < 1)
@@ -1549,6 +1755,115 @@ PKV_API pkv_status paged_attention_decode_append(
     return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
                        num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_seq_len,
                        scale, partition_size, workspace, workspace_bytes, dtype, stream, k_new, v_new);
+}
+
+// ---------------------------------------------------------------------------
+// Grouped decode: shared prefixes attended once per group.
+// ---------------------------------------------------------------------------
+static int64_t prefix_slots(int max_seq_len) { return ((int64_t)max_seq_len + kPrefixPart - 1) / kPrefixPart; }
+
+static WorkspaceLayout grouped_layout(int64_t S, int64_t Hq, int64_t D, int max_seq_len, size_t *tok0_off) {
+    WorkspaceLayout w = workspace_layout(S, Hq, D, balanced_slots(max_seq_len) + prefix_slots(max_seq_len), true);
+    *tok0_off = w.total;
+    w.total += round256((size_t)(S * 4));
+    return w;
+}
+
+template <int D>
+static pkv_status launch_prefix(const DecodeArgs &a, const int32_t *group_offsets, const int32_t *prefix_lens,
+                                int num_groups, cudaStream_t st) {
+    constexpr int NS = 8;
+    static bool done[128] = {};
+    constexpr int smem = prefix_smem_bytes<D, NS>();
+    auto kern = decode_bf16_prefix_kernel<D, NS>;
+    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
+    const dim3 grid((unsigned)num_groups, (unsigned)a.num_kv_heads, (unsigned)prefix_slots(a.max_seq_len));
+    return launch_pdl(kern, grid, dim3((kPrefixMembers + 1) * 32), smem, st, mk, mv, a, group_offsets,
+                      prefix_lens, num_groups);
+}
+
+PKV_API size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                                      int max_seq_len) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
+    size_t tok0_off = 0;
+    return grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off).total;
+}
+
+PKV_API pkv_status paged_attention_decode_grouped(
+    void *out, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+    const int32_t *block_tables, const int32_t *seq_lens, const int32_t *group_offsets,
+    const int32_t *prefix_lens, int num_groups, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale, void *workspace,
+    size_t workspace_bytes, int dtype, void *stream) {
+    if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        max_seq_len < 0 || !std::isfinite(scale) || num_groups < 1)
+        return PKV_ERR_INVALID;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
+    if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > kGMax || num_seqs > kMaxBalancedSeqs) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_seq_len == 0) return PKV_OK;
+    if (num_groups > num_seqs || (int64_t)num_groups > 0x7fffffff) return PKV_ERR_INVALID;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !group_offsets || !prefix_lens)
+        return PKV_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
+    if (rows > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
+        return PKV_ERR_UNSUPPORTED;
+    if (prefix_slots(max_seq_len) > 65535) return PKV_ERR_INVALID;
+    size_t tok0_off = 0;
+    const WorkspaceLayout lay = grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_INVALID;
+
+    DecodeArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.partition_size = kDefaultPartition;
+    a.scale = scale;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.err = device_error_word();
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache_w = k_cache;
+    a.v_cache_w = v_cache;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
+    a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
+    a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
+    a.pieces = reinterpret_cast<int *>(ws + lay.pieces_off);
+    a.seq_tok0 = reinterpret_cast<int *>(ws + tok0_off);
+    a.max_parts = (int)(balanced_slots(max_seq_len) + prefix_slots(max_seq_len));
+    a.prefix_slot = (int)balanced_slots(max_seq_len);
+    a.prefix_part = kPrefixPart;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    pkv_status rc = head_dim == 128 ? launch_prefix<128>(a, group_offsets, prefix_lens, num_groups, st)
+                                    : launch_prefix<64>(a, group_offsets, prefix_lens, num_groups, st);
+    if (rc == PKV_OK) rc = head_dim == 128 ? dispatch_balanced<128>(a, st) : dispatch_balanced<64>(a, st);
+    if (rc == PKV_OK)
+        rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, true>(a, st)
+                             : launch_reduce<__nv_bfloat16, 64, true, true>(a, st);
+    return rc;
 }
 
 // ---------------------------------------------------------------------------

@@ -109,3 +109,52 @@ def assert_f32_close(got: torch.Tensor, ref: np.ndarray, what=""):
 def bits(t: torch.Tensor) -> torch.Tensor:
     """Integer view for bit-exact comparisons (NaN payloads included)."""
     return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def build_beam_pool(shape, shared, num_prompts, width, divergent, seed=2, append_last=False):
+    """Beam search through the library's allocator: `num_prompts` prompts of
+    `shared` tokens, each forked into `width` beams; beam b then produces
+    divergent[b] tokens (copy-on-write pairs executed with block_copy, tokens
+    stored with kv_cache_write).  With append_last, every beam's last token is
+    left unwritten (for a decode-and-append call) and returned as k_new/v_new.
+    Returns a dict with the pool, allocator, tables, lengths and the contiguous
+    K/V of every beam (prompt followed by its own tokens)."""
+    B, Hkv, D = shape.block_size, shape.num_kv_heads, shape.head_dim
+    div = [int(d) for d in divergent]
+    nbeams = num_prompts * width
+    NB = num_prompts * (-(-shared // B) + 1) + sum(-(-d // B) + 1 for d in div) + 64
+    alloc = pkv.BlockAllocator(NB, B)
+    kc = torch.full((NB, Hkv, B, D), float("nan"), dtype=shape.dtype, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    prefix = [wl.draw_seq_kv(shape, seed, p, shared) for p in range(num_prompts)]
+    own = [wl.draw_seq_kv(shape, seed + 1, b, div[b]) for b in range(nbeams)]
+    for p in range(num_prompts):
+        assert alloc.add_seq(p * width, shared) == 0
+        slots = torch.from_numpy(alloc.slots(p * width, 0, shared)).cuda()
+        pkv.kv_cache_write(prefix[p][0].cuda(), prefix[p][1].cuda(), kc, vc, slots)
+        for c in range(1, width):
+            assert alloc.fork(p * width, p * width + c) == 0
+    copies = 0
+    for t in range(max(div) if div else 0):
+        beams = [b for b in range(nbeams) if div[b] > t]
+        st, slots, pairs = alloc.append_slots(beams)
+        assert st == 0
+        if len(pairs):
+            copies += len(pairs)
+            pkv.block_copy([kc], [vc], torch.from_numpy(np.ascontiguousarray(pairs)).cuda())
+        keep = [i for i, b in enumerate(beams) if not (append_last and t == div[b] - 1)]
+        if keep:
+            kn = torch.stack([own[beams[i]][0][t] for i in keep]).cuda()
+            vn = torch.stack([own[beams[i]][1][t] for i in keep]).cuda()
+            pkv.kv_cache_write(kn, vn, kc, vc, torch.from_numpy(slots[keep]).cuda())
+    seqs = list(range(nbeams))
+    cap = max(len(alloc.block_table(s)) for s in seqs)
+    tables, lens = alloc.block_tables(seqs, cap=cap)
+    ks = [torch.cat([prefix[b // width][0], own[b][0]]) for b in seqs]
+    vs = [torch.cat([prefix[b // width][1], own[b][1]]) for b in seqs]
+    k_new = torch.stack([own[b][0][div[b] - 1] if div[b] else torch.zeros(Hkv, D, dtype=shape.dtype)
+                         for b in seqs])
+    v_new = torch.stack([own[b][1][div[b] - 1] if div[b] else torch.zeros(Hkv, D, dtype=shape.dtype)
+                         for b in seqs])
+    return dict(kc=kc, vc=vc, alloc=alloc, tables=tables, lens=lens, ks=ks, vs=vs, copies=copies,
+                seqs=seqs, k_new=k_new, v_new=v_new)

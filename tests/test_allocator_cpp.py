@@ -148,3 +148,27 @@ def test_batched_append_matches_sequential_model(seed):
         assert_same_state(c, m, live)
     st, _, _ = c.append_slots([live[0], live[0]])
     assert st == 1  # repeated id
+
+
+def test_prefix_groups_follow_forks():
+    c = pkv.BlockAllocator(600, 16)
+    for p in range(3):
+        assert c.add_seq(10 * p, 1032) == 0
+        for k in range(1, 4):
+            assert c.fork(10 * p, 10 * p + k) == 0
+    assert c.add_seq(100, 40) == 0
+    order = [0, 1, 2, 3, 10, 11, 12, 13, 100, 20, 21, 22, 23]
+    offs, pre = c.prefix_groups(order)
+    assert offs.tolist() == [0, 4, 8, 9, 13]
+    assert pre.tolist() == [1024, 1024, 0, 1024]  # 64 full shared blocks; singleton 0
+    # after every beam appends (copy-on-write of the partial block) the full blocks stay shared
+    for s in order:
+        assert c.append_slot(s)[0] == 0
+    offs2, pre2 = c.prefix_groups(order)
+    assert offs2.tolist() == offs.tolist() and pre2.tolist() == [1024, 1024, 0, 1024]
+    # block size 8 rounds the shared length down to whole 16-token tiles
+    c8 = pkv.BlockAllocator(100, 8)
+    c8.add_seq(0, 100)
+    c8.fork(0, 1)
+    offs8, pre8 = c8.prefix_groups([0, 1])
+    assert offs8.tolist() == [0, 2] and pre8.tolist() == [96]
