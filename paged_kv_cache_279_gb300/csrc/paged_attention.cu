@@ -62,6 +62,7 @@ struct DecodeArgs {
     float *part_l;  // [S][Hq][max_parts]
     int *pieces;    // [S][Hkv]: partials of each segment (balanced path)
     int *seq_tok0;  // [S]: tokens of a shared prefix attended elsewhere (grouped path), or nullptr
+    int *prefix_pieces;   // [S][Hkv]: prefix partials of each member (tensor-core prefix kernel), or nullptr
     int prefix_slot;      // grouped path: first partial slot of the prefix partials
     int prefix_part;      // grouped path: tokens per prefix partition
     int num_seqs, num_heads, num_kv_heads, group;
@@ -773,11 +774,14 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int cap = min(a.max_seq_len, a.max_blocks * a.block_size);
 
     // prefix[s] = tiles of all segments of the sequences before s
+    __shared__ int seg_max;  // tiles of the longest segment
     if (threadIdx.x == 0) {
         prefix[0] = 0;
         carry = 0;
+        seg_max = 0;
     }
     __syncthreads();
+    int my_max = 0;
     for (int base = 0; base < S; base += NW * 32) {
         const int sq = base + threadIdx.x;
         int v = 0;
@@ -789,6 +793,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int t0 = grouped ? min(max(a.seq_tok0[sq], 0), len) : 0;
             if (grouped) toff[sq] = t0;
             v = Hkv * ((len - t0 + kTile - 1) / kTile);
+            my_max = max(my_max, (len - t0 + kTile - 1) / kTile);
         }
         int x = v;  // inclusive warp scan
 #pragma unroll
@@ -805,8 +810,19 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (threadIdx.x == NW * 32 - 1) carry = before + x;
         __syncthreads();
     }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, sh));
+    if (lane == 0) atomicMax(&seg_max, my_max);
+    __syncthreads();
     const int64_t T = prefix[S];
-    int64_t parts = T / kMinTilesPerCta;  // warps that get a share
+    // Warps that get a share.  A segment of n tiles meets at most
+    // ceil(n / share) + 1 shares and has own_slots partial slots, so shares
+    // hold at least ceil(seg_max / (own_slots - 1)) tiles; that is at most
+    // kMinTilesPerCta, and less when every segment is short, which spreads
+    // many short contexts over more warps.
+    const int own_slots = grouped ? a.prefix_slot : a.max_parts;
+    const int64_t min_share = own_slots > 1 ? max(1, (seg_max + own_slots - 2) / (own_slots - 1)) : (int64_t)T;
+    int64_t parts = T / max((int64_t)1, min_share);
     if (parts < 1) parts = 1;
     if (parts > (int64_t)gridDim.x * NW) parts = (int64_t)gridDim.x * NW;
     const int64_t gw0 = (int64_t)blockIdx.x * NW;
@@ -1218,6 +1234,583 @@ decode_bf16_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // ---------------------------------------------------------------------------
+// Shared prefixes on the 5th-generation tensor cores (tcgen05).
+//
+// Per kv head, a group's prefix is one dense contraction: the queries of all
+// members (members x G rows) against the same K and V tiles.  One CTA per SM
+// takes an equal contiguous share of the 64-token tiles of all contexts
+// (group, member chunk, kv head) and walks it piece by piece (a piece = the
+// share's tiles of one context).  Warp roles:
+//   warps 0-3  softmax: one thread per query row = one TMEM lane.  Reads S
+//              from TMEM, keeps the row's running max and sum, writes P
+//              (bf16) to shared memory, and at the end of a piece reads O
+//              from TMEM and stores the partial.
+//   warp 4     producer: the leader's block ids of a piece staged in shared
+//              memory by the whole warp (many loads in flight), then TMA loads
+//              of K and V tiles into an NS-stage ring from one lane.
+//   warp 5     MMA: one thread issues S = Q K^T (double-buffered in TMEM)
+//              and O += P V (accumulated in TMEM); the warp owns the TMEM
+//              allocation.
+//   warp 6     checks that every member's block table holds the leader's
+//              blocks over the prefix (flags PKV_DEVERR_PREFIX otherwise).
+// The MMA is M = 128 rows; rows past members x G are zero queries whose
+// results are never stored.  The running max is only moved (and O rescaled)
+// when a tile's max exceeds it by more than 2^8, so most tiles rescale
+// nothing; the merge uses whatever max each partial carries.
+// ---------------------------------------------------------------------------
+namespace tc {
+constexpr int kTok = 64;          // tokens per tile: N of Q K^T, K of P V
+constexpr int kRows = 128;        // MMA M: query rows of one context
+constexpr int kMinTiles = 4;      // shares hold >= 256 tokens
+constexpr int kMaxGroups = 2048;  // groups whose tile counts are scanned in shared memory
+constexpr int kThreads = 224;
+constexpr int kIdCache = 512;     // leader block ids staged by the producer warp
+constexpr float kRescale = 8.f;   // headroom (log2 units) before the running max moves
+constexpr uint32_t kTmemCols = 512;  // S0 | S1 (64 columns each) | O0 | O1 (128 each, by piece parity)
+
+template <int D, int NS>
+struct Layout {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kQBytes = kHalves * kRows * 128;  // [half][row][128 B]
+    static constexpr int kKVBytes = kHalves * kTok * 128;  // K or V of one tile: [half][token][128 B]
+    static constexpr int kStageBytes = 2 * kKVBytes;
+    static constexpr int kPBytes = kRows * kTok * 2;       // [row][64 tokens] bf16
+    static constexpr int q = 0;
+    static constexpr int ring = q + kQBytes;
+    static constexpr int p = ring + NS * kStageBytes;
+    static constexpr int scan = p + 2 * kPBytes;           // cum[kMaxGroups + 1], tiles[kMaxGroups]
+    static constexpr int ids = scan + ((2 * kMaxGroups + 1) * 4 + 7) / 8 * 8;
+    static constexpr int bars = ids + kIdCache * 4;
+    static constexpr int kBars = 2 * NS + 8;               // kv_full, kv_empty, s_full2, p_full2, o_done2, ready, fin
+    static constexpr int misc = bars + kBars * 8;          // TMEM address, scan scratch (8 ints + carry)
+    static constexpr int total = misc + 64 + 1024;         // + alignment slack
+};
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    // start >> 4 | LBO >> 4 << 16 | SBO >> 4 << 32 | version 1 << 46 | 128-byte swizzle (2) << 61
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16 instruction descriptor: bf16 A and B, fp32 D, M = 128.
+__host__ __device__ constexpr uint32_t instr_desc(int n, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// One context of the tile list: group g, context c of the group (member
+// chunk c / Hkv, kv head c % Hkv), tiles [start, start + n).
+struct Cursor {
+    int g, c, n, contexts;
+    int64_t start;
+    // largest group with cum[g] <= t (t < cum[num_groups])
+    __device__ __forceinline__ void seek(const int *cum, const int *tiles, int num_groups, int64_t t) {
+        int lo = 0, hi = num_groups;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cum[mid] <= t) lo = mid; else hi = mid;
+        }
+        g = lo;
+        n = tiles[g];
+        contexts = (cum[g + 1] - cum[g]) / n;
+        c = (int)((t - cum[g]) / n);
+        start = cum[g] + (int64_t)c * n;
+    }
+    __device__ __forceinline__ void next(const int *cum, const int *tiles) {
+        start += n;
+        if (++c == contexts) {
+            do { ++g; } while (cum[g + 1] == cum[g]);
+            n = tiles[g];
+            contexts = (cum[g + 1] - cum[g]) / n;
+            c = 0;
+            start = cum[g];
+        }
+    }
+};
+}  // namespace tc
+
+template <int D, int NS>
+__global__ void __launch_bounds__(tc::kThreads, 1)
+decode_bf16_prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
+                             const int32_t *__restrict__ group_offsets,
+                             const int32_t *__restrict__ prefix_lens, int num_groups) {
+    using L = tc::Layout<D, NS>;
+    constexpr int H = L::kHalves;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    int *cum = reinterpret_cast<int *>(smem + L::scan);
+    int *tiles = cum + tc::kMaxGroups + 1;
+    uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + L::bars);
+    uint64_t *kv_empty = kv_full + NS;
+    uint64_t *s_full = kv_empty + NS;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2;
+    uint64_t *ready = o_done + 2;
+    uint64_t *fin = ready + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
+    int *warp_sums = reinterpret_cast<int *>(smem + L::misc + 16);  // one per warp + carry
+    int *idc = reinterpret_cast<int *>(smem + L::ids);
+    constexpr int kCarry = tc::kThreads / 32;
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.num_seqs, Hkv = a.num_kv_heads, G = a.group, B = a.block_size;
+    const int cap = min(a.max_seq_len, a.max_blocks * B);
+    const int align = B > kTile ? B : kTile;
+    const int mpc = tc::kRows / G;  // members per chunk
+
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0 && (group_offsets[0] != 0 || group_offsets[num_groups] != S))
+            flag_error(a.err, PKV_DEVERR_PREFIX);
+        for (int i = threadIdx.x; i < S; i += blockDim.x) a.seq_tok0[i] = 0;
+    }
+    if (threadIdx.x == 0) {
+        cum[0] = 0;
+        warp_sums[kCarry] = 0;
+    }
+    __syncthreads();
+
+    // per group: the prefix actually attended (cut to the shortest member,
+    // minus the appended token, and to whole tiles), then a scan of the
+    // groups' tiles over all their contexts
+    for (int base = 0; base < num_groups; base += tc::kThreads) {
+        const int g = base + threadIdx.x;
+        int v = 0;
+        if (g < num_groups) {
+            int m0 = group_offsets[g], m1 = group_offsets[g + 1];
+            if (m0 < 0 || m1 > S || m1 < m0) {
+                if (blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+                m0 = m1 = 0;
+            }
+            const int raw = prefix_lens[g];
+            if (raw % align != 0 && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+            int mn = cap;
+            for (int i = m0; i < m1; ++i) mn = min(mn, clamp_len(a.seq_lens[i], cap));
+            int pre = min(raw < 0 ? 0 : raw, mn - (a.k_new ? 1 : 0));
+            pre = m1 > m0 && pre > 0 ? pre / tc::kTok * tc::kTok : 0;
+            if (blockIdx.x == 0)
+                for (int i = m0; i < m1; ++i) a.seq_tok0[i] = pre;
+            tiles[g] = pre / tc::kTok;
+            v = tiles[g] * ((m1 - m0 + mpc - 1) / mpc) * Hkv;
+        }
+        int x = v;
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, sh);
+            if (lane >= sh) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        int before = warp_sums[kCarry];
+        for (int w = 0; w < warp; ++w) before += warp_sums[w];
+        if (g < num_groups) cum[g + 1] = before + x;
+        __syncthreads();
+        if (threadIdx.x == tc::kThreads - 1) warp_sums[kCarry] = before + x;
+        __syncthreads();
+    }
+    const int64_t T = cum[num_groups];
+    const int64_t parts = min((int64_t)gridDim.x, max((int64_t)1, T / tc::kMinTiles));
+    if (T == 0 || blockIdx.x >= parts) return;  // before any TMEM is taken
+    const int64_t s0 = (int64_t)blockIdx.x * T / parts, s1 = ((int64_t)blockIdx.x + 1) * T / parts;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(ready, 4);
+        mbar_init(fin, 1);
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(tc::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const uint32_t q_s = smem_u32(smem + L::q);
+    const uint32_t ring_s = smem_u32(smem + L::ring);
+    const uint32_t p_s = smem_u32(smem + L::p);
+
+    if (warp == 4) {
+        // ---------------- producer ----------------
+        tc::Cursor cur;
+        cur.seek(cum, tiles, num_groups, s0);
+        int64_t j = 0, issued = 0;
+        bool dead = false;
+        const int boxh = B < kTile ? B : kTile;
+        const int bpt = tc::kTok / B;  // blocks per tile
+        for (int64_t t = s0; t < s1;) {
+            const int64_t t1 = min(s1, cur.start + cur.n);
+            const int i0 = (int)(t - cur.start), i1 = (int)(t1 - cur.start);
+            const int kvh = cur.c % Hkv;
+            const int32_t *bt = a.block_tables + (int64_t)group_offsets[cur.g] * a.max_blocks;
+            for (int cb = i0 * bpt; cb < i1 * bpt; cb += tc::kIdCache) {
+                const int nb = min(tc::kIdCache, i1 * bpt - cb);
+                __syncwarp();  // the previous chunk has been issued
+                for (int k0 = 0; k0 < nb; k0 += 128) {
+                    int v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int k = k0 + u * 32 + lane;
+                        v[u] = k < nb ? bt[cb + k] : 0;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (k0 + u * 32 + lane < nb) idc[k0 + u * 32 + lane] = v[u];
+                }
+                __syncwarp();
+                // one tile per step: lane 0 claims the stage, then lane i issues box i
+                // (sub-block i / (2H), half (i / 2) % H, K or V by i % 2)
+                for (int tl = 0; tl < nb / bpt; ++tl, ++j) {
+                    const int st = (int)(j % NS);
+                    if (lane == 0 && !dead && j >= NS &&
+                        !mbar_wait_bounded(&kv_empty[st], (uint32_t)(((j / NS) - 1) & 1))) {
+                        flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                        dead = true;
+                    }
+                    dead = __shfl_sync(0xffffffffu, dead, 0);
+                    if (dead) continue;
+                    ++issued;
+                    if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)L::kStageBytes);
+                    __syncwarp();
+                    const int nbox = (tc::kTok / boxh) * 2 * H;
+                    for (int bi = lane; bi < nbox; bi += 32) {
+                        const int sb = bi / (2 * H), h = (bi >> 1) % H;
+                        const int tok = sb * boxh;  // within the tile
+                        int blk = idc[tl * bpt + tok / B];
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                            blk = 0;
+                        }
+                        const int y = (int)(((int64_t)blk * Hkv + kvh) * B + tok % B);
+                        const uint32_t dst = ring_s + st * L::kStageBytes + (bi & 1) * L::kKVBytes +
+                                             h * (tc::kTok * 128) + sb * boxh * 128;
+                        tma_load_2d(dst, (bi & 1) ? &tm_v : &tm_k, smem_u32(&kv_full[st]), h * 64, y);
+                    }
+                }
+            }
+            t = t1;
+            if (t < s1) cur.next(cum, tiles);
+        }
+        // copies still in flight (only after a timeout) land before the CTA exits
+        if (lane == 0)
+            for (int64_t k = max((int64_t)0, issued - NS); k < issued; ++k)
+                mbar_wait_bounded(&kv_full[k % NS], (uint32_t)((k / NS) & 1));
+    } else if (warp == 6) {
+        // ---------------- members' block tables ----------------
+        // the kv head 0 contexts cover every prefix block of every member once
+        tc::Cursor cur;
+        cur.seek(cum, tiles, num_groups, s0);
+        const int bpt = tc::kTok / B;
+        bool bad = false;
+        for (int64_t t = s0; t < s1;) {
+            const int64_t t1 = min(s1, cur.start + cur.n);
+            if (cur.c % Hkv == 0) {
+                const int i0 = (int)(t - cur.start), i1 = (int)(t1 - cur.start);
+                const int chunk = cur.c / Hkv;
+                const int m0 = group_offsets[cur.g], m1 = group_offsets[cur.g + 1];
+                const int c0 = m0 + chunk * mpc, c1 = min(m1, c0 + mpc);
+                const int32_t *bt = a.block_tables + (int64_t)m0 * a.max_blocks;
+                const int lb0 = i0 * bpt, nb = (i1 - i0) * bpt;
+                const int total = (c1 - c0) * nb;
+                for (int k0 = 0; k0 < total; k0 += 128) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int k = k0 + u * 32 + lane;
+                        if (k < total) {
+                            const int m = c0 + k / nb, lb = lb0 + k % nb;
+                            if (m != m0 && a.block_tables[(int64_t)m * a.max_blocks + lb] != bt[lb]) bad = true;
+                        }
+                    }
+                }
+            }
+            t = t1;
+            if (t < s1) cur.next(cum, tiles);
+        }
+        if (bad) flag_error(a.err, PKV_DEVERR_PREFIX);
+    } else if (warp == 5) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc::instr_desc(tc::kTok, false);
+            constexpr uint32_t idesc_pv = tc::instr_desc(D, true);
+            tc::Cursor cur;
+            cur.seek(cum, tiles, num_groups, s0);
+            int64_t j = 0, piece = 0;
+            bool dead = false;
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                if (!dead && !mbar_wait_bounded(bar, parity)) {
+                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                    dead = true;
+                }
+                tc::fence_after();
+            };
+            auto pv = [&](int64_t jj, bool first, uint32_t ob) {
+                const int b = (int)(jj & 1), st = (int)(jj % NS);
+                wait(&p_full[b], (uint32_t)((jj >> 1) & 1));
+                const uint32_t pb = p_s + b * L::kPBytes;
+                const uint32_t vb = ring_s + st * L::kStageBytes + L::kKVBytes;
+                if (!dead) {
+#pragma unroll
+                    for (int k = 0; k < tc::kTok / 16; ++k)
+                        tc::mma(tmem + ob, tc::smem_desc(pb + k * 32, 16, 1024),
+                                tc::smem_desc(vb + k * 2048, tc::kTok * 128, 1024), idesc_pv,
+                                (first && k == 0) ? 0u : 1u);
+                }
+                tc::commit(&o_done[b]);
+                tc::commit(&kv_empty[st]);
+            };
+            for (int64_t t = s0; t < s1;) {
+                const int64_t t1 = min(s1, cur.start + cur.n);
+                const int nt = (int)(t1 - t);
+                wait(ready, (uint32_t)(piece & 1));
+                const uint32_t ob = 128 + (uint32_t)(piece & 1) * 128;
+                for (int i = 0; i < nt; ++i, ++j) {
+                    const int st = (int)(j % NS), b = (int)(j & 1);
+                    wait(&kv_full[st], (uint32_t)((j / NS) & 1));
+                    const uint32_t kb = ring_s + st * L::kStageBytes;
+                    if (!dead) {
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k)
+                            tc::mma(tmem + b * tc::kTok,
+                                    tc::smem_desc(q_s + (k >> 2) * (tc::kRows * 128) + (k & 3) * 32, 16, 1024),
+                                    tc::smem_desc(kb + (k >> 2) * (tc::kTok * 128) + (k & 3) * 32, 16, 1024),
+                                    idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                    tc::commit(&s_full[b]);
+                    if (i > 0) pv(j - 1, i == 1, ob);
+                }
+                pv(j - 1, nt == 1, ob);
+                ++piece;
+                t = t1;
+                if (t < s1) cur.next(cum, tiles);
+            }
+            // every MMA has completed before the TMEM is freed
+            tc::commit(fin);
+            mbar_wait_bounded(fin, 0u);
+        }
+    } else if (warp < 4) {
+        // ---------------- softmax (warps 0-3: rows 32w .. 32w+31) ----------------
+        const int r = warp * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        tc::Cursor cur;
+        cur.seek(cum, tiles, num_groups, s0);
+        int64_t j = 0, piece = 0;
+        bool dead = false;
+        auto wait = [&](uint64_t *bar, uint32_t parity) {
+            if (!dead && !mbar_wait_bounded(bar, parity)) {
+                flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                dead = true;
+            }
+            tc::fence_after();
+        };
+        // this thread's query row of the context at cursor c into Q (128-byte
+        // swizzled, K-major; zero past the context's rows), copied asynchronously
+        auto copy_q = [&](const tc::Cursor &c) {
+            const int kvh = c.c % Hkv, chunk = c.c / Hkv;
+            const int m0 = group_offsets[c.g], m1 = group_offsets[c.g + 1];
+            const int c0 = m0 + chunk * mpc, rows = (min(m1, c0 + mpc) - c0) * G;
+            const __nv_bfloat16 *src =
+                static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)(c0 + r / G) * a.num_heads + kvh * G + r % G) * D;
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) {
+                const uint32_t dst = q_s + (k >> 3) * (tc::kRows * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
+                if (r < rows)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k * 8) : "memory");
+                else
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto q_ready = [&]() {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            fence_proxy_async();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ready);
+        };
+        copy_q(cur);
+        q_ready();
+        for (int64_t t = s0; t < s1;) {
+            const int64_t t1 = min(s1, cur.start + cur.n);
+            const int nt = (int)(t1 - t);
+            const int kvh = cur.c % Hkv, chunk = cur.c / Hkv;
+            const int m0 = group_offsets[cur.g], m1 = group_offsets[cur.g + 1];
+            const int c0 = m0 + chunk * mpc, c1 = min(m1, c0 + mpc);
+            const int rows = (c1 - c0) * G;
+            const bool live = warp * 32 < rows;
+            const int seq = c0 + (r < rows ? r / G : 0), head = kvh * G + r % G;
+            const uint32_t ob = 128 + (uint32_t)(piece & 1) * 128;  // this piece's O in TMEM
+            tc::Cursor nx = cur;
+            if (t1 < s1) nx.next(cum, tiles);
+
+            float m_run = -INFINITY, l = 0.f;
+            for (int i = 0; i < nt; ++i, ++j) {
+                const int b = (int)(j & 1);
+                wait(&s_full[b], (uint32_t)((j >> 1) & 1));
+                // every Q K^T of this piece has completed: Q may take the next piece's rows
+                if (i == nt - 1 && t1 < s1) copy_q(nx);
+                if (live) {
+                    float s[64];
+                    tc::ld32(trow + b * tc::kTok, s);
+                    tc::ld32(trow + b * tc::kTok + 32, s + 32);
+                    tc::wait_ld();
+                    float mt = -INFINITY;
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) {
+                        s[k] *= a.scale_log2;
+                        mt = fmaxf(mt, s[k]);
+                    }
+                    const float m_new = i == 0 ? mt : (mt > m_run + tc::kRescale ? mt : m_run);
+                    const bool move = i > 0 && m_new != m_run;
+                    if (__any_sync(0xffffffffu, move)) {
+                        // O must hold P V of the previous tile before it is rescaled
+                        wait(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
+                        const float alpha = move ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            tc::ld32(trow + ob + c * 32, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                            tc::st32(trow + ob + c * 32, o);
+                        }
+                        tc::wait_st();
+                        l *= alpha;
+                    }
+                    m_run = m_new;
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        pk[k] = pack_bf16x2(exp2f(s[2 * k] - m_run), exp2f(s[2 * k + 1] - m_run));
+                        l += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
+                    }
+                    // P buffer b was last read by the P V of tile j - 2
+                    if (i >= 2) wait(&o_done[b], (uint32_t)(((j - 2) >> 1) & 1));
+                    const uint32_t prow = p_s + b * L::kPBytes + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((c ^ (r & 7)) << 4)),
+                                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
+                                     : "memory");
+                }
+                fence_proxy_async();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
+            }
+            // the next piece's MMAs may start while this one's O is read out
+            if (t1 < s1) q_ready();
+            // the piece's partial: unnormalised O row, running max, sum
+            wait(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
+            if (live) {
+                const int64_t first = share_owner(cur.start, T, parts);
+                const int slot = a.prefix_slot + (int)(share_owner(t, T, parts) - first);
+                const int64_t prow = (int64_t)seq * a.num_heads + head;
+                float *dst = a.part_o + (prow * a.max_parts + slot) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tc::ld32(trow + ob + c * 32, o);
+                    tc::wait_ld();
+                    if (r < rows) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 4)
+                            *reinterpret_cast<float4 *>(dst + c * 32 + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+                    }
+                }
+                if (r < rows) {
+                    a.part_m[prow * a.max_parts + slot] = dead ? -INFINITY : m_run;
+                    a.part_l[prow * a.max_parts + slot] = dead ? 0.f : l;
+                    if (t == cur.start && r % G == 0)
+                        a.prefix_pieces[(int64_t)seq * Hkv + kvh] =
+                            (int)(share_owner(cur.start + cur.n - 1, T, parts) - first + 1);
+                }
+            }
+            ++piece;
+            t = t1;
+            cur = nx;
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tc::kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
 // CUDA-core kernel (fp32 I/O; also instantiated for bf16 storage)
 // ---------------------------------------------------------------------------
 template <typename T, int D, int NW>
@@ -1321,16 +1914,16 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     const float *pm = a.part_m + row * a.max_parts;
     const float *pl = a.part_l + row * a.max_parts;
     const float *po = a.part_o + row * a.max_parts * D + lane * E;
-    // issue the length, the piece count and the first 32 (max, sum) pairs at
+    // issue the length, the piece counts and the first 32 (max, sum) pairs at
     // once; pairs past the piece count are masked below
     const int raw_len = a.seq_lens[seq];
-    int nparts = 0, tok0 = 0;
+    int nparts = 0, tok0 = 0, npre_given = -1;
     if (PIECES) {
         const int h = (int)(row - (int64_t)seq * a.num_heads);
         nparts = a.pieces[(int64_t)seq * a.num_kv_heads + h / a.group];
         if (a.seq_tok0) tok0 = a.seq_tok0[seq];
+        if (a.prefix_pieces) npre_given = a.prefix_pieces[(int64_t)seq * a.num_kv_heads + h / a.group];
     }
-    // speculative (max, sum) of the first 32 own pieces; masked below
     float mj = -INFINITY, lj = 0.f;
     if (lane < a.max_parts) {
         mj = pm[lane];
@@ -1347,9 +1940,11 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
         }
         tok0 = min(max(tok0, 0), len);
         if (tok0 > 0) {
-            npre = (tok0 + a.prefix_part - 1) / a.prefix_part;
+            npre = npre_given >= 0 ? npre_given : (tok0 + a.prefix_part - 1) / a.prefix_part;
+            npre = min(max(npre, 0), a.max_parts - a.prefix_slot);
             if (len == tok0) nparts = 0;  // nothing of its own: no piece was written
         }
+        nparts = min(max(nparts, 0), a.seq_tok0 ? a.prefix_slot : a.max_parts);
     } else {
         nparts = (len + a.partition_size - 1) / a.partition_size;
     }
@@ -1762,11 +2357,34 @@ PKV_API pkv_status paged_attention_decode_append(
 // ---------------------------------------------------------------------------
 static int64_t prefix_slots(int max_seq_len) { return ((int64_t)max_seq_len + kPrefixPart - 1) / kPrefixPart; }
 
-static WorkspaceLayout grouped_layout(int64_t S, int64_t Hq, int64_t D, int max_seq_len, size_t *tok0_off) {
-    WorkspaceLayout w = workspace_layout(S, Hq, D, balanced_slots(max_seq_len) + prefix_slots(max_seq_len), true);
+// Prefix partial slots: a prefix of L tokens spans at most ceil(L / 256) + 1
+// shares of the tensor-core prefix kernel (shares hold >= 256 tokens), and
+// ceil(L / 256) partitions of the other prefix kernel.
+static WorkspaceLayout grouped_layout(int64_t S, int64_t Hq, int64_t D, int max_seq_len, size_t *tok0_off,
+                                      size_t *npre_off) {
+    WorkspaceLayout w =
+        workspace_layout(S, Hq, D, balanced_slots(max_seq_len) + prefix_slots(max_seq_len) + 1, true);
     *tok0_off = w.total;
     w.total += round256((size_t)(S * 4));
+    *npre_off = w.total;
+    w.total += round256((size_t)(S * Hq * 4));
     return w;
+}
+
+template <int D>
+static pkv_status launch_prefix_tc(const DecodeArgs &a, const int32_t *group_offsets, const int32_t *prefix_lens,
+                                   int num_groups, cudaStream_t st) {
+    constexpr int NS = D == 128 ? 4 : 8;
+    constexpr int smem = tc::Layout<D, NS>::total;
+    static bool done[128] = {};
+    auto kern = decode_bf16_prefix_tc_kernel<D, NS>;
+    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    return launch_pdl(kern, dim3((unsigned)sms), dim3(tc::kThreads), smem, st, mk, mv, a, group_offsets,
+                      prefix_lens, num_groups);
 }
 
 template <int D>
@@ -1787,8 +2405,8 @@ static pkv_status launch_prefix(const DecodeArgs &a, const int32_t *group_offset
 PKV_API size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim,
                                                       int max_seq_len) {
     if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
-    size_t tok0_off = 0;
-    return grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off).total;
+    size_t tok0_off = 0, npre_off = 0;
+    return grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off, &npre_off).total;
 }
 
 PKV_API pkv_status paged_attention_decode_grouped(
@@ -1818,8 +2436,8 @@ PKV_API pkv_status paged_attention_decode_grouped(
     if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
         return PKV_ERR_UNSUPPORTED;
     if (prefix_slots(max_seq_len) > 65535) return PKV_ERR_INVALID;
-    size_t tok0_off = 0;
-    const WorkspaceLayout lay = grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off);
+    size_t tok0_off = 0, npre_off = 0;
+    const WorkspaceLayout lay = grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off, &npre_off);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PKV_ERR_INVALID;
 
@@ -1852,13 +2470,24 @@ PKV_API pkv_status paged_attention_decode_grouped(
     a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
     a.pieces = reinterpret_cast<int *>(ws + lay.pieces_off);
     a.seq_tok0 = reinterpret_cast<int *>(ws + tok0_off);
-    a.max_parts = (int)(balanced_slots(max_seq_len) + prefix_slots(max_seq_len));
+    a.max_parts = (int)(balanced_slots(max_seq_len) + prefix_slots(max_seq_len) + 1);
     a.prefix_slot = (int)balanced_slots(max_seq_len);
     a.prefix_part = kPrefixPart;
 
+    // shared prefixes: tensor-core kernel (groups scanned in shared memory),
+    // else one CTA per (group, kv head, 256 tokens) on mma.sync;
+    // PKV_PREFIX_VARIANT=1 selects the latter for comparisons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    pkv_status rc = head_dim == 128 ? launch_prefix<128>(a, group_offsets, prefix_lens, num_groups, st)
-                                    : launch_prefix<64>(a, group_offsets, prefix_lens, num_groups, st);
+    const bool use_tc = num_groups <= tc::kMaxGroups && env_variant("PKV_PREFIX_VARIANT") != 1;
+    pkv_status rc;
+    if (use_tc) {
+        a.prefix_pieces = reinterpret_cast<int *>(ws + npre_off);
+        rc = head_dim == 128 ? launch_prefix_tc<128>(a, group_offsets, prefix_lens, num_groups, st)
+                             : launch_prefix_tc<64>(a, group_offsets, prefix_lens, num_groups, st);
+    } else {
+        rc = head_dim == 128 ? launch_prefix<128>(a, group_offsets, prefix_lens, num_groups, st)
+                             : launch_prefix<64>(a, group_offsets, prefix_lens, num_groups, st);
+    }
     if (rc == PKV_OK) rc = head_dim == 128 ? dispatch_balanced<128>(a, st) : dispatch_balanced<64>(a, st);
     if (rc == PKV_OK)
         rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, true>(a, st)
