@@ -197,14 +197,15 @@ def algorithmic_decode_bytes(lens, shape) -> int:
 class Batch:
     """One resident decode batch: pool, allocator, tables and step inputs."""
 
-    def __init__(self, pkv, shape, lens, seed, device, partition_size):
+    def __init__(self, pkv, shape, lens, seed, device, partition_size, reserve_tokens=0):
         B = shape.block_size
         self.shape = shape
         self.device = device
         self.lens = [int(x) for x in lens]
         S = len(self.lens)
         need = sum(-(-L // B) for L in self.lens)
-        self.num_blocks = max(1, math.ceil(1.1 * need)) + 2 * S
+        # +10% and room for `reserve_tokens` more tokens per sequence; at least 64 blocks
+        self.num_blocks = max(64, math.ceil(1.1 * need) + S * (2 + -(-reserve_tokens // B)))
         self.alloc = pkv.BlockAllocator(self.num_blocks, B)
         # hand blocks out in a random order, as after a long run of frees
         order = wl.draw_block_ids(self.num_blocks, seed)
@@ -256,7 +257,7 @@ class Batch:
         self.pkv = pkv
 
     @classmethod
-    def beam(cls, pkv, shape, seed, device, partition_size, shared):
+    def beam(cls, pkv, shape, seed, device, partition_size, shared, reserve_tokens=0):
         """Beam search: prompts of `shared` tokens, each forked into a beam
         group that shares the prompt's blocks; every beam then produced its own
         0-256 tokens (copy-on-write where a shared block was partially filled),
@@ -267,8 +268,9 @@ class Batch:
         div = wl.draw_divergent_lengths(P_ * W, seed)
         self.shape, self.device = shape, device
         self.lens = [shared + int(d) + 1 for d in div]  # after this step's token
-        # room for the appended tokens of the e2e loop too (8 blocks per beam)
-        self.num_blocks = P_ * (-(-shared // B) + 1) + sum(-(-int(d) // B) + 10 for d in div) + 64
+        # room for `reserve_tokens` appended tokens per beam (the e2e loop)
+        self.num_blocks = (P_ * (-(-shared // B) + 1) + sum(-(-int(d) // B) + 2 for d in div) + 64
+                           + P_ * W * -(-reserve_tokens // B))
         self.alloc = pkv.BlockAllocator(self.num_blocks, B)
         order = wl.draw_block_ids(self.num_blocks, seed)
         for i in range(self.num_blocks):
@@ -551,11 +553,12 @@ def run_ours(args):
     return 0
 
 
-def make_batch(pkv, shape, args, seed, device):
+def make_batch(pkv, shape, args, seed, device, reserve_tokens=0):
     if args.workload.startswith("beam"):
         shared = wl.BEAM_SHARED_PARTIAL if args.workload == "beam1032" else wl.BEAM_SHARED
-        return Batch.beam(pkv, shape, seed, device, args.partition_size, shared)
-    return Batch(pkv, shape, wl.draw_lengths(shape, seed).tolist(), seed, device, args.partition_size)
+        return Batch.beam(pkv, shape, seed, device, args.partition_size, shared, reserve_tokens)
+    return Batch(pkv, shape, wl.draw_lengths(shape, seed).tolist(), seed, device, args.partition_size,
+                 reserve_tokens)
 
 
 def context_lengths(args, shape, seed):
@@ -571,9 +574,9 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     """The step through the public API with host buffers: the allocator appends
     a token for every sequence on the host, the step's inputs go H2D from
     pinned memory, the kernels run, the output comes back D2H."""
-    b = make_batch(pkv, shape, args, seed + 77, device)
-    S = len(b.lens)
     steps = args.steps
+    b = make_batch(pkv, shape, args, seed + 77, device, reserve_tokens=steps + args.warmup + 1)
+    S = len(b.lens)
     h_q = b.q.cpu().pin_memory()
     h_k = b.k_new.cpu().pin_memory()
     h_v = b.v_new.cpu().pin_memory()

@@ -240,12 +240,18 @@ PKV_EXPORT pkv_status paged_attention_decode_append(void *out, const void *q, co
  *                  in paged_attention_decode_append
  *   workspace      at least paged_attention_grouped_workspace_size() bytes,
  *                  256-byte aligned, no initialisation needed
- * The shared part of each group is attended by one CTA per (group, kv head,
- * 256 tokens), one warp per member, reading each tile once; each member's own
- * tokens go through the balanced kernel; a merge kernel joins the two.
- * A bad group description flags PKV_DEVERR_PREFIX; a member whose prefix
- * blocks differ from the first member's has those blocks left out and flags
- * PKV_DEVERR_PREFIX.  bf16 only, num_seqs <= 8192 (else PKV_ERR_UNSUPPORTED).
+ * The shared part of each group, cut to whole 64-token tiles, is one dense
+ * contraction per kv head (members x query heads rows against each tile) and
+ * runs on the tensor cores (tcgen05, accumulators in tensor memory), each
+ * tile read once; each member's own tokens go through the balanced kernel; a
+ * merge kernel joins the two.  With more than 2048 groups the shared part
+ * runs on a kernel with one CTA per (group, kv head, 256 tokens) instead.
+ * A bad group description (offsets out of order or not covering 0..num_seqs,
+ * a prefix length that is not a multiple of max(16, block_size)) flags
+ * PKV_DEVERR_PREFIX.  A member whose prefix blocks differ from the first
+ * member's also flags PKV_DEVERR_PREFIX; that member's result is then
+ * unspecified (finite).  bf16 only, num_seqs <= 8192 (else
+ * PKV_ERR_UNSUPPORTED).
  */
 PKV_EXPORT size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim,
                                               int max_seq_len);

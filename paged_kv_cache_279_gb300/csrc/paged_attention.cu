@@ -589,6 +589,7 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 constexpr int kMinTilesPerCta = 16;  // >= 256 tokens per share: bounds pieces per segment
 
 constexpr int kYCache = 768;  // tiles of a share whose TMA rows are staged in shared memory
+constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended last
 
 // Shared-memory layout of the balanced kernel (host and device agree on it).
 // Offsets are from the 1024-aligned base.
@@ -830,21 +831,45 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int64_t cta_lo = gw0 * T / parts;
     const int64_t cta_hi = (gw0 + NW < parts ? gw0 + NW : parts) * T / parts;
 
-    // The first piece's queries: fetched now, used after the staging below.
+    // Walk order.  Tiles [lo, hi) are attended from r to hi, then from lo to
+    // r.  Normally r = lo; but a warp whose share starts with a short piece
+    // (the tail of a segment begun by the previous warp) takes that piece
+    // last (r = its end): storing a partial early, while every warp's first
+    // tile loads are queued, stalls the warp for many microseconds.  Only when
+    // every tile of the CTA has its rows staged (no cursor walks past them).
     const int64_t gw = gw0 + warp;
     const int64_t lo = gw * T / parts, hi = (gw + 1) * T / parts;
+    const int ncache = (int)(cta_hi - cta_lo < kYCache ? cta_hi - cta_lo : kYCache);
+    SegCursor seg_lo;  // segment of tile lo
+    int64_t r = lo;
     SegCursor seg;  // the segment being attended
     uint32_t qb[D / 16][2], qn[D / 16][2];
+    bool qn_loaded = false;  // qn holds the second piece's queries
+    // The queries of the first two pieces: fetched now, ahead of the burst of
+    // tile loads that every warp issues after the staging below.
     if (gw < parts) {
-        seg.seek(prefix, S, Hkv, lo);
+        seg_lo.seek(prefix, S, Hkv, lo);
+        const int64_t first_end = seg_lo.seg_start + seg_lo.n;
+        if (first_end < hi && first_end - lo < kRotateTiles && ncache == cta_hi - cta_lo) r = first_end;
+        seg = seg_lo;
+        if (r != lo) seg.advance_to(prefix, Hkv, r);
         load_q_fragments<D>(a, seg.seq, seg.kvh, lane, qb);
+        const int64_t end1 = seg.seg_start + seg.n;  // the first piece ends at min(hi, end1)
+        if (end1 < hi || r != lo) {
+            SegCursor second = seg_lo;
+            if (end1 < hi) {
+                second = seg;
+                second.advance_to(prefix, Hkv, end1);
+            }
+            load_q_fragments<D>(a, second.seq, second.kvh, lane, qn);
+            qn_loaded = true;
+        }
     }
 
     // Stage the TMA rows and valid-row masks of the CTA's first tiles, so that
     // neither issuing nor attending a tile waits on a global load.  Each thread
     // handles up to kPer tiles and issues all their loads (lengths and block
     // ids, read speculatively and masked afterwards) before using any.
-    const int ncache = (int)(cta_hi - cta_lo < kYCache ? cta_hi - cta_lo : kYCache);
     {
         constexpr int kPer = (kYCache + NW * 32 - 1) / (NW * 32);
         const int B = a.block_size;
@@ -922,7 +947,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of one K (or V) row
         constexpr int kBatch = 4;
         const int part = lane / kChunks, ch = lane % kChunks;  // lanes past 2*kChunks idle
-        SegCursor c = seg;
+        SegCursor c = seg_lo;
         bool more = true;
         while (more) {
             int64_t src_row[kBatch], dst_row[kBatch];
@@ -980,10 +1005,13 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                          grouped ? toff[c.seq] : 0);
     };
 
-    SegCursor prod;  // lane 0: segment of the tile being issued (needed past the cache)
+    // k-th tile in walk order
+    const int64_t run1 = hi - r;
+    auto tile_at = [&](int k) -> int64_t { return k < run1 ? r + k : lo + (k - run1); };
+    SegCursor prod;  // lane 0: segment of the tile being issued (needed past the cache; r == lo then)
     if (lane == 0) prod.seek(prefix, S, Hkv, lo);
     auto issue = [&](int k, int buf) {
-        const int64_t t = lo + k;
+        const int64_t t = tile_at(k);
         if (t - cta_lo >= ncache) prod.advance_to(prefix, Hkv, t);
         issue_rows<D>(&tm_k, &tm_v, ring + buf * Lay::kStageBytes, &bars[buf], boxh, rows_of(t, prod));
     };
@@ -995,25 +1023,30 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     bool dead = false;
     WarpAcc<D> acc;
     for (;;) {
-        const int64_t pa = lo + k;  // this piece: tiles [pa, pb)
+        const int64_t pa = tile_at(k);  // this piece: tiles [pa, pb), walk positions [k, kend)
         const int64_t seg_end = seg.seg_start + seg.n;
-        const int64_t pb = hi < seg_end ? hi : seg_end;
+        const int64_t run_end = k < run1 ? hi : r;
+        const int64_t pb = run_end < seg_end ? run_end : seg_end;
+        const int kend = k + (int)(pb - pa);
         SegCursor nxt = seg;
-        if (pb < hi) {  // fetch the next piece's queries while this one runs
-            nxt.advance_to(prefix, Hkv, pb);
-            load_q_fragments<D>(a, nxt.seq, nxt.kvh, lane, qn);
+        if (kend < ntiles) {  // fetch the next piece's queries while this one runs
+            const int64_t tn = tile_at(kend);
+            if (tn == pb) nxt.advance_to(prefix, Hkv, tn);
+            else nxt = seg_lo;  // the walk wraps to lo
+            if (!qn_loaded) load_q_fragments<D>(a, nxt.seq, nxt.kvh, lane, qn);
+            qn_loaded = false;
         }
         acc.reset();
-        for (; lo + k < pb; ++k) {
+        for (; k < kend; ++k) {
             const int buf = k % NS;
             if (!dead && !mbar_wait_bounded(&bars[buf], (uint32_t)((k / NS) & 1))) {
                 if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
                 dead = true;
             }
             if (dead) continue;
-            const TileRows r = rows_of(lo + k, seg);
+            const TileRows rw = rows_of(tile_at(k), seg);
             unsigned char *sk = ring + buf * Lay::kStageBytes;
-            attend_tile<D>(sk, sk + Lay::kKVBytes, r.mask, qb, a.scale_log2, acc, lane);
+            attend_tile<D>(sk, sk + Lay::kKVBytes, rw.mask, qb, a.scale_log2, acc, lane);
             __syncwarp();
             if (lane == 0 && k + NS < ntiles) {
                 fence_proxy_async();
@@ -1029,7 +1062,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int64_t w1 = share_owner(seg_end - 1, T, parts);
             a.pieces[(int64_t)seg.seq * a.num_kv_heads + seg.kvh] = (int)(w1 - w0 + 1);
         }
-        if (pb >= hi) break;
+        if (kend >= ntiles) break;
         seg = nxt;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {

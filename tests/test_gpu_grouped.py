@@ -97,3 +97,38 @@ def test_bad_group_description_is_flagged_not_faulted():
     pre = np.array([250, 256], dtype=np.int32)        # not a whole number of tiles
     grouped(case, shape, q, offs, pre, int(case["lens"].max()))
     assert pkv.read_device_errors() & pkv.DEVERR_PREFIX
+
+
+@pytest.mark.parametrize("D,B,Hq,Hkv,prompts,width,shared", [
+    (64, 8, 16, 4, 3, 5, 256),     # head_dim 64, 8-token blocks (8 TMA boxes per 64-token tile)
+    (128, 32, 8, 8, 2, 40, 320),   # one query head per kv head, 32-token blocks
+    (128, 16, 32, 4, 1, 20, 200),  # 20 members x 8 heads = 160 rows: two row chunks
+    (128, 8, 8, 8, 1, 150, 128),   # 150 members x 1 head: chunks of 128 and 22 rows
+])
+def test_grouped_shapes_match_oracle(D, B, Hq, Hkv, prompts, width, shared):
+    shape = wl.DecodeShape("grouped_shape", 0, Hq, Hkv, D, B, torch.bfloat16)
+    div = np.random.default_rng(D + B + width).integers(0, 41, prompts * width)
+    case = build_beam_pool(shape, shared, prompts, width, div, seed=17)
+    offs, pre = case["alloc"].prefix_groups(case["seqs"])
+    assert len(pre) == prompts and (pre > 0).all()
+    q = wl.draw_query(shape, 18, num_seqs=prompts * width).cuda()
+    out = grouped(case, shape, q, offs, pre, int(case["lens"].max()))
+    ref = oracle.decode_attention(q.float().cpu().numpy(), [k.float().numpy() for k in case["ks"]],
+                                  [v.float().numpy() for v in case["vs"]], shape.scale)
+    assert_bf16_close(out, ref, f"grouped D={D} B={B} {Hq}/{Hkv} {prompts}x{width}")
+    assert pkv.read_device_errors() == 0
+
+
+def test_grouped_fallback_prefix_kernel_matches_oracle(monkeypatch):
+    # the kernel used past 2048 groups (one CTA per group, kv head and 256 tokens)
+    monkeypatch.setenv("PKV_PREFIX_VARIANT", "1")
+    shape = wl.DecodeShape("beam_fallback", 0, 64, 8, 128, 16, torch.bfloat16)
+    div = np.random.default_rng(5).integers(0, 200, 4 * 8)
+    case = build_beam_pool(shape, 1032, 4, 8, div, seed=19)
+    offs, pre = case["alloc"].prefix_groups(case["seqs"])
+    q = wl.draw_query(shape, 20, num_seqs=32).cuda()
+    out = grouped(case, shape, q, offs, pre, int(case["lens"].max()))
+    ref = oracle.decode_attention(q.float().cpu().numpy(), [k.float().numpy() for k in case["ks"]],
+                                  [v.float().numpy() for v in case["vs"]], shape.scale)
+    assert_bf16_close(out, ref, "grouped, fallback prefix kernel")
+    assert pkv.read_device_errors() == 0
