@@ -588,7 +588,7 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 // ---------------------------------------------------------------------------
 constexpr int kMinTilesPerCta = 16;  // >= 256 tokens per share: bounds pieces per segment
 
-constexpr int kYCache = 768;  // tiles of a share whose TMA rows are staged in shared memory
+constexpr int kYCache = 512;  // tiles of a CTA whose TMA rows are staged in shared memory (sized so 3 CTAs of 4 warps fit an SM up to ~500 sequences)
 constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended last
 
 // Shared-memory layout of the balanced kernel (host and device agree on it).
