@@ -63,6 +63,7 @@ struct DecodeArgs {
     int *pieces;    // [S][Hkv]: partials of each segment (balanced path)
     int *seq_tok0;  // [S]: tokens of a shared prefix attended elsewhere (grouped path), or nullptr
     int *prefix_pieces;   // [S][Hkv]: prefix partials of each member (tensor-core prefix kernel), or nullptr
+    int merge_trigger;    // merge kernel: let the next kernel start early (small merges only)
     int prefix_slot;      // grouped path: first partial slot of the prefix partials
     int prefix_part;      // grouped path: tokens per prefix partition
     int num_seqs, num_heads, num_kv_heads, group;
@@ -767,7 +768,15 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     __shared__ int warp_sums[NW];
     __shared__ int carry;
 
-    grid_dependency_wait();
+    // Programmatic dependent launch.  The grouped path reads the first own
+    // token of each sequence, written by the prefix kernel, so it waits now.
+    // Otherwise the prologue below (length scan, row staging, first queries)
+    // reads only this call's inputs (lengths, block tables, queries) and
+    // writes only shared memory, so it may overlap the previous kernel (the
+    // previous call's merge); the wait comes before the first access to the
+    // cache (new-token stores, then TMA) and to the workspace.  Kernels that
+    // let this one start early must not write those inputs after their trigger.
+    if (grouped) grid_dependency_wait();
     grid_launch_dependents();
 
     const int S = a.num_seqs, Hkv = a.num_kv_heads;
@@ -935,6 +944,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     __syncthreads();
 
     if (gw >= parts) return;  // no CTA-wide barrier follows
+    if (!grouped) grid_dependency_wait();
     const int ntiles = (int)(hi - lo);
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
 
@@ -1939,6 +1949,10 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     constexpr int E = D / 32;  // consecutive head_dim elements per lane
     constexpr int U = 8;       // partials whose rows are loaded together
     grid_dependency_wait();
+    // the next kernel may start its prologue (it waits before touching what this
+    // one writes); only for merges of at most one CTA per SM, whose CTAs leave
+    // the next kernel room instead of competing with it for every SM
+    if (a.merge_trigger) grid_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // (sequence, query head)
     if (row >= (int64_t)a.num_seqs * a.num_heads) return;
@@ -2207,7 +2221,9 @@ template <typename T, int D, bool LOG2, bool PIECES>
 static pkv_status launch_reduce(const DecodeArgs &a, cudaStream_t st) {
     const int64_t rows = (int64_t)a.num_seqs * a.num_heads;
     const unsigned blocks = (unsigned)((rows + 3) / 4);
-    return launch_pdl(decode_reduce_kernel<T, D, LOG2, PIECES>, dim3(blocks), dim3(128), 0, st, a);
+    DecodeArgs m = a;
+    m.merge_trigger = (int64_t)blocks <= (int64_t)sm_count() ? 1 : 0;
+    return launch_pdl(decode_reduce_kernel<T, D, LOG2, PIECES>, dim3(blocks), dim3(128), 0, st, m);
 }
 
 }  // namespace pkv
