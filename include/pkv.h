@@ -17,6 +17,14 @@
  *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Device work is enqueued on it; no call synchronises the device, except
  *     pkv_read_device_errors, which waits for the stream.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the previous kernel on the stream finishes if that kernel
+ *     triggers its dependents early (griddepcontrol.launch_dependents), and
+ *     waits for it before touching its results.  The decode kernels read their
+ *     inputs (queries, block tables, lengths) before that wait, so a kernel of
+ *     the caller that triggers early must not write those inputs after its
+ *     trigger.  Kernels that do not trigger early (the usual case) are waited
+ *     for in full, as without programmatic launch.
  *   - Arguments are checked on the host before any launch; a bad argument
  *     returns PKV_ERR_INVALID (or PKV_ERR_UNSUPPORTED for a valid but
  *     unsupported shape) and enqueues nothing.  A failed launch returns
