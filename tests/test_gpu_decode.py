@@ -216,14 +216,21 @@ def test_balanced_workspace_reused_across_calls():
     assert pkv.read_device_errors() == 0
 
 
-@pytest.mark.parametrize("P,dtype,B", [(0, torch.bfloat16, 16), (0, torch.bfloat16, 8), (0, torch.bfloat16, 32),
-                                       (64, torch.bfloat16, 16), (0, torch.float32, 16)])
-def test_decode_append_equals_write_then_decode(P, dtype, B):
+@pytest.mark.parametrize("P,dtype,B,split,nseq", [
+    (0, torch.bfloat16, 16, "", 7), (0, torch.bfloat16, 8, "", 7), (0, torch.bfloat16, 32, "", 7),
+    (64, torch.bfloat16, 16, "", 7), (0, torch.float32, 16, "", 7),
+    (0, torch.bfloat16, 16, "1", 7),    # balanced kernel after the separate store kernel
+    (0, torch.bfloat16, 16, "2", 150),  # fused store with many segments
+    (0, torch.bfloat16, 16, "", 150)])  # 150 x 8 segments: the separate store kernel by default
+def test_decode_append_equals_write_then_decode(P, dtype, B, split, nseq, monkeypatch):
     """paged_attention_decode_append = store the newest token of every
     sequence at position len - 1, then attend (fused into the balanced bf16
-    kernel, a separate store kernel on the other paths)."""
+    kernel for batches of few segments, a separate store kernel otherwise)."""
+    if split:
+        monkeypatch.setenv("PKV_APPEND_SPLIT", split)
     shape = shape_of(32, 8, 128, B, dtype)
-    lens = [1, 16, 17, 300, 0, 1500, 33]
+    base = [1, 16, 17, 300, 0, 1500, 33]
+    lens = (base * (nseq // len(base) + 1))[:nseq] if nseq != len(base) else base
     case = make_decode_case(shape, lens, seed=31 + B + P)
     kc, vc = case["kc"].clone(), case["vc"].clone()
     k_new = torch.zeros((len(lens), 8, 128), dtype=dtype)
