@@ -386,6 +386,52 @@ PKV_EXPORT pkv_status block_allocator_prefix_groups(const pkv_allocator *a, cons
                                          int32_t *group_offsets_out, int32_t *prefix_lens_out,
                                          int *num_groups_out);
 
+/*
+ * block_allocator_add_seq_cached -- block_allocator_add_seq for a prompt
+ * whose token ids are known, reusing the K/V of earlier prompts that start
+ * with the same tokens (prefix caching).
+ *
+ * Source: "vLLM PagedAttention: Buoc dot pha ve thong luong suy luan LLM",
+ * list of advanced features, "Prefix caching" (the KV cache of a prompt
+ * prefix shared by several requests is reused instead of recomputed); and
+ * "PagedAttention (vLLM) -- Virtual memory cho AI", related posts ("Prefix
+ * Caching" for system prompts reused many times).  The pages give no
+ * mechanism; this one: every full block of a prompt added here is registered
+ * under a 64-bit hash of its whole token prefix (FNV-1a over the parent's
+ * hash and the block's token ids).  A later prompt whose leading full blocks
+ * have registered prefixes with equal token ids (compared exactly) shares
+ * those blocks (reference count + 1) instead of taking new ones; the first
+ * block that does not match, and everything after it, is allocated as usual
+ * (a partially filled last block is never shared this way).
+ *
+ *   tokens              host int32 [num_tokens]: the prompt's token ids
+ *   cached_tokens_out   tokens at the start of the prompt whose K and V are
+ *                       already in the pool (a multiple of block_size); the
+ *                       caller writes K/V for positions cached_tokens_out ..
+ *                       num_tokens - 1 only.  A registered block holds valid
+ *                       K/V once the prompt that registered it has been
+ *                       written.
+ * A registered block whose last holder is freed stays registered and is kept
+ * (evictable) until the free stack runs dry: then the one released longest
+ * ago is handed out and unregistered (a freed prompt's blocks are released
+ * last block first, so a prefix loses its tail before its head).
+ * block_allocator_num_free counts free and evictable blocks.  All-or-nothing:
+ * PKV_ERR_OOM and PKV_ERR_INVALID change nothing.
+ */
+PKV_EXPORT pkv_status block_allocator_add_seq_cached(pkv_allocator *a, int64_t seq, const int32_t *tokens,
+                                          int64_t num_tokens, int64_t *cached_tokens_out);
+
+/* Prefix cache counters: full blocks found (hits) and not found (misses) by
+ * block_allocator_add_seq_cached so far, blocks registered now, and how many
+ * of those are evictable (no holder).  Any output may be NULL. */
+PKV_EXPORT pkv_status block_allocator_cache_stats(const pkv_allocator *a, int64_t *hits, int64_t *misses,
+                                       int *cached_blocks, int *evictable_blocks);
+
+/* Empty the prefix cache: evictable blocks return to the free stack (released
+ * longest ago first); blocks still held keep their holders but are no longer
+ * found by block_allocator_add_seq_cached. */
+PKV_EXPORT pkv_status block_allocator_cache_clear(pkv_allocator *a);
+
 /* Slots of token positions start .. start+count-1 of `seq` (all must exist). */
 PKV_EXPORT pkv_status block_allocator_slots(const pkv_allocator *a, int64_t seq, int64_t start,
                                  int64_t count, int64_t *out);

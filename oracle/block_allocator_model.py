@@ -25,6 +25,23 @@ Readings where the pages are silent (each listed in the design notes):
 * running out of blocks returns ERR_OOM and changes nothing;
 * waste = 1 - occupied slots / allocated slots, every physical block counted
   once however many sequences share it.
+
+Prefix caching ("vLLM PagedAttention: Buoc dot pha ve thong luong suy luan
+LLM", list of advanced features: the KV cache of a prompt prefix shared by
+several requests is reused instead of recomputed).  The pages give no
+mechanism; the reading modelled here (and listed in the design notes):
+* only full blocks of prompts added with ``add_seq_cached`` are registered,
+  each under its whole token prefix (here the prefix itself is the key; the
+  library uses a hash of it plus an exact comparison of the block's tokens);
+* a prompt shares its leading full blocks whose prefixes are registered
+  (reference count + 1) and allocates the rest; ``cached_tokens`` = shared
+  blocks x block_size;
+* a registered block left without holders stays registered in an evictable
+  queue; a freed prompt's blocks join it last block first; blocks are taken
+  from the free stack first, then from the front of the queue (unregistering
+  them); ``num_free`` counts both;
+* ``cache_clear`` moves the evictable blocks (front first) to the free stack
+  and forgets every registration.
 """
 from __future__ import annotations
 
@@ -43,16 +60,28 @@ class BlockAllocatorModel:
         self._free = list(range(self.num_blocks - 1, -1, -1))
         self._ref = [0] * self.num_blocks
         self._seqs = {}  # seq id -> [table (list of block ids), num_tokens]
+        self._cache = {}      # token prefix (tuple) -> block
+        self._key = {}        # registered block -> its token prefix
+        self._evictable = []  # registered blocks without holders, front = released longest ago
+        self.hits = 0
+        self.misses = 0
 
     # -- internal -----------------------------------------------------------
+    def _available(self) -> int:
+        return len(self._free) + len(self._evictable)
+
     def _take(self) -> int:
-        b = self._free.pop()
+        if self._free:
+            b = self._free.pop()
+        else:
+            b = self._evictable.pop(0)
+            del self._cache[self._key.pop(b)]
         self._ref[b] = 1
         return b
 
     def _release(self, b: int) -> None:
         self._ref[b] -= 1
-        if self._ref[b] == 0:
+        if self._ref[b] == 0 and b not in self._key:
             self._free.append(b)
 
     # -- operations (return a status, plus results) --------------------------
@@ -61,10 +90,57 @@ class BlockAllocatorModel:
         if seq in self._seqs or num_tokens < 0:
             return ERR_INVALID
         need = -(-num_tokens // self.block_size)
-        if need > len(self._free):
+        if need > self._available():
             return ERR_OOM
         table = [self._take() for _ in range(need)]
         self._seqs[seq] = [table, num_tokens]
+        return OK
+
+    def add_seq_cached(self, seq: int, tokens):
+        """A prompt with known token ids.  Returns (status, cached_tokens)."""
+        tokens = [int(t) for t in tokens]
+        if seq in self._seqs:
+            return ERR_INVALID, 0
+        B = self.block_size
+        n = len(tokens)
+        nfull, need = n // B, -(-n // B)
+        hit = []
+        for i in range(nfull):
+            b = self._cache.get(tuple(tokens[:(i + 1) * B]))
+            if b is None:
+                break
+            hit.append(b)
+        revived = sum(1 for b in hit if self._ref[b] == 0)
+        if need - len(hit) > self._available() - revived:
+            return ERR_OOM, 0
+        table = []
+        for b in hit:
+            if self._ref[b] == 0:
+                self._evictable.remove(b)
+            self._ref[b] += 1
+            table.append(b)
+        for i in range(len(hit), need):
+            b = self._take()
+            table.append(b)
+            key = tuple(tokens[:(i + 1) * B])
+            if i < nfull and key not in self._cache:
+                self._cache[key] = b
+                self._key[b] = key
+        self._seqs[seq] = [table, n]
+        self.hits += len(hit)
+        self.misses += nfull - len(hit)
+        return OK, len(hit) * B
+
+    def cache_stats(self):
+        return {"hits": self.hits, "misses": self.misses, "cached_blocks": len(self._cache),
+                "evictable_blocks": len(self._evictable)}
+
+    def cache_clear(self) -> int:
+        for b in self._evictable:
+            self._free.append(b)
+        self._evictable = []
+        self._cache = {}
+        self._key = {}
         return OK
 
     def append_slot(self, seq: int):
@@ -77,12 +153,12 @@ class BlockAllocatorModel:
         src = dst = -1
         if offset == 0:
             # last block full (or no block yet): a fresh block for this token
-            if not self._free:
+            if not self._available():
                 return ERR_OOM, -1, -1, -1
             table.append(self._take())
         elif self._ref[table[-1]] > 1:
             # the partially filled last block is shared: copy before writing
-            if not self._free:
+            if not self._available():
                 return ERR_OOM, -1, -1, -1
             src = table[-1]
             dst = self._take()
@@ -108,6 +184,10 @@ class BlockAllocatorModel:
         table, _ = self._seqs.pop(seq)
         for b in table:
             self._release(b)
+        # registered blocks left without holders: evictable, last block first
+        for b in reversed(table):
+            if self._ref[b] == 0 and b in self._key:
+                self._evictable.append(b)
         return OK
 
     # -- queries --------------------------------------------------------------
@@ -118,7 +198,7 @@ class BlockAllocatorModel:
         return self._seqs[seq][1]
 
     def num_free(self) -> int:
-        return len(self._free)
+        return self._available()
 
     def refcount(self, block: int) -> int:
         return self._ref[block]

@@ -267,6 +267,27 @@ class BlockAllocator:
     def add_seq(self, seq: int, num_tokens: int) -> int:
         return self._lib.block_allocator_add_seq(self._h, int(seq), int(num_tokens))
 
+    def add_seq_cached(self, seq: int, tokens):
+        """A prompt whose leading full blocks may already be in the pool
+        (prefix caching).  Returns (status, cached_tokens): the caller writes
+        K/V for positions cached_tokens .. len(tokens) - 1 only."""
+        ids = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        cached = ctypes.c_int64(0)
+        st = self._lib.block_allocator_add_seq_cached(self._h, int(seq), ids.ctypes.data if ids.size else None,
+                                                      int(ids.size), ctypes.byref(cached))
+        return st, int(cached.value)
+
+    def cache_stats(self) -> dict:
+        """Prefix cache counters: hits, misses, cached_blocks, evictable_blocks."""
+        h, m = ctypes.c_int64(0), ctypes.c_int64(0)
+        c, e = ctypes.c_int(0), ctypes.c_int(0)
+        _check(self._lib.block_allocator_cache_stats(self._h, ctypes.byref(h), ctypes.byref(m), ctypes.byref(c),
+                                                     ctypes.byref(e)), "cache_stats")
+        return {"hits": h.value, "misses": m.value, "cached_blocks": c.value, "evictable_blocks": e.value}
+
+    def cache_clear(self) -> int:
+        return self._lib.block_allocator_cache_clear(self._h)
+
     def append_slot(self, seq: int):
         """(status, slot, cow_src, cow_dst)."""
         slot, src, dst = ctypes.c_int64(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)

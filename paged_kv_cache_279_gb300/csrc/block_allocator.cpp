@@ -1,17 +1,41 @@
 // Host block allocator: free stack, per-sequence block tables, reference
-// counts and copy-on-write.  Semantics are documented in include/pkv.h.
+// counts, copy-on-write and a prefix cache of full prompt blocks.  Semantics
+// are documented in include/pkv.h.
 //
 // "PagedAttention (vLLM) -- Virtual memory cho AI", section "Co che Block
 // Table": blocks are handed out only when a token needs one and freed blocks
 // are reused at once without defragmentation; section "Copy-on-Write cho Beam
 // Search": branches share prefix blocks and split a block when they diverge.
+// "vLLM PagedAttention: Buoc dot pha ve thong luong suy luan LLM", list of
+// advanced features, "Prefix caching": the KV cache of a prompt prefix shared
+// by several requests is reused instead of recomputed.
 #include "pkv.h"
 
 #include <algorithm>
 #include <climits>
+#include <cstring>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
+
+namespace {
+// FNV-1a over the parent prefix hash and a block's token ids: a deterministic
+// 64-bit digest of the whole token prefix up to and including the block.
+uint64_t prefix_hash(uint64_t parent, const int32_t *tokens, int n) {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](uint64_t v, int bytes) {
+        for (int i = 0; i < bytes; ++i) {
+            h ^= (v >> (8 * i)) & 0xffu;
+            h *= 1099511628211ull;
+        }
+    };
+    mix(parent, 8);
+    for (int i = 0; i < n; ++i) mix((uint32_t)tokens[i], 4);
+    return h;
+}
+constexpr uint64_t kRootHash = 0x9e3779b97f4a7c15ull;  // parent of a prompt's first block
+}  // namespace
 
 struct pkv_allocator {
     struct Seq {
@@ -24,14 +48,43 @@ struct pkv_allocator {
     std::vector<int32_t> refcnt;
     std::unordered_map<int64_t, Seq> seqs;
 
-    int32_t take() {
-        int32_t b = free_stack.back();
-        free_stack.pop_back();
+    // Prefix cache: full prompt blocks registered under the hash of their whole
+    // token prefix.  A registered block whose last holder goes away stays
+    // registered and joins `evictable` (front = released longest ago); it is
+    // handed out again, losing its registration, only when the free stack is
+    // empty.
+    std::unordered_map<uint64_t, int32_t> cache;    // prefix hash -> block
+    std::vector<char> cached;                        // block is registered
+    std::vector<uint64_t> key, parent;               // its prefix hash, its parent's
+    std::vector<int32_t> toks;                       // its block_size token ids
+    std::list<int32_t> evictable;
+    std::vector<std::list<int32_t>::iterator> ev_pos;
+    int64_t hits = 0, misses = 0;
+
+    int64_t available() const { return (int64_t)free_stack.size() + (int64_t)evictable.size(); }
+    void unregister(int32_t b) {
+        cache.erase(key[b]);
+        cached[b] = 0;
+    }
+    int32_t take() {  // callers checked available() > 0
+        int32_t b;
+        if (!free_stack.empty()) {
+            b = free_stack.back();
+            free_stack.pop_back();
+        } else {
+            b = evictable.front();
+            evictable.pop_front();
+            unregister(b);
+        }
         refcnt[b] = 1;
         return b;
     }
     void release(int32_t b) {
-        if (--refcnt[b] == 0) free_stack.push_back(b);
+        if (--refcnt[b] == 0 && !cached[b]) free_stack.push_back(b);
+    }
+    void park(int32_t b) {  // a registered block without holders
+        evictable.push_back(b);
+        ev_pos[b] = std::prev(evictable.end());
     }
 };
 
@@ -45,6 +98,11 @@ pkv_allocator *block_allocator_create(int num_blocks, int block_size) {
         a->num_blocks = num_blocks;
         a->block_size = block_size;
         a->refcnt.assign(num_blocks, 0);
+        a->cached.assign(num_blocks, 0);
+        a->key.assign(num_blocks, 0);
+        a->parent.assign(num_blocks, 0);
+        a->toks.assign((size_t)num_blocks * block_size, 0);
+        a->ev_pos.resize(num_blocks);
         a->free_stack.resize(num_blocks);
         for (int i = 0; i < num_blocks; ++i) a->free_stack[i] = num_blocks - 1 - i;
     } catch (...) {
@@ -59,7 +117,7 @@ void block_allocator_destroy(pkv_allocator *a) { delete a; }
 pkv_status block_allocator_add_seq(pkv_allocator *a, int64_t seq, int64_t num_tokens) {
     if (!a || num_tokens < 0 || a->seqs.count(seq)) return PKV_ERR_INVALID;
     const int64_t need = (num_tokens + a->block_size - 1) / a->block_size;
-    if (need > (int64_t)a->free_stack.size()) return PKV_ERR_OOM;
+    if (need > a->available()) return PKV_ERR_OOM;
     try {
         pkv_allocator::Seq s;
         s.table.reserve((size_t)need + 1);
@@ -82,7 +140,7 @@ pkv_status block_allocator_append_slot(pkv_allocator *a, int64_t seq, int64_t *s
     int32_t src = -1, dst = -1;
     if (offset == 0) {
         // last block full (or none yet): a fresh block for this token
-        if (a->free_stack.empty()) return PKV_ERR_OOM;
+        if (a->available() == 0) return PKV_ERR_OOM;
         try {
             s.table.push_back(-1);
         } catch (...) {
@@ -91,7 +149,7 @@ pkv_status block_allocator_append_slot(pkv_allocator *a, int64_t seq, int64_t *s
         s.table.back() = a->take();
     } else if (a->refcnt[s.table.back()] > 1) {
         // shared, partially filled last block: copy it before writing
-        if (a->free_stack.empty()) return PKV_ERR_OOM;
+        if (a->available() == 0) return PKV_ERR_OOM;
         src = s.table.back();
         dst = a->take();
         a->refcnt[src] -= 1;
@@ -123,7 +181,7 @@ pkv_status block_allocator_append_slots(pkv_allocator *a, const int64_t *seqs, i
     } catch (...) {
         return PKV_ERR_INVALID;
     }
-    if (need > (int64_t)a->free_stack.size()) return PKV_ERR_OOM;
+    if (need > a->available()) return PKV_ERR_OOM;
     int ncow = 0;
     for (int i = 0; i < n; ++i) {
         int32_t src = -1, dst = -1;
@@ -157,8 +215,97 @@ pkv_status block_allocator_free_seq(pkv_allocator *a, int64_t seq) {
     if (!a) return PKV_ERR_INVALID;
     auto it = a->seqs.find(seq);
     if (it == a->seqs.end()) return PKV_ERR_INVALID;
-    for (int32_t b : it->second.table) a->release(b);
+    const auto &t = it->second.table;
+    for (int32_t b : t) a->release(b);
+    // registered blocks left without holders become evictable, the last block
+    // of the prefix first (evicted before the blocks it extends)
+    for (size_t i = t.size(); i-- > 0;)
+        if (a->refcnt[t[i]] == 0 && a->cached[t[i]]) a->park(t[i]);
     a->seqs.erase(it);
+    return PKV_OK;
+}
+
+pkv_status block_allocator_add_seq_cached(pkv_allocator *a, int64_t seq, const int32_t *tokens,
+                                          int64_t num_tokens, int64_t *cached_tokens_out) {
+    if (!a || num_tokens < 0 || (num_tokens > 0 && !tokens) || a->seqs.count(seq)) return PKV_ERR_INVALID;
+    const int B = a->block_size;
+    const int64_t nfull = num_tokens / B, need = (num_tokens + B - 1) / B;
+    // leading full blocks already registered (exact token match)
+    std::vector<int32_t> hit;
+    std::vector<uint64_t> keys((size_t)nfull);
+    uint64_t h = kRootHash;
+    bool missed = false;
+    for (int64_t i = 0; i < nfull; ++i) {
+        const int32_t *bt = tokens + i * B;
+        const uint64_t k = prefix_hash(h, bt, B);
+        keys[(size_t)i] = k;
+        if (!missed) {
+            auto c = a->cache.find(k);
+            if (c != a->cache.end() && a->parent[c->second] == h &&
+                std::memcmp(&a->toks[(size_t)c->second * B], bt, (size_t)B * sizeof(int32_t)) == 0)
+                hit.push_back(c->second);
+            else
+                missed = true;
+        }
+        h = k;
+    }
+    int64_t revived = 0;  // hits that are evictable now and leave the pool
+    for (int32_t b : hit) revived += a->refcnt[b] == 0;
+    if (need - (int64_t)hit.size() > a->available() - revived) return PKV_ERR_OOM;
+    try {
+        pkv_allocator::Seq s;
+        s.table.reserve((size_t)need + 1);
+        s.tokens = num_tokens;
+        auto it = a->seqs.emplace(seq, std::move(s)).first;
+        auto &table = it->second.table;
+        for (int32_t b : hit) {
+            if (a->refcnt[b] == 0) a->evictable.erase(a->ev_pos[b]);
+            a->refcnt[b] += 1;
+            table.push_back(b);
+        }
+        uint64_t ph = hit.empty() ? kRootHash : keys[hit.size() - 1];
+        for (int64_t i = (int64_t)hit.size(); i < need; ++i) {
+            const int32_t b = a->take();
+            table.push_back(b);
+            if (i < nfull && !a->cache.count(keys[(size_t)i])) {  // register the new full block
+                a->cache.emplace(keys[(size_t)i], b);
+                a->cached[b] = 1;
+                a->key[b] = keys[(size_t)i];
+                a->parent[b] = ph;
+                std::memcpy(&a->toks[(size_t)b * B], tokens + i * B, (size_t)B * sizeof(int32_t));
+            }
+            if (i < nfull) ph = keys[(size_t)i];
+        }
+    } catch (...) {
+        return PKV_ERR_INVALID;
+    }
+    a->hits += (int64_t)hit.size();
+    a->misses += nfull - (int64_t)hit.size();
+    if (cached_tokens_out) *cached_tokens_out = (int64_t)hit.size() * B;
+    return PKV_OK;
+}
+
+pkv_status block_allocator_cache_stats(const pkv_allocator *a, int64_t *hits, int64_t *misses,
+                                       int *cached_blocks, int *evictable_blocks) {
+    if (!a) return PKV_ERR_INVALID;
+    if (hits) *hits = a->hits;
+    if (misses) *misses = a->misses;
+    if (cached_blocks) *cached_blocks = (int)a->cache.size();
+    if (evictable_blocks) *evictable_blocks = (int)a->evictable.size();
+    return PKV_OK;
+}
+
+pkv_status block_allocator_cache_clear(pkv_allocator *a) {
+    if (!a) return PKV_ERR_INVALID;
+    // unreferenced registered blocks go back to the free stack, oldest first;
+    // registered blocks still held keep their blocks but leave the cache
+    for (int32_t b : a->evictable) {
+        a->cached[b] = 0;
+        a->free_stack.push_back(b);
+    }
+    a->evictable.clear();
+    for (auto &kv : a->cache) a->cached[kv.second] = 0;
+    a->cache.clear();
     return PKV_OK;
 }
 
@@ -253,7 +400,7 @@ int64_t block_allocator_num_tokens(const pkv_allocator *a, int64_t seq) {
 }
 
 int block_allocator_num_free(const pkv_allocator *a) {
-    return a ? (int)a->free_stack.size() : -1;
+    return a ? (int)a->available() : -1;
 }
 
 int block_allocator_refcount(const pkv_allocator *a, int32_t block) {

@@ -33,7 +33,12 @@ def run_ops(ops, num_blocks, block_size):
             assert c.fork(op[1], op[2]) == m.fork(op[1], op[2])
         elif kind == "free":
             assert c.free_seq(op[1]) == m.free_seq(op[1])
+        elif kind == "cached":
+            assert c.add_seq_cached(op[1], op[2]) == m.add_seq_cached(op[1], op[2])
+        elif kind == "clear":
+            assert c.cache_clear() == m.cache_clear()
         assert_same_state(c, m, m.sequences())
+        assert c.cache_stats() == m.cache_stats()
     return c, m
 
 
@@ -172,3 +177,53 @@ def test_prefix_groups_follow_forks():
     c8.fork(0, 1)
     offs8, pre8 = c8.prefix_groups([0, 1])
     assert offs8.tolist() == [0, 2] and pre8.tolist() == [96]
+
+
+def prompt_ops(rnd, n, block_size, vocab=3):
+    """Prompts drawn from a few shared prefixes (prefix caching), mixed with
+    appends, forks, frees, plain prompts and cache clears."""
+    bases = [[rnd.randrange(vocab) for _ in range(4 * block_size)] for _ in range(3)]
+    ops, ids = [], []
+    for _ in range(n):
+        r = rnd.random()
+        if r < 0.35 or not ids:
+            base = rnd.choice(bases)
+            cut = rnd.randint(0, len(base))
+            tail = [rnd.randrange(vocab) for _ in range(rnd.randint(0, block_size + 3))]
+            ids.append(len(ids) + 1000 * rnd.randint(0, 1))
+            ops.append(("cached", ids[-1], base[:cut] + tail))
+        elif r < 0.4:
+            ids.append(len(ids) + 5000)
+            ops.append(("add", ids[-1], rnd.randint(0, 2 * block_size)))
+        elif r < 0.65:
+            ops.append(("append", rnd.choice(ids)))
+        elif r < 0.75:
+            child = len(ids) + 10000
+            ops.append(("fork", rnd.choice(ids), child))
+            ids.append(child)
+        elif r < 0.97:
+            ops.append(("free", rnd.choice(ids)))
+        else:
+            ops.append(("clear",))
+    return ops
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_prefix_cache_sequences_match_model(seed):
+    """add_seq_cached with hits, misses, evictions under pressure and clears:
+    tables, refcounts, free counts and cache counters equal the model's."""
+    rnd = random.Random(1000 + seed)
+    B = rnd.choice([2, 4, 16])
+    run_ops(prompt_ops(rnd, 250, B), num_blocks=rnd.choice([6, 12, 40]), block_size=B)
+
+
+def test_prefix_cache_reports_cached_tokens_and_shares_blocks():
+    c = pkv.BlockAllocator(64, 16)
+    system = list(range(1000, 1040))                 # 40 shared tokens: 2 full blocks
+    assert c.add_seq_cached(0, system + [1, 2, 3]) == (pkv.PKV_OK, 0)
+    assert c.add_seq_cached(1, system + [4, 5]) == (pkv.PKV_OK, 32)
+    assert c.block_table(1)[:2] == c.block_table(0)[:2]
+    assert c.cache_stats() == {"hits": 2, "misses": 2, "cached_blocks": 2, "evictable_blocks": 0}
+    # the shared blocks are prefix groups for the grouped decode
+    offs, pre = c.prefix_groups([0, 1])
+    assert offs.tolist() == [0, 2] and pre.tolist() == [32]

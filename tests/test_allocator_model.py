@@ -142,3 +142,67 @@ def test_random_operation_sequences_keep_invariants():
             for s in m.sequences():
                 n, t = m.num_tokens(s), m.block_table(s)
                 assert len(t) * B - n < B or n == 0
+
+
+# -- prefix caching ("vLLM PagedAttention: Buoc dot pha ve thong luong suy luan LLM",
+#    advanced features, "Prefix caching": a shared prompt prefix's KV is reused) --
+
+def test_prefix_cache_shares_leading_full_blocks():
+    m = BlockAllocatorModel(16, 16)
+    system = list(range(100, 140))                       # a 40-token system prompt
+    st, cached = m.add_seq_cached(0, system + [1, 2, 3])  # 43 tokens: blocks 0, 1, 2
+    assert (st, cached) == (OK, 0) and m.block_table(0) == [0, 1, 2]
+    st, cached = m.add_seq_cached(1, system + [7, 8])    # 42 tokens: the two full blocks are found
+    assert (st, cached) == (OK, 32)
+    assert m.block_table(1)[:2] == [0, 1] and m.block_table(1)[2] == 3
+    assert m.refcount(0) == m.refcount(1) == 2 and m.refcount(2) == 1
+    # the third block of the first prompt held tokens 32..42: not full, never registered
+    # prompt 0: 2 full blocks, both new (misses); prompt 1: both found (hits)
+    assert m.cache_stats() == {"hits": 2, "misses": 2, "cached_blocks": 2, "evictable_blocks": 0}
+
+
+def test_prefix_cache_counts_only_full_blocks():
+    m = BlockAllocatorModel(8, 4)
+    st, c = m.add_seq_cached(0, [1, 2, 3, 4, 5, 6])   # one full block, one partial
+    assert (st, c) == (OK, 0)
+    st, c = m.add_seq_cached(1, [1, 2, 3, 4, 5, 6])   # the same prompt: only the full block is shared
+    assert (st, c) == (OK, 4)
+    assert m.block_table(1)[0] == m.block_table(0)[0] and m.block_table(1)[1] != m.block_table(0)[1]
+    st, c = m.add_seq_cached(2, [1, 2, 3, 9, 5, 6])   # differs inside the first block: nothing shared
+    assert (st, c) == (OK, 0)
+    st, c = m.add_seq_cached(3, [1, 2, 3, 4])         # exactly the first block
+    assert (st, c) == (OK, 4)
+
+
+def test_prefix_cache_survives_free_and_evicts_tail_first():
+    m = BlockAllocatorModel(6, 2)
+    prompt = [5, 6, 7, 8, 9, 10]                      # three full blocks
+    assert m.add_seq_cached(0, prompt) == (OK, 0)
+    table = m.block_table(0)
+    assert m.free_seq(0) == OK
+    # nothing holds the blocks, yet they stay registered and count as free
+    assert m.num_free() == 6 and m.cache_stats()["evictable_blocks"] == 3
+    assert m.add_seq_cached(1, prompt) == (OK, 6)      # found again, same blocks
+    assert m.block_table(1) == table and m.cache_stats()["evictable_blocks"] == 0
+    assert m.free_seq(1) == OK
+    # 3 free + 3 evictable; a 4-block prompt takes the free ones, then evicts the
+    # prompt's last block first
+    assert m.add_seq(2, 8) == OK
+    assert m.cache_stats()["evictable_blocks"] == 2 and m.cache_stats()["cached_blocks"] == 2
+    assert table[2] in m.block_table(2)
+    # no room for the prompt's third block while sequence 2 holds the rest
+    assert m.add_seq_cached(3, prompt) == (ERR_OOM, 0)
+    assert m.free_seq(2) == OK
+    assert m.add_seq_cached(3, prompt) == (OK, 4)      # the first two blocks are still there
+    assert m.block_table(3)[:2] == table[:2]
+
+
+def test_prefix_cache_oom_changes_nothing_and_clear_forgets():
+    m = BlockAllocatorModel(3, 2)
+    assert m.add_seq_cached(0, [1, 2, 3, 4]) == (OK, 0)
+    before = (m.block_table(0), m.num_free(), m.cache_stats())
+    assert m.add_seq_cached(1, [1, 2, 9, 9, 9, 9]) == (ERR_OOM, 0)   # needs 2 new blocks, 1 left
+    assert (m.block_table(0), m.num_free(), m.cache_stats()) == before and 1 not in m.sequences()
+    assert m.free_seq(0) == OK and m.cache_clear() == OK
+    assert m.cache_stats()["cached_blocks"] == 0 and m.num_free() == 3
+    assert m.add_seq_cached(1, [1, 2, 3, 4]) == (OK, 0)
