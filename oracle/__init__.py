@@ -28,6 +28,10 @@ Contents and the passages they follow (page titles as given at each address):
   (waste remains only in each sequence's last block).
 * ``BlockAllocatorModel`` (``block_allocator_model.py``) -- the allocator's
   host semantics.
+* ``fp8_e4m3`` -- the FP8 (E4M3) KV cache: quantiser, dequantiser and cache
+  write.  aiwiki.vn page, paragraph on quantisation and offloading (K/V kept
+  in a lower-precision representation to cut bytes, at a conversion cost and
+  an error risk); the format and scaling readings are in that module.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` to values the pages
 print, closed forms, invariants or an independent library routine.

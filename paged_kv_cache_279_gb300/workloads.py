@@ -115,6 +115,24 @@ def draw_seq_kv(shape: DecodeShape, seed: int, seq: int, length: int, layer: int
     return k, v
 
 
+def draw_e4m3_codes(shape_, seed: int, exp_center: float = 11.0, exp_sigma: float = 1.5) -> np.ndarray:
+    """Random 8-bit E4M3 bit patterns (uint8) for an FP8 cache.
+
+    Drawn field by field -- a fair sign bit, an exponent field from a rounded
+    normal clipped to 0..15, a uniform 3-bit mantissa -- with the NaN pattern
+    (all exponent and mantissa bits set) replaced by the largest finite one.
+    The default centre (field 11, magnitudes around 16-32) matches N(0, 1)
+    data quantised with a scale of about 1/32.
+    """
+    rng = np.random.default_rng(sub_seed(seed, 7))
+    n = int(np.prod(shape_))
+    sign = rng.integers(0, 2, n, dtype=np.int64)
+    e = np.clip(np.rint(rng.normal(exp_center, exp_sigma, n)), 0, 15).astype(np.int64)
+    m = rng.integers(0, 8, n, dtype=np.int64)
+    m = np.where((e == 15) & (m == 7), 6, m)
+    return ((sign << 7) | (e << 3) | m).astype(np.uint8).reshape(shape_)
+
+
 def draw_block_ids(num_blocks: int, seed: int) -> np.ndarray:
     """A random order of the physical block ids 0..num_blocks-1."""
     rng = np.random.default_rng(sub_seed(seed, 6))
