@@ -176,6 +176,58 @@ PKV_EXPORT pkv_status paged_attention_decode(void *out, const void *q, const voi
                                   size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * FP8 (E4M3) KV cache -- kv_cache_write_fp8 and paged_attention_decode_fp8.
+ *
+ * Source: aiwiki.vn page above, the paragraph on quantisation and offloading:
+ * a quantised KV cache stores keys and values in a lower-precision
+ * representation to cut the bytes per element, at a conversion cost and a
+ * risk of numerical error.  The page fixes no format; this library uses the
+ * OCP FP8 E4M3 encoding (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, subnormals, no infinities, S.1111.111 = NaN, largest value 448) with
+ * one float32 scale per tensor (k_scale for K, v_scale for V):
+ *     code(x)  = the E4M3 value nearest to the float32 quotient x / scale
+ *                (ties to the even code; beyond +-448, infinities included,
+ *                saturate to +-448; NaN gives a NaN code)
+ *     value(c) = e4m3(c) * scale
+ * FP8 cache layout (one byte per element; base addresses 16-byte aligned):
+ *     K: [num_blocks][num_kv_heads][block_size][head_dim]  (as the bf16 cache)
+ *     V: [num_blocks][num_kv_heads][head_dim][block_size]  (transposed per
+ *        block, so the attention kernel reads runs of consecutive tokens)
+ * block_copy copies FP8 blocks unchanged (block_bytes = Hkv * B * D).
+ * Supported: head_dim 128, block_size 16 or 32, bf16 new K/V, queries and
+ * outputs, at most 8 query heads per KV head, at most 8192 sequences.
+ *
+ * kv_cache_write_fp8 -- quantise and store the K/V of new tokens.
+ *   k_new, v_new   device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   k_cache, v_cache  device uint8, FP8 layout above, written in place
+ *   slot_mapping   device int64 [num_tokens], as for kv_cache_write
+ *   k_scale, v_scale  positive finite float32 scales (else PKV_ERR_INVALID)
+ * The codes are bit-exact functions of the inputs (code() above).
+ *
+ * paged_attention_decode_fp8 -- paged_attention_decode over an FP8 cache:
+ *     out[s,h,:] = sum_t softmax_t(scale * q[s,h,:] . K'[s,t,g,:]) * V'[s,t,g,:]
+ * with K' = value(K codes, k_scale), V' = value(V codes, v_scale), g the KV
+ * head of h, and the same block-table lookup, length rules, zero rows for
+ * empty contexts and device error bits as paged_attention_decode.  q and out
+ * are bf16 [num_seqs][num_heads][head_dim].  Always the balanced split: the
+ * workspace is paged_attention_workspace_size(num_seqs, num_heads, head_dim,
+ * max_seq_len, 0) bytes, 256-byte aligned (may be NULL when max_seq_len is 0).
+ * Results do not depend on which physical blocks hold the tokens.
+ */
+PKV_EXPORT pkv_status kv_cache_write_fp8(const void *k_new, const void *v_new, void *k_cache,
+                                         void *v_cache, const int64_t *slot_mapping, int num_tokens,
+                                         int num_kv_heads, int head_dim, int block_size,
+                                         int num_blocks, float k_scale, float v_scale, void *stream);
+
+PKV_EXPORT pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                                 const void *v_cache, const int32_t *block_tables,
+                                                 const int32_t *seq_lens, int num_seqs, int num_heads,
+                                                 int num_kv_heads, int head_dim, int block_size,
+                                                 int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                                 float scale, float k_scale, float v_scale,
+                                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * block_copy -- copy whole physical blocks, in every layer, for K and V.
  *
  * Source: troisinh page, section "Copy-on-Write cho Beam Search": sequences

@@ -64,31 +64,19 @@ def float_to_e4m3(x) -> np.ndarray:
     exact for every float32 input.
     """
     x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    flat = x.reshape(-1)
-    out = np.empty(flat.shape, dtype=np.uint8)
-    for i, v in enumerate(flat.tolist()):
-        if v != v:  # NaN
-            out[i] = NAN_CODE
-            continue
-        sign = 0x80 if np.signbit(v) else 0
-        a = abs(v)
-        if a >= E4M3_MAX:
-            out[i] = 0x7E | sign
-            continue
-        hi = int(np.searchsorted(_GRID, a, side="left"))  # _GRID[hi - 1] < a <= _GRID[hi]
-        if _GRID[hi] == a:
-            code = hi
-        else:
-            lo = hi - 1
-            mid = (_GRID[lo] + _GRID[hi]) / 2.0
-            if a < mid:
-                code = lo
-            elif a > mid:
-                code = hi
-            else:
-                code = lo if lo % 2 == 0 else hi
-        out[i] = code | sign
-    return out.reshape(x.shape)
+    a = np.abs(x)
+    nan = np.isnan(x)
+    sat = ~nan & (a >= E4M3_MAX)
+    a_in = np.where(nan | sat, 0.0, a)
+    hi = np.minimum(np.searchsorted(_GRID, a_in, side="left"), len(_GRID) - 1)
+    lo = np.maximum(hi - 1, 0)
+    mid = (_GRID[lo] + _GRID[hi]) / 2.0  # exact in float64
+    code = np.where(_GRID[hi] == a_in, hi,
+                    np.where(a_in < mid, lo,
+                             np.where(a_in > mid, hi, np.where(lo % 2 == 0, lo, hi))))
+    code = np.where(sat, 0x7E, code) | np.where(np.signbit(x), 0x80, 0)
+    code = np.where(nan, NAN_CODE, code)
+    return code.astype(np.uint8)
 
 
 def quantize(x, scale: float) -> np.ndarray:

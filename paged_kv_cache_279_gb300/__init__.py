@@ -29,7 +29,8 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, 
     1, 2, 4, 8, 16, 32)
 
 __all__ = [
-    "PkvError", "kv_cache_write", "paged_attention_decode", "paged_attention_workspace_size",
+    "PkvError", "kv_cache_write", "kv_cache_write_fp8", "paged_attention_decode",
+    "paged_attention_decode_fp8", "paged_attention_workspace_size",
     "paged_attention_decode_append", "paged_attention_decode_grouped",
     "paged_attention_grouped_workspace_size", "block_copy", "read_device_errors", "BlockAllocator",
     "library_path",
@@ -134,6 +135,54 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, sca
         S, Hq, Hkv, D, B, block_tables.shape[1], NB, int(max_seq_len), float(scale),
         int(partition_size), ws_ptr, ws_bytes, dt, _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def kv_cache_write_fp8(k_new, v_new, k_cache, v_cache, slot_mapping, k_scale: float, v_scale: float,
+                       stream=None) -> None:
+    """Quantise bf16 K/V rows [T, Hkv, D] to E4M3 codes and store them: K in
+    k_cache uint8 [NB, Hkv, B, D], V transposed in v_cache uint8 [NB, Hkv, D, B]
+    (code = e4m3(x / scale), nearest even, saturating)."""
+    lib = _lib.load()
+    NB, Hkv, B, D = k_cache.shape
+    T = k_new.shape[0]
+    if tuple(k_new.shape) != (T, Hkv, D) or k_new.shape != v_new.shape or \
+            tuple(v_cache.shape) != (NB, Hkv, D, B):
+        raise ValueError("shape mismatch between new tokens and FP8 caches")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping needs one entry per token")
+    st = lib.kv_cache_write_fp8(
+        _dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16),
+        _dev(k_cache, "k_cache", torch.uint8), _dev(v_cache, "v_cache", torch.uint8),
+        _dev(slot_mapping, "slot_mapping", torch.int64, 1), T, Hkv, D, B, NB,
+        float(k_scale), float(v_scale), _stream(stream))
+    _check(st, "kv_cache_write_fp8")
+
+
+def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, seq_lens, scale: float,
+                               k_scale: float, v_scale: float, max_seq_len: int,
+                               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention over an FP8 (E4M3) cache: K codes [NB, Hkv, B, D], V
+    codes transposed [NB, Hkv, D, B], values code * k_scale / code * v_scale.
+    q/out bf16 [S, Hq, D]; block_tables int32 [S, maxB]; seq_lens int32 [S]."""
+    lib = _lib.load()
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if Dk != D or tuple(out.shape) != (S, Hq, D) or tuple(v_cache.shape) != (NB, Hkv, D, B):
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables must be [S, maxB] and seq_lens [S]")
+    need = paged_attention_workspace_size(S, Hq, D, max_seq_len, 0)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.paged_attention_decode_fp8(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache", torch.uint8),
+        _dev(v_cache, "v_cache", torch.uint8), _dev(block_tables, "block_tables", torch.int32, 2),
+        _dev(seq_lens, "seq_lens", torch.int32, 1), S, Hq, Hkv, D, B, block_tables.shape[1], NB,
+        int(max_seq_len), float(scale), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "paged_attention_decode_fp8")
     return out
 
 

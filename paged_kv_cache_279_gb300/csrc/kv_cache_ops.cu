@@ -10,6 +10,7 @@
 // Both kernels move 16-byte vectors: consecutive threads own consecutive
 // 16-byte chunks of a K/V row (or of a whole physical block), so every warp
 // reads and writes fully coalesced 512-byte spans.
+#include <cmath>
 #include <mutex>
 
 #include "pkv_internal.cuh"
@@ -61,6 +62,68 @@ kv_cache_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__
         const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
         k_cache[dst] = k_new[i];
         v_cache[dst] = v_new[i];
+    }
+}
+
+// FP8 (E4M3) cache write.  One thread per 16 head_dim entries of one (token,
+// kv head): the K codes go out as one 16-byte row chunk; the V codes go to
+// the transposed V block ([D][block_size] per (block, kv head)), one byte per
+// head_dim row.  code = e4m3(fl32(x / scale)), nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void quantize16(const uint4 (&x)[2], float scale, uint32_t (&w)[4]) {
+    const uint32_t *e = reinterpret_cast<const uint32_t *>(x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bf16 pairs (4 values) -> 4 codes, low byte first
+        const uint32_t p0 = e[2 * i], p1 = e[2 * i + 1];
+        const float f0 = __fdiv_rn(__uint_as_float(p0 << 16), scale);
+        const float f1 = __fdiv_rn(__uint_as_float(p0 & 0xffff0000u), scale);
+        const float f2 = __fdiv_rn(__uint_as_float(p1 << 16), scale);
+        const float f3 = __fdiv_rn(__uint_as_float(p1 & 0xffff0000u), scale);
+        w[i] = e4m3x2(f0, f1) | (e4m3x2(f2, f3) << 16);
+    }
+}
+
+__global__ void __launch_bounds__(256)
+kv_cache_write_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                          unsigned char *__restrict__ k_cache, unsigned char *__restrict__ v_cache,
+                          const int64_t *__restrict__ slot_mapping, int64_t num_tokens, int num_kv_heads,
+                          int head_dim, int block_size, int64_t num_slots, float k_scale, float v_scale,
+                          unsigned int *err) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int chunks = head_dim / 16;
+    const int64_t per_token = (int64_t)num_kv_heads * chunks;
+    const int64_t total = num_tokens * per_token;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t t = i / per_token;
+        const int64_t r = i - t * per_token;
+        const int64_t h = r / chunks;
+        const int c = (int)(r - h * chunks);
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (r == 0) flag_error(err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / block_size;
+        const int off = (int)(slot - blk * block_size);
+        const int64_t bh = blk * num_kv_heads + h;
+        uint4 kx[2] = {k_new[2 * i], k_new[2 * i + 1]};
+        uint4 vx[2] = {v_new[2 * i], v_new[2 * i + 1]};
+        uint32_t kw[4], vw[4];
+        quantize16(kx, k_scale, kw);
+        quantize16(vx, v_scale, vw);
+        *reinterpret_cast<uint4 *>(k_cache + (bh * block_size + off) * head_dim + 16 * c) =
+            make_uint4(kw[0], kw[1], kw[2], kw[3]);
+        unsigned char *vcol = v_cache + (bh * head_dim + 16 * c) * block_size + off;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) vcol[(int64_t)j * block_size] = (unsigned char)(vw[j >> 2] >> (8 * (j & 3)));
     }
 }
 
@@ -130,6 +193,30 @@ PKV_API pkv_status kv_cache_write(const void *k_new, const void *v_new, void *k_
         (const uint4 *)k_new, (const uint4 *)v_new, (uint4 *)k_cache, (uint4 *)v_cache,
         slot_mapping, num_tokens, num_kv_heads, chunks, block_size,
         (int64_t)num_blocks * block_size, device_error_word());
+    return launch_status();
+}
+
+PKV_API pkv_status kv_cache_write_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                                      const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks, float k_scale,
+                                      float v_scale, void *stream) {
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_blocks < 1)
+        return PKV_ERR_INVALID;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID;
+    if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_INVALID;
+    const int64_t total = (int64_t)num_tokens * num_kv_heads * (head_dim / 16);
+    const int64_t blocks = (total + 255) / 256;
+    const unsigned grid = (unsigned)(blocks < 1048576 ? blocks : 1048576);
+    kv_cache_write_fp8_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+        (const uint4 *)k_new, (const uint4 *)v_new, (unsigned char *)k_cache, (unsigned char *)v_cache,
+        slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, (int64_t)num_blocks * block_size,
+        k_scale, v_scale, device_error_word());
     return launch_status();
 }
 

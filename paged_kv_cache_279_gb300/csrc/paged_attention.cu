@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 #include <climits>
@@ -71,6 +72,9 @@ struct DecodeArgs {
     int partition_size, max_parts;
     float scale;       // multiplies q.k
     float scale_log2;  // scale * log2(e), for the exp2 form of the softmax
+    float f8_kscale_log2;  // FP8 cache: scale * k_scale * log2(e)
+    float f8_vscale;       // FP8 cache: v_scale
+    int f8_bshift;         // FP8 cache: log2(block_size)
     unsigned int *err;
     // fused append: each sequence's new token [S][Hkv][D] goes to position
     // seq_lens[s] - 1 before it is attended (nullptr: no append)
@@ -596,8 +600,9 @@ constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended
 // Offsets are from the 1024-aligned base.
 struct StreamKLayout {
     int ring, bars, ycache, masks, prefix, toff, total;
-    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, bool grouped) {
-        ring = NW * NS * 2 * (D / 64) * kTile * 128;
+    // kv_bytes: bytes per cached element (2 for bf16, 1 for FP8)
+    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, bool grouped, int kv_bytes = 2) {
+        ring = NW * NS * 2 * D * kTile * kv_bytes;
         bars = ring;
         ycache = bars + NW * NS * 8;   // int2 per cached tile
         masks = ycache + kYCache * 8;  // valid-row mask per cached tile
@@ -699,11 +704,222 @@ __device__ __forceinline__ void issue_rows(const CUtensorMap *tm_k, const CUtens
     }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) cache.  K tiles are 16 token rows x D codes (128-byte swizzle);
+// V is stored transposed inside each block, so a V tile is D rows x 16 token
+// codes.  Codes widen exactly to f16 (every E4M3 value is an f16 value), the
+// queries are scaled by a power of two per head into f16's range, and both
+// contractions run as f16 mma.sync with fp32 accumulation; the scales (the
+// per-tensor k_scale and v_scale, the softmax scale, the query's power of
+// two) are applied to the fp32 results.
+// ---------------------------------------------------------------------------
+// Four E4M3 codes (bytes 0..3 of x) -> f16x2 {byte0, byte1} and {byte2, byte3}.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+// D += A(16x16, row) . B(16x8, col), f16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float f16x2_lo(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu)));
+}
+__device__ __forceinline__ float f16x2_hi(uint32_t v) {
+    return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+// Stage sizes of one 16-token tile (K then V) for either cache type.
+template <int D, bool F8>
+struct TileBytes {
+    static constexpr int kKV = F8 ? kTile * D : Bf16Layout<D>::kKVBytes;  // offset of V
+    static constexpr int kStage = 2 * kKV;
+};
+
+// Q^T as the f16 MMA B operand for the FP8 path.  The lane with g = lane/4,
+// t = lane%4 holds query head g, head_dim entries 16c + 4t .. 16c + 4t + 3 of
+// chunk c: that is the order in which the K fragment below receives the
+// codes, so the contraction pairs every key entry with its query entry.  Each
+// head is multiplied by 2^e so that its largest |q| lies in [2^14, 2^15)
+// (exact: bf16 has 8 significant bits, f16 11).  s0 / s1 return the score
+// factors scale * k_scale * log2(e) * 2^-e of heads 2t and 2t+1, the columns
+// of S^T this lane accumulates.
+template <int D>
+__device__ __forceinline__ void load_q_f16(const DecodeArgs &a, int seq, int kvh, int lane,
+                                           uint32_t (&qb)[D / 16][2], float &s0, float &s1) {
+    const int g = lane >> 2, t = lane & 3;
+    const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(a.q) +
+                                ((int64_t)seq * a.num_heads + kvh * a.group + g) * D;
+    uint2 w[D / 16];
+    float amax = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        w[c] = g < a.group ? *reinterpret_cast<const uint2 *>(qrow + 16 * c + 4 * t) : make_uint2(0u, 0u);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16x2_lo(w[c].x)), fabsf(bf16x2_hi(w[c].x))),
+                                 fmaxf(fabsf(bf16x2_lo(w[c].y)), fabsf(bf16x2_hi(w[c].y)))));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // amax in [2^(E-127), 2^(E-126)): multiply by 2^(141-E), biased exponent 268-E
+    const int E = (int)((__float_as_uint(amax) >> 23) & 0xffu);
+    const int fe = min(253, max(1, 268 - E));
+    const float f = __uint_as_float((uint32_t)fe << 23);
+    const float desc = a.f8_kscale_log2 * __uint_as_float((uint32_t)(254 - fe) << 23);
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+        qb[c][0] = pack_f16x2(bf16x2_lo(w[c].x) * f, bf16x2_hi(w[c].x) * f);
+        qb[c][1] = pack_f16x2(bf16x2_lo(w[c].y) * f, bf16x2_hi(w[c].y) * f);
+    }
+    s0 = __shfl_sync(0xffffffffu, desc, 8 * t);
+    s1 = __shfl_sync(0xffffffffu, desc, 8 * t + 4);
+}
+
+// FP8 counterpart of attend_tile: K tile at sk (16 x D codes, swizzled), V^T
+// tile at sv (D x 16 codes), per-column score factors s0 / s1.
+template <int D>
+__device__ __forceinline__ void attend_tile_f8(unsigned char *sk, unsigned char *sv, uint32_t row_ok,
+                                               const uint32_t (&qb)[D / 16][2], float s0, float s1,
+                                               WarpAcc<D> &acc, int lane) {
+    static_assert(D == 128, "FP8 tiles assume 128-byte K rows");
+    const int g = lane >> 2, t = lane & 3;
+    if (row_ok != 0xffffu) {
+        // masked tokens hold stale or unwritten codes (possibly NaN): clear
+        // their bytes in every V^T row so that a zero weight meets a zero
+        uint32_t m[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) m[w] = ((((row_ok >> (4 * w)) & 0xfu) * 0x00204081u) & 0x01010101u) * 0xffu;
+        for (int r = lane; r < D; r += 32) {
+            uint4 *p = reinterpret_cast<uint4 *>(sv + r * kTile);
+            uint4 v = *p;
+            v.x &= m[0];
+            v.y &= m[1];
+            v.z &= m[2];
+            v.w &= m[3];
+            *p = v;
+        }
+        __syncwarp();
+    }
+    const uint32_t ska = smem_u32(sk), sva = smem_u32(sv);
+    const int lj = lane >> 3, lr = lane & 7;
+    // ldmatrix rows: token lr (+8 for matrices 1 and 3), 16-byte chunk 2kk (+1 for matrices 2, 3)
+    const uint32_t krow = ska + (lr + 8 * (lj & 1)) * D;
+
+    // S^T (16 tokens x 8 heads) = K_tile . Q^T; a lane's 4 codes of a chunk are
+    // head_dim entries 4t..4t+3, split as the fragment's k pairs (2t, 2t+1) and
+    // (2t+8, 2t+9) -- the same split load_q_f16 gives the queries
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+        const int chunk = 2 * kk + (lj >> 1);
+        uint32_t x0, x1, x2, x3, a0, a1, a2, a3;
+        ldmatrix_x4(krow + ((chunk ^ lr) << 4), x0, x1, x2, x3);
+        e4m3x4_to_f16(x0, a0, a2);
+        e4m3x4_to_f16(x1, a1, a3);
+        mma_f16_16816(sc, a0, a1, a2, a3, qb[2 * kk][0], qb[2 * kk][1]);
+        e4m3x4_to_f16(x2, a0, a2);
+        e4m3x4_to_f16(x3, a1, a3);
+        mma_f16_16816(sc, a0, a1, a2, a3, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
+    }
+
+    // online softmax, base 2; rows g and g+8, columns 2t and 2t+1
+    const bool ok_lo = (row_ok >> g) & 1u, ok_hi = (row_ok >> (g + 8)) & 1u;
+    const float v0 = ok_lo ? sc[0] * s0 : -INFINITY;
+    const float v1 = ok_lo ? sc[1] * s1 : -INFINITY;
+    const float v2 = ok_hi ? sc[2] * s0 : -INFINITY;
+    const float v3 = ok_hi ? sc[3] * s1 : -INFINITY;
+    float mx0 = fmaxf(v0, v2), mx1 = fmaxf(v1, v3);
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+    }
+    const float mn0 = fmaxf(acc.m0, mx0), mn1 = fmaxf(acc.m1, mx1);
+    const float rf0 = mn0 == -INFINITY ? 0.f : mn0, rf1 = mn1 == -INFINITY ? 0.f : mn1;
+    const bool moved = __any_sync(0xffffffffu, mn0 != acc.m0 || mn1 != acc.m1);
+    const float al0 = exp2f(acc.m0 - rf0), al1 = exp2f(acc.m1 - rf1);
+    acc.m0 = mn0;
+    acc.m1 = mn1;
+    const uint32_t p01 = pack_f16x2(exp2f(v0 - rf0), exp2f(v1 - rf1));
+    const uint32_t p23 = pack_f16x2(exp2f(v2 - rf0), exp2f(v3 - rf1));
+    if (moved) {
+        acc.l0 = acc.l0 * al0;
+        acc.l1 = acc.l1 * al1;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            acc.o[mt][0] *= al0;
+            acc.o[mt][1] *= al1;
+            acc.o[mt][2] *= al0;
+            acc.o[mt][3] *= al1;
+        }
+    }
+    acc.l0 += f16x2_lo(p01) + f16x2_lo(p23);
+    acc.l1 += f16x2_hi(p01) + f16x2_hi(p23);
+
+    // P^T as the B operand of O^T += V^T . P^T.  A lane's V^T fragment holds
+    // tokens 4t..4t+3 of its head_dim row (k pairs (2t, 2t+1) = tokens 4t,
+    // 4t+1 and (2t+8, 2t+9) = tokens 4t+2, 4t+3), so P^T must hold the same
+    // tokens: after the transposes lane t' has tokens 2t', 2t'+1 (m0) and
+    // 8+2t', 9+2t' (m1) of its head; gather them from the lanes of that head.
+    const uint32_t m0 = movmatrix_trans(p01), m1 = movmatrix_trans(p23);
+    const int src = (lane & ~3) | (2 * (t & 1));
+    const uint32_t e0 = __shfl_sync(0xffffffffu, m0, src), e1 = __shfl_sync(0xffffffffu, m1, src);
+    const uint32_t f0 = __shfl_sync(0xffffffffu, m0, src + 1), f1 = __shfl_sync(0xffffffffu, m1, src + 1);
+    const uint32_t pb0 = t < 2 ? e0 : e1, pb1 = t < 2 ? f0 : f1;
+
+    // O^T (head_dim x 8 heads) += V^T tile . P^T; matrices of one ldmatrix.x4
+    // are head_dim rows 32j + 0..7, 8..15, 16..23, 24..31
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+        uint32_t x0, x1, x2, x3, a0, a1, a2, a3;
+        ldmatrix_x4(sva + (32 * j + lane) * kTile, x0, x1, x2, x3);
+        e4m3x4_to_f16(x0, a0, a2);
+        e4m3x4_to_f16(x1, a1, a3);
+        mma_f16_16816(acc.o[2 * j], a0, a1, a2, a3, pb0, pb1);
+        e4m3x4_to_f16(x2, a0, a2);
+        e4m3x4_to_f16(x3, a1, a3);
+        mma_f16_16816(acc.o[2 * j + 1], a0, a1, a2, a3, pb0, pb1);
+    }
+}
+
+// Gather one FP8 tile: K rows y0 .. y0+15 of the [blocks * Hkv * B][D] view and
+// the V^T box of 16 token columns x D rows of the [blocks * Hkv * D][B] view.
+// Tiles never straddle blocks (block_size is a multiple of 16).
+template <int D>
+__device__ __forceinline__ void issue_rows_f8(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                              unsigned char *stage, uint64_t *bar, int bshift, TileRows r) {
+    const uint32_t b = smem_u32(bar);
+    if (r.y0 < 0) {
+        mbar_arrive_expect_tx(bar, 0u);
+        return;
+    }
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * kTile * D));
+    const uint32_t dk = smem_u32(stage);
+    tma_load_2d(dk, tm_k, b, 0, r.y0);
+    const int bh = r.y0 >> bshift;  // block * Hkv + kv head
+    tma_load_2d(dk + kTile * D, tm_v, b, r.y0 - (bh << bshift), bh * D);
+}
+
 // Store a warp's result for the piece [pa, pb) of segment `seg`: the final
 // rows when the piece is the whole segment, otherwise partial slot j.
 template <int D>
 __device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc, bool empty,
-                                            const SegCursor &seg, bool whole, int j, int lane) {
+                                            const SegCursor &seg, bool whole, int j, int lane,
+                                            float oscale = 1.f) {
     const int r0 = lane >> 2, tq = lane & 3, G = a.group;
 #pragma unroll
     for (int sh = 4; sh < 32; sh <<= 1) {  // column sums over the 16 token rows
@@ -715,7 +931,7 @@ __device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc
         acc.l0 = acc.l1 = 0.f;
     }
     const int64_t row0 = (int64_t)seg.seq * a.num_heads + seg.kvh * G;
-    const float inv0 = acc.l0 > 0.f ? 1.f / acc.l0 : 0.f, inv1 = acc.l1 > 0.f ? 1.f / acc.l1 : 0.f;
+    const float inv0 = acc.l0 > 0.f ? oscale / acc.l0 : 0.f, inv1 = acc.l1 > 0.f ? oscale / acc.l1 : 0.f;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
 #pragma unroll
@@ -728,7 +944,7 @@ __device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc
                 store_out(static_cast<__nv_bfloat16 *>(a.out) + row * D + d,
                           acc.o[mt][jj] * ((jj & 1) ? inv1 : inv0));
             } else {
-                a.part_o[(row * a.max_parts + j) * D + d] = acc.o[mt][jj];
+                a.part_o[(row * a.max_parts + j) * D + d] = acc.o[mt][jj] * oscale;
             }
         }
     }
@@ -750,16 +966,20 @@ __device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc
 // head) ends inside a share, the warp stores its result for that piece -- the
 // final rows if the share holds the whole segment, otherwise a partial that
 // the merge kernel combines -- and carries on with the next segment.
-template <int D, int NW, int NS>
+//
+// F8: the cache holds E4M3 codes (K rows, V transposed per block); tiles are
+// attended by attend_tile_f8 and the queries are loaded by load_q_f16.  The
+// FP8 path has no fused append and no grouped (shared-prefix) mode.
+template <int D, int NW, int NS, bool F8 = false>
 __global__ void __launch_bounds__(NW * 32)
 decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-    using Lay = Bf16Layout<D>;
+    using Lay = TileBytes<D, F8>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const bool grouped = a.seq_tok0 != nullptr;
-    const StreamKLayout L(D, NW, NS, a.num_seqs, grouped);
+    const bool grouped = !F8 && a.seq_tok0 != nullptr;
+    const StreamKLayout L(D, NW, NS, a.num_seqs, grouped, F8 ? 1 : 2);
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + L.bars);
     int2 *ycache = reinterpret_cast<int2 *>(smem + L.ycache);
     uint32_t *mcache = reinterpret_cast<uint32_t *>(smem + L.masks);
@@ -853,6 +1073,11 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     int64_t r = lo;
     SegCursor seg;  // the segment being attended
     uint32_t qb[D / 16][2], qn[D / 16][2];
+    float qs0 = 0.f, qs1 = 0.f, qns0 = 0.f, qns1 = 0.f;  // FP8: score factors of qb / qn
+    auto load_q = [&](const SegCursor &c, uint32_t(&dst)[D / 16][2], float &f0, float &f1) {
+        if constexpr (F8) load_q_f16<D>(a, c.seq, c.kvh, lane, dst, f0, f1);
+        else load_q_fragments<D>(a, c.seq, c.kvh, lane, dst);
+    };
     bool qn_loaded = false;  // qn holds the second piece's queries
     // The queries of the first two pieces: fetched now, ahead of the burst of
     // tile loads that every warp issues after the staging below.
@@ -862,7 +1087,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (first_end < hi && first_end - lo < kRotateTiles && ncache == cta_hi - cta_lo) r = first_end;
         seg = seg_lo;
         if (r != lo) seg.advance_to(prefix, Hkv, r);
-        load_q_fragments<D>(a, seg.seq, seg.kvh, lane, qb);
+        load_q(seg, qb, qs0, qs1);
         const int64_t end1 = seg.seg_start + seg.n;  // the first piece ends at min(hi, end1)
         if (end1 < hi || r != lo) {
             SegCursor second = seg_lo;
@@ -870,7 +1095,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 second = seg;
                 second.advance_to(prefix, Hkv, end1);
             }
-            load_q_fragments<D>(a, second.seq, second.kvh, lane, qn);
+            load_q(second, qn, qns0, qns1);
             qn_loaded = true;
         }
     }
@@ -934,7 +1159,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             mcache[i] = r.mask | ((uint32_t)valid << 16);  // valid rows in bits 16..20
         }
     }
-    unsigned char *ring = smem + warp * NS * Lay::kStageBytes;
+    unsigned char *ring = smem + warp * NS * Lay::kStage;
     uint64_t *bars = bars_all + warp * NS;
     if (lane == 0) {
 #pragma unroll
@@ -948,7 +1173,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int ntiles = (int)(hi - lo);
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
 
-    if (a.k_new) {
+    if (!F8 && a.k_new) {
         // Fused append: the warp whose share holds a segment's last tile stores
         // that segment's new token (position len - 1) before any TMA reads it.
         // Only this warp ever reads that tile, so no other ordering is needed.
@@ -1023,7 +1248,10 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     auto issue = [&](int k, int buf) {
         const int64_t t = tile_at(k);
         if (t - cta_lo >= ncache) prod.advance_to(prefix, Hkv, t);
-        issue_rows<D>(&tm_k, &tm_v, ring + buf * Lay::kStageBytes, &bars[buf], boxh, rows_of(t, prod));
+        if constexpr (F8)
+            issue_rows_f8<D>(&tm_k, &tm_v, ring + buf * Lay::kStage, &bars[buf], a.f8_bshift, rows_of(t, prod));
+        else
+            issue_rows<D>(&tm_k, &tm_v, ring + buf * Lay::kStage, &bars[buf], boxh, rows_of(t, prod));
     };
     if (lane == 0) {
         for (int i = 0; i < NS && i < ntiles; ++i) issue(i, i);
@@ -1043,7 +1271,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int64_t tn = tile_at(kend);
             if (tn == pb) nxt.advance_to(prefix, Hkv, tn);
             else nxt = seg_lo;  // the walk wraps to lo
-            if (!qn_loaded) load_q_fragments<D>(a, nxt.seq, nxt.kvh, lane, qn);
+            if (!qn_loaded) load_q(nxt, qn, qns0, qns1);
             qn_loaded = false;
         }
         acc.reset();
@@ -1055,8 +1283,11 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
             if (dead) continue;
             const TileRows rw = rows_of(tile_at(k), seg);
-            unsigned char *sk = ring + buf * Lay::kStageBytes;
-            attend_tile<D>(sk, sk + Lay::kKVBytes, rw.mask, qb, a.scale_log2, acc, lane);
+            unsigned char *sk = ring + buf * Lay::kStage;
+            if constexpr (F8)
+                attend_tile_f8<D>(sk, sk + Lay::kKV, rw.mask, qb, qs0, qs1, acc, lane);
+            else
+                attend_tile<D>(sk, sk + Lay::kKV, rw.mask, qb, a.scale_log2, acc, lane);
             __syncwarp();
             if (lane == 0 && k + NS < ntiles) {
                 fence_proxy_async();
@@ -1066,7 +1297,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         // a grouped sequence's own part is always a partial: the prefix joins it in the merge
         const bool whole = pa == seg.seg_start && pb == seg_end && !(grouped && toff[seg.seq] > 0);
         const int64_t w0 = share_owner(seg.seg_start, T, parts);
-        store_piece<D>(a, acc, dead, seg, whole, (int)(gw - w0), lane);
+        store_piece<D>(a, acc, dead, seg, whole, (int)(gw - w0), lane, F8 ? a.f8_vscale : 1.f);
         if (lane == 0 && pa == seg.seg_start) {
             // the warp holding a segment's first tile records its number of pieces
             const int64_t w1 = share_owner(seg_end - 1, T, parts);
@@ -1079,6 +1310,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             qb[ks][0] = qn[ks][0];
             qb[ks][1] = qn[ks][1];
         }
+        qs0 = qns0;
+        qs1 = qns1;
     }
 }
 
@@ -2212,6 +2445,56 @@ static pkv_status dispatch_balanced(const DecodeArgs &a, cudaStream_t st) {
     }
 }
 
+// FP8 cache views.  K: [blocks * Hkv * B][D] bytes, box D x 16 rows, 128-byte
+// swizzle.  V (transposed per block): [blocks * Hkv * D][B] bytes, box 16
+// token columns x D rows, unswizzled (a row of the box is one 16-byte vector).
+static bool make_f8_maps(const DecodeArgs &a, int D, CUtensorMap *mk, CUtensorMap *mv) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t nbh = (int64_t)a.num_blocks * a.num_kv_heads;
+    cuuint32_t estr[2] = {1u, 1u};
+    cuuint64_t kdims[2] = {(cuuint64_t)D, (cuuint64_t)(nbh * a.block_size)};
+    cuuint64_t kstr[1] = {(cuuint64_t)D};
+    cuuint32_t kbox[2] = {(cuuint32_t)D, (cuuint32_t)kTile};
+    if (enc(mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(a.k_cache), kdims, kstr, kbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    cuuint64_t vdims[2] = {(cuuint64_t)a.block_size, (cuuint64_t)(nbh * D)};
+    cuuint64_t vstr[1] = {(cuuint64_t)a.block_size};
+    cuuint32_t vbox[2] = {(cuuint32_t)kTile, (cuuint32_t)D};
+    return enc(mv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(a.v_cache), vdims, vstr, vbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int NW, int NS>
+static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
+    static bool done[128] = {};
+    auto kern = decode_bf16_streamk_kernel<D, NW, NS, true>;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, false, 1).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, false, 1).total;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
+        per_sm < 1)
+        return PKV_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms < 1) return PKV_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!make_f8_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
+    return launch_pdl(kern, dim3((unsigned)(sms * per_sm)), dim3(NW * 32), smem, st, mk, mv, a);
+}
+
+static pkv_status dispatch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
+    static const int v = env_variant("PKV_FP8_VARIANT");
+    switch (v) {
+        case 1: return launch_balanced_f8<128, 4, 2>(a, st);
+        case 2: return launch_balanced_f8<128, 4, 3>(a, st);
+        case 3: return launch_balanced_f8<128, 8, 4>(a, st);
+        default: return launch_balanced_f8<128, 4, 4>(a, st);
+    }
+}
+
 template <typename T, int D>
 static pkv_status dispatch_simt(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
     return launch_pdl(decode_simt_kernel<T, D, 4>, grid, dim3(128), 0, st, a);
@@ -2356,6 +2639,73 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
             rc = head_dim == 128 ? launch_reduce<float, 128, false, false>(a, st)
                                  : launch_reduce<float, 64, false, false>(a, st);
     }
+    return rc;
+}
+
+PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_tables,
+                                              const int32_t *seq_lens, int num_seqs, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                              float scale, float k_scale, float v_scale, void *workspace,
+                                              size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        max_seq_len < 0 || !std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale) ||
+        !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
+    if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > kGMax) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > kMaxBalancedSeqs) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PKV_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
+    // TMA row coordinates are 32-bit: K rows (block, head, token) and V^T rows (block, head, dim)
+    if (((int64_t)num_blocks + 1) * num_kv_heads * std::max(block_size, head_dim) > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
+        return PKV_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (max_seq_len == 0)  // every context is empty: all-zero rows
+        return cudaMemsetAsync(out, 0, (size_t)num_seqs * num_heads * head_dim * 2, st) == cudaSuccess
+                   ? PKV_OK : PKV_ERR_CUDA;
+    const int64_t slots = balanced_slots(max_seq_len);
+    const WorkspaceLayout lay = workspace_layout(num_seqs, num_heads, head_dim, slots, true);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_INVALID;
+
+    DecodeArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.partition_size = kDefaultPartition;
+    a.scale = scale;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.f8_kscale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+    a.f8_vscale = v_scale;
+    a.f8_bshift = block_size == 16 ? 4 : 5;
+    a.err = device_error_word();
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
+    a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
+    a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
+    a.pieces = reinterpret_cast<int *>(ws + lay.pieces_off);
+    a.max_parts = (int)slots;
+    pkv_status rc = dispatch_balanced_f8(a, st);
+    if (rc == PKV_OK) rc = launch_reduce<__nv_bfloat16, 128, true, true>(a, st);
     return rc;
 }
 

@@ -69,6 +69,31 @@ def test_host_validation_rejects_before_launch():
     del flags
 
 
+def test_fp8_host_validation_rejects_before_launch():
+    lib = _lib.load()
+    w = lib.kv_cache_write_fp8
+    assert w(None, None, None, None, None, 4, 8, 64, 16, 64, 0.1, 0.1, None) == pkv.PKV_ERR_UNSUPPORTED   # D 64
+    assert w(None, None, None, None, None, 4, 8, 128, 8, 64, 0.1, 0.1, None) == pkv.PKV_ERR_UNSUPPORTED   # B 8
+    assert w(None, None, None, None, None, 4, 8, 128, 16, 64, 0.0, 0.1, None) == pkv.PKV_ERR_INVALID      # scale 0
+    assert w(None, None, None, None, None, 4, 8, 128, 16, 64, 0.1, float("inf"), None) == pkv.PKV_ERR_INVALID
+    assert w(None, None, None, None, None, 4, 8, 128, 16, 64, 0.1, 0.1, None) == pkv.PKV_ERR_INVALID      # null
+    assert w(None, None, None, None, None, 0, 8, 128, 32, 64, 0.1, 0.1, None) == pkv.PKV_OK
+
+    def dec(S=2, Hq=32, Hkv=8, D=128, B=16, maxB=4, NB=16, maxL=64, scale=0.1, ks=0.05, vs=0.05):
+        return lib.paged_attention_decode_fp8(None, None, None, None, None, None, S, Hq, Hkv, D, B, maxB,
+                                              NB, maxL, scale, ks, vs, None, 0, None)
+    assert dec(D=64) == pkv.PKV_ERR_UNSUPPORTED
+    assert dec(B=8) == pkv.PKV_ERR_UNSUPPORTED
+    assert dec(Hq=72) == pkv.PKV_ERR_UNSUPPORTED       # 9 query heads per KV head
+    assert dec(S=9000) == pkv.PKV_ERR_UNSUPPORTED      # more sequences than the balanced scan holds
+    assert dec(Hq=30) == pkv.PKV_ERR_INVALID
+    assert dec(ks=-1.0) == pkv.PKV_ERR_INVALID
+    assert dec(vs=float("nan")) == pkv.PKV_ERR_INVALID
+    assert dec(scale=float("inf")) == pkv.PKV_ERR_INVALID
+    assert dec(S=0) == pkv.PKV_OK
+    assert dec() == pkv.PKV_ERR_INVALID                # null pointers
+
+
 def test_workspace_size_formula():
     lib = _lib.load()
     # a single partition needs no scratch

@@ -1,0 +1,203 @@
+"""GPU parity of the FP8 (E4M3) KV cache against the oracle.
+
+kv_cache_write_fp8 must produce the oracle's codes bit for bit (the rounding
+decision is taken in float32 on both sides: the IEEE quotient x / scale, then
+nearest-even E4M3 with saturation).  paged_attention_decode_fp8 must match the
+fp64 oracle's attention over the dequantised cache (code value x scale)
+within the bf16 output tolerance.  Slots that no sequence owns hold NaN codes,
+so any read of a masked token shows up as a non-finite output.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8_e4m3 as f8
+import paged_kv_cache_279_gb300 as pkv
+from paged_kv_cache_279_gb300 import workloads as wl
+from harness import assert_bf16_close, token_slots
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+K_SCALE, V_SCALE = 1.0 / 32, 1.0 / 40
+
+
+def _pool_with_codes(lens, Hkv, B, seed, extra_blocks=3, fill=0x7F):
+    """Random E4M3 codes per sequence placed at random physical blocks: K rows
+    at [blk, h, off, :], V columns at [blk, h, :, off]; unowned slots = fill."""
+    counts = [-(-L // B) for L in lens]
+    NB = max(1, sum(counts) + extra_blocks)
+    maxB = max(1, max(counts))
+    tables = wl.random_block_tables(counts, NB, maxB, seed + 1)
+    kc = np.full((NB, Hkv, B, D), fill, dtype=np.uint8)
+    vc = np.full((NB, Hkv, D, B), fill, dtype=np.uint8)
+    kq, vq = [], []
+    for s, L in enumerate(lens):
+        k = wl.draw_e4m3_codes((L, Hkv, D), wl.sub_seed(seed, 10, s))
+        v = wl.draw_e4m3_codes((L, Hkv, D), wl.sub_seed(seed, 11, s))
+        kq.append(k)
+        vq.append(v)
+        if L:
+            slots = token_slots(tables[s], L, B)
+            kc[slots // B, :, slots % B, :] = k
+            vc[slots // B, :, :, slots % B] = v  # advanced indices first: [L, Hkv, D]
+    return dict(kc=kc, vc=vc, kq=kq, vq=vq, tables=tables, NB=NB)
+
+
+def _run(pool, q, lens, scale, max_seq_len=None):
+    dev = "cuda"
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    pkv.paged_attention_decode_fp8(
+        out, q.to(dev), torch.from_numpy(pool["kc"]).to(dev), torch.from_numpy(pool["vc"]).to(dev),
+        torch.from_numpy(pool["tables"]).to(dev), torch.tensor(lens, dtype=torch.int32, device=dev),
+        scale, K_SCALE, V_SCALE, max_seq_len or max(1, max(lens)))
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def _oracle(pool, q, scale):
+    ks = [f8.dequantize(k, K_SCALE) for k in pool["kq"]]
+    vs = [f8.dequantize(v, V_SCALE) for v in pool["vq"]]
+    return oracle.decode_attention(q.float().numpy(), ks, vs, scale)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (64, 8), (12, 4)])
+@pytest.mark.parametrize("B", [16, 32])
+def test_decode_fp8_matches_oracle(Hq, Hkv, B):
+    lens = [1, 17, 100, 0, 16, 2048, 513, 33, 255, 1000]
+    shape = wl.DecodeShape("fp8", len(lens), Hq, Hkv, D, B, torch.bfloat16)
+    pool = _pool_with_codes(lens, Hkv, B, seed=Hq * 7 + B)
+    q = wl.draw_query(shape, seed=B + Hq)
+    got = _run(pool, q, lens, shape.scale)
+    assert_bf16_close(got, _oracle(pool, q, shape.scale), f"fp8 decode Hq={Hq} Hkv={Hkv} B={B}")
+    assert torch.all(got[3] == 0)  # empty context: zero rows
+    assert pkv.read_device_errors() == 0
+
+
+def test_decode_fp8_full_gqa_workload():
+    """The GQA decode workload (64 sequences, lengths uniform in [64, 2048],
+    32 query / 8 KV heads, block 16) on an FP8 cache, every output checked."""
+    shape = wl.GQA_BF16
+    lens = wl.draw_lengths(shape, seed=3).tolist()
+    pool = _pool_with_codes(lens, shape.num_kv_heads, shape.block_size, seed=3,
+                            extra_blocks=sum(-(-L // 16) for L in lens) // 10)
+    q = wl.draw_query(shape, seed=3)
+    got = _run(pool, q, lens, shape.scale)
+    assert_bf16_close(got, _oracle(pool, q, shape.scale), "fp8 GQA workload")
+
+
+def test_decode_fp8_long_contexts_and_permutation_invariance():
+    lens = [16000, 12345, 7]
+    Hkv, B = 8, 16
+    shape = wl.DecodeShape("fp8_long", len(lens), 32, Hkv, D, B, torch.bfloat16)
+    pool = _pool_with_codes(lens, Hkv, B, seed=21)
+    q = wl.draw_query(shape, seed=21)
+    got = _run(pool, q, lens, shape.scale)
+    assert_bf16_close(got, _oracle(pool, q, shape.scale), "fp8 long contexts")
+    # move every block to another physical id: bit-identical output
+    perm = np.random.default_rng(5).permutation(pool["NB"])
+    moved = dict(pool)
+    moved["kc"] = np.empty_like(pool["kc"])
+    moved["vc"] = np.empty_like(pool["vc"])
+    moved["kc"][perm] = pool["kc"]
+    moved["vc"][perm] = pool["vc"]
+    t = pool["tables"]
+    moved["tables"] = np.where(t >= 0, perm[np.maximum(t, 0)], t).astype(np.int32)
+    assert torch.equal(_run(moved, q, lens, shape.scale).view(torch.int16), got.view(torch.int16))
+
+
+def test_decode_fp8_single_token_returns_its_value():
+    lens = [1, 1]
+    Hkv, B = 2, 16
+    shape = wl.DecodeShape("fp8_one", 2, 8, Hkv, D, B, torch.bfloat16)
+    pool = _pool_with_codes(lens, Hkv, B, seed=4)
+    q = wl.draw_query(shape, seed=4)
+    got = _run(pool, q, lens, shape.scale).double().numpy()
+    for s in range(2):
+        v = f8.dequantize(pool["vq"][s][0], V_SCALE)  # [Hkv, D]
+        want = np.repeat(v, 4, axis=0)
+        assert np.all(np.abs(got[s] - want) <= np.maximum(np.abs(want) * 2.0 ** -8, 1e-6))
+
+
+def _bf16_tokens(T, Hkv, seed):
+    k = wl.draw_normal((T, Hkv, D), torch.bfloat16, seed)
+    v = wl.draw_normal((T, Hkv, D), torch.bfloat16, seed + 1)
+    return k, v
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_write_fp8_bit_exact(B):
+    T, Hkv, NB = 300, 8, 40
+    k, v = _bf16_tokens(T, Hkv, 31 + B)
+    # specials: ties, subnormal-range values, saturation, zeros of both signs
+    specials = torch.tensor([1.0625, 1.1875, 2.0 ** -10 / 32, -0.0, 0.0, 432.0 / 32, 1e4, -1e4,
+                             float("inf"), float("-inf"), 1.5 * 2.0 ** -9 / 32, 7.5 * 2.0 ** -9 / 32],
+                            dtype=torch.bfloat16)
+    k[0, 0, :specials.numel()] = specials
+    v[1, 3, -specials.numel():] = specials
+    rng = np.random.default_rng(B)
+    slots = rng.choice(NB * B, size=T, replace=False).astype(np.int64)
+    slots[::17] = -1  # padding tokens
+    kc0 = wl.draw_e4m3_codes((NB, Hkv, B, D), 91)
+    vc0 = wl.draw_e4m3_codes((NB, Hkv, D, B), 92)
+    kc, vc = torch.from_numpy(kc0).cuda(), torch.from_numpy(vc0).cuda()
+    pkv.kv_cache_write_fp8(k.cuda(), v.cuda(), kc, vc, torch.from_numpy(slots).cuda(), K_SCALE, V_SCALE)
+    torch.cuda.synchronize()
+    want_k, want_v = kc0.copy(), vc0.copy()
+    f8.kv_cache_write_fp8(want_k, want_v, k.float().numpy(), v.float().numpy(), slots, B, K_SCALE, V_SCALE)
+    assert np.array_equal(kc.cpu().numpy(), want_k)
+    assert np.array_equal(vc.cpu().numpy(), want_v)
+    assert pkv.read_device_errors() == 0
+
+
+def test_write_fp8_nan_gives_a_nan_code_and_bad_slots_are_flagged():
+    Hkv, B, NB = 2, 16, 4
+    k, v = _bf16_tokens(3, Hkv, 7)
+    k[0, 1, 5] = float("nan")
+    kc = torch.zeros((NB, Hkv, B, D), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros((NB, Hkv, D, B), dtype=torch.uint8, device="cuda")
+    pkv.read_device_errors()
+    slots = torch.tensor([3, NB * B + 5, 40], dtype=torch.int64, device="cuda")
+    pkv.kv_cache_write_fp8(k.cuda(), v.cuda(), kc, vc, slots, 0.5, 0.5)
+    torch.cuda.synchronize()
+    assert (int(kc[0, 1, 3, 5]) & 0x7F) == 0x7F
+    assert pkv.read_device_errors() & 4  # PKV_DEVERR_SLOT
+    # the out-of-range token wrote nothing: only tokens 0 and 2 are present
+    assert int((kc != 0).sum()) <= 2 * Hkv * D
+
+
+def test_write_then_decode_end_to_end():
+    """bf16 K/V written through kv_cache_write_fp8, attended by
+    paged_attention_decode_fp8; the oracle quantises the same bf16 values
+    itself.  Also reports the quantisation error against bf16 attention."""
+    lens = [300, 64, 1, 1777]
+    Hq, Hkv, B = 32, 8, 16
+    shape = wl.DecodeShape("fp8_e2e", len(lens), Hq, Hkv, D, B, torch.bfloat16)
+    counts = [-(-L // B) for L in lens]
+    NB = sum(counts) + 5
+    tables = wl.random_block_tables(counts, NB, max(counts), 77)
+    ks, vs = zip(*[wl.draw_seq_kv(shape, 77, s, L) for s, L in enumerate(lens)])
+    slots = np.concatenate([token_slots(tables[s], L, B) for s, L in enumerate(lens)])
+    kc = torch.full((NB, Hkv, B, D), 0x7F, dtype=torch.uint8, device="cuda")
+    vc = torch.full((NB, Hkv, D, B), 0x7F, dtype=torch.uint8, device="cuda")
+    pkv.kv_cache_write_fp8(torch.cat(ks).cuda(), torch.cat(vs).cuda(), kc, vc,
+                           torch.from_numpy(slots).cuda(), K_SCALE, V_SCALE)
+    q = wl.draw_query(shape, 77)
+    out = torch.empty((len(lens), Hq, D), dtype=torch.bfloat16, device="cuda")
+    pkv.paged_attention_decode_fp8(out, q.cuda(), kc, vc, torch.from_numpy(tables).cuda(),
+                                   torch.tensor(lens, dtype=torch.int32, device="cuda"), shape.scale,
+                                   K_SCALE, V_SCALE, max(lens))
+    torch.cuda.synchronize()
+    kd = [f8.dequantize(f8.quantize(k.float().numpy(), K_SCALE), K_SCALE) for k in ks]
+    vd = [f8.dequantize(f8.quantize(v.float().numpy(), V_SCALE), V_SCALE) for v in vs]
+    ref = oracle.decode_attention(q.float().numpy(), kd, vd, shape.scale)
+    assert_bf16_close(out.cpu(), ref, "fp8 write + decode")
+    # the price of the 8-bit cache (not a parity bound): distance to bf16 attention
+    exact = oracle.decode_attention(q.float().numpy(), [k.float().numpy() for k in ks],
+                                    [v.float().numpy() for v in vs], shape.scale)
+    qerr = np.abs(out.cpu().double().numpy() - exact)
+    print(f"fp8 cache vs bf16 cache: max abs {qerr.max():.3e}, mean abs {qerr.mean():.3e}")
+    assert qerr.mean() < 0.05
