@@ -61,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa")
     p.add_argument("--block-size", type=int, default=0, help="override the block size (mixed sweep)")
     p.add_argument("--partition-size", type=int, default=0)
+    p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                   help="cache element type: bf16, or E4M3 codes with per-tensor scales")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -178,27 +180,35 @@ def shape_for(args) -> wl.DecodeShape:
     return shape
 
 
-def kv_bytes(lens, shape) -> int:
-    """Unique K and V bytes one attention pass reads (every cached token once)."""
-    elt = torch.tensor([], dtype=shape.dtype).element_size()
+# per-tensor scales of the FP8 cache: N(0, 1) data stays below 448 * scale
+FP8_K_SCALE = FP8_V_SCALE = 1.0 / 64
+
+
+def kv_bytes(lens, shape, kv_elt=None) -> int:
+    """Unique K and V bytes one attention pass reads (every cached token once);
+    kv_elt = bytes per cached element (default: the workload's dtype)."""
+    elt = kv_elt or torch.tensor([], dtype=shape.dtype).element_size()
     return int(sum(int(x) for x in lens)) * shape.num_kv_heads * shape.head_dim * 2 * elt
 
 
-def algorithmic_decode_bytes(lens, shape) -> int:
+def algorithmic_decode_bytes(lens, shape, kv_elt=None) -> int:
     """Bytes one paged_attention_decode call must move: the K/V of every cached
     token, the query and output rows, the block-table entries and lengths."""
     elt = torch.tensor([], dtype=shape.dtype).element_size()
     S = len(lens)
     blocks = sum(-(-int(x) // shape.block_size) for x in lens)
     qo = 2 * S * shape.num_heads * shape.head_dim * elt
-    return kv_bytes(lens, shape) + qo + 4 * blocks + 4 * S
+    return kv_bytes(lens, shape, kv_elt) + qo + 4 * blocks + 4 * S
 
 
 class Batch:
     """One resident decode batch: pool, allocator, tables and step inputs."""
 
-    def __init__(self, pkv, shape, lens, seed, device, partition_size, reserve_tokens=0):
+    kv = "bf16"
+
+    def __init__(self, pkv, shape, lens, seed, device, partition_size, reserve_tokens=0, kv="bf16"):
         B = shape.block_size
+        self.kv = kv
         self.shape = shape
         self.device = device
         self.lens = [int(x) for x in lens]
@@ -216,8 +226,12 @@ class Batch:
         g = torch.Generator(device=device)
         g.manual_seed(int(wl.sub_seed(seed, 9)))
         Hkv, D = shape.num_kv_heads, shape.head_dim
-        self.k_cache = torch.zeros((self.num_blocks, Hkv, B, D), dtype=shape.dtype, device=device)
-        self.v_cache = torch.zeros_like(self.k_cache)
+        if kv == "fp8":  # E4M3 codes; V transposed inside each block
+            self.k_cache = torch.zeros((self.num_blocks, Hkv, B, D), dtype=torch.uint8, device=device)
+            self.v_cache = torch.zeros((self.num_blocks, Hkv, D, B), dtype=torch.uint8, device=device)
+        else:
+            self.k_cache = torch.zeros((self.num_blocks, Hkv, B, D), dtype=shape.dtype, device=device)
+            self.v_cache = torch.zeros_like(self.k_cache)
         # the context before this step: written through the library
         for s, L in enumerate(self.lens):
             assert self.alloc.add_seq(s, L - 1) == 0
@@ -225,10 +239,14 @@ class Batch:
                 slots = torch.from_numpy(self.alloc.slots(s, 0, L - 1)).to(device)
                 k = torch.randn((L - 1, Hkv, D), generator=g, device=device).to(shape.dtype)
                 v = torch.randn((L - 1, Hkv, D), generator=g, device=device).to(shape.dtype)
-                pkv.kv_cache_write(k, v, self.k_cache, self.v_cache, slots)
+                if kv == "fp8":
+                    pkv.kv_cache_write_fp8(k, v, self.k_cache, self.v_cache, slots, FP8_K_SCALE, FP8_V_SCALE)
+                else:
+                    pkv.kv_cache_write(k, v, self.k_cache, self.v_cache, slots)
         self._finish(pkv, g, np.arange(S, dtype=np.int64), partition_size)
-        self.unique_bytes = kv_bytes(self.lens, shape)
-        self.alg_bytes = algorithmic_decode_bytes(self.lens, shape)
+        elt = 1 if kv == "fp8" else None
+        self.unique_bytes = kv_bytes(self.lens, shape, elt)
+        self.alg_bytes = algorithmic_decode_bytes(self.lens, shape, elt)
 
     def _finish(self, pkv, g, seq_ids, partition_size):
         """This step's new token for every sequence: slots from the allocator
@@ -317,9 +335,18 @@ class Batch:
     group_offsets = None
 
     def write(self):
+        if self.kv == "fp8":
+            self.pkv.kv_cache_write_fp8(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slot_mapping,
+                                        FP8_K_SCALE, FP8_V_SCALE)
+            return
         self.pkv.kv_cache_write(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slot_mapping)
 
     def decode(self):
+        if self.kv == "fp8":
+            self.pkv.paged_attention_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                                self.seq_lens, self.shape.scale, FP8_K_SCALE, FP8_V_SCALE,
+                                                self.max_seq_len, self.workspace)
+            return
         if self.group_offsets is not None:
             self.pkv.paged_attention_decode_grouped(self.out, self.q, self.k_cache, self.v_cache,
                                                     self.block_tables, self.seq_lens, self.group_offsets,
@@ -332,7 +359,12 @@ class Batch:
 
     def step(self):
         """Store every sequence's new token and attend: one library call
-        (grouped by shared prefix for beam search)."""
+        (grouped by shared prefix for beam search); with an FP8 cache the
+        quantising write, then the FP8 decode."""
+        if self.kv == "fp8":
+            self.write()
+            self.decode()
+            return
         if self.group_offsets is not None:
             self.pkv.paged_attention_decode_grouped(self.out, self.q, self.k_cache, self.v_cache,
                                                     self.block_tables, self.seq_lens, self.group_offsets,
@@ -353,6 +385,8 @@ class Batch:
                                                      self.max_seq_len, self.partition_size)
         if self.group_offsets is not None:
             return 3  # prefix kernel, attention kernel, merge
+        if self.kv == "fp8":
+            return 3  # quantising write, attention kernel, merge
         fused = self.partition_size == 0 and self.shape.dtype == torch.bfloat16
         return 1 + (1 if ws > 0 else 0) + (0 if fused else 1)
 
@@ -388,28 +422,38 @@ def time_graph(graph, stream, repeats=1):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_sample(shape, seed, budget_s, lens):
+def oracle_sample(shape, seed, budget_s, lens, kv="bf16"):
     """Time the fp64 oracle, as it stands, on one freshly drawn batch of the
     same workload (context lengths `lens`), repeating the call until about
-    `budget_s` seconds of work.  Returns (GB/s, cores, description, seconds,
-    calls)."""
+    `budget_s` seconds of work.  With an FP8 cache each call dequantises the
+    E4M3 codes first.  Returns (GB/s, cores, description, seconds, calls)."""
     import oracle
+    from oracle import fp8_e4m3
     cores = oracle.max_threads()
     q = wl.draw_query(shape, seed + 1, num_seqs=len(lens)).float().numpy()
     ks, vs = [], []
     for i, L in enumerate(lens):
-        k, v = wl.draw_seq_kv(shape, seed + 1, i, L)
-        ks.append(k.float().numpy())
-        vs.append(v.float().numpy())
+        if kv == "fp8":
+            shp = (L, shape.num_kv_heads, shape.head_dim)
+            ks.append(wl.draw_e4m3_codes(shp, wl.sub_seed(seed + 1, 10, i)))
+            vs.append(wl.draw_e4m3_codes(shp, wl.sub_seed(seed + 1, 11, i)))
+        else:
+            k, v = wl.draw_seq_kv(shape, seed + 1, i, L)
+            ks.append(k.float().numpy())
+            vs.append(v.float().numpy())
     done_s, calls = 0.0, 0
     while done_s < budget_s and calls < 1000:
         t0 = time.perf_counter()
-        oracle.decode_attention(q, ks, vs, shape.scale)
+        if kv == "fp8":
+            oracle.decode_attention(q, [fp8_e4m3.dequantize(k, FP8_K_SCALE) for k in ks],
+                                    [fp8_e4m3.dequantize(v, FP8_V_SCALE) for v in vs], shape.scale)
+        else:
+            oracle.decode_attention(q, ks, vs, shape.scale)
         done_s += time.perf_counter() - t0
         calls += 1
-    gbs = calls * kv_bytes(lens, shape) / done_s / 1e9
-    desc = (f"fp64 oracle, {calls} call(s) over one {len(lens)}-sequence batch of the "
-            f"{shape.name} workload, {cores} threads, {done_s:.1f} s")
+    gbs = calls * kv_bytes(lens, shape, 1 if kv == "fp8" else None) / done_s / 1e9
+    desc = (f"fp64 oracle{' (E4M3 codes dequantised per call)' if kv == 'fp8' else ''}, {calls} call(s) "
+            f"over one {len(lens)}-sequence batch of the {shape.name} workload, {cores} threads, {done_s:.1f} s")
     return gbs, cores, desc, done_s, calls
 
 
@@ -425,16 +469,27 @@ def run_reference(args):
     cores = oracle.max_threads()
     times, bytes_ = [], []
     q = wl.draw_query(shape, args.seed + 1, num_seqs=len(lens)).float().numpy()
-    kv = [tuple(t.float().numpy() for t in wl.draw_seq_kv(shape, args.seed + 1, s, L))
-          for s, L in enumerate(lens)]
+    fp8 = args.kv == "fp8"
+    if fp8:
+        from oracle import fp8_e4m3
+        shp = lambda L: (L, shape.num_kv_heads, shape.head_dim)  # noqa: E731
+        kv = [(wl.draw_e4m3_codes(shp(L), wl.sub_seed(args.seed + 1, 10, s)),
+               wl.draw_e4m3_codes(shp(L), wl.sub_seed(args.seed + 1, 11, s))) for s, L in enumerate(lens)]
+    else:
+        kv = [tuple(t.float().numpy() for t in wl.draw_seq_kv(shape, args.seed + 1, s, L))
+              for s, L in enumerate(lens)]
     for i in range(args.warmup + args.steps):
         idx = [((i * per_step) + j) % len(lens) for j in range(per_step)]
         t0 = time.perf_counter()
-        oracle.decode_attention(q[idx], [kv[s][0] for s in idx], [kv[s][1] for s in idx], shape.scale)
+        if fp8:  # the oracle dequantises the codes, then attends
+            oracle.decode_attention(q[idx], [fp8_e4m3.dequantize(kv[s][0], FP8_K_SCALE) for s in idx],
+                                    [fp8_e4m3.dequantize(kv[s][1], FP8_V_SCALE) for s in idx], shape.scale)
+        else:
+            oracle.decode_attention(q[idx], [kv[s][0] for s in idx], [kv[s][1] for s in idx], shape.scale)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
-            bytes_.append(kv_bytes([lens[s] for s in idx], shape))
+            bytes_.append(kv_bytes([lens[s] for s in idx], shape, 1 if fp8 else None))
     total_s = sum(times)
     value = sum(bytes_) / total_s / 1e9
     line = {
@@ -453,8 +508,9 @@ def run_reference(args):
 
 
 def config_of(shape, args, S):
+    kv = (f", E4M3 cache (k/v scale {FP8_K_SCALE:g})" if getattr(args, "kv", "bf16") == "fp8" else "")
     return {"workload": f"{shape.name}: {S} seqs, {shape.num_heads}q/{shape.num_kv_heads}kv heads, "
-                        f"head_dim {shape.head_dim}, block {shape.block_size}",
+                        f"head_dim {shape.head_dim}, block {shape.block_size}{kv}",
             "num_seqs": S, "num_heads": shape.num_heads, "num_kv_heads": shape.num_kv_heads,
             "head_dim": shape.head_dim, "block_size": shape.block_size,
             "partition_size": args.partition_size or "auto",
@@ -475,6 +531,7 @@ def run_ours(args):
     batches = []
     for r in range(nrot):
         batches.append(make_batch(pkv, shape, args, seed + r, device))
+    elt = 1 if args.kv == "fp8" else None
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device)
     steps, warmup = args.steps, max(3, args.warmup)
@@ -495,7 +552,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(world)
     bytes_per = [b.unique_bytes for b in batches]
-    logical_per = [kv_bytes(b.lens, shape) for b in batches]
+    logical_per = [kv_bytes(b.lens, shape, elt) for b in batches]
     step_bytes = sum(bytes_per[i % nrot] for i in range(steps))
     local_s = step_total_ms / 1e3
     total_s = max_over_ranks(local_s, world, device)
@@ -520,7 +577,8 @@ def run_ours(args):
     achieved = dec_alg_bytes / (dec_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
-                "kernel": "paged_attention_decode (attention kernel + merge kernel)",
+                "kernel": ("paged_attention_decode_fp8" if args.kv == "fp8" else "paged_attention_decode")
+                          + " (attention kernel + merge kernel)",
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
                 "decode_us": round(dec_ms * 1e3, 2)}
 
@@ -530,7 +588,7 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, desc, secs, _ = oracle_sample(shape, seed, args.cpu_budget,
-                                                  context_lengths(args, shape, seed + 1))
+                                                  context_lengths(args, shape, seed + 1), kv=args.kv)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": desc}
     if rank == 0:
@@ -538,7 +596,8 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if shape.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "dtype": ("e4m3" if args.kv == "fp8" else "bf16") if shape.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic",
             "config": config_of(shape, args, len(batches[0].lens)),
             "decode_tokens_per_s": round(tokens_per_s, 1),
             "logical_kv_gbs": round(sum(logical_per[i % nrot] for i in range(steps)) / total_s / 1e9 * world, 2),
@@ -554,6 +613,10 @@ def run_ours(args):
 
 
 def make_batch(pkv, shape, args, seed, device, reserve_tokens=0):
+    if args.kv == "fp8":
+        if args.workload not in ("gqa", "long", "mixed") or args.partition_size:
+            raise SystemExit("--kv fp8 runs the balanced split on the gqa, long and mixed workloads")
+        return Batch(pkv, shape, wl.draw_lengths(shape, seed).tolist(), seed, device, 0, reserve_tokens, kv="fp8")
     if args.workload.startswith("beam"):
         shared = wl.BEAM_SHARED_PARTIAL if args.workload == "beam1032" else wl.BEAM_SHARED
         return Batch.beam(pkv, shape, seed, device, args.partition_size, shared, reserve_tokens)
@@ -593,7 +656,11 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
                 pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim, max_seq_len,
                                                    args.partition_size))
     ws = torch.zeros(max(256, ws_bytes), dtype=torch.uint8, device=device)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len))
+    fp8 = args.kv == "fp8"
+    h_slot = torch.empty(S, dtype=torch.int64).pin_memory()
+    d_slot = torch.empty(S, dtype=torch.int64, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len) + ((h_slot,) if fp8 else ()))
+    elt = 1 if fp8 else None
     d2h = h_out.numel() * h_out.element_size()
     ms, byts = [], []
     with torch.cuda.stream(stream):
@@ -608,7 +675,13 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             h_len.numpy()[:] = ln
             for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len)):
                 d.copy_(h, non_blocking=True)
-            if b.group_offsets is not None:
+            if fp8:  # the quantising store needs the slots; then the FP8 decode
+                h_slot.numpy()[:] = slots
+                d_slot.copy_(h_slot, non_blocking=True)
+                pkv.kv_cache_write_fp8(d_k, d_v, b.k_cache, b.v_cache, d_slot, FP8_K_SCALE, FP8_V_SCALE)
+                pkv.paged_attention_decode_fp8(b.out, d_q, b.k_cache, b.v_cache, d_tab, d_len, shape.scale,
+                                               FP8_K_SCALE, FP8_V_SCALE, max_seq_len, ws)
+            elif b.group_offsets is not None:
                 offs, pre = b.alloc.prefix_groups(b.seq_ids)  # beams sharing a prompt
                 d_offs = torch.from_numpy(offs).pin_memory().to(device, non_blocking=True)
                 d_pre = torch.from_numpy(pre).pin_memory().to(device, non_blocking=True)
@@ -624,7 +697,7 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             if i >= args.warmup:
                 ms.append(ev0.elapsed_time(ev1))
                 # unique bytes: what the batch started with plus the tokens added since
-                byts.append(b.unique_bytes + kv_bytes(ln.tolist(), shape) - kv_bytes(b.lens, shape))
+                byts.append(b.unique_bytes + kv_bytes(ln.tolist(), shape, elt) - kv_bytes(b.lens, shape, elt))
     local_s = sum(ms) / 1e3
     total_s = max_over_ranks(local_s, world, device)
     total_b = sum_over_ranks(sum(byts), world, device)

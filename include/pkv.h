@@ -157,12 +157,18 @@ PKV_EXPORT size_t paged_attention_workspace_size(int num_seqs, int num_heads, in
  *                  0 = balanced split (bf16): all (sequence, kv head) contexts
  *                  are laid end to end and cut into equal shares of at least
  *                  256 tokens, one per resident warp; a context cut by share
- *                  boundaries is merged by the same reduction kernel.  fp32
- *                  (or more than 8192 sequences) uses 512-token partitions.
+ *                  boundaries is merged inside the attention kernel by the
+ *                  warp holding its first tokens, once the other pieces have
+ *                  flagged their partials (one kernel per call).  fp32 (or
+ *                  more than 8192 sequences) uses 512-token partitions and a
+ *                  reduction kernel.
  *   workspace      device scratch of at least paged_attention_workspace_size()
  *                  bytes for the same arguments (may be NULL when that is 0),
- *                  256-byte aligned.  Contents need no initialisation; calls
- *                  that share a workspace must be ordered on the device.
+ *                  256-byte aligned.  Contents need no initialisation (the
+ *                  balanced split's ready flags carry a per-call 64-bit tag and
+ *                  are cleared after use, so CUDA graph replays of one call
+ *                  work too); calls that share a workspace must be ordered on
+ *                  the device.
  * Results do not depend on which physical blocks hold the tokens: the order of
  * arithmetic depends only on logical positions, so any permutation of the pool
  * gives bit-identical outputs.

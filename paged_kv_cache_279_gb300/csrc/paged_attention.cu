@@ -36,7 +36,11 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <climits>
 #include <cmath>
 #include <cstdlib>
@@ -61,7 +65,13 @@ struct DecodeArgs {
     float *part_o;  // [S][Hq][max_parts][D]
     float *part_m;  // [S][Hq][max_parts]
     float *part_l;  // [S][Hq][max_parts]
-    int *pieces;    // [S][Hkv]: partials of each segment (balanced path)
+    int *pieces;    // [S][Hkv]: partials of each segment (balanced path with the merge kernel)
+    // balanced path with the merge in the attention kernel: one ready flag per
+    // (segment, partial slot) [S][Hkv][max_parts], set to this call's tag
+    // (never 0) once the slot's partial is stored; nullptr = the merge kernel
+    // runs afterwards
+    unsigned long long *flags;
+    unsigned long long tag;
     int *seq_tok0;  // [S]: tokens of a shared prefix attended elsewhere (grouped path), or nullptr
     int *prefix_pieces;   // [S][Hkv]: prefix partials of each member (tensor-core prefix kernel), or nullptr
     int merge_trigger;    // merge kernel: let the next kernel start early (small merges only)
@@ -600,9 +610,9 @@ constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended
 // Offsets are from the 1024-aligned base.
 struct StreamKLayout {
     int ring, bars, ycache, masks, prefix, toff, total;
-    // kv_bytes: bytes per cached element (2 for bf16, 1 for FP8)
-    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, bool grouped, int kv_bytes = 2) {
-        ring = NW * NS * 2 * D * kTile * kv_bytes;
+    // stage_bytes: one ring stage (K and V of one tile); 0 = a 16-token bf16 tile
+    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, bool grouped, int stage_bytes = 0) {
+        ring = NW * NS * (stage_bytes ? stage_bytes : 2 * D * kTile * 2);
         bars = ring;
         ycache = bars + NW * NS * 8;   // int2 per cached tile
         masks = ycache + kYCache * 8;  // valid-row mask per cached tile
@@ -658,19 +668,23 @@ struct TileRows {
     uint32_t mask;
 };
 
+__device__ __forceinline__ uint32_t low_bits(int n) { return n >= 32 ? 0xffffffffu : (1u << n) - 1u; }
+
+// TT = tokens per tile (16, or 32 for the FP8 path); at most two sub-blocks
+template <int TT = kTile>
 __device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int kvh, int tile, int len,
                                               int tok_off = 0) {
     const int B = a.block_size;
-    const int boxh = B < kTile ? B : kTile;
+    const int boxh = B < TT ? B : TT;
     const int32_t *bt = a.block_tables + (int64_t)seq * a.max_blocks;
     TileRows r{-1, -1, 0u};
-    for (int sb = 0; sb < kTile / boxh; ++sb) {
-        const int tok = tok_off + tile * kTile + sb * boxh;
+    for (int sb = 0; sb < TT / boxh; ++sb) {
+        const int tok = tok_off + tile * TT + sb * boxh;
         if (tok >= len) break;
         const int lb = tok / B;
         int blk = bt[lb];
         if (blk >= 0 && blk < a.num_blocks) {
-            r.mask |= ((1u << boxh) - 1u) << (sb * boxh);
+            r.mask |= low_bits(boxh) << (sb * boxh);
         } else {
             // never dereferenced out of range: read block 0, rows masked out
             flag_error(a.err, PKV_DEVERR_BLOCK_ID);
@@ -679,8 +693,8 @@ __device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int 
         const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
         if (sb == 0) r.y0 = y; else r.y1 = y;
     }
-    const int valid = min(kTile, len - tok_off - tile * kTile);
-    r.mask &= (1u << valid) - 1u;
+    const int valid = min(TT, len - tok_off - tile * TT);
+    r.mask &= low_bits(valid);
     return r;
 }
 
@@ -747,7 +761,7 @@ __device__ __forceinline__ float f16x2_hi(uint32_t v) {
 // Stage sizes of one 16-token tile (K then V) for either cache type.
 template <int D, bool F8>
 struct TileBytes {
-    static constexpr int kKV = F8 ? kTile * D : Bf16Layout<D>::kKVBytes;  // offset of V
+    static constexpr int kKV = F8 ? 2 * kTile * D : Bf16Layout<D>::kKVBytes;  // offset of V
     static constexpr int kStage = 2 * kKV;
 };
 
@@ -789,60 +803,73 @@ __device__ __forceinline__ void load_q_f16(const DecodeArgs &a, int seq, int kvh
     s1 = __shfl_sync(0xffffffffu, desc, 8 * t + 4);
 }
 
-// FP8 counterpart of attend_tile: K tile at sk (16 x D codes, swizzled), V^T
-// tile at sv (D x 16 codes), per-column score factors s0 / s1.
+// FP8 counterpart of attend_tile for a 32-token tile: K at sk (32 token rows
+// x D codes, 128-byte swizzle), V^T at sv as two halves (tokens 0-15, then
+// 16-31), each D rows x 16 codes; per-column score factors s0 / s1.  The two
+// 16-row halves give two independent MMA chains.
 template <int D>
 __device__ __forceinline__ void attend_tile_f8(unsigned char *sk, unsigned char *sv, uint32_t row_ok,
                                                const uint32_t (&qb)[D / 16][2], float s0, float s1,
                                                WarpAcc<D> &acc, int lane) {
     static_assert(D == 128, "FP8 tiles assume 128-byte K rows");
     const int g = lane >> 2, t = lane & 3;
-    if (row_ok != 0xffffu) {
+    if (row_ok != 0xffffffffu) {
         // masked tokens hold stale or unwritten codes (possibly NaN): clear
         // their bytes in every V^T row so that a zero weight meets a zero
-        uint32_t m[4];
+        uint32_t m[8];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) m[w] = ((((row_ok >> (4 * w)) & 0xfu) * 0x00204081u) & 0x01010101u) * 0xffu;
-        for (int r = lane; r < D; r += 32) {
-            uint4 *p = reinterpret_cast<uint4 *>(sv + r * kTile);
+        for (int w = 0; w < 8; ++w) m[w] = ((((row_ok >> (4 * w)) & 0xfu) * 0x00204081u) & 0x01010101u) * 0xffu;
+#pragma unroll
+        for (int i = 0; i < 2 * D / 32; ++i) {
+            const int h = (32 * i) / D;  // half: tokens 0-15 or 16-31
+            uint4 *p = reinterpret_cast<uint4 *>(sv + (32 * i + lane) * kTile);
             uint4 v = *p;
-            v.x &= m[0];
-            v.y &= m[1];
-            v.z &= m[2];
-            v.w &= m[3];
+            v.x &= m[4 * h];
+            v.y &= m[4 * h + 1];
+            v.z &= m[4 * h + 2];
+            v.w &= m[4 * h + 3];
             *p = v;
         }
         __syncwarp();
     }
     const uint32_t ska = smem_u32(sk), sva = smem_u32(sv);
     const int lj = lane >> 3, lr = lane & 7;
-    // ldmatrix rows: token lr (+8 for matrices 1 and 3), 16-byte chunk 2kk (+1 for matrices 2, 3)
-    const uint32_t krow = ska + (lr + 8 * (lj & 1)) * D;
+    // ldmatrix rows: token lr (+8 for matrices 1 and 3; +16 for the second
+    // half), 16-byte chunk 2kk (+1 for matrices 2 and 3); row & 7 == lr
+    const uint32_t krow0 = ska + (lr + 8 * (lj & 1)) * D, krow1 = krow0 + kTile * D;
 
-    // S^T (16 tokens x 8 heads) = K_tile . Q^T; a lane's 4 codes of a chunk are
-    // head_dim entries 4t..4t+3, split as the fragment's k pairs (2t, 2t+1) and
-    // (2t+8, 2t+9) -- the same split load_q_f16 gives the queries
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T (tokens x 8 heads) = K_tile . Q^T; a lane's 4 codes of a chunk are
+    // head_dim entries 4t..4t+3, split as the fragment's k pairs (2t, 2t+1)
+    // and (2t+8, 2t+9) -- the same split load_q_f16 gives the queries
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < D / 32; ++kk) {
-        const int chunk = 2 * kk + (lj >> 1);
-        uint32_t x0, x1, x2, x3, a0, a1, a2, a3;
-        ldmatrix_x4(krow + ((chunk ^ lr) << 4), x0, x1, x2, x3);
+        const uint32_t off = ((2 * kk + (lj >> 1)) ^ lr) << 4;
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3, a0, a1, a2, a3;
+        ldmatrix_x4(krow0 + off, x0, x1, x2, x3);
+        ldmatrix_x4(krow1 + off, y0, y1, y2, y3);
         e4m3x4_to_f16(x0, a0, a2);
         e4m3x4_to_f16(x1, a1, a3);
-        mma_f16_16816(sc, a0, a1, a2, a3, qb[2 * kk][0], qb[2 * kk][1]);
+        mma_f16_16816(sa, a0, a1, a2, a3, qb[2 * kk][0], qb[2 * kk][1]);
+        e4m3x4_to_f16(y0, a0, a2);
+        e4m3x4_to_f16(y1, a1, a3);
+        mma_f16_16816(sb, a0, a1, a2, a3, qb[2 * kk][0], qb[2 * kk][1]);
         e4m3x4_to_f16(x2, a0, a2);
         e4m3x4_to_f16(x3, a1, a3);
-        mma_f16_16816(sc, a0, a1, a2, a3, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
+        mma_f16_16816(sa, a0, a1, a2, a3, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
+        e4m3x4_to_f16(y2, a0, a2);
+        e4m3x4_to_f16(y3, a1, a3);
+        mma_f16_16816(sb, a0, a1, a2, a3, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
     }
 
-    // online softmax, base 2; rows g and g+8, columns 2t and 2t+1
-    const bool ok_lo = (row_ok >> g) & 1u, ok_hi = (row_ok >> (g + 8)) & 1u;
-    const float v0 = ok_lo ? sc[0] * s0 : -INFINITY;
-    const float v1 = ok_lo ? sc[1] * s1 : -INFINITY;
-    const float v2 = ok_hi ? sc[2] * s0 : -INFINITY;
-    const float v3 = ok_hi ? sc[3] * s1 : -INFINITY;
-    float mx0 = fmaxf(v0, v2), mx1 = fmaxf(v1, v3);
+    // online softmax, base 2; rows g, g+8, 16+g, 24+g; columns 2t and 2t+1
+    const bool ok0 = (row_ok >> g) & 1u, ok1 = (row_ok >> (g + 8)) & 1u;
+    const bool ok2 = (row_ok >> (g + 16)) & 1u, ok3 = (row_ok >> (g + 24)) & 1u;
+    const float v0 = ok0 ? sa[0] * s0 : -INFINITY, v1 = ok0 ? sa[1] * s1 : -INFINITY;
+    const float v2 = ok1 ? sa[2] * s0 : -INFINITY, v3 = ok1 ? sa[3] * s1 : -INFINITY;
+    const float v4 = ok2 ? sb[0] * s0 : -INFINITY, v5 = ok2 ? sb[1] * s1 : -INFINITY;
+    const float v6 = ok3 ? sb[2] * s0 : -INFINITY, v7 = ok3 ? sb[3] * s1 : -INFINITY;
+    float mx0 = fmaxf(fmaxf(v0, v2), fmaxf(v4, v6)), mx1 = fmaxf(fmaxf(v1, v3), fmaxf(v5, v7));
 #pragma unroll
     for (int sh = 4; sh < 32; sh <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
@@ -856,6 +883,8 @@ __device__ __forceinline__ void attend_tile_f8(unsigned char *sk, unsigned char 
     acc.m1 = mn1;
     const uint32_t p01 = pack_f16x2(exp2f(v0 - rf0), exp2f(v1 - rf1));
     const uint32_t p23 = pack_f16x2(exp2f(v2 - rf0), exp2f(v3 - rf1));
+    const uint32_t p45 = pack_f16x2(exp2f(v4 - rf0), exp2f(v5 - rf1));
+    const uint32_t p67 = pack_f16x2(exp2f(v6 - rf0), exp2f(v7 - rf1));
     if (moved) {
         acc.l0 = acc.l0 * al0;
         acc.l1 = acc.l1 * al1;
@@ -867,38 +896,60 @@ __device__ __forceinline__ void attend_tile_f8(unsigned char *sk, unsigned char 
             acc.o[mt][3] *= al1;
         }
     }
-    acc.l0 += f16x2_lo(p01) + f16x2_lo(p23);
-    acc.l1 += f16x2_hi(p01) + f16x2_hi(p23);
+    acc.l0 += (f16x2_lo(p01) + f16x2_lo(p23)) + (f16x2_lo(p45) + f16x2_lo(p67));
+    acc.l1 += (f16x2_hi(p01) + f16x2_hi(p23)) + (f16x2_hi(p45) + f16x2_hi(p67));
 
     // P^T as the B operand of O^T += V^T . P^T.  A lane's V^T fragment holds
     // tokens 4t..4t+3 of its head_dim row (k pairs (2t, 2t+1) = tokens 4t,
     // 4t+1 and (2t+8, 2t+9) = tokens 4t+2, 4t+3), so P^T must hold the same
-    // tokens: after the transposes lane t' has tokens 2t', 2t'+1 (m0) and
-    // 8+2t', 9+2t' (m1) of its head; gather them from the lanes of that head.
-    const uint32_t m0 = movmatrix_trans(p01), m1 = movmatrix_trans(p23);
+    // tokens: after the transposes lane t' has tokens 2t', 2t'+1 (first
+    // matrix) and 8+2t', 9+2t' (second) of its head; gather them from the
+    // lanes of that head.
     const int src = (lane & ~3) | (2 * (t & 1));
-    const uint32_t e0 = __shfl_sync(0xffffffffu, m0, src), e1 = __shfl_sync(0xffffffffu, m1, src);
-    const uint32_t f0 = __shfl_sync(0xffffffffu, m0, src + 1), f1 = __shfl_sync(0xffffffffu, m1, src + 1);
-    const uint32_t pb0 = t < 2 ? e0 : e1, pb1 = t < 2 ? f0 : f1;
+    uint32_t pa0, pa1, pb0, pb1;
+    {
+        const uint32_t m0 = movmatrix_trans(p01), m1 = movmatrix_trans(p23);
+        const uint32_t e0 = __shfl_sync(0xffffffffu, m0, src), e1 = __shfl_sync(0xffffffffu, m1, src);
+        const uint32_t f0 = __shfl_sync(0xffffffffu, m0, src + 1), f1 = __shfl_sync(0xffffffffu, m1, src + 1);
+        pa0 = t < 2 ? e0 : e1;
+        pa1 = t < 2 ? f0 : f1;
+    }
+    {
+        const uint32_t m0 = movmatrix_trans(p45), m1 = movmatrix_trans(p67);
+        const uint32_t e0 = __shfl_sync(0xffffffffu, m0, src), e1 = __shfl_sync(0xffffffffu, m1, src);
+        const uint32_t f0 = __shfl_sync(0xffffffffu, m0, src + 1), f1 = __shfl_sync(0xffffffffu, m1, src + 1);
+        pb0 = t < 2 ? e0 : e1;
+        pb1 = t < 2 ? f0 : f1;
+    }
 
-    // O^T (head_dim x 8 heads) += V^T tile . P^T; matrices of one ldmatrix.x4
-    // are head_dim rows 32j + 0..7, 8..15, 16..23, 24..31
+    // O^T (head_dim x 8 heads) += V^T . P^T over both halves; the matrices of
+    // one ldmatrix.x4 are head_dim rows 32j + 0..7, 8..15, 16..23, 24..31
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
-        uint32_t x0, x1, x2, x3, a0, a1, a2, a3;
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3, a0, a1, a2, a3;
         ldmatrix_x4(sva + (32 * j + lane) * kTile, x0, x1, x2, x3);
+        ldmatrix_x4(sva + kTile * D + (32 * j + lane) * kTile, y0, y1, y2, y3);
         e4m3x4_to_f16(x0, a0, a2);
         e4m3x4_to_f16(x1, a1, a3);
-        mma_f16_16816(acc.o[2 * j], a0, a1, a2, a3, pb0, pb1);
+        mma_f16_16816(acc.o[2 * j], a0, a1, a2, a3, pa0, pa1);
         e4m3x4_to_f16(x2, a0, a2);
         e4m3x4_to_f16(x3, a1, a3);
+        mma_f16_16816(acc.o[2 * j + 1], a0, a1, a2, a3, pa0, pa1);
+        e4m3x4_to_f16(y0, a0, a2);
+        e4m3x4_to_f16(y1, a1, a3);
+        mma_f16_16816(acc.o[2 * j], a0, a1, a2, a3, pb0, pb1);
+        e4m3x4_to_f16(y2, a0, a2);
+        e4m3x4_to_f16(y3, a1, a3);
         mma_f16_16816(acc.o[2 * j + 1], a0, a1, a2, a3, pb0, pb1);
     }
 }
 
-// Gather one FP8 tile: K rows y0 .. y0+15 of the [blocks * Hkv * B][D] view and
-// the V^T box of 16 token columns x D rows of the [blocks * Hkv * D][B] view.
-// Tiles never straddle blocks (block_size is a multiple of 16).
+// Gather one 32-token FP8 tile as two 16-token halves: K rows of the
+// [blocks * Hkv * B][D] view (box D x 16) and V^T boxes of 16 token columns x D
+// rows of the [blocks * Hkv * D][B] view.  With block_size 32 both halves lie
+// in one block (rows y0 and y0 + 16); with block_size 16 the second half is
+// the next block's (y1, or nothing past the context).  Rows of a half that
+// lie past the context are loaded from inside its block and masked later.
 template <int D>
 __device__ __forceinline__ void issue_rows_f8(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                               unsigned char *stage, uint64_t *bar, int bshift, TileRows r) {
@@ -907,11 +958,17 @@ __device__ __forceinline__ void issue_rows_f8(const CUtensorMap *tm_k, const CUt
         mbar_arrive_expect_tx(bar, 0u);
         return;
     }
-    mbar_arrive_expect_tx(bar, (uint32_t)(2 * kTile * D));
-    const uint32_t dk = smem_u32(stage);
+    const int y1 = bshift == 5 ? r.y0 + kTile : r.y1;
+    mbar_arrive_expect_tx(bar, (uint32_t)((y1 >= 0 ? 2 : 1) * 2 * kTile * D));
+    const uint32_t dk = smem_u32(stage), dv = dk + 2 * kTile * D;
+    const int bh0 = r.y0 >> bshift;  // block * Hkv + kv head
     tma_load_2d(dk, tm_k, b, 0, r.y0);
-    const int bh = r.y0 >> bshift;  // block * Hkv + kv head
-    tma_load_2d(dk + kTile * D, tm_v, b, r.y0 - (bh << bshift), bh * D);
+    tma_load_2d(dv, tm_v, b, r.y0 - (bh0 << bshift), bh0 * D);
+    if (y1 >= 0) {
+        const int bh1 = y1 >> bshift;
+        tma_load_2d(dk + kTile * D, tm_k, b, 0, y1);
+        tma_load_2d(dv + kTile * D, tm_v, b, y1 - (bh1 << bshift), bh1 * D);
+    }
 }
 
 // Store a warp's result for the piece [pa, pb) of segment `seg`: the final
@@ -960,12 +1017,133 @@ __device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc
     }
 }
 
+// Ordering of the in-kernel merge: a writer's lanes store their partial,
+// fence, and lane 0 then sets the slot's flag; the merger sees every flag,
+// fences, and reads the partials through L2.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Merge of a segment's n partials by the warp holding its first tile: for
+// every query head of the group, with M = max_j m_j,
+//     out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j
+// over the partial slots j = 0 .. n-1 in order (the same order whichever warp
+// merges), evaluated chunk by chunk with the running maximum (earlier sums
+// rescaled when it grows).  Lanes are split evenly over the (padded) heads,
+// each owning a run of NV float4 of its head's row.  A warp merges after its
+// share is done, when its ring is idle: each lane stages the rows it needs in
+// its own kLaneBytes of the ring with cp.async (L2, no registers held), so a
+// chunk costs one round trip.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+template <int D, int NV, int kLaneBytes>
+__device__ __forceinline__ void merge_rows(const float4 *po, const float *pm, const float *pl, int n,
+                                           uint2 *dst, uint32_t stage) {
+    constexpr int kChunk = kLaneBytes / (16 * NV) < 16 ? kLaneBytes / (16 * NV) : 16;  // partials per round trip
+    static_assert(kChunk >= 1, "a lane must stage at least one partial row");
+    float M = -INFINITY, L = 0.f;
+    float4 acc[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n; c0 += kChunk) {
+        float mj[kChunk], lj[kChunk];
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            if (c0 + r < n) {
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    cp_async16(stage + (r * NV + v) * 16, po + (int64_t)(c0 + r) * (D / 4) + v);
+            }
+            mj[r] = c0 + r < n ? __ldcg(pm + c0 + r) : -INFINITY;
+            lj[r] = c0 + r < n ? __ldcg(pl + c0 + r) : 0.f;
+        }
+        float cm = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) cm = fmaxf(cm, mj[r]);
+        const float Mn = fmaxf(M, cm);
+        if (Mn != M && M != -INFINITY) {  // rescale what the earlier chunks summed
+            const float a = exp2f(M - Mn);
+            L *= a;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                acc[v].x *= a;
+                acc[v].y *= a;
+                acc[v].z *= a;
+                acc[v].w *= a;
+            }
+        }
+        M = Mn;
+        cp_async_wait_all();
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            if (c0 + r < n && mj[r] != -INFINITY) {
+                const float w = exp2f(mj[r] - M);
+                L += w * lj[r];
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const float4 x = lds128(stage + (r * NV + v) * 16);
+                    acc[v].x += w * x.x;
+                    acc[v].y += w * x.y;
+                    acc[v].z += w * x.z;
+                    acc[v].w += w * x.w;
+                }
+            }
+        }
+    }
+    // every piece empty (all blocks invalid, flagged): L stays 0, zero rows
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+        dst[v] = make_uint2(pack_bf16x2(acc[v].x * inv, acc[v].y * inv), pack_bf16x2(acc[v].z * inv, acc[v].w * inv));
+}
+
+template <int D, int kLaneBytes>
+__device__ __forceinline__ void merge_segment(const float *part_o, const float *part_m, const float *part_l,
+                                              __nv_bfloat16 *out, int64_t row0, int G, int max_parts, int n,
+                                              int lane, uint32_t ring) {
+    const int gp = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
+    const int lph = min(32 / gp, D / 4);  // lanes per head
+    const int dpl = D / lph;              // head_dim entries per lane
+    const int h = lane / lph, part = lane % lph;
+    if (h >= G) return;
+    const int64_t row = row0 + h;
+    const float *pm = part_m + row * max_parts, *pl = part_l + row * max_parts;
+    const float4 *po = reinterpret_cast<const float4 *>(part_o + row * max_parts * D + part * dpl);
+    uint2 *dst = reinterpret_cast<uint2 *>(out + row * D + part * dpl);
+    const uint32_t stage = ring + lane * kLaneBytes;
+    switch (dpl / 4) {
+        case 1: merge_rows<D, 1, kLaneBytes>(po, pm, pl, n, dst, stage); break;
+        case 2: merge_rows<D, 2, kLaneBytes>(po, pm, pl, n, dst, stage); break;
+        case 4: merge_rows<D, 4, kLaneBytes>(po, pm, pl, n, dst, stage); break;
+        default: merge_rows<D, 8, kLaneBytes>(po, pm, pl, n, dst, stage); break;
+    }
+}
+
 // Balanced kernel: every warp of the grid takes an equal contiguous share of
 // the tile list (at least kMinTilesPerCta tiles) and streams it through its own
-// TMA ring.  Warps never wait for one another: where a segment (sequence, kv
-// head) ends inside a share, the warp stores its result for that piece -- the
-// final rows if the share holds the whole segment, otherwise a partial that
-// the merge kernel combines -- and carries on with the next segment.
+// TMA ring.  Where a segment (sequence, kv head) ends inside a share, the warp
+// stores its result for that piece -- the final rows if the share holds the
+// whole segment, otherwise a partial -- and carries on with the next segment.
+// Partials are merged either by the merge kernel afterwards (grouped calls)
+// or in this kernel: a share cuts at most its first and last segment, and the
+// warp holding a split segment's first tile (its share's last segment) merges
+// it once the other pieces -- processed at the start of their own shares --
+// have flagged their partials.  That is the only wait between warps; it is
+// bounded, and every warp it waits for is already resident (the grid is one
+// wave) and never waits itself.
 //
 // F8: the cache holds E4M3 codes (K rows, V transposed per block); tiles are
 // attended by attend_tile_f8 and the queries are loaded by load_q_f16.  The
@@ -975,11 +1153,12 @@ __global__ void __launch_bounds__(NW * 32)
 decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using Lay = TileBytes<D, F8>;
+    constexpr int TT = F8 ? 2 * kTile : kTile;  // tokens per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const bool grouped = !F8 && a.seq_tok0 != nullptr;
-    const StreamKLayout L(D, NW, NS, a.num_seqs, grouped, F8 ? 1 : 2);
+    const StreamKLayout L(D, NW, NS, a.num_seqs, grouped, Lay::kStage);
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + L.bars);
     int2 *ycache = reinterpret_cast<int2 *>(smem + L.ycache);
     uint32_t *mcache = reinterpret_cast<uint32_t *>(smem + L.masks);
@@ -1022,8 +1201,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             // grouped: the shared prefix was attended by the prefix kernel
             const int t0 = grouped ? min(max(a.seq_tok0[sq], 0), len) : 0;
             if (grouped) toff[sq] = t0;
-            v = Hkv * ((len - t0 + kTile - 1) / kTile);
-            my_max = max(my_max, (len - t0 + kTile - 1) / kTile);
+            v = Hkv * ((len - t0 + TT - 1) / TT);
+            my_max = max(my_max, (len - t0 + TT - 1) / TT);
         }
         int x = v;  // inclusive warp scan
 #pragma unroll
@@ -1044,6 +1223,23 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int sh = 16; sh > 0; sh >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, sh));
     if (lane == 0) atomicMax(&seg_max, my_max);
     __syncthreads();
+    if (a.flags) {
+        // No merge kernel follows: this kernel writes the zero rows of empty
+        // contexts (no tile, hence no piece).  CTA c takes sequences c, c + grid, ...
+        bool mine = false;
+        for (int sq = blockIdx.x; sq < S && !mine; sq += gridDim.x) mine = prefix[sq + 1] == prefix[sq];
+        if (mine) {
+            grid_dependency_wait();  // `out` may still be read by the previous kernel
+            constexpr int kRowChunks = D * 2 / 16;
+            for (int sq = blockIdx.x; sq < S; sq += gridDim.x) {
+                if (prefix[sq + 1] != prefix[sq]) continue;
+                uint4 *row = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                                       (int64_t)sq * a.num_heads * D);
+                for (int i = threadIdx.x; i < a.num_heads * kRowChunks; i += NW * 32)
+                    row[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
     const int64_t T = prefix[S];
     // Warps that get a share.  A segment of n tiles meets at most
     // ceil(n / share) + 1 shares and has own_slots partial slots, so shares
@@ -1084,7 +1280,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (gw < parts) {
         seg_lo.seek(prefix, S, Hkv, lo);
         const int64_t first_end = seg_lo.seg_start + seg_lo.n;
-        if (first_end < hi && first_end - lo < kRotateTiles && ncache == cta_hi - cta_lo) r = first_end;
+        if (first_end < hi && first_end - lo < kRotateTiles * kTile / TT && ncache == cta_hi - cta_lo)
+            r = first_end;
         seg = seg_lo;
         if (r != lo) seg.advance_to(prefix, Hkv, r);
         load_q(seg, qb, qs0, qs1);
@@ -1107,7 +1304,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     {
         constexpr int kPer = (kYCache + NW * 32 - 1) / (NW * 32);
         const int B = a.block_size;
-        const int boxh = B < kTile ? B : kTile;
+        const int boxh = B < TT ? B : TT;
         int sq[kPer], kv[kPer], tl[kPer], ln[kPer], b0[kPer], b1[kPer];
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
@@ -1127,8 +1324,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int32_t *bt = a.block_tables + (int64_t)sq[u] * a.max_blocks;
             if (grouped) tl[u] += toff[sq[u]] / kTile;  // token offsets are tile aligned
             // the tile's tokens lie inside the clamped length, hence inside the table
-            const int lb0 = min(tl[u] * kTile / B, a.max_blocks - 1);
-            const int lb1 = min((tl[u] * kTile + boxh) / B, a.max_blocks - 1);
+            const int lb0 = min(tl[u] * TT / B, a.max_blocks - 1);
+            const int lb1 = min((tl[u] * TT + boxh) / B, a.max_blocks - 1);
             ln[u] = a.seq_lens[sq[u]];
             b0[u] = bt[lb0];
             b1[u] = bt[lb1];
@@ -1138,13 +1335,13 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (sq[u] < 0) continue;
             const int len = clamp_len(ln[u], cap);
             TileRows r{-1, -1, 0u};
-            for (int sb = 0; sb < kTile / boxh; ++sb) {
-                const int tok = tl[u] * kTile + sb * boxh;
+            for (int sb = 0; sb < TT / boxh; ++sb) {
+                const int tok = tl[u] * TT + sb * boxh;
                 if (tok >= len) break;
                 const int lb = tok / B;
                 int blk = sb == 0 ? b0[u] : b1[u];
                 if (blk >= 0 && blk < a.num_blocks) {
-                    r.mask |= ((1u << boxh) - 1u) << (sb * boxh);
+                    r.mask |= low_bits(boxh) << (sb * boxh);
                 } else {
                     flag_error(a.err, PKV_DEVERR_BLOCK_ID);
                     blk = 0;
@@ -1152,11 +1349,12 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 const int y = (int)(((int64_t)blk * Hkv + kv[u]) * B + (tok - lb * B));
                 if (sb == 0) r.y0 = y; else r.y1 = y;
             }
-            const int valid = min(kTile, len - tl[u] * kTile);
-            r.mask &= (1u << valid) - 1u;
+            const int valid = min(TT, len - tl[u] * TT);
+            r.mask &= low_bits(valid);
             const int i = threadIdx.x + u * NW * 32;
             ycache[i] = make_int2(r.y0, r.y1);
-            mcache[i] = r.mask | ((uint32_t)valid << 16);  // valid rows in bits 16..20
+            // bf16: valid rows in bits 16..20 (the fused append reads them)
+            mcache[i] = F8 ? r.mask : (r.mask | ((uint32_t)valid << 16));
         }
     }
     unsigned char *ring = smem + warp * NS * Lay::kStage;
@@ -1234,10 +1432,10 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         const int64_t i = t - cta_lo;
         if (i < ncache) {
             const int2 y = ycache[i];
-            return TileRows{y.x, y.y, mcache[i] & 0xffffu};
+            return TileRows{y.x, y.y, F8 ? mcache[i] : (mcache[i] & 0xffffu)};
         }
-        return tile_rows(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap),
-                         grouped ? toff[c.seq] : 0);
+        return tile_rows<TT>(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap),
+                             grouped ? toff[c.seq] : 0);
     };
 
     // k-th tile in walk order
@@ -1260,6 +1458,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     int k = 0;
     bool dead = false;
     WarpAcc<D> acc;
+    int64_t merge_seg = -1;  // the split segment this warp merges (its share's last), if any
+    int merge_n = 0;
     for (;;) {
         const int64_t pa = tile_at(k);  // this piece: tiles [pa, pb), walk positions [k, kend)
         const int64_t seg_end = seg.seg_start + seg.n;
@@ -1298,7 +1498,26 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         const bool whole = pa == seg.seg_start && pb == seg_end && !(grouped && toff[seg.seq] > 0);
         const int64_t w0 = share_owner(seg.seg_start, T, parts);
         store_piece<D>(a, acc, dead, seg, whole, (int)(gw - w0), lane, F8 ? a.f8_vscale : 1.f);
-        if (lane == 0 && pa == seg.seg_start) {
+        if (a.flags) {
+            if (!whole) {
+                // Split segment: the warp holding its first tile merges it (the
+                // segment is the last of that warp's share, so the merge waits
+                // for nothing but pieces processed at the start of other shares);
+                // every other piece announces its partial.
+                const int n = (int)(share_owner(seg_end - 1, T, parts) - w0 + 1);
+                const int64_t sg = (int64_t)seg.seq * Hkv + seg.kvh;
+                if (gw == w0) {
+                    merge_seg = sg;
+                    merge_n = n;
+                } else {
+                    fence_acq_rel_gpu();
+                    __syncwarp();
+                    if (lane == 0)
+                        *reinterpret_cast<volatile unsigned long long *>(a.flags + sg * a.max_parts + (gw - w0)) =
+                            a.tag;
+                }
+            }
+        } else if (lane == 0 && pa == seg.seg_start) {
             // the warp holding a segment's first tile records its number of pieces
             const int64_t w1 = share_owner(seg_end - 1, T, parts);
             a.pieces[(int64_t)seg.seq * a.num_kv_heads + seg.kvh] = (int)(w1 - w0 + 1);
@@ -1312,6 +1531,28 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         qs0 = qns0;
         qs1 = qns1;
+    }
+    if (merge_seg >= 0) {
+        // Wait (bounded) until the other pieces' flags carry this call's tag,
+        // merge through the now idle ring, then clear the flags so that a
+        // replay with the same tag waits again.
+        unsigned long long *fl = a.flags + merge_seg * a.max_parts;
+        fence_acq_rel_gpu();  // this warp's own partial (slot 0), before it is read back
+        __syncwarp();
+        bool ready = false;
+        for (uint32_t it = 0; it < kWaitLimit && !ready; ++it) {
+            bool mine = true;
+            for (int j = 1 + lane; j < merge_n; j += 32) mine = mine && ld_volatile_u64(fl + j) == a.tag;
+            ready = __all_sync(0xffffffffu, mine);
+            if (!ready) __nanosleep(64);
+        }
+        if (!ready && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+        fence_acq_rel_gpu();
+        const int sq = (int)(merge_seg / Hkv), kvh = (int)(merge_seg - (int64_t)sq * Hkv);
+        merge_segment<D, NS * Lay::kStage / 32>(a.part_o, a.part_m, a.part_l, static_cast<__nv_bfloat16 *>(a.out),
+                                                (int64_t)sq * a.num_heads + kvh * a.group, a.group, a.max_parts,
+                                                merge_n, lane, smem_u32(ring));
+        for (int j = 1 + lane; j < merge_n; j += 32) fl[j] = 0ull;
     }
 }
 
@@ -2287,7 +2528,7 @@ constexpr int kMaxBalancedSeqs = 8192;
 static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WorkspaceLayout {
-    size_t o_off, m_off, l_off, pieces_off, total;
+    size_t o_off, m_off, l_off, pieces_off, flags_off, total;
 };
 
 // parts = partial slots per (sequence, query head); `pieces` adds the
@@ -2298,7 +2539,10 @@ static WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t D, int64_
     w.m_off = round256((size_t)(S * Hq * parts * D * 4));
     w.l_off = w.m_off + round256((size_t)(S * Hq * parts * 4));
     w.pieces_off = w.l_off + round256((size_t)(S * Hq * parts * 4));
-    w.total = w.pieces_off + (pieces ? round256((size_t)(S * Hq * 4)) : 0);
+    // balanced path: piece counts (merge kernel), and the ready flags of the
+    // partial slots (merge in the attention kernel), 8 bytes per slot
+    w.flags_off = w.pieces_off + (pieces ? round256((size_t)(S * Hq * 4)) : 0);
+    w.total = w.flags_off + (pieces ? round256((size_t)(S * Hq * parts * 8)) : 0);
     return w;
 }
 
@@ -2306,6 +2550,27 @@ static WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t D, int64_
 // because every share holds at least kMinTilesPerCta tiles (256 tokens).
 static int64_t balanced_slots(int max_seq_len) {
     return ((int64_t)max_seq_len + kMinTilesPerCta * kTile - 1) / (kMinTilesPerCta * kTile) + 1;
+}
+
+// A 64-bit tag per balanced call, never 0 (the value of a cleared flag): flags
+// left by other calls, or never written, hold another value.  The sequence
+// starts at a value drawn from the clock, the process and an address, so
+// separate processes start far apart.
+static unsigned long long next_call_tag() {
+    static std::atomic<unsigned long long> count{0};
+    static const unsigned long long base = [] {
+        unsigned long long x = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+        x ^= (unsigned long long)getpid() * 0x9E3779B97F4A7C15ull;
+        x ^= (unsigned long long)reinterpret_cast<uintptr_t>(&count);
+        x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+        x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+        return x ^ (x >> 31);
+    }();
+    unsigned long long t;
+    do {
+        t = base + count.fetch_add(1, std::memory_order_relaxed);
+    } while (t == 0);
+    return t;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -2472,8 +2737,9 @@ template <int D, int NW, int NS>
 static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
     static bool done[128] = {};
     auto kern = decode_bf16_streamk_kernel<D, NW, NS, true>;
-    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, false, 1).total, done)) return PKV_ERR_CUDA;
-    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, false, 1).total;
+    constexpr int stage = TileBytes<D, true>::kStage;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, false, stage).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, false, stage).total;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
         per_sm < 1)
@@ -2488,10 +2754,10 @@ static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
 static pkv_status dispatch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
     static const int v = env_variant("PKV_FP8_VARIANT");
     switch (v) {
-        case 1: return launch_balanced_f8<128, 4, 2>(a, st);
-        case 2: return launch_balanced_f8<128, 4, 3>(a, st);
-        case 3: return launch_balanced_f8<128, 8, 4>(a, st);
-        default: return launch_balanced_f8<128, 4, 4>(a, st);
+        case 1: return launch_balanced_f8<128, 4, 3>(a, st);
+        case 2: return launch_balanced_f8<128, 4, 1>(a, st);
+        case 3: return launch_balanced_f8<128, 8, 2>(a, st);
+        default: return launch_balanced_f8<128, 4, 2>(a, st);
     }
 }
 
@@ -2617,6 +2883,10 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
         a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
         a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
         a.pieces = partition_size == 0 ? reinterpret_cast<int *>(ws + lay.pieces_off) : nullptr;
+        if (balanced) {  // the attention kernel merges split contexts itself
+            a.flags = reinterpret_cast<unsigned long long *>(ws + lay.flags_off);
+            a.tag = next_call_tag();
+        }
         a.max_parts = (int)slots;  // stride of the partial slots
     }
 
@@ -2625,9 +2895,6 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
     pkv_status rc;
     if (balanced) {
         rc = head_dim == 128 ? dispatch_balanced<128>(a, st) : dispatch_balanced<64>(a, st);
-        if (rc == PKV_OK)
-            rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, true>(a, st)
-                                 : launch_reduce<__nv_bfloat16, 64, true, true>(a, st);
     } else if (dtype == PKV_BF16) {
         rc = head_dim == 128 ? dispatch_bf16<128>(a, grid, st) : dispatch_bf16<64>(a, grid, st);
         if (rc == PKV_OK && parts > 1)
@@ -2703,10 +2970,10 @@ PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const vo
     a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
     a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
     a.pieces = reinterpret_cast<int *>(ws + lay.pieces_off);
+    a.flags = reinterpret_cast<unsigned long long *>(ws + lay.flags_off);
+    a.tag = next_call_tag();
     a.max_parts = (int)slots;
-    pkv_status rc = dispatch_balanced_f8(a, st);
-    if (rc == PKV_OK) rc = launch_reduce<__nv_bfloat16, 128, true, true>(a, st);
-    return rc;
+    return dispatch_balanced_f8(a, st);
 }
 
 PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *k_cache,

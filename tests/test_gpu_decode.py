@@ -69,6 +69,15 @@ def test_tiny_fp32_workload_with_cache_write():
     (32, 4, 128, 8, [1, 8, 9, 95, 600], 0),    # balanced split, block 8
     (32, 4, 128, 32, [1, 31, 32, 33, 700], 0),  # balanced split, block 32
     (32, 8, 64, 16, [9, 160, 999], 0),
+    # balanced split with contexts merged inside the attention kernel, every
+    # lane layout of the merge: head_dim 64 and 128, 1, 2, 3, 7 and 8 query
+    # heads per KV head
+    (8, 8, 64, 16, [5, 47, 300, 2000], 0),
+    (16, 8, 64, 16, [33, 1257, 2600], 0),
+    (12, 4, 64, 16, [700, 1500], 0),
+    (64, 8, 64, 32, [3000, 17], 0),
+    (56, 8, 128, 16, [900, 1800], 0),
+    (12, 4, 128, 16, [2500, 64, 1], 0),
 ])
 def test_bf16_decode_matches_oracle(Hq, Hkv, D, B, lens, P):
     shape = shape_of(Hq, Hkv, D, B)
@@ -258,4 +267,55 @@ def test_decode_append_equals_write_then_decode(P, dtype, B, split, nseq, monkey
     else:
         assert_f32_close(out, ref, "append fp32")
     assert torch.all(out[4].float() == 0)
+    assert pkv.read_device_errors() == 0
+
+
+def _replay_checks(call, refresh, check, reps=3):
+    """Capture `call` in a CUDA graph on a side stream, then replay it `reps`
+    times, refreshing the inputs in place before each replay."""
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        call()  # warm (tensor maps, shared-memory opt-in) outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            call()
+    for rep in range(reps):
+        refresh(rep)
+        g.replay()
+        torch.cuda.synchronize()
+        check(rep)
+
+
+def test_balanced_merge_survives_graph_replays_and_random_workspace():
+    """The balanced path merges split contexts inside the attention kernel:
+    per-context arrival counters in the workspace, tagged per call.  A graph
+    replays one call (same tag, same counters) several times, and the
+    workspace starts as random bytes, so every call must both ignore stale
+    counters and leave its own ready for a replay."""
+    shape = shape_of(32, 8, 128, 16)
+    lens = [3000, 1, 0, 2048, 517, 64] * 3
+    case = make_decode_case(shape, lens, seed=55)
+    dev = "cuda"
+    kc, vc = case["kc"].to(dev), case["vc"].to(dev)
+    tables = torch.from_numpy(case["tables"]).to(dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    q = case["q"].to(dev)
+    out = torch.empty_like(q)
+    need = pkv.paged_attention_workspace_size(len(lens), 32, 128, 3000, 0)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device=dev)
+    qs = [wl.draw_query(shape, seed=200 + r, num_seqs=len(lens)) for r in range(3)]
+
+    def call():
+        pkv.paged_attention_decode(out, q, kc, vc, tables, sl, shape.scale, 3000, 0, ws)
+
+    def refresh(r):
+        q.copy_(qs[r].to(dev))
+        out.fill_(float("nan"))
+
+    def check(r):
+        assert_bf16_close(out, oracle_out(dict(case, q=qs[r]), shape), f"replay {r}")
+        assert torch.all(out[2].float() == 0)
+
+    _replay_checks(call, refresh, check)
     assert pkv.read_device_errors() == 0

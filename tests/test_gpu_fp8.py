@@ -201,3 +201,35 @@ def test_write_then_decode_end_to_end():
     qerr = np.abs(out.cpu().double().numpy() - exact)
     print(f"fp8 cache vs bf16 cache: max abs {qerr.max():.3e}, mean abs {qerr.mean():.3e}")
     assert qerr.mean() < 0.05
+
+
+def test_decode_fp8_graph_replays():
+    """Split contexts are merged inside the attention kernel with tagged
+    arrival counters; graph replays reuse one tag and must still merge."""
+    lens = [2048, 700, 0, 1, 1500, 3000]
+    Hkv, B = 8, 32
+    shape = wl.DecodeShape("fp8_graph", len(lens), 32, Hkv, D, B, torch.bfloat16)
+    pool = _pool_with_codes(lens, Hkv, B, seed=12)
+    dev = "cuda"
+    kc, vc = torch.from_numpy(pool["kc"]).to(dev), torch.from_numpy(pool["vc"]).to(dev)
+    tables = torch.from_numpy(pool["tables"]).to(dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    qs = [wl.draw_query(shape, seed=300 + r) for r in range(3)]
+    q = qs[0].to(dev)
+    out = torch.empty_like(q)
+    ws = torch.randint(0, 256, (pkv.paged_attention_workspace_size(len(lens), 32, D, 3000, 0),),
+                       dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        pkv.paged_attention_decode_fp8(out, q, kc, vc, tables, sl, shape.scale, K_SCALE, V_SCALE, 3000, ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            pkv.paged_attention_decode_fp8(out, q, kc, vc, tables, sl, shape.scale, K_SCALE, V_SCALE, 3000, ws)
+    for r in range(3):
+        q.copy_(qs[r].to(dev))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bf16_close(out.cpu(), _oracle(pool, qs[r], shape.scale), f"fp8 replay {r}")
+        assert torch.all(out[2] == 0)
