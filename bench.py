@@ -362,8 +362,10 @@ class Batch:
         (grouped by shared prefix for beam search); with an FP8 cache the
         quantising write, then the FP8 decode."""
         if self.kv == "fp8":
-            self.write()
-            self.decode()
+            self.pkv.paged_attention_decode_append_fp8(self.out, self.q, self.k_new, self.v_new, self.k_cache,
+                                                       self.v_cache, self.block_tables, self.seq_lens,
+                                                       self.shape.scale, FP8_K_SCALE, FP8_V_SCALE,
+                                                       self.max_seq_len, self.workspace)
             return
         if self.group_offsets is not None:
             self.pkv.paged_attention_decode_grouped(self.out, self.q, self.k_cache, self.v_cache,
@@ -378,17 +380,22 @@ class Batch:
                                                self.workspace)
 
     def launches_per_step(self) -> int:
-        """Kernels one step launches: the attention kernel, the merge of split
-        contexts, and a separate store kernel on the paths that do not fuse it."""
+        """Kernels one step launches.  Balanced split (bf16, FP8): the attention
+        kernel stores the new tokens and merges split contexts itself, except
+        that bf16 batches of more than 1024 (sequence, kv head) segments store
+        the tokens in a separate kernel.  Fixed partitions: store kernel,
+        attention kernel and the merge kernel when contexts are split.
+        Grouped beam search: prefix kernel, attention kernel, merge kernel."""
         S = len(self.lens)
+        if self.group_offsets is not None:
+            return 3
+        if self.kv == "fp8":
+            return 1
+        if self.partition_size == 0 and self.shape.dtype == torch.bfloat16:
+            return 1 if S * self.shape.num_kv_heads <= 1024 else 2
         ws = self.pkv.paged_attention_workspace_size(S, self.shape.num_heads, self.shape.head_dim,
                                                      self.max_seq_len, self.partition_size)
-        if self.group_offsets is not None:
-            return 3  # prefix kernel, attention kernel, merge
-        if self.kv == "fp8":
-            return 3  # quantising write, attention kernel, merge
-        fused = self.partition_size == 0 and self.shape.dtype == torch.bfloat16
-        return 1 + (1 if ws > 0 else 0) + (0 if fused else 1)
+        return 2 + (1 if ws > 0 else 0)
 
 
 def capture(fns, stream):
@@ -657,9 +664,7 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
                                                    args.partition_size))
     ws = torch.zeros(max(256, ws_bytes), dtype=torch.uint8, device=device)
     fp8 = args.kv == "fp8"
-    h_slot = torch.empty(S, dtype=torch.int64).pin_memory()
-    d_slot = torch.empty(S, dtype=torch.int64, device=device)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len) + ((h_slot,) if fp8 else ()))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len))
     elt = 1 if fp8 else None
     d2h = h_out.numel() * h_out.element_size()
     ms, byts = [], []
@@ -675,12 +680,9 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             h_len.numpy()[:] = ln
             for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len)):
                 d.copy_(h, non_blocking=True)
-            if fp8:  # the quantising store needs the slots; then the FP8 decode
-                h_slot.numpy()[:] = slots
-                d_slot.copy_(h_slot, non_blocking=True)
-                pkv.kv_cache_write_fp8(d_k, d_v, b.k_cache, b.v_cache, d_slot, FP8_K_SCALE, FP8_V_SCALE)
-                pkv.paged_attention_decode_fp8(b.out, d_q, b.k_cache, b.v_cache, d_tab, d_len, shape.scale,
-                                               FP8_K_SCALE, FP8_V_SCALE, max_seq_len, ws)
+            if fp8:
+                pkv.paged_attention_decode_append_fp8(b.out, d_q, d_k, d_v, b.k_cache, b.v_cache, d_tab, d_len,
+                                                      shape.scale, FP8_K_SCALE, FP8_V_SCALE, max_seq_len, ws)
             elif b.group_offsets is not None:
                 offs, pre = b.alloc.prefix_groups(b.seq_ids)  # beams sharing a prompt
                 d_offs = torch.from_numpy(offs).pin_memory().to(device, non_blocking=True)

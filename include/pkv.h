@@ -225,6 +225,25 @@ PKV_EXPORT pkv_status kv_cache_write_fp8(const void *k_new, const void *v_new, v
                                          int num_kv_heads, int head_dim, int block_size,
                                          int num_blocks, float k_scale, float v_scale, void *stream);
 
+/*
+ * paged_attention_decode_append_fp8 -- one FP8 decode step in one call:
+ * equivalent to kv_cache_write_fp8 of k_new[s] / v_new[s] (bf16
+ * [num_seqs][num_kv_heads][head_dim]) at position seq_lens[s] - 1 of sequence
+ * s (the slot its block table gives for that position), followed by
+ * paged_attention_decode_fp8.  The codes are stored inside the attention
+ * kernel, before any load of their tile.  Every seq_lens[s] must be >= 1 (a
+ * sequence of length 0 stores nothing and gets a zero row); a block-table
+ * entry outside the pool skips the store and is flagged as in the decode.
+ */
+PKV_EXPORT pkv_status paged_attention_decode_append_fp8(void *out, const void *q, const void *k_new,
+                                                        const void *v_new, void *k_cache, void *v_cache,
+                                                        const int32_t *block_tables, const int32_t *seq_lens,
+                                                        int num_seqs, int num_heads, int num_kv_heads,
+                                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                                        int num_blocks, int max_seq_len, float scale,
+                                                        float k_scale, float v_scale, void *workspace,
+                                                        size_t workspace_bytes, void *stream);
+
 PKV_EXPORT pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
                                                  const void *v_cache, const int32_t *block_tables,
                                                  const int32_t *seq_lens, int num_seqs, int num_heads,

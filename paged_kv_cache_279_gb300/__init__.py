@@ -30,7 +30,7 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, 
 
 __all__ = [
     "PkvError", "kv_cache_write", "kv_cache_write_fp8", "paged_attention_decode",
-    "paged_attention_decode_fp8", "paged_attention_workspace_size",
+    "paged_attention_decode_fp8", "paged_attention_decode_append_fp8", "paged_attention_workspace_size",
     "paged_attention_decode_append", "paged_attention_decode_grouped",
     "paged_attention_grouped_workspace_size", "block_copy", "read_device_errors", "BlockAllocator",
     "library_path",
@@ -183,6 +183,36 @@ def paged_attention_decode_fp8(out, q, k_cache, v_cache, block_tables, seq_lens,
         _dev(seq_lens, "seq_lens", torch.int32, 1), S, Hq, Hkv, D, B, block_tables.shape[1], NB,
         int(max_seq_len), float(scale), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "paged_attention_decode_fp8")
+    return out
+
+
+def paged_attention_decode_append_fp8(out, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+                                      scale: float, k_scale: float, v_scale: float, max_seq_len: int,
+                                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One FP8 decode step: quantise and store each sequence's new token (bf16
+    k_new/v_new [S, Hkv, D]) at position seq_lens[s] - 1, then attend; the
+    store happens inside the attention kernel."""
+    lib = _lib.load()
+    S, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    if Dk != D or tuple(out.shape) != (S, Hq, D) or tuple(v_cache.shape) != (NB, Hkv, D, B):
+        raise ValueError("shape mismatch")
+    if tuple(k_new.shape) != (S, Hkv, D) or k_new.shape != v_new.shape:
+        raise ValueError("k_new / v_new must be [S, Hkv, D]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("block_tables must be [S, maxB] and seq_lens [S]")
+    need = paged_attention_workspace_size(S, Hq, D, max_seq_len, 0)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.paged_attention_decode_append_fp8(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_new, "k_new", torch.bfloat16),
+        _dev(v_new, "v_new", torch.bfloat16), _dev(k_cache, "k_cache", torch.uint8),
+        _dev(v_cache, "v_cache", torch.uint8), _dev(block_tables, "block_tables", torch.int32, 2),
+        _dev(seq_lens, "seq_lens", torch.int32, 1), S, Hq, Hkv, D, B, block_tables.shape[1], NB,
+        int(max_seq_len), float(scale), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "paged_attention_decode_append_fp8")
     return out
 
 

@@ -68,27 +68,7 @@ kv_cache_write_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__
 // FP8 (E4M3) cache write.  One thread per 16 head_dim entries of one (token,
 // kv head): the K codes go out as one 16-byte row chunk; the V codes go to
 // the transposed V block ([D][block_size] per (block, kv head)), one byte per
-// head_dim row.  code = e4m3(fl32(x / scale)), nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    unsigned short r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ void quantize16(const uint4 (&x)[2], float scale, uint32_t (&w)[4]) {
-    const uint32_t *e = reinterpret_cast<const uint32_t *>(x);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        // bf16 pairs (4 values) -> 4 codes, low byte first
-        const uint32_t p0 = e[2 * i], p1 = e[2 * i + 1];
-        const float f0 = __fdiv_rn(__uint_as_float(p0 << 16), scale);
-        const float f1 = __fdiv_rn(__uint_as_float(p0 & 0xffff0000u), scale);
-        const float f2 = __fdiv_rn(__uint_as_float(p1 << 16), scale);
-        const float f3 = __fdiv_rn(__uint_as_float(p1 & 0xffff0000u), scale);
-        w[i] = e4m3x2(f0, f1) | (e4m3x2(f2, f3) << 16);
-    }
-}
-
+// head_dim row.  Codes from quantize16 (pkv_internal.cuh).
 __global__ void __launch_bounds__(256)
 kv_cache_write_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                           unsigned char *__restrict__ k_cache, unsigned char *__restrict__ v_cache,

@@ -83,6 +83,7 @@ struct DecodeArgs {
     float scale;       // multiplies q.k
     float scale_log2;  // scale * log2(e), for the exp2 form of the softmax
     float f8_kscale_log2;  // FP8 cache: scale * k_scale * log2(e)
+    float f8_kscale;       // FP8 cache: k_scale (quantising the appended token)
     float f8_vscale;       // FP8 cache: v_scale
     int f8_bshift;         // FP8 cache: log2(block_size)
     unsigned int *err;
@@ -1371,6 +1372,46 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int ntiles = (int)(hi - lo);
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
 
+    if (F8 && a.k_new) {
+        // Fused append, FP8: as below, one segment at a time.  Lanes 0-7
+        // quantise 16 K entries each into one 16-byte chunk of the K row;
+        // lanes 8-15 quantise 16 V entries each into bytes of the transposed
+        // V block (one per head_dim row, block_size bytes apart).
+        SegCursor c = seg_lo;
+        for (;;) {
+            const int64_t last = c.seg_start + c.n - 1;
+            if (last >= lo && last < hi && lane < 16) {
+                const int B = a.block_size;
+                const int pos = clamp_len(a.seq_lens[c.seq], cap) - 1;  // >= 0: the segment has tiles
+                const int lb = pos / B;
+                const int blk = a.block_tables[(int64_t)c.seq * a.max_blocks + lb];
+                if (blk >= 0 && blk < a.num_blocks) {
+                    const int off = pos - lb * B, ch = lane & 7;
+                    const bool isv = lane >= 8;
+                    const int64_t bh = (int64_t)blk * Hkv + c.kvh;
+                    const uint4 *src = static_cast<const uint4 *>(isv ? a.v_new : a.k_new) +
+                                       ((int64_t)c.seq * Hkv + c.kvh) * (D / 8) + 2 * ch;
+                    const uint4 x[2] = {src[0], src[1]};
+                    uint32_t w[4];
+                    quantize16(x, isv ? a.f8_vscale : a.f8_kscale, w);
+                    if (!isv) {
+                        *reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.k_cache_w) +
+                                                   (bh * B + off) * D + 16 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
+                    } else {
+                        unsigned char *col = static_cast<unsigned char *>(a.v_cache_w) + (bh * D + 16 * ch) * B + off;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) col[(int64_t)j * B] = (unsigned char)(w[j >> 2] >> (8 * (j & 3)));
+                    }
+                }
+            }
+            if (c.seg_start + c.n >= hi) break;
+            c.advance_to(prefix, Hkv, c.seg_start + c.n);
+        }
+        // generic-proxy stores, then the TMA (async proxy) of this warp reads them
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     if (!F8 && a.k_new) {
         // Fused append: the warp whose share holds a segment's last tile stores
         // that segment's new token (position len - 1) before any TMA reads it.
@@ -2909,13 +2950,12 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
     return rc;
 }
 
-PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
-                                              const void *v_cache, const int32_t *block_tables,
-                                              const int32_t *seq_lens, int num_seqs, int num_heads,
-                                              int num_kv_heads, int head_dim, int block_size,
-                                              int max_blocks_per_seq, int num_blocks, int max_seq_len,
-                                              float scale, float k_scale, float v_scale, void *workspace,
-                                              size_t workspace_bytes, void *stream) {
+static pkv_status decode_fp8_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                  const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                                  int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+                                  float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                                  void *stream, const void *k_new, const void *v_new) {
     if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
         max_seq_len < 0 || !std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale) ||
         !(k_scale > 0.f) || !(v_scale > 0.f))
@@ -2962,7 +3002,12 @@ PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const vo
     a.scale = scale;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.f8_kscale_log2 = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+    a.f8_kscale = k_scale;
     a.f8_vscale = v_scale;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache_w = const_cast<void *>(k_cache);
+    a.v_cache_w = const_cast<void *>(v_cache);
     a.f8_bshift = block_size == 16 ? 4 : 5;
     a.err = device_error_word();
     unsigned char *ws = static_cast<unsigned char *>(workspace);
@@ -2974,6 +3019,33 @@ PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const vo
     a.tag = next_call_tag();
     a.max_parts = (int)slots;
     return dispatch_balanced_f8(a, st);
+}
+
+PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_tables,
+                                              const int32_t *seq_lens, int num_seqs, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                              float scale, float k_scale, float v_scale, void *workspace,
+                                              size_t workspace_bytes, void *stream) {
+    return decode_fp8_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                           head_dim, block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale, k_scale,
+                           v_scale, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+PKV_API pkv_status paged_attention_decode_append_fp8(void *out, const void *q, const void *k_new,
+                                                     const void *v_new, void *k_cache, void *v_cache,
+                                                     const int32_t *block_tables, const int32_t *seq_lens,
+                                                     int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                                     int block_size, int max_blocks_per_seq, int num_blocks,
+                                                     int max_seq_len, float scale, float k_scale, float v_scale,
+                                                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    // every context holds at least its new token
+    if (num_seqs > 0 && max_seq_len < 1) return PKV_ERR_INVALID;
+    return decode_fp8_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads, num_kv_heads,
+                           head_dim, block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale, k_scale,
+                           v_scale, workspace, workspace_bytes, stream, k_new, v_new);
 }
 
 PKV_API pkv_status paged_attention_decode(void *out, const void *q, const void *k_cache,

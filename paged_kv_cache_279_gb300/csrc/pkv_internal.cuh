@@ -24,4 +24,29 @@ __device__ __forceinline__ void flag_error(unsigned int *err, unsigned int bits)
     if (err) atomicOr(err, bits);
 }
 
+// FP8 (E4M3) quantisation shared by the cache write and the fused append:
+// code = the E4M3 value nearest to the float32 quotient x / scale (IEEE
+// division), ties to even, saturating at +-448 (cvt ... satfinite).
+// Two codes, low byte = lo.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    unsigned short r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void quantize16(const uint4 (&x)[2], float scale, uint32_t (&w)[4]) {
+    const uint32_t *e = reinterpret_cast<const uint32_t *>(x);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bf16 pairs (4 values) -> 4 codes, low byte first
+        const uint32_t p0 = e[2 * i], p1 = e[2 * i + 1];
+        const float f0 = __fdiv_rn(__uint_as_float(p0 << 16), scale);
+        const float f1 = __fdiv_rn(__uint_as_float(p0 & 0xffff0000u), scale);
+        const float f2 = __fdiv_rn(__uint_as_float(p1 << 16), scale);
+        const float f3 = __fdiv_rn(__uint_as_float(p1 & 0xffff0000u), scale);
+        w[i] = e4m3x2(f0, f1) | (e4m3x2(f2, f3) << 16);
+    }
+}
+
+
 }  // namespace pkv

@@ -233,3 +233,49 @@ def test_decode_fp8_graph_replays():
         torch.cuda.synchronize()
         assert_bf16_close(out.cpu(), _oracle(pool, qs[r], shape.scale), f"fp8 replay {r}")
         assert torch.all(out[2] == 0)
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_decode_append_fp8_equals_write_then_decode(B):
+    """The fused step (quantise and store each new token inside the attention
+    kernel) must leave the same cache bytes and give the same output bits as
+    kv_cache_write_fp8 at position len - 1 followed by paged_attention_decode_fp8,
+    and match the oracle."""
+    lens = [1, 2, 17, 300, 1024, 2049, 0, 33]
+    Hq, Hkv = 32, 8
+    shape = wl.DecodeShape("fp8_append", len(lens), Hq, Hkv, D, B, torch.bfloat16)
+    pool = _pool_with_codes(lens, Hkv, B, seed=40 + B)
+    q = wl.draw_query(shape, seed=41)
+    k_new, v_new = _bf16_tokens(len(lens), Hkv, 42)
+    dev = "cuda"
+    tables = torch.from_numpy(pool["tables"]).to(dev)
+    sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+    maxL = max(lens)
+    # path A: separate write (slots of position len - 1), then decode
+    slots = np.array([token_slots(pool["tables"][s], L, B)[-1] if L else -1 for s, L in enumerate(lens)],
+                     dtype=np.int64)
+    kcA, vcA = torch.from_numpy(pool["kc"]).to(dev), torch.from_numpy(pool["vc"]).to(dev)
+    pkv.kv_cache_write_fp8(k_new.to(dev), v_new.to(dev), kcA, vcA, torch.from_numpy(slots).to(dev),
+                           K_SCALE, V_SCALE)
+    outA = torch.empty((len(lens), Hq, D), dtype=torch.bfloat16, device=dev)
+    pkv.paged_attention_decode_fp8(outA, q.to(dev), kcA, vcA, tables, sl, shape.scale, K_SCALE, V_SCALE, maxL)
+    # path B: one call
+    kcB, vcB = torch.from_numpy(pool["kc"]).to(dev), torch.from_numpy(pool["vc"]).to(dev)
+    outB = torch.empty_like(outA)
+    pkv.paged_attention_decode_append_fp8(outB, q.to(dev), k_new.to(dev), v_new.to(dev), kcB, vcB, tables, sl,
+                                          shape.scale, K_SCALE, V_SCALE, maxL)
+    torch.cuda.synchronize()
+    assert torch.equal(kcA, kcB) and torch.equal(vcA, vcB)
+    assert torch.equal(outA.view(torch.int16), outB.view(torch.int16))
+    # oracle: the new token quantised by the oracle replaces position len - 1
+    kq = [k.copy() for k in pool["kq"]]
+    vq = [v.copy() for v in pool["vq"]]
+    for s, L in enumerate(lens):
+        if L:
+            kq[s][L - 1] = f8.quantize(k_new[s].float().numpy(), K_SCALE)
+            vq[s][L - 1] = f8.quantize(v_new[s].float().numpy(), V_SCALE)
+    ref = oracle.decode_attention(q.float().numpy(), [f8.dequantize(k, K_SCALE) for k in kq],
+                                  [f8.dequantize(v, V_SCALE) for v in vq], shape.scale)
+    assert_bf16_close(outB.cpu(), ref, f"fp8 append B={B}")
+    assert torch.all(outB[6] == 0)
+    assert pkv.read_device_errors() == 0
