@@ -183,6 +183,15 @@ def shape_for(args) -> wl.DecodeShape:
 # per-tensor scales of the FP8 cache: N(0, 1) data stays below 448 * scale
 FP8_K_SCALE = FP8_V_SCALE = 1.0 / 64
 
+# DRAM bytes (read + write) of one captured launch of the attention kernel and
+# that launch's algorithmic bytes, from `ncu --set full` of the same command
+# (rotated batch 2); the line reports traffic scaled to the average launch.
+# Only valid for the kernel build the capture was taken from.
+NCU_TRAFFIC = {
+    ("gqa", "bf16"): (314.15e6, 306.07e6, "profiles/decode_balanced_gqa_full.md"),
+    ("gqa", "fp8"): (158.89e6, 153.57e6, "profiles/decode_fp8_gqa_full.md"),
+}
+
 
 def kv_bytes(lens, shape, kv_elt=None) -> int:
     """Unique K and V bytes one attention pass reads (every cached token once);
@@ -582,8 +591,14 @@ def run_ours(args):
         pass
     peak = float(peaks.get("hbm_gbs", 6800.0))
     achieved = dec_alg_bytes / (dec_ms / 1e3) / 1e9
+    traffic, traffic_src = None, None
+    cap = NCU_TRAFFIC.get((args.workload, args.kv))
+    if cap is not None and not args.block_size and not args.partition_size:
+        traffic = round(cap[0] / cap[1] * dec_alg_bytes)
+        traffic_src = f"{cap[2]}: {cap[0] / 1e6:.2f} MB for {cap[1] / 1e6:.2f} MB algorithmic, scaled to this launch"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch",
+                "traffic_source": traffic_src, "algorithmic_bytes": round(dec_alg_bytes),
                 "kernel": ("paged_attention_decode_fp8" if args.kv == "fp8" else "paged_attention_decode")
                           + " (attention kernel + merge kernel)",
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
