@@ -389,19 +389,16 @@ class Batch:
                                                self.workspace)
 
     def launches_per_step(self) -> int:
-        """Kernels one step launches.  Balanced split (bf16, FP8): the attention
-        kernel stores the new tokens and merges split contexts itself, except
-        that bf16 batches of more than 1024 (sequence, kv head) segments store
-        the tokens in a separate kernel.  Fixed partitions: store kernel,
-        attention kernel and the merge kernel when contexts are split.
-        Grouped beam search: prefix kernel, attention kernel, merge kernel."""
+        """Kernels one step launches.  Balanced split (bf16, FP8): one -- the
+        attention kernel stores the new tokens and merges split contexts itself.
+        Fixed partitions: store kernel, attention kernel and the merge kernel
+        when contexts are split.  Grouped beam search: prefix kernel, attention
+        kernel, merge kernel."""
         S = len(self.lens)
         if self.group_offsets is not None:
             return 3
-        if self.kv == "fp8":
+        if self.kv == "fp8" or (self.partition_size == 0 and self.shape.dtype == torch.bfloat16):
             return 1
-        if self.partition_size == 0 and self.shape.dtype == torch.bfloat16:
-            return 1 if S * self.shape.num_kv_heads <= 1024 else 2
         ws = self.pkv.paged_attention_workspace_size(S, self.shape.num_heads, self.shape.head_dim,
                                                      self.max_seq_len, self.partition_size)
         return 2 + (1 if ws > 0 else 0)

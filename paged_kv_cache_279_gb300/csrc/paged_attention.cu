@@ -3066,17 +3066,14 @@ PKV_API pkv_status paged_attention_decode_append(
     int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
     int partition_size, void *workspace, size_t workspace_bytes, int dtype, void *stream) {
     if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
-    // The balanced path stores the new tokens inside the attention kernel,
-    // unless the batch has many (sequence, kv head) segments: then most warps
-    // would store a token while every warp's first loads are queued, which
-    // stalls them; a separate store kernel runs under the attention kernel's
-    // prologue instead (measured: 1024+ segments, e.g. 256 x 8).
-    // PKV_APPEND_SPLIT=1 / 2 forces the separate / fused store for comparisons.
+    // The balanced path stores the new tokens inside the attention kernel (also
+    // for batches of many (sequence, kv head) segments: with the merge inside
+    // the attention kernel, 256 x 8 segments ran 66.6 us fused against 70.1 us
+    // with a separate store kernel).  PKV_APPEND_SPLIT=1 forces the separate
+    // store kernel for comparisons.
     const int split_env = env_variant("PKV_APPEND_SPLIT");
-    const bool many_segments = (int64_t)num_seqs * num_kv_heads > 1024;
     const bool fused = partition_size == 0 && dtype == PKV_BF16 && num_seqs > 0 &&
-                       num_seqs <= kMaxBalancedSeqs && max_seq_len > 0 &&
-                       (split_env == 2 || (split_env != 1 && !many_segments));
+                       num_seqs <= kMaxBalancedSeqs && max_seq_len > 0 && split_env != 1;
     if (!fused) {
         // other paths: the plain write (slot of position seq_lens[s] - 1 is
         // looked up on the device) followed by the decode
