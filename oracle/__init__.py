@@ -28,6 +28,9 @@ Contents and the passages they follow (page titles as given at each address):
   (waste remains only in each sequence's last block).
 * ``BlockAllocatorModel`` (``block_allocator_model.py``) -- the allocator's
   host semantics.
+* ``multi_token`` -- causal attention of several new tokens per sequence
+  (chunked prefill, verification of drafted tokens).  hada.io page, list of
+  advanced features; the causal reading is in that module.
 * ``fp8_e4m3`` -- the FP8 (E4M3) KV cache: quantiser, dequantiser and cache
   write.  aiwiki.vn page, paragraph on quantisation and offloading (K/V kept
   in a lower-precision representation to cut bytes, at a conversion cost and
