@@ -253,6 +253,51 @@ PKV_EXPORT pkv_status paged_attention_decode_fp8(void *out, const void *q, const
                                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_attention_multi_token -- attention of several new tokens per sequence
+ * (chunked prefill, verification of drafted tokens) over the paged cache.
+ *
+ * Source: "vLLM PagedAttention: Buoc dot pha ve thong luong suy luan LLM"
+ * (vi.news.hada.io), the advanced features built on PagedAttention (chunked
+ * prefill; speculative decoding with drafted tokens), with the causal reading
+ * of the aiwiki.vn page's attention (a position attends to the positions it
+ * may see).  Sequence s carries Q_s = q_starts[s+1] - q_starts[s] query
+ * tokens, the last Q_s positions of its context of L_s = seq_lens[s] tokens
+ * (their K/V already written, e.g. by kv_cache_write); query i sits at
+ * position p = L_s - Q_s + i and
+ *     out[q_starts[s]+i, h, :] = sum_{t <= p} softmax_t(scale * q[q_starts[s]+i, h, :] . K[s,t,g,:]) V[s,t,g,:]
+ * with g the KV head of h.  Q_s = 1 is the decode step.
+ *
+ *   q, out         device bf16 [num_q_tokens][num_heads][head_dim]
+ *   k_cache, v_cache, block_tables, seq_lens  as for paged_attention_decode (bf16)
+ *   q_starts       device int32 [num_seqs + 1], q_starts[0] = 0, non-decreasing,
+ *                  q_starts[num_seqs] = num_q_tokens; inconsistent entries are
+ *                  flagged (PKV_DEVERR_SEQ_LEN) and the sequence is skipped
+ *   max_q_len      >= every Q_s (queries past it are not attended, their rows
+ *                  are left unwritten, and PKV_DEVERR_SEQ_LEN is set); a
+ *                  sequence with Q_s > L_s is flagged too and its queries that
+ *                  see no token get zero rows
+ *   workspace      paged_attention_multi_token_workspace_size() bytes for the
+ *                  same (num_q_tokens, num_heads, head_dim, max_seq_len),
+ *                  256-byte aligned (0 bytes, NULL allowed, when max_seq_len <=
+ *                  1024): contexts longer than 1024 tokens are attended in
+ *                  1024-token partitions whose partials a reduction kernel
+ *                  merges.  Contents need no initialisation.
+ * Supported: bf16; head_dim 64 or 128; block_size 8, 16 or 32; at most 8
+ * query heads per KV head.  Results do not depend on which physical blocks
+ * hold the tokens.
+ */
+PKV_EXPORT size_t paged_attention_multi_token_workspace_size(int num_q_tokens, int num_heads, int head_dim,
+                                                             int max_seq_len);
+PKV_EXPORT pkv_status paged_attention_multi_token(void *out, const void *q, const void *k_cache,
+                                                  const void *v_cache, const int32_t *block_tables,
+                                                  const int32_t *seq_lens, const int32_t *q_starts,
+                                                  int num_seqs, int num_q_tokens, int num_heads,
+                                                  int num_kv_heads, int head_dim, int block_size,
+                                                  int max_blocks_per_seq, int num_blocks, int max_q_len,
+                                                  int max_seq_len, float scale, void *workspace,
+                                                  size_t workspace_bytes, void *stream);
+
+/*
  * block_copy -- copy whole physical blocks, in every layer, for K and V.
  *
  * Source: troisinh page, section "Copy-on-Write cho Beam Search": sequences

@@ -31,6 +31,7 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT, 
 __all__ = [
     "PkvError", "kv_cache_write", "kv_cache_write_fp8", "paged_attention_decode",
     "paged_attention_decode_fp8", "paged_attention_decode_append_fp8", "paged_attention_workspace_size",
+    "paged_attention_multi_token", "paged_attention_multi_token_workspace_size",
     "paged_attention_decode_append", "paged_attention_decode_grouped",
     "paged_attention_grouped_workspace_size", "block_copy", "read_device_errors", "BlockAllocator",
     "library_path",
@@ -135,6 +136,43 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, sca
         S, Hq, Hkv, D, B, block_tables.shape[1], NB, int(max_seq_len), float(scale),
         int(partition_size), ws_ptr, ws_bytes, dt, _stream(stream))
     _check(st, "paged_attention_decode")
+    return out
+
+
+def paged_attention_multi_token_workspace_size(num_q_tokens: int, num_heads: int, head_dim: int,
+                                               max_seq_len: int) -> int:
+    return int(_lib.load().paged_attention_multi_token_workspace_size(num_q_tokens, num_heads, head_dim,
+                                                                      max_seq_len))
+
+
+def paged_attention_multi_token(out, q, k_cache, v_cache, block_tables, seq_lens, q_starts, scale: float,
+                                max_q_len: int, max_seq_len: int, workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's last Q_s positions (chunked prefill,
+    verification of drafted tokens): q/out bf16 [T, Hq, D] with sequence s
+    owning rows q_starts[s] .. q_starts[s+1]-1 (int32 [S+1]); caches
+    [NB, Hkv, B, D]; block_tables int32 [S, maxB]; seq_lens int32 [S] (the
+    contexts including the query tokens)."""
+    lib = _lib.load()
+    T, Hq, D = q.shape
+    NB, Hkv, B, Dk = k_cache.shape
+    S = seq_lens.shape[0]
+    if Dk != D or tuple(out.shape) != (T, Hq, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or q_starts.shape[0] != S + 1:
+        raise ValueError("block_tables must be [S, maxB] and q_starts [S + 1]")
+    need = paged_attention_multi_token_workspace_size(T, Hq, D, max_seq_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _dev(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.paged_attention_multi_token(
+        _dev(out, "out", torch.bfloat16), _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache", torch.bfloat16),
+        _dev(v_cache, "v_cache", torch.bfloat16), _dev(block_tables, "block_tables", torch.int32, 2),
+        _dev(seq_lens, "seq_lens", torch.int32, 1), _dev(q_starts, "q_starts", torch.int32, 1), S, T, Hq, Hkv,
+        D, B, block_tables.shape[1], NB, int(max_q_len), int(max_seq_len), float(scale), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check(st, "paged_attention_multi_token")
     return out
 
 

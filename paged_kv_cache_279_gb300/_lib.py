@@ -30,6 +30,10 @@ SIGNATURES = {
                                                   c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                                   c_int, c_int, c_int, c_int, c_int, c_float, c_float,
                                                   c_float, c_void_p, c_size_t, c_void_p]),
+    "paged_attention_multi_token_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "paged_attention_multi_token": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                            c_int, c_int, c_int, c_float, c_void_p, c_size_t, c_void_p]),
     "paged_attention_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "paged_attention_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,

@@ -334,20 +334,22 @@ __device__ __forceinline__ void load_q_fragments(const DecodeArgs &a, int seq, i
 }
 
 // Attend one staged 16-token tile (K at sk, V at sv, 128-byte swizzled
-// halves).  row_ok has a bit per token row that belongs to the context and
-// came from a valid block; other rows are masked and their V zeroed.
+// halves).  row_ok has a bit per token row that this query attends (inside
+// its context, from a valid block); the other rows get zero weight.  Rows
+// cleared in zero_ok (default: row_ok) hold stale, unwritten or substituted
+// slots: their V is zeroed first so that a zero weight never meets a NaN.
+// Warps sharing a stage pass the same zero_ok (only zeros are ever written).
 template <int D, bool kZeroMasked = true>
 __device__ __forceinline__ void attend_tile(unsigned char *sk, unsigned char *sv, uint32_t row_ok,
                                             const uint32_t (&qb)[D / 16][2], float sl2,
-                                            WarpAcc<D> &acc, int lane) {
+                                            WarpAcc<D> &acc, int lane, uint32_t zero_ok = 0x10000u) {
     using Lay = Bf16Layout<D>;
     const int r0 = lane >> 2;
-    if (kZeroMasked && row_ok != 0xffffu) {
-        // masked rows hold stale, unwritten or substituted slots: zero their
-        // V so that a zero weight never meets a NaN
+    if (zero_ok == 0x10000u) zero_ok = row_ok;
+    if (kZeroMasked && zero_ok != 0xffffu) {
         for (int e = lane; e < Lay::kHalves * kTile * 8; e += 32) {
             const int h = e / (kTile * 8), rr = (e / 8) % kTile, c = e % 8;
-            if (!((row_ok >> rr) & 1u))
+            if (!((zero_ok >> rr) & 1u))
                 *reinterpret_cast<uint4 *>(sv + h * Lay::kHalfBytes + rr * 128 + c * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
         }
@@ -1792,6 +1794,179 @@ decode_bf16_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // ---------------------------------------------------------------------------
+// Multi-token paged attention (chunked prefill, verification of drafted
+// tokens): sequence s carries Q_s query tokens, the last Q_s positions of its
+// context; query i sits at position p = L_s - Q_s + i and attends to tokens
+// 0 .. p.  One CTA per (sequence, kv head, block of kMtQueries queries,
+// partition of kMtPart tokens): a producer warp streams the partition's tiles,
+// up to the block's last position, through a CTA-shared ring once; consumer
+// warp j attends query j of the block on the same tiles (S^T = K Q^T with the
+// group's query heads as the MMA's N), masking the tokens past its own
+// position.  A query whose context spans several partitions leaves one
+// partial per partition; the reduction kernel merges them, one virtual
+// sequence per query token with length p + 1 (q_lens).
+// ---------------------------------------------------------------------------
+constexpr int kMtQueries = 8;   // consumer warps: queries per CTA
+constexpr int kMtPart = 1024;   // tokens per partition (64 tiles)
+constexpr int kMtIds = kMtPart / 8 + 2;
+
+template <int D, int NS>
+constexpr int mt_smem_bytes() {
+    return NS * Bf16Layout<D>::kStageBytes + 2 * NS * 8 + kMtIds * 4 + 1024;
+}
+
+template <int D, int NS>
+__global__ void __launch_bounds__((kMtQueries + 1) * 32, 2)
+multi_token_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const DecodeArgs a, const int32_t *__restrict__ q_starts, int *__restrict__ q_lens,
+                   int num_q_tokens, int max_q_len, int parts) {
+    using Lay = Bf16Layout<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * Lay::kStageBytes);
+    uint64_t *empty = full + NS;
+    int *bt_s = reinterpret_cast<int *>(empty + NS);
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int sq = blockIdx.x, kvh = blockIdx.y;
+    const int qblk = blockIdx.z % ((max_q_len + kMtQueries - 1) / kMtQueries);
+    const int part = blockIdx.z / ((max_q_len + kMtQueries - 1) / kMtQueries);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int B = a.block_size;
+    const int cap = min(a.max_seq_len, a.max_blocks * B);
+    const int raw = a.seq_lens[sq];
+    const int L = clamp_len(raw, cap);
+    int q0 = q_starts[sq], q1 = q_starts[sq + 1];
+    const bool first_cta = qblk == 0 && part == 0 && kvh == 0 && threadIdx.x == 0;
+    if (q0 < 0 || q1 < q0 || q1 > num_q_tokens) {
+        if (first_cta) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+        q0 = q1 = 0;
+    }
+    if (first_cta && ((raw < 0 || raw > cap) || q1 - q0 > max_q_len || q1 - q0 > L))
+        flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+    const int Q = min(q1 - q0, max_q_len);  // queries past max_q_len are not attended
+    const int i0 = qblk * kMtQueries;
+    if (i0 >= Q) return;
+    const int nq = min(kMtQueries, Q - i0);
+    const int pos0 = L - Q + i0;            // position of the block's first query (< 0 if Q > L)
+    const int p_last = pos0 + nq - 1;
+    if (q_lens && part == 0 && kvh == 0 && threadIdx.x < nq)  // merge input: each query's context length
+        q_lens[q0 + i0 + threadIdx.x] = max(0, pos0 + (int)threadIdx.x + 1);
+    const int t_begin = part * kMtPart;
+    const int t_end = min(p_last + 1, t_begin + kMtPart);
+    if (t_begin >= t_end) {
+        // nothing of this partition is visible to the block; part 0 still owes
+        // zero rows to queries that see no token at all (Q > L, flagged)
+        if (part == 0 && warp >= 1 && warp - 1 < nq && pos0 + warp - 1 < 0) {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) +
+                               ((int64_t)(q0 + i0 + warp - 1) * a.num_heads + kvh * a.group) * D;
+            for (int e = lane; e < a.group * D; e += 32) o[e] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
+    const int boxh = B < kTile ? B : kTile;
+    const int32_t *bt = a.block_tables + (int64_t)sq * a.max_blocks;
+    const int lb0 = t_begin / B, nblk = (t_begin + ntiles * kTile - 1) / B - lb0 + 1;
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x)
+        bt_s[i] = lb0 + i < a.max_blocks ? bt[lb0 + i] : -1;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kMtQueries);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // rows of tile k that come from a valid block and lie inside the context
+    // at or before the block's last position: what any consumer may attend
+    auto common_ok = [&](int k) -> uint32_t {
+        const int t0 = t_begin + k * kTile;
+        uint32_t m = 0;
+        for (int sb = 0; sb < kTile / boxh; ++sb) {
+            const int blk = bt_s[(t0 + sb * boxh) / B - lb0];
+            if (blk >= 0 && blk < a.num_blocks) m |= ((1u << boxh) - 1u) << (sb * boxh);
+        }
+        const int valid = min(kTile, min(p_last, L - 1) - t0 + 1);
+        return valid <= 0 ? 0u : (m & ((1u << valid) - 1u));
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int k = 0; k < ntiles; ++k) {
+                const int st = k % NS;
+                if (k >= NS && !mbar_wait_bounded(&empty[st], (uint32_t)(((k / NS) - 1) & 1))) {
+                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                    break;
+                }
+                const int t0 = t_begin + k * kTile;
+                TileRows r{-1, -1, 0u};
+                for (int sb = 0; sb < kTile / boxh; ++sb) {
+                    const int tok = t0 + sb * boxh;
+                    const int lb = tok / B;
+                    int blk = bt_s[lb - lb0];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        if (tok < L) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        blk = 0;  // never dereferenced out of range: rows masked out
+                    }
+                    const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
+                    if (sb == 0) r.y0 = y; else r.y1 = y;
+                }
+                issue_rows<D>(&tm_k, &tm_v, smem + st * Lay::kStageBytes, &full[st], boxh, r);
+            }
+        }
+        return;  // no CTA-wide barrier follows
+    }
+
+    const int j = warp - 1;
+    const bool active = j < nq;
+    const int pj = pos0 + j;          // this query's position
+    const int row = q0 + i0 + j;      // its row in q / out
+    uint32_t qb[D / 16][2];
+    if (active && pj >= 0) load_q_fragments<D>(a, row, kvh, lane, qb);
+    WarpAcc<D> acc;
+    acc.reset();
+    bool dead = false;
+    for (int k = 0; k < ntiles; ++k) {
+        const int st = k % NS;
+        if (!dead && !mbar_wait_bounded(&full[st], (uint32_t)((k / NS) & 1))) {
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            dead = true;
+        }
+        if (!dead && active && pj >= 0) {
+            const int t0 = t_begin + k * kTile;
+            const uint32_t zok = common_ok(k);
+            const int mine = min(kTile, pj - t0 + 1);  // rows at or before this query's position
+            const uint32_t row_ok = mine <= 0 ? 0u : (zok & ((1u << mine) - 1u));
+            if (row_ok) {
+                unsigned char *sk = smem + st * Lay::kStageBytes;
+                attend_tile<D, true>(sk, sk + Lay::kKVBytes, row_ok, qb, a.scale_log2, acc, lane, zok);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (!active) return;
+    if (pj < 0) {  // sees no token (Q > L, flagged): a zero row, written once
+        if (part == 0) {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)row * a.num_heads + kvh * a.group) * D;
+            for (int e = lane; e < a.group * D; e += 32) o[e] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+    if (pj < t_begin) return;  // this partition holds nothing this query sees
+    SegCursor c;
+    c.seq = row;
+    c.kvh = kvh;
+    const bool whole = pj + 1 <= kMtPart;  // the query's context fits one partition
+    store_piece<D>(a, acc, dead, c, whole, part, lane);
+}
+
+// ---------------------------------------------------------------------------
 // Shared prefixes on the 5th-generation tensor cores (tcgen05).
 //
 // Per kv head, a group's prefix is one dense contraction: the queries of all
@@ -3019,6 +3194,107 @@ static pkv_status decode_fp8_impl(void *out, const void *q, const void *k_cache,
     a.tag = next_call_tag();
     a.max_parts = (int)slots;
     return dispatch_balanced_f8(a, st);
+}
+
+// ---------------------------------------------------------------------------
+// Multi-token paged attention
+// ---------------------------------------------------------------------------
+static int64_t mt_parts(int max_seq_len) { return ((int64_t)max_seq_len + kMtPart - 1) / kMtPart; }
+
+PKV_API size_t paged_attention_multi_token_workspace_size(int num_q_tokens, int num_heads, int head_dim,
+                                                          int max_seq_len) {
+    if (num_q_tokens <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
+    const int64_t parts = mt_parts(max_seq_len);
+    if (parts <= 1) return 0;
+    return workspace_layout(num_q_tokens, num_heads, head_dim, parts, false).total +
+           round256((size_t)num_q_tokens * 4);
+}
+
+template <int D>
+static pkv_status launch_multi_token(const DecodeArgs &a, const int32_t *q_starts, int *q_lens, int num_q_tokens,
+                                     int max_q_len, int parts, cudaStream_t st) {
+    constexpr int NS = 4;
+    static bool done[128] = {};
+    constexpr int smem = mt_smem_bytes<D, NS>();
+    auto kern = multi_token_kernel<D, NS>;
+    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
+    CUtensorMap mk, mv;
+    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
+    const int nqblk = (max_q_len + kMtQueries - 1) / kMtQueries;
+    const dim3 grid((unsigned)a.num_seqs, (unsigned)a.num_kv_heads, (unsigned)(nqblk * parts));
+    return launch_pdl(kern, grid, dim3((kMtQueries + 1) * 32), smem, st, mk, mv, a, q_starts, q_lens,
+                      num_q_tokens, max_q_len, parts);
+}
+
+PKV_API pkv_status paged_attention_multi_token(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                               const int32_t *block_tables, const int32_t *seq_lens,
+                                               const int32_t *q_starts, int num_seqs, int num_q_tokens,
+                                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                               int max_blocks_per_seq, int num_blocks, int max_q_len,
+                                               int max_seq_len, float scale, void *workspace,
+                                               size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_q_tokens < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || max_seq_len < 0 || max_q_len < 0 || !std::isfinite(scale))
+        return PKV_ERR_INVALID;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > kGMax) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_q_tokens == 0) return PKV_OK;
+    if (max_q_len < 1 || max_seq_len < 1) return PKV_ERR_INVALID;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_starts) return PKV_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
+    if (((int64_t)num_blocks + 1) * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
+    const int64_t parts = mt_parts(max_seq_len);
+    const int64_t nqblk = ((int64_t)max_q_len + kMtQueries - 1) / kMtQueries;
+    if (nqblk * parts > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+
+    DecodeArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.partition_size = kMtPart;
+    a.max_parts = (int)parts;
+    a.scale = scale;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.err = device_error_word();
+    int *q_lens = nullptr;
+    if (parts > 1) {
+        const WorkspaceLayout lay = workspace_layout(num_q_tokens, num_heads, head_dim, parts, false);
+        if (!workspace || workspace_bytes < lay.total + round256((size_t)num_q_tokens * 4) ||
+            (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return PKV_ERR_INVALID;
+        unsigned char *ws = static_cast<unsigned char *>(workspace);
+        a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
+        a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
+        a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
+        q_lens = reinterpret_cast<int *>(ws + lay.total);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    pkv_status rc = head_dim == 128
+                        ? launch_multi_token<128>(a, q_starts, q_lens, num_q_tokens, max_q_len, (int)parts, st)
+                        : launch_multi_token<64>(a, q_starts, q_lens, num_q_tokens, max_q_len, (int)parts, st);
+    if (rc == PKV_OK && parts > 1) {
+        // one virtual sequence per query token, of length p + 1
+        DecodeArgs m = a;
+        m.num_seqs = num_q_tokens;
+        m.seq_lens = q_lens;
+        rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, false>(m, st)
+                             : launch_reduce<__nv_bfloat16, 64, true, false>(m, st);
+    }
+    return rc;
 }
 
 PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
