@@ -48,6 +48,12 @@ WORKLOADS = {
     "beam": wl.BEAM_BF16,
     "beam1032": wl.BEAM_BF16,
 }
+# Multi-token attention (several new tokens per sequence, causal): verification
+# of 4 drafted tokens plus one on the GQA shapes (bandwidth-bound, like decode),
+# and a 512-token prefill chunk at the end of 4096-token contexts (a dense
+# contraction).  (query tokens per sequence, fixed context or None = GQA lengths)
+MULTI_TOKEN = {"verify": (5, None, 64), "prefill": (512, 4096, 8)}
+
 # batches rotated so that no step re-reads the previous step's pool from L2
 ROTATE = {"gqa": 4, "tiny": 1, "long": 1, "mixed": 4, "beam": 4, "beam1032": 4}
 
@@ -58,7 +64,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(MULTI_TOKEN), default="gqa")
     p.add_argument("--block-size", type=int, default=0, help="override the block size (mixed sweep)")
     p.add_argument("--partition-size", type=int, default=0)
     p.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
@@ -471,10 +477,46 @@ def oracle_sample(shape, seed, budget_s, lens, kv="bf16"):
 
 
 # ---------------------------------------------------------------------------
+def run_reference_multi_token(args):
+    """The fp64 multi-token oracle on a bounded sample of the workload: per step
+    one sequence's context and its last min(Q, 16) query tokens."""
+    from oracle.multi_token import multi_token_attention
+    import oracle
+    shape = wl.GQA_BF16
+    Q, L_fixed, S = MULTI_TOKEN[args.workload]
+    lens = [L_fixed] * S if L_fixed else [max(Q, int(x)) for x in wl.draw_lengths(shape, args.seed + 1).tolist()]
+    qn = min(Q, 16)
+    times, bytes_ = [], []
+    for i in range(args.warmup + args.steps):
+        s = i % S
+        L = lens[s]
+        k, v = wl.draw_seq_kv(shape, args.seed + 1, s, L)
+        q = wl.draw_normal((qn, shape.num_heads, shape.head_dim), torch.bfloat16, wl.sub_seed(args.seed, 30, s))
+        t0 = time.perf_counter()
+        # the sample's queries are the context's last qn positions
+        multi_token_attention([q.float().numpy()], [k.float().numpy()], [v.float().numpy()], shape.scale)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            bytes_.append(L * shape.num_kv_heads * shape.head_dim * 2 * 2)
+    value = sum(bytes_) / sum(times) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload} (oracle sample: one sequence, last {qn} query tokens per step)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one sequence and its last {qn} query tokens per step, numpy fp64"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload in MULTI_TOKEN:
+        return run_reference_multi_token(args)
     shape = shape_for(args)
     lens = context_lengths(args, shape, args.seed + 1)
     per_step = max(1, len(lens) // 4)  # a bounded sample per step
@@ -719,10 +761,130 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * total_s / steps, 4)}
 
 
+def multi_token_batch(pkv, args, seed, device):
+    """One resident batch of a multi-token workload: pool written through the
+    library, the query rows of every sequence's last Q positions."""
+    shape = wl.GQA_BF16
+    Q, L_fixed, S = MULTI_TOKEN[args.workload]
+    B, Hkv, Hq, D = shape.block_size, shape.num_kv_heads, shape.num_heads, shape.head_dim
+    lens = [L_fixed] * S if L_fixed else [max(Q, int(x)) for x in wl.draw_lengths(shape, seed).tolist()]
+    need = sum(-(-L // B) for L in lens)
+    NB = max(64, math.ceil(1.1 * need))
+    alloc = pkv.BlockAllocator(NB, B)
+    order = wl.draw_block_ids(NB, seed)
+    for i in range(NB):
+        assert alloc.add_seq(-1 - i, B) == 0
+    for b in order[::-1]:
+        assert alloc.free_seq(-1 - int(b)) == 0
+    g = torch.Generator(device=device)
+    g.manual_seed(int(wl.sub_seed(seed, 9)))
+    kc = torch.zeros((NB, Hkv, B, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    for s, L in enumerate(lens):
+        assert alloc.add_seq(s, L) == 0
+        slots = torch.from_numpy(alloc.slots(s, 0, L)).to(device)
+        k = torch.randn((L, Hkv, D), generator=g, device=device).to(torch.bfloat16)
+        pkv.kv_cache_write(k, torch.randn_like(k), kc, vc, slots)
+    maxb = max(-(-L // B) for L in lens)
+    tables, seq_lens = alloc.block_tables(np.arange(S), maxb)
+    T = Q * S
+    b = dict(lens=lens, Q=Q, kc=kc, vc=vc, tables=torch.from_numpy(tables).to(device),
+             seq_lens=torch.from_numpy(seq_lens).to(device),
+             starts=torch.arange(0, T + 1, Q, dtype=torch.int32, device=device),
+             q=torch.randn((T, Hq, D), generator=g, device=device).to(torch.bfloat16),
+             max_seq_len=maxb * B)
+    b["out"] = torch.empty_like(b["q"])
+    ws = pkv.paged_attention_multi_token_workspace_size(T, Hq, D, b["max_seq_len"])
+    b["ws"] = torch.zeros(max(ws, 256), dtype=torch.uint8, device=device)
+    b["kv_bytes"] = sum(lens) * Hkv * D * 2 * 2
+    # useful flops: per query at position p, per query head: QK^T and PV over p + 1 tokens
+    b["flops"] = sum(4 * D * Hq * (L - Q + i + 1) for L in lens for i in range(Q))
+    b["alg_bytes"] = b["kv_bytes"] + 2 * T * Hq * D * 2 + 4 * need + 4 * S + 4 * (S + 1)
+    return b
+
+
+def run_multi_token_bench(args):
+    """Multi-token attention calls (§ chunked prefill / verification), timed like
+    the decode step: K calls in one CUDA graph over rotated resident batches."""
+    rank, world, local = dist_env()
+    import paged_kv_cache_279_gb300 as pkv
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    shape = wl.GQA_BF16
+    nrot = 4
+    batches = [multi_token_batch(pkv, args, args.seed + 1000 * rank + r, device) for r in range(nrot)]
+
+    def call(b):
+        return lambda: pkv.paged_attention_multi_token(b["out"], b["q"], b["kc"], b["vc"], b["tables"], b["seq_lens"],
+                                                       b["starts"], shape.scale, b["Q"], b["max_seq_len"], b["ws"])
+    stream = torch.cuda.Stream(device)
+    steps, warmup = args.steps, max(3, args.warmup)
+    warm = capture([call(batches[i % nrot]) for i in range(warmup)], stream)
+    timed = capture([call(batches[i % nrot]) for i in range(steps)], stream)
+    assert pkv.read_device_errors() == 0
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time_graph(warm, stream)
+        total_ms = time_graph(timed, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_s = max_over_ranks(total_ms / 1e3, world, device)
+    kvb = sum_over_ranks(sum(batches[i % nrot]["kv_bytes"] for i in range(steps)), world, device)
+    flops = sum(batches[i % nrot]["flops"] for i in range(steps)) * world
+    alg = sum(batches[i % nrot]["alg_bytes"] for i in range(steps)) / steps
+    ms = 1e3 * total_s / steps
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    if args.workload == "prefill":
+        achieved = flops / total_s / 1e12
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": "paged_attention_multi_token (mma.sync bf16, N = 8 query heads of a KV head)",
+                    "peak_source": "measured bf16 GEMM burst" if "bf16_tflops" in peaks else "fallback",
+                    "useful_flops_per_call": round(flops / steps / world)}
+    else:
+        achieved = alg / (ms / 1e3) / 1e9
+        peak = float(peaks.get("hbm_gbs", 6800.0))
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": "paged_attention_multi_token", "algorithmic_bytes": round(alg),
+                    "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
+    Q, L_fixed, S = MULTI_TOKEN[args.workload]
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(kvb / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {S} seqs x {Q} query tokens, "
+                                   f"{'context ' + str(L_fixed) if L_fixed else 'GQA context lengths U[64, 2048]'}, "
+                                   f"32q/8kv heads, head_dim 128, block 16",
+                       "l2": f"inputs larger than L2: {nrot} resident batches rotated"},
+            "query_tokens_per_s": round(world * S * Q / (ms / 1e3), 1),
+            "roofline": roofline, "cpu_baseline": None, "e2e": None,
+            "gpu_launches": steps * (1 + (1 if batches[0]["max_seq_len"] > 1024 else 0)),
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in MULTI_TOKEN:
+        return run_multi_token_bench(args)
     return run_ours(args)
 
 
