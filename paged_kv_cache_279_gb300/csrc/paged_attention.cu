@@ -3213,7 +3213,7 @@ PKV_API size_t paged_attention_multi_token_workspace_size(int num_q_tokens, int 
 template <int D>
 static pkv_status launch_multi_token(const DecodeArgs &a, const int32_t *q_starts, int *q_lens, int num_q_tokens,
                                      int max_q_len, int parts, cudaStream_t st) {
-    constexpr int NS = 4;
+    constexpr int NS = 8;  // 64 KB of tiles in flight per CTA (two CTAs per SM)
     static bool done[128] = {};
     constexpr int smem = mt_smem_bytes<D, NS>();
     auto kern = multi_token_kernel<D, NS>;
