@@ -639,7 +639,8 @@ def run_ours(args):
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch",
                 "traffic_source": traffic_src, "algorithmic_bytes": round(dec_alg_bytes),
                 "kernel": ("paged_attention_decode_fp8" if args.kv == "fp8" else "paged_attention_decode")
-                          + " (attention kernel + merge kernel)",
+                          + (" (prefix, attention and merge kernels)" if args.workload.startswith("beam")
+                             else " (one kernel: attention and in-kernel merge)"),
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
                 "decode_us": round(dec_ms * 1e3, 2)}
 

@@ -1,7 +1,15 @@
 // Paged decode attention: one new query per sequence attends to every cached
 // token of that sequence, whose K/V rows are found through the sequence's
-// block table.  Long contexts are split into partitions that are attended
-// independently; a reduction kernel merges their partial results.
+// block table.  Kernels in this file:
+//   * decode_bf16_streamk_kernel -- the balanced split (bf16, and an FP8
+//     variant): every warp takes an equal share of all contexts' tiles, stores
+//     the step's new tokens, and merges the contexts it cuts (see its header).
+//   * decode_bf16_mma_kernel / decode_simt_kernel -- fixed partitions (bf16 /
+//     fp32), whose partials decode_reduce_kernel merges.
+//   * decode_bf16_prefix_tc_kernel / decode_bf16_prefix_kernel -- shared
+//     prefixes of grouped calls (tcgen05 / mma.sync), merged with each
+//     member's own tokens by decode_reduce_kernel.
+//   * multi_token_kernel -- several causal query tokens per sequence.
 //
 // Sources: "KV cache & PagedAttention -- vi sao chatbot AI ton bo nho"
 // (aiwiki.vn), second paragraph (the current query against the keys of the
@@ -594,15 +602,12 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 }
 
 // ---------------------------------------------------------------------------
-// Balanced (stream-K) bf16 kernel.  All (sequence, kv head) segments are laid
-// end to end as one list of 16-token tiles, and each persistent CTA takes an
-// equal, contiguous share of that list.  Inside a CTA the warps take every
-// NW-th tile and keep their TMA rings running across segment boundaries.
-// Where a segment ends inside the share, the warps merge through shared
-// memory and the CTA stores the result: the final rows if it holds the whole
-// segment, otherwise one partial ("piece") that the piece-merge kernel
-// combines.  Every CTA streams the same number of bytes, so no SM idles in a
-// tail wave and no ring drains between work items.
+// Balanced (stream-K) kernel: all (sequence, kv head) segments are laid end to
+// end as one list of tiles, and every warp of a persistent one-wave grid takes
+// an equal, contiguous share of that list, streaming it through its own TMA
+// ring across segment boundaries.  Every warp streams the same number of
+// bytes, so no SM idles in a tail wave.  The helpers below: the shared-memory
+// layout, a cursor over the tile list, share ownership, tile rows.
 // ---------------------------------------------------------------------------
 constexpr int kMinTilesPerCta = 16;  // >= 256 tokens per share: bounds pieces per segment
 
