@@ -94,6 +94,51 @@ def test_fp8_host_validation_rejects_before_launch():
     assert dec() == pkv.PKV_ERR_INVALID                # null pointers
 
 
+def test_multi_token_host_validation_and_workspace():
+    lib = _lib.load()
+    f = lib.paged_attention_multi_token
+
+    def call(S=2, T=10, Hq=32, Hkv=8, D=128, B=16, maxB=8, NB=64, maxQ=5, maxL=128, scale=0.1):
+        return f(None, None, None, None, None, None, None, S, T, Hq, Hkv, D, B, maxB, NB, maxQ, maxL, scale,
+                 None, 0, None)
+    assert call(D=96) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(B=12) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(Hq=72) == pkv.PKV_ERR_UNSUPPORTED        # 9 query heads per KV head
+    assert call(Hq=30) == pkv.PKV_ERR_INVALID
+    assert call(scale=float("nan")) == pkv.PKV_ERR_INVALID
+    assert call(T=-1) == pkv.PKV_ERR_INVALID
+    assert call(S=0) == pkv.PKV_OK and call(T=0) == pkv.PKV_OK
+    assert call(maxQ=0) == pkv.PKV_ERR_INVALID
+    assert call() == pkv.PKV_ERR_INVALID                 # null pointers
+    # grid.z = query blocks x 1024-token partitions must fit 65535: checked on
+    # the host after the pointers (dummy, 16-byte aligned, never dereferenced:
+    # the call is rejected before any launch)
+    p = ctypes.c_void_p(256)
+    assert f(p, p, p, p, p, p, p, 2, 10, 32, 8, 128, 16, 8, 64, 8 * 4096, 20 * 1024, 0.1, p, 1 << 30,
+             None) == pkv.PKV_ERR_UNSUPPORTED
+    ws = lib.paged_attention_multi_token_workspace_size
+    assert ws(10, 32, 128, 1024) == 0                     # one partition: no scratch
+    r = lambda x: (x + 255) // 256 * 256
+    n = 10 * 32 * 3                                       # 3 partitions of 1024 for 3000 tokens
+    assert ws(10, 32, 128, 3000) == n * 128 * 4 + 2 * r(n * 4) + r(10 * 4)
+    assert ws(0, 32, 128, 3000) == 0
+
+
+def test_decode_append_fp8_host_validation():
+    lib = _lib.load()
+    f = lib.paged_attention_decode_append_fp8
+
+    def call(S=2, D=128, B=16, knew=True, maxL=64, ks=0.1):
+        k = ctypes.c_void_p(16) if knew else None
+        return f(None, None, k, k, None, None, None, None, S, 32, 8, D, B, 4, 16, maxL, 0.1, ks, 0.1, None, 0, None)
+    assert call(knew=False) == pkv.PKV_ERR_INVALID        # no new tokens to store
+    assert call(maxL=0) == pkv.PKV_ERR_INVALID            # every context holds its new token
+    assert call(D=64) == pkv.PKV_ERR_UNSUPPORTED
+    assert call(ks=0.0) == pkv.PKV_ERR_INVALID
+    assert call(S=0) == pkv.PKV_OK
+    assert call() == pkv.PKV_ERR_INVALID                  # null q / out / caches
+
+
 def test_workspace_size_formula():
     lib = _lib.load()
     # a single partition needs no scratch
