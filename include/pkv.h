@@ -509,6 +509,19 @@ PKV_EXPORT pkv_status block_allocator_prefix_groups(const pkv_allocator *a, cons
                                          int *num_groups_out);
 
 /*
+ * block_allocator_truncate -- keep the first num_tokens tokens of `seq`
+ * (0 <= num_tokens <= its length, else PKV_ERR_INVALID), e.g. to roll back
+ * drafted tokens that verification rejected ("vLLM PagedAttention: Buoc dot
+ * pha ...", speculative decoding).  Blocks wholly past the new end lose this
+ * sequence's reference (freed, or parked as evictable if registered in the
+ * prefix cache); a shared last block is copied on the next append as usual; a
+ * registered block that becomes the partially filled last block of its only
+ * holder is unregistered (the next append writes into it).  Device data is
+ * not touched.
+ */
+PKV_EXPORT pkv_status block_allocator_truncate(pkv_allocator *a, int64_t seq, int64_t num_tokens);
+
+/*
  * block_allocator_add_seq_cached -- block_allocator_add_seq for a prompt
  * whose token ids are known, reusing the K/V of earlier prompts that start
  * with the same tokens (prefix caching).

@@ -42,6 +42,10 @@ mechanism; the reading modelled here (and listed in the design notes):
   them); ``num_free`` counts both;
 * ``cache_clear`` moves the evictable blocks (front first) to the free stack
   and forgets every registration.
+
+Truncation (rolling back drafted tokens that verification rejected -- same
+page, speculative decoding): ``truncate(seq, n)`` keeps the first n tokens;
+the reading modelled here is in its docstring.
 """
 from __future__ import annotations
 
@@ -188,6 +192,31 @@ class BlockAllocatorModel:
         for b in reversed(table):
             if self._ref[b] == 0 and b in self._key:
                 self._evictable.append(b)
+        return OK
+
+    def truncate(self, seq: int, num_tokens: int) -> int:
+        """Keep the first ``num_tokens`` tokens of ``seq`` (drafted tokens that
+        verification rejected, for instance).  Blocks wholly past the new end
+        are released in table order; registered ones left without holders join
+        the evictable queue, the later block first.  A registered block that
+        becomes the partially filled last block of its only holder loses its
+        registration: the next append writes into it."""
+        if seq not in self._seqs:
+            return ERR_INVALID
+        table, n = self._seqs[seq]
+        if num_tokens < 0 or num_tokens > n:
+            return ERR_INVALID
+        keep = -(-num_tokens // self.block_size)
+        dropped = table[keep:]
+        del table[keep:]
+        for b in dropped:
+            self._release(b)
+        for b in reversed(dropped):
+            if self._ref[b] == 0 and b in self._key:
+                self._evictable.append(b)
+        self._seqs[seq][1] = num_tokens
+        if keep and num_tokens % self.block_size and table[-1] in self._key and self._ref[table[-1]] == 1:
+            del self._cache[self._key.pop(table[-1])]
         return OK
 
     # -- queries --------------------------------------------------------------

@@ -424,6 +424,10 @@ class BlockAllocator:
                                                     ctypes.byref(ncow))
         return st, slots, pairs[:ncow.value]
 
+    def truncate(self, seq: int, num_tokens: int) -> int:
+        """Keep the first num_tokens tokens of seq (roll back rejected drafts)."""
+        return int(self._lib.block_allocator_truncate(self._h, int(seq), int(num_tokens)))
+
     def fork(self, parent: int, child: int) -> int:
         return self._lib.block_allocator_fork(self._h, int(parent), int(child))
 

@@ -225,6 +225,30 @@ pkv_status block_allocator_free_seq(pkv_allocator *a, int64_t seq) {
     return PKV_OK;
 }
 
+pkv_status block_allocator_truncate(pkv_allocator *a, int64_t seq, int64_t num_tokens) {
+    if (!a) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return PKV_ERR_INVALID;
+    pkv_allocator::Seq &s = it->second;
+    if (num_tokens < 0 || num_tokens > s.tokens) return PKV_ERR_INVALID;
+    const int B = a->block_size;
+    const size_t keep = (size_t)((num_tokens + B - 1) / B);
+    // blocks wholly past the new end: released in table order, registered ones
+    // left without holders parked last block first (as when a sequence is freed)
+    for (size_t i = keep; i < s.table.size(); ++i) a->release(s.table[i]);
+    for (size_t i = s.table.size(); i-- > keep;)
+        if (a->refcnt[s.table[i]] == 0 && a->cached[s.table[i]]) a->park(s.table[i]);
+    s.table.resize(keep);
+    s.tokens = num_tokens;
+    // a registered block that is now this holder's partially filled last block
+    // would be written in place by the next append: it loses its registration
+    if (keep > 0 && num_tokens % B != 0) {
+        const int32_t b = s.table.back();
+        if (a->cached[b] && a->refcnt[b] == 1) a->unregister(b);
+    }
+    return PKV_OK;
+}
+
 pkv_status block_allocator_add_seq_cached(pkv_allocator *a, int64_t seq, const int32_t *tokens,
                                           int64_t num_tokens, int64_t *cached_tokens_out) {
     if (!a || num_tokens < 0 || (num_tokens > 0 && !tokens) || a->seqs.count(seq)) return PKV_ERR_INVALID;

@@ -37,6 +37,8 @@ def run_ops(ops, num_blocks, block_size):
             assert c.add_seq_cached(op[1], op[2]) == m.add_seq_cached(op[1], op[2])
         elif kind == "clear":
             assert c.cache_clear() == m.cache_clear()
+        elif kind == "truncate":
+            assert c.truncate(op[1], op[2]) == m.truncate(op[1], op[2])
         assert_same_state(c, m, m.sequences())
         assert c.cache_stats() == m.cache_stats()
     return c, m
@@ -55,6 +57,8 @@ def random_ops(rnd, n, block_size):
             child = len(ids) + 100
             ops.append(("fork", rnd.choice(ids), child))
             ids.append(child)
+        elif r < 0.9:
+            ops.append(("truncate", rnd.choice(ids), rnd.randint(-1, 3 * block_size)))
         else:
             ops.append(("free", rnd.choice(ids)))
     return ops
@@ -201,6 +205,8 @@ def prompt_ops(rnd, n, block_size, vocab=3):
             child = len(ids) + 10000
             ops.append(("fork", rnd.choice(ids), child))
             ids.append(child)
+        elif r < 0.85:
+            ops.append(("truncate", rnd.choice(ids), rnd.randint(0, 5 * block_size)))
         elif r < 0.97:
             ops.append(("free", rnd.choice(ids)))
         else:

@@ -206,3 +206,59 @@ def test_prefix_cache_oom_changes_nothing_and_clear_forgets():
     assert m.free_seq(0) == OK and m.cache_clear() == OK
     assert m.cache_stats()["cached_blocks"] == 0 and m.num_free() == 3
     assert m.add_seq_cached(1, [1, 2, 3, 4]) == (OK, 0)
+
+
+# ---------------------------------------------------------------------------
+# Truncation (rolling back rejected drafted tokens)
+# ---------------------------------------------------------------------------
+def test_truncate_releases_whole_blocks_and_appends_reuse_the_slots():
+    m = BlockAllocatorModel(16, 16)
+    assert m.add_seq(0, 100) == OK                  # blocks 0..6, the last holds 4 tokens
+    assert m.truncate(0, 40) == OK
+    assert m.block_table(0) == [0, 1, 2] and m.num_tokens(0) == 40
+    assert m.num_free() == 13
+    # position 40 is block 2, offset 8 again
+    assert m.append_slot(0) == (OK, 2 * 16 + 8, -1, -1)
+    # fill block 2 (positions 41..47); blocks 3..6 went back in table order, so the
+    # next fresh block is 6
+    for _ in range(7):
+        assert m.append_slot(0)[0] == OK
+    assert m.append_slot(0) == (OK, 6 * 16, -1, -1)
+    assert m.truncate(0, 0) == OK and m.block_table(0) == [] and m.num_free() == 16
+    # blocks 0, 1, 2, 6 went back in table order: block 6 is handed out next
+    assert m.append_slot(0) == (OK, 6 * 16, -1, -1)
+
+
+def test_truncate_into_a_shared_block_copies_it_on_the_next_append():
+    m = BlockAllocatorModel(16, 16)
+    m.add_seq(0, 40)                                # blocks 0, 1, 2 (2 holds 8 tokens)
+    m.fork(0, 1)
+    assert m.truncate(1, 20) == OK                  # keeps 0, 1; block 1 now partial for seq 1
+    assert m.refcount(2) == 1 and m.refcount(1) == 2
+    st, slot, src, dst = m.append_slot(1)           # position 20 lands in shared block 1: copy
+    assert st == OK and src == 1 and dst not in (0, 1, 2) and slot == dst * 16 + 4
+    assert m.append_slot(0) == (OK, 2 * 16 + 8, -1, -1)  # seq 0 alone holds block 2
+
+
+def test_truncate_unregisters_a_cached_block_it_will_write_and_parks_dropped_ones():
+    m = BlockAllocatorModel(8, 16)
+    prompt = list(range(100, 148))                  # 3 full blocks, all registered
+    assert m.add_seq_cached(0, prompt) == (OK, 0)
+    assert m.cache_stats()["cached_blocks"] == 3
+    assert m.truncate(0, 20) == OK                  # keeps blocks 0, 1 (1 now partial)
+    stats = m.cache_stats()
+    # block 1 (partial, sole holder) unregistered; block 2 dropped but still registered
+    assert stats["cached_blocks"] == 2 and stats["evictable_blocks"] == 1
+    assert m.num_free() == 8 - 2
+    # a new prompt with the same tokens finds only block 0 (its chain stops at block 1)
+    assert m.add_seq_cached(1, prompt) == (OK, 16)
+
+
+def test_truncate_rejects_bad_arguments_and_changes_nothing():
+    m = BlockAllocatorModel(8, 16)
+    m.add_seq(0, 30)
+    before = (m.block_table(0), m.num_tokens(0), m.num_free())
+    assert m.truncate(0, 31) == ERR_INVALID
+    assert m.truncate(0, -1) == ERR_INVALID
+    assert m.truncate(7, 0) == ERR_INVALID
+    assert (m.block_table(0), m.num_tokens(0), m.num_free()) == before
