@@ -8,8 +8,13 @@ is no CPU or PyTorch fallback.
     kv_cache_write(k_new, v_new, k_cache, v_cache, slot_mapping)
     paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens,
                            scale, max_seq_len, partition_size=0, workspace=None)
+    paged_attention_decode_append(...)    # store the step's new tokens, then attend
+    paged_attention_decode_grouped(...)   # beams sharing prefix blocks: each read once
+    paged_attention_multi_token(...)      # several causal query tokens per sequence
+    kv_cache_write_fp8(...), paged_attention_decode_fp8(...),
+    paged_attention_decode_append_fp8(...)  # E4M3 cache, per-tensor scales
     block_copy(k_caches, v_caches, block_pairs)
-    BlockAllocator(num_blocks, block_size)   # host allocator, CoW semantics
+    BlockAllocator(num_blocks, block_size)   # host allocator: CoW, prefix cache, truncation
 """
 from __future__ import annotations
 
