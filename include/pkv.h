@@ -509,6 +509,18 @@ PKV_EXPORT pkv_status block_allocator_prefix_groups(const pkv_allocator *a, cons
                                          int *num_groups_out);
 
 /*
+ * block_allocator_extend -- room for `count` more tokens of `seq` at once (a
+ * prefill chunk, drafted tokens): writes slots_out[count] (host int64) for
+ * positions len .. len+count-1, exactly as `count` calls of
+ * block_allocator_append_slot would, but all or nothing (PKV_ERR_OOM changes
+ * nothing).  At most one copy-on-write pair can arise (a shared, partially
+ * filled last block); it is reported in *cow_src_out / *cow_dst_out (-1 if
+ * none) and must be copied (block_copy) before the new tokens are written.
+ */
+PKV_EXPORT pkv_status block_allocator_extend(pkv_allocator *a, int64_t seq, int64_t count, int64_t *slots_out,
+                                             int32_t *cow_src_out, int32_t *cow_dst_out);
+
+/*
  * block_allocator_truncate -- keep the first num_tokens tokens of `seq`
  * (0 <= num_tokens <= its length, else PKV_ERR_INVALID), e.g. to roll back
  * drafted tokens that verification rejected ("vLLM PagedAttention: Buoc dot

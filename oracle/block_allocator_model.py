@@ -194,6 +194,27 @@ class BlockAllocatorModel:
                 self._evictable.append(b)
         return OK
 
+    def extend(self, seq: int, count: int):
+        """Room for ``count`` more tokens of ``seq`` at once (a prefill chunk):
+        the same slots and copy pair as ``count`` calls of append_slot, but all
+        or nothing.  Returns (status, slots, cow_src, cow_dst)."""
+        if seq not in self._seqs or count < 0:
+            return ERR_INVALID, [], -1, -1
+        table, n = self._seqs[seq]
+        B = self.block_size
+        shared_partial = n % B != 0 and self._ref[table[-1]] > 1
+        need = -(-(n + count) // B) - -(-n // B) + (1 if shared_partial and count > 0 else 0)
+        if need > self._available():
+            return ERR_OOM, [], -1, -1
+        slots, src, dst = [], -1, -1
+        for _ in range(count):
+            st, slot, s_, d_ = self.append_slot(seq)
+            assert st == OK
+            slots.append(slot)
+            if s_ >= 0:
+                src, dst = s_, d_
+        return OK, slots, src, dst
+
     def truncate(self, seq: int, num_tokens: int) -> int:
         """Keep the first ``num_tokens`` tokens of ``seq`` (drafted tokens that
         verification rejected, for instance).  Blocks wholly past the new end

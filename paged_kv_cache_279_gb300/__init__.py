@@ -429,6 +429,18 @@ class BlockAllocator:
                                                     ctypes.byref(ncow))
         return st, slots, pairs[:ncow.value]
 
+    def extend(self, seq: int, count: int):
+        """Slots for ``count`` more tokens of seq (all or nothing).  Returns
+        (status, slots int64 [count], cow_src, cow_dst)."""
+        slots = np.zeros(max(int(count), 1), dtype=np.int64)
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        st = int(self._lib.block_allocator_extend(self._h, int(seq), int(count),
+                                                  slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                                  ctypes.byref(src), ctypes.byref(dst)))
+        if st != PKV_OK:
+            return st, slots[:0], -1, -1
+        return st, slots[:int(count)], int(src.value), int(dst.value)
+
     def truncate(self, seq: int, num_tokens: int) -> int:
         """Keep the first num_tokens tokens of seq (roll back rejected drafts)."""
         return int(self._lib.block_allocator_truncate(self._h, int(seq), int(num_tokens)))

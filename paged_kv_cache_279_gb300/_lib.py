@@ -58,6 +58,7 @@ SIGNATURES = {
     "block_allocator_create": (c_void_p, [c_int, c_int]),
     "block_allocator_destroy": (None, [c_void_p]),
     "block_allocator_add_seq": (c_int, [c_void_p, c_int64, c_int64]),
+    "block_allocator_extend": (c_int, [c_void_p, c_int64, c_int64, P(c_int64), P(c_int32), P(c_int32)]),
     "block_allocator_truncate": (c_int, [c_void_p, c_int64, c_int64]),
     "block_allocator_add_seq_cached": (c_int, [c_void_p, c_int64, c_void_p, c_int64, P(c_int64)]),
     "block_allocator_cache_stats": (c_int, [c_void_p, P(c_int64), P(c_int64), P(c_int), P(c_int)]),

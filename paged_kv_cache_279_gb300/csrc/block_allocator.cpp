@@ -225,6 +225,36 @@ pkv_status block_allocator_free_seq(pkv_allocator *a, int64_t seq) {
     return PKV_OK;
 }
 
+pkv_status block_allocator_extend(pkv_allocator *a, int64_t seq, int64_t count, int64_t *slots_out,
+                                  int32_t *cow_src_out, int32_t *cow_dst_out) {
+    if (!a || count < 0 || (count > 0 && !slots_out)) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq);
+    if (it == a->seqs.end()) return PKV_ERR_INVALID;
+    pkv_allocator::Seq &s = it->second;
+    const int B = a->block_size;
+    const bool shared_partial = s.tokens % B != 0 && a->refcnt[s.table.back()] > 1;
+    const int64_t need = (s.tokens + count + B - 1) / B - (s.tokens + B - 1) / B + (shared_partial && count > 0);
+    if (need > a->available()) return PKV_ERR_OOM;  // nothing changed
+    try {
+        s.table.reserve(s.table.size() + (size_t)need);
+    } catch (...) {
+        return PKV_ERR_INVALID;
+    }
+    int32_t src = -1, dst = -1;
+    for (int64_t i = 0; i < count; ++i) {
+        int32_t cs = -1, cd = -1;
+        const pkv_status st = block_allocator_append_slot(a, seq, &slots_out[i], &cs, &cd);
+        if (st != PKV_OK) return st;  // cannot happen: blocks were counted above
+        if (cs >= 0) {
+            src = cs;
+            dst = cd;
+        }
+    }
+    if (cow_src_out) *cow_src_out = src;
+    if (cow_dst_out) *cow_dst_out = dst;
+    return PKV_OK;
+}
+
 pkv_status block_allocator_truncate(pkv_allocator *a, int64_t seq, int64_t num_tokens) {
     if (!a) return PKV_ERR_INVALID;
     auto it = a->seqs.find(seq);

@@ -39,6 +39,9 @@ def run_ops(ops, num_blocks, block_size):
             assert c.cache_clear() == m.cache_clear()
         elif kind == "truncate":
             assert c.truncate(op[1], op[2]) == m.truncate(op[1], op[2])
+        elif kind == "extend":
+            cs, cslots, csrc, cdst = c.extend(op[1], op[2])
+            assert (cs, cslots.tolist(), csrc, cdst) == m.extend(op[1], op[2])
         assert_same_state(c, m, m.sequences())
         assert c.cache_stats() == m.cache_stats()
     return c, m
@@ -57,8 +60,10 @@ def random_ops(rnd, n, block_size):
             child = len(ids) + 100
             ops.append(("fork", rnd.choice(ids), child))
             ids.append(child)
-        elif r < 0.9:
+        elif r < 0.85:
             ops.append(("truncate", rnd.choice(ids), rnd.randint(-1, 3 * block_size)))
+        elif r < 0.9:
+            ops.append(("extend", rnd.choice(ids + [999]), rnd.randint(-1, 2 * block_size + 3)))
         else:
             ops.append(("free", rnd.choice(ids)))
     return ops
@@ -205,8 +210,10 @@ def prompt_ops(rnd, n, block_size, vocab=3):
             child = len(ids) + 10000
             ops.append(("fork", rnd.choice(ids), child))
             ids.append(child)
-        elif r < 0.85:
+        elif r < 0.82:
             ops.append(("truncate", rnd.choice(ids), rnd.randint(0, 5 * block_size)))
+        elif r < 0.85:
+            ops.append(("extend", rnd.choice(ids), rnd.randint(0, 2 * block_size)))
         elif r < 0.97:
             ops.append(("free", rnd.choice(ids)))
         else:

@@ -262,3 +262,22 @@ def test_truncate_rejects_bad_arguments_and_changes_nothing():
     assert m.truncate(0, -1) == ERR_INVALID
     assert m.truncate(7, 0) == ERR_INVALID
     assert (m.block_table(0), m.num_tokens(0), m.num_free()) == before
+
+
+def test_extend_equals_single_appends_and_is_all_or_nothing():
+    a = BlockAllocatorModel(16, 16)
+    b = BlockAllocatorModel(16, 16)
+    for m in (a, b):
+        m.add_seq(0, 40)
+        m.fork(0, 1)                                # block 2 (8 tokens) shared
+    st, slots, src, dst = a.extend(1, 30)           # positions 40..69 of seq 1
+    singles = [b.append_slot(1) for _ in range(30)]
+    assert st == OK and slots == [x[1] for x in singles]
+    # the shared partial block is copied once, at the first token
+    assert (src, dst) == (singles[0][2], singles[0][3]) and src == 2
+    assert a.block_table(1) == b.block_table(1) and a.num_free() == b.num_free()
+    # not enough blocks: nothing changes
+    before = (a.block_table(1), a.num_tokens(1), a.num_free())
+    assert a.extend(1, 16 * 16)[0] == ERR_OOM
+    assert (a.block_table(1), a.num_tokens(1), a.num_free()) == before
+    assert a.extend(1, 0) == (OK, [], -1, -1) and a.extend(1, -1)[0] == ERR_INVALID
