@@ -1595,7 +1595,10 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (!ready) __nanosleep(64);
         }
         if (!ready && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+        // each lane saw some of the flags: acquire, then order every lane's
+        // reads after every lane's acquire
         fence_acq_rel_gpu();
+        __syncwarp();
         const int sq = (int)(merge_seg / Hkv), kvh = (int)(merge_seg - (int64_t)sq * Hkv);
         merge_segment<D, NS * Lay::kStage / 32>(a.part_o, a.part_m, a.part_l, static_cast<__nv_bfloat16 *>(a.out),
                                                 (int64_t)sq * a.num_heads + kvh * a.group, a.group, a.max_parts,
