@@ -418,7 +418,10 @@ PKV_EXPORT pkv_status paged_attention_decode_grouped(void *out, const void *q, c
  *
  * The first call on a device looks up that device's address of the array
  * (cudaGetSymbolAddress) with the device current; make that first call before
- * any stream capture.  Every call on a device shares the one array and leaves
+ * any stream capture.  The address is cached per device together with the
+ * CUDA context it was taken in; a call from another context (a context the
+ * caller created, or a primary context created anew after cudaDeviceReset)
+ * looks it up again, so make such a call outside stream capture too.  Every call on a device shares the one array and leaves
  * its partials there: nothing in it has to start at zero (each call writes
  * every partial it later reads), but calls whose work overlaps on the GPU --
  * two streams, or two host threads -- race on it and must be serialised by
@@ -594,6 +597,29 @@ PKV_EXPORT int block_allocator_refcount(const pkv_allocator *a, int32_t block);
  * 1 - used / allocated. */
 PKV_EXPORT pkv_status block_allocator_waste(const pkv_allocator *a, int64_t *used_tokens,
                                  int64_t *allocated_slots);
+
+/*
+ * Diagnostics of the balanced split (host only, no device work).  They expose
+ * the arithmetic the balanced decode kernel runs, so that host-side tests can
+ * check the invariants its in-kernel merge relies on against the kernel's own
+ * code rather than a copy.  Not part of the method: the pages say nothing
+ * about how a kernel divides its work.
+ *
+ * pkv_balanced_slots: partial slots per (sequence, query head) that the
+ *   workspace of a balanced call holds for contexts of up to max_seq_len
+ *   tokens (ceil(max_seq_len / 256) + 1); -1 if max_seq_len < 0.
+ * pkv_balanced_split_parts: number of equal shares the kernel cuts
+ *   total_tiles tiles into, when the longest (sequence, kv head) segment has
+ *   max_segment_tiles tiles and at most `warps` warps take shares; 0 when
+ *   there is no tile, -1 for a negative argument or warps < 1.
+ * pkv_balanced_share_owner: the share (0 .. parts-1) holding tile `tile` of
+ *   the total_tiles tiles cut into `parts` shares [floor(c T / parts),
+ *   floor((c + 1) T / parts)); -1 for arguments out of range.
+ */
+PKV_EXPORT int pkv_balanced_slots(int max_seq_len);
+PKV_EXPORT int64_t pkv_balanced_split_parts(int64_t total_tiles, int max_segment_tiles, int max_seq_len,
+                                            int64_t warps);
+PKV_EXPORT int64_t pkv_balanced_share_owner(int64_t tile, int64_t total_tiles, int64_t parts);
 
 #ifdef __cplusplus
 }

@@ -661,12 +661,6 @@ struct SegCursor {
     }
 };
 
-// CTA whose share holds tile t when T tiles are split into `parts` shares
-// [floor(c T / parts), floor((c+1) T / parts)).
-__device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, int64_t parts) {
-    return ((t + 1) * parts + T - 1) / T - 1;
-}
-
 __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
 
 // TMA rows and valid-row mask of one tile: tile `tile` of segment (seq, kvh)
@@ -1255,10 +1249,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     // kMinTilesPerCta, and less when every segment is short, which spreads
     // many short contexts over more warps.
     const int own_slots = grouped ? a.prefix_slot : a.max_parts;
-    const int64_t min_share = own_slots > 1 ? max(1, (seg_max + own_slots - 2) / (own_slots - 1)) : (int64_t)T;
-    int64_t parts = T / max((int64_t)1, min_share);
-    if (parts < 1) parts = 1;
-    if (parts > (int64_t)gridDim.x * NW) parts = (int64_t)gridDim.x * NW;
+    const int64_t parts = balanced_parts(T, seg_max, own_slots, (int64_t)gridDim.x * NW);
     const int64_t gw0 = (int64_t)blockIdx.x * NW;
     if (T == 0 || gw0 >= parts) return;
     const int64_t cta_lo = gw0 * T / parts;
@@ -2875,14 +2866,9 @@ static pkv_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size
     return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? launch_status() : PKV_ERR_CUDA;
 }
 
-// Launch shapes (warps per CTA x ring stages per warp).  The environment
-// variables PKV_DECODE_VARIANT / PKV_BALANCED_VARIANT select another shape
-// for tuning sweeps; the defaults are the shapes measured fastest on GB300.
-static int env_variant(const char *name) {
-    const char *s = std::getenv(name);
-    return s ? std::atoi(s) : 0;
-}
-
+// Launch shapes (warps per CTA x ring stages per warp): the shapes measured
+// fastest on GB300 (4 warps x 2 stages for the fixed-partition and balanced
+// kernels, bf16 and FP8).
 template <int D, int NW, int NS>
 static pkv_status launch_bf16(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
     static bool done[128] = {};
@@ -2896,13 +2882,7 @@ static pkv_status launch_bf16(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
 
 template <int D>
 static pkv_status dispatch_bf16(const DecodeArgs &a, dim3 grid, cudaStream_t st) {
-    static const int v = env_variant("PKV_DECODE_VARIANT");
-    switch (v) {
-        case 1: return launch_bf16<D, 4, 3>(a, grid, st);
-        case 2: return launch_bf16<D, 4, 1>(a, grid, st);
-        case 3: return launch_bf16<D, 8, 2>(a, grid, st);
-        default: return launch_bf16<D, 4, 2>(a, grid, st);
-    }
+    return launch_bf16<D, 4, 2>(a, grid, st);
 }
 
 template <int D, int NW, int NS>
@@ -2924,14 +2904,7 @@ static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
 
 template <int D>
 static pkv_status dispatch_balanced(const DecodeArgs &a, cudaStream_t st) {
-    static const int v = env_variant("PKV_BALANCED_VARIANT");
-    switch (v) {
-        case 1: return launch_balanced<D, 4, 3>(a, st);
-        case 2: return launch_balanced<D, 8, 2>(a, st);
-        case 3: return launch_balanced<D, 4, 4>(a, st);
-        case 4: return launch_balanced<D, 8, 3>(a, st);
-        default: return launch_balanced<D, 4, 2>(a, st);
-    }
+    return launch_balanced<D, 4, 2>(a, st);
 }
 
 // FP8 cache views.  K: [blocks * Hkv * B][D] bytes, box D x 16 rows, 128-byte
@@ -2976,13 +2949,7 @@ static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
 }
 
 static pkv_status dispatch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
-    static const int v = env_variant("PKV_FP8_VARIANT");
-    switch (v) {
-        case 1: return launch_balanced_f8<128, 4, 3>(a, st);
-        case 2: return launch_balanced_f8<128, 4, 1>(a, st);
-        case 3: return launch_balanced_f8<128, 8, 2>(a, st);
-        default: return launch_balanced_f8<128, 4, 2>(a, st);
-    }
+    return launch_balanced_f8<128, 4, 2>(a, st);
 }
 
 template <typename T, int D>
@@ -3353,11 +3320,9 @@ PKV_API pkv_status paged_attention_decode_append(
     // The balanced path stores the new tokens inside the attention kernel (also
     // for batches of many (sequence, kv head) segments: with the merge inside
     // the attention kernel, 256 x 8 segments ran 66.6 us fused against 70.1 us
-    // with a separate store kernel).  PKV_APPEND_SPLIT=1 forces the separate
-    // store kernel for comparisons.
-    const int split_env = env_variant("PKV_APPEND_SPLIT");
+    // with a separate store kernel).
     const bool fused = partition_size == 0 && dtype == PKV_BF16 && num_seqs > 0 &&
-                       num_seqs <= kMaxBalancedSeqs && max_seq_len > 0 && split_env != 1;
+                       num_seqs <= kMaxBalancedSeqs && max_seq_len > 0;
     if (!fused) {
         // other paths: the plain write (slot of position seq_lens[s] - 1 is
         // looked up on the device) followed by the decode
@@ -3506,7 +3471,7 @@ PKV_API pkv_status paged_attention_decode_grouped(
     // else one CTA per (group, kv head, 256 tokens) on mma.sync;
     // PKV_PREFIX_VARIANT=1 selects the latter for comparisons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool use_tc = num_groups <= tc::kMaxGroups && env_variant("PKV_PREFIX_VARIANT") != 1;
+    const bool use_tc = num_groups <= tc::kMaxGroups;
     pkv_status rc;
     if (use_tc) {
         a.prefix_pieces = reinterpret_cast<int *>(ws + npre_off);
@@ -3533,18 +3498,36 @@ PKV_API pkv_status paged_attention_decode_grouped(
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device, looked up on the
-// first call for that device (with the device current).  nullptr on failure.
+// Device address of g_noalloc_scratch in the current CUDA context, looked up
+// on the first call in that context (with the device current) and cached per
+// device together with the context it was taken in: a call from another
+// context (a non-primary context, or a primary context created again after
+// cudaDeviceReset) looks the address up again.  nullptr on failure.
 static void *noalloc_scratch_address() {
     static std::mutex mu;
     static void *ptrs[128] = {};
+    static CUcontext ctxs[128] = {};
+    static PFN_cuCtxGetCurrent_v4000 get_ctx = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (PFN_cuCtxGetCurrent_v4000) nullptr;
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }();
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    if (!get_ctx) return nullptr;
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
+    if (!ctx || !ptrs[dev] || ctxs[dev] != ctx) {
+        // (the lookup makes the device's primary context current if none is)
         void *p = nullptr;
         if (cudaGetSymbolAddress((void **)&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
         ptrs[dev] = p;
+        ctxs[dev] = ctx;
     }
     return ptrs[dev];
 }
@@ -3569,4 +3552,23 @@ PKV_API pkv_status paged_attention_decode_noalloc(void *out, const void *q, cons
                                   num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                   num_blocks, max_seq_len, scale, P, scratch,
                                   need > 0 ? PKV_NOALLOC_SCRATCH_BYTES : 0, dtype, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Diagnostics: the balanced split's arithmetic, for host-side tests.
+// ---------------------------------------------------------------------------
+PKV_API int64_t pkv_balanced_split_parts(int64_t total_tiles, int max_segment_tiles, int max_seq_len,
+                                         int64_t warps) {
+    if (total_tiles < 0 || max_segment_tiles < 0 || max_seq_len < 0 || warps < 1) return -1;
+    if (total_tiles == 0) return 0;
+    return balanced_parts(total_tiles, max_segment_tiles, (int)balanced_slots(max_seq_len), warps);
+}
+
+PKV_API int64_t pkv_balanced_share_owner(int64_t tile, int64_t total_tiles, int64_t parts) {
+    if (total_tiles < 1 || parts < 1 || tile < 0 || tile >= total_tiles) return -1;
+    return share_owner(tile, total_tiles, parts);
+}
+
+PKV_API int pkv_balanced_slots(int max_seq_len) {
+    return max_seq_len < 0 ? -1 : (int)balanced_slots(max_seq_len);
 }

@@ -48,5 +48,24 @@ __device__ __forceinline__ void quantize16(const uint4 (&x)[2], float scale, uin
     }
 }
 
+// Balanced split of the decode kernel: T tiles of all (sequence, kv head)
+// segments laid end to end, cut into `parts` equal contiguous shares, share c
+// = [floor(c T / parts), floor((c + 1) T / parts)).  A segment of n tiles
+// meets at most ceil(n / share) + 1 shares and has `slots` partial slots, so
+// shares hold at least ceil(seg_max / (slots - 1)) tiles; at most `warps`
+// shares.  The kernel and the host diagnostic hooks share this code.
+__host__ __device__ __forceinline__ int64_t balanced_parts(int64_t T, int seg_max, int slots, int64_t warps) {
+    const int64_t min_share = slots > 1 ? ((seg_max + slots - 2) / (slots - 1) > 1 ? (seg_max + slots - 2) / (slots - 1) : 1)
+                                        : (T > 1 ? T : 1);
+    int64_t parts = T / min_share;
+    if (parts < 1) parts = 1;
+    if (parts > warps) parts = warps;
+    return parts;
+}
+
+// Share that holds tile t.
+__host__ __device__ __forceinline__ int64_t share_owner(int64_t t, int64_t T, int64_t parts) {
+    return ((t + 1) * parts + T - 1) / T - 1;
+}
 
 }  // namespace pkv

@@ -1,6 +1,7 @@
 """Invariants of the balanced split that the attention kernel's in-kernel merge
-relies on, checked on the split arithmetic itself (restated here from the
-kernel: share sizing, share ownership) over many random workloads:
+relies on, checked on the library's own split arithmetic (the share sizing and
+share ownership the kernel runs, exported as host diagnostics) over many
+random workloads:
 
 * every context (sequence, kv head) is cut into at most `slots` pieces, the
   partial slots the workspace holds per (sequence, head);
@@ -18,26 +19,37 @@ import random
 
 import pytest
 
-MIN_TILES = 16   # shares hold >= 16 tiles of 16 tokens unless contexts are short
+from paged_kv_cache_279_gb300 import _lib
 
 
-def balanced_slots(max_seq_len):
-    return (max_seq_len + MIN_TILES * 16 - 1) // (MIN_TILES * 16) + 1
+def lib():
+    return _lib.load()
 
 
 def split(lens, hkv, tile, max_seq_len, warps):
-    """Tiles per context, total T, number of shares `parts` (as the kernel sizes them)."""
+    """Tiles per context, total T, number of shares `parts` (from the library)."""
     seg = [math.ceil(L / tile) for L in lens for _ in range(hkv)]
     T = sum(seg)
-    slots = balanced_slots(max_seq_len)
-    seg_max = max(seg) if seg else 0
-    min_share = max(1, (seg_max + slots - 2) // (slots - 1)) if slots > 1 else T
-    parts = min(max(T // max(1, min_share), 1), warps)
+    slots = lib().pkv_balanced_slots(max_seq_len)
+    parts = lib().pkv_balanced_split_parts(T, max(seg) if seg else 0, max_seq_len, warps)
     return seg, T, parts, slots
 
 
 def share_owner(t, T, parts):
-    return ((t + 1) * parts + T - 1) // T - 1
+    return lib().pkv_balanced_share_owner(t, T, parts)
+
+
+def test_slots_and_bad_arguments():
+    L = lib()
+    assert L.pkv_balanced_slots(0) == 1 and L.pkv_balanced_slots(256) == 2 and L.pkv_balanced_slots(257) == 3
+    assert L.pkv_balanced_slots(-1) == -1
+    assert L.pkv_balanced_split_parts(0, 0, 100, 8) == 0
+    assert L.pkv_balanced_split_parts(-1, 0, 100, 8) == -1
+    assert L.pkv_balanced_split_parts(10, 10, 100, 0) == -1
+    assert L.pkv_balanced_share_owner(5, 5, 1) == -1
+    # one share: every tile belongs to share 0; T shares: tile t to share t
+    assert all(L.pkv_balanced_share_owner(t, 7, 1) == 0 for t in range(7))
+    assert all(L.pkv_balanced_share_owner(t, 7, 7) == t for t in range(7))
 
 
 @pytest.mark.parametrize("seed", range(40))
@@ -52,7 +64,9 @@ def test_split_invariants(seed):
     warps = rnd.choice([152 * 3 * 4, 152 * 4, 16, 1])
     seg, T, parts, slots = split(lens, hkv, tile, max_len, warps)
     if T == 0:
+        assert parts == 0
         return
+    assert 1 <= parts <= warps
     bounds = [(g * T // parts, (g + 1) * T // parts) for g in range(parts)]
     assert all(hi > lo for lo, hi in bounds)                        # no empty share
     assert all(share_owner(t, T, parts) == g for g, (lo, hi) in enumerate(bounds) for t in (lo, hi - 1))

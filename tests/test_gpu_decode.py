@@ -225,18 +225,16 @@ def test_balanced_workspace_reused_across_calls():
     assert pkv.read_device_errors() == 0
 
 
-@pytest.mark.parametrize("P,dtype,B,split,nseq", [
-    (0, torch.bfloat16, 16, "", 7), (0, torch.bfloat16, 8, "", 7), (0, torch.bfloat16, 32, "", 7),
-    (64, torch.bfloat16, 16, "", 7), (0, torch.float32, 16, "", 7),
-    (0, torch.bfloat16, 16, "1", 7),    # balanced kernel after the separate store kernel
-    (0, torch.bfloat16, 16, "2", 150),  # fused store with many segments
-    (0, torch.bfloat16, 16, "", 150)])  # 150 x 8 segments: the separate store kernel by default
-def test_decode_append_equals_write_then_decode(P, dtype, B, split, nseq, monkeypatch):
+@pytest.mark.parametrize("P,dtype,B,nseq", [
+    (0, torch.bfloat16, 16, 7), (0, torch.bfloat16, 8, 7), (0, torch.bfloat16, 32, 7),
+    (64, torch.bfloat16, 16, 7),     # fixed partitions: the separate store kernel, then decode
+    (64, torch.bfloat16, 16, 150),
+    (0, torch.float32, 16, 7),       # fp32: the separate store kernel, then decode
+    (0, torch.bfloat16, 16, 150)])   # 150 x 8 segments stored inside the balanced kernel
+def test_decode_append_equals_write_then_decode(P, dtype, B, nseq):
     """paged_attention_decode_append = store the newest token of every
     sequence at position len - 1, then attend (fused into the balanced bf16
-    kernel for batches of few segments, a separate store kernel otherwise)."""
-    if split:
-        monkeypatch.setenv("PKV_APPEND_SPLIT", split)
+    kernel; a separate store kernel on the fixed-partition and fp32 paths)."""
     shape = shape_of(32, 8, 128, B, dtype)
     base = [1, 16, 17, 300, 0, 1500, 33]
     lens = (base * (nseq // len(base) + 1))[:nseq] if nseq != len(base) else base
@@ -289,10 +287,10 @@ def _replay_checks(call, refresh, check, reps=3):
 
 def test_balanced_merge_survives_graph_replays_and_random_workspace():
     """The balanced path merges split contexts inside the attention kernel:
-    per-context arrival counters in the workspace, tagged per call.  A graph
-    replays one call (same tag, same counters) several times, and the
-    workspace starts as random bytes, so every call must both ignore stale
-    counters and leave its own ready for a replay."""
+    one ready flag per partial slot, carrying the call's tag, cleared by the
+    merging warp.  A graph replays one call (same tag, same flags) several
+    times, and the workspace starts as random bytes, so every call must both
+    ignore stale flags and leave its own ready for a replay."""
     shape = shape_of(32, 8, 128, 16)
     lens = [3000, 1, 0, 2048, 517, 64] * 3
     case = make_decode_case(shape, lens, seed=55)
