@@ -21,6 +21,7 @@ oracle on the same workload instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -73,6 +74,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    p.add_argument("--per-workload", choices=["auto", "all", "none"], default="auto",
+                   help="also time every other workload (auto: in the default GQA run)")
     return p.parse_args(argv)
 
 
@@ -271,6 +274,7 @@ class Batch:
         self.seq_ids = seq_ids
         st, slots, pairs = self.alloc.append_slots(self.seq_ids)
         assert st == 0
+        self.cow_copies = getattr(self, "cow_copies", 0) + len(pairs)
         if len(pairs):
             pkv.block_copy([self.k_cache], [self.v_cache], torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
         self.max_blocks = max(-(-L // B) for L in self.lens) + 4
@@ -321,10 +325,12 @@ class Batch:
             pkv.kv_cache_write(k, torch.randn_like(k), self.k_cache, self.v_cache, slots)
             for c in range(1, W):
                 assert self.alloc.fork(p * W, p * W + c) == 0
+        self.cow_copies = 0
         for t in range(int(div.max())):
             beams = [b for b in range(P_ * W) if div[b] > t]
             st, slots, pairs = self.alloc.append_slots(beams)
             assert st == 0
+            self.cow_copies += len(pairs)
             if len(pairs):
                 pkv.block_copy([self.k_cache], [self.v_cache],
                                torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
@@ -572,6 +578,139 @@ def config_of(shape, args, S):
             "l2": f"inputs larger than L2: {ROTATE.get(args.workload, 1)} resident batches rotated"}
 
 
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def timed_replays(graph, stream, min_ms):
+    """Replays of `graph` back to back until at least `min_ms` of device time:
+    (total device ms, replays).  One replay first sizes the count."""
+    one = time_graph(graph, stream, 1)
+    reps = max(1, math.ceil(min_ms / max(one, 1e-3)))
+    return time_graph(graph, stream, reps), reps
+
+
+def measure_decode(pkv, shape, args, device, stream, seed, world, steps, warmup, sustained_ms):
+    """Device timing of one decode workload: exactly `steps` steps in one CUDA
+    graph (the contract's timed region), the same graph replayed for at least
+    `sustained_ms`, and the decode call alone (the roofline's kernel) replayed
+    as long.  Batches rotate so that no step re-reads the previous step's pool."""
+    nrot = ROTATE.get(args.workload, 1)
+    batches = [make_batch(pkv, shape, args, seed + r, device) for r in range(nrot)]
+    elt = 1 if args.kv == "fp8" else None
+    torch.cuda.synchronize()
+    warm_graph = capture([batches[i % nrot].step for i in range(warmup)], stream)
+    step_graph = capture([batches[i % nrot].step for i in range(steps)], stream)
+    decode_graph = capture([batches[i % nrot].decode for i in range(steps)], stream)
+    if pkv.read_device_errors() != 0:
+        raise RuntimeError(f"{args.workload}: device error bits set while capturing")
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        time_graph(warm_graph, stream)                    # W untimed warm-up steps
+        step_ms = time_graph(step_graph, stream)          # exactly `steps` steps
+        sus_ms, sus_reps = timed_replays(step_graph, stream, sustained_ms)
+        dec_ms, dec_reps = timed_replays(decode_graph, stream, sustained_ms / 2)
+    torch.cuda.synchronize()
+    barrier(world)
+    if pkv.read_device_errors() != 0:
+        raise RuntimeError(f"{args.workload}: device error bits set while timing")
+    uniq = [b.unique_bytes for b in batches]
+    logical = [kv_bytes(b.lens, shape, elt) for b in batches]
+    alg = [b.alg_bytes for b in batches]
+    step_bytes = sum(uniq[i % nrot] for i in range(steps))
+    total_s = max_over_ranks(step_ms / 1e3, world, device)
+    sus_s = max_over_ranks(sus_ms / 1e3, world, device)
+    total_bytes = sum_over_ranks(step_bytes, world, device)
+    peaks = load_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    dec_call_ms = dec_ms / (steps * dec_reps)
+    dec_alg = sum(alg[i % nrot] for i in range(steps)) / steps
+    achieved = dec_alg / (dec_call_ms / 1e3) / 1e9
+    seqs = sum(len(b.lens) for b in batches) / nrot
+    res = {
+        "value": total_bytes / total_s / 1e9,
+        "ms_per_step": 1e3 * total_s / steps,
+        "sustained": {"value": round(total_bytes * sus_reps / sus_s / 1e9, 2), "unit": "GB/s",
+                      "steps_timed": steps * sus_reps, "timed_ms": round(sus_ms, 2),
+                      "ms_per_step": round(sus_ms / (steps * sus_reps), 5)},
+        "decode_tokens_per_s": world * seqs / (shape.num_layers * total_s / steps),
+        "logical_kv_gbs": sum(logical[i % nrot] for i in range(steps)) / total_s / 1e9 * world,
+        "peak": peak, "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "algorithmic_bytes": round(dec_alg),
+                     "decode_us": round(dec_call_ms * 1e3, 2), "calls_timed": steps * dec_reps,
+                     "timed_ms": round(dec_ms, 2),
+                     "peak_source": "measured (hbm_gbs)" if "hbm_gbs" in peaks else "fallback 6800 GB/s"},
+        "clocks": clocks.summary(),
+        "batches": batches,
+    }
+    return res
+
+
+def workload_args(args, workload, kv="bf16", block_size=0):
+    a = argparse.Namespace(**vars(args))
+    a.workload, a.kv, a.block_size, a.partition_size = workload, kv, block_size, 0
+    return a
+
+
+# Workloads reported beside the headline in the default run (name -> (workload,
+# kv, block size)); each is timed for at least SUSTAINED_MS of device time.
+EXTRA_WORKLOADS = {
+    "long": ("long", "bf16", 0),
+    "beam": ("beam", "bf16", 0),
+    "beam1032": ("beam1032", "bf16", 0),
+    "mixed_b16": ("mixed", "bf16", 16),
+    "mixed_b8": ("mixed", "bf16", 8),
+    "mixed_b32": ("mixed", "bf16", 32),
+    "gqa_fp8": ("gqa", "fp8", 0),
+    "long_fp8": ("long", "fp8", 0),
+    "mixed_fp8": ("mixed", "fp8", 0),
+    "tiny": ("tiny", "bf16", 0),
+    "verify": ("verify", "bf16", 0),
+    "prefill": ("prefill", "bf16", 0),
+}
+SUSTAINED_MS = 200.0
+
+
+def waste_of(batch):
+    used, alloc = batch.alloc.waste()
+    return 1.0 - used / alloc if alloc else 0.0
+
+
+def extra_workload(pkv, name, args, device, stream, seed, world):
+    """Compact line of one extra workload (device timing only)."""
+    wk, kv, bs = EXTRA_WORKLOADS[name]
+    a = workload_args(args, wk, kv, bs)
+    steps, warmup = args.steps, max(3, args.warmup)
+    if wk in MULTI_TOKEN:
+        r = measure_multi_token(pkv, a, device, stream, seed, world, steps, warmup, SUSTAINED_MS)
+        return {k: r[k] for k in ("value", "unit", "ms_per_step", "query_tokens_per_s", "roofline", "clocks",
+                                  "config", "sustained")}
+    shape = shape_for(a)
+    r = measure_decode(pkv, shape, a, device, stream, seed, world, steps, warmup, SUSTAINED_MS)
+    b0 = r["batches"][0]
+    line = {"value": round(r["sustained"]["value"], 2), "unit": "GB/s",
+            "pct_of_hbm_peak": round(100 * r["sustained"]["value"] / r["peak"], 2),
+            "ms_per_step": r["sustained"]["ms_per_step"], "steps_timed": r["sustained"]["steps_timed"],
+            "timed_ms": r["sustained"]["timed_ms"], "k_steps_value": round(r["value"], 2),
+            "decode_tokens_per_s": round(r["decode_tokens_per_s"], 1),
+            "roofline": r["roofline"], "clocks": r["clocks"],
+            "config": config_of(shape, a, len(b0.lens))["workload"],
+            "dtype": "e4m3" if kv == "fp8" else ("f32" if shape.dtype == torch.float32 else "bf16")}
+    if wk.startswith("beam"):
+        line["logical_kv_gbs"] = round(r["logical_kv_gbs"] * r["sustained"]["value"] / max(r["value"], 1e-9), 2)
+        line["cow_copies_per_batch"] = getattr(b0, "cow_copies", 0)
+    if wk == "mixed":
+        line["allocator_waste"] = round(waste_of(b0), 5)
+    del r
+    return line
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     import paged_kv_cache_279_gb300 as pkv
@@ -581,72 +720,37 @@ def run_ours(args):
     device = torch.device("cuda", local)
     init_dist(world, "nccl")
     shape = shape_for(args)
-    nrot = ROTATE.get(args.workload, 1)
     seed = args.seed + 1000 * rank
-    batches = []
-    for r in range(nrot):
-        batches.append(make_batch(pkv, shape, args, seed + r, device))
-    elt = 1 if args.kv == "fp8" else None
-    torch.cuda.synchronize()
     stream = torch.cuda.Stream(device)
     steps, warmup = args.steps, max(3, args.warmup)
-    # exactly `steps` steps (and `steps` decode calls) in one graph each; the
-    # batches rotate so that no step re-reads the previous step's pool
-    warm_graph = capture([batches[i % nrot].step for i in range(warmup)], stream)
-    step_graph = capture([batches[i % nrot].step for i in range(steps)], stream)
-    decode_graph = capture([batches[i % nrot].decode for i in range(steps)], stream)
-    assert pkv.read_device_errors() == 0
-
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        time_graph(warm_graph, stream)      # W untimed warm-up steps
-        step_total_ms = time_graph(step_graph, stream)
-        time_graph(warm_graph, stream)
-        decode_total_ms = time_graph(decode_graph, stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    bytes_per = [b.unique_bytes for b in batches]
-    logical_per = [kv_bytes(b.lens, shape, elt) for b in batches]
-    step_bytes = sum(bytes_per[i % nrot] for i in range(steps))
-    local_s = step_total_ms / 1e3
-    total_s = max_over_ranks(local_s, world, device)
-    total_bytes = sum_over_ranks(step_bytes, world, device)
-    value = total_bytes / total_s / 1e9
-    ms_per_step = 1e3 * total_s / steps
-    seqs_per_step = sum(len(b.lens) for b in batches) / nrot
-    layers = shape.num_layers
-    tokens_per_s = world * seqs_per_step / (layers * ms_per_step / 1e3)
-
-    # roofline of the dominant kernel (the decode call), timed live above
-    alg = [b.alg_bytes for b in batches]
-    dec_alg_bytes = sum(alg[i % nrot] for i in range(steps)) / steps
-    dec_ms = decode_total_ms / steps
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    peak = float(peaks.get("hbm_gbs", 6800.0))
-    achieved = dec_alg_bytes / (dec_ms / 1e3) / 1e9
+    r = measure_decode(pkv, shape, args, device, stream, seed, world, steps, warmup, SUSTAINED_MS)
+    batches = r.pop("batches")
+    nrot = len(batches)
+    roofline = r["roofline"]
     traffic, traffic_src = None, None
     cap = NCU_TRAFFIC.get((args.workload, args.kv))
     if cap is not None and not args.block_size and not args.partition_size:
-        traffic = round(cap[0] / cap[1] * dec_alg_bytes)
+        traffic = round(cap[0] / cap[1] * roofline["algorithmic_bytes"])
         traffic_src = f"{cap[2]}: {cap[0] / 1e6:.2f} MB for {cap[1] / 1e6:.2f} MB algorithmic, scaled to this launch"
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_unit": "bytes per launch",
-                "traffic_source": traffic_src, "algorithmic_bytes": round(dec_alg_bytes),
-                "kernel": ("paged_attention_decode_fp8" if args.kv == "fp8" else "paged_attention_decode")
-                          + (" (prefix, attention and merge kernels)" if args.workload.startswith("beam")
-                             else " (one kernel: attention and in-kernel merge)"),
-                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback",
-                "decode_us": round(dec_ms * 1e3, 2)}
+    roofline.update({"traffic": traffic, "traffic_unit": "bytes per launch", "traffic_source": traffic_src,
+                     "kernel": KERNEL_NAMES.get((args.workload.startswith("beam"), args.kv),
+                                                "paged_attention_decode")})
+    launches = batches[0].launches_per_step() * steps
+    del batches
 
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(pkv, shape, args, device, stream, seed, world)
+    per_workload = None
+    if args.per_workload == "all" or (args.per_workload == "auto" and args.workload == "gqa" and
+                                      args.kv == "bf16" and not args.block_size and not args.partition_size):
+        per_workload = {}
+        for name in EXTRA_WORKLOADS:
+            try:
+                per_workload[name] = extra_workload(pkv, name, args, device, stream, seed, world)
+            except Exception as exc:  # reported, never hidden
+                per_workload[name] = {"error": f"{type(exc).__name__}: {exc}"}
+            torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, desc, secs, _ = oracle_sample(shape, seed, args.cpu_budget,
@@ -654,24 +758,35 @@ def run_ours(args):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": desc}
     if rank == 0:
+        cfg = config_of(shape, args, shape.num_seqs if not args.workload.startswith("beam")
+                        else wl.BEAM_PROMPTS * wl.BEAM_WIDTH)
+        cfg["l2"] = f"inputs larger than L2: {nrot} resident batches rotated"
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
+            "metric": METRIC, "value": round(r["value"], 2), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(r["ms_per_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("e4m3" if args.kv == "fp8" else "bf16") if shape.dtype == torch.bfloat16 else "f32",
-            "data": "synthetic",
-            "config": config_of(shape, args, len(batches[0].lens)),
-            "decode_tokens_per_s": round(tokens_per_s, 1),
-            "logical_kv_gbs": round(sum(logical_per[i % nrot] for i in range(steps)) / total_s / 1e9 * world, 2),
-            "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "data": "synthetic", "config": cfg,
+            "decode_tokens_per_s": round(r["decode_tokens_per_s"], 1),
+            "logical_kv_gbs": round(r["logical_kv_gbs"], 2),
+            "pct_of_hbm_peak": round(100 * r["value"] / r["peak"], 2),
+            "sustained": r["sustained"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": batches[0].launches_per_step() * steps,
-            "clocks": clocks.summary(),
+            "gpu_launches": launches,
+            "clocks": r["clocks"],
+            "per_workload": per_workload,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+KERNEL_NAMES = {
+    (False, "bf16"): "paged_attention_decode (one kernel: stores, attention and in-kernel merge)",
+    (False, "fp8"): "paged_attention_decode_fp8 (one kernel: stores, attention and in-kernel merge)",
+    (True, "bf16"): "paged_attention_decode_grouped",
+}
 
 
 def make_batch(pkv, shape, args, seed, device, reserve_tokens=0):
@@ -696,70 +811,118 @@ def context_lengths(args, shape, seed):
 
 
 def run_e2e(pkv, shape, args, device, stream, seed, world):
-    """The step through the public API with host buffers: the allocator appends
-    a token for every sequence on the host, the step's inputs go H2D from
-    pinned memory, the kernels run, the output comes back D2H."""
+    """The step through the C ABI with host buffers, as a serving loop runs it:
+    the host allocator appends a token for every sequence, the host copy of
+    the block tables changes only where a sequence took a new block, one H2D
+    copy from a pinned buffer carries the step's queries, new K/V, lengths and
+    tables (and the groups of a beam batch), the library call stores the new
+    tokens and attends, and one D2H copy brings the output back; the host
+    waits for it before the next step."""
+    from paged_kv_cache_279_gb300 import _lib
+    lib = _lib.load()
     steps = args.steps
     b = make_batch(pkv, shape, args, seed + 77, device, reserve_tokens=steps + args.warmup + 1)
-    S = len(b.lens)
-    h_q = b.q.cpu().pin_memory()
-    h_k = b.k_new.cpu().pin_memory()
-    h_v = b.v_new.cpu().pin_memory()
-    h_out = torch.empty_like(h_q).pin_memory()
-    cap = b.max_blocks + (steps + args.warmup) // shape.block_size + 2
-    h_tab = torch.empty((S, cap), dtype=torch.int32).pin_memory()
-    h_len = torch.empty(S, dtype=torch.int32).pin_memory()
-    d_tab = torch.empty((S, cap), dtype=torch.int32, device=device)
-    d_len = torch.empty(S, dtype=torch.int32, device=device)
-    d_q, d_k, d_v = torch.empty_like(b.q), torch.empty_like(b.k_new), torch.empty_like(b.v_new)
-    max_seq_len = cap * shape.block_size
-    ws_bytes = (pkv.paged_attention_grouped_workspace_size(S, shape.num_heads, shape.head_dim, max_seq_len)
-                if b.group_offsets is not None else
-                pkv.paged_attention_workspace_size(S, shape.num_heads, shape.head_dim, max_seq_len,
-                                                   args.partition_size))
-    ws = torch.zeros(max(256, ws_bytes), dtype=torch.uint8, device=device)
+    S, Hq, Hkv, D, B = len(b.lens), shape.num_heads, shape.num_kv_heads, shape.head_dim, shape.block_size
+    cap = b.max_blocks + (steps + args.warmup) // B + 2
+    max_seq_len = cap * B
+    grouped = b.group_offsets is not None
     fp8 = args.kv == "fp8"
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_tab, h_len))
-    elt = 1 if fp8 else None
+    elt = torch.tensor([], dtype=shape.dtype).element_size()
+    # one pinned buffer, one device buffer: q | k_new | v_new | lens | tables | groups
+    parts = [("q", S * Hq * D * elt), ("k", S * Hkv * D * elt), ("v", S * Hkv * D * elt), ("lens", 4 * S),
+             ("tab", 4 * S * cap)]
+    if grouped:
+        offs, pre = b.alloc.prefix_groups(b.seq_ids)
+        parts += [("offs", 4 * len(offs)), ("pre", 4 * len(pre))]
+    off, pos = {}, 0
+    for name, n in parts:
+        off[name] = pos
+        pos += (n + 255) // 256 * 256
+    h_pack = torch.zeros(pos, dtype=torch.uint8).pin_memory()
+    d_pack = torch.zeros(pos, dtype=torch.uint8, device=device)
+
+    def hview(name, dtype, shp):
+        n = int(np.prod(shp)) * torch.tensor([], dtype=dtype).element_size()
+        return h_pack[off[name]:off[name] + n].view(dtype).view(*shp)
+    hview("q", shape.dtype, (S, Hq, D)).copy_(b.q.cpu())
+    hview("k", shape.dtype, (S, Hkv, D)).copy_(b.k_new.cpu())
+    hview("v", shape.dtype, (S, Hkv, D)).copy_(b.v_new.cpu())
+    h_lens = hview("lens", torch.int32, (S,)).numpy()
+    h_tab = hview("tab", torch.int32, (S, cap)).numpy()
+    tab, ln = b.alloc.block_tables(b.seq_ids, cap)
+    h_tab[:] = tab
+    h_lens[:] = ln
+    if grouped:
+        hview("offs", torch.int32, (len(offs),)).numpy()[:] = offs
+        hview("pre", torch.int32, (len(pre),)).numpy()[:] = pre
+    dptr = d_pack.data_ptr()
+    out = torch.empty((S, Hq, D), dtype=shape.dtype, device=device)
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    ws_bytes = (pkv.paged_attention_grouped_workspace_size(S, Hq, D, max_seq_len) if grouped else
+                pkv.paged_attention_workspace_size(S, Hq, D, max_seq_len, 0))
+    ws = torch.zeros(max(256, ws_bytes), dtype=torch.uint8, device=device)
+    st_ptr = ctypes.c_void_p(stream.cuda_stream)
+    kc, vc = b.k_cache.data_ptr(), b.v_cache.data_ptr()
+    NB = b.num_blocks
+    seq_ids = np.ascontiguousarray(b.seq_ids, dtype=np.int64)
+    rows = np.arange(S)
+
+    def call():
+        if fp8:
+            return lib.paged_attention_decode_append_fp8(
+                out.data_ptr(), dptr + off["q"], dptr + off["k"], dptr + off["v"], kc, vc, dptr + off["tab"],
+                dptr + off["lens"], S, Hq, Hkv, D, B, cap, NB, max_seq_len, shape.scale, FP8_K_SCALE,
+                FP8_V_SCALE, ws.data_ptr(), ws.numel(), st_ptr)
+        if grouped:
+            return lib.paged_attention_decode_grouped(
+                out.data_ptr(), dptr + off["q"], dptr + off["k"], dptr + off["v"], kc, vc, dptr + off["tab"],
+                dptr + off["lens"], dptr + off["offs"], dptr + off["pre"], len(pre), S, Hq, Hkv, D, B, cap, NB,
+                max_seq_len, shape.scale, ws.data_ptr(), ws.numel(), pkv.PKV_BF16, st_ptr)
+        return lib.paged_attention_decode_append(
+            out.data_ptr(), dptr + off["q"], dptr + off["k"], dptr + off["v"], kc, vc, dptr + off["tab"],
+            dptr + off["lens"], S, Hq, Hkv, D, B, cap, NB, max_seq_len, shape.scale, 0, ws.data_ptr(),
+            ws.numel(), pkv.PKV_BF16 if shape.dtype == torch.bfloat16 else pkv.PKV_F32, st_ptr)
+
+    h2d = pos
     d2h = h_out.numel() * h_out.element_size()
     ms, byts = [], []
+    base_unique, base_lens = b.unique_bytes, list(b.lens)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for i in range(args.warmup + steps):
-            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ev0.record(stream)
-            st, slots, pairs = b.alloc.append_slots(b.seq_ids)
+            st, slots, pairs = b.alloc.append_slots(seq_ids)
             if st != 0 or len(pairs):
                 raise RuntimeError("allocator could not serve the step")
-            tab, ln = b.alloc.block_tables(b.seq_ids, cap)
-            h_tab.numpy()[:] = tab
-            h_len.numpy()[:] = ln
-            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_tab, h_tab), (d_len, h_len)):
-                d.copy_(h, non_blocking=True)
-            if fp8:
-                pkv.paged_attention_decode_append_fp8(b.out, d_q, d_k, d_v, b.k_cache, b.v_cache, d_tab, d_len,
-                                                      shape.scale, FP8_K_SCALE, FP8_V_SCALE, max_seq_len, ws)
-            elif b.group_offsets is not None:
-                offs, pre = b.alloc.prefix_groups(b.seq_ids)  # beams sharing a prompt
-                d_offs = torch.from_numpy(offs).pin_memory().to(device, non_blocking=True)
-                d_pre = torch.from_numpy(pre).pin_memory().to(device, non_blocking=True)
-                pkv.paged_attention_decode_grouped(b.out, d_q, b.k_cache, b.v_cache, d_tab, d_len, d_offs,
-                                                   d_pre, shape.scale, max_seq_len, k_new=d_k, v_new=d_v,
-                                                   workspace=ws)
-            else:
-                pkv.paged_attention_decode_append(b.out, d_q, d_k, d_v, b.k_cache, b.v_cache, d_tab, d_len,
-                                                  shape.scale, max_seq_len, args.partition_size, ws)
-            h_out.copy_(b.out, non_blocking=True)
+            pos_new = h_lens.astype(np.int64)  # position of each new token
+            h_lens += 1
+            took = (pos_new % B) == 0          # a new block: its id goes into the table
+            if took.any():
+                h_tab[rows[took], pos_new[took] // B] = (slots[took] // B).astype(np.int32)
+            d_pack.copy_(h_pack, non_blocking=True)
+            rc = call()
+            if rc != 0:
+                raise RuntimeError(f"library call failed with status {rc}")
+            h_out.copy_(out, non_blocking=True)
             ev1.record(stream)
             ev1.synchronize()  # the host reads the step's result
             if i >= args.warmup:
                 ms.append(ev0.elapsed_time(ev1))
                 # unique bytes: what the batch started with plus the tokens added since
-                byts.append(b.unique_bytes + kv_bytes(ln.tolist(), shape, elt) - kv_bytes(b.lens, shape, elt))
+                byts.append(base_unique + kv_bytes(h_lens.tolist(), shape, 1 if fp8 else None) -
+                            kv_bytes(base_lens, shape, 1 if fp8 else None))
+    if pkv.read_device_errors() != 0:
+        raise RuntimeError("e2e: device error bits set")
+    # the device tables must equal the allocator's after the loop
+    tab, ln = b.alloc.block_tables(b.seq_ids, cap)
+    if not (np.array_equal(tab[:, :], h_tab) and np.array_equal(ln, h_lens)):
+        raise RuntimeError("e2e: incremental block tables diverged from the allocator")
     local_s = sum(ms) / 1e3
     total_s = max_over_ranks(local_s, world, device)
     total_b = sum_over_ranks(sum(byts), world, device)
     return {"value": round(total_b / total_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * total_s / steps, 4)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * total_s / steps, 4),
+            "copies_per_step": {"h2d": 1, "d2h": 1}}
 
 
 def multi_token_batch(pkv, args, seed, device):
@@ -804,9 +967,70 @@ def multi_token_batch(pkv, args, seed, device):
     return b
 
 
+def measure_multi_token(pkv, args, device, stream, seed, world, steps, warmup, sustained_ms):
+    """Multi-token attention calls (chunked prefill / verification), timed like
+    the decode step: exactly `steps` calls in one CUDA graph over rotated
+    resident batches, then the same graph replayed for `sustained_ms`."""
+    shape = wl.GQA_BF16
+    nrot = 4
+    batches = [multi_token_batch(pkv, args, seed + r, device) for r in range(nrot)]
+
+    def call(b):
+        return lambda: pkv.paged_attention_multi_token(b["out"], b["q"], b["kc"], b["vc"], b["tables"], b["seq_lens"],
+                                                       b["starts"], shape.scale, b["Q"], b["max_seq_len"], b["ws"])
+    warm = capture([call(batches[i % nrot]) for i in range(warmup)], stream)
+    timed = capture([call(batches[i % nrot]) for i in range(steps)], stream)
+    if pkv.read_device_errors() != 0:
+        raise RuntimeError(f"{args.workload}: device error bits set while capturing")
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        time_graph(warm, stream)
+        total_ms = time_graph(timed, stream)
+        sus_ms, sus_reps = timed_replays(timed, stream, sustained_ms)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_s = max_over_ranks(total_ms / 1e3, world, device)
+    sus_s = max_over_ranks(sus_ms / 1e3, world, device)
+    kvb = sum_over_ranks(sum(batches[i % nrot]["kv_bytes"] for i in range(steps)), world, device)
+    flops = sum(batches[i % nrot]["flops"] for i in range(steps)) * world
+    alg = sum(batches[i % nrot]["alg_bytes"] for i in range(steps)) / steps
+    ms = 1e3 * sus_s / (steps * sus_reps)
+    peaks = load_peaks()
+    Q, L_fixed, S = MULTI_TOKEN[args.workload]
+    if args.workload == "prefill":
+        achieved = flops * sus_reps / sus_s / 1e12
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": "paged_attention_multi_token",
+                    "peak_source": "measured bf16 GEMM burst" if "bf16_tflops" in peaks else "fallback",
+                    "useful_flops_per_call": round(flops / steps / world), "call_us": round(ms * 1e3, 2)}
+    else:
+        achieved = alg / (ms / 1e3) / 1e9
+        peak = float(peaks.get("hbm_gbs", 6800.0))
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "kernel": "paged_attention_multi_token", "algorithmic_bytes": round(alg),
+                    "peak_source": "measured" if "hbm_gbs" in peaks else "fallback", "call_us": round(ms * 1e3, 2)}
+    launches = steps * MT_LAUNCHES_PER_CALL
+    return {"value": round(kvb / total_s / 1e9, 2), "unit": "GB/s", "ms_per_step": round(1e3 * total_s / steps, 5),
+            "sustained": {"value": round(kvb * sus_reps / sus_s / 1e9, 2), "unit": "GB/s",
+                          "steps_timed": steps * sus_reps, "timed_ms": round(sus_ms, 2), "ms_per_step": round(ms, 5)},
+            "query_tokens_per_s": round(world * S * Q / (ms / 1e3), 1), "roofline": roofline,
+            "clocks": clocks.summary(), "gpu_launches": launches,
+            "config": (f"{args.workload}: {S} seqs x {Q} query tokens, "
+                       f"{'context ' + str(L_fixed) if L_fixed else 'GQA context lengths U[64, 2048]'}, "
+                       f"32q/8kv heads, head_dim 128, block 16"),
+            "l2": f"inputs larger than L2: {nrot} resident batches rotated"}
+
+
+# kernels one multi-token call launches (the attention kernel merges split
+# contexts itself)
+MT_LAUNCHES_PER_CALL = 1
+
+
 def run_multi_token_bench(args):
-    """Multi-token attention calls (§ chunked prefill / verification), timed like
-    the decode step: K calls in one CUDA graph over rotated resident batches."""
     rank, world, local = dist_env()
     import paged_kv_cache_279_gb300 as pkv
     if not torch.cuda.is_available():
@@ -814,65 +1038,19 @@ def run_multi_token_bench(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     init_dist(world, "nccl")
-    shape = wl.GQA_BF16
-    nrot = 4
-    batches = [multi_token_batch(pkv, args, args.seed + 1000 * rank + r, device) for r in range(nrot)]
-
-    def call(b):
-        return lambda: pkv.paged_attention_multi_token(b["out"], b["q"], b["kc"], b["vc"], b["tables"], b["seq_lens"],
-                                                       b["starts"], shape.scale, b["Q"], b["max_seq_len"], b["ws"])
     stream = torch.cuda.Stream(device)
     steps, warmup = args.steps, max(3, args.warmup)
-    warm = capture([call(batches[i % nrot]) for i in range(warmup)], stream)
-    timed = capture([call(batches[i % nrot]) for i in range(steps)], stream)
-    assert pkv.read_device_errors() == 0
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        time_graph(warm, stream)
-        total_ms = time_graph(timed, stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    total_s = max_over_ranks(total_ms / 1e3, world, device)
-    kvb = sum_over_ranks(sum(batches[i % nrot]["kv_bytes"] for i in range(steps)), world, device)
-    flops = sum(batches[i % nrot]["flops"] for i in range(steps)) * world
-    alg = sum(batches[i % nrot]["alg_bytes"] for i in range(steps)) / steps
-    ms = 1e3 * total_s / steps
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    if args.workload == "prefill":
-        achieved = flops / total_s / 1e12
-        peak = float(peaks.get("bf16_tflops", 1900.0))
-        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": None,
-                    "kernel": "paged_attention_multi_token (mma.sync bf16, N = 8 query heads of a KV head)",
-                    "peak_source": "measured bf16 GEMM burst" if "bf16_tflops" in peaks else "fallback",
-                    "useful_flops_per_call": round(flops / steps / world)}
-    else:
-        achieved = alg / (ms / 1e3) / 1e9
-        peak = float(peaks.get("hbm_gbs", 6800.0))
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": None,
-                    "kernel": "paged_attention_multi_token", "algorithmic_bytes": round(alg),
-                    "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
-    Q, L_fixed, S = MULTI_TOKEN[args.workload]
+    r = measure_multi_token(pkv, args, device, stream, args.seed + 1000 * rank, world, steps, warmup,
+                            SUSTAINED_MS)
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(kvb / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {S} seqs x {Q} query tokens, "
-                                   f"{'context ' + str(L_fixed) if L_fixed else 'GQA context lengths U[64, 2048]'}, "
-                                   f"32q/8kv heads, head_dim 128, block 16",
-                       "l2": f"inputs larger than L2: {nrot} resident batches rotated"},
-            "query_tokens_per_s": round(world * S * Q / (ms / 1e3), 1),
-            "roofline": roofline, "cpu_baseline": None, "e2e": None,
-            "gpu_launches": steps * (1 + (1 if batches[0]["max_seq_len"] > 1024 else 0)),
-            "clocks": clocks.summary(),
+            "config": {"workload": r["config"], "l2": r["l2"]},
+            "query_tokens_per_s": r["query_tokens_per_s"], "sustained": r["sustained"],
+            "roofline": r["roofline"], "cpu_baseline": None, "e2e": None,
+            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
         }
         print(json.dumps(line), flush=True)
     if world > 1:
