@@ -404,11 +404,12 @@ class Batch:
         """Kernels one step launches.  Balanced split (bf16, FP8): one -- the
         attention kernel stores the new tokens and merges split contexts itself.
         Fixed partitions: store kernel, attention kernel and the merge kernel
-        when contexts are split.  Grouped beam search: prefix kernel, attention
-        kernel, merge kernel."""
+        when contexts are split.  Grouped beam search: the store of the new
+        tokens, then one tensor-core kernel (shared prefix, each beam's own
+        tokens and the merge of split contexts)."""
         S = len(self.lens)
         if self.group_offsets is not None:
-            return 3
+            return 2  # the new tokens' store, then the tensor-core kernel (prefix, own tokens, merge)
         if self.kv == "fp8" or (self.partition_size == 0 and self.shape.dtype == torch.bfloat16):
             return 1
         ws = self.pkv.paged_attention_workspace_size(S, self.shape.num_heads, self.shape.head_dim,

@@ -56,12 +56,12 @@
 #include <mutex>
 
 #include "pkv_internal.cuh"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
 
 constexpr int kTile = 16;  // tokens per MMA tile and per pipeline stage
 constexpr int kGMax = 8;   // max query heads per KV head (the MMA N dimension)
-constexpr uint32_t kWaitLimit = 1u << 22;  // bounded mbarrier polling
 
 struct DecodeArgs {
     void *out;
@@ -103,73 +103,6 @@ struct DecodeArgs {
     void *v_cache_w;
 };
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Programmatic dependent launch: wait for the grids this one depends on
-// (no-op when launched without the attribute), and let dependents launch.
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Polls a bounded number of times; false means the wait gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
                                             uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -201,13 +134,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
     return d;
 }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-__device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __device__ __forceinline__ float to_float(float x) { return x; }
 __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -1019,16 +945,6 @@ __device__ __forceinline__ void store_piece(const DecodeArgs &a, WarpAcc<D> &acc
     }
 }
 
-// Ordering of the in-kernel merge: a writer's lanes store their partial,
-// fence, and lane 0 then sets the slot's flag; the merger sees every flag,
-// fences, and reads the partials through L2.
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Merge of a segment's n partials by the warp holding its first tile: for
 // every query head of the group, with M = max_j m_j,
 //     out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j
@@ -1039,18 +955,6 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
 // share is done, when its ring is idle: each lane stages the rows it needs in
 // its own kLaneBytes of the ring with cp.async (L2, no registers held), so a
 // chunk costs one round trip.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ float4 lds128(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
-}
-
 template <int D, int NV, int kLaneBytes>
 __device__ __forceinline__ void merge_rows(const float4 *po, const float *pm, const float *pl, int n,
                                            uint2 *dst, uint32_t stage) {
@@ -1629,920 +1533,6 @@ append_tokens_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
 }
 
 // ---------------------------------------------------------------------------
-// Shared-prefix kernel (grouped decode).  Sequences [off[g], off[g+1]) share
-// the physical blocks of their first prefix_lens[g] tokens (beam search,
-// parallel sampling).  One CTA per (group, kv head, prefix partition): warp 0
-// streams the partition's tiles once, through a ring shared by the whole CTA,
-// and each of the other warps attends one member's queries to every tile.  The
-// per-member partials join the member's own tokens in the merge kernel.
-// ---------------------------------------------------------------------------
-constexpr int kPrefixPart = 256;  // prefix tokens per CTA (at most 32 tiles: one lane each)
-constexpr int kPrefixMembers = 8; // members attended per pass over the prefix
-
-template <int D, int NS>
-constexpr int prefix_smem_bytes() {
-    return NS * Bf16Layout<D>::kStageBytes + 2 * NS * 8 + (kPrefixPart / 8 + 2) * 4 + 1024;
-}
-
-template <int D, int NS>
-__global__ void __launch_bounds__((kPrefixMembers + 1) * 32, 2)
-decode_bf16_prefix_kernel(const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
-                          const int32_t *__restrict__ group_offsets,
-                          const int32_t *__restrict__ prefix_lens, int num_groups) {
-    using Lay = Bf16Layout<D>;
-    constexpr int NWP = kPrefixMembers;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * Lay::kStageBytes);
-    uint64_t *empty = full + NS;
-    int *bt_s = reinterpret_cast<int *>(empty + NS);
-    __shared__ int min_len;
-
-    grid_dependency_wait();
-    grid_launch_dependents();
-
-    const int g = blockIdx.x, kvh = blockIdx.y, part = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = a.num_seqs, B = a.block_size;
-    const int cap = min(a.max_seq_len, a.max_blocks * B);
-    int m0 = group_offsets[g], m1 = group_offsets[g + 1];
-    if (m0 < 0 || m1 > S || m1 < m0) {
-        if (threadIdx.x == 0 && kvh == 0 && part == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
-        m0 = m1 = 0;
-    }
-    if (g == 0 && kvh == 0 && part == 0 && threadIdx.x == 0 &&
-        (group_offsets[0] != 0 || group_offsets[num_groups] != S))
-        flag_error(a.err, PKV_DEVERR_PREFIX);
-
-    // the shared part actually attended here: the group's prefix, cut to whole
-    // tiles and blocks and to the shortest member
-    const int align = B > kTile ? B : kTile;
-    const int pre_raw = prefix_lens[g];
-    if (threadIdx.x == 0) min_len = cap;
-    __syncthreads();
-    for (int i = threadIdx.x; i < m1 - m0; i += blockDim.x) atomicMin(&min_len, clamp_len(a.seq_lens[m0 + i], cap));
-    __syncthreads();
-    int pre = pre_raw < 0 ? 0 : pre_raw;
-    if (pre % align != 0 && threadIdx.x == 0 && kvh == 0 && part == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
-    // with an append, every member's new token must stay in its own part
-    pre = min(pre, min_len - (a.k_new ? 1 : 0)) / align * align;
-    if (pre < 0) pre = 0;
-    if (m1 - m0 < 1) pre = 0;
-    if (kvh == 0 && part == 0)
-        for (int i = threadIdx.x; i < m1 - m0; i += blockDim.x) a.seq_tok0[m0 + i] = pre;
-
-    const int t_begin = part * kPrefixPart;
-    const int t_end = min(pre, t_begin + kPrefixPart);
-    if (t_begin >= t_end) return;
-    const int ntiles = (t_end - t_begin) / kTile;  // pre is a whole number of tiles
-    const int boxh = B < kTile ? B : kTile;
-
-    // leader's block ids of this partition
-    const int32_t *bt = a.block_tables + (int64_t)m0 * a.max_blocks;
-    const int lb0 = t_begin / B, nblk = (t_end - 1) / B - lb0 + 1;
-    for (int i = threadIdx.x; i < nblk; i += blockDim.x) bt_s[i] = bt[lb0 + i];
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NWP);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    const int members = m1 - m0;
-    const int passes = (members + NWP - 1) / NWP;
-    const int iters = passes * ntiles;
-    if (warp == 0) {
-        // producer: the same tiles once per pass of up to NWP members
-        if (lane == 0) {
-            for (int it = 0; it < iters; ++it) {
-                const int st = it % NS;
-                if (it >= NS && !mbar_wait_bounded(&empty[st], (uint32_t)(((it / NS) - 1) & 1))) {
-                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                    break;
-                }
-                const int t0 = t_begin + (it % ntiles) * kTile;
-                TileRows r{-1, -1, 0u};
-                for (int sb = 0; sb < kTile / boxh; ++sb) {
-                    const int tok = t0 + sb * boxh;
-                    const int lb = tok / B;
-                    int blk = bt_s[lb - lb0];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                        blk = 0;
-                    }
-                    const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
-                    if (sb == 0) r.y0 = y; else r.y1 = y;
-                }
-                issue_rows<D>(&tm_k, &tm_v, smem + st * Lay::kStageBytes, &full[st], boxh, r);
-            }
-        }
-        return;  // no CTA-wide barrier follows
-    }
-
-    // consumers: warp w attends member (pass * NWP + w - 1)
-    uint32_t qb[D / 16][2];
-    WarpAcc<D> acc;
-    bool dead = false;
-    for (int pass = 0; pass < passes; ++pass) {
-        const int mi = pass * NWP + warp - 1;
-        const bool active = mi < members;
-        const int sq = m0 + (active ? mi : 0);
-        const int32_t *mbt = a.block_tables + (int64_t)sq * a.max_blocks;
-        if (active) load_q_fragments<D>(a, sq, kvh, lane, qb);
-        // once per pass: lane i checks that tile i's blocks are valid and are this
-        // member's own (shared) blocks; bit i of tile_ok gives the answer
-        bool ok = false, bad = false;
-        if (active && lane < ntiles) {
-            const int ta = t_begin + lane * kTile;
-            const int lba = ta / B, lbb = (ta + kTile - 1) / B;
-            const int ba = bt_s[lba - lb0], bb = bt_s[lbb - lb0];
-            const bool va = ba >= 0 && ba < a.num_blocks, vb = bb >= 0 && bb < a.num_blocks;
-            const bool sa = mbt[lba] == ba, sb = mbt[lbb] == bb;
-            ok = va && vb && sa && sb;
-            bad = (va && !sa) || (vb && !sb);
-        }
-        const uint32_t tile_ok = __ballot_sync(0xffffffffu, ok);
-        if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
-        acc.reset();
-        for (int i = 0; i < ntiles; ++i) {
-            const int it = pass * ntiles + i;
-            const int st = it % NS;
-            if (!dead && !mbar_wait_bounded(&full[st], (uint32_t)((it / NS) & 1))) {
-                if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                dead = true;
-            }
-            if (!dead && active) {
-                const uint32_t row_ok = (tile_ok >> i) & 1u ? 0xffffu : 0u;
-                unsigned char *sk = smem + st * Lay::kStageBytes;
-                attend_tile<D, false>(sk, sk + Lay::kKVBytes, row_ok, qb, a.scale_log2, acc, lane);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
-        }
-        if (active) {
-            SegCursor c;
-            c.seq = sq;
-            c.kvh = kvh;
-            store_piece<D>(a, acc, dead, c, false, a.prefix_slot + part, lane);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Multi-token paged attention (chunked prefill, verification of drafted
-// tokens): sequence s carries Q_s query tokens, the last Q_s positions of its
-// context; query i sits at position p = L_s - Q_s + i and attends to tokens
-// 0 .. p.  One CTA per (sequence, kv head, block of kMtQueries queries,
-// partition of kMtPart tokens): a producer warp streams the partition's tiles,
-// up to the block's last position, through a CTA-shared ring once; consumer
-// warp j attends query j of the block on the same tiles (S^T = K Q^T with the
-// group's query heads as the MMA's N), masking the tokens past its own
-// position.  A query whose context spans several partitions leaves one
-// partial per partition; the reduction kernel merges them, one virtual
-// sequence per query token with length p + 1 (q_lens).
-// ---------------------------------------------------------------------------
-constexpr int kMtQueries = 8;   // consumer warps: queries per CTA
-constexpr int kMtPart = 1024;   // tokens per partition (64 tiles)
-constexpr int kMtIds = kMtPart / 8 + 2;
-
-template <int D, int NS>
-constexpr int mt_smem_bytes() {
-    return NS * Bf16Layout<D>::kStageBytes + 2 * NS * 8 + kMtIds * 4 + 1024;
-}
-
-template <int D, int NS>
-__global__ void __launch_bounds__((kMtQueries + 1) * 32, 2)
-multi_token_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                   const DecodeArgs a, const int32_t *__restrict__ q_starts, int *__restrict__ q_lens,
-                   int num_q_tokens, int max_q_len, int parts) {
-    using Lay = Bf16Layout<D>;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * Lay::kStageBytes);
-    uint64_t *empty = full + NS;
-    int *bt_s = reinterpret_cast<int *>(empty + NS);
-
-    grid_dependency_wait();
-    grid_launch_dependents();
-
-    const int sq = blockIdx.x, kvh = blockIdx.y;
-    const int qblk = blockIdx.z % ((max_q_len + kMtQueries - 1) / kMtQueries);
-    const int part = blockIdx.z / ((max_q_len + kMtQueries - 1) / kMtQueries);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int B = a.block_size;
-    const int cap = min(a.max_seq_len, a.max_blocks * B);
-    const int raw = a.seq_lens[sq];
-    const int L = clamp_len(raw, cap);
-    int q0 = q_starts[sq], q1 = q_starts[sq + 1];
-    const bool first_cta = qblk == 0 && part == 0 && kvh == 0 && threadIdx.x == 0;
-    if (q0 < 0 || q1 < q0 || q1 > num_q_tokens) {
-        if (first_cta) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
-        q0 = q1 = 0;
-    }
-    if (first_cta && ((raw < 0 || raw > cap) || q1 - q0 > max_q_len || q1 - q0 > L))
-        flag_error(a.err, PKV_DEVERR_SEQ_LEN);
-    const int Q = min(q1 - q0, max_q_len);  // queries past max_q_len are not attended
-    const int i0 = qblk * kMtQueries;
-    if (i0 >= Q) return;
-    const int nq = min(kMtQueries, Q - i0);
-    const int pos0 = L - Q + i0;            // position of the block's first query (< 0 if Q > L)
-    const int p_last = pos0 + nq - 1;
-    if (q_lens && part == 0 && kvh == 0 && threadIdx.x < nq)  // merge input: each query's context length
-        q_lens[q0 + i0 + threadIdx.x] = max(0, pos0 + (int)threadIdx.x + 1);
-    const int t_begin = part * kMtPart;
-    const int t_end = min(p_last + 1, t_begin + kMtPart);
-    if (t_begin >= t_end) {
-        // nothing of this partition is visible to the block; part 0 still owes
-        // zero rows to queries that see no token at all (Q > L, flagged)
-        if (part == 0 && warp >= 1 && warp - 1 < nq && pos0 + warp - 1 < 0) {
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) +
-                               ((int64_t)(q0 + i0 + warp - 1) * a.num_heads + kvh * a.group) * D;
-            for (int e = lane; e < a.group * D; e += 32) o[e] = __float2bfloat16_rn(0.f);
-        }
-        return;
-    }
-    const int ntiles = (t_end - t_begin + kTile - 1) / kTile;
-    const int boxh = B < kTile ? B : kTile;
-    const int32_t *bt = a.block_tables + (int64_t)sq * a.max_blocks;
-    const int lb0 = t_begin / B, nblk = (t_begin + ntiles * kTile - 1) / B - lb0 + 1;
-    for (int i = threadIdx.x; i < nblk; i += blockDim.x)
-        bt_s[i] = lb0 + i < a.max_blocks ? bt[lb0 + i] : -1;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kMtQueries);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    // rows of tile k that come from a valid block and lie inside the context
-    // at or before the block's last position: what any consumer may attend
-    auto common_ok = [&](int k) -> uint32_t {
-        const int t0 = t_begin + k * kTile;
-        uint32_t m = 0;
-        for (int sb = 0; sb < kTile / boxh; ++sb) {
-            const int blk = bt_s[(t0 + sb * boxh) / B - lb0];
-            if (blk >= 0 && blk < a.num_blocks) m |= ((1u << boxh) - 1u) << (sb * boxh);
-        }
-        const int valid = min(kTile, min(p_last, L - 1) - t0 + 1);
-        return valid <= 0 ? 0u : (m & ((1u << valid) - 1u));
-    };
-
-    if (warp == 0) {
-        if (lane == 0) {
-            for (int k = 0; k < ntiles; ++k) {
-                const int st = k % NS;
-                if (k >= NS && !mbar_wait_bounded(&empty[st], (uint32_t)(((k / NS) - 1) & 1))) {
-                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                    break;
-                }
-                const int t0 = t_begin + k * kTile;
-                TileRows r{-1, -1, 0u};
-                for (int sb = 0; sb < kTile / boxh; ++sb) {
-                    const int tok = t0 + sb * boxh;
-                    const int lb = tok / B;
-                    int blk = bt_s[lb - lb0];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        if (tok < L) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                        blk = 0;  // never dereferenced out of range: rows masked out
-                    }
-                    const int y = (int)(((int64_t)blk * a.num_kv_heads + kvh) * B + (tok - lb * B));
-                    if (sb == 0) r.y0 = y; else r.y1 = y;
-                }
-                issue_rows<D>(&tm_k, &tm_v, smem + st * Lay::kStageBytes, &full[st], boxh, r);
-            }
-        }
-        return;  // no CTA-wide barrier follows
-    }
-
-    const int j = warp - 1;
-    const bool active = j < nq;
-    const int pj = pos0 + j;          // this query's position
-    const int row = q0 + i0 + j;      // its row in q / out
-    uint32_t qb[D / 16][2];
-    if (active && pj >= 0) load_q_fragments<D>(a, row, kvh, lane, qb);
-    WarpAcc<D> acc;
-    acc.reset();
-    bool dead = false;
-    for (int k = 0; k < ntiles; ++k) {
-        const int st = k % NS;
-        if (!dead && !mbar_wait_bounded(&full[st], (uint32_t)((k / NS) & 1))) {
-            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-            dead = true;
-        }
-        if (!dead && active && pj >= 0) {
-            const int t0 = t_begin + k * kTile;
-            const uint32_t zok = common_ok(k);
-            const int mine = min(kTile, pj - t0 + 1);  // rows at or before this query's position
-            const uint32_t row_ok = mine <= 0 ? 0u : (zok & ((1u << mine) - 1u));
-            if (row_ok) {
-                unsigned char *sk = smem + st * Lay::kStageBytes;
-                attend_tile<D, true>(sk, sk + Lay::kKVBytes, row_ok, qb, a.scale_log2, acc, lane, zok);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    if (!active) return;
-    if (pj < 0) {  // sees no token (Q > L, flagged): a zero row, written once
-        if (part == 0) {
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)row * a.num_heads + kvh * a.group) * D;
-            for (int e = lane; e < a.group * D; e += 32) o[e] = __float2bfloat16_rn(0.f);
-        }
-        return;
-    }
-    if (pj < t_begin) return;  // this partition holds nothing this query sees
-    SegCursor c;
-    c.seq = row;
-    c.kvh = kvh;
-    const bool whole = pj + 1 <= kMtPart;  // the query's context fits one partition
-    store_piece<D>(a, acc, dead, c, whole, part, lane);
-}
-
-// ---------------------------------------------------------------------------
-// Shared prefixes on the 5th-generation tensor cores (tcgen05).
-//
-// Per kv head, a group's prefix is one dense contraction: the queries of all
-// members (members x G rows) against the same K and V tiles.  One CTA per SM
-// takes an equal contiguous share of the 64-token tiles of all contexts
-// (group, member chunk, kv head) and walks it piece by piece (a piece = the
-// share's tiles of one context).  Warp roles:
-//   warps 0-3  softmax: one thread per query row = one TMEM lane.  Reads S
-//              from TMEM, keeps the row's running max and sum, writes P
-//              (bf16) to shared memory, and at the end of a piece reads O
-//              from TMEM and stores the partial.
-//   warp 4     producer: the leader's block ids of a piece staged in shared
-//              memory by the whole warp (many loads in flight), then TMA loads
-//              of K and V tiles into an NS-stage ring from one lane.
-//   warp 5     MMA: one thread issues S = Q K^T (double-buffered in TMEM)
-//              and O += P V (accumulated in TMEM); the warp owns the TMEM
-//              allocation.
-//   warp 6     checks that every member's block table holds the leader's
-//              blocks over the prefix (flags PKV_DEVERR_PREFIX otherwise).
-// The MMA is M = 128 rows; rows past members x G are zero queries whose
-// results are never stored.  The running max is only moved (and O rescaled)
-// when a tile's max exceeds it by more than 2^8, so most tiles rescale
-// nothing; the merge uses whatever max each partial carries.
-// ---------------------------------------------------------------------------
-namespace tc {
-constexpr int kTok = 64;          // tokens per tile: N of Q K^T, K of P V
-constexpr int kRows = 128;        // MMA M: query rows of one context
-constexpr int kMinTiles = 4;      // shares hold >= 256 tokens
-constexpr int kMaxGroups = 2048;  // groups whose tile counts are scanned in shared memory
-constexpr int kThreads = 224;
-constexpr int kIdCache = 512;     // leader block ids staged by the producer warp
-constexpr float kRescale = 8.f;   // headroom (log2 units) before the running max moves
-constexpr uint32_t kTmemCols = 512;  // S0 | S1 (64 columns each) | O0 | O1 (128 each, by piece parity)
-
-template <int D, int NS>
-struct Layout {
-    static constexpr int kHalves = D / 64;
-    static constexpr int kQBytes = kHalves * kRows * 128;  // [half][row][128 B]
-    static constexpr int kKVBytes = kHalves * kTok * 128;  // K or V of one tile: [half][token][128 B]
-    static constexpr int kStageBytes = 2 * kKVBytes;
-    static constexpr int kPBytes = kRows * kTok * 2;       // [row][64 tokens] bf16
-    static constexpr int q = 0;
-    static constexpr int ring = q + kQBytes;
-    static constexpr int p = ring + NS * kStageBytes;
-    static constexpr int scan = p + 2 * kPBytes;           // cum[kMaxGroups + 1], tiles[kMaxGroups]
-    static constexpr int ids = scan + ((2 * kMaxGroups + 1) * 4 + 7) / 8 * 8;
-    static constexpr int bars = ids + kIdCache * 4;
-    static constexpr int kBars = 2 * NS + 8;               // kv_full, kv_empty, s_full2, p_full2, o_done2, ready, fin
-    static constexpr int misc = bars + kBars * 8;          // TMEM address, scan scratch (8 ints + carry)
-    static constexpr int total = misc + 64 + 1024;         // + alignment slack
-};
-
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    // start >> 4 | LBO >> 4 << 16 | SBO >> 4 << 32 | version 1 << 46 | 128-byte swizzle (2) << 61
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// kind::f16 instruction descriptor: bf16 A and B, fp32 D, M = 128.
-__host__ __device__ constexpr uint32_t instr_desc(int n, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void ld32(uint32_t taddr, float *v) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void st32(uint32_t taddr, const float (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-        : "memory");
-}
-
-__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// One context of the tile list: group g, context c of the group (member
-// chunk c / Hkv, kv head c % Hkv), tiles [start, start + n).
-struct Cursor {
-    int g, c, n, contexts;
-    int64_t start;
-    // largest group with cum[g] <= t (t < cum[num_groups])
-    __device__ __forceinline__ void seek(const int *cum, const int *tiles, int num_groups, int64_t t) {
-        int lo = 0, hi = num_groups;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cum[mid] <= t) lo = mid; else hi = mid;
-        }
-        g = lo;
-        n = tiles[g];
-        contexts = (cum[g + 1] - cum[g]) / n;
-        c = (int)((t - cum[g]) / n);
-        start = cum[g] + (int64_t)c * n;
-    }
-    __device__ __forceinline__ void next(const int *cum, const int *tiles) {
-        start += n;
-        if (++c == contexts) {
-            do { ++g; } while (cum[g + 1] == cum[g]);
-            n = tiles[g];
-            contexts = (cum[g + 1] - cum[g]) / n;
-            c = 0;
-            start = cum[g];
-        }
-    }
-};
-}  // namespace tc
-
-template <int D, int NS>
-__global__ void __launch_bounds__(tc::kThreads, 1)
-decode_bf16_prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
-                             const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a,
-                             const int32_t *__restrict__ group_offsets,
-                             const int32_t *__restrict__ prefix_lens, int num_groups) {
-    using L = tc::Layout<D, NS>;
-    constexpr int H = L::kHalves;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    int *cum = reinterpret_cast<int *>(smem + L::scan);
-    int *tiles = cum + tc::kMaxGroups + 1;
-    uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + L::bars);
-    uint64_t *kv_empty = kv_full + NS;
-    uint64_t *s_full = kv_empty + NS;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2;
-    uint64_t *ready = o_done + 2;
-    uint64_t *fin = ready + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
-    int *warp_sums = reinterpret_cast<int *>(smem + L::misc + 16);  // one per warp + carry
-    int *idc = reinterpret_cast<int *>(smem + L::ids);
-    constexpr int kCarry = tc::kThreads / 32;
-
-    grid_dependency_wait();
-    grid_launch_dependents();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = a.num_seqs, Hkv = a.num_kv_heads, G = a.group, B = a.block_size;
-    const int cap = min(a.max_seq_len, a.max_blocks * B);
-    const int align = B > kTile ? B : kTile;
-    const int mpc = tc::kRows / G;  // members per chunk
-
-    if (blockIdx.x == 0) {
-        if (threadIdx.x == 0 && (group_offsets[0] != 0 || group_offsets[num_groups] != S))
-            flag_error(a.err, PKV_DEVERR_PREFIX);
-        for (int i = threadIdx.x; i < S; i += blockDim.x) a.seq_tok0[i] = 0;
-    }
-    if (threadIdx.x == 0) {
-        cum[0] = 0;
-        warp_sums[kCarry] = 0;
-    }
-    __syncthreads();
-
-    // per group: the prefix actually attended (cut to the shortest member,
-    // minus the appended token, and to whole tiles), then a scan of the
-    // groups' tiles over all their contexts
-    for (int base = 0; base < num_groups; base += tc::kThreads) {
-        const int g = base + threadIdx.x;
-        int v = 0;
-        if (g < num_groups) {
-            int m0 = group_offsets[g], m1 = group_offsets[g + 1];
-            if (m0 < 0 || m1 > S || m1 < m0) {
-                if (blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
-                m0 = m1 = 0;
-            }
-            const int raw = prefix_lens[g];
-            if (raw % align != 0 && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
-            int mn = cap;
-            for (int i = m0; i < m1; ++i) mn = min(mn, clamp_len(a.seq_lens[i], cap));
-            int pre = min(raw < 0 ? 0 : raw, mn - (a.k_new ? 1 : 0));
-            pre = m1 > m0 && pre > 0 ? pre / tc::kTok * tc::kTok : 0;
-            if (blockIdx.x == 0)
-                for (int i = m0; i < m1; ++i) a.seq_tok0[i] = pre;
-            tiles[g] = pre / tc::kTok;
-            v = tiles[g] * ((m1 - m0 + mpc - 1) / mpc) * Hkv;
-        }
-        int x = v;
-#pragma unroll
-        for (int sh = 1; sh < 32; sh <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, sh);
-            if (lane >= sh) x += y;
-        }
-        if (lane == 31) warp_sums[warp] = x;
-        __syncthreads();
-        int before = warp_sums[kCarry];
-        for (int w = 0; w < warp; ++w) before += warp_sums[w];
-        if (g < num_groups) cum[g + 1] = before + x;
-        __syncthreads();
-        if (threadIdx.x == tc::kThreads - 1) warp_sums[kCarry] = before + x;
-        __syncthreads();
-    }
-    const int64_t T = cum[num_groups];
-    const int64_t parts = min((int64_t)gridDim.x, max((int64_t)1, T / tc::kMinTiles));
-    if (T == 0 || blockIdx.x >= parts) return;  // before any TMEM is taken
-    const int64_t s0 = (int64_t)blockIdx.x * T / parts, s1 = ((int64_t)blockIdx.x + 1) * T / parts;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&o_done[i], 1);
-        }
-        mbar_init(ready, 4);
-        mbar_init(fin, 1);
-        fence_barrier_init();
-    }
-    if (warp == 5) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(tmem_slot)),
-                     "r"(tc::kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    const uint32_t q_s = smem_u32(smem + L::q);
-    const uint32_t ring_s = smem_u32(smem + L::ring);
-    const uint32_t p_s = smem_u32(smem + L::p);
-
-    if (warp == 4) {
-        // ---------------- producer ----------------
-        tc::Cursor cur;
-        cur.seek(cum, tiles, num_groups, s0);
-        int64_t j = 0, issued = 0;
-        bool dead = false;
-        const int boxh = B < kTile ? B : kTile;
-        const int bpt = tc::kTok / B;  // blocks per tile
-        for (int64_t t = s0; t < s1;) {
-            const int64_t t1 = min(s1, cur.start + cur.n);
-            const int i0 = (int)(t - cur.start), i1 = (int)(t1 - cur.start);
-            const int kvh = cur.c % Hkv;
-            const int32_t *bt = a.block_tables + (int64_t)group_offsets[cur.g] * a.max_blocks;
-            for (int cb = i0 * bpt; cb < i1 * bpt; cb += tc::kIdCache) {
-                const int nb = min(tc::kIdCache, i1 * bpt - cb);
-                __syncwarp();  // the previous chunk has been issued
-                for (int k0 = 0; k0 < nb; k0 += 128) {
-                    int v[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int k = k0 + u * 32 + lane;
-                        v[u] = k < nb ? bt[cb + k] : 0;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (k0 + u * 32 + lane < nb) idc[k0 + u * 32 + lane] = v[u];
-                }
-                __syncwarp();
-                // one tile per step: lane 0 claims the stage, then lane i issues box i
-                // (sub-block i / (2H), half (i / 2) % H, K or V by i % 2)
-                for (int tl = 0; tl < nb / bpt; ++tl, ++j) {
-                    const int st = (int)(j % NS);
-                    if (lane == 0 && !dead && j >= NS &&
-                        !mbar_wait_bounded(&kv_empty[st], (uint32_t)(((j / NS) - 1) & 1))) {
-                        flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                        dead = true;
-                    }
-                    dead = __shfl_sync(0xffffffffu, dead, 0);
-                    if (dead) continue;
-                    ++issued;
-                    if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], (uint32_t)L::kStageBytes);
-                    __syncwarp();
-                    const int nbox = (tc::kTok / boxh) * 2 * H;
-                    for (int bi = lane; bi < nbox; bi += 32) {
-                        const int sb = bi / (2 * H), h = (bi >> 1) % H;
-                        const int tok = sb * boxh;  // within the tile
-                        int blk = idc[tl * bpt + tok / B];
-                        if (blk < 0 || blk >= a.num_blocks) {
-                            flag_error(a.err, PKV_DEVERR_BLOCK_ID);
-                            blk = 0;
-                        }
-                        const int y = (int)(((int64_t)blk * Hkv + kvh) * B + tok % B);
-                        const uint32_t dst = ring_s + st * L::kStageBytes + (bi & 1) * L::kKVBytes +
-                                             h * (tc::kTok * 128) + sb * boxh * 128;
-                        tma_load_2d(dst, (bi & 1) ? &tm_v : &tm_k, smem_u32(&kv_full[st]), h * 64, y);
-                    }
-                }
-            }
-            t = t1;
-            if (t < s1) cur.next(cum, tiles);
-        }
-        // copies still in flight (only after a timeout) land before the CTA exits
-        if (lane == 0)
-            for (int64_t k = max((int64_t)0, issued - NS); k < issued; ++k)
-                mbar_wait_bounded(&kv_full[k % NS], (uint32_t)((k / NS) & 1));
-    } else if (warp == 6) {
-        // ---------------- members' block tables ----------------
-        // the kv head 0 contexts cover every prefix block of every member once
-        tc::Cursor cur;
-        cur.seek(cum, tiles, num_groups, s0);
-        const int bpt = tc::kTok / B;
-        bool bad = false;
-        for (int64_t t = s0; t < s1;) {
-            const int64_t t1 = min(s1, cur.start + cur.n);
-            if (cur.c % Hkv == 0) {
-                const int i0 = (int)(t - cur.start), i1 = (int)(t1 - cur.start);
-                const int chunk = cur.c / Hkv;
-                const int m0 = group_offsets[cur.g], m1 = group_offsets[cur.g + 1];
-                const int c0 = m0 + chunk * mpc, c1 = min(m1, c0 + mpc);
-                const int32_t *bt = a.block_tables + (int64_t)m0 * a.max_blocks;
-                const int lb0 = i0 * bpt, nb = (i1 - i0) * bpt;
-                const int total = (c1 - c0) * nb;
-                for (int k0 = 0; k0 < total; k0 += 128) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int k = k0 + u * 32 + lane;
-                        if (k < total) {
-                            const int m = c0 + k / nb, lb = lb0 + k % nb;
-                            if (m != m0 && a.block_tables[(int64_t)m * a.max_blocks + lb] != bt[lb]) bad = true;
-                        }
-                    }
-                }
-            }
-            t = t1;
-            if (t < s1) cur.next(cum, tiles);
-        }
-        if (bad) flag_error(a.err, PKV_DEVERR_PREFIX);
-    } else if (warp == 5) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::instr_desc(tc::kTok, false);
-            constexpr uint32_t idesc_pv = tc::instr_desc(D, true);
-            tc::Cursor cur;
-            cur.seek(cum, tiles, num_groups, s0);
-            int64_t j = 0, piece = 0;
-            bool dead = false;
-            auto wait = [&](uint64_t *bar, uint32_t parity) {
-                if (!dead && !mbar_wait_bounded(bar, parity)) {
-                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                    dead = true;
-                }
-                tc::fence_after();
-            };
-            auto pv = [&](int64_t jj, bool first, uint32_t ob) {
-                const int b = (int)(jj & 1), st = (int)(jj % NS);
-                wait(&p_full[b], (uint32_t)((jj >> 1) & 1));
-                const uint32_t pb = p_s + b * L::kPBytes;
-                const uint32_t vb = ring_s + st * L::kStageBytes + L::kKVBytes;
-                if (!dead) {
-#pragma unroll
-                    for (int k = 0; k < tc::kTok / 16; ++k)
-                        tc::mma(tmem + ob, tc::smem_desc(pb + k * 32, 16, 1024),
-                                tc::smem_desc(vb + k * 2048, tc::kTok * 128, 1024), idesc_pv,
-                                (first && k == 0) ? 0u : 1u);
-                }
-                tc::commit(&o_done[b]);
-                tc::commit(&kv_empty[st]);
-            };
-            for (int64_t t = s0; t < s1;) {
-                const int64_t t1 = min(s1, cur.start + cur.n);
-                const int nt = (int)(t1 - t);
-                wait(ready, (uint32_t)(piece & 1));
-                const uint32_t ob = 128 + (uint32_t)(piece & 1) * 128;
-                for (int i = 0; i < nt; ++i, ++j) {
-                    const int st = (int)(j % NS), b = (int)(j & 1);
-                    wait(&kv_full[st], (uint32_t)((j / NS) & 1));
-                    const uint32_t kb = ring_s + st * L::kStageBytes;
-                    if (!dead) {
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k)
-                            tc::mma(tmem + b * tc::kTok,
-                                    tc::smem_desc(q_s + (k >> 2) * (tc::kRows * 128) + (k & 3) * 32, 16, 1024),
-                                    tc::smem_desc(kb + (k >> 2) * (tc::kTok * 128) + (k & 3) * 32, 16, 1024),
-                                    idesc_qk, k > 0 ? 1u : 0u);
-                    }
-                    tc::commit(&s_full[b]);
-                    if (i > 0) pv(j - 1, i == 1, ob);
-                }
-                pv(j - 1, nt == 1, ob);
-                ++piece;
-                t = t1;
-                if (t < s1) cur.next(cum, tiles);
-            }
-            // every MMA has completed before the TMEM is freed
-            tc::commit(fin);
-            mbar_wait_bounded(fin, 0u);
-        }
-    } else if (warp < 4) {
-        // ---------------- softmax (warps 0-3: rows 32w .. 32w+31) ----------------
-        const int r = warp * 32 + lane;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        tc::Cursor cur;
-        cur.seek(cum, tiles, num_groups, s0);
-        int64_t j = 0, piece = 0;
-        bool dead = false;
-        auto wait = [&](uint64_t *bar, uint32_t parity) {
-            if (!dead && !mbar_wait_bounded(bar, parity)) {
-                flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                dead = true;
-            }
-            tc::fence_after();
-        };
-        // this thread's query row of the context at cursor c into Q (128-byte
-        // swizzled, K-major; zero past the context's rows), copied asynchronously
-        auto copy_q = [&](const tc::Cursor &c) {
-            const int kvh = c.c % Hkv, chunk = c.c / Hkv;
-            const int m0 = group_offsets[c.g], m1 = group_offsets[c.g + 1];
-            const int c0 = m0 + chunk * mpc, rows = (min(m1, c0 + mpc) - c0) * G;
-            const __nv_bfloat16 *src =
-                static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)(c0 + r / G) * a.num_heads + kvh * G + r % G) * D;
-#pragma unroll
-            for (int k = 0; k < D / 8; ++k) {
-                const uint32_t dst = q_s + (k >> 3) * (tc::kRows * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
-                if (r < rows)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k * 8) : "memory");
-                else
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        auto q_ready = [&]() {
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            fence_proxy_async();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ready);
-        };
-        copy_q(cur);
-        q_ready();
-        for (int64_t t = s0; t < s1;) {
-            const int64_t t1 = min(s1, cur.start + cur.n);
-            const int nt = (int)(t1 - t);
-            const int kvh = cur.c % Hkv, chunk = cur.c / Hkv;
-            const int m0 = group_offsets[cur.g], m1 = group_offsets[cur.g + 1];
-            const int c0 = m0 + chunk * mpc, c1 = min(m1, c0 + mpc);
-            const int rows = (c1 - c0) * G;
-            const bool live = warp * 32 < rows;
-            const int seq = c0 + (r < rows ? r / G : 0), head = kvh * G + r % G;
-            const uint32_t ob = 128 + (uint32_t)(piece & 1) * 128;  // this piece's O in TMEM
-            tc::Cursor nx = cur;
-            if (t1 < s1) nx.next(cum, tiles);
-
-            float m_run = -INFINITY, l = 0.f;
-            for (int i = 0; i < nt; ++i, ++j) {
-                const int b = (int)(j & 1);
-                wait(&s_full[b], (uint32_t)((j >> 1) & 1));
-                // every Q K^T of this piece has completed: Q may take the next piece's rows
-                if (i == nt - 1 && t1 < s1) copy_q(nx);
-                if (live) {
-                    float s[64];
-                    tc::ld32(trow + b * tc::kTok, s);
-                    tc::ld32(trow + b * tc::kTok + 32, s + 32);
-                    tc::wait_ld();
-                    float mt = -INFINITY;
-#pragma unroll
-                    for (int k = 0; k < 64; ++k) {
-                        s[k] *= a.scale_log2;
-                        mt = fmaxf(mt, s[k]);
-                    }
-                    const float m_new = i == 0 ? mt : (mt > m_run + tc::kRescale ? mt : m_run);
-                    const bool move = i > 0 && m_new != m_run;
-                    if (__any_sync(0xffffffffu, move)) {
-                        // O must hold P V of the previous tile before it is rescaled
-                        wait(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
-                        const float alpha = move ? exp2f(m_run - m_new) : 1.f;
-#pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            float o[32];
-                            tc::ld32(trow + ob + c * 32, o);
-                            tc::wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                            tc::st32(trow + ob + c * 32, o);
-                        }
-                        tc::wait_st();
-                        l *= alpha;
-                    }
-                    m_run = m_new;
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        pk[k] = pack_bf16x2(exp2f(s[2 * k] - m_run), exp2f(s[2 * k + 1] - m_run));
-                        l += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
-                    }
-                    // P buffer b was last read by the P V of tile j - 2
-                    if (i >= 2) wait(&o_done[b], (uint32_t)(((j - 2) >> 1) & 1));
-                    const uint32_t prow = p_s + b * L::kPBytes + r * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((c ^ (r & 7)) << 4)),
-                                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                                     : "memory");
-                }
-                fence_proxy_async();
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[b]);
-            }
-            // the next piece's MMAs may start while this one's O is read out
-            if (t1 < s1) q_ready();
-            // the piece's partial: unnormalised O row, running max, sum
-            wait(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1));
-            if (live) {
-                const int64_t first = share_owner(cur.start, T, parts);
-                const int slot = a.prefix_slot + (int)(share_owner(t, T, parts) - first);
-                const int64_t prow = (int64_t)seq * a.num_heads + head;
-                float *dst = a.part_o + (prow * a.max_parts + slot) * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tc::ld32(trow + ob + c * 32, o);
-                    tc::wait_ld();
-                    if (r < rows) {
-#pragma unroll
-                        for (int k = 0; k < 32; k += 4)
-                            *reinterpret_cast<float4 *>(dst + c * 32 + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-                    }
-                }
-                if (r < rows) {
-                    a.part_m[prow * a.max_parts + slot] = dead ? -INFINITY : m_run;
-                    a.part_l[prow * a.max_parts + slot] = dead ? 0.f : l;
-                    if (t == cur.start && r % G == 0)
-                        a.prefix_pieces[(int64_t)seq * Hkv + kvh] =
-                            (int)(share_owner(cur.start + cur.n - 1, T, parts) - first + 1);
-                }
-            }
-            ++piece;
-            t = t1;
-            cur = nx;
-        }
-    }
-    tc::fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc::fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tc::kTmemCols)
-                     : "memory");
-    }
-}
-
-// ---------------------------------------------------------------------------
 // CUDA-core kernel (fp32 I/O; also instantiated for bf16 storage)
 // ---------------------------------------------------------------------------
 template <typename T, int D, int NW>
@@ -2740,8 +1730,6 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
 constexpr int kDefaultPartition = 512;
 constexpr int kMaxBalancedSeqs = 8192;
 
-static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
 struct WorkspaceLayout {
     size_t o_off, m_off, l_off, pieces_off, flags_off, total;
 };
@@ -2767,103 +1755,10 @@ static int64_t balanced_slots(int max_seq_len) {
     return ((int64_t)max_seq_len + kMinTilesPerCta * kTile - 1) / (kMinTilesPerCta * kTile) + 1;
 }
 
-// A 64-bit tag per balanced call, never 0 (the value of a cleared flag): flags
-// left by other calls, or never written, hold another value.  The sequence
-// starts at a value drawn from the clock, the process and an address, so
-// separate processes start far apart.
-static unsigned long long next_call_tag() {
-    static std::atomic<unsigned long long> count{0};
-    static const unsigned long long base = [] {
-        unsigned long long x = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
-        x ^= (unsigned long long)getpid() * 0x9E3779B97F4A7C15ull;
-        x ^= (unsigned long long)reinterpret_cast<uintptr_t>(&count);
-        x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
-        x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
-        return x ^ (x >> 31);
-    }();
-    unsigned long long t;
-    do {
-        t = base + count.fetch_add(1, std::memory_order_relaxed);
-    } while (t == 0);
-    return t;
-}
-
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D view of a bf16 cache: rows = num_blocks * Hkv * B, columns = head_dim.
-// Box = 64 columns (128 bytes, 128-byte swizzle) x min(B, 16) rows.
-static bool make_cache_map(CUtensorMap *map, const void *base, int64_t rows, int D, int boxh) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)boxh};
-    cuuint32_t estr[2] = {1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static bool make_cache_maps(const DecodeArgs &a, int D, CUtensorMap *mk, CUtensorMap *mv) {
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
     const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
     return make_cache_map(mk, a.k_cache, rows, D, boxh) && make_cache_map(mv, a.v_cache, rows, D, boxh);
-}
-
-// Opt a kernel in to the dynamic shared memory it may need (once per device).
-template <typename K>
-static bool ensure_smem(K kernel, int bytes, bool (&done)[128]) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
-    if (!done[dev]) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-            return false;
-        done[dev] = true;
-    }
-    return true;
-}
-
-static int sm_count() {
-    static int counts[128] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
-    if (!counts[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
-}
-
-// Launch with programmatic stream serialization: the kernel may start while
-// the previous kernel in the stream drains; it waits (griddepcontrol.wait)
-// before touching memory, so stream order is preserved.
-template <typename... KArgs, typename... Args>
-static pkv_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t st, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? launch_status() : PKV_ERR_CUDA;
 }
 
 // Launch shapes (warps per CTA x ring stages per warp): the shapes measured
@@ -2983,7 +1878,11 @@ PKV_API size_t paged_attention_workspace_size(int num_seqs, int num_heads, int h
     return workspace_layout(num_seqs, num_heads, head_dim, parts, false).total;
 }
 
-static pkv_status append_tokens(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+namespace pkv {
+
+// The store of each sequence's new token at position seq_lens[s] - 1 (looked
+// up in its block table), for the paths that do not fuse it into attention.
+pkv_status append_new_tokens(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                                 const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
                                 int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                                 int num_blocks, int max_seq_len, int dtype, cudaStream_t st) {
@@ -3001,6 +1900,8 @@ static pkv_status append_tokens(const void *k_new, const void *v_new, void *k_ca
                       block_tables, seq_lens, num_seqs, num_kv_heads, chunks, block_size, max_blocks_per_seq,
                       num_blocks, cap, device_error_word());
 }
+
+}  // namespace pkv
 
 static pkv_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
@@ -3171,107 +2072,6 @@ static pkv_status decode_fp8_impl(void *out, const void *q, const void *k_cache,
     return dispatch_balanced_f8(a, st);
 }
 
-// ---------------------------------------------------------------------------
-// Multi-token paged attention
-// ---------------------------------------------------------------------------
-static int64_t mt_parts(int max_seq_len) { return ((int64_t)max_seq_len + kMtPart - 1) / kMtPart; }
-
-PKV_API size_t paged_attention_multi_token_workspace_size(int num_q_tokens, int num_heads, int head_dim,
-                                                          int max_seq_len) {
-    if (num_q_tokens <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
-    const int64_t parts = mt_parts(max_seq_len);
-    if (parts <= 1) return 0;
-    return workspace_layout(num_q_tokens, num_heads, head_dim, parts, false).total +
-           round256((size_t)num_q_tokens * 4);
-}
-
-template <int D>
-static pkv_status launch_multi_token(const DecodeArgs &a, const int32_t *q_starts, int *q_lens, int num_q_tokens,
-                                     int max_q_len, int parts, cudaStream_t st) {
-    constexpr int NS = 8;  // 64 KB of tiles in flight per CTA (two CTAs per SM)
-    static bool done[128] = {};
-    constexpr int smem = mt_smem_bytes<D, NS>();
-    auto kern = multi_token_kernel<D, NS>;
-    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
-    CUtensorMap mk, mv;
-    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
-    const int nqblk = (max_q_len + kMtQueries - 1) / kMtQueries;
-    const dim3 grid((unsigned)a.num_seqs, (unsigned)a.num_kv_heads, (unsigned)(nqblk * parts));
-    return launch_pdl(kern, grid, dim3((kMtQueries + 1) * 32), smem, st, mk, mv, a, q_starts, q_lens,
-                      num_q_tokens, max_q_len, parts);
-}
-
-PKV_API pkv_status paged_attention_multi_token(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                               const int32_t *block_tables, const int32_t *seq_lens,
-                                               const int32_t *q_starts, int num_seqs, int num_q_tokens,
-                                               int num_heads, int num_kv_heads, int head_dim, int block_size,
-                                               int max_blocks_per_seq, int num_blocks, int max_q_len,
-                                               int max_seq_len, float scale, void *workspace,
-                                               size_t workspace_bytes, void *stream) {
-    if (num_seqs < 0 || num_q_tokens < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||
-        num_blocks < 1 || max_seq_len < 0 || max_q_len < 0 || !std::isfinite(scale))
-        return PKV_ERR_INVALID;
-    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
-    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
-    if (num_heads / num_kv_heads > kGMax) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || num_q_tokens == 0) return PKV_OK;
-    if (max_q_len < 1 || max_seq_len < 1) return PKV_ERR_INVALID;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_starts) return PKV_ERR_INVALID;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
-    if (((int64_t)num_blocks + 1) * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
-    const int64_t parts = mt_parts(max_seq_len);
-    const int64_t nqblk = ((int64_t)max_q_len + kMtQueries - 1) / kMtQueries;
-    if (nqblk * parts > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-
-    DecodeArgs a{};
-    a.out = out;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.num_seqs = num_seqs;
-    a.num_heads = num_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.group = num_heads / num_kv_heads;
-    a.block_size = block_size;
-    a.max_blocks = max_blocks_per_seq;
-    a.num_blocks = num_blocks;
-    a.max_seq_len = max_seq_len;
-    a.partition_size = kMtPart;
-    a.max_parts = (int)parts;
-    a.scale = scale;
-    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    a.err = device_error_word();
-    int *q_lens = nullptr;
-    if (parts > 1) {
-        const WorkspaceLayout lay = workspace_layout(num_q_tokens, num_heads, head_dim, parts, false);
-        if (!workspace || workspace_bytes < lay.total + round256((size_t)num_q_tokens * 4) ||
-            (reinterpret_cast<uintptr_t>(workspace) & 255u))
-            return PKV_ERR_INVALID;
-        unsigned char *ws = static_cast<unsigned char *>(workspace);
-        a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
-        a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
-        a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
-        q_lens = reinterpret_cast<int *>(ws + lay.total);
-    }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    pkv_status rc = head_dim == 128
-                        ? launch_multi_token<128>(a, q_starts, q_lens, num_q_tokens, max_q_len, (int)parts, st)
-                        : launch_multi_token<64>(a, q_starts, q_lens, num_q_tokens, max_q_len, (int)parts, st);
-    if (rc == PKV_OK && parts > 1) {
-        // one virtual sequence per query token, of length p + 1
-        DecodeArgs m = a;
-        m.num_seqs = num_q_tokens;
-        m.seq_lens = q_lens;
-        rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, false>(m, st)
-                             : launch_reduce<__nv_bfloat16, 64, true, false>(m, st);
-    }
-    return rc;
-}
-
 PKV_API pkv_status paged_attention_decode_fp8(void *out, const void *q, const void *k_cache,
                                               const void *v_cache, const int32_t *block_tables,
                                               const int32_t *seq_lens, int num_seqs, int num_heads,
@@ -3330,7 +2130,7 @@ PKV_API pkv_status paged_attention_decode_append(
         if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
         if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
         if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
-        const pkv_status rc = append_tokens(k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
+        const pkv_status rc = append_new_tokens(k_new, v_new, k_cache, v_cache, block_tables, seq_lens,
                                             num_seqs, num_kv_heads, head_dim, block_size,
                                             max_blocks_per_seq, num_blocks, max_seq_len, dtype,
                                             static_cast<cudaStream_t>(stream));
@@ -3343,149 +2143,6 @@ PKV_API pkv_status paged_attention_decode_append(
     return decode_impl(out, q, k_cache, v_cache, block_tables, seq_lens, num_seqs, num_heads,
                        num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, max_seq_len,
                        scale, partition_size, workspace, workspace_bytes, dtype, stream, k_new, v_new);
-}
-
-// ---------------------------------------------------------------------------
-// Grouped decode: shared prefixes attended once per group.
-// ---------------------------------------------------------------------------
-static int64_t prefix_slots(int max_seq_len) { return ((int64_t)max_seq_len + kPrefixPart - 1) / kPrefixPart; }
-
-// Prefix partial slots: a prefix of L tokens spans at most ceil(L / 256) + 1
-// shares of the tensor-core prefix kernel (shares hold >= 256 tokens), and
-// ceil(L / 256) partitions of the other prefix kernel.
-static WorkspaceLayout grouped_layout(int64_t S, int64_t Hq, int64_t D, int max_seq_len, size_t *tok0_off,
-                                      size_t *npre_off) {
-    WorkspaceLayout w =
-        workspace_layout(S, Hq, D, balanced_slots(max_seq_len) + prefix_slots(max_seq_len) + 1, true);
-    *tok0_off = w.total;
-    w.total += round256((size_t)(S * 4));
-    *npre_off = w.total;
-    w.total += round256((size_t)(S * Hq * 4));
-    return w;
-}
-
-template <int D>
-static pkv_status launch_prefix_tc(const DecodeArgs &a, const int32_t *group_offsets, const int32_t *prefix_lens,
-                                   int num_groups, cudaStream_t st) {
-    constexpr int NS = D == 128 ? 4 : 8;
-    constexpr int smem = tc::Layout<D, NS>::total;
-    static bool done[128] = {};
-    auto kern = decode_bf16_prefix_tc_kernel<D, NS>;
-    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
-    CUtensorMap mk, mv;
-    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
-    const int sms = sm_count();
-    if (sms <= 0) return PKV_ERR_CUDA;
-    return launch_pdl(kern, dim3((unsigned)sms), dim3(tc::kThreads), smem, st, mk, mv, a, group_offsets,
-                      prefix_lens, num_groups);
-}
-
-template <int D>
-static pkv_status launch_prefix(const DecodeArgs &a, const int32_t *group_offsets, const int32_t *prefix_lens,
-                                int num_groups, cudaStream_t st) {
-    constexpr int NS = 8;
-    static bool done[128] = {};
-    constexpr int smem = prefix_smem_bytes<D, NS>();
-    auto kern = decode_bf16_prefix_kernel<D, NS>;
-    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
-    CUtensorMap mk, mv;
-    if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
-    const dim3 grid((unsigned)num_groups, (unsigned)a.num_kv_heads, (unsigned)prefix_slots(a.max_seq_len));
-    return launch_pdl(kern, grid, dim3((kPrefixMembers + 1) * 32), smem, st, mk, mv, a, group_offsets,
-                      prefix_lens, num_groups);
-}
-
-PKV_API size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim,
-                                                      int max_seq_len) {
-    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
-    size_t tok0_off = 0, npre_off = 0;
-    return grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off, &npre_off).total;
-}
-
-PKV_API pkv_status paged_attention_decode_grouped(
-    void *out, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
-    const int32_t *block_tables, const int32_t *seq_lens, const int32_t *group_offsets,
-    const int32_t *prefix_lens, int num_groups, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
-    int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale, void *workspace,
-    size_t workspace_bytes, int dtype, void *stream) {
-    if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
-        max_seq_len < 0 || !std::isfinite(scale) || num_groups < 1)
-        return PKV_ERR_INVALID;
-    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
-    if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
-    if (num_heads / num_kv_heads > kGMax || num_seqs > kMaxBalancedSeqs) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || max_seq_len == 0) return PKV_OK;
-    if (num_groups > num_seqs || (int64_t)num_groups > 0x7fffffff) return PKV_ERR_INVALID;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !group_offsets || !prefix_lens)
-        return PKV_ERR_INVALID;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
-    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
-    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
-    const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
-    if (rows > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
-    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
-        return PKV_ERR_UNSUPPORTED;
-    if (prefix_slots(max_seq_len) > 65535) return PKV_ERR_INVALID;
-    size_t tok0_off = 0, npre_off = 0;
-    const WorkspaceLayout lay = grouped_layout(num_seqs, num_heads, head_dim, max_seq_len, &tok0_off, &npre_off);
-    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return PKV_ERR_INVALID;
-
-    DecodeArgs a{};
-    a.out = out;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.num_seqs = num_seqs;
-    a.num_heads = num_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.group = num_heads / num_kv_heads;
-    a.block_size = block_size;
-    a.max_blocks = max_blocks_per_seq;
-    a.num_blocks = num_blocks;
-    a.max_seq_len = max_seq_len;
-    a.partition_size = kDefaultPartition;
-    a.scale = scale;
-    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    a.err = device_error_word();
-    a.k_new = k_new;
-    a.v_new = v_new;
-    a.k_cache_w = k_cache;
-    a.v_cache_w = v_cache;
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
-    a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
-    a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
-    a.pieces = reinterpret_cast<int *>(ws + lay.pieces_off);
-    a.seq_tok0 = reinterpret_cast<int *>(ws + tok0_off);
-    a.max_parts = (int)(balanced_slots(max_seq_len) + prefix_slots(max_seq_len) + 1);
-    a.prefix_slot = (int)balanced_slots(max_seq_len);
-    a.prefix_part = kPrefixPart;
-
-    // shared prefixes: tensor-core kernel (groups scanned in shared memory),
-    // else one CTA per (group, kv head, 256 tokens) on mma.sync;
-    // PKV_PREFIX_VARIANT=1 selects the latter for comparisons
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool use_tc = num_groups <= tc::kMaxGroups;
-    pkv_status rc;
-    if (use_tc) {
-        a.prefix_pieces = reinterpret_cast<int *>(ws + npre_off);
-        rc = head_dim == 128 ? launch_prefix_tc<128>(a, group_offsets, prefix_lens, num_groups, st)
-                             : launch_prefix_tc<64>(a, group_offsets, prefix_lens, num_groups, st);
-    } else {
-        rc = head_dim == 128 ? launch_prefix<128>(a, group_offsets, prefix_lens, num_groups, st)
-                             : launch_prefix<64>(a, group_offsets, prefix_lens, num_groups, st);
-    }
-    if (rc == PKV_OK) rc = head_dim == 128 ? dispatch_balanced<128>(a, st) : dispatch_balanced<64>(a, st);
-    if (rc == PKV_OK)
-        rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, true>(a, st)
-                             : launch_reduce<__nv_bfloat16, 64, true, true>(a, st);
-    return rc;
 }
 
 // ---------------------------------------------------------------------------

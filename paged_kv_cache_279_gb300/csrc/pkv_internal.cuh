@@ -1,8 +1,15 @@
 // Internal helpers shared by the library's CUDA translation units.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <unistd.h>
+
+#include <atomic>
+#include <chrono>
+#include <mutex>
 
 #include "pkv.h"
 
@@ -19,6 +26,131 @@ inline pkv_status launch_status() {
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// A 64-bit tag per balanced call, never 0 (the value of a cleared flag): flags
+// left by other calls, or never written, hold another value.  The sequence
+// starts at a value drawn from the clock, the process and an address, so
+// separate processes start far apart.
+inline unsigned long long next_call_tag() {
+    static std::atomic<unsigned long long> count{0};
+    static const unsigned long long base = [] {
+        unsigned long long x = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+        x ^= (unsigned long long)getpid() * 0x9E3779B97F4A7C15ull;
+        x ^= (unsigned long long)reinterpret_cast<uintptr_t>(&count);
+        x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+        x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+        return x ^ (x >> 31);
+    }();
+    unsigned long long t;
+    do {
+        t = base + count.fetch_add(1, std::memory_order_relaxed);
+    } while (t == 0);
+    return t;
+}
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a bf16 cache: rows = num_blocks * Hkv * B, columns = head_dim.
+// Box = 64 columns (128 bytes, 128-byte swizzle) x min(B, 16) rows.
+inline bool make_cache_map(CUtensorMap *map, const void *base, int64_t rows, int D, int boxh) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)boxh};
+    cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Opt a kernel in to the dynamic shared memory it may need (once per device).
+template <typename K>
+inline bool ensure_smem(K kernel, int bytes, bool (&done)[128]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+            return false;
+        done[dev] = true;
+    }
+    return true;
+}
+
+inline int sm_count() {
+    static int counts[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream drains; it waits (griddepcontrol.wait)
+// before touching memory, so stream order is preserved.
+// With `cooperative`, the launch also asks for every CTA of the grid to be
+// resident at once (cudaLaunchAttributeCooperative): a grid that cannot be is
+// refused at launch (PKV_ERR_CUDA) instead of running in waves.  Kernels whose
+// CTAs wait on one another (the in-kernel merges) rely on that.
+template <typename... KArgs, typename... Args>
+inline pkv_status launch_pdl_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                bool cooperative, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cooperative ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? launch_status() : PKV_ERR_CUDA;
+}
+
+template <typename... KArgs, typename... Args>
+inline pkv_status launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+    return launch_pdl_ex(kern, grid, block, smem, st, false, args...);
+}
+
+// Cooperative launch without programmatic serialization.
+template <typename... KArgs, typename... Args>
+inline pkv_status launch_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? launch_status() : PKV_ERR_CUDA;
+}
+
 
 __device__ __forceinline__ void flag_error(unsigned int *err, unsigned int bits) {
     if (err) atomicOr(err, bits);

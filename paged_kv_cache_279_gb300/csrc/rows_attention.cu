@@ -1,0 +1,1217 @@
+// Attention of many query rows against the same paged K/V tiles on the
+// 5th-generation tensor cores (tcgen05): the kernel behind
+//   * paged_attention_decode_grouped -- beams (or parallel samples) that share
+//     the blocks of a prompt prefix ("PagedAttention (vLLM) -- Virtual memory
+//     cho AI", section "Copy-on-Write cho Beam Search": branches share the
+//     physical blocks of their prefix);
+//   * paged_attention_multi_token -- several new tokens of one sequence
+//     attending causally over its paged context: chunked prefill and the
+//     verification of drafted tokens ("vLLM PagedAttention: Buoc dot pha ...",
+//     list of advanced features: "Chunked Prefill", "speculative decoding").
+//
+// Per KV head the work is a dense contraction: up to 128 query rows (the
+// query heads of that KV head for every member of a group, or for every query
+// token of a block of queries) against the same 64-token K and V tiles:
+//     S = Q K^T (M = 128 rows, N = 64 keys, K = head_dim),
+//     O += P V   (M = 128 rows, N = head_dim, K = 64 keys),
+// with an online softmax per row in between.  A "context" is one such set of
+// rows for one KV head and the tiles it attends:
+//   * grouped: the group's prefix tiles (seen by every row), then each
+//     member's own tiles (seen only by that member's rows; the others get
+//     zero weight) -- so one context yields every member's final result, with
+//     no separate merge of prefix and own parts;
+//   * multi-token: the tiles up to the block's last query position; row r
+//     sees the keys at or before its own position.
+// All contexts' tiles are laid end to end and every CTA (one per SM,
+// persistent) takes an equal contiguous share.  A context cut by share
+// boundaries is merged inside the kernel: every later piece is the first
+// piece of its CTA's share, whose CTA stores a partial (o, m, l) per row in
+// its own slot and raises its flag; the CTA holding the context's first tile
+// (its share's last piece) waits for those flags and merges.  Every CTA is
+// resident at once (cooperative launch), and a CTA never waits for a piece
+// later in its own share, so no chain of waits can close.
+//
+// Warp roles (224 threads):
+//   warps 0-3  softmax: thread r owns query row r = TMEM lane r.  Reads S
+//              from TMEM, keeps the row's running max and sum, writes P (bf16)
+//              back into the S columns (P is the A operand of P V, taken from
+//              tensor memory), zeroes the V rows of keys past a context's end,
+//              loads the next piece's queries, and writes the piece's result.
+//   warp 4     producer: walks the share, publishes one descriptor per piece,
+//              stages block ids in shared memory (many loads in flight) and
+//              issues the K/V TMA boxes (one block per box) into an NS-stage
+//              ring, with each tile's key range in a per-stage record.
+//   warp 5     MMA: allocates tensor memory; one thread issues Q K^T and P V,
+//              each as soon as its inputs are ready (a late tile does not hold
+//              up the P V of the one before).
+//   warp 6     grouped: checks that every member's block table holds the
+//              leader's blocks over the prefix.
+// Every wait is bounded; on a timeout the kernel flags PKV_DEVERR_TIMEOUT,
+// waits (bounded) for its own copies in flight, frees its tensor memory and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+
+#include "pkv_internal.cuh"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+namespace rows {
+
+constexpr int kTok = 64;          // keys per tile
+constexpr int kRows = tc::kRows;  // query rows per context (the MMA's M)
+constexpr int kThreads = 224;
+constexpr int kMaxUnits = 2048;   // groups / sequences scanned per launch
+constexpr int kMinTiles = 4;      // shares hold >= 4 tiles unless the total is small
+constexpr int kIdCache = 512;     // block ids staged by the producer
+constexpr int kDescs = 8;         // piece descriptors in flight
+constexpr float kRescale = 8.f;   // headroom (log2 units) before a row's running max moves
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxCtas = 256;     // partial slots in the workspace: one per CTA
+
+enum { kGrouped = 0, kMulti = 1 };
+enum { kWhole = 1, kContinue = 2, kMerger = 4 };
+
+struct Args {
+    void *out;
+    const void *q;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    int num_heads, num_kv_heads, group, block_size, max_blocks, num_blocks, max_seq_len;
+    float scale_log2;
+    unsigned int *err;
+    float *part_o;                // [kMaxCtas][kRows][D]
+    float *part_ml;               // [kMaxCtas][kRows][2]
+    unsigned long long *flags;    // [kMaxCtas]
+    unsigned long long tag;
+    int mode;
+    int unit0, num_units;         // this launch: groups / sequences unit0 .. unit0 + num_units - 1
+    int per_ctx;                  // members (grouped) or queries (multi-token) per context: kRows / group
+    // grouped
+    const int32_t *group_offsets;
+    const int32_t *prefix_lens;
+    int num_seqs, num_groups, appended;
+    // multi-token
+    const int32_t *q_starts;
+    int num_q_tokens, max_q_len;
+};
+
+// One piece of a context: what the MMA and softmax warps need.
+struct Piece {
+    int ntiles;    // 0: no more pieces
+    int row_base;  // first member (grouped) / first query row of q and out (multi-token)
+    int rows;      // live rows
+    int kvh;
+    int pos0;      // multi-token: position of the first query of the block
+    int kind;      // kWhole, kContinue or kMerger
+    int w0, w1;    // CTAs holding the context's first and last tiles
+};
+
+// Per ring stage: the keys of the tile in it.
+struct TileInfo {
+    int member;    // grouped own tile: member index within the context (rows member*G ..); -1 = every row
+    int nvalid;    // keys 0 .. nvalid-1 of the tile exist
+    uint32_t bad;  // bit j: block j of the tile had an invalid id (its keys are masked)
+    int key0;      // position of the tile's first key
+};
+
+template <int D>
+struct Layout {
+    static constexpr int H = D / 64;                      // 128-byte column halves
+    static constexpr int kQBytes = H * kRows * 128;      // [half][row][128 B]
+    static constexpr int kKVBytes = H * kTok * 128;      // K (or V) of a tile: [half][token][128 B]
+    static constexpr int kStageBytes = 2 * kKVBytes;
+    static constexpr int NS = D == 128 ? 5 : 10;         // 160 KB of tiles in flight
+    static constexpr int q = 0;
+    static constexpr int ring = q + kQBytes;
+    static constexpr int cum = ring + NS * kStageBytes;  // int [kMaxUnits + 1]
+    static constexpr int uval = cum + (kMaxUnits + 4) * 4;  // int [kMaxUnits]: prefix tokens / query count
+    static constexpr int ids = uval + kMaxUnits * 4;     // int [kIdCache]
+    static constexpr int mo = ids + kIdCache * 4;        // int [kRows + 4]: members' first own tile
+    static constexpr int tinfo = mo + (kRows + 4) * 4;   // TileInfo [NS]
+    static constexpr int desc = tinfo + NS * 16;         // Piece [kDescs]
+    static constexpr int bars = desc + kDescs * 32;
+    static constexpr int kBars = 2 * NS + 8 + 2 * kDescs;
+    static constexpr int misc = bars + kBars * 8;        // TMEM address, scan scratch, counters
+    static constexpr int total = misc + 128 + 1024;      // + alignment slack
+    static_assert(sizeof(Piece) == 32 && sizeof(TileInfo) == 16, "descriptor sizes");
+};
+
+__device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
+
+__device__ __forceinline__ void st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Units and contexts.  A unit is a group (grouped) or a sequence (multi-
+// token).  Its contexts are ordered KV head first, then sub-context: the
+// group's member chunks (per_ctx members each) or the sequence's query blocks
+// (per_ctx queries each), so that contexts reading the same K/V are adjacent.
+// ---------------------------------------------------------------------------
+struct Unit {
+    int m0, m1;  // grouped: members; multi-token: query rows q0 .. q0 + Q
+    int pre;     // grouped: prefix tokens attended by every member (a multiple of 64)
+    int Q, L;    // multi-token: queries and context length
+    int nsub;    // member chunks / query blocks
+};
+
+__device__ __forceinline__ Unit load_unit(const Args &a, const int *uval, int u) {
+    Unit x{};
+    const int cap = min(a.max_seq_len, a.max_blocks * a.block_size);
+    const int gu = a.unit0 + u;
+    if (a.mode == kGrouped) {
+        int m0 = a.group_offsets[gu], m1 = a.group_offsets[gu + 1];
+        if (m0 < 0 || m1 > a.num_seqs || m1 < m0) m0 = m1 = 0;  // flagged by the scan
+        x.m0 = m0;
+        x.m1 = m1;
+        x.pre = uval[u];
+        x.nsub = (m1 - m0 + a.per_ctx - 1) / a.per_ctx;
+    } else {
+        int q0 = a.q_starts[gu], q1 = a.q_starts[gu + 1];
+        if (q0 < 0 || q1 < q0 || q1 > a.num_q_tokens) q0 = q1 = 0;  // flagged by the scan
+        x.m0 = q0;
+        x.Q = uval[u];
+        x.m1 = q0 + x.Q;
+        x.L = clamp_len(a.seq_lens[gu], cap);
+        x.nsub = (x.Q + a.per_ctx - 1) / a.per_ctx;
+    }
+    return x;
+}
+
+__device__ __forceinline__ int own_tiles(const Args &a, int seq, int pre, int cap) {
+    const int len = clamp_len(a.seq_lens[seq], cap);
+    return len > pre ? (len - pre + kTok - 1) / kTok : 0;
+}
+
+// Last query position of query block b (-1 if it sees no key).
+__device__ __forceinline__ int block_last_pos(const Unit &x, int b, int per_ctx) {
+    return x.L - x.Q + min(x.Q, (b + 1) * per_ctx) - 1;
+}
+
+// Tiles of sub-context `sub` of a unit (for any one KV head).  per_kvh = the
+// unit's tiles per KV head, which is the answer when there is one sub-context.
+__device__ __forceinline__ int sub_tiles(const Args &a, const Unit &x, int sub, int per_kvh, int cap) {
+    if (x.nsub == 1) return per_kvh;
+    if (a.mode == kGrouped) {
+        int n = x.pre / kTok;
+        const int c0 = x.m0 + sub * a.per_ctx, c1 = min(x.m1, c0 + a.per_ctx);
+        for (int m = c0; m < c1; ++m) n += own_tiles(a, m, x.pre, cap);
+        return n;
+    }
+    const int p = block_last_pos(x, sub, a.per_ctx);
+    return p < 0 ? 0 : (p + kTok) / kTok;
+}
+
+// Position in the tile list: context (unit u, kv head, sub-context) with n
+// tiles starting at global tile `start`.
+struct Ctx {
+    int u, kvh, sub, n;
+    int64_t start;
+    int per_kvh;
+    Unit x;
+
+    __device__ __forceinline__ bool seek(const Args &a, const int *cum, const int *uval, int64_t t, int cap) {
+        int lo = 0, hi = a.num_units;  // largest u with cum[u] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cum[mid] <= t) lo = mid; else hi = mid;
+        }
+        u = lo;
+        x = load_unit(a, uval, u);
+        per_kvh = (cum[u + 1] - cum[u]) / a.num_kv_heads;
+        const int64_t local = t - cum[u];
+        kvh = (int)(local / per_kvh);
+        int64_t rem = local - (int64_t)kvh * per_kvh;
+        start = cum[u] + (int64_t)kvh * per_kvh;
+        for (sub = 0; sub < x.nsub; ++sub) {
+            n = sub_tiles(a, x, sub, per_kvh, cap);
+            if (rem < n) return true;
+            rem -= n;
+            start += n;
+        }
+        return false;  // the scan and the walk disagree: never expected
+    }
+
+    // Next context with at least one tile; false past the launch's last unit.
+    __device__ __forceinline__ bool next(const Args &a, const int *cum, const int *uval, int cap) {
+        start += n;
+        for (;;) {
+            if (++sub >= x.nsub) {
+                sub = 0;
+                if (++kvh == a.num_kv_heads) {
+                    kvh = 0;
+                    do { ++u; } while (u < a.num_units && cum[u + 1] == cum[u]);
+                    if (u >= a.num_units) return false;
+                    x = load_unit(a, uval, u);
+                    per_kvh = (cum[u + 1] - cum[u]) / a.num_kv_heads;
+                }
+            }
+            n = sub_tiles(a, x, sub, per_kvh, cap);
+            if (n > 0) return true;
+        }
+    }
+
+    // Rows of the context: first row of q / out and live rows.
+    __device__ __forceinline__ void rows(const Args &a, int &row_base, int &nrows, int &pos0) const {
+        if (a.mode == kGrouped) {
+            row_base = x.m0 + sub * a.per_ctx;
+            nrows = (min(x.m1, row_base + a.per_ctx) - row_base) * a.group;
+            pos0 = 0;
+        } else {
+            row_base = x.m0 + sub * a.per_ctx;
+            nrows = (min(x.Q, (sub + 1) * a.per_ctx) - sub * a.per_ctx) * a.group;
+            pos0 = x.L - x.Q + sub * a.per_ctx;
+        }
+    }
+};
+
+// Keys of tile i of a context: table row (sequence), first key, valid keys,
+// member.  mo[k] = first own tile (relative to the context) of chunk member
+// k, k = 0 .. members (grouped contexts only).
+struct TileKeys {
+    int seq, key0, nvalid, member;
+};
+
+__device__ __forceinline__ TileKeys tile_keys(const Args &a, const Ctx &c, const int *mo, int members, int i,
+                                              int cap) {
+    TileKeys k;
+    if (a.mode == kGrouped) {
+        const int npt = c.x.pre / kTok;
+        const int c0 = c.x.m0 + c.sub * a.per_ctx;
+        if (i < npt) {
+            k.seq = c.x.m0;  // the leader's blocks
+            k.key0 = i * kTok;
+            k.nvalid = kTok;
+            k.member = -1;
+        } else {
+            int lo = 0, hi = members;  // largest member with mo[m] <= i - npt
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (mo[mid] <= i - npt) lo = mid; else hi = mid;
+            }
+            k.member = lo;
+            k.seq = c0 + lo;
+            k.key0 = c.x.pre + (i - npt - mo[lo]) * kTok;
+            k.nvalid = min(kTok, clamp_len(a.seq_lens[k.seq], cap) - k.key0);
+        }
+    } else {
+        k.seq = a.unit0 + c.u;
+        k.key0 = i * kTok;
+        k.nvalid = min(kTok, block_last_pos(c.x, c.sub, a.per_ctx) + 1 - k.key0);
+        k.member = -1;
+    }
+    return k;
+}
+
+// Bounded wait helper: returns false (and flags) once the wait gives up.
+__device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, bool &dead, unsigned int *err) {
+    if (dead) return false;
+    if (!mbar_wait_bounded(bar, parity)) {
+        flag_error(err, PKV_DEVERR_TIMEOUT);
+        dead = true;
+        return false;
+    }
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const Args a) {
+    using L = Layout<D>;
+    constexpr int H = L::H;
+    constexpr int NS = L::NS;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    int *cum = reinterpret_cast<int *>(smem + L::cum);
+    int *uval = reinterpret_cast<int *>(smem + L::uval);
+    int *ids = reinterpret_cast<int *>(smem + L::ids);
+    int *mo = reinterpret_cast<int *>(smem + L::mo);
+    TileInfo *tinfo = reinterpret_cast<TileInfo *>(smem + L::tinfo);
+    Piece *descs = reinterpret_cast<Piece *>(smem + L::desc);
+    uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + L::bars);
+    uint64_t *kv_empty = kv_full + NS;
+    uint64_t *s_full = kv_empty + NS;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2;
+    uint64_t *ready = o_done + 2;
+    uint64_t *fin = ready + 1;
+    uint64_t *desc_full = fin + 1;
+    uint64_t *desc_empty = desc_full + kDescs;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
+    int *warp_sums = reinterpret_cast<int *>(smem + L::misc + 16);  // [8] + carry
+    int *counters = reinterpret_cast<int *>(smem + L::misc + 64);   // partial-store / merge warp counters
+    constexpr int kCarry = 7;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = a.num_kv_heads, G = a.group, B = a.block_size;
+    const int cap = min(a.max_seq_len, a.max_blocks * B);
+
+    // The prologue reads only this call's inputs (lengths, tables, groups),
+    // which no kernel of this library writes; the cache, the queries' rows
+    // copied later, the workspace and the outputs are touched after the wait.
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    if (threadIdx.x == 0) {
+        cum[0] = 0;
+        warp_sums[kCarry] = 0;
+        counters[0] = counters[1] = 0;
+    }
+    __syncthreads();
+
+    // ---- scan: tiles of every unit (all its contexts, all KV heads) ----
+    for (int base = 0; base < a.num_units; base += kThreads) {
+        const int u = base + threadIdx.x;
+        int v = 0;
+        if (u < a.num_units) {
+            const int gu = a.unit0 + u;
+            if (a.mode == kGrouped) {
+                int m0 = a.group_offsets[gu], m1 = a.group_offsets[gu + 1];
+                if (m0 < 0 || m1 > a.num_seqs || m1 < m0) {
+                    if (blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+                    m0 = m1 = 0;
+                }
+                if (blockIdx.x == 0 && (gu == 0 && m0 != 0 || gu + 1 == a.num_groups && m1 != a.num_seqs))
+                    flag_error(a.err, PKV_DEVERR_PREFIX);
+                const int raw = a.prefix_lens[gu];
+                const int align = B > 16 ? B : 16;
+                if (blockIdx.x == 0 && (raw < 0 || raw % align != 0)) flag_error(a.err, PKV_DEVERR_PREFIX);
+                int mn = cap;
+                for (int m = m0; m < m1; ++m) {
+                    const int raw_len = a.seq_lens[m];
+                    if (blockIdx.x == 0 && (raw_len < 0 || raw_len > cap)) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+                    mn = min(mn, clamp_len(raw_len, cap));
+                }
+                // with an append, every member's new token stays in its own part
+                int pre = min(raw < 0 ? 0 : raw, mn - (a.appended ? 1 : 0));
+                pre = m1 > m0 && pre > 0 ? pre / kTok * kTok : 0;
+                uval[u] = pre;
+                int own = 0;
+                for (int m = m0; m < m1; ++m) own += own_tiles(a, m, pre, cap);
+                const int nch = (m1 - m0 + a.per_ctx - 1) / a.per_ctx;
+                v = Hkv * (nch * (pre / kTok) + own);
+            } else {
+                int q0 = a.q_starts[gu], q1 = a.q_starts[gu + 1];
+                if (q0 < 0 || q1 < q0 || q1 > a.num_q_tokens) {
+                    if (blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+                    q0 = q1 = 0;
+                }
+                const int raw_len = a.seq_lens[gu];
+                const int Lq = clamp_len(raw_len, cap);
+                if (blockIdx.x == 0 && ((raw_len < 0 || raw_len > cap) || q1 - q0 > a.max_q_len || q1 - q0 > Lq))
+                    flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+                const int Q = min(q1 - q0, a.max_q_len);  // queries past max_q_len are not attended
+                uval[u] = Q;
+                Unit x{};
+                x.Q = Q;
+                x.L = Lq;
+                const int nb = (Q + a.per_ctx - 1) / a.per_ctx;
+                int t = 0;
+                for (int b = 0; b < nb; ++b) {
+                    const int p = block_last_pos(x, b, a.per_ctx);
+                    t += p < 0 ? 0 : (p + kTok) / kTok;
+                }
+                v = Hkv * t;
+            }
+        }
+        int x = v;  // inclusive warp scan
+#pragma unroll
+        for (int sh = 1; sh < 32; sh <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, sh);
+            if (lane >= sh) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        int before = warp_sums[kCarry];
+        for (int w = 0; w < warp; ++w) before += warp_sums[w];
+        if (u < a.num_units) cum[u + 1] = before + x;
+        __syncthreads();
+        if (threadIdx.x == kThreads - 1) warp_sums[kCarry] = before + x;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) cum[a.num_units + 1] = cum[a.num_units] + 1;  // sentinel past the last unit
+    __syncthreads();
+    const int64_t T = cum[a.num_units];
+
+    // ---- rows whose context has no tile: zero output (CTA c takes units c, c + grid, ...) ----
+    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+        const Unit x = load_unit(a, uval, u);
+        const int per_kvh = (cum[u + 1] - cum[u]) / Hkv;
+        for (int sub = 0; sub < x.nsub; ++sub) {
+            if (sub_tiles(a, x, sub, per_kvh, cap) > 0) continue;
+            const int r0 = x.m0 + sub * a.per_ctx;
+            const int r1 = a.mode == kGrouped ? min(x.m1, r0 + a.per_ctx) : x.m0 + min(x.Q, (sub + 1) * a.per_ctx);
+            const int per_row = a.num_heads * D / 8;  // 16-byte chunks of one row of out
+            for (int i = threadIdx.x; i < (r1 - r0) * per_row; i += kThreads)
+                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + (int64_t)r0 * a.num_heads * D)[i] =
+                    make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+    const int64_t parts = min((int64_t)gridDim.x, max((int64_t)1, T / kMinTiles));
+    if (T == 0 || blockIdx.x >= parts) return;  // before any tensor memory is taken
+    const int w_me = blockIdx.x;
+    const int64_t s0 = (int64_t)w_me * T / parts, s1 = ((int64_t)w_me + 1) * T / parts;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&kv_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(ready, 4);
+        mbar_init(fin, 1);
+        for (int i = 0; i < kDescs; ++i) {
+            mbar_init(&desc_full[i], 1);
+            mbar_init(&desc_empty[i], 5);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t q_s = smem_u32(smem + L::q);
+    const uint32_t ring_s = smem_u32(smem + L::ring);
+
+    if (warp == 4) {
+        // ======================= producer =======================
+        Ctx c;
+        bool dead = !c.seek(a, cum, uval, s0, cap);
+        if (dead && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+        int64_t j = 0;  // tiles issued
+        int p = 0;      // pieces published
+        const int bpt = kTok / B;  // blocks per tile
+        for (int64_t t = s0; t < s1 && !dead;) {
+            const int64_t ce = c.start + c.n;
+            const int i0 = (int)(t - c.start), i1 = (int)(min(s1, ce) - c.start);
+            int row_base, nrows, pos0;
+            c.rows(a, row_base, nrows, pos0);
+            // members' first own tiles (grouped): mo[k], k = 0 .. members
+            int members = 0;
+            if (a.mode == kGrouped) {
+                const int c0 = row_base, c1 = min(c.x.m1, c0 + a.per_ctx);
+                members = c1 - c0;
+                __syncwarp();
+                for (int k0 = 0; k0 < members; k0 += 32) {
+                    const int k = k0 + lane;
+                    int v = k < members ? own_tiles(a, c0 + k, c.x.pre, cap) : 0;
+                    int x = v;
+#pragma unroll
+                    for (int sh = 1; sh < 32; sh <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, x, sh);
+                        if (lane >= sh) x += y;
+                    }
+                    const int carry = k0 == 0 ? 0 : mo[k0];
+                    if (k < members) mo[k + 1] = carry + x;
+                    if (k0 == 0 && lane == 0) mo[0] = 0;
+                    __syncwarp();
+                }
+                __syncwarp();
+            }
+            // publish the piece
+            if (lane == 0) {
+                const int d = p % kDescs;
+                if (p >= kDescs) wait_or_flag(&desc_empty[d], (uint32_t)(((p / kDescs) - 1) & 1), dead, a.err);
+                Piece pc;
+                pc.ntiles = i1 - i0;
+                pc.row_base = row_base;
+                pc.rows = nrows;
+                pc.kvh = c.kvh;
+                pc.pos0 = pos0;
+                const bool first_here = c.start >= s0, last_here = ce <= s1;
+                pc.kind = first_here ? (last_here ? kWhole : kMerger) : kContinue;
+                pc.w0 = (int)share_owner(c.start, T, parts);
+                pc.w1 = (int)share_owner(ce - 1, T, parts);
+                descs[d] = pc;
+                mbar_arrive(&desc_full[d]);
+            }
+            dead = __shfl_sync(0xffffffffu, dead, 0);
+            ++p;
+            // tiles of the piece, in chunks of staged block ids
+            for (int k0 = i0; k0 < i1 && !dead; k0 += kIdCache / bpt) {
+                const int k1 = min(i1, k0 + kIdCache / bpt);
+                __syncwarp();
+                for (int e = lane; e < (k1 - k0) * bpt; e += 32) {
+                    const int i = k0 + e / bpt, jb = e % bpt;
+                    const TileKeys tk = tile_keys(a, c, mo, members, i, cap);
+                    const int lb = tk.key0 / B + jb;
+                    ids[e] = jb * B < tk.nvalid ? a.block_tables[(int64_t)tk.seq * a.max_blocks + lb] : INT_MIN;
+                }
+                __syncwarp();
+                for (int i = k0; i < k1; ++i, ++j) {
+                    const int st = (int)(j % NS);
+                    if (lane == 0 && j >= NS) wait_or_flag(&kv_empty[st], (uint32_t)(((j / NS) - 1) & 1), dead, a.err);
+                    dead = __shfl_sync(0xffffffffu, dead, 0);
+                    if (dead) break;
+                    const TileKeys tk = tile_keys(a, c, mo, members, i, cap);
+                    const int nblk = (tk.nvalid + B - 1) / B;
+                    // lane jb < nblk checks block jb's id (an invalid id is read as block 0, its keys masked)
+                    bool bad = false;
+                    if (lane < nblk) {
+                        const int id = ids[(i - k0) * bpt + lane];
+                        bad = id < 0 || id >= a.num_blocks;
+                    }
+                    const uint32_t badm = __ballot_sync(0xffffffffu, bad);
+                    if (lane == 0) {
+                        if (badm) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
+                        TileInfo ti;
+                        ti.member = tk.member;
+                        ti.nvalid = tk.nvalid;
+                        ti.bad = badm;
+                        ti.key0 = tk.key0;
+                        tinfo[st] = ti;
+                        mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(nblk * 2 * H * B * 128));
+                    }
+                    __syncwarp();
+                    // boxes: (block jb, half h, K or V) -> one lane each
+                    for (int bi = lane; bi < nblk * 2 * H; bi += 32) {
+                        const int jb = bi / (2 * H), h = (bi >> 1) % H, isv = bi & 1;
+                        const int id = ids[(i - k0) * bpt + jb];
+                        const int b2 = (id < 0 || id >= a.num_blocks) ? 0 : id;
+                        const int y = (int)(((int64_t)b2 * Hkv + c.kvh) * B);
+                        const uint32_t dst =
+                            ring_s + st * L::kStageBytes + isv * L::kKVBytes + h * (kTok * 128) + jb * B * 128;
+                        tma_load_2d(dst, isv ? &tm_v : &tm_k, smem_u32(&kv_full[st]), h * 64, y);
+                    }
+                }
+            }
+            t = min(s1, ce);
+            if (t < s1 && !c.next(a, cum, uval, cap)) {
+                if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                dead = true;
+            }
+        }
+        // end of the share: a descriptor with no tiles
+        if (lane == 0 && !dead) {
+            const int d = p % kDescs;
+            if (p >= kDescs) wait_or_flag(&desc_empty[d], (uint32_t)(((p / kDescs) - 1) & 1), dead, a.err);
+            Piece pc{};
+            pc.ntiles = 0;
+            descs[d] = pc;
+            mbar_arrive(&desc_full[d]);
+        }
+        // copies still in flight (only after a timeout) land before the CTA exits
+        if (lane == 0 && dead)
+            for (int64_t k = max((int64_t)0, j - NS); k < j; ++k)
+                mbar_wait_bounded(&kv_full[k % NS], (uint32_t)((k / NS) & 1));
+    } else if (warp == 5) {
+        // ======================= MMA issuer =======================
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = tc::instr_desc(kTok, false);
+            constexpr uint32_t idesc_pv = tc::instr_desc(D, true);
+            int64_t jq = 0, jp = 0;       // next Q K^T / P V tile
+            int pq = 0, pp = 0;           // their pieces
+            int tq = 0, tp = 0;           // tile within those pieces
+            int ntq = -1;                 // tiles of piece pq (-1: descriptor not read yet)
+            int nt_ring[4] = {0, 0, 0, 0};
+            bool done_q = false, dead = false;
+            uint32_t idle = 0;
+            for (;;) {
+                bool prog = false;
+                if (jp < jq) {
+                    if (mbar_test_wait(&p_full[jp & 1], (uint32_t)((jp >> 1) & 1))) {
+                        tc::fence_after();
+                        const uint32_t ob = 128u + (uint32_t)(pp & 1) * D;
+                        const uint32_t pa = tmem + (uint32_t)(jp & 1) * kTok;  // P in the S columns
+                        const uint32_t vb = ring_s + (uint32_t)(jp % NS) * L::kStageBytes + L::kKVBytes;
+#pragma unroll
+                        for (int k = 0; k < kTok / 16; ++k)
+                            tc::mma_ts(tmem + ob, pa + 8 * k, tc::smem_desc(vb + k * 2048, kTok * 128, 1024), idesc_pv,
+                                       (tp == 0 && k == 0) ? 0u : 1u);
+                        tc::commit(&o_done[jp & 1]);
+                        tc::commit(&kv_empty[jp % NS]);
+                        ++jp;
+                        if (++tp == nt_ring[pp & 3]) {
+                            mbar_arrive(&desc_empty[pp % kDescs]);
+                            ++pp;
+                            tp = 0;
+                        }
+                        prog = true;
+                    }
+                } else if (done_q) {
+                    break;
+                }
+                if (!done_q && jq < jp + 2) {
+                    if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
+                        ntq = descs[pq % kDescs].ntiles;
+                        if (ntq == 0) {
+                            done_q = true;
+                        } else {
+                            nt_ring[pq & 3] = ntq;
+                        }
+                        prog = true;
+                    }
+                    if (ntq > 0 && mbar_test_wait(&kv_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
+                        (tq > 0 || mbar_test_wait(ready, (uint32_t)(pq & 1)))) {
+                        tc::fence_after();
+                        const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k)
+                            tc::mma(tmem + (uint32_t)(jq & 1) * kTok,
+                                    tc::smem_desc(q_s + (k >> 2) * (kRows * 128) + (k & 3) * 32, 16, 1024),
+                                    tc::smem_desc(kb + (k >> 2) * (kTok * 128) + (k & 3) * 32, 16, 1024), idesc_qk,
+                                    k > 0 ? 1u : 0u);
+                        tc::commit(&s_full[jq & 1]);
+                        ++jq;
+                        if (++tq == ntq) {
+                            ++pq;
+                            tq = 0;
+                            ntq = -1;
+                        }
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    idle = 0;
+                } else if (++idle > kWaitLimit) {
+                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                    dead = true;
+                    break;
+                }
+            }
+            // every MMA has completed before the tensor memory is freed
+            tc::commit(fin);
+            mbar_wait_bounded(fin, 0u);
+            (void)dead;
+        }
+    } else if (warp == 6) {
+        // ======================= members' block tables =======================
+        if (a.mode == kGrouped) {
+            Ctx c;
+            const bool found = c.seek(a, cum, uval, s0, cap);
+            const int bpt = kTok / B;
+            bool bad = false;
+            for (int64_t t = s0; t < s1 && found;) {
+                const int64_t ce = c.start + c.n;
+                const int i0 = (int)(t - c.start), i1 = (int)(min(s1, ce) - c.start);
+                const int npt = c.x.pre / kTok;
+                if (c.kvh == 0 && i0 < npt) {
+                    const int c0 = c.x.m0 + c.sub * a.per_ctx, c1 = min(c.x.m1, c0 + a.per_ctx);
+                    const int lb0 = i0 * bpt, nb = (min(i1, npt) - i0) * bpt;
+                    const int32_t *lead = a.block_tables + (int64_t)c.x.m0 * a.max_blocks;
+                    const int total = (c1 - c0) * nb;
+                    for (int k = lane; k < total; k += 32) {
+                        const int m = c0 + k / nb, lb = lb0 + k % nb;
+                        if (m != c.x.m0 && a.block_tables[(int64_t)m * a.max_blocks + lb] != lead[lb]) bad = true;
+                    }
+                }
+                t = min(s1, ce);
+                if (t < s1 && !c.next(a, cum, uval, cap)) break;
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
+        }
+    } else {
+        // ======================= softmax (warps 0-3) =======================
+        const int r = warp * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        bool dead = false;
+        int64_t j = 0;
+        int p = 0;
+        // row r's queries of a piece into Q (128-byte swizzled, K-major; zero past the live rows)
+        auto copy_q = [&](const Piece &pc) {
+            const bool live = r < pc.rows;
+            const int row = pc.row_base + (live ? r / G : 0), head = pc.kvh * G + r % G;
+            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)row * a.num_heads + head) * D;
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) {
+                const uint32_t dst = q_s + (k >> 3) * (kRows * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
+                if (live)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k * 8) : "memory");
+                else
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        auto q_ready = [&]() {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            fence_proxy_async();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ready);
+        };
+        Piece pc{};
+        if (wait_or_flag(&desc_full[0], 0u, dead, a.err)) pc = descs[0];
+        if (pc.ntiles > 0) {
+            copy_q(pc);
+            q_ready();
+        }
+        while (pc.ntiles > 0 && !dead) {
+            const bool live_warp = warp * 32 < pc.rows;
+            const bool live = r < pc.rows;
+            const int my_member = r / G;
+            const int my_pos = pc.pos0 + r / G;  // multi-token: this row's position
+            float m_run = -INFINITY, l = 0.f;
+            Piece nx{};
+            for (int i = 0; i < pc.ntiles; ++i, ++j) {
+                const int st = (int)(j % NS), b = (int)(j & 1);
+                // the stage's record (ordered by the producer's arrive on kv_full)
+                wait_or_flag(&kv_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
+                const TileInfo ti = tinfo[st];
+                wait_or_flag(&s_full[b], (uint32_t)((j >> 1) & 1), dead, a.err);
+                tc::fence_after();
+                if (dead) break;
+                if (i == pc.ntiles - 1) {
+                    // every Q K^T of this piece has completed: Q may take the next piece's rows
+                    const int d = (p + 1) % kDescs;
+                    if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
+                    if (nx.ntiles > 0) copy_q(nx);
+                }
+                // keys past the context's end or in invalid blocks: zero their V rows
+                // (stale slots may hold NaN; a zero weight must meet a zero)
+                if (ti.nvalid < kTok || ti.bad) {
+                    const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
+                    for (int e = r; e < kTok * H * 8; e += 128) {
+                        const int key = (e / 8) % kTok, h = e / (kTok * 8), chk = e % 8;
+                        const bool zero = key >= ti.nvalid || ((ti.bad >> (key / B)) & 1u);
+                        if (zero)
+                            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vbase + h * (kTok * 128) +
+                                                                                   key * 128 + chk * 16),
+                                         "r"(0u)
+                                         : "memory");
+                    }
+                    fence_proxy_async();
+                }
+                if (live_warp) {
+                    float s[kTok];
+                    tc::ld32(trow + b * kTok, s);
+                    tc::ld32(trow + b * kTok + 32, s + 32);
+                    tc::wait_ld();
+                    // keys this row sees in this tile: [0, lim) minus invalid blocks
+                    int lim = ti.nvalid;
+                    if (!live) lim = 0;
+                    if (ti.member >= 0 && ti.member != my_member) lim = 0;
+                    if (a.mode == kMulti) lim = min(lim, my_pos - ti.key0 + 1);
+                    if (lim < kTok || ti.bad) {
+#pragma unroll
+                        for (int k = 0; k < kTok; ++k)
+                            if (k >= lim || ((ti.bad >> (k / B)) & 1u)) s[k] = -INFINITY;
+                    }
+                    // row max (tree), scaled to the log2 domain
+                    float mx[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+                    for (int k = 16; k < kTok; k += 16)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(s[k + q], s[k + 8 + q]));
+                    float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    mt *= a.scale_log2;
+                    // the running max moves only when the tile's exceeds it by more than 2^8
+                    float m_new = m_run;
+                    bool move = false;
+                    if (mt != -INFINITY) {
+                        if (m_run == -INFINITY) {
+                            m_new = mt;  // nothing accumulated yet: O is zero, nothing to rescale
+                        } else if (mt > m_run + kRescale) {
+                            m_new = mt;
+                            move = true;
+                        }
+                    }
+                    if (__any_sync(0xffffffffu, move)) {
+                        // O must hold P V of the previous tile before it is rescaled
+                        wait_or_flag(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), dead, a.err);
+                        tc::fence_after();
+                        const float alpha = move ? exp2f(m_run - m_new) : 1.f;
+                        const uint32_t ob = 128u + (uint32_t)(p & 1) * D;
+#pragma unroll
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            float o[32];
+                            tc::ld32(trow + ob + cc * 32, o);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                            tc::st32(trow + ob + cc * 32, o);
+                        }
+                        tc::wait_st();
+                        l *= alpha;
+                    }
+                    m_run = m_new;
+                    const float nm = m_run == -INFINITY ? 0.f : -m_run;
+                    uint32_t pk[32];
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        pk[k] = pack_bf16x2(exp2f(fmaf(s[2 * k], a.scale_log2, nm)),
+                                            exp2f(fmaf(s[2 * k + 1], a.scale_log2, nm)));
+                        ls[k & 3] += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
+                    }
+                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                    st32u(trow + b * kTok, pk);  // P over the first 32 S columns
+                    tc::wait_st();
+                }
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
+            }
+            if (dead) break;
+            if (nx.ntiles > 0) q_ready();  // the next piece's Q K^T may start
+            // the piece's result: O (TMEM) with the row's running max and sum
+            wait_or_flag(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), dead, a.err);
+            tc::fence_after();
+            const uint32_t ob = 128u + (uint32_t)(p & 1) * D;
+            const int64_t orow = (int64_t)(pc.row_base + (live ? r / G : 0)) * a.num_heads + pc.kvh * G + r % G;
+            if (pc.kind == kWhole) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D);
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float o[32];
+                    if (live_warp) {
+                        tc::ld32(trow + ob + cc * 32, o);
+                        tc::wait_ld();
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[cc * 4 + k] = make_uint4(pack_bf16x2(o[8 * k] * inv, o[8 * k + 1] * inv),
+                                                         pack_bf16x2(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                                                         pack_bf16x2(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                                                         pack_bf16x2(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+                    }
+                }
+            } else if (pc.kind == kContinue) {
+                // a later piece of a context begun in an earlier share: store the
+                // partial in this CTA's slot; the last warp to finish raises the flag
+                float *po = a.part_o + ((int64_t)w_me * kRows + r) * D;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float o[32];
+                    if (live_warp) {
+                        tc::ld32(trow + ob + cc * 32, o);
+                        tc::wait_ld();
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 4)
+                            *reinterpret_cast<float4 *>(po + cc * 32 + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+                    }
+                }
+                if (live)
+                    *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + r) * 2) = make_float2(m_run, l);
+                fence_acq_rel_gpu();
+                __syncwarp();
+                if (lane == 0) {
+                    fence_acq_rel_gpu();
+                    if (atomicAdd(&counters[0], 1) == 3) {
+                        counters[0] = 0;
+                        fence_acq_rel_gpu();
+                        *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
+                    }
+                }
+            } else {
+                // merger: this piece holds the context's first tile and is the last
+                // piece of this share; CTAs w0 + 1 .. w1 stored the rest
+                const int n = pc.w1 - pc.w0;
+                bool ok = true;
+                {
+                    bool got = false;
+                    for (uint32_t it = 0; it < kWaitLimit && !got; ++it) {
+                        bool mine = true;
+                        for (int k = lane; k < n; k += 32)
+                            mine = mine && ld_volatile_u64(a.flags + pc.w0 + 1 + k) == a.tag;
+                        got = __all_sync(0xffffffffu, mine);
+                        if (!got) __nanosleep(64);
+                    }
+                    ok = got;
+                }
+                if (!ok && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                // each lane saw some flags: acquire, then order every lane's reads after them
+                fence_acq_rel_gpu();
+                __syncwarp();
+                float M = m_run;
+                if (live)
+                    for (int w = pc.w0 + 1; w <= pc.w1; ++w)
+                        M = fmaxf(M, __ldcg(a.part_ml + ((int64_t)w * kRows + r) * 2));
+                const float Mr = M == -INFINITY ? 0.f : M;
+                const float e_own = m_run == -INFINITY ? 0.f : exp2f(m_run - Mr);
+                float Ls = l * e_own;
+                if (live)
+                    for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + r);
+                        if (ml.x != -INFINITY) Ls += ml.y * exp2f(ml.x - Mr);
+                    }
+                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D);
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float o[32];
+                    if (live_warp) {
+                        tc::ld32(trow + ob + cc * 32, o);
+                        tc::wait_ld();
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] *= e_own;
+                        for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + r);
+                            if (ml.x == -INFINITY) continue;
+                            const float e = exp2f(ml.x - Mr);
+                            const float4 *src = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)w * kRows + r) * D + cc * 32);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const float4 v = __ldcg(src + k);
+                                o[4 * k] += e * v.x;
+                                o[4 * k + 1] += e * v.y;
+                                o[4 * k + 2] += e * v.z;
+                                o[4 * k + 3] += e * v.w;
+                            }
+                        }
+                        const float f = ok ? inv : __int_as_float(0x7fc00000);  // NaN rows when a piece never came
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[cc * 4 + k] = make_uint4(pack_bf16x2(o[8 * k] * f, o[8 * k + 1] * f),
+                                                         pack_bf16x2(o[8 * k + 2] * f, o[8 * k + 3] * f),
+                                                         pack_bf16x2(o[8 * k + 4] * f, o[8 * k + 5] * f),
+                                                         pack_bf16x2(o[8 * k + 6] * f, o[8 * k + 7] * f));
+                    }
+                }
+                // the last warp done reading clears the flags (a graph replay reuses the tag)
+                __syncwarp();
+                if (lane == 0 && atomicAdd(&counters[1], 1) == 3) {
+                    counters[1] = 0;
+                    for (int k = 0; k < n; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&desc_empty[p % kDescs]);
+            pc = nx;
+            ++p;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // no query copy outlives the CTA
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct WsLayout {
+    size_t o_off, ml_off, flags_off, total;
+};
+
+static WsLayout ws_layout(int D) {
+    WsLayout w;
+    w.o_off = 0;
+    w.ml_off = round256((size_t)kMaxCtas * kRows * D * 4);
+    w.flags_off = w.ml_off + round256((size_t)kMaxCtas * kRows * 2 * 4);
+    w.total = w.flags_off + round256((size_t)kMaxCtas * 8);
+    return w;
+}
+
+// 2-D view of a bf16 cache with one block per box: rows = num_blocks * Hkv *
+// B, columns = head_dim; box = 64 columns (128 bytes, 128-byte swizzle) x B rows.
+static bool make_maps(const void *k_cache, const void *v_cache, int64_t rows, int D, int B, CUtensorMap *mk,
+                      CUtensorMap *mv) {
+    return make_cache_map(mk, k_cache, rows, D, B) && make_cache_map(mv, v_cache, rows, D, B);
+}
+
+template <int D>
+static pkv_status launch(const Args &a, const void *k_cache, const void *v_cache, cudaStream_t st) {
+    constexpr int smem = Layout<D>::total;
+    static bool done[128] = {};
+    auto kern = rows_attention_kernel<D>;
+    if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
+    CUtensorMap mk, mv;
+    const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
+    if (!make_maps(k_cache, v_cache, rows, D, a.block_size, &mk, &mv)) return PKV_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const int grid = std::min(sms, kMaxCtas);
+    // Cooperative launch (every CTA resident at once: the in-kernel merge waits
+    // on other CTAs) together with programmatic launch where the driver takes
+    // both; the first combination that launches is kept for the process.
+    static std::atomic<int> mode{-1};  // 0: cooperative + programmatic, 1: cooperative only
+    int m = mode.load();
+    if (m < 0) {
+        for (m = 0; m < 2; ++m) {
+            const pkv_status rc = m == 0 ? launch_pdl_ex(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, true, mk, mv, a)
+                                         : launch_coop(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, mk, mv, a);
+            if (rc == PKV_OK) {
+                mode.store(m);
+                return rc;
+            }
+            (void)cudaGetLastError();  // the refused combination's error, before the next attempt
+        }
+        return PKV_ERR_CUDA;
+    }
+    return m == 0 ? launch_pdl_ex(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, true, mk, mv, a)
+                  : launch_coop(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, mk, mv, a);
+}
+
+static pkv_status run(Args a, int D, int total_units, const void *k_cache, const void *v_cache, cudaStream_t st) {
+    for (int u0 = 0; u0 < total_units; u0 += kMaxUnits) {
+        a.unit0 = u0;
+        a.num_units = std::min(kMaxUnits, total_units - u0);
+        a.tag = next_call_tag();
+        const pkv_status rc = D == 128 ? launch<128>(a, k_cache, v_cache, st) : launch<64>(a, k_cache, v_cache, st);
+        if (rc != PKV_OK) return rc;
+    }
+    return PKV_OK;
+}
+
+}  // namespace rows
+
+// The store of each sequence's new token at position seq_lens[s] - 1 (defined
+// with the decode kernels).
+pkv_status append_new_tokens(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_kv_heads,
+                             int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                             int dtype, cudaStream_t st);
+
+}  // namespace pkv
+
+using namespace pkv;
+
+PKV_API size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim, int max_seq_len) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    return rows::ws_layout(head_dim).total;
+}
+
+PKV_API size_t paged_attention_multi_token_workspace_size(int num_q_tokens, int num_heads, int head_dim,
+                                                          int max_seq_len) {
+    if (num_q_tokens <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
+    if (head_dim != 64 && head_dim != 128) return 0;
+    return rows::ws_layout(head_dim).total;
+}
+
+static bool fill_common(rows::Args &a, void *out, const void *q, const int32_t *block_tables, const int32_t *seq_lens,
+                        int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                        int num_blocks, int max_seq_len, float scale, void *workspace, size_t workspace_bytes) {
+    const rows::WsLayout lay = rows::ws_layout(head_dim);
+    if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return false;
+    a.out = out;
+    a.q = q;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.err = device_error_word();
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
+    a.part_ml = reinterpret_cast<float *>(ws + lay.ml_off);
+    a.flags = reinterpret_cast<unsigned long long *>(ws + lay.flags_off);
+    a.per_ctx = rows::kRows / a.group;
+    return true;
+}
+
+PKV_API pkv_status paged_attention_decode_grouped(
+    void *out, const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+    const int32_t *block_tables, const int32_t *seq_lens, const int32_t *group_offsets,
+    const int32_t *prefix_lens, int num_groups, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+    int block_size, int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale, void *workspace,
+    size_t workspace_bytes, int dtype, void *stream) {
+    if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        max_seq_len < 0 || !std::isfinite(scale) || num_groups < 1)
+        return PKV_ERR_INVALID;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
+    if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_seq_len == 0) return PKV_OK;
+    if (num_groups > num_seqs) return PKV_ERR_INVALID;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !group_offsets || !prefix_lens)
+        return PKV_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    if (((int64_t)num_blocks + 1) * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
+    // tile counts of a launch's groups are summed in 32-bit integers
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + rows::kTok - 1) / rows::kTok + 1) > INT32_MAX / 2)
+        return PKV_ERR_UNSUPPORTED;
+    rows::Args a{};
+    if (!fill_common(a, out, q, block_tables, seq_lens, num_heads, num_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_seq_len, scale, workspace, workspace_bytes))
+        return PKV_ERR_INVALID;
+    a.mode = rows::kGrouped;
+    a.group_offsets = group_offsets;
+    a.prefix_lens = prefix_lens;
+    a.num_seqs = num_seqs;
+    a.num_groups = num_groups;
+    a.appended = k_new ? 1 : 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (k_new) {
+        // each member's new token goes to its slot first; the attention reads it from there
+        const pkv_status rc = append_new_tokens(k_new, v_new, k_cache, v_cache, block_tables, seq_lens, num_seqs,
+                                                num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                                                max_seq_len, PKV_BF16, st);
+        if (rc != PKV_OK) return rc;
+    }
+    return rows::run(a, head_dim, num_groups, k_cache, v_cache, st);
+}
+
+PKV_API pkv_status paged_attention_multi_token(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                               const int32_t *block_tables, const int32_t *seq_lens,
+                                               const int32_t *q_starts, int num_seqs, int num_q_tokens,
+                                               int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                               int max_blocks_per_seq, int num_blocks, int max_q_len,
+                                               int max_seq_len, float scale, void *workspace,
+                                               size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_q_tokens < 0 || num_heads < 1 || num_kv_heads < 1 || max_blocks_per_seq < 1 ||
+        num_blocks < 1 || max_seq_len < 0 || max_q_len < 0 || !std::isfinite(scale))
+        return PKV_ERR_INVALID;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_q_tokens == 0) return PKV_OK;
+    if (max_q_len < 1 || max_seq_len < 1) return PKV_ERR_INVALID;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_starts) return PKV_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID;
+    if (((int64_t)num_blocks + 1) * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
+    // tiles of a launch's sequences (every query block of every KV head) in 32-bit integers
+    const int64_t per_seq = ((int64_t)max_q_len * (num_heads / num_kv_heads) + rows::kRows - 1) / rows::kRows *
+                            ((max_seq_len + rows::kTok - 1) / rows::kTok);
+    if (std::min<int64_t>(num_seqs, rows::kMaxUnits) * num_kv_heads * per_seq > INT32_MAX / 2)
+        return PKV_ERR_UNSUPPORTED;
+    rows::Args a{};
+    if (!fill_common(a, out, q, block_tables, seq_lens, num_heads, num_kv_heads, head_dim, block_size,
+                     max_blocks_per_seq, num_blocks, max_seq_len, scale, workspace, workspace_bytes))
+        return PKV_ERR_INVALID;
+    a.mode = rows::kMulti;
+    a.q_starts = q_starts;
+    a.num_q_tokens = num_q_tokens;
+    a.max_q_len = max_q_len;
+    return rows::run(a, head_dim, num_seqs, k_cache, v_cache, static_cast<cudaStream_t>(stream));
+}

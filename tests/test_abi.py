@@ -110,18 +110,21 @@ def test_multi_token_host_validation_and_workspace():
     assert call(S=0) == pkv.PKV_OK and call(T=0) == pkv.PKV_OK
     assert call(maxQ=0) == pkv.PKV_ERR_INVALID
     assert call() == pkv.PKV_ERR_INVALID                 # null pointers
-    # grid.z = query blocks x 1024-token partitions must fit 65535: checked on
-    # the host after the pointers (dummy, 16-byte aligned, never dereferenced:
-    # the call is rejected before any launch)
+    # the tiles of a launch's sequences (every query block of every KV head) are
+    # counted in 32-bit integers: checked on the host after the pointers (dummy,
+    # 16-byte aligned, never dereferenced: the call is rejected before any launch)
     p = ctypes.c_void_p(256)
-    assert f(p, p, p, p, p, p, p, 2, 10, 32, 8, 128, 16, 8, 64, 8 * 4096, 20 * 1024, 0.1, p, 1 << 30,
+    assert f(p, p, p, p, p, p, p, 4000, 10, 32, 8, 128, 16, 8, 64, 32768, 1 << 20, 0.1, p, 1 << 30,
              None) == pkv.PKV_ERR_UNSUPPORTED
     ws = lib.paged_attention_multi_token_workspace_size
-    assert ws(10, 32, 128, 1024) == 0                     # one partition: no scratch
+    # one partial slot per CTA (at most 256): 128 rows of (o, max, sum) fp32 and a
+    # ready flag, whatever the number of query tokens or the context length
     r = lambda x: (x + 255) // 256 * 256
-    n = 10 * 32 * 3                                       # 3 partitions of 1024 for 3000 tokens
-    assert ws(10, 32, 128, 3000) == n * 128 * 4 + 2 * r(n * 4) + r(10 * 4)
-    assert ws(0, 32, 128, 3000) == 0
+    fixed = 256 * 128 * 128 * 4 + r(256 * 128 * 2 * 4) + r(256 * 8)
+    assert ws(10, 32, 128, 1024) == ws(10, 32, 128, 3000) == ws(5000, 8, 128, 100000) == fixed
+    assert ws(10, 32, 64, 3000) == 256 * 128 * 64 * 4 + r(256 * 128 * 2 * 4) + r(256 * 8)
+    assert ws(0, 32, 128, 3000) == 0 and ws(10, 32, 96, 3000) == 0
+    assert lib.paged_attention_grouped_workspace_size(256, 64, 128, 1300) == fixed
 
 
 def test_decode_append_fp8_host_validation():

@@ -119,16 +119,61 @@ def test_grouped_shapes_match_oracle(D, B, Hq, Hkv, prompts, width, shared):
     assert pkv.read_device_errors() == 0
 
 
-def test_grouped_fallback_prefix_kernel_matches_oracle(monkeypatch):
-    # the kernel used past 2048 groups (one CTA per group, kv head and 256 tokens)
-    monkeypatch.setenv("PKV_PREFIX_VARIANT", "1")
-    shape = wl.DecodeShape("beam_fallback", 0, 64, 8, 128, 16, torch.bfloat16)
-    div = np.random.default_rng(5).integers(0, 200, 4 * 8)
-    case = build_beam_pool(shape, 1032, 4, 8, div, seed=19)
+def test_more_groups_than_one_launch_scans():
+    """2100 groups (one launch scans at most 2048): the call runs the groups in
+    two launches over the same workspace."""
+    shape = wl.DecodeShape("beam_many", 0, 8, 2, 64, 16, torch.bfloat16)
+    prompts, width = 2100, 2
+    div = np.random.default_rng(7).integers(0, 21, prompts * width)
+    case = build_beam_pool(shape, 64, prompts, width, div, seed=21)
     offs, pre = case["alloc"].prefix_groups(case["seqs"])
-    q = wl.draw_query(shape, 20, num_seqs=32).cuda()
+    assert len(pre) == prompts and (pre == 64).all()
+    q = wl.draw_query(shape, 22, num_seqs=prompts * width).cuda()
     out = grouped(case, shape, q, offs, pre, int(case["lens"].max()))
     ref = oracle.decode_attention(q.float().cpu().numpy(), [k.float().numpy() for k in case["ks"]],
                                   [v.float().numpy() for v in case["vs"]], shape.scale)
-    assert_bf16_close(out, ref, "grouped, fallback prefix kernel")
+    assert_bf16_close(out, ref, "2100 groups")
+    assert pkv.read_device_errors() == 0
+
+
+def test_grouped_graph_replays_over_a_random_workspace():
+    """Contexts split between CTAs are merged inside the kernel through ready
+    flags carrying the call's tag, cleared by the merging CTA: a CUDA graph
+    replays one call (one tag) several times over a workspace that starts as
+    random bytes, with new queries before each replay."""
+    shape = wl.BEAM_BF16
+    div = wl.draw_divergent_lengths(wl.BEAM_PROMPTS * wl.BEAM_WIDTH, seed=3)
+    case = build_beam_pool(shape, wl.BEAM_SHARED_PARTIAL, wl.BEAM_PROMPTS, wl.BEAM_WIDTH, div, seed=5)
+    offs, pre = case["alloc"].prefix_groups(case["seqs"])
+    S = len(case["seqs"])
+    maxL = int(case["lens"].max())
+    need = pkv.paged_attention_grouped_workspace_size(S, shape.num_heads, shape.head_dim, maxL)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda")
+    tables = torch.from_numpy(case["tables"]).cuda()
+    lens = torch.from_numpy(np.asarray(case["lens"], dtype=np.int32)).cuda()
+    d_offs, d_pre = torch.from_numpy(offs).cuda(), torch.from_numpy(pre).cuda()
+    q = torch.empty((S, shape.num_heads, shape.head_dim), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    qs = [wl.draw_query(shape, 40 + r, num_seqs=S) for r in range(3)]
+
+    def call():
+        pkv.paged_attention_decode_grouped(out, q, case["kc"], case["vc"], tables, lens, d_offs, d_pre,
+                                           shape.scale, maxL, workspace=ws)
+    q.copy_(qs[0].cuda())
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            call()
+    ks = [k.float().numpy() for k in case["ks"]]
+    vs = [v.float().numpy() for v in case["vs"]]
+    for r in range(3):
+        q.copy_(qs[r].cuda())
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle.decode_attention(qs[r].float().numpy(), ks, vs, shape.scale)
+        assert_bf16_close(out, ref, f"grouped replay {r}")
     assert pkv.read_device_errors() == 0

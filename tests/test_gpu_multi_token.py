@@ -119,3 +119,38 @@ def test_workspace_too_small_is_rejected():
                                         torch.tensor([3000], dtype=torch.int32, device="cuda"),
                                         torch.from_numpy(c["starts"]).cuda(), c["shape"].scale, 64, 3000,
                                         workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"))
+
+
+def test_graph_replays_over_a_random_workspace():
+    """Prefill chunks long enough to be split between CTAs, merged inside the
+    kernel: a CUDA graph replays one call several times over a workspace that
+    starts as random bytes, with new queries each time."""
+    c = _case(32, 8, 128, 16, [3000, 2500, 900, 4000], [512, 300, 64, 700], seed=14)
+    dev = "cuda"
+    q = c["q"].to(dev)
+    out = torch.empty_like(q)
+    kc, vc = c["kc"].to(dev), c["vc"].to(dev)
+    tables = torch.from_numpy(c["tables"]).to(dev)
+    lens = torch.tensor(c["lens"], dtype=torch.int32, device=dev)
+    starts = torch.from_numpy(c["starts"]).to(dev)
+    need = pkv.paged_attention_multi_token_workspace_size(q.shape[0], 32, 128, 4000)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device=dev)
+    qs = [wl.draw_normal(tuple(q.shape), torch.bfloat16, 300 + r) for r in range(3)]
+
+    def call():
+        pkv.paged_attention_multi_token(out, q, kc, vc, tables, lens, starts, c["shape"].scale, 700, 4000,
+                                        workspace=ws)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            call()
+    for r in range(3):
+        q.copy_(qs[r].to(dev))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_bf16_close(out.cpu(), _oracle(dict(c, q=qs[r])), f"multi-token replay {r}")
+    assert pkv.read_device_errors() == 0
