@@ -629,7 +629,16 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             int pq = 0, pp = 0;           // their pieces
             int tq = 0, tp = 0;           // tile within those pieces
             int ntq = -1;                 // tiles of piece pq (-1: descriptor not read yet)
-            int nt_ring[4] = {0, 0, 0, 0};
+            // tiles of the pieces between the next P V and the next Q K^T (at most
+            // three: Q K^T runs at most two tiles ahead), in registers
+            int nt0 = 0, nt1 = 0, nt2 = 0, nt3 = 0;
+            auto nt_get = [&](int i) { return i == 0 ? nt0 : (i == 1 ? nt1 : (i == 2 ? nt2 : nt3)); };
+            auto nt_set = [&](int i, int v) {
+                if (i == 0) nt0 = v;
+                else if (i == 1) nt1 = v;
+                else if (i == 2) nt2 = v;
+                else nt3 = v;
+            };
             bool done_q = false, dead = false;
             uint32_t idle = 0;
             for (;;) {
@@ -647,7 +656,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         tc::commit(&o_done[jp & 1]);
                         tc::commit(&kv_empty[jp % NS]);
                         ++jp;
-                        if (++tp == nt_ring[pp & 3]) {
+                        if (++tp == nt_get(pp & 3)) {
                             mbar_arrive(&desc_empty[pp % kDescs]);
                             ++pp;
                             tp = 0;
@@ -663,7 +672,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         if (ntq == 0) {
                             done_q = true;
                         } else {
-                            nt_ring[pq & 3] = ntq;
+                            nt_set(pq & 3, ntq);
                         }
                         prog = true;
                     }
@@ -802,17 +811,21 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     tc::ld32(trow + b * kTok, s);
                     tc::ld32(trow + b * kTok + 32, s + 32);
                     tc::wait_ld();
+                    // scores in the log2 domain
+#pragma unroll
+                    for (int k = 0; k < kTok; ++k) s[k] *= a.scale_log2;
                     // keys this row sees in this tile: [0, lim) minus invalid blocks
                     int lim = ti.nvalid;
                     if (!live) lim = 0;
                     if (ti.member >= 0 && ti.member != my_member) lim = 0;
                     if (a.mode == kMulti) lim = min(lim, my_pos - ti.key0 + 1);
                     if (lim < kTok || ti.bad) {
+                        const int bshift = B == 8 ? 3 : (B == 16 ? 4 : 5);
 #pragma unroll
                         for (int k = 0; k < kTok; ++k)
-                            if (k >= lim || ((ti.bad >> (k / B)) & 1u)) s[k] = -INFINITY;
+                            if (k >= lim || ((ti.bad >> (k >> bshift)) & 1u)) s[k] = -INFINITY;
                     }
-                    // row max (tree), scaled to the log2 domain
+                    // row max (tree)
                     float mx[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
@@ -820,9 +833,8 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     for (int k = 16; k < kTok; k += 16)
 #pragma unroll
                         for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(s[k + q], s[k + 8 + q]));
-                    float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                    mt *= a.scale_log2;
+                    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                     // the running max moves only when the tile's exceeds it by more than 2^8
                     float m_new = m_run;
                     bool move = false;
@@ -834,13 +846,27 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             move = true;
                         }
                     }
+                    // P with the new reference point (S is dead once P is in tensor memory)
+                    const float alpha = move ? ex2_approx(m_run - m_new) : 1.f;
+                    m_run = m_new;
+                    const float nm = m_run == -INFINITY ? 0.f : -m_run;
+                    uint32_t pk[32];
+                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        pk[k] = pack_bf16x2(ex2_approx(s[2 * k] + nm), ex2_approx(s[2 * k + 1] + nm));
+                        ls[k & 3] += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
+                    }
+                    l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+                    st32u(trow + b * kTok, pk);  // P over the first 32 S columns
+                    tc::wait_st();
                     if (__any_sync(0xffffffffu, move)) {
-                        // O must hold P V of the previous tile before it is rescaled
+                        // the running max moved: O (which must hold P V of the previous
+                        // tile first) is rescaled before this tile's P V adds to it
                         wait_or_flag(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), dead, a.err);
                         tc::fence_after();
-                        const float alpha = move ? exp2f(m_run - m_new) : 1.f;
                         const uint32_t ob = 128u + (uint32_t)(p & 1) * D;
-#pragma unroll
+#pragma unroll 1
                         for (int cc = 0; cc < D / 32; ++cc) {
                             float o[32];
                             tc::ld32(trow + ob + cc * 32, o);
@@ -850,21 +876,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             tc::st32(trow + ob + cc * 32, o);
                         }
                         tc::wait_st();
-                        l *= alpha;
                     }
-                    m_run = m_new;
-                    const float nm = m_run == -INFINITY ? 0.f : -m_run;
-                    uint32_t pk[32];
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        pk[k] = pack_bf16x2(exp2f(fmaf(s[2 * k], a.scale_log2, nm)),
-                                            exp2f(fmaf(s[2 * k + 1], a.scale_log2, nm)));
-                        ls[k & 3] += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
-                    }
-                    l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                    st32u(trow + b * kTok, pk);  // P over the first 32 S columns
-                    tc::wait_st();
                 }
                 tc::fence_before();
                 __syncwarp();
@@ -880,7 +892,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             if (pc.kind == kWhole) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D);
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     float o[32];
                     if (live_warp) {
@@ -900,7 +912,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 // a later piece of a context begun in an earlier share: store the
                 // partial in this CTA's slot; the last warp to finish raises the flag
                 float *po = a.part_o + ((int64_t)w_me * kRows + r) * D;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     float o[32];
                     if (live_warp) {
@@ -959,7 +971,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     }
                 const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D);
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     float o[32];
                     if (live_warp) {
