@@ -65,12 +65,18 @@ namespace rows {
 
 constexpr int kTok = 64;          // keys per tile
 constexpr int kRows = tc::kRows;  // query rows per context (the MMA's M)
-constexpr int kThreads = 224;
-constexpr int kMaxUnits = 2048;   // groups / sequences scanned per launch
+constexpr int kThreads = 256;
+// Warp roles.  The producer and MMA warps share the schedulers of softmax warps
+// 2 and 3, which have no rows when a context has at most 64 (resp. 96) rows.
+constexpr int kAuxWarp = 5, kProducerWarp = 6, kMmaWarp = 7;
+constexpr int kMaxUnits = 1024;   // groups / sequences scanned per launch
 constexpr int kMinTiles = 4;      // shares hold >= 4 tiles unless the total is small
 constexpr int kIdCache = 512;     // block ids staged by the producer
+constexpr int kChunkTiles = 128;  // tiles whose keys the producer stages at once
 constexpr int kDescs = 8;         // piece descriptors in flight
 constexpr float kRescale = 8.f;   // headroom (log2 units) before a row's running max moves
+constexpr int kSB = 3;            // S / P buffers in tensor memory: Q K^T runs up to two tiles ahead
+constexpr uint32_t kOBase = kSB * kTok;  // O of even / odd pieces at kOBase / kOBase + D
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxCtas = 256;     // partial slots in the workspace: one per CTA
 
@@ -120,26 +126,36 @@ struct TileInfo {
     int key0;      // position of the tile's first key
 };
 
+// Byte offset rounded up to a multiple of 16 (every region below is accessed
+// with up to 16-byte vectors).
+constexpr int align16(int x) { return (x + 15) & ~15; }
+
 template <int D>
 struct Layout {
     static constexpr int H = D / 64;                      // 128-byte column halves
     static constexpr int kQBytes = H * kRows * 128;      // [half][row][128 B]
-    static constexpr int kKVBytes = H * kTok * 128;      // K (or V) of a tile: [half][token][128 B]
+    // K of a tile: [half][token][128 B] (one 2-D box per block and half);
+    // V of a tile: [block][half][block row][128 B] (one box per block)
+    static constexpr int kKVBytes = H * kTok * 128;
     static constexpr int kStageBytes = 2 * kKVBytes;
     static constexpr int NS = D == 128 ? 5 : 10;         // 160 KB of tiles in flight
     static constexpr int q = 0;
     static constexpr int ring = q + kQBytes;
-    static constexpr int cum = ring + NS * kStageBytes;  // int [kMaxUnits + 1]
-    static constexpr int uval = cum + (kMaxUnits + 4) * 4;  // int [kMaxUnits]: prefix tokens / query count
-    static constexpr int ids = uval + kMaxUnits * 4;     // int [kIdCache]
-    static constexpr int mo = ids + kIdCache * 4;        // int [kRows + 4]: members' first own tile
-    static constexpr int tinfo = mo + (kRows + 4) * 4;   // TileInfo [NS]
-    static constexpr int desc = tinfo + NS * 16;         // Piece [kDescs]
-    static constexpr int bars = desc + kDescs * 32;
-    static constexpr int kBars = 2 * NS + 8 + 2 * kDescs;
-    static constexpr int misc = bars + kBars * 8;        // TMEM address, scan scratch, counters
-    static constexpr int total = misc + 128 + 1024;      // + alignment slack
+    static constexpr int cum = ring + NS * kStageBytes;               // int [kMaxUnits + 4]
+    static constexpr int uval = align16(cum + (kMaxUnits + 4) * 4);   // int [kMaxUnits]: prefix tokens / query count
+    static constexpr int ids = align16(uval + kMaxUnits * 4);         // int [kIdCache]
+    static constexpr int tkc = align16(ids + kIdCache * 4);           // int4 [kChunkTiles]: keys of the staged tiles
+    static constexpr int mo = align16(tkc + kChunkTiles * 16);        // int [kRows + 4]: members' first own tile
+    static constexpr int tinfo = align16(mo + (kRows + 4) * 4);       // TileInfo [NS]
+    static constexpr int desc = align16(tinfo + NS * 16);             // Piece [kDescs]
+    static constexpr int bars = align16(desc + kDescs * 32);
+    static constexpr int kBars = 3 * NS + 2 * kSB + 4 + 2 * kDescs;  // k/v full, kv empty, s/p full, o_done[2], ready, fin, descs
+    static constexpr int misc = align16(bars + kBars * 8);            // TMEM address, scan scratch, counters
+    static constexpr int total = misc + 128 + 1024;                   // + alignment slack
     static_assert(sizeof(Piece) == 32 && sizeof(TileInfo) == 16, "descriptor sizes");
+    static_assert(ring % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(tkc % 16 == 0 && tinfo % 16 == 0 && bars % 8 == 0, "vector accesses need aligned regions");
+    static_assert(total <= 227 * 1024, "shared memory per CTA");
 };
 
 __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
@@ -316,6 +332,117 @@ __device__ __forceinline__ TileKeys tile_keys(const Args &a, const Ctx &c, const
     return k;
 }
 
+__device__ __forceinline__ void ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st8u(uint32_t taddr, const uint32_t *v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// One tile of one row's online softmax over its NC x 16 keys [c0, c0 + 16 NC)
+// of the tile: S from tensor memory at sp (scores, 1 column per key), P (bf16
+// pairs) back over the first 32 columns at sp -- this row's keys, zero for the
+// others.  Keys at or past lim, or in a block whose bit is set in `bad`, get
+// zero weight.  The running max moves only when the tile's exceeds it by more
+// than 2^kRescale (then `move`, and O is to be scaled by `alpha`).
+template <int NC>
+__device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint32_t bad, int bshift, float sl2,
+                                             float &m_run, float &l, bool &move, float &alpha) {
+    constexpr int N = NC * 16;
+    float s[N];
+    if constexpr (NC == 4) {
+        tc::ld32(sp, s);
+        tc::ld32(sp + 32, s + 32);
+    } else if constexpr (NC == 2) {
+        tc::ld32(sp + c0, s);
+    } else {
+        ld16(sp + c0, s);
+    }
+    tc::wait_ld();
+    // keys of this row: bit k of (lo, hi) = key c0 + k is seen (below lim, in a valid block)
+    uint32_t lo = 0u, hi = 0u;
+    {
+        const int n = lim - c0;
+        if (n >= 64) {
+            lo = hi = 0xffffffffu;
+        } else if (n > 0) {
+            lo = n >= 32 ? 0xffffffffu : (1u << n) - 1u;
+            hi = n > 32 ? (1u << (n - 32)) - 1u : 0u;
+        }
+        if (bad) {  // invalid blocks: clear their keys (rare)
+            for (int k = 0; k < N; ++k)
+                if ((bad >> ((c0 + k) >> bshift)) & 1u) {
+                    if (k < 32) lo &= ~(1u << k);
+                    else hi &= ~(1u << (k - 32));
+                }
+        }
+    }
+    const bool full = (N == 64 ? (lo & hi) : (N == 32 ? lo : (lo & 0xffffu) | ~0xffffu)) == 0xffffffffu;
+#pragma unroll
+    for (int k = 0; k < N; ++k) s[k] *= sl2;  // scores in the log2 domain
+    if (!full) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) {
+            const uint32_t w = k < 32 ? lo : hi;
+            s[k] = (w >> (k & 31)) & 1u ? s[k] : -INFINITY;
+        }
+    }
+    float mx[8];  // row max (tree)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+    for (int k = 16; k < N; k += 16)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(s[k + q], s[k + 8 + q]));
+    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    float m_new = m_run;
+    move = false;
+    if (mt != -INFINITY) {
+        if (m_run == -INFINITY) {
+            m_new = mt;  // nothing accumulated yet: O is zero, nothing to rescale
+        } else if (mt > m_run + kRescale) {
+            m_new = mt;
+            move = true;
+        }
+    }
+    alpha = move ? ex2_approx(m_run - m_new) : 1.f;
+    m_run = m_new;
+    const float nm = m_run == -INFINITY ? 0.f : -m_run;
+    uint32_t pk[N / 2];
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < N / 2; ++k) {
+        pk[k] = pack_bf16x2(ex2_approx(s[2 * k] + nm), ex2_approx(s[2 * k + 1] + nm));
+        ls[k & 3] += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
+    }
+    l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));  // the sum uses the rounded weights
+    // P: 8 columns per 16 keys; this row's groups, then zeros for the others
+    const int g0 = c0 >> 4;
+    if constexpr (NC == 4) {
+        st32u(sp, pk);
+    } else {
+#pragma unroll
+        for (int gg = 0; gg < NC; ++gg) st8u(sp + 8 * (g0 + gg), pk + 8 * gg);
+    }
+    if (NC < 4) {
+        const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            if (g < g0 || g >= g0 + NC) st8u(sp + 8 * g, z);
+    }
+    tc::wait_st();
+}
+
 // Bounded wait helper: returns false (and flags) once the wait gives up.
 __device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, bool &dead, unsigned int *err) {
     if (dead) return false;
@@ -341,21 +468,24 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     int *uval = reinterpret_cast<int *>(smem + L::uval);
     int *ids = reinterpret_cast<int *>(smem + L::ids);
     int *mo = reinterpret_cast<int *>(smem + L::mo);
+    int4 *tkc = reinterpret_cast<int4 *>(smem + L::tkc);
     TileInfo *tinfo = reinterpret_cast<TileInfo *>(smem + L::tinfo);
     Piece *descs = reinterpret_cast<Piece *>(smem + L::desc);
-    uint64_t *kv_full = reinterpret_cast<uint64_t *>(smem + L::bars);
-    uint64_t *kv_empty = kv_full + NS;
+    uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + L::bars);  // a stage's K (and its record) landed
+    uint64_t *v_full = k_full + NS;                                    // a stage's V landed
+    uint64_t *kv_empty = v_full + NS;
     uint64_t *s_full = kv_empty + NS;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2;
+    uint64_t *p_full = s_full + kSB;
+    uint64_t *o_done = p_full + kSB;  // [2]: one phase per completed P V of that parity
     uint64_t *ready = o_done + 2;
     uint64_t *fin = ready + 1;
     uint64_t *desc_full = fin + 1;
     uint64_t *desc_empty = desc_full + kDescs;
+
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
     int *warp_sums = reinterpret_cast<int *>(smem + L::misc + 16);  // [8] + carry
     int *counters = reinterpret_cast<int *>(smem + L::misc + 64);   // partial-store / merge warp counters
-    constexpr int kCarry = 7;
+    constexpr int kCarry = kThreads / 32;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = a.num_kv_heads, G = a.group, B = a.block_size;
@@ -470,23 +600,25 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&kv_full[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
             mbar_init(&kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
-            mbar_init(&o_done[i], 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
         mbar_init(ready, 4);
         mbar_init(fin, 1);
+
         for (int i = 0; i < kDescs; ++i) {
             mbar_init(&desc_full[i], 1);
             mbar_init(&desc_empty[i], 5);
         }
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(kTmemCols)
                      : "memory");
@@ -499,7 +631,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     const uint32_t q_s = smem_u32(smem + L::q);
     const uint32_t ring_s = smem_u32(smem + L::ring);
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ======================= producer =======================
         Ctx c;
         bool dead = !c.seek(a, cum, uval, s0, cap);
@@ -553,15 +685,22 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             }
             dead = __shfl_sync(0xffffffffu, dead, 0);
             ++p;
-            // tiles of the piece, in chunks of staged block ids
-            for (int k0 = i0; k0 < i1 && !dead; k0 += kIdCache / bpt) {
-                const int k1 = min(i1, k0 + kIdCache / bpt);
+            // tiles of the piece, in chunks: first the chunk's tile keys and block
+            // ids are staged in shared memory (all loads in flight together),
+            // then each tile is issued from there
+            const int cht = min(kChunkTiles, kIdCache / bpt);
+            for (int k0 = i0; k0 < i1 && !dead; k0 += cht) {
+                const int k1 = min(i1, k0 + cht);
+                __syncwarp();
+                for (int i = k0 + lane; i < k1; i += 32) {
+                    const TileKeys tk = tile_keys(a, c, mo, members, i, cap);
+                    tkc[i - k0] = make_int4(tk.key0, tk.nvalid, tk.member, tk.seq);
+                }
                 __syncwarp();
                 for (int e = lane; e < (k1 - k0) * bpt; e += 32) {
-                    const int i = k0 + e / bpt, jb = e % bpt;
-                    const TileKeys tk = tile_keys(a, c, mo, members, i, cap);
-                    const int lb = tk.key0 / B + jb;
-                    ids[e] = jb * B < tk.nvalid ? a.block_tables[(int64_t)tk.seq * a.max_blocks + lb] : INT_MIN;
+                    const int4 tk = tkc[e / bpt];
+                    const int jb = e % bpt;
+                    ids[e] = jb * B < tk.y ? a.block_tables[(int64_t)tk.w * a.max_blocks + tk.x / B + jb] : INT_MIN;
                 }
                 __syncwarp();
                 for (int i = k0; i < k1; ++i, ++j) {
@@ -569,35 +708,38 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     if (lane == 0 && j >= NS) wait_or_flag(&kv_empty[st], (uint32_t)(((j / NS) - 1) & 1), dead, a.err);
                     dead = __shfl_sync(0xffffffffu, dead, 0);
                     if (dead) break;
-                    const TileKeys tk = tile_keys(a, c, mo, members, i, cap);
-                    const int nblk = (tk.nvalid + B - 1) / B;
+                    const int4 tk = tkc[i - k0];
+                    const int nblk = (tk.y + B - 1) / B;
                     // lane jb < nblk checks block jb's id (an invalid id is read as block 0, its keys masked)
-                    bool bad = false;
-                    if (lane < nblk) {
-                        const int id = ids[(i - k0) * bpt + lane];
-                        bad = id < 0 || id >= a.num_blocks;
-                    }
+                    int id = 0;
+                    if (lane < nblk) id = ids[(i - k0) * bpt + lane];
+                    const bool bad = lane < nblk && (id < 0 || id >= a.num_blocks);
                     const uint32_t badm = __ballot_sync(0xffffffffu, bad);
                     if (lane == 0) {
                         if (badm) flag_error(a.err, PKV_DEVERR_BLOCK_ID);
                         TileInfo ti;
-                        ti.member = tk.member;
-                        ti.nvalid = tk.nvalid;
+                        ti.member = tk.z;
+                        ti.nvalid = tk.y;
                         ti.bad = badm;
-                        ti.key0 = tk.key0;
+                        ti.key0 = tk.x;
                         tinfo[st] = ti;
-                        mbar_arrive_expect_tx(&kv_full[st], (uint32_t)(nblk * 2 * H * B * 128));
+                        mbar_arrive_expect_tx(&k_full[st], (uint32_t)(nblk * H * B * 128));
+                        mbar_arrive_expect_tx(&v_full[st], (uint32_t)(nblk * H * B * 128));
                     }
                     __syncwarp();
-                    // boxes: (block jb, half h, K or V) -> one lane each
-                    for (int bi = lane; bi < nblk * 2 * H; bi += 32) {
-                        const int jb = bi / (2 * H), h = (bi >> 1) % H, isv = bi & 1;
-                        const int id = ids[(i - k0) * bpt + jb];
-                        const int b2 = (id < 0 || id >= a.num_blocks) ? 0 : id;
+                    // boxes, one lane each: K by (block, half), then V by block (the
+                    // whole (block, kv head) slab, both column halves)
+                    for (int bi = lane; bi < nblk * (H + 1); bi += 32) {
+                        const bool isv = bi >= nblk * H;
+                        const int jb = isv ? bi - nblk * H : bi / H, h = isv ? 0 : bi % H;
+                        const int bid = ids[(i - k0) * bpt + jb];
+                        const int b2 = (bid < 0 || bid >= a.num_blocks) ? 0 : bid;
                         const int y = (int)(((int64_t)b2 * Hkv + c.kvh) * B);
-                        const uint32_t dst =
-                            ring_s + st * L::kStageBytes + isv * L::kKVBytes + h * (kTok * 128) + jb * B * 128;
-                        tma_load_2d(dst, isv ? &tm_v : &tm_k, smem_u32(&kv_full[st]), h * 64, y);
+                        const uint32_t stage = ring_s + st * L::kStageBytes;
+                        if (isv)
+                            tma_load_3d(stage + L::kKVBytes + jb * (H * B * 128), &tm_v, smem_u32(&v_full[st]), 0, y, 0);
+                        else
+                            tma_load_2d(stage + h * (kTok * 128) + jb * B * 128, &tm_k, smem_u32(&k_full[st]), h * 64, y);
                     }
                 }
             }
@@ -618,13 +760,23 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         }
         // copies still in flight (only after a timeout) land before the CTA exits
         if (lane == 0 && dead)
-            for (int64_t k = max((int64_t)0, j - NS); k < j; ++k)
-                mbar_wait_bounded(&kv_full[k % NS], (uint32_t)((k / NS) & 1));
-    } else if (warp == 5) {
+            for (int64_t k = max((int64_t)0, j - NS); k < j; ++k) {
+                mbar_wait_bounded(&k_full[k % NS], (uint32_t)((k / NS) & 1));
+                mbar_wait_bounded(&v_full[k % NS], (uint32_t)((k / NS) & 1));
+            }
+    } else if (warp == kMmaWarp) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::instr_desc(kTok, false);
             constexpr uint32_t idesc_pv = tc::instr_desc(D, true);
+            constexpr uint32_t idesc_qk = tc::instr_desc(kTok, false);
+            // P V: 16 keys per MMA; V's 64-column halves are B rows apart, its
+            // 8-row groups 1024 bytes apart inside a block (blocks of 8: a block apart)
+            const uint32_t pv_lbo = (uint32_t)(B * 128), pv_sbo = B >= 16 ? 1024u : (uint32_t)(H * B * 128);
+            // descriptors advance by (byte offset >> 4) in their start-address field
+            uint32_t pv_off[kTok / 16];
+#pragma unroll
+            for (int k = 0; k < kTok / 16; ++k) pv_off[k] = (uint32_t)((16 * k / B) * (H * B * 128) + (16 * k % B) * 128);
+            const uint64_t qd = tc::smem_desc(q_s, 16, 1024);
             int64_t jq = 0, jp = 0;       // next Q K^T / P V tile
             int pq = 0, pp = 0;           // their pieces
             int tq = 0, tp = 0;           // tile within those pieces
@@ -644,14 +796,16 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             for (;;) {
                 bool prog = false;
                 if (jp < jq) {
-                    if (mbar_test_wait(&p_full[jp & 1], (uint32_t)((jp >> 1) & 1))) {
+                    if (mbar_test_wait(&p_full[jp % kSB], (uint32_t)((jp / kSB) & 1)) &&
+                        mbar_test_wait(&v_full[jp % NS], (uint32_t)((jp / NS) & 1))) {
                         tc::fence_after();
-                        const uint32_t ob = 128u + (uint32_t)(pp & 1) * D;
-                        const uint32_t pa = tmem + (uint32_t)(jp & 1) * kTok;  // P in the S columns
+                        const uint32_t ob = kOBase + (uint32_t)(pp & 1) * D;
+                        const uint32_t pa = tmem + (uint32_t)(jp % kSB) * kTok;  // P in the S columns
                         const uint32_t vb = ring_s + (uint32_t)(jp % NS) * L::kStageBytes + L::kKVBytes;
+                        const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
 #pragma unroll
                         for (int k = 0; k < kTok / 16; ++k)
-                            tc::mma_ts(tmem + ob, pa + 8 * k, tc::smem_desc(vb + k * 2048, kTok * 128, 1024), idesc_pv,
+                            tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
                                        (tp == 0 && k == 0) ? 0u : 1u);
                         tc::commit(&o_done[jp & 1]);
                         tc::commit(&kv_empty[jp % NS]);
@@ -666,7 +820,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 } else if (done_q) {
                     break;
                 }
-                if (!done_q && jq < jp + 2) {
+                if (!done_q && jq < jp + kSB) {
                     if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
                         ntq = descs[pq % kDescs].ntiles;
                         if (ntq == 0) {
@@ -676,17 +830,18 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         }
                         prog = true;
                     }
-                    if (ntq > 0 && mbar_test_wait(&kv_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
+                    if (ntq > 0 && mbar_test_wait(&k_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
                         (tq > 0 || mbar_test_wait(ready, (uint32_t)(pq & 1)))) {
                         tc::fence_after();
                         const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
+                        const uint64_t kd = tc::smem_desc(kb, 16, 1024);
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k)
-                            tc::mma(tmem + (uint32_t)(jq & 1) * kTok,
-                                    tc::smem_desc(q_s + (k >> 2) * (kRows * 128) + (k & 3) * 32, 16, 1024),
-                                    tc::smem_desc(kb + (k >> 2) * (kTok * 128) + (k & 3) * 32, 16, 1024), idesc_qk,
+                            tc::mma(tmem + (uint32_t)(jq % kSB) * kTok,
+                                    qd + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                                    kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
                                     k > 0 ? 1u : 0u);
-                        tc::commit(&s_full[jq & 1]);
+                        tc::commit(&s_full[jq % kSB]);
                         ++jq;
                         if (++tq == ntq) {
                             ++pq;
@@ -709,7 +864,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             mbar_wait_bounded(fin, 0u);
             (void)dead;
         }
-    } else if (warp == 6) {
+    } else if (warp == kAuxWarp) {
         // ======================= members' block tables =======================
         if (a.mode == kGrouped) {
             Ctx c;
@@ -735,17 +890,28 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
         }
-    } else {
+    } else if (warp < 4) {
         // ======================= softmax (warps 0-3) =======================
-        const int r = warp * 32 + lane;
+        // thread r owns query row r of the piece (TMEM lane r)
+        const int rr = threadIdx.x;
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         bool dead = false;
         int64_t j = 0;
         int p = 0;
-        // row r's queries of a piece into Q (128-byte swizzled, K-major; zero past the live rows)
+        // P V of tile x has completed.  o_done[x & 1] completes one phase per P V
+        // of that parity, and a parity wait is only meaningful for the barrier's
+        // current or preceding phase.  So the P of tile j is released only after
+        // P V of tile j - 2 (same barrier) was waited for: every phase is waited
+        // for in order, and a barrier never runs two phases past its waiter (P V
+        // of tile j needs this tile's P).
+        auto wait_pv = [&](int64_t x) {
+            if (x >= 0) wait_or_flag(&o_done[x & 1], (uint32_t)((x >> 1) & 1), dead, a.err);
+        };
+        // this thread's query row of a piece into Q (128-byte swizzled, K-major; zero past the live rows)
         auto copy_q = [&](const Piece &pc) {
-            const bool live = r < pc.rows;
-            const int row = pc.row_base + (live ? r / G : 0), head = pc.kvh * G + r % G;
+            const bool live = rr < pc.rows;
+            const int row = pc.row_base + (live ? rr / G : 0), head = pc.kvh * G + rr % G;
+            const int r = rr;
             const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)row * a.num_heads + head) * D;
 #pragma unroll
             for (int k = 0; k < D / 8; ++k) {
@@ -772,17 +938,17 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         }
         while (pc.ntiles > 0 && !dead) {
             const bool live_warp = warp * 32 < pc.rows;
-            const bool live = r < pc.rows;
-            const int my_member = r / G;
-            const int my_pos = pc.pos0 + r / G;  // multi-token: this row's position
+            const bool live = rr < pc.rows;
+            const int my_member = rr / G;
+            const int my_pos = pc.pos0 + rr / G;      // multi-token: this row's position
             float m_run = -INFINITY, l = 0.f;
             Piece nx{};
             for (int i = 0; i < pc.ntiles; ++i, ++j) {
-                const int st = (int)(j % NS), b = (int)(j & 1);
-                // the stage's record (ordered by the producer's arrive on kv_full)
-                wait_or_flag(&kv_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
+                const int st = (int)(j % NS), b = (int)(j % kSB);
+                // the stage's record (ordered by the producer's arrive on k_full)
+                wait_or_flag(&k_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
                 const TileInfo ti = tinfo[st];
-                wait_or_flag(&s_full[b], (uint32_t)((j >> 1) & 1), dead, a.err);
+                wait_or_flag(&s_full[b], (uint32_t)((j / kSB) & 1), dead, a.err);
                 tc::fence_after();
                 if (dead) break;
                 if (i == pc.ntiles - 1) {
@@ -794,78 +960,33 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 // keys past the context's end or in invalid blocks: zero their V rows
                 // (stale slots may hold NaN; a zero weight must meet a zero)
                 if (ti.nvalid < kTok || ti.bad) {
+                    wait_or_flag(&v_full[st], (uint32_t)((j / NS) & 1), dead, a.err);  // V landed: zero after it
                     const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
-                    for (int e = r; e < kTok * H * 8; e += 128) {
+                    for (int e = threadIdx.x; e < kTok * H * 8; e += 128) {
                         const int key = (e / 8) % kTok, h = e / (kTok * 8), chk = e % 8;
                         const bool zero = key >= ti.nvalid || ((ti.bad >> (key / B)) & 1u);
-                        if (zero)
-                            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vbase + h * (kTok * 128) +
-                                                                                   key * 128 + chk * 16),
-                                         "r"(0u)
-                                         : "memory");
+                        const uint32_t row = vbase + (key / B) * (H * B * 128) + h * (B * 128) + (key % B) * 128;
+                        if (zero) asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(row + chk * 16), "r"(0u) : "memory");
                     }
                     fence_proxy_async();
                 }
                 if (live_warp) {
-                    float s[kTok];
-                    tc::ld32(trow + b * kTok, s);
-                    tc::ld32(trow + b * kTok + 32, s + 32);
-                    tc::wait_ld();
-                    // scores in the log2 domain
-#pragma unroll
-                    for (int k = 0; k < kTok; ++k) s[k] *= a.scale_log2;
                     // keys this row sees in this tile: [0, lim) minus invalid blocks
                     int lim = ti.nvalid;
                     if (!live) lim = 0;
                     if (ti.member >= 0 && ti.member != my_member) lim = 0;
                     if (a.mode == kMulti) lim = min(lim, my_pos - ti.key0 + 1);
-                    if (lim < kTok || ti.bad) {
-                        const int bshift = B == 8 ? 3 : (B == 16 ? 4 : 5);
-#pragma unroll
-                        for (int k = 0; k < kTok; ++k)
-                            if (k >= lim || ((ti.bad >> (k >> bshift)) & 1u)) s[k] = -INFINITY;
-                    }
-                    // row max (tree)
-                    float mx[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
-#pragma unroll
-                    for (int k = 16; k < kTok; k += 16)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(s[k + q], s[k + 8 + q]));
-                    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                    // the running max moves only when the tile's exceeds it by more than 2^8
-                    float m_new = m_run;
+                    const int bshift = B == 8 ? 3 : (B == 16 ? 4 : 5);
                     bool move = false;
-                    if (mt != -INFINITY) {
-                        if (m_run == -INFINITY) {
-                            m_new = mt;  // nothing accumulated yet: O is zero, nothing to rescale
-                        } else if (mt > m_run + kRescale) {
-                            m_new = mt;
-                            move = true;
-                        }
-                    }
-                    // P with the new reference point (S is dead once P is in tensor memory)
-                    const float alpha = move ? ex2_approx(m_run - m_new) : 1.f;
-                    m_run = m_new;
-                    const float nm = m_run == -INFINITY ? 0.f : -m_run;
-                    uint32_t pk[32];
-                    float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        pk[k] = pack_bf16x2(ex2_approx(s[2 * k] + nm), ex2_approx(s[2 * k + 1] + nm));
-                        ls[k & 3] += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
-                    }
-                    l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-                    st32u(trow + b * kTok, pk);  // P over the first 32 S columns
-                    tc::wait_st();
+                    float alpha = 1.f;
+                    const uint32_t sp = trow + b * kTok;
+                    softmax_tile<4>(sp, 0, lim, ti.bad, bshift, a.scale_log2, m_run, l, move, alpha);
                     if (__any_sync(0xffffffffu, move)) {
                         // the running max moved: O (which must hold P V of the previous
                         // tile first) is rescaled before this tile's P V adds to it
-                        wait_or_flag(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), dead, a.err);
+                        wait_pv(j - 1);
                         tc::fence_after();
-                        const uint32_t ob = 128u + (uint32_t)(p & 1) * D;
+                        const uint32_t ob = kOBase + (uint32_t)(p & 1) * D;
 #pragma unroll 1
                         for (int cc = 0; cc < D / 32; ++cc) {
                             float o[32];
@@ -878,137 +999,121 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         tc::wait_st();
                     }
                 }
+                wait_pv(j - 2);  // keeps this tile's barrier at most one phase ahead
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (dead) break;
             if (nx.ntiles > 0) q_ready();  // the next piece's Q K^T may start
-            // the piece's result: O (TMEM) with the row's running max and sum
-            wait_or_flag(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), dead, a.err);
+            // the piece's result: O (TMEM) with each row's running max and sum
+            wait_pv(j - 1);
             tc::fence_after();
-            const uint32_t ob = 128u + (uint32_t)(p & 1) * D;
-            const int64_t orow = (int64_t)(pc.row_base + (live ? r / G : 0)) * a.num_heads + pc.kvh * G + r % G;
-            if (pc.kind == kWhole) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D);
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    float o[32];
+            const uint32_t ob = kOBase + (uint32_t)(p & 1) * D;
+            const int64_t orow = (int64_t)(pc.row_base + (live ? rr / G : 0)) * a.num_heads + pc.kvh * G + rr % G;
+            constexpr int kNc = D / 16;  // 16-column chunks of an O row
+            {
+                // the piece's result: final rows, a partial for the merger, or the merge
+                const float M = m_run, Lc = l;
+                float f = 1.f, e_own = 1.f, Mtr = 0.f;
+                bool got = true;
+                for (int cc = 0; cc < kNc; ++cc) {
+                    if (cc == 0) {
+                        if (pc.kind == kWhole) {
+                            f = Lc > 0.f ? 1.f / Lc : 0.f;
+                        } else if (pc.kind == kContinue) {
+                            if (live)
+                                *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + rr) * 2) = make_float2(M, Lc);
+                        } else if (live_warp) {
+                            // merger: this piece holds the context's first tile and is the
+                            // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
+                            const int n = pc.w1 - pc.w0;
+                            got = false;
+                            for (uint32_t it = 0; it < kWaitLimit && !got; ++it) {
+                                bool mine = true;
+                                for (int k = lane; k < n; k += 32)
+                                    mine = mine && ld_volatile_u64(a.flags + pc.w0 + 1 + k) == a.tag;
+                                got = __all_sync(0xffffffffu, mine);
+                                if (!got) __nanosleep(64);
+                            }
+                            if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                            // each lane saw some flags: acquire, then order every lane's reads after them
+                            fence_acq_rel_gpu();
+                            __syncwarp();
+                            float Mt = M;
+                            if (live)
+                                for (int w = pc.w0 + 1; w <= pc.w1; ++w)
+                                    Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * kRows + rr) * 2));
+                            Mtr = Mt == -INFINITY ? 0.f : Mt;
+                            e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
+                            float Ls = Lc * e_own;
+                            if (live)
+                                for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
+                                    if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
+                                }
+                            // NaN rows when a piece never came (flagged above)
+                            f = got ? (Ls > 0.f ? 1.f / Ls : 0.f) : __int_as_float(0x7fc00000);
+                        }
+                    }
                     if (live_warp) {
-                        tc::ld32(trow + ob + cc * 32, o);
+                        float o[16];
+                        ld16(trow + ob + cc * 16, o);
                         tc::wait_ld();
-                    }
-                    if (live) {
+                        if (live) {
+                            if (pc.kind == kContinue) {
+                                float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * kRows + rr) * D + cc * 16);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[cc * 4 + k] = make_uint4(pack_bf16x2(o[8 * k] * inv, o[8 * k + 1] * inv),
-                                                         pack_bf16x2(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
-                                                         pack_bf16x2(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
-                                                         pack_bf16x2(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
-                    }
-                }
-            } else if (pc.kind == kContinue) {
-                // a later piece of a context begun in an earlier share: store the
-                // partial in this CTA's slot; the last warp to finish raises the flag
-                float *po = a.part_o + ((int64_t)w_me * kRows + r) * D;
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    float o[32];
-                    if (live_warp) {
-                        tc::ld32(trow + ob + cc * 32, o);
-                        tc::wait_ld();
-                    }
-                    if (live) {
+                                for (int k = 0; k < 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                            } else {
+                                if (pc.kind == kMerger) {
 #pragma unroll
-                        for (int k = 0; k < 32; k += 4)
-                            *reinterpret_cast<float4 *>(po + cc * 32 + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-                    }
-                }
-                if (live)
-                    *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + r) * 2) = make_float2(m_run, l);
-                fence_acq_rel_gpu();
-                __syncwarp();
-                if (lane == 0) {
-                    fence_acq_rel_gpu();
-                    if (atomicAdd(&counters[0], 1) == 3) {
-                        counters[0] = 0;
-                        fence_acq_rel_gpu();
-                        *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
-                    }
-                }
-            } else {
-                // merger: this piece holds the context's first tile and is the last
-                // piece of this share; CTAs w0 + 1 .. w1 stored the rest
-                const int n = pc.w1 - pc.w0;
-                bool ok = true;
-                {
-                    bool got = false;
-                    for (uint32_t it = 0; it < kWaitLimit && !got; ++it) {
-                        bool mine = true;
-                        for (int k = lane; k < n; k += 32)
-                            mine = mine && ld_volatile_u64(a.flags + pc.w0 + 1 + k) == a.tag;
-                        got = __all_sync(0xffffffffu, mine);
-                        if (!got) __nanosleep(64);
-                    }
-                    ok = got;
-                }
-                if (!ok && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                // each lane saw some flags: acquire, then order every lane's reads after them
-                fence_acq_rel_gpu();
-                __syncwarp();
-                float M = m_run;
-                if (live)
-                    for (int w = pc.w0 + 1; w <= pc.w1; ++w)
-                        M = fmaxf(M, __ldcg(a.part_ml + ((int64_t)w * kRows + r) * 2));
-                const float Mr = M == -INFINITY ? 0.f : M;
-                const float e_own = m_run == -INFINITY ? 0.f : exp2f(m_run - Mr);
-                float Ls = l * e_own;
-                if (live)
-                    for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
-                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + r);
-                        if (ml.x != -INFINITY) Ls += ml.y * exp2f(ml.x - Mr);
-                    }
-                const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D);
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    float o[32];
-                    if (live_warp) {
-                        tc::ld32(trow + ob + cc * 32, o);
-                        tc::wait_ld();
-                    }
-                    if (live) {
+                                    for (int k = 0; k < 16; ++k) o[k] *= e_own;
+                                    for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
+                                        if (ml.x == -INFINITY) continue;
+                                        const float e = ex2_approx(ml.x - Mtr);
+                                        const float4 *src =
+                                            reinterpret_cast<const float4 *>(a.part_o + ((int64_t)w * kRows + rr) * D + cc * 16);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] *= e_own;
-                        for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
-                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + r);
-                            if (ml.x == -INFINITY) continue;
-                            const float e = exp2f(ml.x - Mr);
-                            const float4 *src = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)w * kRows + r) * D + cc * 32);
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const float4 v = __ldcg(src + k);
-                                o[4 * k] += e * v.x;
-                                o[4 * k + 1] += e * v.y;
-                                o[4 * k + 2] += e * v.z;
-                                o[4 * k + 3] += e * v.w;
+                                        for (int k = 0; k < 4; ++k) {
+                                            const float4 v = __ldcg(src + k);
+                                            o[4 * k] += e * v.x;
+                                            o[4 * k + 1] += e * v.y;
+                                            o[4 * k + 2] += e * v.z;
+                                            o[4 * k + 3] += e * v.w;
+                                        }
+                                    }
+                                }
+                                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16);
+                                dst[0] = make_uint4(pack_bf16x2(o[0] * f, o[1] * f), pack_bf16x2(o[2] * f, o[3] * f),
+                                                    pack_bf16x2(o[4] * f, o[5] * f), pack_bf16x2(o[6] * f, o[7] * f));
+                                dst[1] = make_uint4(pack_bf16x2(o[8] * f, o[9] * f), pack_bf16x2(o[10] * f, o[11] * f),
+                                                    pack_bf16x2(o[12] * f, o[13] * f), pack_bf16x2(o[14] * f, o[15] * f));
                             }
                         }
-                        const float f = ok ? inv : __int_as_float(0x7fc00000);  // NaN rows when a piece never came
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[cc * 4 + k] = make_uint4(pack_bf16x2(o[8 * k] * f, o[8 * k + 1] * f),
-                                                         pack_bf16x2(o[8 * k + 2] * f, o[8 * k + 3] * f),
-                                                         pack_bf16x2(o[8 * k + 4] * f, o[8 * k + 5] * f),
-                                                         pack_bf16x2(o[8 * k + 6] * f, o[8 * k + 7] * f));
                     }
                 }
-                // the last warp done reading clears the flags (a graph replay reuses the tag)
-                __syncwarp();
-                if (lane == 0 && atomicAdd(&counters[1], 1) == 3) {
-                    counters[1] = 0;
-                    for (int k = 0; k < n; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
+                if (pc.kind == kContinue) {
+                    // a later piece of a context begun in an earlier share: the partial
+                    // is stored; the last warp to finish raises the flag
+                    fence_acq_rel_gpu();
+                    __syncwarp();
+                    if (lane == 0) {
+                        fence_acq_rel_gpu();
+                        if (atomicAdd(&counters[0], 1) == 3) {
+                            counters[0] = 0;
+                            fence_acq_rel_gpu();
+                            *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
+                        }
+                    }
+                } else if (pc.kind == kMerger) {
+                    // the last warp done reading clears the flags (a graph replay reuses the tag)
+                    __syncwarp();
+                    if (lane == 0 && atomicAdd(&counters[1], 1) == 3) {
+                        counters[1] = 0;
+                        for (int k = 0; k < pc.w1 - pc.w0; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
+                    }
                 }
             }
             __syncwarp();
@@ -1020,7 +1125,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc::fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
@@ -1033,6 +1138,8 @@ struct WsLayout {
     size_t o_off, ml_off, flags_off, total;
 };
 
+// Per CTA slot (at most kMaxCtas): the partial (o, max, sum) of its first
+// piece for each of kRows rows, and a ready flag.
 static WsLayout ws_layout(int D) {
     WsLayout w;
     w.o_off = 0;
@@ -1042,11 +1149,26 @@ static WsLayout ws_layout(int D) {
     return w;
 }
 
-// 2-D view of a bf16 cache with one block per box: rows = num_blocks * Hkv *
-// B, columns = head_dim; box = 64 columns (128 bytes, 128-byte swizzle) x B rows.
+// 3-D view of a bf16 cache for one box per (block, kv head) slab: dims (64
+// columns, rows = num_blocks * Hkv * B, D / 64 column halves) with strides
+// (D * 2 bytes per row, 128 bytes per half); box (64, B, D / 64), 128-byte
+// swizzle.  The slab lands as [half][block row][128 B].
+static bool make_slab_map(CUtensorMap *map, const void *base, int64_t rows, int D, int B) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)B, (cuuint32_t)(D / 64)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// K: the 2-D view (64 columns x B rows per box); V: the slab view.
 static bool make_maps(const void *k_cache, const void *v_cache, int64_t rows, int D, int B, CUtensorMap *mk,
                       CUtensorMap *mv) {
-    return make_cache_map(mk, k_cache, rows, D, B) && make_cache_map(mv, v_cache, rows, D, B);
+    return make_cache_map(mk, k_cache, rows, D, B) && make_slab_map(mv, v_cache, rows, D, B);
 }
 
 template <int D>

@@ -117,7 +117,7 @@ def test_multi_token_host_validation_and_workspace():
     assert f(p, p, p, p, p, p, p, 4000, 10, 32, 8, 128, 16, 8, 64, 32768, 1 << 20, 0.1, p, 1 << 30,
              None) == pkv.PKV_ERR_UNSUPPORTED
     ws = lib.paged_attention_multi_token_workspace_size
-    # one partial slot per CTA (at most 256): 128 rows of (o, max, sum) fp32 and a
+    # one slot per CTA (at most 256): 128 rows of a partial (o, max, sum) fp32 and a
     # ready flag, whatever the number of query tokens or the context length
     r = lambda x: (x + 255) // 256 * 256
     fixed = 256 * 128 * 128 * 4 + r(256 * 128 * 2 * 4) + r(256 * 8)

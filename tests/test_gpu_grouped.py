@@ -120,8 +120,8 @@ def test_grouped_shapes_match_oracle(D, B, Hq, Hkv, prompts, width, shared):
 
 
 def test_more_groups_than_one_launch_scans():
-    """2100 groups (one launch scans at most 2048): the call runs the groups in
-    two launches over the same workspace."""
+    """2100 groups (one launch scans at most 1024): the call runs the groups in
+    three launches over the same workspace."""
     shape = wl.DecodeShape("beam_many", 0, 8, 2, 64, 16, torch.bfloat16)
     prompts, width = 2100, 2
     div = np.random.default_rng(7).integers(0, 21, prompts * width)
