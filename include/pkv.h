@@ -120,7 +120,7 @@ PKV_EXPORT pkv_status kv_cache_write(const void *k_new, const void *v_new, void 
  * single pass suffices (every sequence fits one partition).  The scratch holds
  * one partial result per (sequence, query head, piece of context): running
  * max, running sum and an unnormalised output row, all float32; with
- * partition_size == 0 also one piece count per (sequence, query head).
+ * partition_size == 0 also one 8-byte ready flag per partial.
  */
 PKV_EXPORT size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
                                       int max_seq_len, int partition_size);
@@ -276,12 +276,19 @@ PKV_EXPORT pkv_status paged_attention_decode_fp8(void *out, const void *q, const
  *                  are left unwritten, and PKV_DEVERR_SEQ_LEN is set); a
  *                  sequence with Q_s > L_s is flagged too and its queries that
  *                  see no token get zero rows
- *   workspace      paged_attention_multi_token_workspace_size() bytes for the
- *                  same (num_q_tokens, num_heads, head_dim, max_seq_len),
- *                  256-byte aligned (0 bytes, NULL allowed, when max_seq_len <=
- *                  1024): contexts longer than 1024 tokens are attended in
- *                  1024-token partitions whose partials a reduction kernel
- *                  merges.  Contents need no initialisation.
+ *   workspace      paged_attention_multi_token_workspace_size() bytes,
+ *                  256-byte aligned (about 17 MB for head_dim 128, whatever
+ *                  the number of tokens: one partial slot of 128 rows per
+ *                  CTA).  Contents need no initialisation; calls that share a
+ *                  workspace must be ordered on the device.
+ * The attention runs on the tensor cores (tcgen05): per KV head, the query
+ * heads of up to 128 / (num_heads / num_kv_heads) queries form the 128 rows
+ * of one context, attended against 64-token tiles of K and V (Q K^T and P V
+ * with fp32 accumulators in tensor memory, the causal limit applied per row).
+ * All contexts' tiles are cut into equal shares, one per SM; a context cut by
+ * share boundaries is merged inside the kernel.  The CTAs wait on one another,
+ * so the kernel is launched cooperatively: a grid that cannot be resident at
+ * once fails at launch (PKV_ERR_CUDA) instead of waiting.
  * Supported: bf16; head_dim 64 or 128; block_size 8, 16 or 32; at most 8
  * query heads per KV head.  Results do not depend on which physical blocks
  * hold the tokens.
@@ -368,14 +375,18 @@ PKV_EXPORT pkv_status paged_attention_decode_append(void *out, const void *q, co
  *                  member (minus one token when appending).  0 = no sharing.
  *   k_new, v_new   device [num_seqs][num_kv_heads][head_dim] or both NULL: as
  *                  in paged_attention_decode_append
- *   workspace      at least paged_attention_grouped_workspace_size() bytes,
- *                  256-byte aligned, no initialisation needed
- * The shared part of each group, cut to whole 64-token tiles, is one dense
- * contraction per kv head (members x query heads rows against each tile) and
- * runs on the tensor cores (tcgen05, accumulators in tensor memory), each
- * tile read once; each member's own tokens go through the balanced kernel; a
- * merge kernel joins the two.  With more than 2048 groups the shared part
- * runs on a kernel with one CTA per (group, kv head, 256 tokens) instead.
+ *   workspace      at least paged_attention_grouped_workspace_size() bytes
+ *                  (as for paged_attention_multi_token), 256-byte aligned, no
+ *                  initialisation needed
+ * Per KV head, a group (up to 128 / (num_heads / num_kv_heads) members at a
+ * time) is one context of members x query heads rows on the tensor cores
+ * (tcgen05, fp32 accumulators in tensor memory): the shared part, cut to whole
+ * 64-token tiles, is read once and seen by every row; then each member's own
+ * tiles, seen by that member's rows only.  One context gives every member's
+ * final result; a context cut by the kernel's equal per-SM shares is merged
+ * inside the kernel (cooperative launch, as for paged_attention_multi_token).
+ * With k_new/v_new a small kernel stores the new tokens first.  A launch
+ * scans at most 1024 groups; more groups take several launches.
  * A bad group description (offsets out of order or not covering 0..num_seqs,
  * a prefix length that is not a multiple of max(16, block_size)) flags
  * PKV_DEVERR_PREFIX.  A member whose prefix blocks differ from the first

@@ -6,10 +6,8 @@
 //     the step's new tokens, and merges the contexts it cuts (see its header).
 //   * decode_bf16_mma_kernel / decode_simt_kernel -- fixed partitions (bf16 /
 //     fp32), whose partials decode_reduce_kernel merges.
-//   * decode_bf16_prefix_tc_kernel / decode_bf16_prefix_kernel -- shared
-//     prefixes of grouped calls (tcgen05 / mma.sync), merged with each
-//     member's own tokens by decode_reduce_kernel.
-//   * multi_token_kernel -- several causal query tokens per sequence.
+// Grouped (shared-prefix) decode and multi-token attention run on the
+// tensor-core kernel of rows_attention.cu.
 //
 // Sources: "KV cache & PagedAttention -- vi sao chatbot AI ton bo nho"
 // (aiwiki.vn), second paragraph (the current query against the keys of the
@@ -73,18 +71,12 @@ struct DecodeArgs {
     float *part_o;  // [S][Hq][max_parts][D]
     float *part_m;  // [S][Hq][max_parts]
     float *part_l;  // [S][Hq][max_parts]
-    int *pieces;    // [S][Hkv]: partials of each segment (balanced path with the merge kernel)
-    // balanced path with the merge in the attention kernel: one ready flag per
+    // balanced path (merge in the attention kernel): one ready flag per
     // (segment, partial slot) [S][Hkv][max_parts], set to this call's tag
-    // (never 0) once the slot's partial is stored; nullptr = the merge kernel
-    // runs afterwards
+    // (never 0) once the slot's partial is stored
     unsigned long long *flags;
     unsigned long long tag;
-    int *seq_tok0;  // [S]: tokens of a shared prefix attended elsewhere (grouped path), or nullptr
-    int *prefix_pieces;   // [S][Hkv]: prefix partials of each member (tensor-core prefix kernel), or nullptr
     int merge_trigger;    // merge kernel: let the next kernel start early (small merges only)
-    int prefix_slot;      // grouped path: first partial slot of the prefix partials
-    int prefix_part;      // grouped path: tokens per prefix partition
     int num_seqs, num_heads, num_kv_heads, group;
     int block_size, max_blocks, num_blocks, max_seq_len;
     int partition_size, max_parts;
@@ -543,16 +535,15 @@ constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended
 // Shared-memory layout of the balanced kernel (host and device agree on it).
 // Offsets are from the 1024-aligned base.
 struct StreamKLayout {
-    int ring, bars, ycache, masks, prefix, toff, total;
+    int ring, bars, ycache, masks, prefix, total;
     // stage_bytes: one ring stage (K and V of one tile); 0 = a 16-token bf16 tile
-    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, bool grouped, int stage_bytes = 0) {
+    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, int stage_bytes = 0) {
         ring = NW * NS * (stage_bytes ? stage_bytes : 2 * D * kTile * 2);
         bars = ring;
         ycache = bars + NW * NS * 8;   // int2 per cached tile
         masks = ycache + kYCache * 8;  // valid-row mask per cached tile
         prefix = masks + kYCache * 4;
-        toff = prefix + (num_seqs + 1) * 4;  // grouped: first token of each sequence's own part
-        total = toff + (grouped ? num_seqs * 4 : 0) + 1024;  // + alignment slack
+        total = prefix + (num_seqs + 1) * 4 + 1024;  // + alignment slack
     }
 };
 
@@ -1043,8 +1034,7 @@ __device__ __forceinline__ void merge_segment(const float *part_o, const float *
 // TMA ring.  Where a segment (sequence, kv head) ends inside a share, the warp
 // stores its result for that piece -- the final rows if the share holds the
 // whole segment, otherwise a partial -- and carries on with the next segment.
-// Partials are merged either by the merge kernel afterwards (grouped calls)
-// or in this kernel: a share cuts at most its first and last segment, and the
+// Partials are merged in this kernel: a share cuts at most its first and last segment, and the
 // warp holding a split segment's first tile (its share's last segment) merges
 // it once the other pieces -- processed at the start of their own shares --
 // have flagged their partials.  That is the only wait between warps; it is
@@ -1052,8 +1042,7 @@ __device__ __forceinline__ void merge_segment(const float *part_o, const float *
 // wave) and never waits itself.
 //
 // F8: the cache holds E4M3 codes (K rows, V transposed per block); tiles are
-// attended by attend_tile_f8 and the queries are loaded by load_q_f16.  The
-// FP8 path has no fused append and no grouped (shared-prefix) mode.
+// attended by attend_tile_f8 and the queries are loaded by load_q_f16.
 template <int D, int NW, int NS, bool F8 = false>
 __global__ void __launch_bounds__(NW * 32)
 decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -1063,25 +1052,21 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const bool grouped = !F8 && a.seq_tok0 != nullptr;
-    const StreamKLayout L(D, NW, NS, a.num_seqs, grouped, Lay::kStage);
+    const StreamKLayout L(D, NW, NS, a.num_seqs, Lay::kStage);
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + L.bars);
     int2 *ycache = reinterpret_cast<int2 *>(smem + L.ycache);
     uint32_t *mcache = reinterpret_cast<uint32_t *>(smem + L.masks);
     int *prefix = reinterpret_cast<int *>(smem + L.prefix);
-    int *toff = reinterpret_cast<int *>(smem + L.toff);
     __shared__ int warp_sums[NW];
     __shared__ int carry;
 
-    // Programmatic dependent launch.  The grouped path reads the first own
-    // token of each sequence, written by the prefix kernel, so it waits now.
-    // Otherwise the prologue below (length scan, row staging, first queries)
-    // reads only this call's inputs (lengths, block tables, queries) and
-    // writes only shared memory, so it may overlap the previous kernel (the
-    // previous call's merge); the wait comes before the first access to the
-    // cache (new-token stores, then TMA) and to the workspace.  Kernels that
-    // let this one start early must not write those inputs after their trigger.
-    if (grouped) grid_dependency_wait();
+    // Programmatic dependent launch.  The prologue below (length scan, row
+    // staging, first queries) reads only this call's inputs (lengths, block
+    // tables, queries) and writes only shared memory, so it may overlap the
+    // previous kernel (the previous call's tail); the wait comes before the
+    // first access to the cache (new-token stores, then TMA) and to the
+    // workspace.  Kernels that let this one start early must not write those
+    // inputs after their trigger.
     grid_launch_dependents();
 
     const int S = a.num_seqs, Hkv = a.num_kv_heads;
@@ -1104,11 +1089,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int raw = a.seq_lens[sq];
             if ((raw < 0 || raw > cap) && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
             const int len = clamp_len(raw, cap);
-            // grouped: the shared prefix was attended by the prefix kernel
-            const int t0 = grouped ? min(max(a.seq_tok0[sq], 0), len) : 0;
-            if (grouped) toff[sq] = t0;
-            v = Hkv * ((len - t0 + TT - 1) / TT);
-            my_max = max(my_max, (len - t0 + TT - 1) / TT);
+            v = Hkv * ((len + TT - 1) / TT);
+            my_max = max(my_max, (len + TT - 1) / TT);
         }
         int x = v;  // inclusive warp scan
 #pragma unroll
@@ -1129,7 +1111,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     for (int sh = 16; sh > 0; sh >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, sh));
     if (lane == 0) atomicMax(&seg_max, my_max);
     __syncthreads();
-    if (a.flags) {
+    {
         // No merge kernel follows: this kernel writes the zero rows of empty
         // contexts (no tile, hence no piece).  CTA c takes sequences c, c + grid, ...
         bool mine = false;
@@ -1152,8 +1134,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     // hold at least ceil(seg_max / (own_slots - 1)) tiles; that is at most
     // kMinTilesPerCta, and less when every segment is short, which spreads
     // many short contexts over more warps.
-    const int own_slots = grouped ? a.prefix_slot : a.max_parts;
-    const int64_t parts = balanced_parts(T, seg_max, own_slots, (int64_t)gridDim.x * NW);
+    const int64_t parts = balanced_parts(T, seg_max, a.max_parts, (int64_t)gridDim.x * NW);
     const int64_t gw0 = (int64_t)blockIdx.x * NW;
     if (T == 0 || gw0 >= parts) return;
     const int64_t cta_lo = gw0 * T / parts;
@@ -1225,7 +1206,6 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int u = 0; u < kPer; ++u) {
             if (sq[u] < 0) continue;
             const int32_t *bt = a.block_tables + (int64_t)sq[u] * a.max_blocks;
-            if (grouped) tl[u] += toff[sq[u]] / kTile;  // token offsets are tile aligned
             // the tile's tokens lie inside the clamped length, hence inside the table
             const int lb0 = min(tl[u] * TT / B, a.max_blocks - 1);
             const int lb1 = min((tl[u] * TT + boxh) / B, a.max_blocks - 1);
@@ -1270,7 +1250,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     __syncthreads();
 
     if (gw >= parts) return;  // no CTA-wide barrier follows
-    if (!grouped) grid_dependency_wait();
+    grid_dependency_wait();
     const int ntiles = (int)(hi - lo);
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
 
@@ -1377,8 +1357,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int2 y = ycache[i];
             return TileRows{y.x, y.y, F8 ? mcache[i] : (mcache[i] & 0xffffu)};
         }
-        return tile_rows<TT>(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap),
-                             grouped ? toff[c.seq] : 0);
+        return tile_rows<TT>(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap));
     };
 
     // k-th tile in walk order
@@ -1437,33 +1416,25 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 issue(k + NS, buf);
             }
         }
-        // a grouped sequence's own part is always a partial: the prefix joins it in the merge
-        const bool whole = pa == seg.seg_start && pb == seg_end && !(grouped && toff[seg.seq] > 0);
+        const bool whole = pa == seg.seg_start && pb == seg_end;
         const int64_t w0 = share_owner(seg.seg_start, T, parts);
         store_piece<D>(a, acc, dead, seg, whole, (int)(gw - w0), lane, F8 ? a.f8_vscale : 1.f);
-        if (a.flags) {
-            if (!whole) {
-                // Split segment: the warp holding its first tile merges it (the
-                // segment is the last of that warp's share, so the merge waits
-                // for nothing but pieces processed at the start of other shares);
-                // every other piece announces its partial.
-                const int n = (int)(share_owner(seg_end - 1, T, parts) - w0 + 1);
-                const int64_t sg = (int64_t)seg.seq * Hkv + seg.kvh;
-                if (gw == w0) {
-                    merge_seg = sg;
-                    merge_n = n;
-                } else {
-                    fence_acq_rel_gpu();
-                    __syncwarp();
-                    if (lane == 0)
-                        *reinterpret_cast<volatile unsigned long long *>(a.flags + sg * a.max_parts + (gw - w0)) =
-                            a.tag;
-                }
+        if (!whole) {
+            // Split segment: the warp holding its first tile merges it (the
+            // segment is the last of that warp's share, so the merge waits for
+            // nothing but pieces processed at the start of other shares); every
+            // other piece announces its partial.
+            const int n = (int)(share_owner(seg_end - 1, T, parts) - w0 + 1);
+            const int64_t sg = (int64_t)seg.seq * Hkv + seg.kvh;
+            if (gw == w0) {
+                merge_seg = sg;
+                merge_n = n;
+            } else {
+                fence_acq_rel_gpu();
+                __syncwarp();
+                if (lane == 0)
+                    *reinterpret_cast<volatile unsigned long long *>(a.flags + sg * a.max_parts + (gw - w0)) = a.tag;
             }
-        } else if (lane == 0 && pa == seg.seg_start) {
-            // the warp holding a segment's first tile records its number of pieces
-            const int64_t w1 = share_owner(seg_end - 1, T, parts);
-            a.pieces[(int64_t)seg.seq * a.num_kv_heads + seg.kvh] = (int)(w1 - w0 + 1);
         }
         if (kend >= ntiles) break;
         seg = nxt;
@@ -1618,12 +1589,10 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const DecodeArgs a
 }
 
 // ---------------------------------------------------------------------------
-// Partition merge: out = sum_j e^{m_j - M} o_j / sum_j e^{m_j - M} l_j
-// PIECES = false: partials of fixed partitions, ceil(len / P) of them.
-// PIECES = true: partials of the balanced split, counted in a.pieces; this
-// kernel also writes the zero rows of empty contexts on that path.
+// Partition merge (fixed partitions): out = sum_j e^{m_j - M} o_j / sum_j
+// e^{m_j - M} l_j over the ceil(len / P) partials of each (sequence, head).
 // ---------------------------------------------------------------------------
-template <typename T, int D, bool LOG2, bool PIECES>
+template <typename T, int D, bool LOG2>
 __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) {
     constexpr int E = D / 32;  // consecutive head_dim elements per lane
     constexpr int U = 8;       // partials whose rows are loaded together
@@ -1640,16 +1609,9 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     const float *pm = a.part_m + row * a.max_parts;
     const float *pl = a.part_l + row * a.max_parts;
     const float *po = a.part_o + row * a.max_parts * D + lane * E;
-    // issue the length, the piece counts and the first 32 (max, sum) pairs at
-    // once; pairs past the piece count are masked below
+    // issue the length and the first 32 (max, sum) pairs at once; pairs past
+    // the partition count are masked below
     const int raw_len = a.seq_lens[seq];
-    int nparts = 0, tok0 = 0, npre_given = -1;
-    if (PIECES) {
-        const int h = (int)(row - (int64_t)seq * a.num_heads);
-        nparts = a.pieces[(int64_t)seq * a.num_kv_heads + h / a.group];
-        if (a.seq_tok0) tok0 = a.seq_tok0[seq];
-        if (a.prefix_pieces) npre_given = a.prefix_pieces[(int64_t)seq * a.num_kv_heads + h / a.group];
-    }
     float mj = -INFINITY, lj = 0.f;
     if (lane < a.max_parts) {
         mj = pm[lane];
@@ -1657,44 +1619,21 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
     }
     const int len = raw_len < 0 ? 0 : (raw_len > cap ? cap : raw_len);
     T *dst = static_cast<T *>(a.out) + row * D + lane * E;
-    int npre = 0;  // grouped: prefix partials at slots prefix_slot ...
-    if (PIECES) {
-        if (len == 0) {
-#pragma unroll
-            for (int e = 0; e < E; ++e) store_out(dst + e, 0.f);
-            return;
-        }
-        tok0 = min(max(tok0, 0), len);
-        if (tok0 > 0) {
-            npre = npre_given >= 0 ? npre_given : (tok0 + a.prefix_part - 1) / a.prefix_part;
-            npre = min(max(npre, 0), a.max_parts - a.prefix_slot);
-            if (len == tok0) nparts = 0;  // nothing of its own: no piece was written
-        }
-        nparts = min(max(nparts, 0), a.seq_tok0 ? a.prefix_slot : a.max_parts);
-    } else {
-        nparts = (len + a.partition_size - 1) / a.partition_size;
-    }
-    if (npre == 0 && nparts <= 1) return;
-    const int total = nparts + npre;
-    // partial j: own piece j, then prefix partition j - nparts
-    auto slot = [&](int j) { return j < nparts ? j : a.prefix_slot + (j - nparts); };
-    if (npre > 0 && lane < total && lane >= nparts) {
-        mj = pm[slot(lane)];
-        lj = pl[slot(lane)];
-    }
+    const int total = (len + a.partition_size - 1) / a.partition_size;
+    if (total <= 1) return;
     if (lane >= total) {
         mj = -INFINITY;
         lj = 0.f;
     }
     float M = mj;
-    for (int j = lane + 32; j < total; j += 32) M = fmaxf(M, pm[slot(j)]);
+    for (int j = lane + 32; j < total; j += 32) M = fmaxf(M, pm[j]);
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
     if (M == -INFINITY) M = 0.f;  // only if every block was invalid (flagged)
     auto ex = [&](float x) { return x == -INFINITY ? 0.f : (LOG2 ? exp2f(x - M) : expf(x - M)); };
     const float wl = ex(mj);  // weight of partial `lane`
     float lsum = wl * lj;
-    for (int j = lane + 32; j < total; j += 32) lsum += ex(pm[slot(j)]) * pl[slot(j)];
+    for (int j = lane + 32; j < total; j += 32) lsum += ex(pm[j]) * pl[j];
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, sh);
 
@@ -1705,7 +1644,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
         float v[U][E];
 #pragma unroll
         for (int u = 0; u < U; ++u) {  // U independent row loads in flight
-            const int j = slot(j0 + u < total ? j0 + u : total - 1);
+            const int j = j0 + u < total ? j0 + u : total - 1;
 #pragma unroll
             for (int e = 0; e < E; ++e) v[u][e] = po[(int64_t)j * D + e];
         }
@@ -1713,7 +1652,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeArgs a) 
         for (int u = 0; u < U; ++u) {
             const int j = j0 + u;
             const float wsh = __shfl_sync(0xffffffffu, wl, j & 31);
-            const float w = j >= total ? 0.f : (j < 32 ? wsh : ex(pm[slot(j)]));
+            const float w = j >= total ? 0.f : (j < 32 ? wsh : ex(pm[j]));
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[e] += w * v[u][e];
         }
@@ -1731,21 +1670,18 @@ constexpr int kDefaultPartition = 512;
 constexpr int kMaxBalancedSeqs = 8192;
 
 struct WorkspaceLayout {
-    size_t o_off, m_off, l_off, pieces_off, flags_off, total;
+    size_t o_off, m_off, l_off, flags_off, total;
 };
 
-// parts = partial slots per (sequence, query head); `pieces` adds the
-// per-segment piece counts of the balanced path.
-static WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t D, int64_t parts, bool pieces) {
+// parts = partial slots per (sequence, query head); `flags` adds the ready
+// flags of the balanced path's in-kernel merge, 8 bytes per slot.
+static WorkspaceLayout workspace_layout(int64_t S, int64_t Hq, int64_t D, int64_t parts, bool flags) {
     WorkspaceLayout w;
     w.o_off = 0;
     w.m_off = round256((size_t)(S * Hq * parts * D * 4));
     w.l_off = w.m_off + round256((size_t)(S * Hq * parts * 4));
-    w.pieces_off = w.l_off + round256((size_t)(S * Hq * parts * 4));
-    // balanced path: piece counts (merge kernel), and the ready flags of the
-    // partial slots (merge in the attention kernel), 8 bytes per slot
-    w.flags_off = w.pieces_off + (pieces ? round256((size_t)(S * Hq * 4)) : 0);
-    w.total = w.flags_off + (pieces ? round256((size_t)(S * Hq * parts * 8)) : 0);
+    w.flags_off = w.l_off + round256((size_t)(S * Hq * parts * 4));
+    w.total = w.flags_off + (flags ? round256((size_t)(S * Hq * parts * 8)) : 0);
     return w;
 }
 
@@ -1784,8 +1720,8 @@ template <int D, int NW, int NS>
 static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
     static bool done[128] = {};
     auto kern = decode_bf16_streamk_kernel<D, NW, NS>;
-    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, true).total, done)) return PKV_ERR_CUDA;
-    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, a.seq_tok0 != nullptr).total;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs).total;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
         per_sm < 1)
@@ -1830,8 +1766,8 @@ static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
     static bool done[128] = {};
     auto kern = decode_bf16_streamk_kernel<D, NW, NS, true>;
     constexpr int stage = TileBytes<D, true>::kStage;
-    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, false, stage).total, done)) return PKV_ERR_CUDA;
-    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, false, stage).total;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, stage).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, stage).total;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
         per_sm < 1)
@@ -1852,13 +1788,13 @@ static pkv_status dispatch_simt(const DecodeArgs &a, dim3 grid, cudaStream_t st)
     return launch_pdl(decode_simt_kernel<T, D, 4>, grid, dim3(128), 0, st, a);
 }
 
-template <typename T, int D, bool LOG2, bool PIECES>
+template <typename T, int D, bool LOG2>
 static pkv_status launch_reduce(const DecodeArgs &a, cudaStream_t st) {
     const int64_t rows = (int64_t)a.num_seqs * a.num_heads;
     const unsigned blocks = (unsigned)((rows + 3) / 4);
     DecodeArgs m = a;
     m.merge_trigger = (int64_t)blocks <= (int64_t)sm_count() ? 1 : 0;
-    return launch_pdl(decode_reduce_kernel<T, D, LOG2, PIECES>, dim3(blocks), dim3(128), 0, st, m);
+    return launch_pdl(decode_reduce_kernel<T, D, LOG2>, dim3(blocks), dim3(128), 0, st, m);
 }
 
 }  // namespace pkv
@@ -1974,7 +1910,6 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
         a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
         a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
         a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
-        a.pieces = partition_size == 0 ? reinterpret_cast<int *>(ws + lay.pieces_off) : nullptr;
         if (balanced) {  // the attention kernel merges split contexts itself
             a.flags = reinterpret_cast<unsigned long long *>(ws + lay.flags_off);
             a.tag = next_call_tag();
@@ -1990,13 +1925,13 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
     } else if (dtype == PKV_BF16) {
         rc = head_dim == 128 ? dispatch_bf16<128>(a, grid, st) : dispatch_bf16<64>(a, grid, st);
         if (rc == PKV_OK && parts > 1)
-            rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true, false>(a, st)
-                                 : launch_reduce<__nv_bfloat16, 64, true, false>(a, st);
+            rc = head_dim == 128 ? launch_reduce<__nv_bfloat16, 128, true>(a, st)
+                                 : launch_reduce<__nv_bfloat16, 64, true>(a, st);
     } else {
         rc = head_dim == 128 ? dispatch_simt<float, 128>(a, grid, st) : dispatch_simt<float, 64>(a, grid, st);
         if (rc == PKV_OK && parts > 1)
-            rc = head_dim == 128 ? launch_reduce<float, 128, false, false>(a, st)
-                                 : launch_reduce<float, 64, false, false>(a, st);
+            rc = head_dim == 128 ? launch_reduce<float, 128, false>(a, st)
+                                 : launch_reduce<float, 64, false>(a, st);
     }
     return rc;
 }
@@ -2065,7 +2000,6 @@ static pkv_status decode_fp8_impl(void *out, const void *q, const void *k_cache,
     a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
     a.part_m = reinterpret_cast<float *>(ws + lay.m_off);
     a.part_l = reinterpret_cast<float *>(ws + lay.l_off);
-    a.pieces = reinterpret_cast<int *>(ws + lay.pieces_off);
     a.flags = reinterpret_cast<unsigned long long *>(ws + lay.flags_off);
     a.tag = next_call_tag();
     a.max_parts = (int)slots;

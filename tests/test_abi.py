@@ -151,11 +151,10 @@ def test_workspace_size_formula():
     want = n * 128 * 4 + ((n * 4 + 255) // 256) * 256 * 2
     assert lib.paged_attention_workspace_size(8, 32, 128, 16000, 512) == want
     # partition_size 0: the balanced split, ceil(16000 / 256) + 1 = 64 slots per
-    # (sequence, head), one piece count per (sequence, head) and an 8-byte ready
-    # flag per slot
+    # (sequence, head) and an 8-byte ready flag per slot
     n0 = 8 * 32 * 64
     r = lambda x: (x + 255) // 256 * 256
     assert lib.paged_attention_workspace_size(8, 32, 128, 16000, 0) == \
-        n0 * 128 * 4 + 2 * r(n0 * 4) + r(8 * 32 * 4) + r(n0 * 8)
+        n0 * 128 * 4 + 2 * r(n0 * 4) + r(n0 * 8)
     assert lib.paged_attention_workspace_size(8, 32, 128, 300, 0) > 0  # may split anywhere
     assert lib.paged_attention_workspace_size(8, 32, 128, 16000, 24) == 0    # invalid partition
