@@ -453,6 +453,25 @@ PKV_EXPORT pkv_status paged_attention_decode_noalloc(void *out, const void *q, c
  */
 PKV_EXPORT pkv_status pkv_read_device_errors(uint32_t *flags_out, int clear, void *stream);
 
+/*
+ * pkv_bounded_wait_check -- failure-detection check of the two bounded waits
+ * the attention kernels use, so that a test can make each run out without a
+ * GPU fault.  One warp runs, on `stream`:
+ *   1. the merger's flag wait: polls the n_flags 8-byte words at `flags`
+ *      (device memory, read only; skipped when n_flags == 0) until all hold
+ *      `tag`, at most `polls` rounds;
+ *   2. the mbarrier wait: waits for phase 0 of a fresh shared-memory mbarrier
+ *      of one arrival, at most `polls` polls; the warp arrives first only when
+ *      arrive != 0.
+ * A wait that runs out sets PKV_DEVERR_TIMEOUT in the device error word
+ * (pkv_read_device_errors) and the kernel goes on and returns; the context
+ * stays usable.  The attention kernels run the same two waits with a limit of
+ * 2^22 polls.  PKV_ERR_INVALID for n_flags < 0, a null `flags` with
+ * n_flags > 0, or polls == 0.
+ */
+PKV_EXPORT pkv_status pkv_bounded_wait_check(const uint64_t *flags, int n_flags, uint64_t tag, int arrive,
+                                             uint32_t polls, void *stream);
+
 /* ------------------------------------------------------------------------
  * Host block allocator.
  *

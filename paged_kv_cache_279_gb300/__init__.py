@@ -369,6 +369,19 @@ def read_device_errors(clear: bool = True, stream=None) -> int:
     return int(flags.value)
 
 
+def bounded_wait_check(flags: Optional[torch.Tensor], tag: int, arrive: bool, polls: int,
+                       stream=None) -> None:
+    """Runs the attention kernels' two bounded waits once with `polls` as the
+    limit: the flag wait on the int64 words of `flags` (None: skipped) for
+    `tag`, then an mbarrier wait that completes only with `arrive`.  A wait
+    that runs out sets DEVERR_TIMEOUT (read_device_errors)."""
+    ptr, n = 0, 0
+    if flags is not None:
+        ptr, n = _dev(flags, "flags", torch.int64, 1), flags.numel()
+    _check(_lib.load().pkv_bounded_wait_check(ptr, n, int(tag), int(bool(arrive)), int(polls), _stream(stream)),
+           "pkv_bounded_wait_check")
+
+
 class BlockAllocator:
     """Host block allocator (C++): free stack, block tables, refcounts, CoW."""
 

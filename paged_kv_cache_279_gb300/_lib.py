@@ -55,6 +55,7 @@ SIGNATURES = {
     "block_copy": (c_int, [P(c_void_p), P(c_void_p), c_int, c_void_p, c_int, c_int, c_size_t,
                            c_void_p]),
     "pkv_read_device_errors": (c_int, [P(c_uint32), c_int, c_void_p]),
+    "pkv_bounded_wait_check": (c_int, [c_void_p, c_int, ctypes.c_uint64, c_int, c_uint32, c_void_p]),
     "block_allocator_create": (c_void_p, [c_int, c_int]),
     "block_allocator_destroy": (None, [c_void_p]),
     "block_allocator_add_seq": (c_int, [c_void_p, c_int64, c_int64]),

@@ -1038,8 +1038,10 @@ __device__ __forceinline__ void merge_segment(const float *part_o, const float *
 // warp holding a split segment's first tile (its share's last segment) merges
 // it once the other pieces -- processed at the start of their own shares --
 // have flagged their partials.  That is the only wait between warps; it is
-// bounded, and every warp it waits for is already resident (the grid is one
-// wave) and never waits itself.
+// bounded, and every warp it waits for is resident (the grid is one wave,
+// launched cooperatively, so a grid that cannot be resident at once is refused
+// at launch) and never waits itself.  A merge that gives up writes NaN rows and
+// sets PKV_DEVERR_TIMEOUT.
 //
 // F8: the cache holds E4M3 codes (K rows, V transposed per block); tiles are
 // attended by attend_tile_f8 and the queries are loaded by load_q_f16.
@@ -1453,22 +1455,18 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         unsigned long long *fl = a.flags + merge_seg * a.max_parts;
         fence_acq_rel_gpu();  // this warp's own partial (slot 0), before it is read back
         __syncwarp();
-        bool ready = false;
-        for (uint32_t it = 0; it < kWaitLimit && !ready; ++it) {
-            bool mine = true;
-            for (int j = 1 + lane; j < merge_n; j += 32) mine = mine && ld_volatile_u64(fl + j) == a.tag;
-            ready = __all_sync(0xffffffffu, mine);
-            if (!ready) __nanosleep(64);
-        }
-        if (!ready && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-        // each lane saw some of the flags: acquire, then order every lane's
-        // reads after every lane's acquire
-        fence_acq_rel_gpu();
-        __syncwarp();
+        const bool ready = wait_flags_bounded(fl + 1, merge_n - 1, a.tag, lane);
         const int sq = (int)(merge_seg / Hkv), kvh = (int)(merge_seg - (int64_t)sq * Hkv);
-        merge_segment<D, NS * Lay::kStage / 32>(a.part_o, a.part_m, a.part_l, static_cast<__nv_bfloat16 *>(a.out),
-                                                (int64_t)sq * a.num_heads + kvh * a.group, a.group, a.max_parts,
-                                                merge_n, lane, smem_u32(ring));
+        const int64_t row0 = (int64_t)sq * a.num_heads + kvh * a.group;
+        if (ready) {
+            merge_segment<D, NS * Lay::kStage / 32>(a.part_o, a.part_m, a.part_l, static_cast<__nv_bfloat16 *>(a.out),
+                                                    row0, a.group, a.max_parts, merge_n, lane, smem_u32(ring));
+        } else {
+            // a piece never came: NaN rows rather than a merge over stale slots
+            if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.out) + row0 * D;
+            for (int i = lane; i < a.group * D; i += 32) o[i] = __ushort_as_bfloat16((unsigned short)0x7fc0);
+        }
         for (int j = 1 + lane; j < merge_n; j += 32) fl[j] = 0ull;
     }
 }
@@ -1730,7 +1728,9 @@ static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
     if (sms < 1) return PKV_ERR_CUDA;
     CUtensorMap mk, mv;
     if (!make_cache_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
-    return launch_pdl(kern, dim3((unsigned)(sms * per_sm)), dim3(NW * 32), smem, st, mk, mv, a);
+    // every CTA resident at once: the in-kernel merge waits on other CTAs
+    static std::atomic<int> mode{-1};
+    return launch_resident(mode, kern, dim3((unsigned)(sms * per_sm)), dim3(NW * 32), smem, st, mk, mv, a);
 }
 
 template <int D>
@@ -1776,7 +1776,9 @@ static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
     if (sms < 1) return PKV_ERR_CUDA;
     CUtensorMap mk, mv;
     if (!make_f8_maps(a, D, &mk, &mv)) return PKV_ERR_CUDA;
-    return launch_pdl(kern, dim3((unsigned)(sms * per_sm)), dim3(NW * 32), smem, st, mk, mv, a);
+    // every CTA resident at once: the in-kernel merge waits on other CTAs
+    static std::atomic<int> mode{-1};
+    return launch_resident(mode, kern, dim3((unsigned)(sms * per_sm)), dim3(NW * 32), smem, st, mk, mv, a);
 }
 
 static pkv_status dispatch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
@@ -2143,6 +2145,38 @@ PKV_API pkv_status paged_attention_decode_noalloc(void *out, const void *q, cons
                                   num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                   num_blocks, max_seq_len, scale, P, scratch,
                                   need > 0 ? PKV_NOALLOC_SCRATCH_BYTES : 0, dtype, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Failure detection: the two bounded waits of the attention kernels, run once
+// by one warp with a caller-chosen poll limit.
+// ---------------------------------------------------------------------------
+namespace pkv {
+__global__ void __launch_bounds__(32) bounded_wait_kernel(const unsigned long long *flags, int n, unsigned long long tag,
+                                                          int arrive, uint32_t polls, unsigned int *err) {
+    __shared__ uint64_t bar;
+    const int lane = threadIdx.x;
+    if (lane == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (n > 0 && !wait_flags_bounded(flags, n, tag, lane, polls) && lane == 0) flag_error(err, PKV_DEVERR_TIMEOUT);
+    if (lane == 0) {
+        if (arrive) mbar_arrive(&bar);
+        if (!mbar_wait_bounded(&bar, 0u, polls)) flag_error(err, PKV_DEVERR_TIMEOUT);
+    }
+}
+}  // namespace pkv
+
+PKV_API pkv_status pkv_bounded_wait_check(const uint64_t *flags, int n_flags, uint64_t tag, int arrive, uint32_t polls,
+                                          void *stream) {
+    if (n_flags < 0 || (n_flags > 0 && !flags) || polls < 1) return PKV_ERR_INVALID;
+    unsigned int *err = device_error_word();
+    if (!err) return PKV_ERR_CUDA;
+    bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const unsigned long long *>(flags), n_flags, (unsigned long long)tag, arrive, polls, err);
+    return launch_status();
 }
 
 // ---------------------------------------------------------------------------

@@ -151,6 +151,27 @@ inline pkv_status launch_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? launch_status() : PKV_ERR_CUDA;
 }
 
+// Launch of a kernel whose CTAs wait on one another: cooperative (every CTA
+// resident at once, else the launch is refused) together with programmatic
+// serialization where the driver takes both, else cooperative alone.  `mode`
+// keeps, per kernel, the first combination that launched (-1: not tried yet,
+// 0: both attributes, 1: cooperative only).
+template <typename... KArgs, typename... Args>
+inline pkv_status launch_resident(std::atomic<int> &mode, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t st, Args... args) {
+    int m = mode.load();
+    if (m >= 0)
+        return m == 0 ? launch_pdl_ex(kern, grid, block, smem, st, true, args...)
+                      : launch_coop(kern, grid, block, smem, st, args...);
+    if (launch_pdl_ex(kern, grid, block, smem, st, true, args...) == PKV_OK) {
+        mode.store(0);
+        return PKV_OK;
+    }
+    (void)cudaGetLastError();  // the refused combination's error, before the next attempt
+    const pkv_status rc = launch_coop(kern, grid, block, smem, st, args...);
+    if (rc == PKV_OK) mode.store(1);
+    return rc;
+}
 
 __device__ __forceinline__ void flag_error(unsigned int *err, unsigned int bits) {
     if (err) atomicOr(err, bits);

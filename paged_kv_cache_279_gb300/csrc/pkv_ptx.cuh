@@ -62,9 +62,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Polls a bounded number of times; false means the wait gave up.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Polls at most `limit` times; false means the wait gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -123,6 +123,24 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
     unsigned long long v;
     asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
+}
+
+// The merger's wait (warp-collective): polls flags[0 .. n) until every one
+// holds `tag`, at most `limit` rounds.  Returns false if it gave up.  Ends with
+// an acquire fence and a warp barrier, so that every lane's later reads of the
+// partials are ordered after every lane's flag reads.
+__device__ __forceinline__ bool wait_flags_bounded(const unsigned long long *flags, int n, unsigned long long tag,
+                                                   int lane, uint32_t limit = kWaitLimit) {
+    bool got = false;
+    for (uint32_t it = 0; it < limit && !got; ++it) {
+        bool mine = true;
+        for (int k = lane; k < n; k += 32) mine = mine && ld_volatile_u64(flags + k) == tag;
+        got = __all_sync(0xffffffffu, mine);
+        if (!got) __nanosleep(64);
+    }
+    fence_acq_rel_gpu();
+    __syncwarp();
+    return got;
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {

@@ -1028,18 +1028,8 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             // merger: this piece holds the context's first tile and is the
                             // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
                             const int n = pc.w1 - pc.w0;
-                            got = false;
-                            for (uint32_t it = 0; it < kWaitLimit && !got; ++it) {
-                                bool mine = true;
-                                for (int k = lane; k < n; k += 32)
-                                    mine = mine && ld_volatile_u64(a.flags + pc.w0 + 1 + k) == a.tag;
-                                got = __all_sync(0xffffffffu, mine);
-                                if (!got) __nanosleep(64);
-                            }
+                            got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
                             if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                            // each lane saw some flags: acquire, then order every lane's reads after them
-                            fence_acq_rel_gpu();
-                            __syncwarp();
                             float Mt = M;
                             if (live)
                                 for (int w = pc.w0 + 1; w <= pc.w1; ++w)
@@ -1183,25 +1173,9 @@ static pkv_status launch(const Args &a, const void *k_cache, const void *v_cache
     const int sms = sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
     const int grid = std::min(sms, kMaxCtas);
-    // Cooperative launch (every CTA resident at once: the in-kernel merge waits
-    // on other CTAs) together with programmatic launch where the driver takes
-    // both; the first combination that launches is kept for the process.
-    static std::atomic<int> mode{-1};  // 0: cooperative + programmatic, 1: cooperative only
-    int m = mode.load();
-    if (m < 0) {
-        for (m = 0; m < 2; ++m) {
-            const pkv_status rc = m == 0 ? launch_pdl_ex(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, true, mk, mv, a)
-                                         : launch_coop(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, mk, mv, a);
-            if (rc == PKV_OK) {
-                mode.store(m);
-                return rc;
-            }
-            (void)cudaGetLastError();  // the refused combination's error, before the next attempt
-        }
-        return PKV_ERR_CUDA;
-    }
-    return m == 0 ? launch_pdl_ex(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, true, mk, mv, a)
-                  : launch_coop(kern, dim3((unsigned)grid), dim3(kThreads), smem, st, mk, mv, a);
+    // every CTA resident at once: the in-kernel merge waits on other CTAs
+    static std::atomic<int> mode{-1};
+    return launch_resident(mode, kern, dim3((unsigned)grid), dim3(kThreads), smem, st, mk, mv, a);
 }
 
 static pkv_status run(Args a, int D, int total_units, const void *k_cache, const void *v_cache, cudaStream_t st) {

@@ -67,6 +67,10 @@ def test_host_validation_rejects_before_launch():
     flags = ctypes.c_uint32()
     assert lib.pkv_read_device_errors(None, 0, None) == pkv.PKV_ERR_INVALID
     del flags
+    # the bounded-wait check: bad arguments never reach the device
+    assert lib.pkv_bounded_wait_check(None, 4, 7, 1, 100, None) == pkv.PKV_ERR_INVALID
+    assert lib.pkv_bounded_wait_check(None, -1, 7, 1, 100, None) == pkv.PKV_ERR_INVALID
+    assert lib.pkv_bounded_wait_check(None, 0, 7, 1, 0, None) == pkv.PKV_ERR_INVALID
 
 
 def test_fp8_host_validation_rejects_before_launch():
