@@ -818,13 +818,15 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     copy from a pinned buffer carries the step's queries, new K/V, lengths and
     tables (and the groups of a beam batch), the library call stores the new
     tokens and attends, and one D2H copy brings the output back; the host
-    waits for it before the next step."""
+    waits for it before the next step.  The copy in, the call and the copy out
+    are replayed as one CUDA graph; the host's allocator work is timed too."""
     from paged_kv_cache_279_gb300 import _lib
     lib = _lib.load()
     steps = args.steps
-    b = make_batch(pkv, shape, args, seed + 77, device, reserve_tokens=steps + args.warmup + 1)
+    n_tok = steps + max(1, args.warmup) + 1  # tokens the loop appends per sequence
+    b = make_batch(pkv, shape, args, seed + 77, device, reserve_tokens=n_tok + 1)
     S, Hq, Hkv, D, B = len(b.lens), shape.num_heads, shape.num_kv_heads, shape.head_dim, shape.block_size
-    cap = b.max_blocks + (steps + args.warmup) // B + 2
+    cap = b.max_blocks + n_tok // B + 2
     max_seq_len = cap * B
     grouped = b.group_offsets is not None
     fp8 = args.kv == "fp8"
@@ -866,7 +868,6 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     kc, vc = b.k_cache.data_ptr(), b.v_cache.data_ptr()
     NB = b.num_blocks
     seq_ids = np.ascontiguousarray(b.seq_ids, dtype=np.int64)
-    rows = np.arange(S)
 
     def call():
         if fp8:
@@ -888,26 +889,40 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     d2h = h_out.numel() * h_out.element_size()
     ms, byts = [], []
     base_unique, base_lens = b.unique_bytes, list(b.lens)
+
+    def host_step():
+        # the allocator appends one token per sequence and updates the pinned
+        # tables and lengths in place (only entries that changed)
+        st, _, pairs = b.alloc.append_step(seq_ids, h_tab, h_lens)
+        if st != 0 or len(pairs):
+            raise RuntimeError("allocator could not serve the step")
+
+    def device_step():
+        d_pack.copy_(h_pack, non_blocking=True)
+        rc = call()
+        if rc != 0:
+            raise RuntimeError(f"library call failed with status {rc}")
+        h_out.copy_(out, non_blocking=True)
+
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_eager = max(1, args.warmup)
     with torch.cuda.stream(stream):
-        for i in range(args.warmup + steps):
+        for _ in range(n_eager):  # eager steps: the library's one-time host setup
+            host_step()
+            device_step()
+        stream.synchronize()
+        # the step's copy in, library call and copy out as one graph; every
+        # replay copies the pinned buffer's current contents
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            device_step()
+        for i in range(steps + 1):
             ev0.record(stream)
-            st, slots, pairs = b.alloc.append_slots(seq_ids)
-            if st != 0 or len(pairs):
-                raise RuntimeError("allocator could not serve the step")
-            pos_new = h_lens.astype(np.int64)  # position of each new token
-            h_lens += 1
-            took = (pos_new % B) == 0          # a new block: its id goes into the table
-            if took.any():
-                h_tab[rows[took], pos_new[took] // B] = (slots[took] // B).astype(np.int32)
-            d_pack.copy_(h_pack, non_blocking=True)
-            rc = call()
-            if rc != 0:
-                raise RuntimeError(f"library call failed with status {rc}")
-            h_out.copy_(out, non_blocking=True)
+            host_step()
+            graph.replay()
             ev1.record(stream)
             ev1.synchronize()  # the host reads the step's result
-            if i >= args.warmup:
+            if i >= 1:  # the first replay uploads the graph
                 ms.append(ev0.elapsed_time(ev1))
                 # unique bytes: what the batch started with plus the tokens added since
                 byts.append(base_unique + kv_bytes(h_lens.tolist(), shape, 1 if fp8 else None) -
@@ -923,7 +938,7 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     total_b = sum_over_ranks(sum(byts), world, device)
     return {"value": round(total_b / total_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * total_s / steps, 4),
-            "copies_per_step": {"h2d": 1, "d2h": 1}}
+            "copies_per_step": {"h2d": 1, "d2h": 1}, "graph": True}
 
 
 def multi_token_batch(pkv, args, seed, device):

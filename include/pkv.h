@@ -514,6 +514,19 @@ PKV_EXPORT pkv_status block_allocator_append_slots(pkv_allocator *a, const int64
                                         int64_t *slots_out, int64_t *cow_pairs_out,
                                         int *n_cow_out);
 
+/* append_slots plus the incremental update of the caller's dense block
+ * tables, for a serving loop that keeps them between steps: tables is host
+ * int32 [n][cap] (row i belongs to seqs[i], as block_allocator_block_tables
+ * wrote it) and seq_lens host int32 [n].  Per sequence, only the entry of the
+ * block holding the new token is written (the fresh block, the CoW
+ * destination, or the same id again) and seq_lens[i] becomes the new token
+ * count; nothing else in the row changes, so a row that block_tables wrote
+ * before stays equal to what it would write now.  PKV_ERR_INVALID (nothing
+ * changed) also when a new token's block index would be >= cap. */
+PKV_EXPORT pkv_status block_allocator_append_step(pkv_allocator *a, const int64_t *seqs, int n,
+                                                  int32_t *tables, int cap, int32_t *seq_lens,
+                                                  int64_t *slots_out, int64_t *cow_pairs_out, int *n_cow_out);
+
 /* `child` starts as a copy of `parent` that shares every block (refcount + 1). */
 PKV_EXPORT pkv_status block_allocator_fork(pkv_allocator *a, int64_t parent, int64_t child);
 

@@ -442,6 +442,24 @@ class BlockAllocator:
                                                     ctypes.byref(ncow))
         return st, slots, pairs[:ncow.value]
 
+    def append_step(self, seqs, tables: np.ndarray, lens: np.ndarray):
+        """append_slots that also updates the dense tables (int32 [n, cap],
+        row i for seqs[i]) and lens (int32 [n]) in place, writing only the
+        entry of each new token's block.  Both arrays must be C-contiguous
+        (pinned host views are fine).  Returns (status, slots, cow_pairs)."""
+        ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int64))
+        if (tables.dtype != np.int32 or lens.dtype != np.int32 or tables.ndim != 2 or
+                not tables.flags.c_contiguous or not lens.flags.c_contiguous or
+                tables.shape[0] != len(ids) or lens.shape[0] != len(ids)):
+            raise ValueError("tables must be int32 [n, cap] and lens int32 [n], C-contiguous")
+        slots = np.full(len(ids), -1, dtype=np.int64)
+        pairs = np.empty((max(1, len(ids)), 2), dtype=np.int64)
+        ncow = ctypes.c_int(0)
+        st = self._lib.block_allocator_append_step(self._h, ids.ctypes.data, len(ids), tables.ctypes.data,
+                                                   tables.shape[1], lens.ctypes.data, slots.ctypes.data,
+                                                   pairs.ctypes.data, ctypes.byref(ncow))
+        return st, slots, pairs[:ncow.value]
+
     def extend(self, seq: int, count: int):
         """Slots for ``count`` more tokens of seq (all or nothing).  Returns
         (status, slots int64 [count], cow_src, cow_dst)."""

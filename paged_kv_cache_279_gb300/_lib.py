@@ -67,6 +67,8 @@ SIGNATURES = {
     "block_allocator_append_slot": (c_int, [c_void_p, c_int64, P(c_int64), P(c_int32),
                                             P(c_int32)]),
     "block_allocator_append_slots": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P(c_int)]),
+    "block_allocator_append_step": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p,
+                                            c_void_p, P(c_int)]),
     "block_allocator_fork": (c_int, [c_void_p, c_int64, c_int64]),
     "block_allocator_free_seq": (c_int, [c_void_p, c_int64]),
     "block_allocator_block_table": (c_int, [c_void_p, c_int64, c_void_p, c_int, P(c_int)]),

@@ -163,10 +163,12 @@ pkv_status block_allocator_append_slot(pkv_allocator *a, int64_t seq, int64_t *s
     return PKV_OK;
 }
 
-pkv_status block_allocator_append_slots(pkv_allocator *a, const int64_t *seqs, int n,
-                                        int64_t *slots_out, int64_t *cow_pairs_out,
-                                        int *n_cow_out) {
-    if (!a || n < 0 || (n > 0 && (!seqs || !slots_out || !cow_pairs_out))) return PKV_ERR_INVALID;
+// One token for each of n distinct sequences; with `tables`, also the
+// incremental update of the caller's dense tables (row i of `cap` entries
+// belongs to seqs[i]): only the entry of the block that holds the new token is
+// written, and lens[i] gets the new token count.
+static pkv_status append_step(pkv_allocator *a, const int64_t *seqs, int n, int32_t *tables, int cap, int32_t *lens,
+                              int64_t *slots_out, int64_t *cow_pairs_out, int *n_cow_out) {
     // validate and count the blocks this step needs before changing anything
     int64_t need = 0;
     try {
@@ -176,6 +178,7 @@ pkv_status block_allocator_append_slots(pkv_allocator *a, const int64_t *seqs, i
             auto it = a->seqs.find(seqs[i]);
             if (it == a->seqs.end() || !seen.emplace(seqs[i], 1).second) return PKV_ERR_INVALID;
             const pkv_allocator::Seq &s = it->second;
+            if (tables && s.tokens / a->block_size >= cap) return PKV_ERR_INVALID;  // the row cannot hold it
             if (s.tokens % a->block_size == 0 || a->refcnt[s.table.back()] > 1) ++need;
         }
     } catch (...) {
@@ -185,16 +188,39 @@ pkv_status block_allocator_append_slots(pkv_allocator *a, const int64_t *seqs, i
     int ncow = 0;
     for (int i = 0; i < n; ++i) {
         int32_t src = -1, dst = -1;
-        const pkv_status st = block_allocator_append_slot(a, seqs[i], &slots_out[i], &src, &dst);
+        int64_t slot = -1;
+        const pkv_status st = block_allocator_append_slot(a, seqs[i], &slot, &src, &dst);
         if (st != PKV_OK) return st;  // unreachable after the checks above
+        slots_out[i] = slot;
         if (src >= 0) {
             cow_pairs_out[2 * ncow] = src;
             cow_pairs_out[2 * ncow + 1] = dst;
             ++ncow;
         }
+        if (tables) {
+            const int64_t tokens = a->seqs.find(seqs[i])->second.tokens;  // after the append
+            tables[(int64_t)i * cap + (tokens - 1) / a->block_size] = (int32_t)(slot / a->block_size);
+            if (lens) lens[i] = (int32_t)tokens;
+        }
     }
     if (n_cow_out) *n_cow_out = ncow;
     return PKV_OK;
+}
+
+pkv_status block_allocator_append_slots(pkv_allocator *a, const int64_t *seqs, int n,
+                                        int64_t *slots_out, int64_t *cow_pairs_out,
+                                        int *n_cow_out) {
+    if (!a || n < 0 || (n > 0 && (!seqs || !slots_out || !cow_pairs_out))) return PKV_ERR_INVALID;
+    return append_step(a, seqs, n, nullptr, 0, nullptr, slots_out, cow_pairs_out, n_cow_out);
+}
+
+pkv_status block_allocator_append_step(pkv_allocator *a, const int64_t *seqs, int n, int32_t *tables, int cap,
+                                       int32_t *seq_lens, int64_t *slots_out, int64_t *cow_pairs_out,
+                                       int *n_cow_out) {
+    if (!a || n < 0 || cap < 1 ||
+        (n > 0 && (!seqs || !tables || !seq_lens || !slots_out || !cow_pairs_out)))
+        return PKV_ERR_INVALID;
+    return append_step(a, seqs, n, tables, cap, seq_lens, slots_out, cow_pairs_out, n_cow_out);
 }
 
 pkv_status block_allocator_fork(pkv_allocator *a, int64_t parent, int64_t child) {

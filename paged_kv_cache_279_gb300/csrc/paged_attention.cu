@@ -529,20 +529,23 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 // ---------------------------------------------------------------------------
 constexpr int kMinTilesPerCta = 16;  // >= 256 tokens per share: bounds pieces per segment
 
-constexpr int kYCache = 512;  // tiles of a CTA whose TMA rows are staged in shared memory (sized so 3 CTAs of 4 warps fit an SM up to ~500 sequences)
+constexpr int kYCache = 256;  // tiles of a CTA whose TMA rows are staged in shared memory (3 CTAs of 4 warps fit an SM up to ~750 sequences)
 constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended last
 
 // Shared-memory layout of the balanced kernel (host and device agree on it).
 // Offsets are from the 1024-aligned base.
 struct StreamKLayout {
-    int ring, bars, ycache, masks, prefix, total;
-    // stage_bytes: one ring stage (K and V of one tile); 0 = a 16-token bf16 tile
-    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, int stage_bytes = 0) {
-        ring = NW * NS * (stage_bytes ? stage_bytes : 2 * D * kTile * 2);
+    int ring, bars, patch, ycache, masks, srcs, prefix, total;
+    // stage_bytes: one ring stage (K and V of one tile); new_bytes: per stage,
+    // room for one new K row and V row (fused append), or 0 (then no srcs)
+    __host__ __device__ StreamKLayout(int D, int NW, int NS, int num_seqs, int stage_bytes, int new_bytes) {
+        ring = NW * NS * stage_bytes;
         bars = ring;
-        ycache = bars + NW * NS * 8;   // int2 per cached tile
+        patch = bars + NW * NS * 8;      // 16-byte aligned (bulk copies)
+        ycache = patch + NW * NS * new_bytes;  // int2 per cached tile
         masks = ycache + kYCache * 8;  // valid-row mask per cached tile
-        prefix = masks + kYCache * 4;
+        srcs = masks + kYCache * 4;    // fused append: new-token row of a cached last tile, else -1
+        prefix = srcs + (new_bytes ? kYCache * 4 : 0);
         total = prefix + (num_seqs + 1) * 4 + 1024;  // + alignment slack
     }
 };
@@ -619,10 +622,12 @@ __device__ __forceinline__ TileRows tile_rows(const DecodeArgs &a, int seq, int 
 
 template <int D>
 __device__ __forceinline__ void issue_rows(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                           unsigned char *stage, uint64_t *bar, int boxh, TileRows r) {
+                                           unsigned char *stage, uint64_t *bar, int boxh, TileRows r,
+                                           uint32_t extra_bytes = 0) {
     using Lay = Bf16Layout<D>;
     const int nsub = r.y0 < 0 ? 0 : (r.y1 < 0 ? 1 : 2);
-    mbar_arrive_expect_tx(bar, (uint32_t)(nsub * Lay::kHalves * boxh * 128 * 2));
+    // extra_bytes: further copies the caller issues on the same barrier
+    mbar_arrive_expect_tx(bar, (uint32_t)(nsub * Lay::kHalves * boxh * 128 * 2) + extra_bytes);
     const uint32_t b = smem_u32(bar);
     const uint32_t dk = smem_u32(stage);
     const uint32_t dv = dk + Lay::kKVBytes;
@@ -871,14 +876,16 @@ __device__ __forceinline__ void attend_tile_f8(unsigned char *sk, unsigned char 
 // lie past the context are loaded from inside its block and masked later.
 template <int D>
 __device__ __forceinline__ void issue_rows_f8(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                              unsigned char *stage, uint64_t *bar, int bshift, TileRows r) {
+                                              unsigned char *stage, uint64_t *bar, int bshift, TileRows r,
+                                              uint32_t extra_bytes = 0) {
     const uint32_t b = smem_u32(bar);
+    // extra_bytes: further copies the caller issues on the same barrier
     if (r.y0 < 0) {
-        mbar_arrive_expect_tx(bar, 0u);
+        mbar_arrive_expect_tx(bar, extra_bytes);
         return;
     }
     const int y1 = bshift == 5 ? r.y0 + kTile : r.y1;
-    mbar_arrive_expect_tx(bar, (uint32_t)((y1 >= 0 ? 2 : 1) * 2 * kTile * D));
+    mbar_arrive_expect_tx(bar, (uint32_t)((y1 >= 0 ? 2 : 1) * 2 * kTile * D) + extra_bytes);
     const uint32_t dk = smem_u32(stage), dv = dk + 2 * kTile * D;
     const int bh0 = r.y0 >> bshift;  // block * Hkv + kv head
     tma_load_2d(dk, tm_k, b, 0, r.y0);
@@ -887,6 +894,44 @@ __device__ __forceinline__ void issue_rows_f8(const CUtensorMap *tm_k, const CUt
         const int bh1 = y1 >> bshift;
         tma_load_2d(dk + kTile * D, tm_k, b, 0, y1);
         tma_load_2d(dv + kTile * D, tm_v, b, y1 - (bh1 << bshift), bh1 * D);
+    }
+}
+
+// Fused append, FP8: quantise the new token's bf16 K and V rows (landed in
+// `nrow`, K then V) and write the codes over row `row` of the landed 32-token
+// tile `sk` and into the cache (the tile's TMA rows y0 / y1).  Lanes 0-7 make
+// 16 K codes each (one 16-byte chunk of the K row); lanes 8-15 make 16 V codes
+// each, one byte of each of 16 head_dim rows of the transposed V tile (and of
+// the V block in the cache).  Kept out of line: it runs once per context and
+// would otherwise raise the attention loop's register pressure.
+template <int D>
+__device__ __noinline__ void patch_new_row_f8(unsigned char *sk, const unsigned char *nrow, int y0, int y1, int row,
+                                              int lane, float kscale, float vscale, int B, int bshift,
+                                              void *k_cache, void *v_cache) {
+    if (lane >= 16) return;
+    const bool isv = lane >= 8;
+    const int ch = lane & 7;
+    const uint4 *src = reinterpret_cast<const uint4 *>(nrow + (isv ? 2 * D : 0) + 32 * ch);
+    const uint4 x[2] = {src[0], src[1]};
+    uint32_t w[4];
+    quantize16(x, isv ? vscale : kscale, w);
+    const int sub_rows = B < 2 * kTile ? B : 2 * kTile;  // rows of one TMA sub-box
+    const int sub = row >> 4, rr = row & 15;
+    const int64_t y = row < sub_rows ? (int64_t)y0 + row : (int64_t)y1 + (row - sub_rows);
+    const int64_t bh = y >> bshift, off = y & (B - 1);
+    if (!isv) {
+        const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(sk + sub * kTile * D + rr * D + ((ch ^ (rr & 7)) << 4)) = codes;
+        *reinterpret_cast<uint4 *>(static_cast<unsigned char *>(k_cache) + y * D + 16 * ch) = codes;
+    } else {
+        unsigned char *vt = sk + TileBytes<D, true>::kKV + sub * kTile * D + (16 * ch) * kTile + rr;
+        unsigned char *col = static_cast<unsigned char *>(v_cache) + (bh * D + 16 * ch) * B + off;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const unsigned char code = (unsigned char)(w[j >> 2] >> (8 * (j & 3)));
+            vt[j * kTile] = code;
+            col[(int64_t)j * B] = code;
+        }
     }
 }
 
@@ -1045,8 +1090,8 @@ __device__ __forceinline__ void merge_segment(const float *part_o, const float *
 //
 // F8: the cache holds E4M3 codes (K rows, V transposed per block); tiles are
 // attended by attend_tile_f8 and the queries are loaded by load_q_f16.
-template <int D, int NW, int NS, bool F8 = false>
-__global__ void __launch_bounds__(NW * 32)
+template <int D, int NW, int NS, bool F8, bool APPEND>
+__global__ void __launch_bounds__(NW * 32, 3)
 decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
     using Lay = TileBytes<D, F8>;
@@ -1054,10 +1099,14 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const StreamKLayout L(D, NW, NS, a.num_seqs, Lay::kStage);
+    constexpr int kNewBytes = APPEND ? 4 * D : 0;  // one new K row and V row (bf16)
+    constexpr int kChunks = D * 2 / 16;            // 16-byte chunks of one bf16 K (or V) row
+    constexpr bool has_new = APPEND;
+    const StreamKLayout L(D, NW, NS, a.num_seqs, Lay::kStage, kNewBytes);
     uint64_t *bars_all = reinterpret_cast<uint64_t *>(smem + L.bars);
     int2 *ycache = reinterpret_cast<int2 *>(smem + L.ycache);
     uint32_t *mcache = reinterpret_cast<uint32_t *>(smem + L.masks);
+    int *scache = reinterpret_cast<int *>(smem + L.srcs);
     int *prefix = reinterpret_cast<int *>(smem + L.prefix);
     __shared__ int warp_sums[NW];
     __shared__ int carry;
@@ -1160,6 +1209,19 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         if constexpr (F8) load_q_f16<D>(a, c.seq, c.kvh, lane, dst, f0, f1);
         else load_q_fragments<D>(a, c.seq, c.kvh, lane, dst);
     };
+    // Fused append: the new token of a segment (position len - 1) sits
+    // in the segment's last tile; the producer brings its K and V rows into
+    // the stage's new-row slot with the tile, and the piece that attends the
+    // tile writes them over the tile's stale row.  new_row: the token's row
+    // in that tile (-1: no append), read with the piece's queries.
+    int new_row = -1, new_row_n = -1;
+    auto load_new = [&](const SegCursor &c, int &row) {
+        row = -1;
+        if (!has_new) return;
+        const int64_t last = c.seg_start + c.n - 1;
+        if (last < lo || last >= hi) return;
+        row = (clamp_len(a.seq_lens[c.seq], cap) - 1) % TT;  // the segment has tiles: len >= 1
+    };
     bool qn_loaded = false;  // qn holds the second piece's queries
     // The queries of the first two pieces: fetched now, ahead of the burst of
     // tile loads that every warp issues after the staging below.
@@ -1171,6 +1233,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         seg = seg_lo;
         if (r != lo) seg.advance_to(prefix, Hkv, r);
         load_q(seg, qb, qs0, qs1);
+        load_new(seg, new_row);
         const int64_t end1 = seg.seg_start + seg.n;  // the first piece ends at min(hi, end1)
         if (end1 < hi || r != lo) {
             SegCursor second = seg_lo;
@@ -1179,6 +1242,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 second.advance_to(prefix, Hkv, end1);
             }
             load_q(second, qn, qns0, qns1);
+            load_new(second, new_row_n);
             qn_loaded = true;
         }
     }
@@ -1236,6 +1300,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
             const int valid = min(TT, len - tl[u] * TT);
             r.mask &= low_bits(valid);
+            if (APPEND)  // the segment's last tile carries its new token
+                scache[threadIdx.x + u * NW * 32] = (tl[u] + 1) * TT >= len ? sq[u] * Hkv + kv[u] : -1;
             const int i = threadIdx.x + u * NW * 32;
             ycache[i] = make_int2(r.y0, r.y1);
             // bf16: valid rows in bits 16..20 (the fused append reads them)
@@ -1256,102 +1322,6 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int ntiles = (int)(hi - lo);
     const int boxh = a.block_size < kTile ? a.block_size : kTile;
 
-    if (F8 && a.k_new) {
-        // Fused append, FP8: as below, one segment at a time.  Lanes 0-7
-        // quantise 16 K entries each into one 16-byte chunk of the K row;
-        // lanes 8-15 quantise 16 V entries each into bytes of the transposed
-        // V block (one per head_dim row, block_size bytes apart).
-        SegCursor c = seg_lo;
-        for (;;) {
-            const int64_t last = c.seg_start + c.n - 1;
-            if (last >= lo && last < hi && lane < 16) {
-                const int B = a.block_size;
-                const int pos = clamp_len(a.seq_lens[c.seq], cap) - 1;  // >= 0: the segment has tiles
-                const int lb = pos / B;
-                const int blk = a.block_tables[(int64_t)c.seq * a.max_blocks + lb];
-                if (blk >= 0 && blk < a.num_blocks) {
-                    const int off = pos - lb * B, ch = lane & 7;
-                    const bool isv = lane >= 8;
-                    const int64_t bh = (int64_t)blk * Hkv + c.kvh;
-                    const uint4 *src = static_cast<const uint4 *>(isv ? a.v_new : a.k_new) +
-                                       ((int64_t)c.seq * Hkv + c.kvh) * (D / 8) + 2 * ch;
-                    const uint4 x[2] = {src[0], src[1]};
-                    uint32_t w[4];
-                    quantize16(x, isv ? a.f8_vscale : a.f8_kscale, w);
-                    if (!isv) {
-                        *reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.k_cache_w) +
-                                                   (bh * B + off) * D + 16 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
-                    } else {
-                        unsigned char *col = static_cast<unsigned char *>(a.v_cache_w) + (bh * D + 16 * ch) * B + off;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) col[(int64_t)j * B] = (unsigned char)(w[j >> 2] >> (8 * (j & 3)));
-                    }
-                }
-            }
-            if (c.seg_start + c.n >= hi) break;
-            c.advance_to(prefix, Hkv, c.seg_start + c.n);
-        }
-        // generic-proxy stores, then the TMA (async proxy) of this warp reads them
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        __syncwarp();
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
-    if (!F8 && a.k_new) {
-        // Fused append: the warp whose share holds a segment's last tile stores
-        // that segment's new token (position len - 1) before any TMA reads it.
-        // Only this warp ever reads that tile, so no other ordering is needed.
-        // Targets come from the staged rows; all copies of up to kBatch
-        // segments are loaded before any is stored.
-        constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of one K (or V) row
-        constexpr int kBatch = 4;
-        const int part = lane / kChunks, ch = lane % kChunks;  // lanes past 2*kChunks idle
-        SegCursor c = seg_lo;
-        bool more = true;
-        while (more) {
-            int64_t src_row[kBatch], dst_row[kBatch];
-            int n = 0;
-            while (more && n < kBatch) {
-                const int64_t last = c.seg_start + c.n - 1;
-                if (last >= lo && last < hi) {
-                    int64_t dst = -1;
-                    const int64_t i = last - cta_lo;
-                    if (i < ncache) {
-                        const uint32_t m = mcache[i];
-                        const int r = (int)(m >> 16) - 1;  // row of position len - 1 in its tile
-                        if ((m >> r) & 1u) {
-                            const int2 y = ycache[i];
-                            dst = r < boxh ? (int64_t)y.x + r : (int64_t)y.y + (r - boxh);
-                        }
-                    } else {
-                        const int len = clamp_len(a.seq_lens[c.seq], cap);
-                        const int pos = len - 1, lb = pos / a.block_size;
-                        const int blk = a.block_tables[(int64_t)c.seq * a.max_blocks + lb];
-                        if (blk >= 0 && blk < a.num_blocks)
-                            dst = ((int64_t)blk * Hkv + c.kvh) * a.block_size + (pos - lb * a.block_size);
-                    }
-                    src_row[n] = (int64_t)c.seq * Hkv + c.kvh;
-                    dst_row[n] = dst;
-                    ++n;
-                }
-                if (c.seg_start + c.n >= hi) more = false;
-                else c.advance_to(prefix, Hkv, c.seg_start + c.n);
-            }
-            uint4 v[kBatch];
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-                if (j < n && lane < 2 * kChunks && dst_row[j] >= 0)
-                    v[j] = static_cast<const uint4 *>(part ? a.v_new : a.k_new)[src_row[j] * kChunks + ch];
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j)
-                if (j < n && lane < 2 * kChunks && dst_row[j] >= 0)
-                    static_cast<uint4 *>(part ? a.v_cache_w : a.k_cache_w)[dst_row[j] * kChunks + ch] = v[j];
-        }
-        // generic-proxy stores, then the TMA (async proxy) of this warp reads them
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        __syncwarp();
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
-
     // rows/mask of tile t (staged, or computed for tiles past the cache)
     auto rows_of = [&](int64_t t, const SegCursor &c) -> TileRows {
         const int64_t i = t - cta_lo;
@@ -1367,13 +1337,27 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     auto tile_at = [&](int k) -> int64_t { return k < run1 ? r + k : lo + (k - run1); };
     SegCursor prod;  // lane 0: segment of the tile being issued (needed past the cache; r == lo then)
     if (lane == 0) prod.seek(prefix, S, Hkv, lo);
+    unsigned char *newrows = smem + L.patch + warp * NS * kNewBytes;
     auto issue = [&](int k, int buf) {
         const int64_t t = tile_at(k);
-        if (t - cta_lo >= ncache) prod.advance_to(prefix, Hkv, t);
+        const bool cached = t - cta_lo < ncache;
+        if (!cached) prod.advance_to(prefix, Hkv, t);
+        // fused append: the segment's last tile also brings the new token's K and V rows
+        int64_t src = -1;
+        if constexpr (APPEND)
+            src = cached ? scache[t - cta_lo]
+                         : (t == prod.seg_start + prod.n - 1 ? (int64_t)prod.seq * Hkv + prod.kvh : -1);
         if constexpr (F8)
-            issue_rows_f8<D>(&tm_k, &tm_v, ring + buf * Lay::kStage, &bars[buf], a.f8_bshift, rows_of(t, prod));
+            issue_rows_f8<D>(&tm_k, &tm_v, ring + buf * Lay::kStage, &bars[buf], a.f8_bshift, rows_of(t, prod),
+                             src >= 0 ? kNewBytes : 0u);
         else
-            issue_rows<D>(&tm_k, &tm_v, ring + buf * Lay::kStage, &bars[buf], boxh, rows_of(t, prod));
+            issue_rows<D>(&tm_k, &tm_v, ring + buf * Lay::kStage, &bars[buf], boxh, rows_of(t, prod),
+                          src >= 0 ? kNewBytes : 0u);
+        if (APPEND && src >= 0) {
+            const uint32_t dst = smem_u32(newrows + buf * kNewBytes), b = smem_u32(&bars[buf]);
+            bulk_load(dst, static_cast<const __nv_bfloat16 *>(a.k_new) + src * D, 2 * D, b);
+            bulk_load(dst + 2 * D, static_cast<const __nv_bfloat16 *>(a.v_new) + src * D, 2 * D, b);
+        }
     };
     if (lane == 0) {
         for (int i = 0; i < NS && i < ntiles; ++i) issue(i, i);
@@ -1395,7 +1379,10 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int64_t tn = tile_at(kend);
             if (tn == pb) nxt.advance_to(prefix, Hkv, tn);
             else nxt = seg_lo;  // the walk wraps to lo
-            if (!qn_loaded) load_q(nxt, qn, qns0, qns1);
+            if (!qn_loaded) {
+                load_q(nxt, qn, qns0, qns1);
+                load_new(nxt, new_row_n);
+            }
             qn_loaded = false;
         }
         acc.reset();
@@ -1406,8 +1393,30 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 dead = true;
             }
             if (dead) continue;
-            const TileRows rw = rows_of(tile_at(k), seg);
+            const int64_t t = tile_at(k);
+            const TileRows rw = rows_of(t, seg);
             unsigned char *sk = ring + buf * Lay::kStage;
+            if (APPEND && F8 && new_row >= 0 && t == seg.seg_start + seg.n - 1 && ((rw.mask >> new_row) & 1u)) {
+                patch_new_row_f8<D>(sk, newrows + buf * kNewBytes, rw.y0, rw.y1, new_row, lane, a.f8_kscale,
+                                    a.f8_vscale, a.block_size, a.f8_bshift, a.k_cache_w, a.v_cache_w);
+                __syncwarp();
+            }
+            if (APPEND && !F8 && new_row >= 0 && t == seg.seg_start + seg.n - 1 && ((rw.mask >> new_row) & 1u)) {
+                // The new token: its rows, landed in the stage's new-row slot,
+                // overwrite the tile's row (the stale slot the TMA brought)
+                // before the tile is attended, and are stored to the cache for
+                // later calls.  Nothing in this call reads that cache row: only
+                // this warp attends the tile.
+                if (lane < 2 * kChunks) {
+                    const uint4 nv = *reinterpret_cast<const uint4 *>(newrows + buf * kNewBytes + lane * 16);
+                    const int ch = lane % kChunks, h = ch >> 3, c = ch & 7;
+                    *reinterpret_cast<uint4 *>(sk + (lane < kChunks ? 0 : Lay::kKV) + h * (kTile * 128) +
+                                               new_row * 128 + ((c ^ (new_row & 7)) << 4)) = nv;
+                    const int64_t dst = new_row < boxh ? (int64_t)rw.y0 + new_row : (int64_t)rw.y1 + (new_row - boxh);
+                    static_cast<uint4 *>(lane < kChunks ? a.k_cache_w : a.v_cache_w)[dst * kChunks + ch] = nv;
+                }
+                __syncwarp();
+            }
             if constexpr (F8)
                 attend_tile_f8<D>(sk, sk + Lay::kKV, rw.mask, qb, qs0, qs1, acc, lane);
             else
@@ -1447,6 +1456,7 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         qs0 = qns0;
         qs1 = qns1;
+        new_row = new_row_n;
     }
     if (merge_seg >= 0) {
         // Wait (bounded) until the other pieces' flags carry this call's tag,
@@ -1714,12 +1724,13 @@ static pkv_status dispatch_bf16(const DecodeArgs &a, dim3 grid, cudaStream_t st)
     return launch_bf16<D, 4, 2>(a, grid, st);
 }
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool APPEND>
 static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
     static bool done[128] = {};
-    auto kern = decode_bf16_streamk_kernel<D, NW, NS>;
-    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs).total, done)) return PKV_ERR_CUDA;
-    const int smem = StreamKLayout(D, NW, NS, a.num_seqs).total;
+    auto kern = decode_bf16_streamk_kernel<D, NW, NS, false, APPEND>;
+    constexpr int stage = TileBytes<D, false>::kStage, nb = APPEND ? 4 * D : 0;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, stage, nb).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, stage, nb).total;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
         per_sm < 1)
@@ -1735,7 +1746,7 @@ static pkv_status launch_balanced(const DecodeArgs &a, cudaStream_t st) {
 
 template <int D>
 static pkv_status dispatch_balanced(const DecodeArgs &a, cudaStream_t st) {
-    return launch_balanced<D, 4, 2>(a, st);
+    return a.k_new ? launch_balanced<D, 4, 2, true>(a, st) : launch_balanced<D, 4, 2, false>(a, st);
 }
 
 // FP8 cache views.  K: [blocks * Hkv * B][D] bytes, box D x 16 rows, 128-byte
@@ -1761,13 +1772,13 @@ static bool make_f8_maps(const DecodeArgs &a, int D, CUtensorMap *mk, CUtensorMa
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int NW, int NS>
+template <int D, int NW, int NS, bool APPEND>
 static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
     static bool done[128] = {};
-    auto kern = decode_bf16_streamk_kernel<D, NW, NS, true>;
-    constexpr int stage = TileBytes<D, true>::kStage;
-    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, stage).total, done)) return PKV_ERR_CUDA;
-    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, stage).total;
+    auto kern = decode_bf16_streamk_kernel<D, NW, NS, true, APPEND>;
+    constexpr int stage = TileBytes<D, true>::kStage, nb = APPEND ? 4 * D : 0;
+    if (!ensure_smem(kern, StreamKLayout(D, NW, NS, kMaxBalancedSeqs, stage, nb).total, done)) return PKV_ERR_CUDA;
+    const int smem = StreamKLayout(D, NW, NS, a.num_seqs, stage, nb).total;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess ||
         per_sm < 1)
@@ -1782,7 +1793,7 @@ static pkv_status launch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
 }
 
 static pkv_status dispatch_balanced_f8(const DecodeArgs &a, cudaStream_t st) {
-    return launch_balanced_f8<128, 4, 2>(a, st);
+    return a.k_new ? launch_balanced_f8<128, 4, 2, true>(a, st) : launch_balanced_f8<128, 4, 2, false>(a, st);
 }
 
 template <typename T, int D>

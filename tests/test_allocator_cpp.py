@@ -240,3 +240,66 @@ def test_prefix_cache_reports_cached_tokens_and_shares_blocks():
     # the shared blocks are prefix groups for the grouped decode
     offs, pre = c.prefix_groups([0, 1])
     assert offs.tolist() == [0, 2] and pre.tolist() == [32]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_append_step_keeps_dense_tables_equal_to_a_rebuild(seed):
+    """The serving loop's incremental tables: after every step (fresh blocks,
+    CoW of shared last blocks after forks, OOM refusals) the tables and lengths
+    that append_step updated in place equal a full block_tables rebuild, and the
+    slots and copy pairs equal append_slots' on the reference model."""
+    rnd = random.Random(300 + seed)
+    B = rnd.choice([4, 8, 16])
+    NB = rnd.randint(20, 80)
+    c = pkv.BlockAllocator(NB, B)
+    m = BlockAllocatorModel(NB, B)
+    live = []
+    for sid in range(5):
+        n = rnd.randint(1, 3 * B)
+        if c.add_seq(sid, n) == 0:
+            assert m.add_seq(sid, n) == 0
+            live.append(sid)
+    for sid in list(live)[:2]:
+        for k in range(2):
+            child = 100 * (k + 1) + sid
+            if c.fork(sid, child) == 0:
+                m.fork(sid, child)
+                live.append(child)
+    cap = 40
+    tables, lens = c.block_tables(live, cap=cap, pad=-1)
+    tables, lens = np.ascontiguousarray(tables), np.ascontiguousarray(lens)
+    for step in range(30):
+        before = tables.copy(), lens.copy()
+        st, slots, pairs = c.append_step(live, tables, lens)
+        need = sum(1 for s in live if m.num_tokens(s) % B == 0 or m.refcount(m.block_table(s)[-1]) > 1)
+        if need > m.num_free():
+            assert st == 2
+            assert np.array_equal(tables, before[0]) and np.array_equal(lens, before[1])
+            break
+        assert st == 0
+        want_slots, want_pairs = [], []
+        for s in live:
+            mst, slot, src, dst = m.append_slot(s)
+            assert mst == 0
+            want_slots.append(slot)
+            if src >= 0:
+                want_pairs.append((src, dst))
+        assert slots.tolist() == want_slots
+        assert [tuple(p) for p in pairs.tolist()] == want_pairs
+        ref_t, ref_l = c.block_tables(live, cap=cap, pad=-1)
+        assert np.array_equal(tables, ref_t) and np.array_equal(lens, ref_l)
+        assert_same_state(c, m, live)
+
+
+def test_append_step_refuses_a_row_too_narrow():
+    c = pkv.BlockAllocator(16, 4)
+    assert c.add_seq(0, 8) == 0 and c.add_seq(1, 3) == 0
+    tables, lens = c.block_tables([0, 1], cap=2, pad=-1)
+    tables, lens = np.ascontiguousarray(tables), np.ascontiguousarray(lens)
+    st, _, _ = c.append_step([0, 1], tables, lens)  # seq 0's ninth token needs block index 2
+    assert st == 1
+    assert c.num_tokens(0) == 8 and c.num_tokens(1) == 3 and c.num_free() == 13
+    st, slots, _ = c.append_step([1], tables[1:], lens[1:])
+    assert st == 0 and lens[1] == 4 and slots[0] == tables[1, 0] * 4 + 3
+    with pytest.raises(ValueError):
+        c.append_step([0], tables[:, :1], lens[:1])  # not C-contiguous

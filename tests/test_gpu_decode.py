@@ -13,7 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_279_gb300 as pkv
 from paged_kv_cache_279_gb300 import workloads as wl
-from harness import (assert_bf16_close, assert_f32_close, bits, make_decode_case, oracle_out,
+from harness import (assert_bf16_close, assert_f32_close, bits, make_decode_case, oracle_out, token_slots,
                      run_decode)
 
 pytestmark = pytest.mark.gpu
@@ -225,22 +225,25 @@ def test_balanced_workspace_reused_across_calls():
     assert pkv.read_device_errors() == 0
 
 
-@pytest.mark.parametrize("P,dtype,B,nseq", [
-    (0, torch.bfloat16, 16, 7), (0, torch.bfloat16, 8, 7), (0, torch.bfloat16, 32, 7),
-    (64, torch.bfloat16, 16, 7),     # fixed partitions: the separate store kernel, then decode
-    (64, torch.bfloat16, 16, 150),
-    (0, torch.float32, 16, 7),       # fp32: the separate store kernel, then decode
-    (0, torch.bfloat16, 16, 150)])   # 150 x 8 segments stored inside the balanced kernel
-def test_decode_append_equals_write_then_decode(P, dtype, B, nseq):
+@pytest.mark.parametrize("P,dtype,B,nseq,D", [
+    (0, torch.bfloat16, 16, 7, 128), (0, torch.bfloat16, 8, 7, 128), (0, torch.bfloat16, 32, 7, 128),
+    (0, torch.bfloat16, 16, 7, 64), (0, torch.bfloat16, 8, 150, 64),
+    (64, torch.bfloat16, 16, 7, 128),     # fixed partitions: the separate store kernel, then decode
+    (64, torch.bfloat16, 16, 150, 128),
+    (0, torch.float32, 16, 7, 128),       # fp32: the separate store kernel, then decode
+    (0, torch.bfloat16, 16, 150, 128)])   # 150 x 8 segments: new rows patched into landed tiles
+def test_decode_append_equals_write_then_decode(P, dtype, B, nseq, D):
     """paged_attention_decode_append = store the newest token of every
     sequence at position len - 1, then attend (fused into the balanced bf16
-    kernel; a separate store kernel on the fixed-partition and fp32 paths)."""
-    shape = shape_of(32, 8, 128, B, dtype)
+    kernel: the new row replaces the stale slot in the landed tile and is
+    stored to the pool; a separate store kernel on the fixed-partition and fp32
+    paths)."""
+    shape = shape_of(32, 8, D, B, dtype)
     base = [1, 16, 17, 300, 0, 1500, 33]
     lens = (base * (nseq // len(base) + 1))[:nseq] if nseq != len(base) else base
-    case = make_decode_case(shape, lens, seed=31 + B + P)
+    case = make_decode_case(shape, lens, seed=31 + B + P + D)
     kc, vc = case["kc"].clone(), case["vc"].clone()
-    k_new = torch.zeros((len(lens), 8, 128), dtype=dtype)
+    k_new = torch.zeros((len(lens), 8, D), dtype=dtype)
     v_new = torch.zeros_like(k_new)
     for s, L in enumerate(lens):
         if L == 0:
@@ -316,4 +319,66 @@ def test_balanced_merge_survives_graph_replays_and_random_workspace():
         assert torch.all(out[2].float() == 0)
 
     _replay_checks(call, refresh, check)
+    assert pkv.read_device_errors() == 0
+
+
+def test_decode_append_graph_replays_advance_one_token_each():
+    """The serving loop: one decode_append call captured in a CUDA graph and
+    replayed step after step, the lengths and new tokens refreshed in place
+    before each replay.  Every replay must store its token at the new
+    position (pool bit-exact), attend over the context including it (oracle),
+    and the tokens not yet appended stay NaN in the pool."""
+    shape = shape_of(32, 8, 128, 16)
+    lens0 = [1, 15, 16, 31, 300, 2047, 64] * 3
+    steps = 4
+    full = [L + steps for L in lens0]
+    case = make_decode_case(shape, full, seed=77, extra_blocks=8)
+    kc, vc = case["kc"].clone(), case["vc"].clone()
+    B = shape.block_size
+    for s, L in enumerate(lens0):  # positions L-1 .. L+steps-1 are not in the pool yet
+        slots = torch.from_numpy(token_slots(case["tables"][s], full[s], B)[L - 1:])
+        kc[slots // B, :, slots % B] = float("nan")
+        vc[slots // B, :, slots % B] = float("nan")
+    dkc, dvc = kc.cuda(), vc.cuda()
+    tables = torch.from_numpy(case["tables"]).cuda()
+    q = case["q"].cuda()
+    out = torch.empty_like(q)
+    S = len(lens0)
+    sl = torch.tensor(lens0, dtype=torch.int32, device="cuda")
+    k_new = torch.empty((S, 8, 128), dtype=torch.bfloat16, device="cuda")
+    v_new = torch.empty_like(k_new)
+
+    def refresh(rep):
+        lens = [L + rep for L in lens0]
+        sl.copy_(torch.tensor(lens, dtype=torch.int32))
+        k_new.copy_(torch.stack([case["ks"][s][L - 1] for s, L in enumerate(lens)]))
+        v_new.copy_(torch.stack([case["vs"][s][L - 1] for s, L in enumerate(lens)]))
+
+    refresh(0)
+    call = lambda: pkv.paged_attention_decode_append(out, q, k_new, v_new, dkc, dvc, tables, sl, shape.scale,
+                                                     max(full))
+
+    def check(rep):
+        lens = [L + rep for L in lens0]
+        sub = dict(case, ks=[k[:L] for k, L in zip(case["ks"], lens)], vs=[v[:L] for v, L in zip(case["vs"], lens)],
+                   lens=lens)
+        assert_bf16_close(out, oracle_out(sub, shape), f"replay {rep}")
+        hk = dkc.cpu()
+        for s, L in enumerate(lens):
+            sl_ = torch.from_numpy(token_slots(case["tables"][s], full[s], B))
+            assert torch.equal(bits(hk[sl_[:L] // B, :, sl_[:L] % B]), bits(case["kc"][sl_[:L] // B, :, sl_[:L] % B]))
+            assert torch.isnan(hk[sl_[L:] // B, :, sl_[L:] % B].float()).all()
+
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        call()  # warm (tensor maps, shared-memory opt-in); stores replay 0's tokens
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            call()
+    for rep in range(steps + 1):
+        refresh(rep)
+        g.replay()
+        torch.cuda.synchronize()
+        check(rep)
     assert pkv.read_device_errors() == 0
