@@ -636,7 +636,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         Ctx c;
         bool dead = !c.seek(a, cum, uval, s0, cap);
         if (dead && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-        int64_t j = 0;  // tiles issued
+        int j = 0;  // tiles issued (32-bit: ring slots and phases are cheap to derive)
         int p = 0;      // pieces published
         const int bpt = kTok / B;  // blocks per tile
         for (int64_t t = s0; t < s1 && !dead;) {
@@ -760,7 +760,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         }
         // copies still in flight (only after a timeout) land before the CTA exits
         if (lane == 0 && dead)
-            for (int64_t k = max((int64_t)0, j - NS); k < j; ++k) {
+            for (int k = max(0, j - NS); k < j; ++k) {
                 mbar_wait_bounded(&k_full[k % NS], (uint32_t)((k / NS) & 1));
                 mbar_wait_bounded(&v_full[k % NS], (uint32_t)((k / NS) & 1));
             }
@@ -777,7 +777,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
 #pragma unroll
             for (int k = 0; k < kTok / 16; ++k) pv_off[k] = (uint32_t)((16 * k / B) * (H * B * 128) + (16 * k % B) * 128);
             const uint64_t qd = tc::smem_desc(q_s, 16, 1024);
-            int64_t jq = 0, jp = 0;       // next Q K^T / P V tile
+            int jq = 0, jp = 0;           // next Q K^T / P V tile
             int pq = 0, pp = 0;           // their pieces
             int tq = 0, tp = 0;           // tile within those pieces
             int ntq = -1;                 // tiles of piece pq (-1: descriptor not read yet)
@@ -896,7 +896,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         const int rr = threadIdx.x;
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         bool dead = false;
-        int64_t j = 0;
+        int j = 0;
         int p = 0;
         // P V of tile x has completed.  o_done[x & 1] completes one phase per P V
         // of that parity, and a parity wait is only meaningful for the barrier's
@@ -904,7 +904,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         // P V of tile j - 2 (same barrier) was waited for: every phase is waited
         // for in order, and a barrier never runs two phases past its waiter (P V
         // of tile j needs this tile's P).
-        auto wait_pv = [&](int64_t x) {
+        auto wait_pv = [&](int x) {
             if (x >= 0) wait_or_flag(&o_done[x & 1], (uint32_t)((x >> 1) & 1), dead, a.err);
         };
         // this thread's query row of a piece into Q (128-byte swizzled, K-major; zero past the live rows)
