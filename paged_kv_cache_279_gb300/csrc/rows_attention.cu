@@ -31,21 +31,26 @@
 // resident at once (cooperative launch), and a CTA never waits for a piece
 // later in its own share, so no chain of waits can close.
 //
-// Warp roles (224 threads):
-//   warps 0-3  softmax: thread r owns query row r = TMEM lane r.  Reads S
+// Warp roles (384 threads):
+//   warps 0-3, 4-7  two softmax groups; group g takes the tiles j with
+//              j % 2 == g of every piece (two independent chains per SM).
+//              Thread r of a group owns query row r = TMEM lane r.  Reads S
 //              from TMEM, keeps the row's running max and sum, writes P (bf16)
 //              back into the S columns (P is the A operand of P V, taken from
-//              tensor memory), zeroes the V rows of keys past a context's end,
-//              loads the next piece's queries, and writes the piece's result.
-//   warp 4     producer: walks the share, publishes one descriptor per piece,
+//              tensor memory), zeroes the V rows of keys past a context's end
+//              and, on a piece's last tile, loads the next piece's queries.
+//              Each group accumulates its own O; group 0 combines the two
+//              partial states of a piece and writes its result.
+//   warp 8     idle.
+//   warp 9     grouped: checks that every member's block table holds the
+//              leader's blocks over the prefix.
+//   warp 10    producer: walks the share, publishes one descriptor per piece,
 //              stages block ids in shared memory (many loads in flight) and
 //              issues the K/V TMA boxes (one block per box) into an NS-stage
 //              ring, with each tile's key range in a per-stage record.
-//   warp 5     MMA: allocates tensor memory; one thread issues Q K^T and P V,
+//   warp 11    MMA: allocates tensor memory; one thread issues Q K^T and P V,
 //              each as soon as its inputs are ready (a late tile does not hold
 //              up the P V of the one before).
-//   warp 6     grouped: checks that every member's block table holds the
-//              leader's blocks over the prefix.
 // Every wait is bounded; on a timeout the kernel flags PKV_DEVERR_TIMEOUT,
 // waits (bounded) for its own copies in flight, frees its tensor memory and
 // returns.
@@ -65,18 +70,20 @@ namespace rows {
 
 constexpr int kTok = 64;          // keys per tile
 constexpr int kRows = tc::kRows;  // query rows per context (the MMA's M)
-constexpr int kThreads = 256;
-// Warp roles.  The producer and MMA warps share the schedulers of softmax warps
-// 2 and 3, which have no rows when a context has at most 64 (resp. 96) rows.
-constexpr int kAuxWarp = 5, kProducerWarp = 6, kMmaWarp = 7;
+constexpr int kSG = 2;           // softmax groups (warps 0-3 and 4-7), one chain of tiles each
+constexpr int kThreads = 384;
+// Warp roles.  Warp 8 is idle.  The producer and MMA warps share the
+// schedulers of softmax warps 2, 6 and 3, 7, which have no rows when a context
+// has at most 64 (resp. 96) rows.
+constexpr int kAuxWarp = 9, kProducerWarp = 10, kMmaWarp = 11;
 constexpr int kMaxUnits = 1024;   // groups / sequences scanned per launch
 constexpr int kMinTiles = 4;      // shares hold >= 4 tiles unless the total is small
 constexpr int kIdCache = 512;     // block ids staged by the producer
 constexpr int kChunkTiles = 128;  // tiles whose keys the producer stages at once
 constexpr int kDescs = 8;         // piece descriptors in flight
 constexpr float kRescale = 8.f;   // headroom (log2 units) before a row's running max moves
-constexpr int kSB = 3;            // S / P buffers in tensor memory: Q K^T runs up to two tiles ahead
-constexpr uint32_t kOBase = kSB * kTok;  // O of even / odd pieces at kOBase / kOBase + D
+constexpr int kSB = 4;            // S / P buffers in tensor memory: two per softmax group
+constexpr uint32_t kOBase = kSB * kTok;  // O of softmax group g at kOBase + g * D
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxCtas = 256;     // partial slots in the workspace: one per CTA
 
@@ -130,6 +137,13 @@ struct TileInfo {
 // with up to 16-byte vectors).
 constexpr int align16(int x) { return (x + 15) & ~15; }
 
+// Tile j (counted per CTA) belongs to softmax group j % 2; each group has two
+// S / P buffers, used by its tiles in turn: buffer 2 g + (j / 2) % 2, which
+// completes one phase per use (every fourth tile).
+__device__ __forceinline__ int sbuf(int j) { return 2 * (j & 1) + ((j >> 1) & 1); }
+__device__ __forceinline__ uint32_t sphase(int j) { return (uint32_t)((j >> 2) & 1); }
+static_assert(kSB == 2 * kSG, "two S / P buffers per softmax group");
+
 template <int D>
 struct Layout {
     static constexpr int H = D / 64;                      // 128-byte column halves
@@ -148,8 +162,10 @@ struct Layout {
     static constexpr int mo = align16(tkc + kChunkTiles * 16);        // int [kRows + 4]: members' first own tile
     static constexpr int tinfo = align16(mo + (kRows + 4) * 4);       // TileInfo [NS]
     static constexpr int desc = align16(tinfo + NS * 16);             // Piece [kDescs]
-    static constexpr int bars = align16(desc + kDescs * 32);
-    static constexpr int kBars = 3 * NS + 2 * kSB + 4 + 2 * kDescs;  // k/v full, kv empty, s/p full, o_done[2], ready, fin, descs
+    static constexpr int xch = align16(desc + kDescs * 32);           // float2 [kRows]: group 1's (max, sum) per row
+    static constexpr int bars = align16(xch + kRows * 8);
+    // k/v full, kv empty, s/p full, o_done[2], ready, fin, o_free, xch full/empty, descs
+    static constexpr int kBars = 3 * NS + 2 * kSB + 7 + 2 * kDescs;
     static constexpr int misc = align16(bars + kBars * 8);            // TMEM address, scan scratch, counters
     static constexpr int total = misc + 128 + 1024;                   // + alignment slack
     static_assert(sizeof(Piece) == 32 && sizeof(TileInfo) == 16, "descriptor sizes");
@@ -476,15 +492,19 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     uint64_t *kv_empty = v_full + NS;
     uint64_t *s_full = kv_empty + NS;
     uint64_t *p_full = s_full + kSB;
-    uint64_t *o_done = p_full + kSB;  // [2]: one phase per completed P V of that parity
-    uint64_t *ready = o_done + 2;
+    uint64_t *o_done = p_full + kSB;  // [2]: one phase per completed P V of that parity (softmax group)
+    uint64_t *ready = o_done + 2;     // the next piece's Q is in place
     uint64_t *fin = ready + 1;
-    uint64_t *desc_full = fin + 1;
+    uint64_t *o_free = fin + 1;       // group 0 has read a piece's O parts
+    uint64_t *xch_full = o_free + 1;  // group 1's (max, sum) of a piece are in xch
+    uint64_t *xch_empty = xch_full + 1;
+    uint64_t *desc_full = xch_empty + 1;
     uint64_t *desc_empty = desc_full + kDescs;
+    float2 *xch = reinterpret_cast<float2 *>(smem + L::xch);
 
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
-    int *warp_sums = reinterpret_cast<int *>(smem + L::misc + 16);  // [8] + carry
-    int *counters = reinterpret_cast<int *>(smem + L::misc + 64);   // partial-store / merge warp counters
+    int *warp_sums = reinterpret_cast<int *>(smem + L::misc + 16);  // [12] + carry
+    int *counters = reinterpret_cast<int *>(smem + L::misc + 96);   // partial-store / merge warp counters
     constexpr int kCarry = kThreads / 32;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -611,10 +631,13 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
         mbar_init(ready, 4);
         mbar_init(fin, 1);
+        mbar_init(o_free, 4);
+        mbar_init(xch_full, 4);
+        mbar_init(xch_empty, 4);
 
         for (int i = 0; i < kDescs; ++i) {
             mbar_init(&desc_full[i], 1);
-            mbar_init(&desc_empty[i], 5);
+            mbar_init(&desc_empty[i], 4 * kSG + 1);  // softmax warps and the MMA thread
         }
         fence_barrier_init();
     }
@@ -781,36 +804,30 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             int pq = 0, pp = 0;           // their pieces
             int tq = 0, tp = 0;           // tile within those pieces
             int ntq = -1;                 // tiles of piece pq (-1: descriptor not read yet)
-            // tiles of the pieces between the next P V and the next Q K^T (at most
-            // three: Q K^T runs at most two tiles ahead), in registers
-            int nt0 = 0, nt1 = 0, nt2 = 0, nt3 = 0;
-            auto nt_get = [&](int i) { return i == 0 ? nt0 : (i == 1 ? nt1 : (i == 2 ? nt2 : nt3)); };
-            auto nt_set = [&](int i, int v) {
-                if (i == 0) nt0 = v;
-                else if (i == 1) nt1 = v;
-                else if (i == 2) nt2 = v;
-                else nt3 = v;
-            };
             bool done_q = false, dead = false;
             uint32_t idle = 0;
             for (;;) {
                 bool prog = false;
                 if (jp < jq) {
-                    if (mbar_test_wait(&p_full[jp % kSB], (uint32_t)((jp / kSB) & 1)) &&
-                        mbar_test_wait(&v_full[jp % NS], (uint32_t)((jp / NS) & 1))) {
+                    // P V of tile jp into its softmax group's O; the first P V of a
+                    // piece waits until the previous piece's O has been read
+                    const int sb = sbuf(jp);
+                    if (mbar_test_wait(&p_full[sb], sphase(jp)) &&
+                        mbar_test_wait(&v_full[jp % NS], (uint32_t)((jp / NS) & 1)) &&
+                        (tp > 0 || pp == 0 || mbar_test_wait(o_free, (uint32_t)((pp - 1) & 1)))) {
                         tc::fence_after();
-                        const uint32_t ob = kOBase + (uint32_t)(pp & 1) * D;
-                        const uint32_t pa = tmem + (uint32_t)(jp % kSB) * kTok;  // P in the S columns
+                        const uint32_t ob = kOBase + (uint32_t)(jp & 1) * D;
+                        const uint32_t pa = tmem + (uint32_t)sb * kTok;  // P in the S columns
                         const uint32_t vb = ring_s + (uint32_t)(jp % NS) * L::kStageBytes + L::kKVBytes;
                         const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
 #pragma unroll
                         for (int k = 0; k < kTok / 16; ++k)
                             tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
-                                       (tp == 0 && k == 0) ? 0u : 1u);
+                                       (tp < kSG && k == 0) ? 0u : 1u);  // a group's first tile of the piece starts O
                         tc::commit(&o_done[jp & 1]);
                         tc::commit(&kv_empty[jp % NS]);
                         ++jp;
-                        if (++tp == nt_get(pp & 3)) {
+                        if (++tp == descs[pp % kDescs].ntiles) {
                             mbar_arrive(&desc_empty[pp % kDescs]);
                             ++pp;
                             tp = 0;
@@ -820,14 +837,12 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 } else if (done_q) {
                     break;
                 }
+                // Q K^T of tile jq once its S buffer is free: the buffer's last user,
+                // tile jq - kSB, has had its P V issued (the tensor pipe runs in order)
                 if (!done_q && jq < jp + kSB) {
                     if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
                         ntq = descs[pq % kDescs].ntiles;
-                        if (ntq == 0) {
-                            done_q = true;
-                        } else {
-                            nt_set(pq & 3, ntq);
-                        }
+                        if (ntq == 0) done_q = true;
                         prog = true;
                     }
                     if (ntq > 0 && mbar_test_wait(&k_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
@@ -835,13 +850,14 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         tc::fence_after();
                         const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
                         const uint64_t kd = tc::smem_desc(kb, 16, 1024);
+                        const int sb = sbuf(jq);
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k)
-                            tc::mma(tmem + (uint32_t)(jq % kSB) * kTok,
+                            tc::mma(tmem + (uint32_t)sb * kTok,
                                     qd + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
                                     kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
                                     k > 0 ? 1u : 0u);
-                        tc::commit(&s_full[jq % kSB]);
+                        tc::commit(&s_full[sb]);
                         ++jq;
                         if (++tq == ntq) {
                             ++pq;
@@ -890,20 +906,24 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
         }
-    } else if (warp < 4) {
-        // ======================= softmax (warps 0-3) =======================
-        // thread r owns query row r of the piece (TMEM lane r)
-        const int rr = threadIdx.x;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    } else if (warp < 4 * kSG) {
+        // ======================= softmax (two groups of warps 0-3, 4-7) =======================
+        // Group g takes the tiles j with j % 2 == g of every piece, with its own
+        // running max and sum per row and its own O accumulator in tensor memory
+        // (two independent chains per SM).  Thread rr of a group owns query row
+        // rr = TMEM lane rr.  Group 0 combines both halves of a piece (the two
+        // partial softmax states, as in a split context) and writes the result.
+        const int g = warp >> 2, wq = warp & 3;
+        const int rr = wq * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
         bool dead = false;
-        int j = 0;
         int p = 0;
         // P V of tile x has completed.  o_done[x & 1] completes one phase per P V
-        // of that parity, and a parity wait is only meaningful for the barrier's
-        // current or preceding phase.  So the P of tile j is released only after
-        // P V of tile j - 2 (same barrier) was waited for: every phase is waited
-        // for in order, and a barrier never runs two phases past its waiter (P V
-        // of tile j needs this tile's P).
+        // of that parity (one group's tiles), and a parity wait is only meaningful
+        // for the barrier's current or preceding phase.  So the P of tile j is
+        // released only after P V of tile j - 2 (the group's previous tile) was
+        // waited for: every phase is waited for in order, and a barrier never
+        // runs two phases past its waiter (P V of tile j needs this tile's P).
         auto wait_pv = [&](int x) {
             if (x >= 0) wait_or_flag(&o_done[x & 1], (uint32_t)((x >> 1) & 1), dead, a.err);
         };
@@ -932,37 +952,44 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         };
         Piece pc{};
         if (wait_or_flag(&desc_full[0], 0u, dead, a.err)) pc = descs[0];
-        if (pc.ntiles > 0) {
+        if (g == 0 && pc.ntiles > 0) {
             copy_q(pc);
             q_ready();
         }
+        int j0 = 0;  // the piece's first tile
         while (pc.ntiles > 0 && !dead) {
-            const bool live_warp = warp * 32 < pc.rows;
+            const bool live_warp = wq * 32 < pc.rows;
             const bool live = rr < pc.rows;
             const int my_member = rr / G;
             const int my_pos = pc.pos0 + rr / G;      // multi-token: this row's position
+            const int jl = j0 + pc.ntiles - 1;       // the piece's last tile
             float m_run = -INFINITY, l = 0.f;
             Piece nx{};
-            for (int i = 0; i < pc.ntiles; ++i, ++j) {
-                const int st = (int)(j % NS), b = (int)(j % kSB);
+            bool have_nx = false, copied = false;
+            for (int j = j0 + ((j0 & 1) != g ? 1 : 0); j <= jl; j += kSG) {
+                const int st = j % NS, b = sbuf(j);
                 // the stage's record (ordered by the producer's arrive on k_full)
                 wait_or_flag(&k_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
                 const TileInfo ti = tinfo[st];
-                wait_or_flag(&s_full[b], (uint32_t)((j / kSB) & 1), dead, a.err);
+                wait_or_flag(&s_full[b], sphase(j), dead, a.err);
                 tc::fence_after();
                 if (dead) break;
-                if (i == pc.ntiles - 1) {
+                if (j == jl) {
                     // every Q K^T of this piece has completed: Q may take the next piece's rows
                     const int d = (p + 1) % kDescs;
                     if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
-                    if (nx.ntiles > 0) copy_q(nx);
+                    have_nx = true;
+                    if (nx.ntiles > 0) {
+                        copy_q(nx);
+                        copied = true;
+                    }
                 }
                 // keys past the context's end or in invalid blocks: zero their V rows
                 // (stale slots may hold NaN; a zero weight must meet a zero)
                 if (ti.nvalid < kTok || ti.bad) {
                     wait_or_flag(&v_full[st], (uint32_t)((j / NS) & 1), dead, a.err);  // V landed: zero after it
                     const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
-                    for (int e = threadIdx.x; e < kTok * H * 8; e += 128) {
+                    for (int e = rr; e < kTok * H * 8; e += kRows) {
                         const int key = (e / 8) % kTok, h = e / (kTok * 8), chk = e % 8;
                         const bool zero = key >= ti.nvalid || ((ti.bad >> (key / B)) & 1u);
                         const uint32_t row = vbase + (key / B) * (H * B * 128) + h * (B * 128) + (key % B) * 128;
@@ -982,11 +1009,11 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     const uint32_t sp = trow + b * kTok;
                     softmax_tile<4>(sp, 0, lim, ti.bad, bshift, a.scale_log2, m_run, l, move, alpha);
                     if (__any_sync(0xffffffffu, move)) {
-                        // the running max moved: O (which must hold P V of the previous
-                        // tile first) is rescaled before this tile's P V adds to it
-                        wait_pv(j - 1);
+                        // the running max moved: the group's O (which must hold P V of
+                        // its previous tile first) is rescaled before this tile's P V
+                        wait_pv(j - kSG);
                         tc::fence_after();
-                        const uint32_t ob = kOBase + (uint32_t)(p & 1) * D;
+                        const uint32_t ob = kOBase + (uint32_t)g * D;
 #pragma unroll 1
                         for (int cc = 0; cc < D / 32; ++cc) {
                             float o[32];
@@ -999,22 +1026,54 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         tc::wait_st();
                     }
                 }
-                wait_pv(j - 2);  // keeps this tile's barrier at most one phase ahead
+                wait_pv(j - kSG);  // keeps this tile's barrier at most one phase ahead
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (dead) break;
-            if (nx.ntiles > 0) q_ready();  // the next piece's Q K^T may start
-            // the piece's result: O (TMEM) with each row's running max and sum
-            wait_pv(j - 1);
+            if (!have_nx) {
+                const int d = (p + 1) % kDescs;
+                if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
+            }
+            if (copied) q_ready();  // the next piece's Q K^T may start
+            // this group's part of the piece: its O (TMEM) with each row's running max and sum
+            const bool has0 = pc.ntiles >= kSG || (j0 & 1) == 0, has1 = pc.ntiles >= kSG || (j0 & 1) == 1;
+            const bool has_me = g == 0 ? has0 : has1;
+            if (has_me) wait_pv((jl & 1) == g ? jl : jl - 1);
             tc::fence_after();
-            const uint32_t ob = kOBase + (uint32_t)(p & 1) * D;
-            const int64_t orow = (int64_t)(pc.row_base + (live ? rr / G : 0)) * a.num_heads + pc.kvh * G + rr % G;
-            constexpr int kNc = D / 16;  // 16-column chunks of an O row
-            {
+            if (g == 1) {
+                // hand (max, sum) of every row to group 0, which reads both O parts
+                if (p > 0) wait_or_flag(xch_empty, (uint32_t)((p - 1) & 1), dead, a.err);
+                xch[rr] = has_me ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xch_full);
+            } else {
+                float2 x1 = make_float2(-INFINITY, 0.f);
+                if (wait_or_flag(xch_full, (uint32_t)(p & 1), dead, a.err)) x1 = xch[rr];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xch_empty);
+                tc::fence_after();
+                // both parts on the common max M: o = sum_g O_g 2^(m_g - M), L likewise
+                const float m0 = has0 ? m_run : -INFINITY, m1 = has1 ? x1.x : -INFINITY;
+                const float Mc = fmaxf(m0, m1);
+                const float Mr = Mc == -INFINITY ? 0.f : Mc;
+                const float f0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - Mr);
+                const float f1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - Mr);
+                const float Lc = (has0 ? l : 0.f) * f0 + (has1 ? x1.y : 0.f) * f1;
+                const float M = Mc;
+                auto load_o = [&](int cc, float (&o)[16]) {
+                    // the piece's combined, unnormalised O (16 columns)
+                    float o1[16];
+                    if (has0) ld16(trow + kOBase + cc * 16, o);
+                    if (has1) ld16(trow + kOBase + D + cc * 16, o1);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) o[k] = (has0 ? o[k] * f0 : 0.f) + (has1 ? o1[k] * f1 : 0.f);
+                };
+                const int64_t orow = (int64_t)(pc.row_base + (live ? rr / G : 0)) * a.num_heads + pc.kvh * G + rr % G;
+                constexpr int kNc = D / 16;  // 16-column chunks of an O row
                 // the piece's result: final rows, a partial for the merger, or the merge
-                const float M = m_run, Lc = l;
                 float f = 1.f, e_own = 1.f, Mtr = 0.f;
                 bool got = true;
                 for (int cc = 0; cc < kNc; ++cc) {
@@ -1048,8 +1107,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     }
                     if (live_warp) {
                         float o[16];
-                        ld16(trow + ob + cc * 16, o);
-                        tc::wait_ld();
+                        load_o(cc, o);
                         if (live) {
                             if (pc.kind == kContinue) {
                                 float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * kRows + rr) * D + cc * 16);
@@ -1084,6 +1142,10 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         }
                     }
                 }
+                // both O parts have been read: the next piece's P V may start
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
                 if (pc.kind == kContinue) {
                     // a later piece of a context begun in an earlier share: the partial
                     // is stored; the last warp to finish raises the flag
@@ -1109,6 +1171,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(&desc_empty[p % kDescs]);
             pc = nx;
+            j0 = jl + 1;
             ++p;
         }
         asm volatile("cp.async.wait_all;" ::: "memory");  // no query copy outlives the CTA
