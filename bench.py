@@ -194,11 +194,10 @@ FP8_K_SCALE = FP8_V_SCALE = 1.0 / 64
 
 # DRAM bytes (read + write) of one captured launch of the attention kernel and
 # that launch's algorithmic bytes, from `ncu --set full` of the same command
-# (rotated batch 2); the line reports traffic scaled to the average launch.
+# (rotated batch 0); the line reports traffic scaled to the average launch.
 # Only valid for the kernel build the capture was taken from.
 NCU_TRAFFIC = {
-    ("gqa", "bf16"): (314.15e6, 306.07e6, "profiles/decode_balanced_gqa_full.md"),
-    ("gqa", "fp8"): (158.89e6, 153.57e6, "profiles/decode_fp8_gqa_full.md"),
+    ("gqa", "bf16"): (269.98e6, 263.95e6, "profiles/decode_balanced_gqa_full.md"),
 }
 
 
