@@ -81,7 +81,11 @@ typedef enum pkv_dtype {
 #define PKV_DEVERR_SEQ_LEN 2u   /* seq_len < 0 or above max_seq_len / table capacity */
 #define PKV_DEVERR_SLOT 4u      /* slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEVERR_COPY_PAIR 8u /* block_copy pair outside [0, num_blocks) or src == dst */
-#define PKV_DEVERR_TIMEOUT 16u  /* a bounded wait inside a kernel ran out */
+#define PKV_DEVERR_TIMEOUT 16u  /* a bounded wait inside a kernel ran out; the rows of a
+                                   merge that gave up are NaN.  A piece that arrives after
+                                   its merger gave up may leave its ready flag set: zero
+                                   the call's workspace before reusing it (a CUDA graph
+                                   replays the same flag tag) */
 #define PKV_DEVERR_PREFIX 32u   /* grouped decode: bad group offsets or prefix length, or a
                                    member whose blocks differ from the leader's in the prefix */
 
