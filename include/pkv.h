@@ -281,14 +281,16 @@ PKV_EXPORT pkv_status paged_attention_decode_fp8(void *out, const void *q, const
  *                  sequence with Q_s > L_s is flagged too and its queries that
  *                  see no token get zero rows
  *   workspace      paged_attention_multi_token_workspace_size() bytes,
- *                  256-byte aligned (about 17 MB for head_dim 128, whatever
- *                  the number of tokens: one partial slot of 128 rows per
+ *                  256-byte aligned (about 34 MB for head_dim 128, whatever
+ *                  the number of tokens: one partial slot of 256 rows per
  *                  CTA).  Contents need no initialisation; calls that share a
  *                  workspace must be ordered on the device.
  * The attention runs on the tensor cores (tcgen05): per KV head, the query
  * heads of up to 128 / (num_heads / num_kv_heads) queries form the 128 rows
- * of one context, attended against 64-token tiles of K and V (Q K^T and P V
- * with fp32 accumulators in tensor memory, the causal limit applied per row).
+ * of one query block, attended against 64-token tiles of K and V (Q K^T and
+ * P V with fp32 accumulators in tensor memory, the causal limit applied per
+ * row).  When max_q_len spans more than one block (a prefill chunk), two
+ * consecutive blocks form one context: each tile is read once for both.
  * All contexts' tiles are cut into equal shares, one per SM; a context cut by
  * share boundaries is merged inside the kernel.  The CTAs wait on one another,
  * so the kernel is launched cooperatively: a grid that cannot be resident at

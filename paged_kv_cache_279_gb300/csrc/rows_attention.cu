@@ -137,22 +137,29 @@ struct TileInfo {
 // with up to 16-byte vectors).
 constexpr int align16(int x) { return (x + 15) & ~15; }
 
-// Tile j (counted per CTA) belongs to softmax group j % 2; each group has two
-// S / P buffers, used by its tiles in turn: buffer 2 g + (j / 2) % 2, which
-// completes one phase per use (every fourth tile).
-__device__ __forceinline__ int sbuf(int j) { return 2 * (j & 1) + ((j >> 1) & 1); }
-__device__ __forceinline__ uint32_t sphase(int j) { return (uint32_t)((j >> 2) & 1); }
+// Alternating mode: tile j (counted per CTA) belongs to softmax group j % 2;
+// each group has two S / P buffers, used by its tiles in turn: buffer
+// 2 g + (j / 2) % 2, which completes one phase per use (every fourth tile).
+// Paired mode (a context of two query blocks, one per group): both groups
+// take every tile; group g's buffer for tile j is 2 g + j % 2, one phase per
+// use (every second tile).
+template <bool PAIRED>
+__device__ __forceinline__ int sbuf(int j, int g) { return PAIRED ? 2 * g + (j & 1) : 2 * (j & 1) + ((j >> 1) & 1); }
+template <bool PAIRED>
+__device__ __forceinline__ uint32_t sphase(int j) { return (uint32_t)((PAIRED ? j >> 1 : j >> 2) & 1); }
 static_assert(kSB == 2 * kSG, "two S / P buffers per softmax group");
 
-template <int D>
+template <int D, bool PAIRED>
 struct Layout {
     static constexpr int H = D / 64;                      // 128-byte column halves
-    static constexpr int kQBytes = H * kRows * 128;      // [half][row][128 B]
+    static constexpr int kQTile = H * kRows * 128;        // one group's Q: [half][row][128 B]
+    static constexpr int kQBytes = (PAIRED ? 2 : 1) * kQTile;
     // K of a tile: [half][token][128 B] (one 2-D box per block and half);
     // V of a tile: [block][half][block row][128 B] (one box per block)
     static constexpr int kKVBytes = H * kTok * 128;
     static constexpr int kStageBytes = 2 * kKVBytes;
-    static constexpr int NS = D == 128 ? 5 : 10;         // 160 KB of tiles in flight
+    // 160 KB of Q and tiles in flight (paired: the second Q tile takes a stage)
+    static constexpr int NS = D == 128 ? (PAIRED ? 4 : 5) : (PAIRED ? 9 : 10);
     static constexpr int q = 0;
     static constexpr int ring = q + kQBytes;
     static constexpr int cum = ring + NS * kStageBytes;               // int [kMaxUnits + 4]
@@ -164,8 +171,8 @@ struct Layout {
     static constexpr int desc = align16(tinfo + NS * 16);             // Piece [kDescs]
     static constexpr int xch = align16(desc + kDescs * 32);           // float2 [kRows]: group 1's (max, sum) per row
     static constexpr int bars = align16(xch + kRows * 8);
-    // k/v full, kv empty, s/p full, o_done[2], ready, fin, o_free, xch full/empty, descs
-    static constexpr int kBars = 3 * NS + 2 * kSB + 7 + 2 * kDescs;
+    // k/v full, kv empty, s/p full, o_done[4], ready, fin, o_free[2], xch full/empty, descs
+    static constexpr int kBars = 3 * NS + 2 * kSB + 10 + 2 * kDescs;
     static constexpr int misc = align16(bars + kBars * 8);            // TMEM address, scan scratch, counters
     static constexpr int total = misc + 128 + 1024;                   // + alignment slack
     static_assert(sizeof(Piece) == 32 && sizeof(TileInfo) == 16, "descriptor sizes");
@@ -470,11 +477,120 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, boo
     return true;
 }
 
-template <int D>
+// Paired contexts: the result of one piece for this thread's row: final rows (whole context), a
+// partial in this CTA's slot with its ready flag (a later piece of a context
+// begun in an earlier share), or the merge of the other CTAs' partials (the
+// context's first piece).  M, Lc: the row's max and sum; load_o(cc, o) gives 16
+// unnormalised O columns on the scale of M.  cr: the row within the context
+// (and the slot); `last` + 1 warps finish each piece; o_free_bar is arrived
+// once O has been read.
+template <int D, typename LoadO>
+__device__ __forceinline__ void finish_piece(const Args &a, const Piece &pc, float M, float Lc, LoadO &load_o, int cr,
+                                             int slot_rows, bool live, bool live_warp, int lane, int w_me, int G,
+                                             int last, int *counters, uint64_t *o_free_bar) {
+    const int64_t orow = (int64_t)(pc.row_base + (live ? cr / G : 0)) * a.num_heads + pc.kvh * G + cr % G;
+    constexpr int kNc = D / 16;  // 16-column chunks of an O row
+    // the piece's result: final rows, a partial for the merger, or the merge
+    float f = 1.f, e_own = 1.f, Mtr = 0.f;
+    bool got = true;
+    for (int cc = 0; cc < kNc; ++cc) {
+        if (cc == 0) {
+            if (pc.kind == kWhole) {
+                f = Lc > 0.f ? 1.f / Lc : 0.f;
+            } else if (pc.kind == kContinue) {
+                if (live)
+                    *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * slot_rows + cr) * 2) = make_float2(M, Lc);
+            } else if (live_warp) {
+                // merger: this piece holds the context's first tile and is the
+                // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
+                const int n = pc.w1 - pc.w0;
+                got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
+                if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                float Mt = M;
+                if (live)
+                    for (int w = pc.w0 + 1; w <= pc.w1; ++w)
+                        Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * slot_rows + cr) * 2));
+                Mtr = Mt == -INFINITY ? 0.f : Mt;
+                e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
+                float Ls = Lc * e_own;
+                if (live)
+                    for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * slot_rows + cr);
+                        if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
+                    }
+                // NaN rows when a piece never came (flagged above)
+                f = got ? (Ls > 0.f ? 1.f / Ls : 0.f) : __int_as_float(0x7fc00000);
+            }
+        }
+        if (live_warp) {
+            float o[16];
+            load_o(cc, o);
+            if (live) {
+                if (pc.kind == kContinue) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * slot_rows + cr) * D + cc * 16);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                } else {
+                    if (pc.kind == kMerger) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] *= e_own;
+                        for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * slot_rows + cr);
+                            if (ml.x == -INFINITY) continue;
+                            const float e = ex2_approx(ml.x - Mtr);
+                            const float4 *src =
+                                reinterpret_cast<const float4 *>(a.part_o + ((int64_t)w * slot_rows + cr) * D + cc * 16);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const float4 v = __ldcg(src + k);
+                                o[4 * k] += e * v.x;
+                                o[4 * k + 1] += e * v.y;
+                                o[4 * k + 2] += e * v.z;
+                                o[4 * k + 3] += e * v.w;
+                            }
+                        }
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16);
+                    dst[0] = make_uint4(pack_bf16x2(o[0] * f, o[1] * f), pack_bf16x2(o[2] * f, o[3] * f),
+                                        pack_bf16x2(o[4] * f, o[5] * f), pack_bf16x2(o[6] * f, o[7] * f));
+                    dst[1] = make_uint4(pack_bf16x2(o[8] * f, o[9] * f), pack_bf16x2(o[10] * f, o[11] * f),
+                                        pack_bf16x2(o[12] * f, o[13] * f), pack_bf16x2(o[14] * f, o[15] * f));
+                }
+            }
+        }
+    }
+    // O has been read: the next piece's P V may start
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(o_free_bar);
+    if (pc.kind == kContinue) {
+        // a later piece of a context begun in an earlier share: the partial
+        // is stored; the last warp to finish raises the flag
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane == 0) {
+            fence_acq_rel_gpu();
+            if (atomicAdd(&counters[0], 1) == last) {
+                counters[0] = 0;
+                fence_acq_rel_gpu();
+                *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
+            }
+        }
+    } else if (pc.kind == kMerger) {
+        // the last warp done reading clears the flags (a graph replay reuses the tag)
+        __syncwarp();
+        if (lane == 0 && atomicAdd(&counters[1], 1) == last) {
+            counters[1] = 0;
+            for (int k = 0; k < pc.w1 - pc.w0; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
+        }
+    }
+}
+
+template <int D, bool PAIRED>
 __global__ void __launch_bounds__(kThreads, 1)
 rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const Args a) {
-    using L = Layout<D>;
+    using L = Layout<D, PAIRED>;
     constexpr int H = L::H;
     constexpr int NS = L::NS;
     extern __shared__ unsigned char smem_raw[];
@@ -492,11 +608,13 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     uint64_t *kv_empty = v_full + NS;
     uint64_t *s_full = kv_empty + NS;
     uint64_t *p_full = s_full + kSB;
-    uint64_t *o_done = p_full + kSB;  // [2]: one phase per completed P V of that parity (softmax group)
-    uint64_t *ready = o_done + 2;     // the next piece's Q is in place
+    // [4] one phase per completed P V: alternating mode o_done[j % 2] (the tile's
+    // group), paired mode o_done[2 g + j % 2]
+    uint64_t *o_done = p_full + kSB;
+    uint64_t *ready = o_done + 4;     // the next piece's Q is in place
     uint64_t *fin = ready + 1;
-    uint64_t *o_free = fin + 1;       // group 0 has read a piece's O parts
-    uint64_t *xch_full = o_free + 1;  // group 1's (max, sum) of a piece are in xch
+    uint64_t *o_free = fin + 1;       // [2] a piece's O has been read: by group 0 (both parts) / by group g (paired)
+    uint64_t *xch_full = o_free + 2;  // group 1's (max, sum) of a piece are in xch
     uint64_t *xch_empty = xch_full + 1;
     uint64_t *desc_full = xch_empty + 1;
     uint64_t *desc_empty = desc_full + kDescs;
@@ -622,22 +740,22 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         for (int i = 0; i < NS; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&kv_empty[i], PAIRED ? 2 : 1);  // paired: each group's P V of the tile
         }
         for (int i = 0; i < kSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&o_done[i], 1);
-        mbar_init(ready, 4);
+        for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
+        mbar_init(ready, PAIRED ? 8 : 4);
         mbar_init(fin, 1);
-        mbar_init(o_free, 4);
+        for (int i = 0; i < 2; ++i) mbar_init(&o_free[i], 4);
         mbar_init(xch_full, 4);
         mbar_init(xch_empty, 4);
 
         for (int i = 0; i < kDescs; ++i) {
             mbar_init(&desc_full[i], 1);
-            mbar_init(&desc_empty[i], 4 * kSG + 1);  // softmax warps and the MMA thread
+            mbar_init(&desc_empty[i], 4 * kSG + (PAIRED ? 2 : 1));  // softmax warps and the MMA thread (once per group if paired)
         }
         fence_barrier_init();
     }
@@ -800,85 +918,169 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
 #pragma unroll
             for (int k = 0; k < kTok / 16; ++k) pv_off[k] = (uint32_t)((16 * k / B) * (H * B * 128) + (16 * k % B) * 128);
             const uint64_t qd = tc::smem_desc(q_s, 16, 1024);
-            int jq = 0, jp = 0;           // next Q K^T / P V tile
-            int pq = 0, pp = 0;           // their pieces
-            int tq = 0, tp = 0;           // tile within those pieces
-            int ntq = -1;                 // tiles of piece pq (-1: descriptor not read yet)
-            bool done_q = false, dead = false;
-            uint32_t idle = 0;
-            for (;;) {
-                bool prog = false;
-                if (jp < jq) {
-                    // P V of tile jp into its softmax group's O; the first P V of a
-                    // piece waits until the previous piece's O has been read
-                    const int sb = sbuf(jp);
-                    if (mbar_test_wait(&p_full[sb], sphase(jp)) &&
-                        mbar_test_wait(&v_full[jp % NS], (uint32_t)((jp / NS) & 1)) &&
-                        (tp > 0 || pp == 0 || mbar_test_wait(o_free, (uint32_t)((pp - 1) & 1)))) {
-                        tc::fence_after();
-                        const uint32_t ob = kOBase + (uint32_t)(jp & 1) * D;
-                        const uint32_t pa = tmem + (uint32_t)sb * kTok;  // P in the S columns
-                        const uint32_t vb = ring_s + (uint32_t)(jp % NS) * L::kStageBytes + L::kKVBytes;
-                        const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
+            if constexpr (PAIRED) {
+                // Paired contexts: every tile's Q K^T and P V for both groups (Q of
+                // group g at q + g * kQTile, S / P in its two buffers, O at kOBase + g * D)
+                const uint64_t qd1 = tc::smem_desc(q_s + L::kQTile, 16, 1024);
+                int jq = 0, jp0 = 0, jp1 = 0;  // next Q K^T tile, next P V tile of each group
+                int pq = 0, pp0 = 0, pp1 = 0;  // their pieces
+                int tq = 0, tp0 = 0, tp1 = 0;  // tile within those pieces
+                int ntq = -1;
+                bool done_q = false, dead = false;
+                uint32_t idle = 0;
+                // P V of group g's tile jp (group 1 after group 0: only group 0 clears
+                // the V rows of a partial tile before its P arrives)
+                auto try_pv = [&](int g, int &jpg, int &ppg, int &tpg) -> bool {
+                    if (jpg >= jq || (g == 1 && jpg >= jp0)) return false;
+                    const int sb = sbuf<true>(jpg, g);
+                    if (!(mbar_test_wait(&p_full[sb], sphase<true>(jpg)) &&
+                          mbar_test_wait(&v_full[jpg % NS], (uint32_t)((jpg / NS) & 1)) &&
+                          (tpg > 0 || ppg == 0 || mbar_test_wait(&o_free[g], (uint32_t)((ppg - 1) & 1)))))
+                        return false;
+                    tc::fence_after();
+                    const uint32_t ob = kOBase + (uint32_t)g * D;
+                    const uint32_t pa = tmem + (uint32_t)sb * kTok;
+                    const uint32_t vb = ring_s + (uint32_t)(jpg % NS) * L::kStageBytes + L::kKVBytes;
+                    const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
 #pragma unroll
-                        for (int k = 0; k < kTok / 16; ++k)
-                            tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
-                                       (tp < kSG && k == 0) ? 0u : 1u);  // a group's first tile of the piece starts O
-                        tc::commit(&o_done[jp & 1]);
-                        tc::commit(&kv_empty[jp % NS]);
-                        ++jp;
-                        if (++tp == descs[pp % kDescs].ntiles) {
-                            mbar_arrive(&desc_empty[pp % kDescs]);
-                            ++pp;
-                            tp = 0;
+                    for (int k = 0; k < kTok / 16; ++k)
+                        tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
+                                   (tpg == 0 && k == 0) ? 0u : 1u);
+                    tc::commit(&o_done[2 * g + (jpg & 1)]);
+                    tc::commit(&kv_empty[jpg % NS]);
+                    ++jpg;
+                    if (++tpg == descs[ppg % kDescs].ntiles) {
+                        mbar_arrive(&desc_empty[ppg % kDescs]);
+                        ++ppg;
+                        tpg = 0;
+                    }
+                    return true;
+                };
+                for (;;) {
+                    bool prog = try_pv(0, jp0, pp0, tp0);
+                    prog = try_pv(1, jp1, pp1, tp1) || prog;
+                    if (done_q && jp0 >= jq && jp1 >= jq) break;
+                    if (!done_q && jq < jp0 + 2 && jq < jp1 + 2) {
+                        if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
+                            ntq = descs[pq % kDescs].ntiles;
+                            if (ntq == 0) done_q = true;
+                            prog = true;
                         }
-                        prog = true;
-                    }
-                } else if (done_q) {
-                    break;
-                }
-                // Q K^T of tile jq once its S buffer is free: the buffer's last user,
-                // tile jq - kSB, has had its P V issued (the tensor pipe runs in order)
-                if (!done_q && jq < jp + kSB) {
-                    if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
-                        ntq = descs[pq % kDescs].ntiles;
-                        if (ntq == 0) done_q = true;
-                        prog = true;
-                    }
-                    if (ntq > 0 && mbar_test_wait(&k_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
-                        (tq > 0 || mbar_test_wait(ready, (uint32_t)(pq & 1)))) {
-                        tc::fence_after();
-                        const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
-                        const uint64_t kd = tc::smem_desc(kb, 16, 1024);
-                        const int sb = sbuf(jq);
+                        if (ntq > 0 && mbar_test_wait(&k_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
+                            (tq > 0 || mbar_test_wait(ready, (uint32_t)(pq & 1)))) {
+                            tc::fence_after();
+                            const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
+                            const uint64_t kd = tc::smem_desc(kb, 16, 1024);
 #pragma unroll
-                        for (int k = 0; k < D / 16; ++k)
-                            tc::mma(tmem + (uint32_t)sb * kTok,
-                                    qd + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
-                                    kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
-                                    k > 0 ? 1u : 0u);
-                        tc::commit(&s_full[sb]);
-                        ++jq;
-                        if (++tq == ntq) {
-                            ++pq;
-                            tq = 0;
-                            ntq = -1;
+                            for (int g = 0; g < 2; ++g) {
+                                const int sb = sbuf<true>(jq, g);
+                                const uint64_t qdg = g == 0 ? qd : qd1;
+#pragma unroll
+                                for (int k = 0; k < D / 16; ++k)
+                                    tc::mma(tmem + (uint32_t)sb * kTok,
+                                            qdg + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                                            kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
+                                            k > 0 ? 1u : 0u);
+                                tc::commit(&s_full[sb]);
+                            }
+                            ++jq;
+                            if (++tq == ntq) {
+                                ++pq;
+                                tq = 0;
+                                ntq = -1;
+                            }
+                            prog = true;
                         }
-                        prog = true;
+                    }
+                    if (prog) {
+                        idle = 0;
+                    } else if (++idle > kWaitLimit) {
+                        flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                        dead = true;
+                        break;
                     }
                 }
-                if (prog) {
-                    idle = 0;
-                } else if (++idle > kWaitLimit) {
-                    flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                    dead = true;
-                    break;
+                (void)dead;
+            } else {
+                int jq = 0, jp = 0;           // next Q K^T / P V tile
+                int pq = 0, pp = 0;           // their pieces
+                int tq = 0, tp = 0;           // tile within those pieces
+                int ntq = -1;                 // tiles of piece pq (-1: descriptor not read yet)
+                bool done_q = false, dead = false;
+                uint32_t idle = 0;
+                for (;;) {
+                    bool prog = false;
+                    if (jp < jq) {
+                        // P V of tile jp into its softmax group's O; the first P V of a
+                        // piece waits until the previous piece's O has been read
+                        const int sb = sbuf<false>(jp, 0);
+                        if (mbar_test_wait(&p_full[sb], sphase<false>(jp)) &&
+                            mbar_test_wait(&v_full[jp % NS], (uint32_t)((jp / NS) & 1)) &&
+                            (tp > 0 || pp == 0 || mbar_test_wait(o_free, (uint32_t)((pp - 1) & 1)))) {
+                            tc::fence_after();
+                            const uint32_t ob = kOBase + (uint32_t)(jp & 1) * D;
+                            const uint32_t pa = tmem + (uint32_t)sb * kTok;  // P in the S columns
+                            const uint32_t vb = ring_s + (uint32_t)(jp % NS) * L::kStageBytes + L::kKVBytes;
+                            const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
+    #pragma unroll
+                            for (int k = 0; k < kTok / 16; ++k)
+                                tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
+                                           (tp < kSG && k == 0) ? 0u : 1u);  // a group's first tile of the piece starts O
+                            tc::commit(&o_done[jp & 1]);
+                            tc::commit(&kv_empty[jp % NS]);
+                            ++jp;
+                            if (++tp == descs[pp % kDescs].ntiles) {
+                                mbar_arrive(&desc_empty[pp % kDescs]);
+                                ++pp;
+                                tp = 0;
+                            }
+                            prog = true;
+                        }
+                    } else if (done_q) {
+                        break;
+                    }
+                    // Q K^T of tile jq once its S buffer is free: the buffer's last user,
+                    // tile jq - kSB, has had its P V issued (the tensor pipe runs in order)
+                    if (!done_q && jq < jp + kSB) {
+                        if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
+                            ntq = descs[pq % kDescs].ntiles;
+                            if (ntq == 0) done_q = true;
+                            prog = true;
+                        }
+                        if (ntq > 0 && mbar_test_wait(&k_full[jq % NS], (uint32_t)((jq / NS) & 1)) &&
+                            (tq > 0 || mbar_test_wait(ready, (uint32_t)(pq & 1)))) {
+                            tc::fence_after();
+                            const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
+                            const uint64_t kd = tc::smem_desc(kb, 16, 1024);
+                            const int sb = sbuf<false>(jq, 0);
+    #pragma unroll
+                            for (int k = 0; k < D / 16; ++k)
+                                tc::mma(tmem + (uint32_t)sb * kTok,
+                                        qd + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                                        kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
+                                        k > 0 ? 1u : 0u);
+                            tc::commit(&s_full[sb]);
+                            ++jq;
+                            if (++tq == ntq) {
+                                ++pq;
+                                tq = 0;
+                                ntq = -1;
+                            }
+                            prog = true;
+                        }
+                    }
+                    if (prog) {
+                        idle = 0;
+                    } else if (++idle > kWaitLimit) {
+                        flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                        dead = true;
+                        break;
+                    }
                 }
             }
             // every MMA has completed before the tensor memory is freed
             tc::commit(fin);
             mbar_wait_bounded(fin, 0u);
-            (void)dead;
         }
     } else if (warp == kAuxWarp) {
         // ======================= members' block tables =======================
@@ -907,274 +1109,403 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
         }
     } else if (warp < 4 * kSG) {
-        // ======================= softmax (two groups of warps 0-3, 4-7) =======================
-        // Group g takes the tiles j with j % 2 == g of every piece, with its own
-        // running max and sum per row and its own O accumulator in tensor memory
-        // (two independent chains per SM).  Thread rr of a group owns query row
-        // rr = TMEM lane rr.  Group 0 combines both halves of a piece (the two
-        // partial softmax states, as in a split context) and writes the result.
-        const int g = warp >> 2, wq = warp & 3;
-        const int rr = wq * 32 + lane;
-        const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
-        bool dead = false;
-        int p = 0;
-        // P V of tile x has completed.  o_done[x & 1] completes one phase per P V
-        // of that parity (one group's tiles), and a parity wait is only meaningful
-        // for the barrier's current or preceding phase.  So the P of tile j is
-        // released only after P V of tile j - 2 (the group's previous tile) was
-        // waited for: every phase is waited for in order, and a barrier never
-        // runs two phases past its waiter (P V of tile j needs this tile's P).
-        auto wait_pv = [&](int x) {
-            if (x >= 0) wait_or_flag(&o_done[x & 1], (uint32_t)((x >> 1) & 1), dead, a.err);
-        };
-        // this thread's query row of a piece into Q (128-byte swizzled, K-major; zero past the live rows)
-        auto copy_q = [&](const Piece &pc) {
-            const bool live = rr < pc.rows;
-            const int row = pc.row_base + (live ? rr / G : 0), head = pc.kvh * G + rr % G;
-            const int r = rr;
-            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)row * a.num_heads + head) * D;
+        if constexpr (PAIRED) {
+            // ============ softmax, paired contexts: group g owns rows g * 128 .. ============
+            // Both groups take every tile of a piece; each keeps its rows' running
+            // max and sum and its own O, and writes its rows' result.
+            const int g = warp >> 2, wq = warp & 3;
+            const int rr = wq * 32 + lane;  // TMEM lane and row of the group's Q tile
+            const int cr = g * kRows + rr;  // row of the context
+            const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
+            bool dead = false;
+            int p = 0;
+            // P V of the group's tile x has completed: o_done[2 g + x % 2] completes
+            // one phase per P V of that parity; P of tile j is released only after
+            // P V of tile j - 2 was waited for, so no barrier runs two phases ahead
+            auto wait_pv = [&](int x) {
+                if (x >= 0) wait_or_flag(&o_done[2 * g + (x & 1)], (uint32_t)((x >> 1) & 1), dead, a.err);
+            };
+            auto copy_q = [&](const Piece &pc) {
+                const bool live = cr < pc.rows;
+                const int row = pc.row_base + (live ? cr / G : 0), head = pc.kvh * G + cr % G;
+                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)row * a.num_heads + head) * D;
 #pragma unroll
-            for (int k = 0; k < D / 8; ++k) {
-                const uint32_t dst = q_s + (k >> 3) * (kRows * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
-                if (live)
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k * 8) : "memory");
-                else
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
-            }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        auto q_ready = [&]() {
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            fence_proxy_async();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ready);
-        };
-        Piece pc{};
-        if (wait_or_flag(&desc_full[0], 0u, dead, a.err)) pc = descs[0];
-        if (g == 0 && pc.ntiles > 0) {
-            copy_q(pc);
-            q_ready();
-        }
-        int j0 = 0;  // the piece's first tile
-        while (pc.ntiles > 0 && !dead) {
-            const bool live_warp = wq * 32 < pc.rows;
-            const bool live = rr < pc.rows;
-            const int my_member = rr / G;
-            const int my_pos = pc.pos0 + rr / G;      // multi-token: this row's position
-            const int jl = j0 + pc.ntiles - 1;       // the piece's last tile
-            float m_run = -INFINITY, l = 0.f;
-            Piece nx{};
-            bool have_nx = false, copied = false;
-            for (int j = j0 + ((j0 & 1) != g ? 1 : 0); j <= jl; j += kSG) {
-                const int st = j % NS, b = sbuf(j);
-                // the stage's record (ordered by the producer's arrive on k_full)
-                wait_or_flag(&k_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
-                const TileInfo ti = tinfo[st];
-                wait_or_flag(&s_full[b], sphase(j), dead, a.err);
-                tc::fence_after();
-                if (dead) break;
-                if (j == jl) {
-                    // every Q K^T of this piece has completed: Q may take the next piece's rows
-                    const int d = (p + 1) % kDescs;
-                    if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
-                    have_nx = true;
-                    if (nx.ntiles > 0) {
-                        copy_q(nx);
-                        copied = true;
-                    }
+                for (int k = 0; k < D / 8; ++k) {
+                    const uint32_t dst = q_s + (uint32_t)g * L::kQTile + (k >> 3) * (kRows * 128) + rr * 128 +
+                                         (((k & 7) ^ (rr & 7)) << 4);
+                    if (live)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k * 8) : "memory");
+                    else
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
                 }
-                // keys past the context's end or in invalid blocks: zero their V rows
-                // (stale slots may hold NaN; a zero weight must meet a zero)
-                if (ti.nvalid < kTok || ti.bad) {
-                    wait_or_flag(&v_full[st], (uint32_t)((j / NS) & 1), dead, a.err);  // V landed: zero after it
-                    const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
-                    for (int e = rr; e < kTok * H * 8; e += kRows) {
-                        const int key = (e / 8) % kTok, h = e / (kTok * 8), chk = e % 8;
-                        const bool zero = key >= ti.nvalid || ((ti.bad >> (key / B)) & 1u);
-                        const uint32_t row = vbase + (key / B) * (H * B * 128) + h * (B * 128) + (key % B) * 128;
-                        if (zero) asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(row + chk * 16), "r"(0u) : "memory");
-                    }
-                    fence_proxy_async();
-                }
-                if (live_warp) {
-                    // keys this row sees in this tile: [0, lim) minus invalid blocks
-                    int lim = ti.nvalid;
-                    if (!live) lim = 0;
-                    if (ti.member >= 0 && ti.member != my_member) lim = 0;
-                    if (a.mode == kMulti) lim = min(lim, my_pos - ti.key0 + 1);
-                    const int bshift = B == 8 ? 3 : (B == 16 ? 4 : 5);
-                    bool move = false;
-                    float alpha = 1.f;
-                    const uint32_t sp = trow + b * kTok;
-                    softmax_tile<4>(sp, 0, lim, ti.bad, bshift, a.scale_log2, m_run, l, move, alpha);
-                    if (__any_sync(0xffffffffu, move)) {
-                        // the running max moved: the group's O (which must hold P V of
-                        // its previous tile first) is rescaled before this tile's P V
-                        wait_pv(j - kSG);
-                        tc::fence_after();
-                        const uint32_t ob = kOBase + (uint32_t)g * D;
-#pragma unroll 1
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            float o[32];
-                            tc::ld32(trow + ob + cc * 32, o);
-                            tc::wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                            tc::st32(trow + ob + cc * 32, o);
-                        }
-                        tc::wait_st();
-                    }
-                }
-                wait_pv(j - kSG);  // keeps this tile's barrier at most one phase ahead
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+            auto q_ready = [&]() {
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                fence_proxy_async();
                 tc::fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[b]);
+                if (lane == 0) mbar_arrive(ready);
+            };
+            Piece pc{};
+            if (wait_or_flag(&desc_full[0], 0u, dead, a.err)) pc = descs[0];
+            if (pc.ntiles > 0) {
+                copy_q(pc);
+                q_ready();
             }
-            if (dead) break;
-            if (!have_nx) {
-                const int d = (p + 1) % kDescs;
-                if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
-            }
-            if (copied) q_ready();  // the next piece's Q K^T may start
-            // this group's part of the piece: its O (TMEM) with each row's running max and sum
-            const bool has0 = pc.ntiles >= kSG || (j0 & 1) == 0, has1 = pc.ntiles >= kSG || (j0 & 1) == 1;
-            const bool has_me = g == 0 ? has0 : has1;
-            if (has_me) wait_pv((jl & 1) == g ? jl : jl - 1);
-            tc::fence_after();
-            if (g == 1) {
-                // hand (max, sum) of every row to group 0, which reads both O parts
-                if (p > 0) wait_or_flag(xch_empty, (uint32_t)((p - 1) & 1), dead, a.err);
-                xch[rr] = has_me ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xch_full);
-            } else {
-                float2 x1 = make_float2(-INFINITY, 0.f);
-                if (wait_or_flag(xch_full, (uint32_t)(p & 1), dead, a.err)) x1 = xch[rr];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xch_empty);
-                tc::fence_after();
-                // both parts on the common max M: o = sum_g O_g 2^(m_g - M), L likewise
-                const float m0 = has0 ? m_run : -INFINITY, m1 = has1 ? x1.x : -INFINITY;
-                const float Mc = fmaxf(m0, m1);
-                const float Mr = Mc == -INFINITY ? 0.f : Mc;
-                const float f0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - Mr);
-                const float f1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - Mr);
-                const float Lc = (has0 ? l : 0.f) * f0 + (has1 ? x1.y : 0.f) * f1;
-                const float M = Mc;
-                auto load_o = [&](int cc, float (&o)[16]) {
-                    // the piece's combined, unnormalised O (16 columns)
-                    float o1[16];
-                    if (has0) ld16(trow + kOBase + cc * 16, o);
-                    if (has1) ld16(trow + kOBase + D + cc * 16, o1);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) o[k] = (has0 ? o[k] * f0 : 0.f) + (has1 ? o1[k] * f1 : 0.f);
-                };
-                const int64_t orow = (int64_t)(pc.row_base + (live ? rr / G : 0)) * a.num_heads + pc.kvh * G + rr % G;
-                constexpr int kNc = D / 16;  // 16-column chunks of an O row
-                // the piece's result: final rows, a partial for the merger, or the merge
-                float f = 1.f, e_own = 1.f, Mtr = 0.f;
-                bool got = true;
-                for (int cc = 0; cc < kNc; ++cc) {
-                    if (cc == 0) {
-                        if (pc.kind == kWhole) {
-                            f = Lc > 0.f ? 1.f / Lc : 0.f;
-                        } else if (pc.kind == kContinue) {
-                            if (live)
-                                *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + rr) * 2) = make_float2(M, Lc);
-                        } else if (live_warp) {
-                            // merger: this piece holds the context's first tile and is the
-                            // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
-                            const int n = pc.w1 - pc.w0;
-                            got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
-                            if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                            float Mt = M;
-                            if (live)
-                                for (int w = pc.w0 + 1; w <= pc.w1; ++w)
-                                    Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * kRows + rr) * 2));
-                            Mtr = Mt == -INFINITY ? 0.f : Mt;
-                            e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
-                            float Ls = Lc * e_own;
-                            if (live)
-                                for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
-                                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
-                                    if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
-                                }
-                            // NaN rows when a piece never came (flagged above)
-                            f = got ? (Ls > 0.f ? 1.f / Ls : 0.f) : __int_as_float(0x7fc00000);
+            int j0 = 0;
+            while (pc.ntiles > 0 && !dead) {
+                const bool live_warp = g * kRows + wq * 32 < pc.rows;
+                const bool live = cr < pc.rows;
+                const int my_pos = pc.pos0 + cr / G;  // this row's position
+                const int jl = j0 + pc.ntiles - 1;
+                float m_run = -INFINITY, l = 0.f;
+                Piece nx{};
+                bool copied = false;
+                for (int j = j0; j <= jl; ++j) {
+                    const int st = j % NS, b = sbuf<true>(j, g);
+                    wait_or_flag(&k_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
+                    const TileInfo ti = tinfo[st];
+                    wait_or_flag(&s_full[b], sphase<true>(j), dead, a.err);
+                    tc::fence_after();
+                    if (dead) break;
+                    if (j == jl) {
+                        // every Q K^T of this piece has completed: Q may take the next piece's rows
+                        const int d = (p + 1) % kDescs;
+                        if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
+                        if (nx.ntiles > 0) {
+                            copy_q(nx);
+                            copied = true;
                         }
                     }
+                    // keys past the context's end or in invalid blocks: group 0 zeroes their V
+                    // rows (group 1's P V of a tile is issued after group 0's)
+                    if (g == 0 && (ti.nvalid < kTok || ti.bad)) {
+                        wait_or_flag(&v_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
+                        const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
+                        for (int e = rr; e < kTok * H * 8; e += kRows) {
+                            const int key = (e / 8) % kTok, h = e / (kTok * 8), chk = e % 8;
+                            const bool zero = key >= ti.nvalid || ((ti.bad >> (key / B)) & 1u);
+                            const uint32_t row = vbase + (key / B) * (H * B * 128) + h * (B * 128) + (key % B) * 128;
+                            if (zero) asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(row + chk * 16), "r"(0u) : "memory");
+                        }
+                        fence_proxy_async();
+                    }
                     if (live_warp) {
-                        float o[16];
-                        load_o(cc, o);
-                        if (live) {
-                            if (pc.kind == kContinue) {
-                                float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * kRows + rr) * D + cc * 16);
+                        int lim = live ? min(ti.nvalid, my_pos - ti.key0 + 1) : 0;
+                        const int bshift = B == 8 ? 3 : (B == 16 ? 4 : 5);
+                        bool move = false;
+                        float alpha = 1.f;
+                        const uint32_t sp = trow + b * kTok;
+                        softmax_tile<4>(sp, 0, lim, ti.bad, bshift, a.scale_log2, m_run, l, move, alpha);
+                        if (__any_sync(0xffffffffu, move)) {
+                            wait_pv(j - 1);
+                            tc::fence_after();
+                            const uint32_t ob = kOBase + (uint32_t)g * D;
+#pragma unroll 1
+                            for (int cc = 0; cc < D / 32; ++cc) {
+                                float o[32];
+                                tc::ld32(trow + ob + cc * 32, o);
+                                tc::wait_ld();
 #pragma unroll
-                                for (int k = 0; k < 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                            } else {
-                                if (pc.kind == kMerger) {
-#pragma unroll
-                                    for (int k = 0; k < 16; ++k) o[k] *= e_own;
+                                for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                                tc::st32(trow + ob + cc * 32, o);
+                            }
+                            tc::wait_st();
+                        }
+                    }
+                    wait_pv(j - 2);
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[b]);
+                }
+                if (dead) break;
+                if (copied) q_ready();  // the next piece's Q K^T may start
+                wait_pv(jl);
+                tc::fence_after();
+                auto load_o = [&](int cc, float (&o)[16]) {
+                    ld16(trow + kOBase + (uint32_t)g * D + cc * 16, o);
+                    tc::wait_ld();
+                };
+                finish_piece<D>(a, pc, m_run, l, load_o, cr, 2 * kRows, live, live_warp, lane, w_me, G, 7, counters,
+                                &o_free[g]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&desc_empty[p % kDescs]);
+                pc = nx;
+                j0 = jl + 1;
+                ++p;
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");  // no query copy outlives the CTA
+        } else {
+            // ======================= softmax (two groups of warps 0-3, 4-7) =======================
+            // Group g takes the tiles j with j % 2 == g of every piece, with its own
+            // running max and sum per row and its own O accumulator in tensor memory
+            // (two independent chains per SM).  Thread rr of a group owns query row
+            // rr = TMEM lane rr.  Group 0 combines both halves of a piece (the two
+            // partial softmax states, as in a split context) and writes the result.
+            const int g = warp >> 2, wq = warp & 3;
+            const int rr = wq * 32 + lane;
+            const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
+            bool dead = false;
+            int p = 0;
+            // P V of tile x has completed.  o_done[x & 1] completes one phase per P V
+            // of that parity (one group's tiles), and a parity wait is only meaningful
+            // for the barrier's current or preceding phase.  So the P of tile j is
+            // released only after P V of tile j - 2 (the group's previous tile) was
+            // waited for: every phase is waited for in order, and a barrier never
+            // runs two phases past its waiter (P V of tile j needs this tile's P).
+            auto wait_pv = [&](int x) {
+                if (x >= 0) wait_or_flag(&o_done[x & 1], (uint32_t)((x >> 1) & 1), dead, a.err);
+            };
+            // this thread's query row of a piece into Q (128-byte swizzled, K-major; zero past the live rows)
+            auto copy_q = [&](const Piece &pc) {
+                const bool live = rr < pc.rows;
+                const int row = pc.row_base + (live ? rr / G : 0), head = pc.kvh * G + rr % G;
+                const int r = rr;
+                const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)row * a.num_heads + head) * D;
+    #pragma unroll
+                for (int k = 0; k < D / 8; ++k) {
+                    const uint32_t dst = q_s + (k >> 3) * (kRows * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4);
+                    if (live)
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k * 8) : "memory");
+                    else
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0u) : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+            auto q_ready = [&]() {
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                fence_proxy_async();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ready);
+            };
+            Piece pc{};
+            if (wait_or_flag(&desc_full[0], 0u, dead, a.err)) pc = descs[0];
+            if (g == 0 && pc.ntiles > 0) {
+                copy_q(pc);
+                q_ready();
+            }
+            int j0 = 0;  // the piece's first tile
+            while (pc.ntiles > 0 && !dead) {
+                const bool live_warp = wq * 32 < pc.rows;
+                const bool live = rr < pc.rows;
+                const int my_member = rr / G;
+                const int my_pos = pc.pos0 + rr / G;      // multi-token: this row's position
+                const int jl = j0 + pc.ntiles - 1;       // the piece's last tile
+                float m_run = -INFINITY, l = 0.f;
+                Piece nx{};
+                bool have_nx = false, copied = false;
+                for (int j = j0 + ((j0 & 1) != g ? 1 : 0); j <= jl; j += kSG) {
+                    const int st = j % NS, b = sbuf<false>(j, g);
+                    // the stage's record (ordered by the producer's arrive on k_full)
+                    wait_or_flag(&k_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
+                    const TileInfo ti = tinfo[st];
+                    wait_or_flag(&s_full[b], sphase<false>(j), dead, a.err);
+                    tc::fence_after();
+                    if (dead) break;
+                    if (j == jl) {
+                        // every Q K^T of this piece has completed: Q may take the next piece's rows
+                        const int d = (p + 1) % kDescs;
+                        if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
+                        have_nx = true;
+                        if (nx.ntiles > 0) {
+                            copy_q(nx);
+                            copied = true;
+                        }
+                    }
+                    // keys past the context's end or in invalid blocks: zero their V rows
+                    // (stale slots may hold NaN; a zero weight must meet a zero)
+                    if (ti.nvalid < kTok || ti.bad) {
+                        wait_or_flag(&v_full[st], (uint32_t)((j / NS) & 1), dead, a.err);  // V landed: zero after it
+                        const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
+                        for (int e = rr; e < kTok * H * 8; e += kRows) {
+                            const int key = (e / 8) % kTok, h = e / (kTok * 8), chk = e % 8;
+                            const bool zero = key >= ti.nvalid || ((ti.bad >> (key / B)) & 1u);
+                            const uint32_t row = vbase + (key / B) * (H * B * 128) + h * (B * 128) + (key % B) * 128;
+                            if (zero) asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(row + chk * 16), "r"(0u) : "memory");
+                        }
+                        fence_proxy_async();
+                    }
+                    if (live_warp) {
+                        // keys this row sees in this tile: [0, lim) minus invalid blocks
+                        int lim = ti.nvalid;
+                        if (!live) lim = 0;
+                        if (ti.member >= 0 && ti.member != my_member) lim = 0;
+                        if (a.mode == kMulti) lim = min(lim, my_pos - ti.key0 + 1);
+                        const int bshift = B == 8 ? 3 : (B == 16 ? 4 : 5);
+                        bool move = false;
+                        float alpha = 1.f;
+                        const uint32_t sp = trow + b * kTok;
+                        softmax_tile<4>(sp, 0, lim, ti.bad, bshift, a.scale_log2, m_run, l, move, alpha);
+                        if (__any_sync(0xffffffffu, move)) {
+                            // the running max moved: the group's O (which must hold P V of
+                            // its previous tile first) is rescaled before this tile's P V
+                            wait_pv(j - kSG);
+                            tc::fence_after();
+                            const uint32_t ob = kOBase + (uint32_t)g * D;
+    #pragma unroll 1
+                            for (int cc = 0; cc < D / 32; ++cc) {
+                                float o[32];
+                                tc::ld32(trow + ob + cc * 32, o);
+                                tc::wait_ld();
+    #pragma unroll
+                                for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                                tc::st32(trow + ob + cc * 32, o);
+                            }
+                            tc::wait_st();
+                        }
+                    }
+                    wait_pv(j - kSG);  // keeps this tile's barrier at most one phase ahead
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[b]);
+                }
+                if (dead) break;
+                if (!have_nx) {
+                    const int d = (p + 1) % kDescs;
+                    if (wait_or_flag(&desc_full[d], (uint32_t)(((p + 1) / kDescs) & 1), dead, a.err)) nx = descs[d];
+                }
+                if (copied) q_ready();  // the next piece's Q K^T may start
+                // this group's part of the piece: its O (TMEM) with each row's running max and sum
+                const bool has0 = pc.ntiles >= kSG || (j0 & 1) == 0, has1 = pc.ntiles >= kSG || (j0 & 1) == 1;
+                const bool has_me = g == 0 ? has0 : has1;
+                if (has_me) wait_pv((jl & 1) == g ? jl : jl - 1);
+                tc::fence_after();
+                if (g == 1) {
+                    // hand (max, sum) of every row to group 0, which reads both O parts
+                    if (p > 0) wait_or_flag(xch_empty, (uint32_t)((p - 1) & 1), dead, a.err);
+                    xch[rr] = has_me ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xch_full);
+                } else {
+                    float2 x1 = make_float2(-INFINITY, 0.f);
+                    if (wait_or_flag(xch_full, (uint32_t)(p & 1), dead, a.err)) x1 = xch[rr];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xch_empty);
+                    tc::fence_after();
+                    // both parts on the common max M: o = sum_g O_g 2^(m_g - M), L likewise
+                    const float m0 = has0 ? m_run : -INFINITY, m1 = has1 ? x1.x : -INFINITY;
+                    const float Mc = fmaxf(m0, m1);
+                    const float Mr = Mc == -INFINITY ? 0.f : Mc;
+                    const float f0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - Mr);
+                    const float f1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - Mr);
+                    const float Lc = (has0 ? l : 0.f) * f0 + (has1 ? x1.y : 0.f) * f1;
+                    const float M = Mc;
+                    auto load_o = [&](int cc, float (&o)[16]) {
+                        // the piece's combined, unnormalised O (16 columns)
+                        float o1[16];
+                        if (has0) ld16(trow + kOBase + cc * 16, o);
+                        if (has1) ld16(trow + kOBase + D + cc * 16, o1);
+                        tc::wait_ld();
+    #pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = (has0 ? o[k] * f0 : 0.f) + (has1 ? o1[k] * f1 : 0.f);
+                    };
+                    const int64_t orow = (int64_t)(pc.row_base + (live ? rr / G : 0)) * a.num_heads + pc.kvh * G + rr % G;
+                    constexpr int kNc = D / 16;  // 16-column chunks of an O row
+                    // the piece's result: final rows, a partial for the merger, or the merge
+                    float f = 1.f, e_own = 1.f, Mtr = 0.f;
+                    bool got = true;
+                    for (int cc = 0; cc < kNc; ++cc) {
+                        if (cc == 0) {
+                            if (pc.kind == kWhole) {
+                                f = Lc > 0.f ? 1.f / Lc : 0.f;
+                            } else if (pc.kind == kContinue) {
+                                if (live)
+                                    *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + rr) * 2) = make_float2(M, Lc);
+                            } else if (live_warp) {
+                                // merger: this piece holds the context's first tile and is the
+                                // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
+                                const int n = pc.w1 - pc.w0;
+                                got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
+                                if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                                float Mt = M;
+                                if (live)
+                                    for (int w = pc.w0 + 1; w <= pc.w1; ++w)
+                                        Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * kRows + rr) * 2));
+                                Mtr = Mt == -INFINITY ? 0.f : Mt;
+                                e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
+                                float Ls = Lc * e_own;
+                                if (live)
                                     for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
                                         const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
-                                        if (ml.x == -INFINITY) continue;
-                                        const float e = ex2_approx(ml.x - Mtr);
-                                        const float4 *src =
-                                            reinterpret_cast<const float4 *>(a.part_o + ((int64_t)w * kRows + rr) * D + cc * 16);
-#pragma unroll
-                                        for (int k = 0; k < 4; ++k) {
-                                            const float4 v = __ldcg(src + k);
-                                            o[4 * k] += e * v.x;
-                                            o[4 * k + 1] += e * v.y;
-                                            o[4 * k + 2] += e * v.z;
-                                            o[4 * k + 3] += e * v.w;
+                                        if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
+                                    }
+                                // NaN rows when a piece never came (flagged above)
+                                f = got ? (Ls > 0.f ? 1.f / Ls : 0.f) : __int_as_float(0x7fc00000);
+                            }
+                        }
+                        if (live_warp) {
+                            float o[16];
+                            load_o(cc, o);
+                            if (live) {
+                                if (pc.kind == kContinue) {
+                                    float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * kRows + rr) * D + cc * 16);
+    #pragma unroll
+                                    for (int k = 0; k < 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                                } else {
+                                    if (pc.kind == kMerger) {
+    #pragma unroll
+                                        for (int k = 0; k < 16; ++k) o[k] *= e_own;
+                                        for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                                            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
+                                            if (ml.x == -INFINITY) continue;
+                                            const float e = ex2_approx(ml.x - Mtr);
+                                            const float4 *src =
+                                                reinterpret_cast<const float4 *>(a.part_o + ((int64_t)w * kRows + rr) * D + cc * 16);
+    #pragma unroll
+                                            for (int k = 0; k < 4; ++k) {
+                                                const float4 v = __ldcg(src + k);
+                                                o[4 * k] += e * v.x;
+                                                o[4 * k + 1] += e * v.y;
+                                                o[4 * k + 2] += e * v.z;
+                                                o[4 * k + 3] += e * v.w;
+                                            }
                                         }
                                     }
+                                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16);
+                                    dst[0] = make_uint4(pack_bf16x2(o[0] * f, o[1] * f), pack_bf16x2(o[2] * f, o[3] * f),
+                                                        pack_bf16x2(o[4] * f, o[5] * f), pack_bf16x2(o[6] * f, o[7] * f));
+                                    dst[1] = make_uint4(pack_bf16x2(o[8] * f, o[9] * f), pack_bf16x2(o[10] * f, o[11] * f),
+                                                        pack_bf16x2(o[12] * f, o[13] * f), pack_bf16x2(o[14] * f, o[15] * f));
                                 }
-                                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16);
-                                dst[0] = make_uint4(pack_bf16x2(o[0] * f, o[1] * f), pack_bf16x2(o[2] * f, o[3] * f),
-                                                    pack_bf16x2(o[4] * f, o[5] * f), pack_bf16x2(o[6] * f, o[7] * f));
-                                dst[1] = make_uint4(pack_bf16x2(o[8] * f, o[9] * f), pack_bf16x2(o[10] * f, o[11] * f),
-                                                    pack_bf16x2(o[12] * f, o[13] * f), pack_bf16x2(o[14] * f, o[15] * f));
                             }
                         }
                     }
-                }
-                // both O parts have been read: the next piece's P V may start
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(o_free);
-                if (pc.kind == kContinue) {
-                    // a later piece of a context begun in an earlier share: the partial
-                    // is stored; the last warp to finish raises the flag
-                    fence_acq_rel_gpu();
+                    // both O parts have been read: the next piece's P V may start
+                    tc::fence_before();
                     __syncwarp();
-                    if (lane == 0) {
+                    if (lane == 0) mbar_arrive(o_free);
+                    if (pc.kind == kContinue) {
+                        // a later piece of a context begun in an earlier share: the partial
+                        // is stored; the last warp to finish raises the flag
                         fence_acq_rel_gpu();
-                        if (atomicAdd(&counters[0], 1) == 3) {
-                            counters[0] = 0;
+                        __syncwarp();
+                        if (lane == 0) {
                             fence_acq_rel_gpu();
-                            *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
+                            if (atomicAdd(&counters[0], 1) == 3) {
+                                counters[0] = 0;
+                                fence_acq_rel_gpu();
+                                *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
+                            }
+                        }
+                    } else if (pc.kind == kMerger) {
+                        // the last warp done reading clears the flags (a graph replay reuses the tag)
+                        __syncwarp();
+                        if (lane == 0 && atomicAdd(&counters[1], 1) == 3) {
+                            counters[1] = 0;
+                            for (int k = 0; k < pc.w1 - pc.w0; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
                         }
                     }
-                } else if (pc.kind == kMerger) {
-                    // the last warp done reading clears the flags (a graph replay reuses the tag)
-                    __syncwarp();
-                    if (lane == 0 && atomicAdd(&counters[1], 1) == 3) {
-                        counters[1] = 0;
-                        for (int k = 0; k < pc.w1 - pc.w0; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
-                    }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&desc_empty[p % kDescs]);
+                pc = nx;
+                j0 = jl + 1;
+                ++p;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&desc_empty[p % kDescs]);
-            pc = nx;
-            j0 = jl + 1;
-            ++p;
+            asm volatile("cp.async.wait_all;" ::: "memory");  // no query copy outlives the CTA
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");  // no query copy outlives the CTA
     }
     tc::fence_before();
     __syncthreads();
@@ -1192,12 +1523,13 @@ struct WsLayout {
 };
 
 // Per CTA slot (at most kMaxCtas): the partial (o, max, sum) of its first
-// piece for each of kRows rows, and a ready flag.
-static WsLayout ws_layout(int D) {
+// piece for each of `rows` rows (kRows; 2 kRows for paired contexts), and a
+// ready flag.
+static WsLayout ws_layout(int D, int rows) {
     WsLayout w;
     w.o_off = 0;
-    w.ml_off = round256((size_t)kMaxCtas * kRows * D * 4);
-    w.flags_off = w.ml_off + round256((size_t)kMaxCtas * kRows * 2 * 4);
+    w.ml_off = round256((size_t)kMaxCtas * rows * D * 4);
+    w.flags_off = w.ml_off + round256((size_t)kMaxCtas * rows * 2 * 4);
     w.total = w.flags_off + round256((size_t)kMaxCtas * 8);
     return w;
 }
@@ -1224,11 +1556,11 @@ static bool make_maps(const void *k_cache, const void *v_cache, int64_t rows, in
     return make_cache_map(mk, k_cache, rows, D, B) && make_slab_map(mv, v_cache, rows, D, B);
 }
 
-template <int D>
+template <int D, bool PAIRED>
 static pkv_status launch(const Args &a, const void *k_cache, const void *v_cache, cudaStream_t st) {
-    constexpr int smem = Layout<D>::total;
+    constexpr int smem = Layout<D, PAIRED>::total;
     static bool done[128] = {};
-    auto kern = rows_attention_kernel<D>;
+    auto kern = rows_attention_kernel<D, PAIRED>;
     if (!ensure_smem(kern, smem, done)) return PKV_ERR_CUDA;
     CUtensorMap mk, mv;
     const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * a.block_size;
@@ -1241,12 +1573,16 @@ static pkv_status launch(const Args &a, const void *k_cache, const void *v_cache
     return launch_resident(mode, kern, dim3((unsigned)grid), dim3(kThreads), smem, st, mk, mv, a);
 }
 
-static pkv_status run(Args a, int D, int total_units, const void *k_cache, const void *v_cache, cudaStream_t st) {
+static pkv_status run(Args a, int D, bool paired, int total_units, const void *k_cache, const void *v_cache,
+                      cudaStream_t st) {
     for (int u0 = 0; u0 < total_units; u0 += kMaxUnits) {
         a.unit0 = u0;
         a.num_units = std::min(kMaxUnits, total_units - u0);
         a.tag = next_call_tag();
-        const pkv_status rc = D == 128 ? launch<128>(a, k_cache, v_cache, st) : launch<64>(a, k_cache, v_cache, st);
+        const pkv_status rc = paired ? (D == 128 ? launch<128, true>(a, k_cache, v_cache, st)
+                                                 : launch<64, true>(a, k_cache, v_cache, st))
+                                     : (D == 128 ? launch<128, false>(a, k_cache, v_cache, st)
+                                                 : launch<64, false>(a, k_cache, v_cache, st));
         if (rc != PKV_OK) return rc;
     }
     return PKV_OK;
@@ -1268,20 +1604,21 @@ using namespace pkv;
 PKV_API size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim, int max_seq_len) {
     if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
     if (head_dim != 64 && head_dim != 128) return 0;
-    return rows::ws_layout(head_dim).total;
+    return rows::ws_layout(head_dim, rows::kRows).total;
 }
 
 PKV_API size_t paged_attention_multi_token_workspace_size(int num_q_tokens, int num_heads, int head_dim,
                                                           int max_seq_len) {
     if (num_q_tokens <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
     if (head_dim != 64 && head_dim != 128) return 0;
-    return rows::ws_layout(head_dim).total;
+    return rows::ws_layout(head_dim, 2 * rows::kRows).total;  // room for paired contexts
 }
 
 static bool fill_common(rows::Args &a, void *out, const void *q, const int32_t *block_tables, const int32_t *seq_lens,
                         int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
-                        int num_blocks, int max_seq_len, float scale, void *workspace, size_t workspace_bytes) {
-    const rows::WsLayout lay = rows::ws_layout(head_dim);
+                        int num_blocks, int max_seq_len, float scale, void *workspace, size_t workspace_bytes,
+                        int slot_rows) {
+    const rows::WsLayout lay = rows::ws_layout(head_dim, slot_rows);
     if (!workspace || workspace_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return false;
     a.out = out;
     a.q = q;
@@ -1300,7 +1637,7 @@ static bool fill_common(rows::Args &a, void *out, const void *q, const int32_t *
     a.part_o = reinterpret_cast<float *>(ws + lay.o_off);
     a.part_ml = reinterpret_cast<float *>(ws + lay.ml_off);
     a.flags = reinterpret_cast<unsigned long long *>(ws + lay.flags_off);
-    a.per_ctx = rows::kRows / a.group;
+    a.per_ctx = slot_rows / a.group;
     return true;
 }
 
@@ -1332,7 +1669,7 @@ PKV_API pkv_status paged_attention_decode_grouped(
         return PKV_ERR_UNSUPPORTED;
     rows::Args a{};
     if (!fill_common(a, out, q, block_tables, seq_lens, num_heads, num_kv_heads, head_dim, block_size,
-                     max_blocks_per_seq, num_blocks, max_seq_len, scale, workspace, workspace_bytes))
+                     max_blocks_per_seq, num_blocks, max_seq_len, scale, workspace, workspace_bytes, rows::kRows))
         return PKV_ERR_INVALID;
     a.mode = rows::kGrouped;
     a.group_offsets = group_offsets;
@@ -1348,7 +1685,7 @@ PKV_API pkv_status paged_attention_decode_grouped(
                                                 max_seq_len, PKV_BF16, st);
         if (rc != PKV_OK) return rc;
     }
-    return rows::run(a, head_dim, num_groups, k_cache, v_cache, st);
+    return rows::run(a, head_dim, false, num_groups, k_cache, v_cache, st);
 }
 
 PKV_API pkv_status paged_attention_multi_token(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -1376,13 +1713,17 @@ PKV_API pkv_status paged_attention_multi_token(void *out, const void *q, const v
                             ((max_seq_len + rows::kTok - 1) / rows::kTok);
     if (std::min<int64_t>(num_seqs, rows::kMaxUnits) * num_kv_heads * per_seq > INT32_MAX / 2)
         return PKV_ERR_UNSUPPORTED;
+    // Paired contexts (two 128-row query blocks sharing every tile, one per
+    // softmax group) when a sequence may have more than one block of queries
+    const bool paired = (int64_t)max_q_len * (num_heads / num_kv_heads) > rows::kRows;
     rows::Args a{};
     if (!fill_common(a, out, q, block_tables, seq_lens, num_heads, num_kv_heads, head_dim, block_size,
-                     max_blocks_per_seq, num_blocks, max_seq_len, scale, workspace, workspace_bytes))
+                     max_blocks_per_seq, num_blocks, max_seq_len, scale, workspace, workspace_bytes,
+                     paired ? 2 * rows::kRows : rows::kRows))
         return PKV_ERR_INVALID;
     a.mode = rows::kMulti;
     a.q_starts = q_starts;
     a.num_q_tokens = num_q_tokens;
     a.max_q_len = max_q_len;
-    return rows::run(a, head_dim, num_seqs, k_cache, v_cache, static_cast<cudaStream_t>(stream));
+    return rows::run(a, head_dim, paired, num_seqs, k_cache, v_cache, static_cast<cudaStream_t>(stream));
 }

@@ -121,14 +121,17 @@ def test_multi_token_host_validation_and_workspace():
     assert f(p, p, p, p, p, p, p, 4000, 10, 32, 8, 128, 16, 8, 64, 32768, 1 << 20, 0.1, p, 1 << 30,
              None) == pkv.PKV_ERR_UNSUPPORTED
     ws = lib.paged_attention_multi_token_workspace_size
-    # one slot per CTA (at most 256): 128 rows of a partial (o, max, sum) fp32 and a
-    # ready flag, whatever the number of query tokens or the context length
+    # one slot per CTA (at most 256): 256 rows (a paired context) of a partial
+    # (o, max, sum) fp32 and a ready flag, whatever the number of query tokens or
+    # the context length
     r = lambda x: (x + 255) // 256 * 256
-    fixed = 256 * 128 * 128 * 4 + r(256 * 128 * 2 * 4) + r(256 * 8)
+    fixed = 256 * 256 * 128 * 4 + r(256 * 256 * 2 * 4) + r(256 * 8)
     assert ws(10, 32, 128, 1024) == ws(10, 32, 128, 3000) == ws(5000, 8, 128, 100000) == fixed
-    assert ws(10, 32, 64, 3000) == 256 * 128 * 64 * 4 + r(256 * 128 * 2 * 4) + r(256 * 8)
+    assert ws(10, 32, 64, 3000) == 256 * 256 * 64 * 4 + r(256 * 256 * 2 * 4) + r(256 * 8)
     assert ws(0, 32, 128, 3000) == 0 and ws(10, 32, 96, 3000) == 0
-    assert lib.paged_attention_grouped_workspace_size(256, 64, 128, 1300) == fixed
+    # grouped calls: 128 rows per slot
+    assert lib.paged_attention_grouped_workspace_size(256, 64, 128, 1300) == \
+        256 * 128 * 128 * 4 + r(256 * 128 * 2 * 4) + r(256 * 8)
 
 
 def test_decode_append_fp8_host_validation():
