@@ -279,3 +279,69 @@ def test_decode_append_fp8_equals_write_then_decode(B):
     assert_bf16_close(outB.cpu(), ref, f"fp8 append B={B}")
     assert torch.all(outB[6] == 0)
     assert pkv.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_decode_append_fp8_graph_replays_advance_one_token_each(B):
+    """The serving loop over an E4M3 cache: one paged_attention_decode_append_fp8
+    call captured in a CUDA graph and replayed, the lengths and new bf16 tokens
+    refreshed in place before each replay.  Each replay must quantise and store
+    its tokens at the new position (the oracle's codes, bit for bit), attend over
+    the grown context (oracle over the dequantised codes, the new token's own
+    codes included), and leave later positions untouched."""
+    lens0 = [1, 31, 32, 33, 300, 2047, 64]
+    steps = 4
+    full = [L + steps for L in lens0]
+    Hq, Hkv = 32, 8
+    shape = wl.DecodeShape("fp8_replay", len(lens0), Hq, Hkv, D, B, torch.bfloat16)
+    pool = _pool_with_codes(full, Hkv, B, seed=70 + B)
+    kc, vc = pool["kc"].copy(), pool["vc"].copy()
+    for s, L in enumerate(lens0):  # positions L-1 .. are not in the pool yet: NaN codes there
+        slots = token_slots(pool["tables"][s], full[s], B)[L - 1:]
+        kc[slots // B, :, slots % B, :] = 0x7F
+        vc[slots // B, :, :, slots % B] = 0x7F
+    dev = "cuda"
+    dkc, dvc = torch.from_numpy(kc).to(dev), torch.from_numpy(vc).to(dev)
+    tables = torch.from_numpy(pool["tables"]).to(dev)
+    q = wl.draw_query(shape, seed=71).to(dev)
+    out = torch.empty((len(lens0), Hq, D), dtype=torch.bfloat16, device=dev)
+    sl = torch.tensor(lens0, dtype=torch.int32, device=dev)
+    toks = [_bf16_tokens(len(lens0), Hkv, 80 + r) for r in range(steps + 1)]
+    k_new = torch.empty((len(lens0), Hkv, D), dtype=torch.bfloat16, device=dev)
+    v_new = torch.empty_like(k_new)
+
+    def refresh(rep):
+        sl.copy_(torch.tensor([L + rep for L in lens0], dtype=torch.int32))
+        k_new.copy_(toks[rep][0])
+        v_new.copy_(toks[rep][1])
+
+    call = lambda: pkv.paged_attention_decode_append_fp8(out, q, k_new, v_new, dkc, dvc, tables, sl, shape.scale,
+                                                         K_SCALE, V_SCALE, max(full))
+    refresh(0)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        call()  # warm; stores replay 0's tokens
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            call()
+    kq = [k.copy() for k in pool["kq"]]
+    vq = [v.copy() for v in pool["vq"]]
+    for rep in range(steps + 1):
+        refresh(rep)
+        g.replay()
+        torch.cuda.synchronize()
+        lens = [L + rep for L in lens0]
+        for s, L in enumerate(lens):
+            kq[s][L - 1] = f8.quantize(toks[rep][0][s].float().numpy(), K_SCALE)
+            vq[s][L - 1] = f8.quantize(toks[rep][1][s].float().numpy(), V_SCALE)
+        hk, hv = dkc.cpu().numpy(), dvc.cpu().numpy()
+        for s, L in enumerate(lens):
+            slots = token_slots(pool["tables"][s], full[s], B)
+            assert np.array_equal(hk[slots[:L] // B, :, slots[:L] % B, :], kq[s][:L]), f"K codes, replay {rep}"
+            assert np.array_equal(hv[slots[:L] // B, :, :, slots[:L] % B], vq[s][:L]), f"V codes, replay {rep}"
+            assert (hk[slots[L:] // B, :, slots[L:] % B, :] == 0x7F).all()
+        ref = oracle.decode_attention(q.cpu().float().numpy(), [f8.dequantize(k[:L], K_SCALE) for k, L in zip(kq, lens)],
+                                      [f8.dequantize(v[:L], V_SCALE) for v, L in zip(vq, lens)], shape.scale)
+        assert_bf16_close(out.cpu(), ref, f"fp8 append replay {rep} B={B}")
+    assert pkv.read_device_errors() == 0

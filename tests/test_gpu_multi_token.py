@@ -1,6 +1,8 @@
 """GPU parity of multi-token paged attention (chunked prefill, verification of
 drafted tokens) against the fp64 oracle: each sequence's last Q_s positions
-attend causally over its paged context.  Unowned slots of the pool hold NaN,
+attend causally over its paged context.  Calls whose queries span more than one
+128-row block run as paired contexts (two blocks per context, one per softmax
+group); shorter ones (verification) in the alternating form.  Unowned slots of the pool hold NaN,
 so a read of a masked token would show as a non-finite output."""
 import numpy as np
 import pytest
@@ -62,6 +64,8 @@ def _oracle(c):
     (8, 8, 64, 8, [129, 1100], [16, 9]),                                      # MHA, head_dim 64, block 8
     (64, 8, 128, 32, [2500, 31], [24, 31]),                                   # 8 heads per KV head, block 32
     (12, 4, 64, 32, [1024, 1025, 2049], [8, 8, 8]),                           # partition edges
+    (16, 4, 64, 8, [600, 333, 100], [200, 45, 33]),                           # paired blocks, head_dim 64, block 8
+    (32, 8, 128, 16, [100, 65, 4000], [33, 65, 129]),                         # a pair's second block of 1 query
 ])
 def test_multi_token_matches_oracle(Hq, Hkv, D, B, lens, qlens):
     c = _case(Hq, Hkv, D, B, lens, qlens, seed=Hq + D + B + len(lens))
