@@ -163,9 +163,12 @@ PKV_EXPORT size_t paged_attention_workspace_size(int num_seqs, int num_heads, in
  *                  256 tokens, one per resident warp; a context cut by share
  *                  boundaries is merged inside the attention kernel by the
  *                  warp holding its first tokens, once the other pieces have
- *                  flagged their partials (one kernel per call).  fp32 (or
- *                  more than 8192 sequences) uses 512-token partitions and a
- *                  reduction kernel.
+ *                  flagged their partials (one kernel per call).  Its warps
+ *                  wait on one another, so it is launched cooperatively: a
+ *                  grid that cannot be resident at once fails at launch
+ *                  (PKV_ERR_CUDA) instead of waiting.  fp32 (or more than
+ *                  8192 sequences) uses 512-token partitions and a reduction
+ *                  kernel.
  *   workspace      device scratch of at least paged_attention_workspace_size()
  *                  bytes for the same arguments (may be NULL when that is 0),
  *                  256-byte aligned.  Contents need no initialisation (the
