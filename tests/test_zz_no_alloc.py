@@ -5,10 +5,10 @@ host that only passes input and output buffers, a decode path where
 allocation is forbidden) call paged_attention_decode_noalloc, which keeps
 its split-K partials in an array built into the library instead of a
 caller-provided workspace.  These tests call it through the C ABI and check
-it against paged_attention_decode (same inputs, workspace from PyTorch) on two
-calls in a row, so the second call runs over the first call's leftovers in
-the shared array, and check that a problem too large for the array is
-refused before any launch.
+it against the fp64 oracle and against paged_attention_decode (same inputs,
+workspace from PyTorch) on two calls in a row, so the second call runs over
+the first call's leftovers in the shared array, and check that a problem too
+large for the array is refused before any launch.
 
 The file is named to be collected last: it must pass alone in a fresh
 process and after every other test.
@@ -21,7 +21,8 @@ import torch
 import paged_kv_cache_279_gb300 as pkv
 from paged_kv_cache_279_gb300 import _lib
 from paged_kv_cache_279_gb300 import workloads as wl
-from harness import BF16_MAX_ABS, BF16_MEAN_ABS, F32_MAX_ABS, make_decode_case, run_decode
+from harness import (BF16_MAX_ABS, BF16_MEAN_ABS, F32_MAX_ABS, assert_bf16_close, assert_f32_close,
+                     make_decode_case, oracle_out, run_decode)
 
 pytestmark = pytest.mark.gpu
 
@@ -61,13 +62,16 @@ def test_noalloc_matches_workspace_decode_on_two_calls(dtype):
     shape = wl.DecodeShape("noalloc", 0, 32, 8, 128, 16, dtype)
     # first call: long contexts split into many partitions
     first = make_decode_case(shape, [1, 700, 2048, 33, 1500], seed=21)
+    close = assert_bf16_close if dtype == torch.bfloat16 else assert_f32_close
     st, out1 = call_noalloc(first, shape, partition_size=0)
     assert st == pkv.PKV_OK
+    close(out1.cpu(), oracle_out(first, shape), "noalloc, first call")
     assert_matches(out1, run_decode(first, shape, partition_size=512), dtype)
     # second call in a row: other data and another split over the same array
     second = make_decode_case(shape, [900, 5, 1200], seed=22)
     st, out2 = call_noalloc(second, shape, partition_size=64)
     assert st == pkv.PKV_OK
+    close(out2.cpu(), oracle_out(second, shape), "noalloc, second call")
     assert_matches(out2, run_decode(second, shape, partition_size=64), dtype)
     assert pkv.read_device_errors() == 0
 
