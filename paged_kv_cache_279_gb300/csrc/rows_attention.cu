@@ -21,7 +21,9 @@
 //     zero weight) -- so one context yields every member's final result, with
 //     no separate merge of prefix and own parts;
 //   * multi-token: the tiles up to the block's last query position; row r
-//     sees the keys at or before its own position.
+//     sees the keys at or before its own position.  When queries span more
+//     than one 128-row block (prefill chunks), a context is a pair of
+//     consecutive blocks (paired mode): both read every tile once.
 // All contexts' tiles are laid end to end and every CTA (one per SM,
 // persistent) takes an equal contiguous share.  A context cut by share
 // boundaries is merged inside the kernel: every later piece is the first
@@ -33,14 +35,16 @@
 //
 // Warp roles (384 threads):
 //   warps 0-3, 4-7  two softmax groups; group g takes the tiles j with
-//              j % 2 == g of every piece (two independent chains per SM).
-//              Thread r of a group owns query row r = TMEM lane r.  Reads S
+//              j % 2 == g of every piece (two independent chains per SM);
+//              in paired mode group g owns block g's rows and takes every
+//              tile.  Thread r of a group owns query row r = TMEM lane r.  Reads S
 //              from TMEM, keeps the row's running max and sum, writes P (bf16)
 //              back into the S columns (P is the A operand of P V, taken from
 //              tensor memory), zeroes the V rows of keys past a context's end
 //              and, on a piece's last tile, loads the next piece's queries.
 //              Each group accumulates its own O; group 0 combines the two
-//              partial states of a piece and writes its result.
+//              partial states of a piece and writes its result (paired: each
+//              group writes its own rows).
 //   warp 8     idle.
 //   warp 9     grouped: checks that every member's block table holds the
 //              leader's blocks over the prefix.
