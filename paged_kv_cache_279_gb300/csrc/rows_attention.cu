@@ -45,7 +45,8 @@
 //              Each group accumulates its own O; group 0 combines the two
 //              partial states of a piece and writes its result (paired: each
 //              group writes its own rows).
-//   warp 8     idle.
+//   warp 8     paired contexts: issues softmax group 1's Q K^T and P V (one
+//              thread); idle otherwise.
 //   warp 9     grouped: checks that every member's block table holds the
 //              leader's blocks over the prefix.
 //   warp 10    producer: walks the share, publishes one descriptor per piece,
@@ -54,7 +55,7 @@
 //              ring, with each tile's key range in a per-stage record.
 //   warp 11    MMA: allocates tensor memory; one thread issues Q K^T and P V,
 //              each as soon as its inputs are ready (a late tile does not hold
-//              up the P V of the one before).
+//              up the P V of the one before); paired contexts: group 0's only.
 // Every wait is bounded; on a timeout the kernel flags PKV_DEVERR_TIMEOUT,
 // waits (bounded) for its own copies in flight, frees its tensor memory and
 // returns.
@@ -76,10 +77,11 @@ constexpr int kTok = 64;          // keys per tile
 constexpr int kRows = tc::kRows;  // query rows per context (the MMA's M)
 constexpr int kSG = 2;           // softmax groups (warps 0-3 and 4-7), one chain of tiles each
 constexpr int kThreads = 384;
-// Warp roles.  Warp 8 is idle.  The producer and MMA warps share the
+// Warp roles.  Warp 8 issues group 1's MMAs in paired mode.  The producer and MMA warps share the
 // schedulers of softmax warps 2, 6 and 3, 7, which have no rows when a context
 // has at most 64 (resp. 96) rows.
 constexpr int kAuxWarp = 9, kProducerWarp = 10, kMmaWarp = 11;
+constexpr int kMma1Warp = 8;  // paired contexts: issues softmax group 1's MMAs
 constexpr int kMaxUnits = 1024;   // groups / sequences scanned per launch
 constexpr int kMinTiles = 4;      // shares hold >= 4 tiles unless the total is small
 constexpr int kIdCache = 512;     // block ids staged by the producer
@@ -752,7 +754,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         }
         for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
         mbar_init(ready, PAIRED ? 8 : 4);
-        mbar_init(fin, 1);
+        mbar_init(fin, PAIRED ? 2 : 1);  // one commit per MMA-issuing thread
         for (int i = 0; i < 2; ++i) mbar_init(&o_free[i], 4);
         mbar_init(xch_full, 4);
         mbar_init(xch_empty, 4);
@@ -909,8 +911,8 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 mbar_wait_bounded(&k_full[k % NS], (uint32_t)((k / NS) & 1));
                 mbar_wait_bounded(&v_full[k % NS], (uint32_t)((k / NS) & 1));
             }
-    } else if (warp == kMmaWarp) {
-        // ======================= MMA issuer =======================
+    } else if (warp == kMmaWarp || (PAIRED && warp == kMma1Warp)) {
+        // ======================= MMA issuer(s) =======================
         if (lane == 0) {
             constexpr uint32_t idesc_pv = tc::instr_desc(D, true);
             constexpr uint32_t idesc_qk = tc::instr_desc(kTok, false);
@@ -923,48 +925,48 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             for (int k = 0; k < kTok / 16; ++k) pv_off[k] = (uint32_t)((16 * k / B) * (H * B * 128) + (16 * k % B) * 128);
             const uint64_t qd = tc::smem_desc(q_s, 16, 1024);
             if constexpr (PAIRED) {
-                // Paired contexts: every tile's Q K^T and P V for both groups (Q of
-                // group g at q + g * kQTile, S / P in its two buffers, O at kOBase + g * D)
-                const uint64_t qd1 = tc::smem_desc(q_s + L::kQTile, 16, 1024);
-                int jq = 0, jp0 = 0, jp1 = 0;  // next Q K^T tile, next P V tile of each group
-                int pq = 0, pp0 = 0, pp1 = 0;  // their pieces
-                int tq = 0, tp0 = 0, tp1 = 0;  // tile within those pieces
+                // Paired contexts: group g's Q K^T and P V of every tile (Q at q + g *
+                // kQTile, S / P in the group's two buffers, O at kOBase + g * D), issued
+                // by the group's own thread (warp kMmaWarp: group 0, kMma1Warp: group 1).
+                // One thread issuing both groups' instructions next to busy softmax
+                // warps was the limit; two threads on two schedulers halve it.
+                const int g = warp == kMmaWarp ? 0 : 1;
+                const uint64_t qdg = tc::smem_desc(q_s + (uint32_t)g * L::kQTile, 16, 1024);
+                const uint32_t ob = kOBase + (uint32_t)g * D;
+                int jq = 0, jp = 0;  // next Q K^T tile, next P V tile
+                int pq = 0, pp = 0;  // their pieces
+                int tq = 0, tp = 0;  // tile within those pieces
                 int ntq = -1;
                 bool done_q = false, dead = false;
                 uint32_t idle = 0;
-                // P V of group g's tile jp (group 1 after group 0: only group 0 clears
-                // the V rows of a partial tile before its P arrives)
-                auto try_pv = [&](int g, int &jpg, int &ppg, int &tpg) -> bool {
-                    if (jpg >= jq || (g == 1 && jpg >= jp0)) return false;
-                    const int sb = sbuf<true>(jpg, g);
-                    if (!(mbar_test_wait(&p_full[sb], sphase<true>(jpg)) &&
-                          mbar_test_wait(&v_full[jpg % NS], (uint32_t)((jpg / NS) & 1)) &&
-                          (tpg > 0 || ppg == 0 || mbar_test_wait(&o_free[g], (uint32_t)((ppg - 1) & 1)))))
-                        return false;
-                    tc::fence_after();
-                    const uint32_t ob = kOBase + (uint32_t)g * D;
-                    const uint32_t pa = tmem + (uint32_t)sb * kTok;
-                    const uint32_t vb = ring_s + (uint32_t)(jpg % NS) * L::kStageBytes + L::kKVBytes;
-                    const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
-#pragma unroll
-                    for (int k = 0; k < kTok / 16; ++k)
-                        tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
-                                   (tpg == 0 && k == 0) ? 0u : 1u);
-                    tc::commit(&o_done[2 * g + (jpg & 1)]);
-                    tc::commit(&kv_empty[jpg % NS]);
-                    ++jpg;
-                    if (++tpg == descs[ppg % kDescs].ntiles) {
-                        mbar_arrive(&desc_empty[ppg % kDescs]);
-                        ++ppg;
-                        tpg = 0;
-                    }
-                    return true;
-                };
                 for (;;) {
-                    bool prog = try_pv(0, jp0, pp0, tp0);
-                    prog = try_pv(1, jp1, pp1, tp1) || prog;
-                    if (done_q && jp0 >= jq && jp1 >= jq) break;
-                    if (!done_q && jq < jp0 + 2 && jq < jp1 + 2) {
+                    bool prog = false;
+                    if (jp < jq) {
+                        const int sb = sbuf<true>(jp, g);
+                        if (mbar_test_wait(&p_full[sb], sphase<true>(jp)) &&
+                            mbar_test_wait(&v_full[jp % NS], (uint32_t)((jp / NS) & 1)) &&
+                            (tp > 0 || pp == 0 || mbar_test_wait(&o_free[g], (uint32_t)((pp - 1) & 1)))) {
+                            tc::fence_after();
+                            const uint32_t pa = tmem + (uint32_t)sb * kTok;
+                            const uint32_t vb = ring_s + (uint32_t)(jp % NS) * L::kStageBytes + L::kKVBytes;
+                            const uint64_t vd = tc::smem_desc(vb, pv_lbo, pv_sbo);
+#pragma unroll
+                            for (int k = 0; k < kTok / 16; ++k)
+                                tc::mma_ts(tmem + ob, pa + 8 * k, vd + (uint64_t)(pv_off[k] >> 4), idesc_pv,
+                                           (tp == 0 && k == 0) ? 0u : 1u);
+                            tc::commit(&o_done[2 * g + (jp & 1)]);
+                            tc::commit(&kv_empty[jp % NS]);
+                            ++jp;
+                            if (++tp == descs[pp % kDescs].ntiles) {
+                                mbar_arrive(&desc_empty[pp % kDescs]);
+                                ++pp;
+                                tp = 0;
+                            }
+                            prog = true;
+                        }
+                    }
+                    if (done_q && jp >= jq) break;
+                    if (!done_q && jq < jp + 2) {
                         if (ntq < 0 && mbar_test_wait(&desc_full[pq % kDescs], (uint32_t)((pq / kDescs) & 1))) {
                             ntq = descs[pq % kDescs].ntiles;
                             if (ntq == 0) done_q = true;
@@ -975,18 +977,14 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             tc::fence_after();
                             const uint32_t kb = ring_s + (uint32_t)(jq % NS) * L::kStageBytes;
                             const uint64_t kd = tc::smem_desc(kb, 16, 1024);
+                            const int sb = sbuf<true>(jq, g);
 #pragma unroll
-                            for (int g = 0; g < 2; ++g) {
-                                const int sb = sbuf<true>(jq, g);
-                                const uint64_t qdg = g == 0 ? qd : qd1;
-#pragma unroll
-                                for (int k = 0; k < D / 16; ++k)
-                                    tc::mma(tmem + (uint32_t)sb * kTok,
-                                            qdg + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
-                                            kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
-                                            k > 0 ? 1u : 0u);
-                                tc::commit(&s_full[sb]);
-                            }
+                            for (int k = 0; k < D / 16; ++k)
+                                tc::mma(tmem + (uint32_t)sb * kTok,
+                                        qdg + (uint64_t)(((k >> 2) * (kRows * 128) + (k & 3) * 32) >> 4),
+                                        kd + (uint64_t)(((k >> 2) * (kTok * 128) + (k & 3) * 32) >> 4), idesc_qk,
+                                        k > 0 ? 1u : 0u);
+                            tc::commit(&s_full[sb]);
                             ++jq;
                             if (++tq == ntq) {
                                 ++pq;
@@ -1082,7 +1080,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     }
                 }
             }
-            // every MMA has completed before the tensor memory is freed
+            // every MMA (of both issuing threads) has completed before the tensor memory is freed
             tc::commit(fin);
             mbar_wait_bounded(fin, 0u);
         }
@@ -1182,9 +1180,10 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             copied = true;
                         }
                     }
-                    // keys past the context's end or in invalid blocks: group 0 zeroes their V
-                    // rows (group 1's P V of a tile is issued after group 0's)
-                    if (g == 0 && (ti.nvalid < kTok || ti.bad)) {
+                    // keys past the context's end or in invalid blocks: their V rows are
+                    // zeroed before this group's P is released.  Both groups zero them (the
+                    // same rows, the same zeros), so neither group's P V waits on the other.
+                    if (ti.nvalid < kTok || ti.bad) {
                         wait_or_flag(&v_full[st], (uint32_t)((j / NS) & 1), dead, a.err);
                         const uint32_t vbase = ring_s + st * L::kStageBytes + L::kKVBytes;
                         for (int e = rr; e < kTok * H * 8; e += kRows) {
