@@ -84,6 +84,12 @@ constexpr int kAuxWarp = 9, kProducerWarp = 10, kMmaWarp = 11;
 constexpr int kMma1Warp = 8;  // paired contexts: issues softmax group 1's MMAs
 constexpr int kMaxUnits = 1024;   // groups / sequences scanned per launch
 constexpr int kMinTiles = 4;      // shares hold >= 4 tiles unless the total is small
+// Scheduling charge of a context, in tiles: a context with n tiles is laid out
+// as kPieceTiles virtual tiles (never loaded) and then its n real ones, so that
+// equal shares of the layout also balance the fixed cost of each piece (its
+// queries' load, the combine and the write of its rows) and not only its
+// tiles.  Below kMinTiles, so every share holds a real tile.
+constexpr int kPieceTiles = 3;
 constexpr int kIdCache = 512;     // block ids staged by the producer
 constexpr int kChunkTiles = 128;  // tiles whose keys the producer stages at once
 constexpr int kDescs = 8;         // piece descriptors in flight
@@ -246,10 +252,11 @@ __device__ __forceinline__ int block_last_pos(const Unit &x, int b, int per_ctx)
     return x.L - x.Q + min(x.Q, (b + 1) * per_ctx) - 1;
 }
 
-// Tiles of sub-context `sub` of a unit (for any one KV head).  per_kvh = the
-// unit's tiles per KV head, which is the answer when there is one sub-context.
+// Real tiles of sub-context `sub` of a unit (for any one KV head).  per_kvh =
+// the unit's laid-out tiles per KV head (real and virtual), which gives the
+// answer when there is one sub-context.
 __device__ __forceinline__ int sub_tiles(const Args &a, const Unit &x, int sub, int per_kvh, int cap) {
-    if (x.nsub == 1) return per_kvh;
+    if (x.nsub == 1) return per_kvh > 0 ? per_kvh - kPieceTiles : 0;
     if (a.mode == kGrouped) {
         int n = x.pre / kTok;
         const int c0 = x.m0 + sub * a.per_ctx, c1 = min(x.m1, c0 + a.per_ctx);
@@ -260,8 +267,12 @@ __device__ __forceinline__ int sub_tiles(const Args &a, const Unit &x, int sub, 
     return p < 0 ? 0 : (p + kTok) / kTok;
 }
 
+// Laid-out tiles of a context with n real ones (none when it has none).
+__device__ __forceinline__ int laid_out(int n) { return n > 0 ? n + kPieceTiles : 0; }
+
 // Position in the tile list: context (unit u, kv head, sub-context) with n
-// tiles starting at global tile `start`.
+// laid-out tiles starting at global tile `start` (its first kPieceTiles are
+// virtual).
 struct Ctx {
     int u, kvh, sub, n;
     int64_t start;
@@ -282,7 +293,7 @@ struct Ctx {
         int64_t rem = local - (int64_t)kvh * per_kvh;
         start = cum[u] + (int64_t)kvh * per_kvh;
         for (sub = 0; sub < x.nsub; ++sub) {
-            n = sub_tiles(a, x, sub, per_kvh, cap);
+            n = laid_out(sub_tiles(a, x, sub, per_kvh, cap));
             if (rem < n) return true;
             rem -= n;
             start += n;
@@ -304,7 +315,7 @@ struct Ctx {
                     per_kvh = (cum[u + 1] - cum[u]) / a.num_kv_heads;
                 }
             }
-            n = sub_tiles(a, x, sub, per_kvh, cap);
+            n = laid_out(sub_tiles(a, x, sub, per_kvh, cap));
             if (n > 0) return true;
         }
     }
@@ -675,10 +686,13 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 int pre = min(raw < 0 ? 0 : raw, mn - (a.appended ? 1 : 0));
                 pre = m1 > m0 && pre > 0 ? pre / kTok * kTok : 0;
                 uval[u] = pre;
-                int own = 0;
-                for (int m = m0; m < m1; ++m) own += own_tiles(a, m, pre, cap);
-                const int nch = (m1 - m0 + a.per_ctx - 1) / a.per_ctx;
-                v = Hkv * (nch * (pre / kTok) + own);
+                int tot = 0;  // laid-out tiles of the member chunks (one context each per KV head)
+                for (int c0 = m0; c0 < m1; c0 += a.per_ctx) {
+                    int n = pre / kTok;
+                    for (int m = c0; m < min(m1, c0 + a.per_ctx); ++m) n += own_tiles(a, m, pre, cap);
+                    tot += laid_out(n);
+                }
+                v = Hkv * tot;
             } else {
                 int q0 = a.q_starts[gu], q1 = a.q_starts[gu + 1];
                 if (q0 < 0 || q1 < q0 || q1 > a.num_q_tokens) {
@@ -698,7 +712,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 int t = 0;
                 for (int b = 0; b < nb; ++b) {
                     const int p = block_last_pos(x, b, a.per_ctx);
-                    t += p < 0 ? 0 : (p + kTok) / kTok;
+                    t += laid_out(p < 0 ? 0 : (p + kTok) / kTok);
                 }
                 v = Hkv * t;
             }
@@ -788,7 +802,17 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         const int bpt = kTok / B;  // blocks per tile
         for (int64_t t = s0; t < s1 && !dead;) {
             const int64_t ce = c.start + c.n;
-            const int i0 = (int)(t - c.start), i1 = (int)(min(s1, ce) - c.start);
+            // the context's real tiles in this share; none when the share ends
+            // inside its virtual ones
+            const int i0 = max(0, (int)(t - c.start) - kPieceTiles), i1 = (int)(min(s1, ce) - c.start) - kPieceTiles;
+            if (i1 <= i0) {
+                t = min(s1, ce);
+                if (t < s1 && !c.next(a, cum, uval, cap)) {
+                    if (lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                    dead = true;
+                }
+                continue;
+            }
             int row_base, nrows, pos0;
             c.rows(a, row_base, nrows, pos0);
             // members' first own tiles (grouped): mo[k], k = 0 .. members
@@ -823,9 +847,9 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 pc.rows = nrows;
                 pc.kvh = c.kvh;
                 pc.pos0 = pos0;
-                const bool first_here = c.start >= s0, last_here = ce <= s1;
+                const bool first_here = c.start + kPieceTiles >= s0, last_here = ce <= s1;
                 pc.kind = first_here ? (last_here ? kWhole : kMerger) : kContinue;
-                pc.w0 = (int)share_owner(c.start, T, parts);
+                pc.w0 = (int)share_owner(c.start + kPieceTiles, T, parts);
                 pc.w1 = (int)share_owner(ce - 1, T, parts);
                 descs[d] = pc;
                 mbar_arrive(&desc_full[d]);
@@ -1093,9 +1117,9 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             bool bad = false;
             for (int64_t t = s0; t < s1 && found;) {
                 const int64_t ce = c.start + c.n;
-                const int i0 = (int)(t - c.start), i1 = (int)(min(s1, ce) - c.start);
+                const int i0 = max(0, (int)(t - c.start) - kPieceTiles), i1 = (int)(min(s1, ce) - c.start) - kPieceTiles;
                 const int npt = c.x.pre / kTok;
-                if (c.kvh == 0 && i0 < npt) {
+                if (c.kvh == 0 && i0 < npt && i0 < i1) {
                     const int c0 = c.x.m0 + c.sub * a.per_ctx, c1 = min(c.x.m1, c0 + a.per_ctx);
                     const int lb0 = i0 * bpt, nb = (min(i1, npt) - i0) * bpt;
                     const int32_t *lead = a.block_tables + (int64_t)c.x.m0 * a.max_blocks;
@@ -1668,7 +1692,8 @@ PKV_API pkv_status paged_attention_decode_grouped(
     if (((int64_t)num_blocks + 1) * num_kv_heads * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
     // tile counts of a launch's groups are summed in 32-bit integers
-    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + rows::kTok - 1) / rows::kTok + 1) > INT32_MAX / 2)
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + rows::kTok - 1) / rows::kTok + 1 + rows::kPieceTiles) >
+        INT32_MAX / 2)
         return PKV_ERR_UNSUPPORTED;
     rows::Args a{};
     if (!fill_common(a, out, q, block_tables, seq_lens, num_heads, num_kv_heads, head_dim, block_size,
@@ -1713,7 +1738,7 @@ PKV_API pkv_status paged_attention_multi_token(void *out, const void *q, const v
     if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
     // tiles of a launch's sequences (every query block of every KV head) in 32-bit integers
     const int64_t per_seq = ((int64_t)max_q_len * (num_heads / num_kv_heads) + rows::kRows - 1) / rows::kRows *
-                            ((max_seq_len + rows::kTok - 1) / rows::kTok);
+                            ((max_seq_len + rows::kTok - 1) / rows::kTok + rows::kPieceTiles);
     if (std::min<int64_t>(num_seqs, rows::kMaxUnits) * num_kv_heads * per_seq > INT32_MAX / 2)
         return PKV_ERR_UNSUPPORTED;
     // Paired contexts (two 128-row query blocks sharing every tile, one per
