@@ -181,10 +181,10 @@ struct Layout {
     static constexpr int mo = align16(tkc + kChunkTiles * 16);        // int [kRows + 4]: members' first own tile
     static constexpr int tinfo = align16(mo + (kRows + 4) * 4);       // TileInfo [NS]
     static constexpr int desc = align16(tinfo + NS * 16);             // Piece [kDescs]
-    static constexpr int xch = align16(desc + kDescs * 32);           // float2 [kRows]: group 1's (max, sum) per row
-    static constexpr int bars = align16(xch + kRows * 8);
-    // k/v full, kv empty, s/p full, o_done[4], ready, fin, o_free[2], xch full/empty, descs
-    static constexpr int kBars = 3 * NS + 2 * kSB + 10 + 2 * kDescs;
+    static constexpr int xch = align16(desc + kDescs * 32);           // float2 [2][kRows]: each group's (max, sum) per row
+    static constexpr int bars = align16(xch + 2 * kRows * 8);
+    // k/v full, kv empty, s/p full, o_done[4], ready, fin, o_free[2], xch full[2]/empty[2], descs
+    static constexpr int kBars = 3 * NS + 2 * kSB + 12 + 2 * kDescs;
     static constexpr int misc = align16(bars + kBars * 8);            // TMEM address, scan scratch, counters
     static constexpr int total = misc + 128 + 1024;                   // + alignment slack
     static_assert(sizeof(Piece) == 32 && sizeof(TileInfo) == 16, "descriptor sizes");
@@ -630,10 +630,10 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     uint64_t *o_done = p_full + kSB;
     uint64_t *ready = o_done + 4;     // the next piece's Q is in place
     uint64_t *fin = ready + 1;
-    uint64_t *o_free = fin + 1;       // [2] a piece's O has been read: by group 0 (both parts) / by group g (paired)
-    uint64_t *xch_full = o_free + 2;  // group 1's (max, sum) of a piece are in xch
-    uint64_t *xch_empty = xch_full + 1;
-    uint64_t *desc_full = xch_empty + 1;
+    uint64_t *o_free = fin + 1;       // [2] a piece's O has been read: by both groups (alternating) / by group g (paired)
+    uint64_t *xch_full = o_free + 2;  // [2] group g's (max, sum) of a piece are in xch[g]
+    uint64_t *xch_empty = xch_full + 2;  // [2] the other group has read them
+    uint64_t *desc_full = xch_empty + 2;
     uint64_t *desc_empty = desc_full + kDescs;
     float2 *xch = reinterpret_cast<float2 *>(smem + L::xch);
 
@@ -769,9 +769,11 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         for (int i = 0; i < 4; ++i) mbar_init(&o_done[i], 1);
         mbar_init(ready, PAIRED ? 8 : 4);
         mbar_init(fin, PAIRED ? 2 : 1);  // one commit per MMA-issuing thread
-        for (int i = 0; i < 2; ++i) mbar_init(&o_free[i], 4);
-        mbar_init(xch_full, 4);
-        mbar_init(xch_empty, 4);
+        for (int i = 0; i < 2; ++i) mbar_init(&o_free[i], PAIRED ? 4 : 4 * kSG);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xch_full[i], 4);
+            mbar_init(&xch_empty[i], 4);
+        }
 
         for (int i = 0; i < kDescs; ++i) {
             mbar_init(&desc_full[i], 1);
@@ -1399,25 +1401,30 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 const bool has_me = g == 0 ? has0 : has1;
                 if (has_me) wait_pv((jl & 1) == g ? jl : jl - 1);
                 tc::fence_after();
-                if (g == 1) {
-                    // hand (max, sum) of every row to group 0, which reads both O parts
-                    if (p > 0) wait_or_flag(xch_empty, (uint32_t)((p - 1) & 1), dead, a.err);
-                    xch[rr] = has_me ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xch_full);
-                } else {
-                    float2 x1 = make_float2(-INFINITY, 0.f);
-                    if (wait_or_flag(xch_full, (uint32_t)(p & 1), dead, a.err)) x1 = xch[rr];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xch_empty);
-                    tc::fence_after();
+                // Both groups finish the piece: each hands its rows' (max, sum) to the
+                // other, then combines both O parts for its half of the columns (group
+                // g: 16-column chunks g * kNc / 2 ..), so neither waits while the other
+                // reads tensor memory and writes.
+                if (p > 0) wait_or_flag(&xch_empty[g], (uint32_t)((p - 1) & 1), dead, a.err);
+                const float2 mine = has_me ? make_float2(m_run, l) : make_float2(-INFINITY, 0.f);
+                xch[g * kRows + rr] = mine;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xch_full[g]);
+                float2 other = make_float2(-INFINITY, 0.f);
+                if (wait_or_flag(&xch_full[1 - g], (uint32_t)(p & 1), dead, a.err)) other = xch[(1 - g) * kRows + rr];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xch_empty[1 - g]);
+                tc::fence_after();
+                {
+                    const float2 x0 = g == 0 ? mine : other, x1 = g == 0 ? other : mine;
                     // both parts on the common max M: o = sum_g O_g 2^(m_g - M), L likewise
-                    const float m0 = has0 ? m_run : -INFINITY, m1 = has1 ? x1.x : -INFINITY;
+                    // (the same arithmetic on the same values in both groups)
+                    const float m0 = has0 ? x0.x : -INFINITY, m1 = has1 ? x1.x : -INFINITY;
                     const float Mc = fmaxf(m0, m1);
                     const float Mr = Mc == -INFINITY ? 0.f : Mc;
                     const float f0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - Mr);
                     const float f1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - Mr);
-                    const float Lc = (has0 ? l : 0.f) * f0 + (has1 ? x1.y : 0.f) * f1;
+                    const float Lc = (has0 ? x0.y : 0.f) * f0 + (has1 ? x1.y : 0.f) * f1;
                     const float M = Mc;
                     auto load_o = [&](int cc, float (&o)[16]) {
                         // the piece's combined, unnormalised O (16 columns)
@@ -1433,35 +1440,33 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     // the piece's result: final rows, a partial for the merger, or the merge
                     float f = 1.f, e_own = 1.f, Mtr = 0.f;
                     bool got = true;
-                    for (int cc = 0; cc < kNc; ++cc) {
-                        if (cc == 0) {
-                            if (pc.kind == kWhole) {
-                                f = Lc > 0.f ? 1.f / Lc : 0.f;
-                            } else if (pc.kind == kContinue) {
-                                if (live)
-                                    *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + rr) * 2) = make_float2(M, Lc);
-                            } else if (live_warp) {
-                                // merger: this piece holds the context's first tile and is the
-                                // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
-                                const int n = pc.w1 - pc.w0;
-                                got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
-                                if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
-                                float Mt = M;
-                                if (live)
-                                    for (int w = pc.w0 + 1; w <= pc.w1; ++w)
-                                        Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * kRows + rr) * 2));
-                                Mtr = Mt == -INFINITY ? 0.f : Mt;
-                                e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
-                                float Ls = Lc * e_own;
-                                if (live)
-                                    for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
-                                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
-                                        if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
-                                    }
-                                // NaN rows when a piece never came (flagged above)
-                                f = got ? (Ls > 0.f ? 1.f / Ls : 0.f) : __int_as_float(0x7fc00000);
+                    if (pc.kind == kWhole) {
+                        f = Lc > 0.f ? 1.f / Lc : 0.f;
+                    } else if (pc.kind == kContinue) {
+                        if (live && g == 0)
+                            *reinterpret_cast<float2 *>(a.part_ml + ((int64_t)w_me * kRows + rr) * 2) = make_float2(M, Lc);
+                    } else if (live_warp) {
+                        // merger: this piece holds the context's first tile and is the
+                        // last piece of this share; CTAs w0 + 1 .. w1 stored the rest
+                        const int n = pc.w1 - pc.w0;
+                        got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
+                        if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
+                        float Mt = M;
+                        if (live)
+                            for (int w = pc.w0 + 1; w <= pc.w1; ++w)
+                                Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * kRows + rr) * 2));
+                        Mtr = Mt == -INFINITY ? 0.f : Mt;
+                        e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
+                        float Ls = Lc * e_own;
+                        if (live)
+                            for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
+                                if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
                             }
-                        }
+                        // NaN rows when a piece never came (flagged above)
+                        f = got ? (Ls > 0.f ? 1.f / Ls : 0.f) : __int_as_float(0x7fc00000);
+                    }
+                    for (int cc = g * (kNc / 2); cc < (g + 1) * (kNc / 2); ++cc) {
                         if (live_warp) {
                             float o[16];
                             load_o(cc, o);
@@ -1499,18 +1504,19 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             }
                         }
                     }
-                    // both O parts have been read: the next piece's P V may start
+                    // both O parts of this group's columns have been read: once both
+                    // groups have, the next piece's P V may start
                     tc::fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(o_free);
                     if (pc.kind == kContinue) {
                         // a later piece of a context begun in an earlier share: the partial
-                        // is stored; the last warp to finish raises the flag
+                        // is stored; the last of the eight warps to finish raises the flag
                         fence_acq_rel_gpu();
                         __syncwarp();
                         if (lane == 0) {
                             fence_acq_rel_gpu();
-                            if (atomicAdd(&counters[0], 1) == 3) {
+                            if (atomicAdd(&counters[0], 1) == 4 * kSG - 1) {
                                 counters[0] = 0;
                                 fence_acq_rel_gpu();
                                 *reinterpret_cast<volatile unsigned long long *>(a.flags + w_me) = a.tag;
@@ -1519,7 +1525,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     } else if (pc.kind == kMerger) {
                         // the last warp done reading clears the flags (a graph replay reuses the tag)
                         __syncwarp();
-                        if (lane == 0 && atomicAdd(&counters[1], 1) == 3) {
+                        if (lane == 0 && atomicAdd(&counters[1], 1) == 4 * kSG - 1) {
                             counters[1] = 0;
                             for (int k = 0; k < pc.w1 - pc.w0; ++k) a.flags[pc.w0 + 1 + k] = 0ull;
                         }
