@@ -657,6 +657,11 @@ PKV_EXPORT pkv_status block_allocator_waste(const pkv_allocator *a, int64_t *use
  * code rather than a copy.  Not part of the method: the pages say nothing
  * about how a kernel divides its work.
  *
+ * pkv_balanced_segment_tiles: the tiles a (sequence, kv head) segment of
+ *   `tiles` real tiles takes in the kernel's tile list: the real ones after
+ *   a fixed number of empty lead tiles (a scheduling charge for the piece's
+ *   fixed costs and the merge), 0 for an empty segment; -1 if tiles < 0.
+ *   Shares, slots and ownership below count these laid-out tiles.
  * pkv_balanced_slots: partial slots per (sequence, query head) that the
  *   workspace of a balanced call holds for contexts of up to max_seq_len
  *   tokens (ceil(max_seq_len / 256) + 1); -1 if max_seq_len < 0.
@@ -668,6 +673,7 @@ PKV_EXPORT pkv_status block_allocator_waste(const pkv_allocator *a, int64_t *use
  *   the total_tiles tiles cut into `parts` shares [floor(c T / parts),
  *   floor((c + 1) T / parts)); -1 for arguments out of range.
  */
+PKV_EXPORT int pkv_balanced_segment_tiles(int tiles);
 PKV_EXPORT int pkv_balanced_slots(int max_seq_len);
 PKV_EXPORT int64_t pkv_balanced_split_parts(int64_t total_tiles, int max_segment_tiles, int max_seq_len,
                                             int64_t warps);

@@ -528,6 +528,13 @@ decode_bf16_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 // layout, a cursor over the tile list, share ownership, tile rows.
 // ---------------------------------------------------------------------------
 constexpr int kMinTilesPerCta = 16;  // >= 256 tokens per share: bounds pieces per segment
+// Scheduling charge of a segment, in tiles: a segment with n tiles is laid
+// out as kLeadTiles empty tiles (no loads, nothing attended) and then its n
+// real ones, so that equal shares of the layout also balance the fixed cost
+// of a piece (its queries, the store of its rows or partial) and of the merge,
+// which falls to the warp holding the segment's first laid-out tile.
+constexpr int kLeadTiles = 3;
+__host__ __device__ __forceinline__ int laid_out_tiles(int n) { return n > 0 ? n + kLeadTiles : 0; }
 
 constexpr int kYCache = 256;  // tiles of a CTA whose TMA rows are staged in shared memory (3 CTAs of 4 warps fit an SM up to ~750 sequences)
 constexpr int kRotateTiles = 10;  // a first piece shorter than this is attended last
@@ -1140,8 +1147,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int raw = a.seq_lens[sq];
             if ((raw < 0 || raw > cap) && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
             const int len = clamp_len(raw, cap);
-            v = Hkv * ((len + TT - 1) / TT);
-            my_max = max(my_max, (len + TT - 1) / TT);
+            v = Hkv * laid_out_tiles((len + TT - 1) / TT);
+            my_max = max(my_max, laid_out_tiles((len + TT - 1) / TT));
         }
         int x = v;  // inclusive warp scan
 #pragma unroll
@@ -1263,9 +1270,15 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (i < ncache) {
                 SegCursor c;
                 c.seek(prefix, S, Hkv, cta_lo + i);
-                sq[u] = c.seq;
-                kv[u] = c.kvh;
-                tl[u] = (int)(cta_lo + i - c.seg_start);
+                tl[u] = (int)(cta_lo + i - c.seg_start) - kLeadTiles;  // < 0: a lead tile
+                if (tl[u] >= 0) {
+                    sq[u] = c.seq;
+                    kv[u] = c.kvh;
+                } else {
+                    ycache[i] = make_int2(-1, -1);  // nothing to load or attend
+                    mcache[i] = 0u;
+                    if (APPEND) scache[i] = -1;
+                }
             }
         }
 #pragma unroll
@@ -1329,7 +1342,9 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int2 y = ycache[i];
             return TileRows{y.x, y.y, F8 ? mcache[i] : (mcache[i] & 0xffffu)};
         }
-        return tile_rows<TT>(a, c.seq, c.kvh, (int)(t - c.seg_start), clamp_len(a.seq_lens[c.seq], cap));
+        const int tl = (int)(t - c.seg_start) - kLeadTiles;
+        if (tl < 0) return TileRows{-1, -1, 0u};  // a lead tile: nothing to load or attend
+        return tile_rows<TT>(a, c.seq, c.kvh, tl, clamp_len(a.seq_lens[c.seq], cap));
     };
 
     // k-th tile in walk order
@@ -1417,10 +1432,12 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 __syncwarp();
             }
-            if constexpr (F8)
-                attend_tile_f8<D>(sk, sk + Lay::kKV, rw.mask, qb, qs0, qs1, acc, lane);
-            else
-                attend_tile<D>(sk, sk + Lay::kKV, rw.mask, qb, a.scale_log2, acc, lane);
+            if (rw.mask != 0u) {  // lead tiles have no rows
+                if constexpr (F8)
+                    attend_tile_f8<D>(sk, sk + Lay::kKV, rw.mask, qb, qs0, qs1, acc, lane);
+                else
+                    attend_tile<D>(sk, sk + Lay::kKV, rw.mask, qb, a.scale_log2, acc, lane);
+            }
             __syncwarp();
             if (lane == 0 && k + NS < ntiles) {
                 fence_proxy_async();
@@ -1876,7 +1893,7 @@ static pkv_status decode_impl(void *out, const void *q, const void *k_cache, con
     if (rows > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
     // the balanced path counts tiles of all segments in 32-bit integers
-    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile + kLeadTiles) > INT32_MAX / 2)
         return PKV_ERR_UNSUPPORTED;
 
     const bool balanced = partition_size == 0 && dtype == PKV_BF16 && max_seq_len > 0 &&
@@ -1971,7 +1988,7 @@ static pkv_status decode_fp8_impl(void *out, const void *q, const void *k_cache,
     if (((int64_t)num_blocks + 1) * num_kv_heads * std::max(block_size, head_dim) > INT32_MAX)
         return PKV_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * block_size > INT32_MAX) return PKV_ERR_INVALID;
-    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile) > INT32_MAX / 2)
+    if ((int64_t)num_seqs * num_kv_heads * ((max_seq_len + kTile - 1) / kTile + kLeadTiles) > INT32_MAX / 2)
         return PKV_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (max_seq_len == 0)  // every context is empty: all-zero rows
@@ -2204,6 +2221,8 @@ PKV_API int64_t pkv_balanced_share_owner(int64_t tile, int64_t total_tiles, int6
     if (total_tiles < 1 || parts < 1 || tile < 0 || tile >= total_tiles) return -1;
     return share_owner(tile, total_tiles, parts);
 }
+
+PKV_API int pkv_balanced_segment_tiles(int tiles) { return tiles < 0 ? -1 : laid_out_tiles(tiles); }
 
 PKV_API int pkv_balanced_slots(int max_seq_len) {
     return max_seq_len < 0 ? -1 : (int)balanced_slots(max_seq_len);

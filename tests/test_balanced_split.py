@@ -27,8 +27,9 @@ def lib():
 
 
 def split(lens, hkv, tile, max_seq_len, warps):
-    """Tiles per context, total T, number of shares `parts` (from the library)."""
-    seg = [math.ceil(L / tile) for L in lens for _ in range(hkv)]
+    """Laid-out tiles per context (the real ones after the library's lead
+    tiles), total T, number of shares `parts` (from the library)."""
+    seg = [lib().pkv_balanced_segment_tiles(math.ceil(L / tile)) for L in lens for _ in range(hkv)]
     T = sum(seg)
     slots = lib().pkv_balanced_slots(max_seq_len)
     parts = lib().pkv_balanced_split_parts(T, max(seg) if seg else 0, max_seq_len, warps)
@@ -41,6 +42,9 @@ def share_owner(t, T, parts):
 
 def test_slots_and_bad_arguments():
     L = lib()
+    lead = L.pkv_balanced_segment_tiles(1) - 1
+    assert lead >= 0 and L.pkv_balanced_segment_tiles(0) == 0 and L.pkv_balanced_segment_tiles(-1) == -1
+    assert all(L.pkv_balanced_segment_tiles(n) == n + lead for n in (1, 2, 17, 1000))
     assert L.pkv_balanced_slots(0) == 1 and L.pkv_balanced_slots(256) == 2 and L.pkv_balanced_slots(257) == 3
     assert L.pkv_balanced_slots(-1) == -1
     assert L.pkv_balanced_split_parts(0, 0, 100, 8) == 0
