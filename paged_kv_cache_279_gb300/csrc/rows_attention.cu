@@ -428,8 +428,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint3
         }
     }
     const bool full = (N == 64 ? (lo & hi) : (N == 32 ? lo : (lo & 0xffffu) | ~0xffffu)) == 0xffffffffu;
-#pragma unroll
-    for (int k = 0; k < N; ++k) s[k] *= sl2;  // scores in the log2 domain
     if (!full) {
 #pragma unroll
         for (int k = 0; k < N; ++k) {
@@ -437,6 +435,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint3
             s[k] = (w >> (k & 31)) & 1u ? s[k] : -INFINITY;
         }
     }
+    // Row max of the raw scores, then the log2 scale: sl2 > 0, so the max
+    // commutes with the scaling and its rounding.
     float mx[8];  // row max (tree)
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
@@ -444,7 +444,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint3
     for (int k = 16; k < N; k += 16)
 #pragma unroll
         for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(s[k + q], s[k + 8 + q]));
-    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    const float mt = sl2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
     float m_new = m_run;
     move = false;
     if (mt != -INFINITY) {
@@ -458,14 +459,22 @@ __device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint3
     alpha = move ? ex2_approx(m_run - m_new) : 1.f;
     m_run = m_new;
     const float nm = m_run == -INFINITY ? 0.f : -m_run;
+    // weights 2^(s sl2 - m): the arguments of two keys from one packed FMA; the
+    // denominator sums the fp32 weights (packed adds), P holds them rounded to bf16
+    const uint64_t sl2x2 = f32x2(sl2, sl2), nmx2 = f32x2(nm, nm);
     uint32_t pk[N / 2];
-    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t ls[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int k = 0; k < N / 2; ++k) {
-        pk[k] = pack_bf16x2(ex2_approx(s[2 * k] + nm), ex2_approx(s[2 * k + 1] + nm));
-        ls[k & 3] += bf16x2_lo(pk[k]) + bf16x2_hi(pk[k]);
+        float a0, a1;
+        f32x2_split(fma_f32x2(f32x2(s[2 * k], s[2 * k + 1]), sl2x2, nmx2), a0, a1);
+        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+        pk[k] = pack_bf16x2(e0, e1);
+        ls[k & 3] = add_f32x2(ls[k & 3], f32x2(e0, e1));
     }
-    l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));  // the sum uses the rounded weights
+    float sum[2];
+    f32x2_split(add_f32x2(add_f32x2(ls[0], ls[1]), add_f32x2(ls[2], ls[3])), sum[0], sum[1]);
+    l = l * alpha + (sum[0] + sum[1]);
     // P: 8 columns per 16 keys; this row's groups, then zeros for the others
     const int g0 = c0 >> 4;
     if constexpr (NC == 4) {
