@@ -437,15 +437,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint3
     }
     // Row max of the raw scores, then the log2 scale: sl2 > 0, so the max
     // commutes with the scaling and its rounding.
-    float mx[8];  // row max (tree)
+    float mx[8];  // eight independent chains of three-input maxima over keys q, q + 8, ...
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
+    for (int q = 0; q < 8; ++q) {
+        mx[q] = s[q];
 #pragma unroll
-    for (int k = 16; k < N; k += 16)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(mx[q], fmaxf(s[k + q], s[k + 8 + q]));
-    const float mt = sl2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int k = q + 8; k < N; k += 16) mx[q] = k + 8 < N ? fmax3(mx[q], s[k], s[k + 8]) : fmaxf(mx[q], s[k]);
+    }
+    const float mt = sl2 * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
     float m_new = m_run;
     move = false;
     if (mt != -INFINITY) {
