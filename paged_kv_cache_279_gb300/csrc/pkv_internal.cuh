@@ -187,16 +187,36 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return r;
 }
 
+// 1 / scale when scale is a positive power of two whose reciprocal is a normal
+// float, else 0.  Then x * (1 / scale) is the same real number as x / scale,
+// rounded once, so its codes are the division's, bit for bit.
+__device__ __forceinline__ float pow2_reciprocal(float scale) {
+    const uint32_t b = __float_as_uint(scale);
+    const uint32_t ex = (b >> 23) & 0xffu;
+    return (b & 0x807fffffu) == 0u && ex >= 1u && ex <= 253u ? __uint_as_float((254u - ex) << 23) : 0.f;
+}
+
 __device__ __forceinline__ void quantize16(const uint4 (&x)[2], float scale, uint32_t (&w)[4]) {
     const uint32_t *e = reinterpret_cast<const uint32_t *>(x);
+    const float inv = pow2_reciprocal(scale);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         // bf16 pairs (4 values) -> 4 codes, low byte first
         const uint32_t p0 = e[2 * i], p1 = e[2 * i + 1];
-        const float f0 = __fdiv_rn(__uint_as_float(p0 << 16), scale);
-        const float f1 = __fdiv_rn(__uint_as_float(p0 & 0xffff0000u), scale);
-        const float f2 = __fdiv_rn(__uint_as_float(p1 << 16), scale);
-        const float f3 = __fdiv_rn(__uint_as_float(p1 & 0xffff0000u), scale);
+        const float x0 = __uint_as_float(p0 << 16), x1 = __uint_as_float(p0 & 0xffff0000u);
+        const float x2 = __uint_as_float(p1 << 16), x3 = __uint_as_float(p1 & 0xffff0000u);
+        float f0, f1, f2, f3;
+        if (inv != 0.f) {  // a power-of-two scale: one multiply each
+            f0 = __fmul_rn(x0, inv);
+            f1 = __fmul_rn(x1, inv);
+            f2 = __fmul_rn(x2, inv);
+            f3 = __fmul_rn(x3, inv);
+        } else {
+            f0 = __fdiv_rn(x0, scale);
+            f1 = __fdiv_rn(x1, scale);
+            f2 = __fdiv_rn(x2, scale);
+            f3 = __fdiv_rn(x3, scale);
+        }
         w[i] = e4m3x2(f0, f1) | (e4m3x2(f2, f3) << 16);
     }
 }
