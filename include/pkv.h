@@ -674,6 +674,19 @@ PKV_EXPORT pkv_status block_allocator_waste(const pkv_allocator *a, int64_t *use
  *   floor((c + 1) T / parts)); -1 for arguments out of range.
  */
 PKV_EXPORT int pkv_balanced_segment_tiles(int tiles);
+
+/*
+ * Diagnostics of the rows kernel's split (grouped decode, multi-token
+ * attention; host only, no device work), for host-side tests:
+ * pkv_rows_context_tiles: the tiles a context of `tiles` real 64-key tiles
+ *   takes in the kernel's tile list (its real tiles after a fixed number of
+ *   virtual ones, a scheduling charge), 0 for none; -1 if tiles < 0.
+ * pkv_rows_split_parts: the shares (one per CTA) that total_tiles laid-out
+ *   tiles are cut into with `ctas` CTAs, share c = [floor(c T / parts),
+ *   floor((c + 1) T / parts)); 0 for no tile, -1 for bad arguments.
+ */
+PKV_EXPORT int pkv_rows_context_tiles(int tiles);
+PKV_EXPORT int64_t pkv_rows_split_parts(int64_t total_tiles, int64_t ctas);
 PKV_EXPORT int pkv_balanced_slots(int max_seq_len);
 PKV_EXPORT int64_t pkv_balanced_split_parts(int64_t total_tiles, int max_segment_tiles, int max_seq_len,
                                             int64_t warps);

@@ -80,6 +80,8 @@ SIGNATURES = {
     "block_allocator_refcount": (c_int, [c_void_p, c_int32]),
     "block_allocator_waste": (c_int, [c_void_p, P(c_int64), P(c_int64)]),
     "pkv_balanced_segment_tiles": (c_int, [c_int]),
+    "pkv_rows_context_tiles": (c_int, [c_int]),
+    "pkv_rows_split_parts": (c_int64, [c_int64, c_int64]),
     "pkv_balanced_slots": (c_int, [c_int]),
     "pkv_balanced_split_parts": (c_int64, [c_int64, c_int, c_int, c_int64]),
     "pkv_balanced_share_owner": (c_int64, [c_int64, c_int64, c_int64]),

@@ -268,7 +268,14 @@ __device__ __forceinline__ int sub_tiles(const Args &a, const Unit &x, int sub, 
 }
 
 // Laid-out tiles of a context with n real ones (none when it has none).
-__device__ __forceinline__ int laid_out(int n) { return n > 0 ? n + kPieceTiles : 0; }
+__host__ __device__ __forceinline__ int laid_out(int n) { return n > 0 ? n + kPieceTiles : 0; }
+
+// Shares the T laid-out tiles of a launch are cut into: one per CTA, each of
+// at least kMinTiles tiles unless the total is small.
+__host__ __device__ __forceinline__ int64_t split_parts(int64_t T, int64_t ctas) {
+    const int64_t by_size = T / kMinTiles > 1 ? T / kMinTiles : 1;
+    return ctas < by_size ? ctas : by_size;
+}
 
 // Position in the tile list: context (unit u, kv head, sub-context) with n
 // laid-out tiles starting at global tile `start` (its first kPieceTiles are
@@ -759,7 +766,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         }
     }
 
-    const int64_t parts = min((int64_t)gridDim.x, max((int64_t)1, T / kMinTiles));
+    const int64_t parts = split_parts(T, gridDim.x);
     if (T == 0 || blockIdx.x >= parts) return;  // before any tensor memory is taken
     const int w_me = blockIdx.x;
     const int64_t s0 = (int64_t)w_me * T / parts, s1 = ((int64_t)w_me + 1) * T / parts;
@@ -1641,6 +1648,14 @@ pkv_status append_new_tokens(const void *k_new, const void *v_new, void *k_cache
 }  // namespace pkv
 
 using namespace pkv;
+
+// Diagnostics of the rows kernel's split (host only), for host-side tests.
+PKV_API int pkv_rows_context_tiles(int tiles) { return tiles < 0 ? -1 : rows::laid_out(tiles); }
+
+PKV_API int64_t pkv_rows_split_parts(int64_t total_tiles, int64_t ctas) {
+    if (total_tiles < 0 || ctas < 1) return -1;
+    return total_tiles == 0 ? 0 : rows::split_parts(total_tiles, ctas);
+}
 
 PKV_API size_t paged_attention_grouped_workspace_size(int num_seqs, int num_heads, int head_dim, int max_seq_len) {
     if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len <= 0) return 0;
