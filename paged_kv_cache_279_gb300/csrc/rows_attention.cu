@@ -24,12 +24,14 @@
 //     sees the keys at or before its own position.  When queries span more
 //     than one 128-row block (prefill chunks), a context is a pair of
 //     consecutive blocks (paired mode): both read every tile once.
-// All contexts' tiles are laid end to end and every CTA (one per SM,
-// persistent) takes an equal contiguous share.  A context cut by share
-// boundaries is merged inside the kernel: every later piece is the first
-// piece of its CTA's share, whose CTA stores a partial (o, m, l) per row in
-// its own slot and raises its flag; the CTA holding the context's first tile
-// (its share's last piece) waits for those flags and merges.  Every CTA is
+// All contexts' tiles are laid end to end, each context behind a few virtual
+// tiles that nothing loads (a scheduling charge for its fixed costs), and
+// every CTA (one per SM, persistent) takes an equal contiguous share.  A
+// context cut by share boundaries is merged inside the kernel: every later
+// piece is the first piece of its CTA's share, whose CTA stores a partial
+// (o, m, l) per row in its own slot and raises its flag; the CTA holding the
+// context's first real tile (its share's last piece) waits for those flags
+// and merges.  Every CTA is
 // resident at once (cooperative launch), and a CTA never waits for a piece
 // later in its own share, so no chain of waits can close.
 //
@@ -42,9 +44,10 @@
 //              back into the S columns (P is the A operand of P V, taken from
 //              tensor memory), zeroes the V rows of keys past a context's end
 //              and, on a piece's last tile, loads the next piece's queries.
-//              Each group accumulates its own O; group 0 combines the two
-//              partial states of a piece and writes its result (paired: each
-//              group writes its own rows).
+//              Each group accumulates its own O; at a piece's end the groups
+//              exchange their rows' (max, sum) and each combines the two
+//              partial states for half of the columns and writes them
+//              (paired: each group writes its own rows).
 //   warp 8     paired contexts: issues softmax group 1's Q K^T and P V (one
 //              thread); idle otherwise.
 //   warp 9     grouped: checks that every member's block table holds the
