@@ -1288,8 +1288,9 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             // Group g takes the tiles j with j % 2 == g of every piece, with its own
             // running max and sum per row and its own O accumulator in tensor memory
             // (two independent chains per SM).  Thread rr of a group owns query row
-            // rr = TMEM lane rr.  Group 0 combines both halves of a piece (the two
-            // partial softmax states, as in a split context) and writes the result.
+            // rr = TMEM lane rr.  At a piece's end the two groups' partial softmax
+            // states are combined (as in a split context), each group taking half
+            // of the columns.
             const int g = warp >> 2, wq = warp & 3;
             const int rr = wq * 32 + lane;
             const uint32_t trow = tmem + ((uint32_t)(wq * 32) << 16);
