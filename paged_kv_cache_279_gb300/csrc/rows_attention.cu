@@ -695,10 +695,15 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 const int align = B > 16 ? B : 16;
                 if (blockIdx.x == 0 && (raw < 0 || raw % align != 0)) flag_error(a.err, PKV_DEVERR_PREFIX);
                 int mn = cap;
-                for (int m = m0; m < m1; ++m) {
-                    const int raw_len = a.seq_lens[m];
-                    if (blockIdx.x == 0 && (raw_len < 0 || raw_len > cap)) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
-                    mn = min(mn, clamp_len(raw_len, cap));
+                for (int mb = m0; mb < m1; mb += 8) {
+                    int raw[8];  // eight members' lengths in flight at once
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) raw[k] = mb + k < m1 ? a.seq_lens[mb + k] : cap;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if (blockIdx.x == 0 && (raw[k] < 0 || raw[k] > cap)) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
+                        mn = min(mn, clamp_len(raw[k], cap));
+                    }
                 }
                 // with an append, every member's new token stays in its own part
                 int pre = min(raw < 0 ? 0 : raw, mn - (a.appended ? 1 : 0));
