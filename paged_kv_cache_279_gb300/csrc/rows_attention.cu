@@ -186,8 +186,8 @@ struct Layout {
     static constexpr int desc = align16(tinfo + NS * 16);             // Piece [kDescs]
     static constexpr int xch = align16(desc + kDescs * 32);           // float2 [2][kRows]: each group's (max, sum) per row
     static constexpr int bars = align16(xch + 2 * kRows * 8);
-    // k/v full, kv empty, s/p full, o_done[4], ready, fin, o_free[2], xch full[2]/empty[2], descs
-    static constexpr int kBars = 3 * NS + 2 * kSB + 12 + 2 * kDescs;
+    // k/v full, kv empty, s/p full, o_done[4], ready, fin, o_free[2], xch full[2]/empty[2], o_last[2], descs
+    static constexpr int kBars = 3 * NS + 2 * kSB + 14 + 2 * kDescs;
     static constexpr int misc = align16(bars + kBars * 8);            // TMEM address, scan scratch, counters
     static constexpr int total = misc + 128 + 1024;                   // + alignment slack
     static_assert(sizeof(Piece) == 32 && sizeof(TileInfo) == 16, "descriptor sizes");
@@ -651,7 +651,8 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     uint64_t *o_free = fin + 1;       // [2] a piece's O has been read: by both groups (alternating) / by group g (paired)
     uint64_t *xch_full = o_free + 2;  // [2] group g's (max, sum) of a piece are in xch[g]
     uint64_t *xch_empty = xch_full + 2;  // [2] the other group has read them
-    uint64_t *desc_full = xch_empty + 2;
+    uint64_t *o_last = xch_empty + 2;    // [2] alternating mode: every P V of a piece has completed (per group)
+    uint64_t *desc_full = o_last + 2;
     uint64_t *desc_empty = desc_full + kDescs;
     float2 *xch = reinterpret_cast<float2 *>(smem + L::xch);
 
@@ -796,6 +797,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         for (int i = 0; i < 2; ++i) {
             mbar_init(&xch_full[i], 4);
             mbar_init(&xch_empty[i], 4);
+            mbar_init(&o_last[i], 1);
         }
 
         for (int i = 0; i < kDescs; ++i) {
@@ -1081,6 +1083,10 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             tc::commit(&kv_empty[jp % NS]);
                             ++jp;
                             if (++tp == descs[pp % kDescs].ntiles) {
+                                // the piece's P V are all issued: one phase of o_last per
+                                // group (its softmax waits for it before reading O)
+                                tc::commit(&o_last[0]);
+                                tc::commit(&o_last[1]);
                                 mbar_arrive(&desc_empty[pp % kDescs]);
                                 ++pp;
                                 tp = 0;
@@ -1171,8 +1177,12 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             bool dead = false;
             int p = 0;
             // P V of the group's tile x has completed: o_done[2 g + x % 2] completes
-            // one phase per P V of that parity; P of tile j is released only after
-            // P V of tile j - 2 was waited for, so no barrier runs two phases ahead
+            // one phase per P V of that parity.  A wait for tile x is only made once
+            // S of tile x (or a later one) has landed: the group's MMA thread issued
+            // Q K^T of x after P V of x - 2 (that S buffer's previous user), and a
+            // commit signals only when every earlier MMA of its thread is done, so
+            // the barrier's previous phase (tile x - 2) is complete, and its next one
+            // (tile x + 2) cannot be, P V of x + 2 needing P that is not yet out.
             auto wait_pv = [&](int x) {
                 if (x >= 0) wait_or_flag(&o_done[2 * g + (x & 1)], (uint32_t)((x >> 1) & 1), dead, a.err);
             };
@@ -1266,13 +1276,13 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             tc::wait_st();
                         }
                     }
-                    wait_pv(j - 2);
                     tc::fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p_full[b]);
                 }
                 if (dead) break;
                 if (copied) q_ready();  // the next piece's Q K^T may start
+                wait_pv(jl - 1);  // the group's last P V of each parity, in order
                 wait_pv(jl);
                 tc::fence_after();
                 auto load_o = [&](int cc, float (&o)[16]) {
@@ -1303,10 +1313,13 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             int p = 0;
             // P V of tile x has completed.  o_done[x & 1] completes one phase per P V
             // of that parity (one group's tiles), and a parity wait is only meaningful
-            // for the barrier's current or preceding phase.  So the P of tile j is
-            // released only after P V of tile j - 2 (the group's previous tile) was
-            // waited for: every phase is waited for in order, and a barrier never
-            // runs two phases past its waiter (P V of tile j needs this tile's P).
+            // for the barrier's current or preceding phase.  It is waited for only
+            // before a rescale of O, for the group's tile j - 2 once S of its tile j
+            // has landed: the MMA thread issued Q K^T of j after P V of j - 4 (the S
+            // buffer's previous user), and a commit signals only when every earlier
+            // MMA of the thread is done, so the previous phase is complete and the
+            // next (P V of j, needing P that is not yet out) is not.  At a piece's
+            // end the group waits on o_last instead: one phase per piece.
             auto wait_pv = [&](int x) {
                 if (x >= 0) wait_or_flag(&o_done[x & 1], (uint32_t)((x >> 1) & 1), dead, a.err);
             };
@@ -1409,7 +1422,6 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             tc::wait_st();
                         }
                     }
-                    wait_pv(j - kSG);  // keeps this tile's barrier at most one phase ahead
                     tc::fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p_full[b]);
@@ -1423,7 +1435,9 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 // this group's part of the piece: its O (TMEM) with each row's running max and sum
                 const bool has0 = pc.ntiles >= kSG || (j0 & 1) == 0, has1 = pc.ntiles >= kSG || (j0 & 1) == 1;
                 const bool has_me = g == 0 ? has0 : has1;
-                if (has_me) wait_pv((jl & 1) == g ? jl : jl - 1);
+                // every P V of the piece has completed (each group waits every piece,
+                // so o_last is never more than one phase ahead of its waiter)
+                wait_or_flag(&o_last[g], (uint32_t)(p & 1), dead, a.err);
                 tc::fence_after();
                 // Both groups finish the piece: each hands its rows' (max, sum) to the
                 // other, then combines both O parts for its half of the columns (group
