@@ -140,6 +140,15 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// 32 bytes to global memory in one 256-bit store (a whole L2 sector); the
+// address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                              uint32_t f, uint32_t g, uint32_t h) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d), "r"(e),
+                 "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
+
 // Maximum of three (Blackwell's three-input max): half the instructions of a
 // two-input tree.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

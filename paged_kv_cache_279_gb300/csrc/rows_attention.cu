@@ -501,6 +501,29 @@ __device__ __forceinline__ void softmax_tile(uint32_t sp, int c0, int lim, uint3
     tc::wait_st();
 }
 
+// A row's 16 output columns (bf16, scaled by f) and 16 partial columns (f32):
+// whole 32-byte sectors per store where the address allows (the partial slots
+// always do; the caller's output is only promised 16-byte alignment).
+__device__ __forceinline__ void store_out16(__nv_bfloat16 *p, const float (&o)[16], float f, bool wide) {
+    const uint32_t w0 = pack_bf16x2(o[0] * f, o[1] * f), w1 = pack_bf16x2(o[2] * f, o[3] * f);
+    const uint32_t w2 = pack_bf16x2(o[4] * f, o[5] * f), w3 = pack_bf16x2(o[6] * f, o[7] * f);
+    const uint32_t w4 = pack_bf16x2(o[8] * f, o[9] * f), w5 = pack_bf16x2(o[10] * f, o[11] * f);
+    const uint32_t w6 = pack_bf16x2(o[12] * f, o[13] * f), w7 = pack_bf16x2(o[14] * f, o[15] * f);
+    if (wide) {
+        st_global_32B(p, w0, w1, w2, w3, w4, w5, w6, w7);
+    } else {
+        uint4 *d = reinterpret_cast<uint4 *>(p);
+        d[0] = make_uint4(w0, w1, w2, w3);
+        d[1] = make_uint4(w4, w5, w6, w7);
+    }
+}
+__device__ __forceinline__ void store_part16(float *p, const float (&o)[16]) {
+    st_global_32B(p, __float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]), __float_as_uint(o[3]),
+                  __float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]), __float_as_uint(o[7]));
+    st_global_32B(p + 8, __float_as_uint(o[8]), __float_as_uint(o[9]), __float_as_uint(o[10]), __float_as_uint(o[11]),
+                  __float_as_uint(o[12]), __float_as_uint(o[13]), __float_as_uint(o[14]), __float_as_uint(o[15]));
+}
+
 // Bounded wait helper: returns false (and flags) once the wait gives up.
 __device__ __forceinline__ bool wait_or_flag(uint64_t *bar, uint32_t parity, bool &dead, unsigned int *err) {
     if (dead) return false;
@@ -562,9 +585,7 @@ __device__ __forceinline__ void finish_piece(const Args &a, const Piece &pc, flo
             load_o(cc, o);
             if (live) {
                 if (pc.kind == kContinue) {
-                    float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * slot_rows + cr) * D + cc * 16);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    store_part16(a.part_o + ((int64_t)w_me * slot_rows + cr) * D + cc * 16, o);
                 } else {
                     if (pc.kind == kMerger) {
 #pragma unroll
@@ -585,11 +606,8 @@ __device__ __forceinline__ void finish_piece(const Args &a, const Piece &pc, flo
                             }
                         }
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16);
-                    dst[0] = make_uint4(pack_bf16x2(o[0] * f, o[1] * f), pack_bf16x2(o[2] * f, o[3] * f),
-                                        pack_bf16x2(o[4] * f, o[5] * f), pack_bf16x2(o[6] * f, o[7] * f));
-                    dst[1] = make_uint4(pack_bf16x2(o[8] * f, o[9] * f), pack_bf16x2(o[10] * f, o[11] * f),
-                                        pack_bf16x2(o[12] * f, o[13] * f), pack_bf16x2(o[14] * f, o[15] * f));
+                    store_out16(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16, o, f,
+                                (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0u);
                 }
             }
         }
@@ -1510,9 +1528,7 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                             load_o(cc, o);
                             if (live) {
                                 if (pc.kind == kContinue) {
-                                    float4 *dst = reinterpret_cast<float4 *>(a.part_o + ((int64_t)w_me * kRows + rr) * D + cc * 16);
-    #pragma unroll
-                                    for (int k = 0; k < 4; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                                    store_part16(a.part_o + ((int64_t)w_me * kRows + rr) * D + cc * 16, o);
                                 } else {
                                     if (pc.kind == kMerger) {
     #pragma unroll
@@ -1533,11 +1549,8 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                                             }
                                         }
                                     }
-                                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16);
-                                    dst[0] = make_uint4(pack_bf16x2(o[0] * f, o[1] * f), pack_bf16x2(o[2] * f, o[3] * f),
-                                                        pack_bf16x2(o[4] * f, o[5] * f), pack_bf16x2(o[6] * f, o[7] * f));
-                                    dst[1] = make_uint4(pack_bf16x2(o[8] * f, o[9] * f), pack_bf16x2(o[10] * f, o[11] * f),
-                                                        pack_bf16x2(o[12] * f, o[13] * f), pack_bf16x2(o[14] * f, o[15] * f));
+                                    store_out16(static_cast<__nv_bfloat16 *>(a.out) + orow * D + cc * 16, o, f,
+                                                (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0u);
                                 }
                             }
                         }

@@ -158,3 +158,24 @@ def test_graph_replays_over_a_random_workspace():
         torch.cuda.synchronize()
         assert_bf16_close(out.cpu(), _oracle(dict(c, q=qs[r])), f"multi-token replay {r}")
     assert pkv.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("qlens", [[64, 7], [300, 200]])  # alternating and paired contexts
+def test_output_at_a_16_byte_offset_gives_the_same_bits(qlens):
+    """The output is promised 16-byte alignment only: rows are written in whole
+    32-byte sectors where the address allows, else in 16-byte halves; both
+    forms give the same bits."""
+    c = _case(32, 8, 128, 16, [1800, 400], qlens, seed=15)
+    a = _run(c)
+    dev = "cuda"
+    q = c["q"].to(dev)
+    buf = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device=dev)
+    out = buf[8:].view(q.shape)  # 16 bytes past a 256-byte aligned allocation
+    assert out.data_ptr() % 32 == 16
+    pkv.paged_attention_multi_token(out, q, c["kc"].to(dev), c["vc"].to(dev), torch.from_numpy(c["tables"]).to(dev),
+                                    torch.tensor(c["lens"], dtype=torch.int32, device=dev),
+                                    torch.from_numpy(c["starts"]).to(dev), c["shape"].scale, max(c["qlens"]),
+                                    max(c["lens"]))
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), out.cpu().view(torch.int16))
+    assert pkv.read_device_errors() == 0
