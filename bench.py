@@ -910,7 +910,12 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
         for _ in range(n_eager):  # eager steps: the library's one-time host setup
             host_step()
             device_step()
-        stream.synchronize()
+            # the next host step rewrites the pinned tables and lengths that
+            # this step's copy in reads: wait for it, as the timed loop does
+            stream.synchronize()
+        bits = pkv.read_device_errors()
+        if bits != 0:
+            raise RuntimeError(f"e2e: device error bits {bits:#x} set by the eager steps")
         # the step's copy in, library call and copy out as one graph; every
         # replay copies the pinned buffer's current contents
         graph = torch.cuda.CUDAGraph()
@@ -927,8 +932,9 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
                 # unique bytes: what the batch started with plus the tokens added since
                 byts.append(base_unique + kv_bytes(h_lens.tolist(), shape, 1 if fp8 else None) -
                             kv_bytes(base_lens, shape, 1 if fp8 else None))
-    if pkv.read_device_errors() != 0:
-        raise RuntimeError("e2e: device error bits set")
+    bits = pkv.read_device_errors()
+    if bits != 0:
+        raise RuntimeError(f"e2e: device error bits {bits:#x} set")
     # the device tables must equal the allocator's after the loop
     tab, ln = b.alloc.block_tables(b.seq_ids, cap)
     if not (np.array_equal(tab[:, :], h_tab) and np.array_equal(ln, h_lens)):
