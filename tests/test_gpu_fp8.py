@@ -204,8 +204,9 @@ def test_write_then_decode_end_to_end():
 
 
 def test_decode_fp8_graph_replays():
-    """Split contexts are merged inside the attention kernel with tagged
-    arrival counters; graph replays reuse one tag and must still merge."""
+    """Split contexts are merged inside the attention kernel: each partial has a
+    ready flag set to the call's tag and cleared by the merging warp; graph
+    replays reuse one tag and must still merge."""
     lens = [2048, 700, 0, 1, 1500, 3000]
     Hkv, B = 8, 32
     shape = wl.DecodeShape("fp8_graph", len(lens), 32, Hkv, D, B, torch.bfloat16)
