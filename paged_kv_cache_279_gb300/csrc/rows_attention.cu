@@ -86,16 +86,19 @@ constexpr int kThreads = 384;
 constexpr int kAuxWarp = 9, kProducerWarp = 10, kMmaWarp = 11;
 constexpr int kMma1Warp = 8;  // paired contexts: issues softmax group 1's MMAs
 constexpr int kMaxUnits = 1024;   // groups / sequences scanned per launch
-constexpr int kMinTiles = 4;      // shares hold >= 4 tiles unless the total is small
+constexpr int kMinTiles = 6;      // shares hold >= 6 tiles unless the total is small
 // Scheduling charge of a context, in tiles: a context with n tiles is laid out
 // as kPieceTiles virtual tiles (never loaded) and then its n real ones, so that
 // equal shares of the layout also balance the fixed cost of each piece (its
-// queries' load, the combine and the write of its rows) and not only its
-// tiles.  Below kMinTiles, so every share holds a real tile.
-constexpr int kPieceTiles = 3;
+// queries' load, the wait for its last P V, the combine and the write of its
+// rows; about five tiles' streaming time) and not only its tiles.  Below
+// kMinTiles, so every share holds a real tile.
+constexpr int kPieceTiles = 5;
+static_assert(kPieceTiles < kMinTiles, "a share of kMinTiles laid-out tiles holds a real tile");
 constexpr int kIdCache = 512;     // block ids staged by the producer
 constexpr int kChunkTiles = 128;  // tiles whose keys the producer stages at once
 constexpr int kDescs = 8;         // piece descriptors in flight
+constexpr int kMergeHeld = 1;     // partials a merger keeps in registers (the rest are re-read)
 constexpr float kRescale = 8.f;   // headroom (log2 units) before a row's running max moves
 constexpr int kSB = 4;            // S / P buffers in tensor memory: two per softmax group
 constexpr uint32_t kOBase = kSB * kTok;  // O of softmax group g at kOBase + g * D
@@ -1496,6 +1499,15 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     // the piece's result: final rows, a partial for the merger, or the merge
                     float f = 1.f, e_own = 1.f, Mtr = 0.f;
                     bool got = true;
+                    // merger: the first kMergeHeld other pieces' (max, sum) and scale,
+                    // read once; later pieces (long contexts only) are re-read per chunk
+                    float2 mlh[kMergeHeld];
+                    float eh[kMergeHeld];
+    #pragma unroll
+                    for (int i = 0; i < kMergeHeld; ++i) {
+                        mlh[i] = make_float2(-INFINITY, 0.f);
+                        eh[i] = 0.f;
+                    }
                     if (pc.kind == kWhole) {
                         f = Lc > 0.f ? 1.f / Lc : 0.f;
                     } else if (pc.kind == kContinue) {
@@ -1508,14 +1520,26 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                         got = wait_flags_bounded(a.flags + pc.w0 + 1, n, a.tag, lane);
                         if (!got && lane == 0) flag_error(a.err, PKV_DEVERR_TIMEOUT);
                         float Mt = M;
+    #pragma unroll
+                        for (int i = 0; i < kMergeHeld; ++i) {
+                            if (live && i < n)
+                                mlh[i] = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)(pc.w0 + 1 + i) * kRows + rr);
+                            Mt = fmaxf(Mt, mlh[i].x);
+                        }
                         if (live)
-                            for (int w = pc.w0 + 1; w <= pc.w1; ++w)
+                            for (int w = pc.w0 + 1 + kMergeHeld; w <= pc.w1; ++w)
                                 Mt = fmaxf(Mt, __ldcg(a.part_ml + ((int64_t)w * kRows + rr) * 2));
                         Mtr = Mt == -INFINITY ? 0.f : Mt;
                         e_own = M == -INFINITY ? 0.f : ex2_approx(M - Mtr);
                         float Ls = Lc * e_own;
+    #pragma unroll
+                        for (int i = 0; i < kMergeHeld; ++i)
+                            if (mlh[i].x != -INFINITY) {
+                                eh[i] = ex2_approx(mlh[i].x - Mtr);
+                                Ls += mlh[i].y * eh[i];
+                            }
                         if (live)
-                            for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+                            for (int w = pc.w0 + 1 + kMergeHeld; w <= pc.w1; ++w) {
                                 const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
                                 if (ml.x != -INFINITY) Ls += ml.y * ex2_approx(ml.x - Mtr);
                             }
@@ -1524,6 +1548,16 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     }
                     for (int cc = g * (kNc / 2); cc < (g + 1) * (kNc / 2); ++cc) {
                         if (live_warp) {
+                            // the held partials' 16 columns: in flight with the tensor-memory load
+                            float4 ph[kMergeHeld][4];
+    #pragma unroll
+                            for (int i = 0; i < kMergeHeld; ++i)
+                                if (live && pc.kind == kMerger && mlh[i].x != -INFINITY) {
+                                    const float4 *src = reinterpret_cast<const float4 *>(
+                                        a.part_o + ((int64_t)(pc.w0 + 1 + i) * kRows + rr) * D + cc * 16);
+    #pragma unroll
+                                    for (int k = 0; k < 4; ++k) ph[i][k] = __ldcg(src + k);
+                                }
                             float o[16];
                             load_o(cc, o);
                             if (live) {
@@ -1533,7 +1567,18 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                                     if (pc.kind == kMerger) {
     #pragma unroll
                                         for (int k = 0; k < 16; ++k) o[k] *= e_own;
-                                        for (int w = pc.w0 + 1; w <= pc.w1; ++w) {
+    #pragma unroll
+                                        for (int i = 0; i < kMergeHeld; ++i)
+                                            if (mlh[i].x != -INFINITY) {
+    #pragma unroll
+                                                for (int k = 0; k < 4; ++k) {
+                                                    o[4 * k] += eh[i] * ph[i][k].x;
+                                                    o[4 * k + 1] += eh[i] * ph[i][k].y;
+                                                    o[4 * k + 2] += eh[i] * ph[i][k].z;
+                                                    o[4 * k + 3] += eh[i] * ph[i][k].w;
+                                                }
+                                            }
+                                        for (int w = pc.w0 + 1 + kMergeHeld; w <= pc.w1; ++w) {
                                             const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.part_ml) + (int64_t)w * kRows + rr);
                                             if (ml.x == -INFINITY) continue;
                                             const float e = ex2_approx(ml.x - Mtr);
