@@ -1140,11 +1140,24 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     __syncthreads();
     int my_max = 0;
-    for (int base = 0; base < S; base += NW * 32) {
+    // the first kScanAhead passes' lengths, all loads in flight at once (one
+    // memory latency instead of one per pass of NW * 32 sequences)
+    constexpr int kScanAhead = 4;
+    int ahead[kScanAhead];
+#pragma unroll
+    for (int k = 0; k < kScanAhead; ++k) {
+        const int sq = k * NW * 32 + threadIdx.x;
+        ahead[k] = sq < S ? a.seq_lens[sq] : 0;
+    }
+    for (int base = 0, pass = 0; base < S; base += NW * 32, ++pass) {
         const int sq = base + threadIdx.x;
         int v = 0;
         if (sq < S) {
-            const int raw = a.seq_lens[sq];
+            int raw = ahead[0];
+#pragma unroll
+            for (int k = 1; k < kScanAhead; ++k)
+                if (pass == k) raw = ahead[k];
+            if (pass >= kScanAhead) raw = a.seq_lens[sq];
             if ((raw < 0 || raw > cap) && blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
             const int len = clamp_len(raw, cap);
             v = Hkv * laid_out_tiles((len + TT - 1) / TT);

@@ -706,14 +706,15 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
         if (u < a.num_units) {
             const int gu = a.unit0 + u;
             if (a.mode == kGrouped) {
+                // loads first: a flag's atomic between them would order them one after another
                 int m0 = a.group_offsets[gu], m1 = a.group_offsets[gu + 1];
+                const int raw = a.prefix_lens[gu];
                 if (m0 < 0 || m1 > a.num_seqs || m1 < m0) {
                     if (blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_PREFIX);
                     m0 = m1 = 0;
                 }
                 if (blockIdx.x == 0 && (gu == 0 && m0 != 0 || gu + 1 == a.num_groups && m1 != a.num_seqs))
                     flag_error(a.err, PKV_DEVERR_PREFIX);
-                const int raw = a.prefix_lens[gu];
                 const int align = B > 16 ? B : 16;
                 if (blockIdx.x == 0 && (raw < 0 || raw % align != 0)) flag_error(a.err, PKV_DEVERR_PREFIX);
                 int mn = cap;
@@ -739,12 +740,13 @@ rows_attention_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 }
                 v = Hkv * tot;
             } else {
+                // loads first: a flag's atomic between them would order them one after another
                 int q0 = a.q_starts[gu], q1 = a.q_starts[gu + 1];
+                const int raw_len = a.seq_lens[gu];
                 if (q0 < 0 || q1 < q0 || q1 > a.num_q_tokens) {
                     if (blockIdx.x == 0) flag_error(a.err, PKV_DEVERR_SEQ_LEN);
                     q0 = q1 = 0;
                 }
-                const int raw_len = a.seq_lens[gu];
                 const int Lq = clamp_len(raw_len, cap);
                 if (blockIdx.x == 0 && ((raw_len < 0 || raw_len > cap) || q1 - q0 > a.max_q_len || q1 - q0 > Lq))
                     flag_error(a.err, PKV_DEVERR_SEQ_LEN);
