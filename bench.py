@@ -819,11 +819,14 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     tables (and the groups of a beam batch), the library call stores the new
     tokens and attends, and one D2H copy brings the output back; the host
     waits for it before the next step.  The copy in, the call and the copy out
-    are replayed as one CUDA graph; the host's allocator work is timed too."""
+    are replayed as one CUDA graph.  The allocator's work for the next step
+    (which needs only that a token is appended, not which) runs on the host
+    while the device runs the current step, into the other of two pinned
+    buffers; it is inside the timed region."""
     from paged_kv_cache_279_gb300 import _lib
     lib = _lib.load()
     steps = args.steps
-    n_tok = steps + max(1, args.warmup) + 1  # tokens the loop appends per sequence
+    n_tok = steps + max(1, args.warmup) + 3  # tokens the loop appends per sequence
     b = make_batch(pkv, shape, args, seed + 77, device, reserve_tokens=n_tok + 1)
     S, Hq, Hkv, D, B = len(b.lens), shape.num_heads, shape.num_kv_heads, shape.head_dim, shape.block_size
     cap = b.max_blocks + n_tok // B + 2
@@ -831,7 +834,8 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     grouped = b.group_offsets is not None
     fp8 = args.kv == "fp8"
     elt = torch.tensor([], dtype=shape.dtype).element_size()
-    # one pinned buffer, one device buffer: q | k_new | v_new | lens | tables | groups
+    # two pinned buffers (steps alternate between them), one device buffer:
+    # q | k_new | v_new | lens | tables | groups
     parts = [("q", S * Hq * D * elt), ("k", S * Hkv * D * elt), ("v", S * Hkv * D * elt), ("lens", 4 * S),
              ("tab", 4 * S * cap)]
     if grouped:
@@ -841,23 +845,28 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     for name, n in parts:
         off[name] = pos
         pos += (n + 255) // 256 * 256
-    h_pack = torch.zeros(pos, dtype=torch.uint8).pin_memory()
+    h_packs = [torch.zeros(pos, dtype=torch.uint8).pin_memory() for _ in range(2)]
     d_pack = torch.zeros(pos, dtype=torch.uint8, device=device)
 
-    def hview(name, dtype, shp):
+    def hview(pk, name, dtype, shp):
         n = int(np.prod(shp)) * torch.tensor([], dtype=dtype).element_size()
-        return h_pack[off[name]:off[name] + n].view(dtype).view(*shp)
-    hview("q", shape.dtype, (S, Hq, D)).copy_(b.q.cpu())
-    hview("k", shape.dtype, (S, Hkv, D)).copy_(b.k_new.cpu())
-    hview("v", shape.dtype, (S, Hkv, D)).copy_(b.v_new.cpu())
-    h_lens = hview("lens", torch.int32, (S,)).numpy()
-    h_tab = hview("tab", torch.int32, (S, cap)).numpy()
-    tab, ln = b.alloc.block_tables(b.seq_ids, cap)
-    h_tab[:] = tab
-    h_lens[:] = ln
-    if grouped:
-        hview("offs", torch.int32, (len(offs),)).numpy()[:] = offs
-        hview("pre", torch.int32, (len(pre),)).numpy()[:] = pre
+        return h_packs[pk][off[name]:off[name] + n].view(dtype).view(*shp)
+    # the allocator's tables and lengths (host memory the device never reads)
+    m_tab, m_lens = b.alloc.block_tables(b.seq_ids, cap)
+    m_tab = np.ascontiguousarray(m_tab, dtype=np.int32)
+    m_lens = np.ascontiguousarray(m_lens, dtype=np.int32)
+    p_lens, p_tab = [], []
+    for pk in range(2):
+        hview(pk, "q", shape.dtype, (S, Hq, D)).copy_(b.q.cpu())
+        hview(pk, "k", shape.dtype, (S, Hkv, D)).copy_(b.k_new.cpu())
+        hview(pk, "v", shape.dtype, (S, Hkv, D)).copy_(b.v_new.cpu())
+        p_lens.append(hview(pk, "lens", torch.int32, (S,)).numpy())
+        p_tab.append(hview(pk, "tab", torch.int32, (S, cap)).numpy())
+        p_tab[pk][:] = m_tab
+        p_lens[pk][:] = m_lens
+        if grouped:
+            hview(pk, "offs", torch.int32, (len(offs),)).numpy()[:] = offs
+            hview(pk, "pre", torch.int32, (len(pre),)).numpy()[:] = pre
     dptr = d_pack.data_ptr()
     out = torch.empty((S, Hq, D), dtype=shape.dtype, device=device)
     h_out = torch.empty_like(out, device="cpu").pin_memory()
@@ -890,15 +899,21 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     ms, byts = [], []
     base_unique, base_lens = b.unique_bytes, list(b.lens)
 
-    def host_step():
-        # the allocator appends one token per sequence and updates the pinned
-        # tables and lengths in place (only entries that changed)
-        st, _, pairs = b.alloc.append_step(seq_ids, h_tab, h_lens)
+    def prepare(pk):
+        # the next step's bookkeeping: the allocator appends one token per
+        # sequence (tables and lengths updated in place, only entries that
+        # changed), then pinned buffer pk, two steps behind, takes the new
+        # lengths and the table rows whose block count changed
+        st, _, pairs = b.alloc.append_step(seq_ids, m_tab, m_lens)
         if st != 0 or len(pairs):
             raise RuntimeError("allocator could not serve the step")
+        rows = np.nonzero((p_lens[pk] + B - 1) // B != (m_lens + B - 1) // B)[0]
+        if rows.size:
+            p_tab[pk][rows] = m_tab[rows]
+        p_lens[pk][:] = m_lens
 
-    def device_step():
-        d_pack.copy_(h_pack, non_blocking=True)
+    def device_step(pk):
+        d_pack.copy_(h_packs[pk], non_blocking=True)
         rc = call()
         if rc != 0:
             raise RuntimeError(f"library call failed with status {rc}")
@@ -908,36 +923,48 @@ def run_e2e(pkv, shape, args, device, stream, seed, world):
     n_eager = max(1, args.warmup)
     with torch.cuda.stream(stream):
         for _ in range(n_eager):  # eager steps: the library's one-time host setup
-            host_step()
-            device_step()
-            # the next host step rewrites the pinned tables and lengths that
-            # this step's copy in reads: wait for it, as the timed loop does
-            stream.synchronize()
+            prepare(0)
+            device_step(0)
+            stream.synchronize()  # the next prepare rewrites the buffer this copy reads
+        p_tab[1][:] = m_tab
+        p_lens[1][:] = m_lens
         bits = pkv.read_device_errors()
         if bits != 0:
             raise RuntimeError(f"e2e: device error bits {bits:#x} set by the eager steps")
-        # the step's copy in, library call and copy out as one graph; every
-        # replay copies the pinned buffer's current contents
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            device_step()
-        for i in range(steps + 1):
+        # per pinned buffer, the step's copy in, library call and copy out as
+        # one graph; every replay copies the buffer's current contents
+        graphs = []
+        for pk in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                device_step(pk)
+            graphs.append(g)
+        cur = 0
+        prepare(cur)
+        for i in range(steps + 2):
             ev0.record(stream)
-            host_step()
-            graph.replay()
+            graphs[cur].replay()
+            used = p_lens[cur].tolist()  # the lengths this step attends
+            # while the device runs this step, the host prepares the next one in
+            # the other buffer (the one the previous step read, already done);
+            # the step's result is read before the next step starts
+            prepare(1 - cur)
             ev1.record(stream)
             ev1.synchronize()  # the host reads the step's result
-            if i >= 1:  # the first replay uploads the graph
+            if i >= 2:  # the first replay of each graph uploads it
                 ms.append(ev0.elapsed_time(ev1))
                 # unique bytes: what the batch started with plus the tokens added since
-                byts.append(base_unique + kv_bytes(h_lens.tolist(), shape, 1 if fp8 else None) -
+                byts.append(base_unique + kv_bytes(used, shape, 1 if fp8 else None) -
                             kv_bytes(base_lens, shape, 1 if fp8 else None))
+            cur = 1 - cur
     bits = pkv.read_device_errors()
     if bits != 0:
         raise RuntimeError(f"e2e: device error bits {bits:#x} set")
-    # the device tables must equal the allocator's after the loop
+    # the allocator's tables after the loop equal the incrementally kept ones,
+    # and the last buffer prepared holds them too
     tab, ln = b.alloc.block_tables(b.seq_ids, cap)
-    if not (np.array_equal(tab[:, :], h_tab) and np.array_equal(ln, h_lens)):
+    if not (np.array_equal(tab, m_tab) and np.array_equal(ln, m_lens) and
+            np.array_equal(p_tab[cur], m_tab) and np.array_equal(p_lens[cur], m_lens)):
         raise RuntimeError("e2e: incremental block tables diverged from the allocator")
     local_s = sum(ms) / 1e3
     total_s = max_over_ranks(local_s, world, device)
