@@ -1493,7 +1493,8 @@ decode_bf16_streamk_kernel(const __grid_constant__ CUtensorMap tm_k,
         // merge through the now idle ring, then clear the flags so that a
         // replay with the same tag waits again.
         unsigned long long *fl = a.flags + merge_seg * a.max_parts;
-        fence_acq_rel_gpu();  // this warp's own partial (slot 0), before it is read back
+        // this warp's own partial (slot 0) is read back by its own lanes: the
+        // warp barrier orders those stores before the reads
         __syncwarp();
         const bool ready = wait_flags_bounded(fl + 1, merge_n - 1, a.tag, lane);
         const int sq = (int)(merge_seg / Hkv), kvh = (int)(merge_seg - (int64_t)sq * Hkv);

@@ -160,29 +160,31 @@ __device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(
 __device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // Ordering of the in-kernel merge: a writer's lanes store their partial,
-// fence, and lane 0 then sets the slot's flag; the merger sees every flag,
-// fences, and reads the partials through L2.
+// fence, and lane 0 then sets the slot's flag; the merger reads every flag
+// with an acquire load, then reads the partials through L2.
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long *p) {
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
     unsigned long long v;
-    asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
 // The merger's wait (warp-collective): polls flags[0 .. n) until every one
-// holds `tag`, at most `limit` rounds.  Returns false if it gave up.  Ends with
-// an acquire fence and a warp barrier, so that every lane's later reads of the
-// partials are ordered after every lane's flag reads.
+// holds `tag`, at most `limit` rounds.  Returns false if it gave up.  The flags
+// are read with acquire loads (each pairs with its writer's fence and flag
+// store) and the wait ends with a warp barrier, so that every lane's later
+// reads of the partials are ordered after every lane's flag reads.  No fence:
+// the merger's own earlier stores need not complete first.
 __device__ __forceinline__ bool wait_flags_bounded(const unsigned long long *flags, int n, unsigned long long tag,
                                                    int lane, uint32_t limit = kWaitLimit) {
     bool got = false;
     for (uint32_t it = 0; it < limit && !got; ++it) {
         bool mine = true;
-        for (int k = lane; k < n; k += 32) mine = mine && ld_volatile_u64(flags + k) == tag;
+        for (int k = lane; k < n; k += 32) mine = mine && ld_acquire_u64(flags + k) == tag;
         got = __all_sync(0xffffffffu, mine);
         if (!got) __nanosleep(64);
     }
-    fence_acq_rel_gpu();
     __syncwarp();
     return got;
 }
