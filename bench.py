@@ -197,8 +197,8 @@ FP8_K_SCALE = FP8_V_SCALE = 1.0 / 64
 # (rotated batch 0); the line reports traffic scaled to the average launch.
 # Only valid for the kernel build the capture was taken from.
 NCU_TRAFFIC = {
-    ("gqa", "bf16"): (269.41e6, 263.95e6, "profiles/decode_balanced_gqa_full.md"),
-    ("gqa", "fp8"): (137.16e6, 132.51e6, "profiles/decode_fp8_gqa_full.md"),
+    ("gqa", "bf16"): (269.27e6, 263.95e6, "profiles/decode_balanced_gqa_full.md"),
+    ("gqa", "fp8"): (136.92e6, 132.51e6, "profiles/decode_fp8_gqa_full.md"),
 }
 
 
